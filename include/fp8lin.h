@@ -1,0 +1,237 @@
+/*
+ * fp8lin — FP8 dynamic-scaling linear for NVIDIA GB300 (sm_103a): C ABI.
+ *
+ * What it computes (sources are web pages, cited by title and section):
+ *  [Q]  "FP8 Training: Quantization, Autograd, Torchao", section 2 "The quantization math":
+ *       per group (tensor, row or column) amax = max|x| in fp32; scale = fp8_max / max(amax, eps)
+ *       in fp64; q = cast(clamp(x * scale, -fp8_max, fp8_max)); the GEMM receives the inverse
+ *       scale (the fp64 reciprocal of scale) and multiplies its result by scale_a * scale_b.
+ *  [F]  same page, section 3 "Format choice: e4m3 vs e5m2": e4m3 (max 448) for activations and
+ *       weights, e5m2 (max 57344) for gradients.
+ *  [L]  same page, section 4 "_scaled_mm layout requirements": the three GEMMs of a Linear
+ *       (forward out = x W^T, grad-input dX = dY W, grad-weight dW = dY^T x) with A row-major
+ *       and B column-major, i.e. both operands contiguous along the contraction dimension
+ *       ("K-major"); section 5 "use_fast_accum" (forward True, backward False).
+ *  [G]  "FP8 training on AMD GPUs with TorchTitan and TorchAO", section "Scaling FP8 to MoE
+ *       Architectures" and Figure 3: a grouped GEMM over experts routed by an offsets tensor,
+ *       with per-row activation scales and per-expert per-column weight scales.
+ *  [W]  same page, Figure 1 caption: the high-precision weight-gradient recipe (forward and
+ *       grad-input GEMMs in FP8, the weight-gradient GEMM in BF16).
+ *  [T]  same page, "Level 1" and "Level 2" of "Triton Kernel Optimization": one fused kernel per
+ *       quantization (no intermediate tensors in HBM), the column-wise variant that writes a
+ *       column-major output through on-chip staging (no separate transpose copy), and the
+ *       dual output (row- and column-major from one read).
+ *
+ * Conventions for every entry point:
+ *  - Tensors are described by fp8_tensor: a DEVICE pointer (global memory, 16-byte aligned),
+ *    a dtype, and a logical shape, always dense and row-major (last index contiguous). A
+ *    "column-major [R, C]" operand is passed as the row-major tensor of shape [C, R].
+ *  - Ownership: the caller allocates and frees every buffer, including the workspace. The
+ *    library never allocates device memory, never synchronizes the host, and never reads a
+ *    device buffer (offsets included) on the host.
+ *  - Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream). Outputs are defined once the stream reaches the call, and only if both the
+ *    return value and the device status word are 0.
+ *  - Return value: synchronous argument checking. FP8_OK, or an FP8_ERR_* code; on error
+ *    nothing was launched.
+ *  - d_status (optional, device int32): conditions found on the device are OR-ed into it
+ *    (FP8_DEV_*). The caller zeroes it and reads it after its own synchronization. When a
+ *    call's kernels find such a condition they stop early and leave outputs undefined.
+ *  - Scales, in and out, are always fp32 INVERSE (dequantization) scales ([Q]).
+ *  - Not re-entrant on one workspace: calls that share a workspace must be stream-ordered.
+ */
+#ifndef FP8LIN_H
+#define FP8LIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types */
+enum {
+  FP8_DT_BF16 = 1,
+  FP8_DT_F32 = 2,
+  FP8_DT_E4M3 = 3, /* OCP float8 e4m3fn: bias 7, no Inf, max 448 */
+  FP8_DT_E5M2 = 4, /* OCP float8 e5m2: bias 15, max 57344 */
+  FP8_DT_I32 = 5
+};
+
+/* scale granularity */
+enum { FP8_GRAN_TENSOR = 0, FP8_GRAN_ROW = 1, FP8_GRAN_COL = 2 };
+
+/* output layouts of fp8_quantize (bit mask) */
+enum { FP8_LAYOUT_ROW_MAJOR = 1, FP8_LAYOUT_COL_MAJOR = 2, FP8_LAYOUT_BOTH = 3 };
+
+/* GEMM flags (bit mask) */
+enum {
+  FP8_MM_FAST_ACCUM = 1, /* accepted for parity with the pages' forward GEMM; the tcgen05
+                            accumulator is fp32 in tensor memory either way */
+  FP8_MM_A_MN_MAJOR = 2, /* BF16 only: A is given as [K, M] (M contiguous) */
+  FP8_MM_B_MN_MAJOR = 4  /* BF16 only: B is given as [K, N] (N contiguous) */
+};
+
+/* grouped GEMM modes */
+enum { FP8_GROUPED_JAGGED_M = 0, FP8_GROUPED_JAGGED_K = 1 };
+
+/* weight-gradient recipe of fp8_linear_bwd */
+enum { FP8_WGRAD_FP8 = 0, FP8_WGRAD_BF16 = 1 };
+
+/* operations for fp8_workspace_size */
+enum { FP8_OP_QUANTIZE = 0, FP8_OP_LINEAR_FWD = 1, FP8_OP_LINEAR_BWD = 2 };
+
+/* synchronous return codes */
+enum {
+  FP8_OK = 0,
+  FP8_ERR_INVALID_ARG = 1, /* null pointer, wrong dtype, rank or shape mismatch */
+  FP8_ERR_UNSUPPORTED = 2, /* a valid request this library does not implement */
+  FP8_ERR_ALIGNMENT = 3,   /* pointer not 16-byte aligned, or a contiguous dimension whose
+                              byte length is not a multiple of 16 (e.g. K % 16 for FP8) */
+  FP8_ERR_WORKSPACE = 4,   /* workspace missing or smaller than fp8_workspace_size() */
+  FP8_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  FP8_ERR_DEVICE = 6       /* no usable sm_103 device current */
+};
+
+/* device status bits (OR-ed into *d_status) */
+enum {
+  FP8_DEV_BAD_OFFSETS = 1 << 8, /* offsets not non-decreasing, or last entry != total rows */
+  FP8_DEV_TIMEOUT = 1 << 9      /* a bounded on-device wait ran out; the kernel drained and
+                                   returned */
+};
+
+typedef struct fp8_tensor {
+  void* ptr;        /* device pointer, 16-byte aligned */
+  int32_t dtype;    /* FP8_DT_* */
+  int32_t ndim;     /* 1, 2 or 3 */
+  int64_t shape[3]; /* logical shape, dense row-major */
+} fp8_tensor;
+
+/*
+ * fp8_quantize — the quantization chain of [Q] in one fused pass per output ([T]).
+ *
+ *  x           bf16 [R, C], or [B, R, C] for a batch of matrices (e.g. MoE expert weights).
+ *              C % 8 == 0 (16-byte rows).
+ *  granularity FP8_GRAN_TENSOR: one scale for all of x.
+ *              FP8_GRAN_ROW:    one scale per row (amax over the C entries of the row);
+ *                               a 3-D x is treated as [B*R, C].
+ *              FP8_GRAN_COL:    one scale per column (amax over the R rows of the column), per
+ *                               batch entry for 3-D x; with `offsets`, one scale per
+ *                               (segment, column) where segment e holds rows
+ *                               [offsets[e-1], offsets[e]) (offsets[-1] = 0) of a 2-D x.
+ *  out_dtype   FP8_DT_E4M3 or FP8_DT_E5M2 ([F]).
+ *  layout      FP8_LAYOUT_ROW_MAJOR: `out` = codes in x's shape.
+ *              FP8_LAYOUT_COL_MAJOR: `out_t` = codes transposed: [C, R] (2-D), [B, C, R]
+ *                (3-D), or, with offsets, [C, P] in the segment-padded layout: segment e
+ *                starts at column pstart_e = sum_{j<e} roundup(count_j, 128) and is followed
+ *                by zero codes up to the next multiple of 128. P >=
+ *                fp8_jagged_padded_rows(R, E) and P % 16 == 0. For 2-D/3-D, R % 16 == 0.
+ *              FP8_LAYOUT_BOTH: both (tensor granularity only: one read, two outputs).
+ *              ROW granularity supports ROW_MAJOR; COL granularity supports COL_MAJOR.
+ *  inv_scales  fp32: [1] (tensor), [R] or [B*R] (row), [C], [B, C] or [E, C] (col).
+ *  offsets     NULL, or int32 [E] cumulative segment ends (COL granularity, 2-D x only).
+ *              Checked on the device: a bad vector sets FP8_DEV_BAD_OFFSETS.
+ *  workspace   device memory of fp8_workspace_size(FP8_OP_QUANTIZE, ...) bytes (4 bytes for
+ *              tensor granularity, 0 otherwise); may be NULL when that size is 0.
+ * Bit-exactness: codes and inverse scales equal the recipe evaluated with an fp64 division,
+ * an fp32 multiply and a round-to-nearest-even saturating cast (eps = 1e-12).
+ */
+int fp8_quantize(const fp8_tensor* x, int granularity, int out_dtype, int layout, fp8_tensor* out,
+                 fp8_tensor* out_t, fp8_tensor* inv_scales, const fp8_tensor* offsets,
+                 void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream);
+
+/*
+ * fp8_scaled_mm — out[m, n] = sA[m] * sB[n] * sum_k A[m, k] * B[n, k]   ([Q], [L]).
+ *
+ *  A    FP8 (e4m3 or e5m2) [M, K], K-major. Or BF16 [M, K] (or [K, M] with FP8_MM_A_MN_MAJOR).
+ *  B    FP8 [N, K], K-major (the pages' column-major B). Or BF16 [N, K] (or [K, N] with
+ *       FP8_MM_B_MN_MAJOR). FP8 operand pairs: e4m3 x e4m3, e5m2 x e4m3, e4m3 x e5m2.
+ *  sA   fp32 [1] (tensorwise) or [M] (rowwise) inverse scales; NULL for BF16 operands.
+ *  sB   fp32 [1] or [N]; NULL for BF16 operands.
+ *  out  bf16 or fp32 [M, N]. Accumulation is fp32 in tensor memory; the dequantization
+ *       sA[m] * sB[n] is applied once in the epilogue, followed by one rounding to out's type.
+ *  K * element size must be a multiple of 16 bytes; M and N are arbitrary (>= 1).
+ */
+int fp8_scaled_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA,
+                  const fp8_tensor* sB, fp8_tensor* out, int flags, int32_t* d_status,
+                  void* stream);
+
+/*
+ * fp8_grouped_mm — the MoE grouped GEMM of [G], one persistent launch; the offsets stay on the
+ * device. offsets: int32 [E] cumulative segment ends (non-decreasing, last = total rows);
+ * empty segments are allowed anywhere.
+ *
+ * FP8_GROUPED_JAGGED_M (forward / grad-input):
+ *   out[r, n] = sA[r] * sB[e, n] * sum_k A[r, k] * B[e, n, k]   for r in segment e.
+ *   A FP8 [M, K]; B FP8 [E, N, K] (K-major per expert); sA fp32 [M]; sB fp32 [E, N];
+ *   out bf16/fp32 [M, N]. Rows of empty experts do not exist; no other rows are touched.
+ * FP8_GROUPED_JAGGED_K (per-expert weight gradient):
+ *   out[e, n, k] = sA[e, n] * sB[e, k] * sum_{r in segment e} G[r, n] * X[r, k].
+ *   A = G^T and B = X^T in the segment-padded column-major layout written by fp8_quantize
+ *   (COL granularity with offsets): A FP8 [N, P], B FP8 [K, P]; sA fp32 [E, N]; sB fp32 [E, K];
+ *   out bf16/fp32 [E, N, K]. An empty segment gives out[e] = 0.
+ */
+int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* offsets,
+                   const fp8_tensor* sA, const fp8_tensor* sB, fp8_tensor* out, int mode,
+                   int flags, int32_t* d_status, void* stream);
+
+/* FP8 copies and inverse scales kept from the forward pass for the backward pass
+ * ([Q] section 6: the autograd function saves the quantized tensors, not the bf16 inputs).
+ * All buffers are caller-owned. */
+typedef struct fp8_linear_saved {
+  fp8_tensor x_q;   /* e4m3 [M, K] */
+  fp8_tensor x_inv; /* fp32 [1] (tensor) or [M] (row) */
+  fp8_tensor w_q;   /* e4m3 [N, K] */
+  fp8_tensor w_inv; /* fp32 [1] or [N] */
+  fp8_tensor xt_q;  /* tensor granularity: e4m3 [K, M], x column-major (FP8 weight-gradient);
+                       ptr may be NULL when the backward pass uses FP8_WGRAD_BF16 */
+  fp8_tensor wt_q;  /* tensor granularity: e4m3 [K, N], W column-major (grad-input) */
+} fp8_linear_saved;
+
+/*
+ * fp8_linear_fwd — y = x W^T through FP8 ([Q], [L]): quantize x and W (e4m3; tensor or row
+ * granularity), then one scaled GEMM. x bf16 [M, K], w bf16 [N, K], y bf16/fp32 [M, N].
+ * Tensor granularity writes x and W in both layouts (dual output) so that the backward pass
+ * needs no transpose copy.
+ */
+int fp8_linear_fwd(const fp8_tensor* x, const fp8_tensor* w, int granularity, int flags,
+                   fp8_tensor* y, fp8_linear_saved* saved, void* workspace,
+                   size_t workspace_bytes, int32_t* d_status, void* stream);
+
+/*
+ * fp8_linear_bwd — dX = dY W and dW = dY^T x ([L], [W]).
+ *  dy      bf16 [M, N]; quantized to e5m2 ([F]).
+ *  saved   from fp8_linear_fwd with the same granularity.
+ *  x, w    the bf16 forward inputs. Row granularity needs w (W quantized per column over N for
+ *          the grad-input GEMM). FP8_WGRAD_BF16 needs x; FP8_WGRAD_FP8 with row granularity
+ *          needs x (quantized per column over M).
+ *  dx      bf16/fp32 [M, K]; dw bf16/fp32 [N, K]. Either may be NULL to skip that GEMM.
+ *  Both backward GEMMs run with full accumulation ([Q] section 5).
+ */
+int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* saved, const fp8_tensor* x,
+                   const fp8_tensor* w, int granularity, int wgrad_mode, fp8_tensor* dx,
+                   fp8_tensor* dw, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                   void* stream);
+
+/* Workspace bytes for an operation. FP8_OP_QUANTIZE: (d0, d1, d2) unused except that
+ * granularity selects 4 bytes (tensor) or 0. FP8_OP_LINEAR_FWD / FP8_OP_LINEAR_BWD:
+ * (d0, d1, d2) = (M, K, N). */
+size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granularity,
+                          int wgrad_mode);
+
+/* Minimum padded row count P of the segment-padded column-major layout (see fp8_quantize). */
+int64_t fp8_jagged_padded_rows(int64_t rows, int64_t n_segments);
+
+/* Text for an FP8_ERR_* return code or an FP8_DEV_* status word. */
+const char* fp8_status_string(int code);
+
+/* Upper bound, in nanoseconds, of every on-device wait (default 4e9). A wait that runs out
+ * sets FP8_DEV_TIMEOUT and the kernel drains and returns. Tests lower it to exercise that
+ * path without faulting the GPU. Returns the previous value. */
+uint64_t fp8_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8LIN_H */

@@ -1,0 +1,220 @@
+"""Python binding of the fp8lin C ABI (include/fp8lin.h): argument marshalling only.
+
+Every function named like a C entry point takes torch tensors (device memory), turns each into
+an fp8_tensor descriptor and calls the shared library; all arithmetic runs in the library's CUDA
+kernels. Outputs are caller-provided; the `*_alloc` helpers only allocate torch buffers of the
+right shape before calling the same entry points.
+
+The library is built in-tree by `build.py` (`_lib/libfp8lin.so`). Importing this module raises
+if it is missing: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libfp8lin.so")
+
+# enums of include/fp8lin.h
+DT_BF16, DT_F32, DT_E4M3, DT_E5M2, DT_I32 = 1, 2, 3, 4, 5
+GRAN_TENSOR, GRAN_ROW, GRAN_COL = 0, 1, 2
+LAYOUT_ROW_MAJOR, LAYOUT_COL_MAJOR, LAYOUT_BOTH = 1, 2, 3
+MM_FAST_ACCUM, MM_A_MN_MAJOR, MM_B_MN_MAJOR = 1, 2, 4
+GROUPED_JAGGED_M, GROUPED_JAGGED_K = 0, 1
+WGRAD_FP8, WGRAD_BF16 = 0, 1
+OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD = 0, 1, 2
+OK = 0
+DEV_BAD_OFFSETS = 1 << 8
+DEV_TIMEOUT = 1 << 9
+
+_TORCH_DT = {
+    torch.bfloat16: DT_BF16,
+    torch.float32: DT_F32,
+    torch.float8_e4m3fn: DT_E4M3,
+    torch.float8_e5m2: DT_E5M2,
+    torch.int32: DT_I32,
+}
+FP8_TORCH = {DT_E4M3: torch.float8_e4m3fn, DT_E5M2: torch.float8_e5m2}
+
+
+class Fp8Tensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 3)]
+
+
+class Fp8LinearSaved(ctypes.Structure):
+    _fields_ = [(n, Fp8Tensor) for n in ("x_q", "x_inv", "w_q", "w_inv", "xt_q", "wt_q")]
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (code {code})")
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"fp8lin library not built: {LIB_PATH} missing (run __graft_entry__.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    T = ctypes.POINTER(Fp8Tensor)
+    L.fp8_quantize.argtypes = [T, ctypes.c_int, ctypes.c_int, ctypes.c_int, T, T, T, T, P, ctypes.c_size_t, P, P]
+    L.fp8_scaled_mm.argtypes = [T, T, T, T, T, ctypes.c_int, P, P]
+    L.fp8_grouped_mm.argtypes = [T, T, T, T, T, T, ctypes.c_int, ctypes.c_int, P, P]
+    L.fp8_linear_fwd.argtypes = [T, T, ctypes.c_int, ctypes.c_int, T, ctypes.POINTER(Fp8LinearSaved), P,
+                                 ctypes.c_size_t, P, P]
+    L.fp8_linear_bwd.argtypes = [T, ctypes.POINTER(Fp8LinearSaved), T, T, ctypes.c_int, ctypes.c_int, T, T, P,
+                                 ctypes.c_size_t, P, P]
+    L.fp8_workspace_size.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                     ctypes.c_int]
+    L.fp8_workspace_size.restype = ctypes.c_size_t
+    L.fp8_jagged_padded_rows.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    L.fp8_jagged_padded_rows.restype = ctypes.c_int64
+    L.fp8_status_string.argtypes = [ctypes.c_int]
+    L.fp8_status_string.restype = ctypes.c_char_p
+    L.fp8_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.fp8_set_wait_limit_ns.restype = ctypes.c_uint64
+    return L
+
+
+lib = _load()
+
+# Symbols include/fp8lin.h declares (checked by the CPU tests against the header and the .so).
+EXPORTS = ("fp8_quantize", "fp8_scaled_mm", "fp8_grouped_mm", "fp8_linear_fwd", "fp8_linear_bwd",
+           "fp8_workspace_size", "fp8_jagged_padded_rows", "fp8_status_string", "fp8_set_wait_limit_ns")
+
+
+def status_string(code: int) -> str:
+    return lib.fp8_status_string(int(code)).decode()
+
+
+def desc(t: torch.Tensor | None, dtype: int | None = None):
+    """fp8_tensor descriptor of a dense torch tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to fp8lin must be contiguous")
+    if t.dim() < 1 or t.dim() > 3:
+        raise ValueError("fp8lin tensors have 1 to 3 dimensions")
+    d = Fp8Tensor()
+    d.ptr = t.data_ptr() if t.numel() else 0
+    d.dtype = dtype if dtype is not None else _TORCH_DT[t.dtype]
+    d.ndim = t.dim()
+    for i, s in enumerate(t.shape):
+        d.shape[i] = s
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise Fp8Error(rc, where)
+
+
+def fp8_quantize(x, granularity, out_dtype, layout, out=None, out_t=None, inv_scales=None, offsets=None,
+                 workspace=None, status=None, stream=None):
+    rc = lib.fp8_quantize(_ref(desc(x)), granularity, out_dtype, layout, _ref(desc(out)), _ref(desc(out_t)),
+                          _ref(desc(inv_scales)), _ref(desc(offsets)), _ptr(workspace),
+                          0 if workspace is None else workspace.numel() * workspace.element_size(),
+                          _ptr(status), _stream(stream))
+    _check(rc, "fp8_quantize")
+
+
+def fp8_scaled_mm(A, B, sA, sB, out, flags=0, status=None, stream=None):
+    rc = lib.fp8_scaled_mm(_ref(desc(A)), _ref(desc(B)), _ref(desc(sA)), _ref(desc(sB)), _ref(desc(out)), flags,
+                           _ptr(status), _stream(stream))
+    _check(rc, "fp8_scaled_mm")
+
+
+def fp8_grouped_mm(A, B, offsets, sA, sB, out, mode, flags=0, status=None, stream=None):
+    rc = lib.fp8_grouped_mm(_ref(desc(A)), _ref(desc(B)), _ref(desc(offsets)), _ref(desc(sA)), _ref(desc(sB)),
+                            _ref(desc(out)), mode, flags, _ptr(status), _stream(stream))
+    _check(rc, "fp8_grouped_mm")
+
+
+def make_saved(x_q, x_inv, w_q, w_inv, xt_q=None, wt_q=None) -> Fp8LinearSaved:
+    s = Fp8LinearSaved()
+    s.x_q, s.x_inv, s.w_q, s.w_inv = desc(x_q), desc(x_inv), desc(w_q), desc(w_inv)
+    if xt_q is not None:
+        s.xt_q = desc(xt_q)
+    if wt_q is not None:
+        s.wt_q = desc(wt_q)
+    return s
+
+
+def fp8_linear_fwd(x, w, granularity, flags, y, saved: Fp8LinearSaved, workspace=None, status=None, stream=None):
+    rc = lib.fp8_linear_fwd(_ref(desc(x)), _ref(desc(w)), granularity, flags, _ref(desc(y)), ctypes.byref(saved),
+                            _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+                            _ptr(status), _stream(stream))
+    _check(rc, "fp8_linear_fwd")
+
+
+def fp8_linear_bwd(dy, saved: Fp8LinearSaved, x, w, granularity, wgrad_mode, dx, dw, workspace=None, status=None,
+                   stream=None):
+    rc = lib.fp8_linear_bwd(_ref(desc(dy)), ctypes.byref(saved), _ref(desc(x)), _ref(desc(w)), granularity,
+                            wgrad_mode, _ref(desc(dx)), _ref(desc(dw)), _ptr(workspace),
+                            0 if workspace is None else workspace.numel() * workspace.element_size(),
+                            _ptr(status), _stream(stream))
+    _check(rc, "fp8_linear_bwd")
+
+
+def fp8_workspace_size(op, d0=0, d1=0, d2=0, granularity=0, wgrad_mode=0) -> int:
+    return int(lib.fp8_workspace_size(op, d0, d1, d2, granularity, wgrad_mode))
+
+
+def fp8_jagged_padded_rows(rows: int, n_segments: int) -> int:
+    return int(lib.fp8_jagged_padded_rows(rows, n_segments))
+
+
+def fp8_set_wait_limit_ns(ns: int) -> int:
+    return int(lib.fp8_set_wait_limit_ns(ns))
+
+
+# ------------------------------------------------------------------------------------------
+# allocation helpers (torch buffers of the right shapes, then the entry points above)
+
+def quantize_alloc(x, granularity, out_dtype, layout=None, offsets=None, padded_rows=None, stream=None):
+    """Returns (out or None, out_t or None, inv_scales). Shapes follow include/fp8lin.h."""
+    dev = x.device
+    if layout is None:
+        layout = LAYOUT_COL_MAJOR if granularity == GRAN_COL else LAYOUT_ROW_MAJOR
+    fdt = FP8_TORCH[out_dtype]
+    R, C = x.shape[-2], x.shape[-1]
+    B = x.shape[0] if x.dim() == 3 else 1
+    out = torch.empty(x.shape, dtype=fdt, device=dev) if layout & LAYOUT_ROW_MAJOR else None
+    out_t = None
+    ws = None
+    if granularity == GRAN_TENSOR:
+        inv = torch.empty(1, dtype=torch.float32, device=dev)
+        ws = torch.empty(1, dtype=torch.int32, device=dev)
+        if layout & LAYOUT_COL_MAJOR:
+            out_t = torch.empty((C, R), dtype=fdt, device=dev)
+    elif granularity == GRAN_ROW:
+        inv = torch.empty(x.shape[:-1], dtype=torch.float32, device=dev)
+    else:
+        if offsets is not None:
+            E = offsets.numel()
+            P = padded_rows or fp8_jagged_padded_rows(R, E)
+            out_t = torch.empty((C, P), dtype=fdt, device=dev)
+            inv = torch.empty((E, C), dtype=torch.float32, device=dev)
+        else:
+            out_t = torch.empty((B, C, R) if x.dim() == 3 else (C, R), dtype=fdt, device=dev)
+            inv = torch.empty((B, C) if x.dim() == 3 else (C,), dtype=torch.float32, device=dev)
+    fp8_quantize(x, granularity, out_dtype, layout, out, out_t, inv, offsets, ws, stream=stream)
+    return out, out_t, inv

@@ -1,0 +1,505 @@
+// C ABI of fp8lin: argument checking, launch context, TMA descriptor encoding, and the
+// composition of the Linear forward / backward passes from the quantize and GEMM launchers.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+
+namespace fp8lin {
+
+static std::atomic<uint64_t> g_wait_ns{4000000000ull};
+
+int make_ctx(Ctx* ctx, void* stream, int32_t* status) {
+  static std::mutex mu;
+  static int sms[64];
+  static int ok[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8_ERR_DEVICE;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (ok[dev] == 0) {
+      int major = 0, minor = 0, n = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FP8_ERR_DEVICE;
+      ok[dev] = (major == 10 && minor == 3) ? 1 : -1;  // the kernels are built for sm_103a only
+      sms[dev] = n;
+    }
+    if (ok[dev] < 0) return FP8_ERR_DEVICE;
+    ctx->sm_count = sms[dev];
+  }
+  ctx->device = dev;
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  ctx->status = status;
+  ctx->wait_ns = g_wait_ns.load();
+  return FP8_OK;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int make_tmap(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int rank, const uint64_t* dims,
+              const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return FP8_ERR_CUDA;
+  cuuint64_t d[5];
+  cuuint64_t s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  CUresult r = fn(map, dt, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // namespace fp8lin
+
+using namespace fp8lin;
+
+// ------------------------------------------------------------------------------------------
+// argument helpers
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool is_fp8(int dt) { return dt == FP8_DT_E4M3 || dt == FP8_DT_E5M2; }
+static bool is_out(int dt) { return dt == FP8_DT_BF16 || dt == FP8_DT_F32; }
+static int64_t numel(const fp8_tensor* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+static bool valid_desc(const fp8_tensor* t) {
+  if (!t || t->ndim < 1 || t->ndim > 3) return false;
+  for (int i = 0; i < t->ndim; ++i)
+    if (t->shape[i] < 0) return false;
+  return t->ptr != nullptr || numel(t) == 0;
+}
+static bool shape_is(const fp8_tensor* t, int nd, int64_t a, int64_t b = -1, int64_t c = -1) {
+  if (t->ndim != nd) return false;
+  const int64_t s[3] = {a, b, c};
+  for (int i = 0; i < nd; ++i)
+    if (t->shape[i] != s[i]) return false;
+  return true;
+}
+static int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+#define FP8_CHECK(cond, code) \
+  do {                        \
+    if (!(cond)) return (code); \
+  } while (0)
+#define FP8_TRY(expr)        \
+  do {                       \
+    int rc_ = (expr);        \
+    if (rc_ != FP8_OK) return rc_; \
+  } while (0)
+
+// ------------------------------------------------------------------------------------------
+
+extern "C" int64_t fp8_jagged_padded_rows(int64_t rows, int64_t n_segments) {
+  if (rows < 0 || n_segments < 0) return -1;
+  return round_up(rows + 127 * n_segments, 16);
+}
+
+extern "C" uint64_t fp8_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns ? ns : 1); }
+
+extern "C" const char* fp8_status_string(int code) {
+  switch (code) {
+    case FP8_OK: return "ok";
+    case FP8_ERR_INVALID_ARG: return "invalid argument (null pointer, dtype, rank or shape)";
+    case FP8_ERR_UNSUPPORTED: return "unsupported combination of arguments";
+    case FP8_ERR_ALIGNMENT: return "pointer or contiguous row not 16-byte aligned";
+    case FP8_ERR_WORKSPACE: return "workspace missing or too small";
+    case FP8_ERR_CUDA: return "CUDA runtime or launch failure";
+    case FP8_ERR_DEVICE: return "no sm_103 device current";
+    case FP8_DEV_BAD_OFFSETS: return "device: offsets not non-decreasing or last != total rows";
+    case FP8_DEV_TIMEOUT: return "device: a bounded wait ran out";
+    case FP8_DEV_BAD_OFFSETS | FP8_DEV_TIMEOUT: return "device: bad offsets and a wait ran out";
+    default: return "unknown status";
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// fp8_quantize
+
+static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layout, fp8_tensor* out,
+                         fp8_tensor* out_t, fp8_tensor* inv, const fp8_tensor* offsets, void* ws, size_t ws_bytes,
+                         const Ctx& c) {
+  FP8_CHECK(valid_desc(x) && x->dtype == FP8_DT_BF16 && (x->ndim == 2 || x->ndim == 3), FP8_ERR_INVALID_ARG);
+  FP8_CHECK(is_fp8(out_dtype), FP8_ERR_INVALID_ARG);
+  FP8_CHECK(layout >= 1 && layout <= 3, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(valid_desc(inv) && inv->dtype == FP8_DT_F32, FP8_ERR_INVALID_ARG);
+  const int nd = x->ndim;
+  const int64_t B = nd == 3 ? x->shape[0] : 1, R = x->shape[nd - 2], C = x->shape[nd - 1];
+  FP8_CHECK(C % 8 == 0 && aligned16(x->ptr), FP8_ERR_ALIGNMENT);
+  FP8_CHECK(B * R < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
+  const bool want_row = layout & FP8_LAYOUT_ROW_MAJOR, want_col = layout & FP8_LAYOUT_COL_MAJOR;
+  if (want_row) {
+    FP8_CHECK(valid_desc(out) && out->dtype == out_dtype && out->ndim == nd, FP8_ERR_INVALID_ARG);
+    for (int i = 0; i < nd; ++i) FP8_CHECK(out->shape[i] == x->shape[i], FP8_ERR_INVALID_ARG);
+    FP8_CHECK(aligned16(out->ptr), FP8_ERR_ALIGNMENT);
+  }
+  if (want_col) {
+    FP8_CHECK(valid_desc(out_t) && out_t->dtype == out_dtype, FP8_ERR_INVALID_ARG);
+    FP8_CHECK(aligned16(out_t->ptr), FP8_ERR_ALIGNMENT);
+  }
+  switch (gran) {
+    case FP8_GRAN_TENSOR: {
+      FP8_CHECK(offsets == nullptr, FP8_ERR_UNSUPPORTED);
+      FP8_CHECK(numel(inv) == 1, FP8_ERR_INVALID_ARG);
+      if (want_col) {
+        FP8_CHECK(nd == 2, FP8_ERR_UNSUPPORTED);
+        FP8_CHECK(shape_is(out_t, 2, C, R), FP8_ERR_INVALID_ARG);
+        FP8_CHECK(R % 16 == 0, FP8_ERR_ALIGNMENT);
+      }
+      FP8_CHECK(ws && ws_bytes >= 4 && (reinterpret_cast<uintptr_t>(ws) & 3u) == 0, FP8_ERR_WORKSPACE);
+      return launch_quant_tensor(x->ptr, B * R, C, out_dtype, want_row ? out->ptr : nullptr,
+                                 want_col ? out_t->ptr : nullptr, static_cast<float*>(inv->ptr),
+                                 static_cast<uint32_t*>(ws), c);
+    }
+    case FP8_GRAN_ROW: {
+      FP8_CHECK(offsets == nullptr, FP8_ERR_UNSUPPORTED);
+      FP8_CHECK(layout == FP8_LAYOUT_ROW_MAJOR, FP8_ERR_UNSUPPORTED);
+      FP8_CHECK(numel(inv) == B * R, FP8_ERR_INVALID_ARG);
+      FP8_CHECK(C <= 65536, FP8_ERR_UNSUPPORTED);
+      return launch_quant_rows(x->ptr, B * R, C, out_dtype, out->ptr, static_cast<float*>(inv->ptr), c);
+    }
+    case FP8_GRAN_COL: {
+      FP8_CHECK(layout == FP8_LAYOUT_COL_MAJOR, FP8_ERR_UNSUPPORTED);
+      if (offsets) {
+        FP8_CHECK(nd == 2, FP8_ERR_UNSUPPORTED);
+        FP8_CHECK(valid_desc(offsets) && offsets->dtype == FP8_DT_I32 && offsets->ndim == 1 && offsets->shape[0] >= 1,
+                  FP8_ERR_INVALID_ARG);
+        const int64_t E = offsets->shape[0];
+        FP8_CHECK(out_t->ndim == 2 && out_t->shape[0] == C, FP8_ERR_INVALID_ARG);
+        const int64_t P = out_t->shape[1];
+        FP8_CHECK(P >= fp8_jagged_padded_rows(R, E), FP8_ERR_INVALID_ARG);
+        FP8_CHECK(P % 16 == 0, FP8_ERR_ALIGNMENT);
+        FP8_CHECK(numel(inv) == E * C, FP8_ERR_INVALID_ARG);
+        return launch_quant_cols(x->ptr, R, C, E, 0, static_cast<const int32_t*>(offsets->ptr), out_dtype,
+                                 out_t->ptr, P, static_cast<float*>(inv->ptr), c);
+      }
+      FP8_CHECK(R % 16 == 0, FP8_ERR_ALIGNMENT);
+      if (nd == 2)
+        FP8_CHECK(shape_is(out_t, 2, C, R), FP8_ERR_INVALID_ARG);
+      else
+        FP8_CHECK(shape_is(out_t, 3, B, C, R), FP8_ERR_INVALID_ARG);
+      FP8_CHECK(numel(inv) == B * C, FP8_ERR_INVALID_ARG);
+      return launch_quant_cols(x->ptr, B * R, C, B, R, nullptr, out_dtype, out_t->ptr, R,
+                               static_cast<float*>(inv->ptr), c);
+    }
+    default:
+      return FP8_ERR_INVALID_ARG;
+  }
+}
+
+extern "C" int fp8_quantize(const fp8_tensor* x, int granularity, int out_dtype, int layout, fp8_tensor* out,
+                            fp8_tensor* out_t, fp8_tensor* inv_scales, const fp8_tensor* offsets, void* workspace,
+                            size_t workspace_bytes, int32_t* d_status, void* stream) {
+  Ctx c;
+  FP8_TRY(make_ctx(&c, stream, d_status));
+  return quantize_impl(x, granularity, out_dtype, layout, out, out_t, inv_scales, offsets, workspace,
+                       workspace_bytes, c);
+}
+
+// ------------------------------------------------------------------------------------------
+// fp8_scaled_mm
+
+static int dense_gemm(const void* A, int a_dt, int a_mn, const void* B, int b_dt, int b_mn, const float* sA,
+                      int64_t sA_len, const float* sB, int64_t sB_len, void* out, int out_dt, int64_t M, int64_t N,
+                      int64_t K, const Ctx& c) {
+  GemmArgs g = {};
+  g.A = A;
+  g.B = B;
+  g.a_dtype = a_dt;
+  g.b_dtype = b_dt;
+  g.a_mn = a_mn;
+  g.b_mn = b_mn;
+  g.sA = sA;
+  g.sB = sB;
+  g.sA_len = sA_len;
+  g.sB_len = sB_len;
+  g.out = out;
+  g.out_dtype = out_dt;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.mode = -1;
+  return launch_gemm(g, c);
+}
+
+static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA, const fp8_tensor* sB,
+                          fp8_tensor* out, int flags, const Ctx& c) {
+  FP8_CHECK(valid_desc(A) && valid_desc(B) && valid_desc(out) && A->ndim == 2 && B->ndim == 2 && out->ndim == 2,
+            FP8_ERR_INVALID_ARG);
+  FP8_CHECK(is_out(out->dtype), FP8_ERR_INVALID_ARG);
+  FP8_CHECK(aligned16(A->ptr) && aligned16(B->ptr) && aligned16(out->ptr), FP8_ERR_ALIGNMENT);
+  const bool fp8 = is_fp8(A->dtype);
+  if (fp8) {
+    FP8_CHECK(is_fp8(B->dtype), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(!(A->dtype == FP8_DT_E5M2 && B->dtype == FP8_DT_E5M2), FP8_ERR_UNSUPPORTED);
+    FP8_CHECK((flags & (FP8_MM_A_MN_MAJOR | FP8_MM_B_MN_MAJOR)) == 0, FP8_ERR_UNSUPPORTED);
+    const int64_t M = A->shape[0], K = A->shape[1], N = B->shape[0];
+    FP8_CHECK(B->shape[1] == K && shape_is(out, 2, M, N), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(K % 16 == 0, FP8_ERR_ALIGNMENT);
+    FP8_CHECK(valid_desc(sA) && valid_desc(sB) && sA->dtype == FP8_DT_F32 && sB->dtype == FP8_DT_F32,
+              FP8_ERR_INVALID_ARG);
+    const int64_t la = numel(sA), lb = numel(sB);
+    FP8_CHECK((la == 1 || la == M) && (lb == 1 || lb == N), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
+    if (M == 0 || N == 0) return FP8_OK;
+    return dense_gemm(A->ptr, A->dtype, 0, B->ptr, B->dtype, 0, static_cast<const float*>(sA->ptr), la,
+                      static_cast<const float*>(sB->ptr), lb, out->ptr, out->dtype, M, N, K, c);
+  }
+  FP8_CHECK(A->dtype == FP8_DT_BF16 && B->dtype == FP8_DT_BF16, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(sA == nullptr && sB == nullptr, FP8_ERR_INVALID_ARG);
+  const int a_mn = (flags & FP8_MM_A_MN_MAJOR) ? 1 : 0, b_mn = (flags & FP8_MM_B_MN_MAJOR) ? 1 : 0;
+  const int64_t M = a_mn ? A->shape[1] : A->shape[0], K = a_mn ? A->shape[0] : A->shape[1];
+  const int64_t N = b_mn ? B->shape[1] : B->shape[0], K2 = b_mn ? B->shape[0] : B->shape[1];
+  FP8_CHECK(K == K2 && shape_is(out, 2, M, N), FP8_ERR_INVALID_ARG);
+  FP8_CHECK(A->shape[1] % 8 == 0 && B->shape[1] % 8 == 0, FP8_ERR_ALIGNMENT);
+  if (M == 0 || N == 0) return FP8_OK;
+  return dense_gemm(A->ptr, FP8_DT_BF16, a_mn, B->ptr, FP8_DT_BF16, b_mn, nullptr, 0, nullptr, 0, out->ptr,
+                    out->dtype, M, N, K, c);
+}
+
+extern "C" int fp8_scaled_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA, const fp8_tensor* sB,
+                             fp8_tensor* out, int flags, int32_t* d_status, void* stream) {
+  Ctx c;
+  FP8_TRY(make_ctx(&c, stream, d_status));
+  return scaled_mm_impl(A, B, sA, sB, out, flags, c);
+}
+
+// ------------------------------------------------------------------------------------------
+// fp8_grouped_mm
+
+extern "C" int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* offsets,
+                              const fp8_tensor* sA, const fp8_tensor* sB, fp8_tensor* out, int mode, int flags,
+                              int32_t* d_status, void* stream) {
+  (void)flags;
+  Ctx c;
+  FP8_TRY(make_ctx(&c, stream, d_status));
+  FP8_CHECK(valid_desc(A) && valid_desc(B) && valid_desc(out) && valid_desc(offsets) && valid_desc(sA) &&
+                valid_desc(sB),
+            FP8_ERR_INVALID_ARG);
+  FP8_CHECK(is_fp8(A->dtype) && is_fp8(B->dtype) && is_out(out->dtype), FP8_ERR_INVALID_ARG);
+  FP8_CHECK(!(A->dtype == FP8_DT_E5M2 && B->dtype == FP8_DT_E5M2), FP8_ERR_UNSUPPORTED);
+  FP8_CHECK(offsets->dtype == FP8_DT_I32 && offsets->ndim == 1 && offsets->shape[0] >= 1, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(sA->dtype == FP8_DT_F32 && sB->dtype == FP8_DT_F32, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(aligned16(A->ptr) && aligned16(B->ptr) && aligned16(out->ptr), FP8_ERR_ALIGNMENT);
+  const int64_t E = offsets->shape[0];
+  GemmArgs g = {};
+  g.A = A->ptr;
+  g.B = B->ptr;
+  g.a_dtype = A->dtype;
+  g.b_dtype = B->dtype;
+  g.sA = static_cast<const float*>(sA->ptr);
+  g.sB = static_cast<const float*>(sB->ptr);
+  g.out = out->ptr;
+  g.out_dtype = out->dtype;
+  g.mode = mode;
+  g.ends = static_cast<const int32_t*>(offsets->ptr);
+  g.E = E;
+  if (mode == FP8_GROUPED_JAGGED_M) {
+    FP8_CHECK(A->ndim == 2 && B->ndim == 3 && B->shape[0] == E, FP8_ERR_INVALID_ARG);
+    const int64_t M = A->shape[0], K = A->shape[1], N = B->shape[1];
+    FP8_CHECK(B->shape[2] == K && shape_is(out, 2, M, N), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(numel(sA) == M && numel(sB) == E * N, FP8_ERR_INVALID_ARG);
+    FP8_CHECK(K % 16 == 0, FP8_ERR_ALIGNMENT);
+    FP8_CHECK(M < (int64_t(1) << 31) && E * N < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.sA_len = M;
+    g.sB_len = E * N;
+    if (M == 0 || N == 0) return FP8_OK;
+    return launch_gemm(g, c);
+  }
+  if (mode == FP8_GROUPED_JAGGED_K) {
+    FP8_CHECK(A->ndim == 2 && B->ndim == 2 && A->shape[1] == B->shape[1], FP8_ERR_INVALID_ARG);
+    const int64_t N = A->shape[0], Kd = B->shape[0], P = A->shape[1];
+    FP8_CHECK(shape_is(out, 3, E, N, Kd), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(numel(sA) == E * N && numel(sB) == E * Kd, FP8_ERR_INVALID_ARG);
+    FP8_CHECK(P % 16 == 0, FP8_ERR_ALIGNMENT);
+    g.M = N;
+    g.N = Kd;
+    g.K = P;
+    g.k_dim = Kd;
+    g.sA_len = E * N;
+    g.sB_len = E * Kd;
+    if (N == 0 || Kd == 0) return FP8_OK;
+    return launch_gemm(g, c);
+  }
+  return FP8_ERR_INVALID_ARG;
+}
+
+// ------------------------------------------------------------------------------------------
+// Linear forward / backward
+
+static fp8_tensor T2(void* p, int dt, int64_t a, int64_t b) {
+  fp8_tensor t = {};
+  t.ptr = p;
+  t.dtype = dt;
+  t.ndim = 2;
+  t.shape[0] = a;
+  t.shape[1] = b;
+  return t;
+}
+static fp8_tensor T1(void* p, int dt, int64_t a) {
+  fp8_tensor t = {};
+  t.ptr = p;
+  t.dtype = dt;
+  t.ndim = 1;
+  t.shape[0] = a;
+  return t;
+}
+
+// Workspace layout of the backward pass (each piece 256-byte aligned).
+struct BwdLayout {
+  size_t amax, dy_q, dy_inv, dyt_q, dyt_inv, wt_q, wt_inv, xt_q, xt_inv, total;
+};
+static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad) {
+  BwdLayout L = {};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += (size_t)round_up((int64_t)bytes, 256);
+    return o;
+  };
+  const bool rows = gran == FP8_GRAN_ROW, fp8w = wgrad == FP8_WGRAD_FP8;
+  L.amax = take(4);
+  L.dy_q = take((size_t)(M * N));
+  L.dy_inv = take((size_t)(rows ? M : 1) * 4);
+  L.dyt_q = fp8w ? take((size_t)(N * M)) : 0;
+  L.dyt_inv = (fp8w && rows) ? take((size_t)N * 4) : 0;
+  L.wt_q = rows ? take((size_t)(K * N)) : 0;
+  L.wt_inv = rows ? take((size_t)K * 4) : 0;
+  L.xt_q = (fp8w && rows) ? take((size_t)(K * M)) : 0;
+  L.xt_inv = (fp8w && rows) ? take((size_t)K * 4) : 0;
+  L.total = off;
+  return L;
+}
+
+extern "C" size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granularity, int wgrad_mode) {
+  switch (op) {
+    case FP8_OP_QUANTIZE:
+      return granularity == FP8_GRAN_TENSOR ? 4 : 0;
+    case FP8_OP_LINEAR_FWD:
+      return granularity == FP8_GRAN_TENSOR ? 256 : 0;
+    case FP8_OP_LINEAR_BWD:
+      return bwd_layout(d0, d1, d2, granularity, wgrad_mode).total;
+    default:
+      return 0;
+  }
+}
+
+extern "C" int fp8_linear_fwd(const fp8_tensor* x, const fp8_tensor* w, int granularity, int flags, fp8_tensor* y,
+                              fp8_linear_saved* saved, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                              void* stream) {
+  Ctx c;
+  FP8_TRY(make_ctx(&c, stream, d_status));
+  FP8_CHECK(valid_desc(x) && valid_desc(w) && valid_desc(y) && saved, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(x->ndim == 2 && w->ndim == 2 && x->dtype == FP8_DT_BF16 && w->dtype == FP8_DT_BF16, FP8_ERR_INVALID_ARG);
+  const int64_t M = x->shape[0], K = x->shape[1], N = w->shape[0];
+  FP8_CHECK(w->shape[1] == K, FP8_ERR_INVALID_ARG);
+  if (granularity == FP8_GRAN_TENSOR) {
+    FP8_CHECK(workspace && workspace_bytes >= 4, FP8_ERR_WORKSPACE);
+    const int xl = saved->xt_q.ptr ? FP8_LAYOUT_BOTH : FP8_LAYOUT_ROW_MAJOR;
+    FP8_TRY(quantize_impl(x, FP8_GRAN_TENSOR, FP8_DT_E4M3, xl, &saved->x_q, &saved->xt_q, &saved->x_inv, nullptr,
+                          workspace, workspace_bytes, c));
+    FP8_TRY(quantize_impl(w, FP8_GRAN_TENSOR, FP8_DT_E4M3, FP8_LAYOUT_BOTH, &saved->w_q, &saved->wt_q, &saved->w_inv,
+                          nullptr, workspace, workspace_bytes, c));
+  } else if (granularity == FP8_GRAN_ROW) {
+    FP8_TRY(quantize_impl(x, FP8_GRAN_ROW, FP8_DT_E4M3, FP8_LAYOUT_ROW_MAJOR, &saved->x_q, nullptr, &saved->x_inv,
+                          nullptr, nullptr, 0, c));
+    FP8_TRY(quantize_impl(w, FP8_GRAN_ROW, FP8_DT_E4M3, FP8_LAYOUT_ROW_MAJOR, &saved->w_q, nullptr, &saved->w_inv,
+                          nullptr, nullptr, 0, c));
+  } else {
+    return FP8_ERR_INVALID_ARG;
+  }
+  (void)M;
+  (void)N;
+  return scaled_mm_impl(&saved->x_q, &saved->w_q, &saved->x_inv, &saved->w_inv, y, flags & FP8_MM_FAST_ACCUM, c);
+}
+
+extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* saved, const fp8_tensor* x,
+                              const fp8_tensor* w, int granularity, int wgrad_mode, fp8_tensor* dx, fp8_tensor* dw,
+                              void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream) {
+  Ctx c;
+  FP8_TRY(make_ctx(&c, stream, d_status));
+  FP8_CHECK(valid_desc(dy) && saved && dy->ndim == 2 && dy->dtype == FP8_DT_BF16, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(granularity == FP8_GRAN_TENSOR || granularity == FP8_GRAN_ROW, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(wgrad_mode == FP8_WGRAD_FP8 || wgrad_mode == FP8_WGRAD_BF16, FP8_ERR_INVALID_ARG);
+  const int64_t M = dy->shape[0], N = dy->shape[1];
+  FP8_CHECK(saved->x_q.ndim == 2 && saved->x_q.shape[0] == M, FP8_ERR_INVALID_ARG);
+  const int64_t K = saved->x_q.shape[1];
+  const bool rows = granularity == FP8_GRAN_ROW, fp8w = wgrad_mode == FP8_WGRAD_FP8;
+  const bool need_dw = dw && dw->ptr;
+  const BwdLayout L = bwd_layout(M, K, N, granularity, wgrad_mode);
+  FP8_CHECK(workspace && workspace_bytes >= L.total, FP8_ERR_WORKSPACE);
+  FP8_CHECK(aligned16(workspace), FP8_ERR_ALIGNMENT);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fp8_tensor dy_q = T2(ws + L.dy_q, FP8_DT_E5M2, M, N);
+  fp8_tensor dy_inv = T1(ws + L.dy_inv, FP8_DT_F32, rows ? M : 1);
+  fp8_tensor dyt_q = T2(fp8w ? ws + L.dyt_q : nullptr, FP8_DT_E5M2, N, M);
+  if (!rows) {
+    const int layout = (fp8w && need_dw) ? FP8_LAYOUT_BOTH : FP8_LAYOUT_ROW_MAJOR;
+    FP8_TRY(quantize_impl(dy, FP8_GRAN_TENSOR, FP8_DT_E5M2, layout, &dy_q, &dyt_q, &dy_inv, nullptr, ws + L.amax, 4,
+                          c));
+    if (dx && dx->ptr)
+      FP8_TRY(scaled_mm_impl(&dy_q, &saved->wt_q, &dy_inv, &saved->w_inv, dx, 0, c));
+    if (need_dw) {
+      if (fp8w) {
+        FP8_CHECK(saved->xt_q.ptr, FP8_ERR_INVALID_ARG);
+        FP8_TRY(scaled_mm_impl(&dyt_q, &saved->xt_q, &dy_inv, &saved->x_inv, dw, 0, c));
+      } else {
+        FP8_CHECK(valid_desc(x) && x->dtype == FP8_DT_BF16, FP8_ERR_INVALID_ARG);
+        FP8_TRY(scaled_mm_impl(dy, x, nullptr, nullptr, dw, FP8_MM_A_MN_MAJOR | FP8_MM_B_MN_MAJOR, c));
+      }
+    }
+    return FP8_OK;
+  }
+  // row granularity
+  FP8_TRY(quantize_impl(dy, FP8_GRAN_ROW, FP8_DT_E5M2, FP8_LAYOUT_ROW_MAJOR, &dy_q, nullptr, &dy_inv, nullptr,
+                        nullptr, 0, c));
+  if (dx && dx->ptr) {
+    FP8_CHECK(valid_desc(w) && w->dtype == FP8_DT_BF16 && shape_is(w, 2, N, K), FP8_ERR_INVALID_ARG);
+    fp8_tensor wt_q = T2(ws + L.wt_q, FP8_DT_E4M3, K, N);
+    fp8_tensor wt_inv = T1(ws + L.wt_inv, FP8_DT_F32, K);
+    FP8_TRY(quantize_impl(w, FP8_GRAN_COL, FP8_DT_E4M3, FP8_LAYOUT_COL_MAJOR, nullptr, &wt_q, &wt_inv, nullptr,
+                          nullptr, 0, c));
+    FP8_TRY(scaled_mm_impl(&dy_q, &wt_q, &dy_inv, &wt_inv, dx, 0, c));
+  }
+  if (need_dw) {
+    FP8_CHECK(valid_desc(x) && x->dtype == FP8_DT_BF16 && shape_is(x, 2, M, K), FP8_ERR_INVALID_ARG);
+    if (fp8w) {
+      fp8_tensor dyt_inv = T1(ws + L.dyt_inv, FP8_DT_F32, N);
+      fp8_tensor xt_q = T2(ws + L.xt_q, FP8_DT_E4M3, K, M);
+      fp8_tensor xt_inv = T1(ws + L.xt_inv, FP8_DT_F32, K);
+      FP8_TRY(quantize_impl(dy, FP8_GRAN_COL, FP8_DT_E5M2, FP8_LAYOUT_COL_MAJOR, nullptr, &dyt_q, &dyt_inv, nullptr,
+                            nullptr, 0, c));
+      FP8_TRY(quantize_impl(x, FP8_GRAN_COL, FP8_DT_E4M3, FP8_LAYOUT_COL_MAJOR, nullptr, &xt_q, &xt_inv, nullptr,
+                            nullptr, 0, c));
+      FP8_TRY(scaled_mm_impl(&dyt_q, &xt_q, &dyt_inv, &xt_inv, dw, 0, c));
+    } else {
+      FP8_TRY(scaled_mm_impl(dy, x, nullptr, nullptr, dw, FP8_MM_A_MN_MAJOR | FP8_MM_B_MN_MAJOR, c));
+    }
+  }
+  return FP8_OK;
+}

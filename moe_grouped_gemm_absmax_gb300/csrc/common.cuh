@@ -1,0 +1,250 @@
+// Device helpers shared by the fp8lin kernels (sm_103a): inline PTX for mbarriers, TMA,
+// tcgen05 / tensor memory, FP8 conversion, bounded waits and the status word.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp8lin.h"
+
+#define FP8_DEVI __device__ __forceinline__
+
+namespace fp8lin {
+
+// ------------------------------------------------------------------------------------------
+// Formats: largest finite magnitude (e4m3fn 1.75 * 2^8, e5m2 1.75 * 2^15).
+constexpr float kE4M3Max = 448.0f;
+constexpr float kE5M2Max = 57344.0f;
+// Lower clamp of amax before the fp64 division.
+constexpr double kEps = 1e-12;
+
+FP8_DEVI uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+FP8_DEVI uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Status word: conditions found on the device are OR-ed in with a relaxed atomic.
+FP8_DEVI void set_status(int32_t* st, int32_t bits) {
+  if (st) atomicOr(st, bits);
+}
+
+// ------------------------------------------------------------------------------------------
+// Scale step: scale64 = fp8_max / max(amax, eps) with an IEEE fp64 division; the fp32 multiply
+// uses scale64 rounded to fp32; the inverse handed to the GEMM is the correctly rounded fp64
+// reciprocal of scale64, rounded to fp32.
+struct Scale {
+  float s32;
+  float inv32;
+};
+FP8_DEVI Scale make_scale(float amax, float fp8_max) {
+  double a = static_cast<double>(amax);
+  a = a < kEps ? kEps : a;
+  double s = __ddiv_rn(static_cast<double>(fp8_max), a);
+  Scale r;
+  r.s32 = __double2float_rn(s);
+  r.inv32 = __double2float_rn(__drcp_rn(s));
+  return r;
+}
+
+// bf16 bit pattern -> fp32 (exact).
+FP8_DEVI float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// Round-to-nearest-even, saturating casts of two fp32 values into two packed FP8 codes;
+// `lo` lands in the low byte (the lower address).
+template <int FMT>
+FP8_DEVI uint32_t cvt_fp8x2(float lo, float hi) {
+  uint16_t r;
+  if (FMT == FP8_DT_E4M3)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// x * scale in fp32, clamp to +-fp8_max (NaN passes through), cast. Two bf16 in, two codes out.
+template <int FMT>
+FP8_DEVI uint32_t quant_bf16x2(uint32_t two_bf16, float s32, float fmax) {
+  float a = __fmul_rn(__uint_as_float(two_bf16 << 16), s32);
+  float b = __fmul_rn(__uint_as_float(two_bf16 & 0xFFFF0000u), s32);
+  a = a > fmax ? fmax : (a < -fmax ? -fmax : a);
+  b = b > fmax ? fmax : (b < -fmax ? -fmax : b);
+  return cvt_fp8x2<FMT>(a, b);
+}
+
+// 8 bf16 (one 16-byte vector) -> 8 codes (8 bytes).
+template <int FMT>
+FP8_DEVI uint2 quant_vec8(uint4 v, float s32, float fmax) {
+  uint2 o;
+  o.x = quant_bf16x2<FMT>(v.x, s32, fmax) | (quant_bf16x2<FMT>(v.y, s32, fmax) << 16);
+  o.y = quant_bf16x2<FMT>(v.z, s32, fmax) | (quant_bf16x2<FMT>(v.w, s32, fmax) << 16);
+  return o;
+}
+
+// Elementwise unsigned max of the |bf16| patterns in two packed pairs. For non-negative
+// bf16 values the bit pattern orders like the value, so amax needs no float compare.
+FP8_DEVI uint32_t absmax2(uint32_t acc, uint32_t v) { return __vmaxu2(acc, v & 0x7FFF7FFFu); }
+FP8_DEVI uint32_t absmax_vec8(uint32_t acc, uint4 v) {
+  acc = absmax2(acc, v.x);
+  acc = absmax2(acc, v.y);
+  acc = absmax2(acc, v.z);
+  return absmax2(acc, v.w);
+}
+// Larger of the two halves of a packed pair, as a bf16 pattern in the low 16 bits.
+FP8_DEVI uint32_t absmax_fold(uint32_t acc) {
+  uint32_t lo = acc & 0xFFFFu, hi = acc >> 16;
+  return lo > hi ? lo : hi;
+}
+
+// Relaxed (no fences) atomic max, for the commutative amax reduction.
+FP8_DEVI void red_max_relaxed(uint32_t* addr, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+// ------------------------------------------------------------------------------------------
+// Streaming global loads / stores.
+FP8_DEVI uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ------------------------------------------------------------------------------------------
+// mbarrier
+FP8_DEVI void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+FP8_DEVI void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+FP8_DEVI void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+FP8_DEVI void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+FP8_DEVI void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+FP8_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete. Returns false when `limit_ns` elapsed or
+// when another role raised `*abort` (abort may be null).
+FP8_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// TMA (cp.async.bulk.tensor): global -> shared, completion counted on an mbarrier in bytes.
+FP8_DEVI void tma_prefetch_desc(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+FP8_DEVI void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+FP8_DEVI void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// ------------------------------------------------------------------------------------------
+// tcgen05: tensor memory allocation, MMA issue, commit, loads, fences.
+FP8_DEVI void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+FP8_DEVI void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory"); }
+FP8_DEVI void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+FP8_DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+FP8_DEVI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D(tmem) (+)= A(smem desc) * B(smem desc); kind::f8f6f4 (FP8 operands, K = 32 per issue).
+FP8_DEVI void umma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// kind::f16 (BF16 operands, K = 16 per issue).
+FP8_DEVI void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
+FP8_DEVI void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 32 bit, 16 consecutive columns: thread i of the warp receives lane (base + i).
+FP8_DEVI void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+FP8_DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading- and
+// stride-dimension byte offsets (in 16-byte units), version 1, swizzle mode in bits 61..63
+// (2 = 128-byte swizzle).
+FP8_DEVI uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16 / kind::f8f6f4: fp32 accumulator, operand formats,
+// operand majors (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t a_mn, uint32_t b_mn,
+                                                  uint32_t M, uint32_t N) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
+}
+// Operand format codes: kind::f8f6f4 e4m3 = 0, e5m2 = 1; kind::f16 bf16 = 1.
+constexpr uint32_t kFmtE4M3 = 0, kFmtE5M2 = 1, kFmtBF16 = 1;
+
+}  // namespace fp8lin

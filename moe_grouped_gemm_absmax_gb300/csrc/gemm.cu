@@ -1,0 +1,550 @@
+// Scaled FP8 (and BF16) GEMMs on the 5th-generation tensor cores (sm_103a): dense, and the MoE
+// grouped GEMM with rows or contraction jagged by expert.
+//
+//   D[m, n] = sA[m] * sB[n] * sum_k A[m, k] * B[n, k]       (dequant contract: "FP8 Training:
+//   Quantization, Autograd, Torchao", section 2; operand layouts: section 4)
+//   grouped: per-row sA, per-expert-column sB, rows routed by cumulative offsets ("FP8 training
+//   on AMD GPUs with TorchTitan and TorchAO", "Scaling FP8 to MoE Architectures", Figure 3).
+//
+// Design (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: 128 x 128-byte A tile + 256 x 128-byte B tile per stage, 128-byte
+//               swizzle, into a 4-stage ring guarded by full/empty mbarriers;
+//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma (M=128, N=256; K=32 for
+//               FP8, K=16 for BF16) into one of two fp32 accumulators, and commits each stage
+//               back to the producer and each finished tile to the epilogue;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns 32 TMEM lanes = rows),
+//               sA[m] * sB[n] applied once, one rounding to bf16/fp32, masked stores. The
+//               second accumulator lets the next tile's MMAs overlap this epilogue.
+// Every wait is bounded; on a timeout the kernel raises FP8_DEV_TIMEOUT, drains in-flight TMA
+// and MMA work, frees its tensor memory and returns.
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp8lin {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BKB = 128;  // tile rows, tile columns, K bytes per stage
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BKB;
+constexpr int B_BYTES = BN * BKB;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 2 * BN;
+constexpr int kMaxExperts = 2048;
+constexpr int kGroupM = 16;  // rasterization: tiles walk 16 M-blocks per N-block
+
+enum { kDense = 0, kJagM = 1, kJagK = 2 };
+enum { kFP8 = 0, kBF16 = 1 };
+
+struct GemmParams {
+  int64_t M, N, K;     // tile space: rows of D, columns of D, contraction length (elements)
+  int64_t num_m, num_n;
+  int64_t nkb;         // K blocks per tile (dense, jagged M)
+  const float* sA;
+  const float* sB;
+  int sa_scalar, sb_scalar;
+  void* out;
+  int out_f32;
+  int vec_ok;          // 16-byte aligned output rows
+  int64_t ldo;         // output row stride (elements)
+  const int32_t* ends;
+  int E;
+  int64_t total_rows;  // jagged: last valid offset
+  uint32_t idesc;
+  int32_t* status;
+  uint64_t wait_ns;
+};
+
+struct Tile {
+  int64_t m0, n0;   // first row / column of D
+  int64_t row_end;  // rows >= row_end are masked (segment end, or M)
+  int64_t k0;       // first contraction coordinate
+  int64_t nkb;      // K blocks
+  int e;            // expert (jagged)
+};
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+FP8_DEVI int find_expert(const int32_t* tpre, int E, int64_t t) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tpre[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int SCHED>
+FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t, const int32_t* tpre, const int32_t* aux) {
+  Tile T;
+  if (SCHED == kDense) {
+    const int64_t per_group = (int64_t)kGroupM * p.num_n;
+    const int64_t g = t / per_group, r = t % per_group;
+    const int64_t first_m = g * kGroupM;
+    const int64_t gsz = p.num_m - first_m < kGroupM ? p.num_m - first_m : kGroupM;
+    const int64_t mb = first_m + r % gsz, nb = r / gsz;
+    T.m0 = mb * BM;
+    T.n0 = nb * BN;
+    T.row_end = p.M;
+    T.k0 = 0;
+    T.nkb = p.nkb;
+    T.e = 0;
+  } else if (SCHED == kJagM) {
+    const int e = find_expert(tpre, p.E, t);
+    const int64_t local = t - tpre[e];
+    const int64_t mb = local / p.num_n, nb = local % p.num_n;
+    T.m0 = aux[e] + mb * BM;  // aux[e] = segment start row
+    T.n0 = nb * BN;
+    T.row_end = aux[e + 1];
+    T.k0 = 0;
+    T.nkb = p.nkb;
+    T.e = e;
+  } else {
+    const int64_t per = p.num_m * p.num_n;
+    const int e = (int)(t / per);
+    const int64_t local = t % per;
+    T.m0 = (local / p.num_n) * BM;
+    T.n0 = (local % p.num_n) * BN;
+    T.row_end = p.M;
+    T.k0 = aux[e];                             // aux[e] = padded start of segment e
+    T.nkb = (aux[e + 1] - aux[e]) / BKB;       // padded length / 128
+    T.e = e;
+  }
+  return T;
+}
+
+template <int KIND, int SCHED, int A_MN, int B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Shared& S = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES);
+  int32_t* tpre = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + 256);
+  int32_t* aux = tpre + (p.E + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* abort_flag = &S.abort;
+
+  // ---- jagged schedules: validate offsets, per-expert tile prefix and row / K starts ----
+  int64_t total;
+  if (SCHED == kDense) {
+    total = p.num_m * p.num_n;
+  } else {
+    int bad = 0;
+    for (int e = tid; e < p.E; e += kThreads) {
+      const int32_t cur = p.ends[e], prev = e ? p.ends[e - 1] : 0;
+      if (cur < prev || (SCHED != kJagK && e == p.E - 1 && cur != p.total_rows)) bad = 1;
+      const int64_t cnt = cur > prev ? cur - prev : 0;
+      if (SCHED == kJagM) {
+        tpre[e + 1] = (int32_t)(((cnt + BM - 1) / BM) * p.num_n);
+        aux[e + 1] = cur;
+      } else {
+        tpre[e + 1] = (int32_t)(p.num_m * p.num_n);
+        aux[e + 1] = (int32_t)(((cnt + BKB - 1) / BKB) * BKB);
+      }
+    }
+    if (tid == 0) {
+      tpre[0] = 0;
+      aux[0] = 0;
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+      if (blockIdx.x == 0 && tid == 0) set_status(p.status, FP8_DEV_BAD_OFFSETS);
+      return;
+    }
+    if (warp == 0) {  // inclusive scans (tile prefix always; padded K prefix for jagged K)
+      int carry = 0, carry2 = 0;
+      for (int base = 0; base < p.E; base += 32) {
+        const int i = base + lane;
+        int v = i < p.E ? tpre[i + 1] : 0;
+        int w = (SCHED == kJagK && i < p.E) ? aux[i + 1] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, v, o);
+          const int z = __shfl_up_sync(0xffffffffu, w, o);
+          if (lane >= o) {
+            v += y;
+            w += z;
+          }
+        }
+        if (i < p.E) {
+          tpre[i + 1] = v + carry;
+          if (SCHED == kJagK) aux[i + 1] = w + carry2;
+        }
+        carry += __shfl_sync(0xffffffffu, v, 31);
+        carry2 += __shfl_sync(0xffffffffu, w, 31);
+      }
+    }
+    __syncthreads();
+    total = tpre[p.E];
+    if (SCHED == kJagK && aux[p.E] > p.K) {  // segments do not fit the padded operand
+      if (blockIdx.x == 0 && tid == 0) set_status(p.status, FP8_DEV_BAD_OFFSETS);
+      return;
+    }
+  }
+
+  // ---- barriers and tensor memory ----
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.tfull[b], 1);
+      mbar_init(&S.tempty[b], 4);
+    }
+    mbar_init(&S.drain, 1);
+    S.abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = S.tmem_base;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(p.status, FP8_DEV_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ================================ TMA producer ================================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile T = get_tile<SCHED>(p, t, tpre, aux);
+        for (int64_t kb = 0; kb < T.nkb; ++kb) {
+          if (!mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
+            if (!*abort_flag) fail();
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          uint8_t* sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(&S.full[stage], STAGE_BYTES);
+          if (KIND == kFP8) {
+            const int32_t kx = (int32_t)(T.k0 + kb * BKB);
+            tma_load_2d(sa, &tmA, &S.full[stage], kx, (int32_t)T.m0);
+            if (SCHED == kJagM)
+              tma_load_3d(sb, &tmB, &S.full[stage], kx, (int32_t)T.n0, T.e);
+            else
+              tma_load_2d(sb, &tmB, &S.full[stage], kx, (int32_t)T.n0);
+          } else {
+            const int32_t kx = (int32_t)(kb * (BKB / 2));  // 64 bf16 per block
+            if (A_MN) {
+              tma_load_2d(sa, &tmA, &S.full[stage], (int32_t)T.m0, kx);
+              tma_load_2d(sa + 8192, &tmA, &S.full[stage], (int32_t)T.m0 + 64, kx);
+            } else {
+              tma_load_2d(sa, &tmA, &S.full[stage], kx, (int32_t)T.m0);
+            }
+            if (B_MN) {
+#pragma unroll
+              for (int h = 0; h < 4; ++h) tma_load_2d(sb + h * 8192, &tmB, &S.full[stage], (int32_t)T.n0 + 64 * h, kx);
+            } else {
+              tma_load_2d(sb, &tmB, &S.full[stage], kx, (int32_t)T.n0);
+            }
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Drain: the last (up to STAGES) loads must land before the CTA may exit.
+      const int64_t first = issued > STAGES ? issued - STAGES : 0;
+      for (int64_t i = first; i < issued; ++i)
+        mbar_wait(&S.full[i % STAGES], (uint32_t)((i / STAGES) & 1), nullptr, p.wait_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================ MMA issuer ================================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile T = get_tile<SCHED>(p, t, tpre, aux);
+        if (T.nkb == 0) continue;
+        if (!mbar_wait(&S.tempty[buf], aphase ^ 1, abort_flag, p.wait_ns)) {
+          if (!*abort_flag) fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        for (int64_t kb = 0; kb < T.nkb; ++kb) {
+          if (!mbar_wait(&S.full[stage], phase, abort_flag, p.wait_ns)) {
+            if (!*abort_flag) fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, 8192, 1024) : smem_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc(sb + kk * 2048, 8192, 1024) : smem_desc(sb + kk * 32, 16, 1024);
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            if (KIND == kFP8)
+              umma_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
+            else
+              umma_f16(d_tmem, ad, bd, p.idesc, acc);
+          }
+          umma_commit(&S.empty[stage]);  // frees the stage once these MMAs have read it
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&S.tfull[buf]);  // accumulator ready for the epilogue
+        if (++buf == 2) {
+          buf = 0;
+          aphase ^= 1;
+        }
+      }
+      // Drain every MMA this thread issued before the tensor memory is released.
+      umma_commit(&S.drain);
+      mbar_wait(&S.drain, 0, nullptr, p.wait_ns);
+    }
+    __syncwarp();
+  } else {
+    // ================================ epilogue ================================
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int buf = 0;
+    uint32_t aphase = 0;
+    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile T = get_tile<SCHED>(p, t, tpre, aux);
+      const int64_t m = T.m0 + row;
+      const bool row_ok = m < T.row_end;
+      int64_t orow = m;  // output row index
+      if (SCHED == kJagK) orow = (int64_t)T.e * p.M + m;
+      if (T.nkb == 0) {  // empty segment (jagged K): the result is zero
+        if (row_ok) {
+          for (int64_t n = T.n0; n < T.n0 + BN && n < p.N; ++n) {
+            if (p.out_f32)
+              static_cast<float*>(p.out)[orow * p.ldo + n] = 0.0f;
+            else
+              static_cast<uint16_t*>(p.out)[orow * p.ldo + n] = 0;
+          }
+        }
+        continue;
+      }
+      if (!mbar_wait(&S.tfull[buf], aphase, abort_flag, p.wait_ns)) {
+        if (!*abort_flag) fail();
+        break;
+      }
+      tc_fence_after();
+      float sa = 1.0f;
+      if (KIND == kFP8 && row_ok) {
+        if (SCHED == kJagK)
+          sa = __ldg(p.sA + (int64_t)T.e * p.M + m);
+        else
+          sa = p.sa_scalar ? __ldg(p.sA) : __ldg(p.sA + m);
+      }
+      const float* sbp = p.sB;
+      if (KIND == kFP8) {
+        if (SCHED == kJagM) sbp += (int64_t)T.e * p.N;
+        if (SCHED == kJagK) sbp += (int64_t)T.e * p.N;
+      }
+      const uint32_t taddr = tmem_base + (uint32_t)(buf * BN) + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 16; ++ch) {
+        uint32_t v[16];
+        tmem_ld16(taddr + ch * 16, v);
+        tmem_ld_wait();
+        const int64_t n = T.n0 + ch * 16;
+        if (row_ok && n < p.N) {
+          float f[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float sb = 1.0f;
+            if (KIND == kFP8) {
+              if (p.sb_scalar) sb = __ldg(sbp);
+              else if (n + j < p.N) sb = __ldg(sbp + n + j);
+            }
+            f[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sa), sb);
+          }
+          const bool full16 = p.vec_ok && n + 16 <= p.N;
+          if (p.out_f32) {
+            float* o = static_cast<float*>(p.out) + orow * p.ldo + n;
+            if (full16) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(o + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+            } else {
+              for (int j = 0; j < 16 && n + j < p.N; ++j) o[j] = f[j];
+            }
+          } else {
+            uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + n;
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+              w[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            if (full16) {
+              *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4*>(o + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+              for (int j = 0; j < 16 && n + j < p.N; ++j) o[j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.tempty[buf]);
+      if (++buf == 2) {
+        buf = 0;
+        aphase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int KIND, int SCHED, int A_MN, int B_MN>
+int run(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int64_t total_tiles_hint, const Ctx& c) {
+  auto kern = gemm_kernel<KIND, SCHED, A_MN, B_MN>;
+  const size_t smem = 1024 + STAGES * STAGE_BYTES + 256 + (SCHED == kDense ? 0 : 2 * 4 * (p.E + 1));
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return FP8_ERR_CUDA;
+  int64_t grid = c.sm_count;
+  if (total_tiles_hint > 0 && total_tiles_hint < grid) grid = total_tiles_hint;
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kThreads, smem, c.stream>>>(a, b, p);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_gemm(const GemmArgs& g, const Ctx& c) {
+  const bool fp8 = g.a_dtype != FP8_DT_BF16;
+  GemmParams p = {};
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.sA = g.sA;
+  p.sB = g.sB;
+  p.out = g.out;
+  p.out_f32 = g.out_dtype == FP8_DT_F32;
+  p.status = c.status;
+  p.wait_ns = c.wait_ns;
+  p.ends = g.ends;
+  p.E = (int)g.E;
+  p.num_m = (g.M + BM - 1) / BM;
+  p.num_n = (g.N + BN - 1) / BN;
+  const int esz = fp8 ? 1 : 2;
+  p.nkb = (g.K * esz + BKB - 1) / BKB;
+  p.ldo = g.N;
+  p.vec_ok = p.out_f32 ? (p.ldo % 4 == 0) : (p.ldo % 8 == 0);
+  if (g.mode != -1 && (g.E < 1 || g.E > kMaxExperts)) return FP8_ERR_UNSUPPORTED;
+
+  if (fp8) {
+    const uint32_t af = g.a_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
+    const uint32_t bf = g.b_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
+    p.idesc = make_idesc(af, bf, 0, 0, BM, BN);
+    p.sa_scalar = g.sA_len == 1;
+    p.sb_scalar = g.sB_len == 1;
+    CUtensorMap ta, tb;
+    const uint32_t boxA[2] = {BKB, BM};
+    const uint64_t dA[2] = {(uint64_t)g.K, (uint64_t)g.M};
+    const uint64_t sA_[1] = {(uint64_t)g.K};
+    if (g.mode == -1) {
+      int rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, sA_, boxA, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc) return rc;
+      const uint64_t dB[2] = {(uint64_t)g.K, (uint64_t)g.N};
+      const uint32_t boxB[2] = {BKB, BN};
+      rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dB, sA_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc) return rc;
+      return run<kFP8, kDense, 0, 0>(ta, tb, p, p.num_m * p.num_n, c);
+    }
+    if (g.mode == FP8_GROUPED_JAGGED_M) {
+      p.total_rows = g.M;
+      int rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, sA_, boxA, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc) return rc;
+      const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.E};
+      const uint64_t sB_[2] = {(uint64_t)g.K, (uint64_t)(g.N * g.K)};
+      const uint32_t boxB[3] = {BKB, BN, 1};
+      rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dB, sB_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc) return rc;
+      return run<kFP8, kJagM, 0, 0>(ta, tb, p, 0, c);
+    }
+    // jagged K: A = G^T [N_out, P], B = X^T [Kd, P]; tile space M = N_out, N = Kd. The offsets
+    // are checked for order and for fitting the padded length P.
+    p.total_rows = -1;
+    int rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, sA_, boxA, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    const uint64_t dB[2] = {(uint64_t)g.K, (uint64_t)g.N};
+    const uint32_t boxB[2] = {BKB, BN};
+    rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dB, sA_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    return run<kFP8, kJagK, 0, 0>(ta, tb, p, (int64_t)g.E * p.num_m * p.num_n, c);
+  }
+
+  // BF16 (dense only)
+  if (g.mode != -1) return FP8_ERR_UNSUPPORTED;
+  p.idesc = make_idesc(kFmtBF16, kFmtBF16, (uint32_t)g.a_mn, (uint32_t)g.b_mn, BM, BN);
+  CUtensorMap ta, tb;
+  int rc;
+  if (g.a_mn) {
+    const uint64_t d[2] = {(uint64_t)g.M, (uint64_t)g.K};
+    const uint64_t s[1] = {(uint64_t)g.M * 2};
+    const uint32_t box[2] = {64, 64};
+    rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, s, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    const uint64_t d[2] = {(uint64_t)g.K, (uint64_t)g.M};
+    const uint64_t s[1] = {(uint64_t)g.K * 2};
+    const uint32_t box[2] = {64, BM};
+    rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, s, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (rc) return rc;
+  if (g.b_mn) {
+    const uint64_t d[2] = {(uint64_t)g.N, (uint64_t)g.K};
+    const uint64_t s[1] = {(uint64_t)g.N * 2};
+    const uint32_t box[2] = {64, 64};
+    rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, s, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    const uint64_t d[2] = {(uint64_t)g.K, (uint64_t)g.N};
+    const uint64_t s[1] = {(uint64_t)g.K * 2};
+    const uint32_t box[2] = {64, BN};
+    rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, s, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (rc) return rc;
+  const int64_t tiles = p.num_m * p.num_n;
+  if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1>(ta, tb, p, tiles, c);
+  if (g.a_mn) return run<kBF16, kDense, 1, 0>(ta, tb, p, tiles, c);
+  if (g.b_mn) return run<kBF16, kDense, 0, 1>(ta, tb, p, tiles, c);
+  return run<kBF16, kDense, 0, 0>(ta, tb, p, tiles, c);
+}
+
+}  // namespace fp8lin

@@ -1,0 +1,64 @@
+// Host-side internals of fp8lin: launch context, tensor-map encoding and the kernel launchers
+// that the C ABI (api.cu) composes.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp8lin.h"
+
+namespace fp8lin {
+
+struct Ctx {
+  cudaStream_t stream;
+  int32_t* status;   // device status word (may be null)
+  uint64_t wait_ns;  // bound of every on-device wait
+  int sm_count;
+  int device;
+};
+
+// Fills ctx for the current device; returns FP8_OK or FP8_ERR_DEVICE.
+int make_ctx(Ctx* ctx, void* stream, int32_t* status);
+
+// 2-D / 3-D tiled tensor maps (row-major tensors; dims listed innermost first).
+int make_tmap(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int rank, const uint64_t* dims,
+              const uint64_t* strides_bytes /* rank-1 entries */, const uint32_t* box, CUtensorMapSwizzle swz);
+
+// --- quantize launchers (quantize.cu) ---
+// Rowwise: x bf16 [R, C] -> q [R, C], inv [R].
+int launch_quant_rows(const void* x, int64_t R, int64_t C, int fmt, void* q, float* inv, const Ctx& c);
+// Tensorwise: amax of x [R, C] into amax_ws (one u32, zeroed here), then the cast into q (row-major,
+// may be null) and/or qt ([C, R], may be null); inv [1].
+int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
+                        uint32_t* amax_ws, const Ctx& c);
+// Columnwise with column-major output. x viewed as [rows_total, C]. Groups of rows share one
+// scale per column: either n_groups consecutive groups of group_rows rows (ends == null) or the
+// segments given by ends[n_groups] (segment-padded output, padded row count ld_out).
+// out_t row (g, c) starts at out_t + (g * C + c) * ld_out (dense) or out_t + c * ld_out + pstart_g
+// (segments). inv [n_groups, C].
+int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
+                      const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, const Ctx& c);
+
+// --- GEMM launchers (gemm.cu) ---
+struct GemmArgs {
+  // operands
+  const void* A;
+  const void* B;
+  int a_dtype, b_dtype;   // FP8_DT_*
+  int a_mn, b_mn;         // BF16 only: operand stored MN-major
+  const float* sA;        // [1] or [M] (dense), [M] (jagged M), [E, M-dim] (jagged K); null for BF16
+  const float* sB;
+  int64_t sA_len, sB_len; // dense: 1 or M / 1 or N
+  void* out;
+  int out_dtype;          // FP8_DT_BF16 / FP8_DT_F32
+  int64_t M, N, K;        // dense problem; jagged M: M = total rows; jagged K: K = padded rows P
+  // grouped
+  int mode;               // -1 dense, FP8_GROUPED_JAGGED_M, FP8_GROUPED_JAGGED_K
+  const int32_t* ends;
+  int64_t E;
+  int64_t k_dim;          // jagged K: the output's last dimension (X's columns)
+};
+int launch_gemm(const GemmArgs& g, const Ctx& c);
+
+}  // namespace fp8lin
