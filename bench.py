@@ -1,0 +1,586 @@
+"""Benchmark of the FP8 dynamic-scaling linear on one or more GB300s (one process per GPU).
+
+Default workload: the Llama3-8B-shaped MLP-up Linear, forward + backward, rowwise scaling,
+M=8192 tokens, K=4096, N=14336, x with 1% outlier channels, forward and grad-input GEMMs in FP8
+(e4m3 / e5m2), the weight-gradient GEMM in bf16 (the high-precision wgrad recipe). One step =
+quantize x, quantize W, FP8 forward GEMM, quantize dY, quantize W column-wise (column-major
+output), FP8 grad-input GEMM, bf16 weight-gradient GEMM: 7 kernels, 2.886 TFLOP.
+
+Other workloads (`--workload`): linear-tensorwise-256x512, colwise-8192x14336, dsv3-moe-fwd,
+llama4-moe-fwdbwd.
+
+`value` = whole-job throughput with inputs resident in HBM (CUDA events around each step on the
+launching stream, L2 flushed between steps by writing a 256 MiB buffer outside the events);
+`e2e` = the same metric through the public entry points with host buffers (pinned host->device
+copies of the step's inputs and device->host copies of its outputs inside the timed region).
+`--impl reference` times the CPU oracle (the plain C restatement used by the tests) on a bounded
+sample of the same workload; it is a deliberately slow reference, not a target.
+
+Under torchrun (WORLD_SIZE > 1) every rank runs an independent replica of the workload on its
+own GPU (the path shards by tokens / experts with no data exchange): weak scaling, the timing is
+the max over ranks, and `value` counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "quantize GB/s & FP8 (grouped) GEMM TFLOPS at 1 GB300; % of roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sust=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------------------------------
+# Workload steps. Each builds its buffers once; run(mark) launches the step's kernels in order,
+# calling mark(label) before each launch (used to drop CUDA events between kernels).
+
+class Step:
+    name = ""
+    unit = "TFLOP/s"
+    kernels: list = []  # (label, kind "tensor"|"hbm", amount per launch (flop or byte), peak key)
+
+    def total_units(self):  # flop (TFLOP/s metrics) or byte (GB/s metrics) per step
+        raise NotImplementedError
+
+
+class DenseLinearStep(Step):
+    """Linear fwd+bwd, rowwise FP8 (fwd, dX) and bf16 dW."""
+
+    def __init__(self, fp8, M, K, N, seed=0, device="cuda"):
+        self.fp8, self.M, self.K, self.N = fp8, M, K, N
+        self.name = "llama3-8b-mlp-up" if (M, K, N) == (8192, 4096, 14336) else f"linear-rowwise-{M}x{K}x{N}"
+        self.x, self.w, self.dy = W.linear_inputs(M, K, N, seed=seed, device=device, outliers=True)
+        d = device
+        e4, e5 = torch.float8_e4m3fn, torch.float8_e5m2
+        self.xq = torch.empty((M, K), dtype=e4, device=d)
+        self.xi = torch.empty(M, device=d)
+        self.wq = torch.empty((N, K), dtype=e4, device=d)
+        self.wi = torch.empty(N, device=d)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+        self.dyq = torch.empty((M, N), dtype=e5, device=d)
+        self.dyi = torch.empty(M, device=d)
+        self.wtq = torch.empty((K, N), dtype=e4, device=d)
+        self.wti = torch.empty(K, device=d)
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=d)
+        self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=d)
+        f = 2.0 * M * N * K
+        self.kernels = [
+            ("quantize_rows x e4m3", "hbm", 3 * M * K + 4 * M, "hbm"),
+            ("quantize_rows W e4m3", "hbm", 3 * N * K + 4 * N, "hbm"),
+            ("gemm_fp8 fwd", "tensor", f, "fp8"),
+            ("quantize_rows dY e5m2", "hbm", 3 * M * N + 4 * M, "hbm"),
+            ("quantize_cols W e4m3 col-major", "hbm", 3 * N * K + 4 * K, "hbm"),
+            ("gemm_fp8 dX", "tensor", f, "fp8"),
+            ("gemm_bf16 dW", "tensor", f, "bf16"),
+        ]
+
+    def total_units(self):
+        return 3 * 2.0 * self.M * self.N * self.K
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_quantize(self.x, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.xq, None, self.xi)
+        mark(1)
+        f.fp8_quantize(self.w, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.wq, None, self.wi)
+        mark(2)
+        f.fp8_scaled_mm(self.xq, self.wq, self.xi, self.wi, self.y, f.MM_FAST_ACCUM)
+        mark(3)
+        f.fp8_quantize(self.dy, f.GRAN_ROW, f.DT_E5M2, f.LAYOUT_ROW_MAJOR, self.dyq, None, self.dyi)
+        mark(4)
+        f.fp8_quantize(self.w, f.GRAN_COL, f.DT_E4M3, f.LAYOUT_COL_MAJOR, None, self.wtq, self.wti)
+        mark(5)
+        f.fp8_scaled_mm(self.dyq, self.wtq, self.dyi, self.wti, self.dx, 0)
+        mark(6)
+        f.fp8_scaled_mm(self.dy, self.x, None, None, self.dw, f.MM_A_MN_MAJOR | f.MM_B_MN_MAJOR)
+
+    # e2e: the public Linear entry points with host buffers
+    def e2e_setup(self):
+        f = self.fp8
+        self.h_in = [t.cpu().pin_memory() for t in (self.x, self.w, self.dy)]
+        self.h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (self.y, self.dx, self.dw)]
+        self.saved = f.make_saved(self.xq, self.xi, self.wq, self.wi)
+        self.ws = torch.empty(max(f.fp8_workspace_size(f.OP_LINEAR_BWD, self.M, self.K, self.N, f.GRAN_ROW,
+                                                       f.WGRAD_BF16), 256), dtype=torch.uint8, device="cuda")
+        return sum(t.numel() * t.element_size() for t in self.h_in), \
+            sum(t.numel() * t.element_size() for t in self.h_out)
+
+    def e2e_run(self):
+        f = self.fp8
+        for d, h in zip((self.x, self.w, self.dy), self.h_in):
+            d.copy_(h, non_blocking=True)
+        f.fp8_linear_fwd(self.x, self.w, f.GRAN_ROW, f.MM_FAST_ACCUM, self.y, self.saved)
+        f.fp8_linear_bwd(self.dy, self.saved, self.x, self.w, f.GRAN_ROW, f.WGRAD_BF16, self.dx, self.dw, self.ws)
+        for d, h in zip((self.y, self.dx, self.dw), self.h_out):
+            h.copy_(d, non_blocking=True)
+
+    def cpu_sample(self, rows):
+        return dense_cpu_sample(self.x[:rows].cpu(), self.w.cpu(), self.dy[:rows].cpu(), self.M)
+
+
+def dense_cpu_sample(x, w, dy, full_rows):
+    """The oracle (as it stands) on the first rows of x / dY and all of W: the same quantize and
+    GEMM steps as one dense Linear step, on fewer tokens."""
+    import oracle
+    M, K = x.shape
+    N = w.shape[0]
+    xb, wb, db = W.bf16_bits(x), W.bf16_bits(w), W.bf16_bits(dy)
+
+    def run():
+        xq, xi = oracle.quantize_rows(xb, oracle.E4M3)
+        wq, wi = oracle.quantize_rows(wb, oracle.E4M3)
+        oracle.gemm_fp8(xq, oracle.E4M3, wq, oracle.E4M3, xi, wi)
+        dq, di = oracle.quantize_rows(db, oracle.E5M2)
+        wc, wci = oracle.quantize_cols(wb, oracle.E4M3)
+        oracle.gemm_fp8(dq, oracle.E5M2, wc, oracle.E4M3, di, wci, b_trans=True)
+        oracle.gemm_bf16(db, xb, a_trans=True, b_trans=True)
+    return run, 3 * 2.0 * M * N * K, f"llama3-8b-mlp-up step on the first {M} of {full_rows} tokens (all of W)"
+
+
+class TensorwiseLinearStep(Step):
+    """Single Linear fwd+bwd, tensorwise, fp32 outputs (latency-bound)."""
+
+    def __init__(self, fp8, M=256, K=512, N=256, seed=0, device="cuda"):
+        self.fp8, self.M, self.K, self.N = fp8, M, K, N
+        self.name = "linear-tensorwise-256x512"
+        self.x, self.w, self.dy = W.linear_inputs(M, K, N, seed=seed, device=device)
+        e4 = torch.float8_e4m3fn
+        d = device
+        self.xq, self.xtq = torch.empty((M, K), dtype=e4, device=d), torch.empty((K, M), dtype=e4, device=d)
+        self.wq, self.wtq = torch.empty((N, K), dtype=e4, device=d), torch.empty((K, N), dtype=e4, device=d)
+        self.xi, self.wi = torch.empty(1, device=d), torch.empty(1, device=d)
+        self.saved = fp8.make_saved(self.xq, self.xi, self.wq, self.wi, self.xtq, self.wtq)
+        self.y = torch.empty((M, N), device=d)
+        self.dx = torch.empty((M, K), device=d)
+        self.dw = torch.empty((N, K), device=d)
+        self.wsf = torch.empty(256, dtype=torch.uint8, device=d)
+        self.wsb = torch.empty(fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_TENSOR, fp8.WGRAD_FP8),
+                               dtype=torch.uint8, device=d)
+        f = 2.0 * M * N * K
+        self.kernels = [("linear_fwd (2x quantize tensor dual, gemm)", "tensor", f, "fp8"),
+                        ("linear_bwd (quantize dY dual, gemm dX, gemm dW)", "tensor", 2 * f, "fp8")]
+
+    def total_units(self):
+        return 3 * 2.0 * self.M * self.N * self.K
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_linear_fwd(self.x, self.w, f.GRAN_TENSOR, f.MM_FAST_ACCUM, self.y, self.saved, self.wsf)
+        mark(1)
+        f.fp8_linear_bwd(self.dy, self.saved, self.x, self.w, f.GRAN_TENSOR, f.WGRAD_FP8, self.dx, self.dw, self.wsb)
+
+    def launches_per_step(self):
+        return 9  # three tensorwise quantizes (amax + cast kernels each) and three GEMMs
+
+
+class ColwiseStep(Step):
+    unit = "GB/s"
+
+    def __init__(self, fp8, R=8192, C=14336, RX=8192, CX=4096, seed=0, device="cuda"):
+        self.fp8 = fp8
+        self.name = "colwise-8192x14336"
+        self.g = W.column_gain_bf16((R, C), 1e-3, -2, 2, seed, device)
+        self.xx = W.normal_bf16((RX, CX), 1.0, seed + 1, device)
+        self.gt = torch.empty((C, R), dtype=torch.float8_e5m2, device=device)
+        self.gi = torch.empty(C, device=device)
+        self.xq = torch.empty((RX, CX), dtype=torch.float8_e4m3fn, device=device)
+        self.xi = torch.empty(RX, device=device)
+        self.R, self.C, self.RX, self.CX = R, C, RX, CX
+        self.kernels = [("quantize_cols G e5m2 col-major", "hbm", 3 * R * C + 4 * C, "hbm"),
+                        ("quantize_rows X e4m3", "hbm", 3 * RX * CX + 4 * RX, "hbm")]
+
+    def total_units(self):
+        return float(sum(k[2] for k in self.kernels))
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_quantize(self.g, f.GRAN_COL, f.DT_E5M2, f.LAYOUT_COL_MAJOR, None, self.gt, self.gi)
+        mark(1)
+        f.fp8_quantize(self.xx, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.xq, None, self.xi)
+
+
+class MoeFwdStep(Step):
+    """DeepSeek-V3-shaped grouped GEMM forward: quantize A rowwise, W per (expert, n), grouped GEMM."""
+
+    def __init__(self, fp8, seed=0, device="cuda"):
+        self.fp8 = fp8
+        self.name = "dsv3-moe-fwd"
+        d = W.WORKLOADS[self.name].dims
+        E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+        counts = W.dsv3_counts(seed)
+        self.A, self.Wt, ends, _ = W.moe_inputs(E, M, K, N, counts, seed=seed, device=device)
+        self.ends = torch.from_numpy(ends).to(device)
+        self.counts = counts
+        self.Aq = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=device)
+        self.Ai = torch.empty(M, device=device)
+        self.Wq = torch.empty((E, N, K), dtype=torch.float8_e4m3fn, device=device)
+        self.Wi = torch.empty((E, N), device=device)
+        self.out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.E, self.M, self.K, self.N = E, M, K, N
+        f = 2.0 * M * N * K
+        self.kernels = [("quantize_rows A e4m3", "hbm", 3 * M * K + 4 * M, "hbm"),
+                        ("quantize_rows W[e] e4m3 (per expert column)", "hbm", 3 * E * N * K + 4 * E * N, "hbm"),
+                        ("grouped_gemm_fp8 jagged-M", "tensor", f, "fp8")]
+
+    def total_units(self):
+        return 2.0 * self.M * self.N * self.K
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_quantize(self.A, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Aq, None, self.Ai)
+        mark(1)
+        f.fp8_quantize(self.Wt, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Wq, None, self.Wi)
+        mark(2)
+        f.fp8_grouped_mm(self.Aq, self.Wq, self.ends, self.Ai, self.Wi, self.out, f.GROUPED_JAGGED_M)
+
+
+class MoeFwdBwdStep(Step):
+    """Llama4-shaped grouped fwd + bwd: fwd, dX (per-expert W quantized over N, column-major),
+    dW with jagged column-wise quantization of dY and x inside each segment."""
+
+    def __init__(self, fp8, seed=0, device="cuda"):
+        self.fp8 = fp8
+        self.name = "llama4-moe-fwdbwd"
+        d = W.WORKLOADS[self.name].dims
+        E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+        counts = W.llama4_counts(seed)
+        self.A, self.Wt, ends, self.dY = W.moe_inputs(E, M, K, N, counts, seed=seed, device=device, with_grad=True)
+        self.ends = torch.from_numpy(ends).to(device)
+        e4, e5 = torch.float8_e4m3fn, torch.float8_e5m2
+        P = fp8.fp8_jagged_padded_rows(M, E)
+        self.Aq, self.Ai = torch.empty((M, K), dtype=e4, device=device), torch.empty(M, device=device)
+        self.Wq, self.Wi = torch.empty((E, N, K), dtype=e4, device=device), torch.empty((E, N), device=device)
+        self.out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.dYq, self.dYi = torch.empty((M, N), dtype=e5, device=device), torch.empty(M, device=device)
+        self.Wtq, self.Wti = torch.empty((E, K, N), dtype=e4, device=device), torch.empty((E, K), device=device)
+        self.dX = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+        self.dYt, self.dYti = torch.empty((N, P), dtype=e5, device=device), torch.empty((E, N), device=device)
+        self.At, self.Ati = torch.empty((K, P), dtype=e4, device=device), torch.empty((E, K), device=device)
+        self.dW = torch.empty((E, N, K), dtype=torch.bfloat16, device=device)
+        self.E, self.M, self.K, self.N = E, M, K, N
+        f = 2.0 * M * N * K
+        self.kernels = [("quantize_rows A e4m3", "hbm", 3 * M * K + 4 * M, "hbm"),
+                        ("quantize_rows W[e] e4m3", "hbm", 3 * E * N * K + 4 * E * N, "hbm"),
+                        ("grouped_gemm_fp8 fwd jagged-M", "tensor", f, "fp8"),
+                        ("quantize_rows dY e5m2", "hbm", 3 * M * N + 4 * M, "hbm"),
+                        ("quantize_cols W[e] e4m3 col-major (over N)", "hbm", 3 * E * N * K + 4 * E * K, "hbm"),
+                        ("grouped_gemm_fp8 dX jagged-M", "tensor", f, "fp8"),
+                        ("quantize_cols jagged dY e5m2", "hbm", 3 * M * N + 4 * E * N, "hbm"),
+                        ("quantize_cols jagged A e4m3", "hbm", 3 * M * K + 4 * E * K, "hbm"),
+                        ("grouped_gemm_fp8 dW jagged-K", "tensor", f, "fp8")]
+
+    def total_units(self):
+        return 3 * 2.0 * self.M * self.N * self.K
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_quantize(self.A, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Aq, None, self.Ai)
+        mark(1)
+        f.fp8_quantize(self.Wt, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Wq, None, self.Wi)
+        mark(2)
+        f.fp8_grouped_mm(self.Aq, self.Wq, self.ends, self.Ai, self.Wi, self.out, f.GROUPED_JAGGED_M)
+        mark(3)
+        f.fp8_quantize(self.dY, f.GRAN_ROW, f.DT_E5M2, f.LAYOUT_ROW_MAJOR, self.dYq, None, self.dYi)
+        mark(4)
+        f.fp8_quantize(self.Wt, f.GRAN_COL, f.DT_E4M3, f.LAYOUT_COL_MAJOR, None, self.Wtq, self.Wti)
+        mark(5)
+        f.fp8_grouped_mm(self.dYq, self.Wtq, self.ends, self.dYi, self.Wti, self.dX, f.GROUPED_JAGGED_M)
+        mark(6)
+        f.fp8_quantize(self.dY, f.GRAN_COL, f.DT_E5M2, f.LAYOUT_COL_MAJOR, None, self.dYt, self.dYti, self.ends)
+        mark(7)
+        f.fp8_quantize(self.A, f.GRAN_COL, f.DT_E4M3, f.LAYOUT_COL_MAJOR, None, self.At, self.Ati, self.ends)
+        mark(8)
+        f.fp8_grouped_mm(self.dYt, self.At, self.ends, self.dYti, self.Ati, self.dW, f.GROUPED_JAGGED_K)
+
+
+def make_step(fp8, name):
+    if name == "llama3-8b-mlp-up":
+        return DenseLinearStep(fp8, 8192, 4096, 14336)
+    if name == "linear-tensorwise-256x512":
+        return TensorwiseLinearStep(fp8)
+    if name == "colwise-8192x14336":
+        return ColwiseStep(fp8)
+    if name == "dsv3-moe-fwd":
+        return MoeFwdStep(fp8)
+    if name == "llama4-moe-fwdbwd":
+        return MoeFwdBwdStep(fp8)
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ------------------------------------------------------------------------------------------
+# clocks: nvidia-smi sampled during the timed region
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def traffic_for(label: str):
+    """ncu DRAM bytes per launch for a kernel label, from profiles/ncu_traffic.json; null when the
+    kernel's source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(label)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != ent["sha256"]:
+        return None
+    return ent["bytes_per_launch"]
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, ws, rank):
+    """The oracle as it stands, on the host cores, on a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import oracle
+    if args.workload != "llama3-8b-mlp-up":
+        print(json.dumps({"impl": "reference", "unavailable": "reference arm implemented for the default workload"}))
+        return
+    rows = 16
+    x, w, dy = W.linear_inputs(rows, 4096, 14336, seed=0, outliers=True)
+    run, flops, sample = dense_cpu_sample(x, w, dy, 8192)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = flops * args.steps / dt / 1e12
+    cores = oracle.num_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama3-8b-mlp-up", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="fp8lin", choices=["fp8lin", "reference"])
+    ap.add_argument("--workload", default="llama3-8b-mlp-up", choices=list(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import moe_grouped_gemm_absmax_gb300 as fp8
+    peaks = load_peaks()
+    peak_of = {"hbm": peaks["hbm"], "fp8": 2.0 * peaks["bf16"], "bf16": peaks["bf16"]}
+    step = make_step(fp8, args.workload)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    nk = len(step.kernels)
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # evict L2 (outside the events)
+        ev = evs[i]
+        step.run(lambda k: ev[k].record(stream))
+        ev[nk].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+
+    per_kernel = np.zeros(nk)
+    step_ms = []
+    for ev in evs:
+        t = [ev[k].elapsed_time(ev[k + 1]) for k in range(nk)]
+        per_kernel += t
+        step_ms.append(ev[0].elapsed_time(ev[nk]))
+    per_kernel /= args.steps
+    total_ms = float(np.sum(step_ms))
+    total_ms_max = max_over_ranks(total_ms, ws)
+    units = step.total_units()
+    scale = 1e9 if step.unit == "TFLOP/s" else 1e6  # flop/ms -> TFLOP/s, byte/ms -> GB/s
+    value = units * args.steps * ws / total_ms_max / scale
+
+    kernels = []
+    for (label, kind, amount, pk), ms in zip(step.kernels, per_kernel):
+        if kind == "tensor":
+            ach, unit = amount / ms / 1e9, "TFLOP/s"
+        else:
+            ach, unit = amount / ms / 1e6, "GB/s"
+        kernels.append({"kernel": label, "ms": round(float(ms), 5), "achieved": round(ach, 1), "unit": unit,
+                        "peak": peak_of[pk], "frac": round(ach / peak_of[pk], 4),
+                        "algorithmic": amount, "share": round(float(ms / per_kernel.sum()), 4)})
+    dom = max(range(nk), key=lambda k: per_kernel[k])
+    dk = kernels[dom]
+    roofline = {"kernel": dk["kernel"], "bound": "tensor" if step.kernels[dom][1] == "tensor" else "hbm",
+                "achieved": dk["achieved"], "peak": dk["peak"], "unit": dk["unit"], "frac": dk["frac"],
+                "traffic": traffic_for(dk["kernel"]),
+                "peak_source": f"{peaks['src']} ({'2 x bf16 burst' if step.kernels[dom][3] == 'fp8' else step.kernels[dom][3]})"}
+
+    # e2e through the public entry points with host buffers
+    e2e = None
+    if hasattr(step, "e2e_setup"):
+        h2d, d2h = step.e2e_setup()
+        for _ in range(2):
+            step.e2e_run()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.e2e_steps):
+            step.e2e_run()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(s0.elapsed_time(s1), ws)
+        e2e = {"value": units * args.e2e_steps * ws / ems / scale, "unit": step.unit,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and hasattr(step, "cpu_sample"):
+        import oracle
+        run, work, sample = step.cpu_sample(args.cpu_rows)
+        t0 = time.perf_counter()
+        run()
+        dt = time.perf_counter() - t0
+        cpu = {"value": work / dt / (1e12 if step.unit == "TFLOP/s" else 1e9), "unit": step.unit,
+               "cores": oracle.num_threads(), "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+
+    launches = getattr(step, "launches_per_step", lambda: nk)() * args.steps
+    if rank == 0:
+        cfg = {"workload": step.name, "l2": "flushed between steps (256 MiB write outside the timed events)",
+               "inputs": "seeded synthetic, resident in HBM"}
+        for k in ("M", "K", "N", "E"):
+            if hasattr(step, k):
+                cfg[k] = getattr(step, k)
+        line = {"metric": METRIC, "value": round(value, 2), "unit": step.unit, "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(total_ms_max / args.steps, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp8 e4m3/e5m2 (fp32 accumulate), bf16 wgrad",
+                "data": "synthetic", "config": cfg, "roofline": roofline, "kernels": kernels,
+                "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
+                "wall_s": round(wall, 3), "impl": "fp8lin"}
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
