@@ -214,6 +214,34 @@ int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* saved, const fp
                    fp8_tensor* dw, void* workspace, size_t workspace_bytes, int32_t* d_status,
                    void* stream);
 
+/*
+ * fp8_quantize_tensor_noalloc — the tensorwise quantize of fp8_quantize (FP8_GRAN_TENSOR) for
+ * callers that cannot allocate device memory. The pages have no counterpart: this entry point
+ * exists for callers that hold no allocator and receive no workspace, such as plugin or callback
+ * interfaces that hand the library only its input and output buffers, and runtimes that reserve
+ * all device memory at start-up and forbid cudaMalloc afterwards (cudaMalloc may also
+ * synchronize the device, which latency-bound callers avoid).
+ *
+ * Same arguments and results as fp8_quantize with FP8_GRAN_TENSOR, minus the workspace and the
+ * status word: x bf16 [R, C] (2-D), out / out_t / inv_scale as there. The amax reduction uses a
+ * fixed array in the library's own device memory instead of a workspace: one partial maximum per
+ * 32768 input elements, FP8_NOALLOC_MAX_PARTIALS of them (about 64 KiB), allocated when the
+ * library is loaded on a device and held by every device that loads it until the process exits.
+ *  - x with more than FP8_NOALLOC_MAX_ELEMENTS elements is rejected with FP8_ERR_UNSUPPORTED
+ *    before anything is launched.
+ *  - The first call on each device looks up the array's device address (with that device
+ *    current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its last contents there; each call
+ *    writes every slot it reads before reading it, so nothing needs clearing between calls. Calls
+ *    that can run at the same time on the GPU (different streams without ordering between them)
+ *    race on the array and give wrong scales: order them on one stream or with events.
+ *  - Allocates nothing: no cudaMalloc / cudaFree and no allocating library routine.
+ */
+#define FP8_NOALLOC_MAX_PARTIALS 16384
+#define FP8_NOALLOC_MAX_ELEMENTS (16384LL * 32768LL)
+int fp8_quantize_tensor_noalloc(const fp8_tensor* x, int out_dtype, int layout, fp8_tensor* out,
+                                fp8_tensor* out_t, fp8_tensor* inv_scale, void* stream);
+
 /* Workspace bytes for an operation. FP8_OP_QUANTIZE: (d0, d1, d2) unused except that
  * granularity selects 4 bytes (tensor) or 0. FP8_OP_LINEAR_FWD / FP8_OP_LINEAR_BWD:
  * (d0, d1, d2) = (M, K, N). */

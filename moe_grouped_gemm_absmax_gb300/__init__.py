@@ -77,6 +77,7 @@ def _load():
     L.fp8_status_string.restype = ctypes.c_char_p
     L.fp8_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.fp8_set_wait_limit_ns.restype = ctypes.c_uint64
+    L.fp8_quantize_tensor_noalloc.argtypes = [T, ctypes.c_int, ctypes.c_int, T, T, T, P]
     return L
 
 
@@ -84,7 +85,8 @@ lib = _load()
 
 # Symbols include/fp8lin.h declares (checked by the CPU tests against the header and the .so).
 EXPORTS = ("fp8_quantize", "fp8_scaled_mm", "fp8_grouped_mm", "fp8_linear_fwd", "fp8_linear_bwd",
-           "fp8_workspace_size", "fp8_jagged_padded_rows", "fp8_status_string", "fp8_set_wait_limit_ns")
+           "fp8_workspace_size", "fp8_jagged_padded_rows", "fp8_status_string", "fp8_set_wait_limit_ns",
+           "fp8_quantize_tensor_noalloc")
 
 
 def status_string(code: int) -> str:
@@ -172,6 +174,14 @@ def fp8_linear_bwd(dy, saved: Fp8LinearSaved, x, w, granularity, wgrad_mode, dx,
                             0 if workspace is None else workspace.numel() * workspace.element_size(),
                             _ptr(status), _stream(stream))
     _check(rc, "fp8_linear_bwd")
+
+
+def fp8_quantize_tensor_noalloc(x, out_dtype, layout, out=None, out_t=None, inv_scale=None, stream=None):
+    """Tensorwise quantize without a workspace (the library's fixed device array holds the amax
+    reduction); for callers that cannot allocate. Same results as fp8_quantize(GRAN_TENSOR)."""
+    rc = lib.fp8_quantize_tensor_noalloc(_ref(desc(x)), out_dtype, layout, _ref(desc(out)), _ref(desc(out_t)),
+                                         _ref(desc(inv_scale)), _stream(stream))
+    _check(rc, "fp8_quantize_tensor_noalloc")
 
 
 def fp8_workspace_size(op, d0=0, d1=0, d2=0, granularity=0, wgrad_mode=0) -> int:

@@ -62,3 +62,10 @@ struct GemmArgs {
 int launch_gemm(const GemmArgs& g, const Ctx& c);
 
 }  // namespace fp8lin
+
+namespace fp8lin {
+// Cast phase of the tensorwise quantize alone: reads the bf16 pattern of amax at `amax_word`
+// (already reduced) and writes q / qt / inv exactly as launch_quant_tensor does.
+int launch_quant_tensor_cast(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
+                             const uint32_t* amax_word, const Ctx& c);
+}  // namespace fp8lin

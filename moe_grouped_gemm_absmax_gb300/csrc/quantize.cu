@@ -480,3 +480,20 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
 }
 
 }  // namespace fp8lin
+
+namespace fp8lin {
+
+int launch_quant_tensor_cast(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
+                             const uint32_t* amax_word, const Ctx& c) {
+  dim3 grid((unsigned)ceil_div64(C, kTcCols), (unsigned)ceil_div64(R, kTcRows));
+  if (grid.x == 0 || grid.y == 0) grid = dim3(1, 1);
+  if (fmt == FP8_DT_E4M3)
+    quant_tensor_cast_kernel<FP8_DT_E4M3><<<grid, 256, 0, c.stream>>>(
+        static_cast<const uint16_t*>(x), R, C, amax_word, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv);
+  else
+    quant_tensor_cast_kernel<FP8_DT_E5M2><<<grid, 256, 0, c.stream>>>(
+        static_cast<const uint16_t*>(x), R, C, amax_word, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // namespace fp8lin
