@@ -6,15 +6,17 @@
 //   grouped: per-row sA, per-expert-column sB, rows routed by cumulative offsets ("FP8 training
 //   on AMD GPUs with TorchTitan and TorchAO", "Scaling FP8 to MoE Architectures", Figure 3).
 //
-// Design (one persistent CTA per SM, 192 threads):
+// Design (one persistent CTA per SM, 320 threads):
 //   warp 0      TMA producer: 128 x 128-byte A tile + 256 x 128-byte B tile per stage, 128-byte
 //               swizzle, into a 4-stage ring guarded by full/empty mbarriers;
 //   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma (M=128, N=256; K=32 for
 //               FP8, K=16 for BF16) into one of two fp32 accumulators, and commits each stage
 //               back to the producer and each finished tile to the epilogue;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns 32 TMEM lanes = rows),
-//               sA[m] * sB[n] applied once, one rounding to bf16/fp32, masked stores. The
-//               second accumulator lets the next tile's MMAs overlap this epilogue.
+//   warps 2..9  epilogue: each warp owns 32 TMEM lanes (tile rows) and one half (128 columns)
+//               of the tile; the tile's column scales are staged once in shared memory;
+//               tcgen05.ld 32 columns at a time, sA[m] * sB[n] applied once, one rounding to
+//               bf16/fp32, masked stores. The second accumulator lets the next tile's MMAs
+//               overlap this epilogue.
 // Every wait is bounded; on a timeout the kernel raises FP8_DEV_TIMEOUT, drains in-flight TMA
 // and MMA work, frees its tensor memory and returns.
 #include "common.cuh"
@@ -29,7 +31,8 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BKB;
 constexpr int B_BYTES = BN * BKB;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;  // warps 2..9
 constexpr int kTmemCols = 2 * BN;
 constexpr int kMaxExperts = 2048;
 constexpr int kGroupM = 16;  // rasterization: tiles walk 16 M-blocks per N-block
@@ -65,6 +68,7 @@ struct Tile {
 };
 
 struct Shared {
+  float sb[2][BN];  // per-tile column scales, alternating between consecutive tiles
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tfull[2];
@@ -73,6 +77,8 @@ struct Shared {
   uint32_t tmem_base;
   int abort;
 };
+constexpr int kSharedBytes = 2304;
+static_assert(sizeof(Shared) <= kSharedBytes, "shared block");
 
 FP8_DEVI int find_expert(const int32_t* tpre, int E, int64_t t) {
   int lo = 0, hi = E - 1;
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Shared& S = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES);
-  int32_t* tpre = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + 256);
+  int32_t* tpre = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + kSharedBytes);
   int32_t* aux = tpre + (p.E + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &S.abort;
@@ -201,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.tfull[b], 1);
-      mbar_init(&S.tempty[b], 4);
+      mbar_init(&S.tempty[b], kEpiThreads / 32);
     }
     mbar_init(&S.drain, 1);
     S.abort = 0;
@@ -332,19 +338,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ================================ epilogue ================================
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int c0 = ((warp - 2) >> 2) * (BN / 2);  // first tile column of this warp's half
+    const int etid = tid - 64;           // 0..255 across the epilogue warps
     const int row = q * 32 + lane;
-    int buf = 0;
+    const bool stage_sb = KIND == kFP8 && !p.sb_scalar;
+    int buf = 0, sbi = 0;
     uint32_t aphase = 0;
     for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile T = get_tile<SCHED>(p, t, tpre, aux);
       const int64_t m = T.m0 + row;
       const bool row_ok = m < T.row_end;
-      int64_t orow = m;  // output row index
-      if (SCHED == kJagK) orow = (int64_t)T.e * p.M + m;
+      const int64_t orow = SCHED == kJagK ? (int64_t)T.e * p.M + m : m;
+      const float* sbp = p.sB;
+      if (KIND == kFP8 && SCHED != kDense) sbp += (int64_t)T.e * p.N;
+      if (stage_sb) {  // one column scale per epilogue thread; reused by all 128 rows
+        const int64_t n = T.n0 + etid;
+        S.sb[sbi][etid] = n < p.N ? __ldg(sbp + n) : 0.0f;
+        named_bar_sync(1, kEpiThreads);
+      }
+      const float* sbs = S.sb[sbi];
+      sbi ^= 1;
       if (T.nkb == 0) {  // empty segment (jagged K): the result is zero
         if (row_ok) {
-          for (int64_t n = T.n0; n < T.n0 + BN && n < p.N; ++n) {
+          for (int64_t n = T.n0 + c0; n < T.n0 + c0 + BN / 2 && n < p.N; ++n) {
             if (p.out_f32)
               static_cast<float*>(p.out)[orow * p.ldo + n] = 0.0f;
             else
@@ -353,8 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if (!mbar_wait(&S.tfull[buf], aphase, abort_flag, p.wait_ns)) {
-        if (!*abort_flag) fail();
+      const bool got = mbar_wait(&S.tfull[buf], aphase, abort_flag, p.wait_ns);
+      if (!named_bar_and(2, kEpiThreads, got)) {  // uniform decision across the epilogue warps
+        if (!got && !*abort_flag) fail();
         break;
       }
       tc_fence_after();
@@ -365,51 +383,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           sa = p.sa_scalar ? __ldg(p.sA) : __ldg(p.sA + m);
       }
-      const float* sbp = p.sB;
-      if (KIND == kFP8) {
-        if (SCHED == kJagM) sbp += (int64_t)T.e * p.N;
-        if (SCHED == kJagK) sbp += (int64_t)T.e * p.N;
-      }
-      const uint32_t taddr = tmem_base + (uint32_t)(buf * BN) + ((uint32_t)(q * 32) << 16);
+      const float sb_all = (KIND == kFP8 && p.sb_scalar) ? __ldg(sbp) : 1.0f;
+      const uint32_t taddr = tmem_base + (uint32_t)(buf * BN + c0) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 16; ++ch) {
-        uint32_t v[16];
-        tmem_ld16(taddr + ch * 16, v);
+      for (int ch = 0; ch < BN / 64; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(taddr + ch * 32, v);
         tmem_ld_wait();
-        const int64_t n = T.n0 + ch * 16;
+        const int cl = c0 + ch * 32;  // tile column of v[0]
+        const int64_t n = T.n0 + cl;
         if (row_ok && n < p.N) {
-          float f[16];
+          float f[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float sb = 1.0f;
-            if (KIND == kFP8) {
-              if (p.sb_scalar) sb = __ldg(sbp);
-              else if (n + j < p.N) sb = __ldg(sbp + n + j);
-            }
+          for (int j = 0; j < 32; ++j) {
+            const float sb = stage_sb ? sbs[cl + j] : sb_all;
             f[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sa), sb);
           }
-          const bool full16 = p.vec_ok && n + 16 <= p.N;
+          const bool full = p.vec_ok && n + 32 <= p.N;
           if (p.out_f32) {
             float* o = static_cast<float*>(p.out) + orow * p.ldo + n;
-            if (full16) {
+            if (full) {
 #pragma unroll
-              for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(o + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+              for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(o + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
             } else {
-              for (int j = 0; j < 16 && n + j < p.N; ++j) o[j] = f[j];
+              for (int j = 0; j < 32 && n + j < p.N; ++j) o[j] = f[j];
             }
           } else {
             uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + n;
-            uint32_t w[8];
+            uint32_t w[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 16; ++j) {
               const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
               w[j] = *reinterpret_cast<const uint32_t*>(&h);
             }
-            if (full16) {
-              *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
-              *reinterpret_cast<uint4*>(o + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+            if (full) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 4) *reinterpret_cast<uint4*>(o + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
             } else {
-              for (int j = 0; j < 16 && n + j < p.N; ++j) o[j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+              for (int j = 0; j < 32 && n + j < p.N; ++j) o[j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
             }
           }
         }
@@ -435,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int KIND, int SCHED, int A_MN, int B_MN>
 int run(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int64_t total_tiles_hint, const Ctx& c) {
   auto kern = gemm_kernel<KIND, SCHED, A_MN, B_MN>;
-  const size_t smem = 1024 + STAGES * STAGE_BYTES + 256 + (SCHED == kDense ? 0 : 2 * 4 * (p.E + 1));
+  const size_t smem = 1024 + STAGES * STAGE_BYTES + kSharedBytes + (SCHED == kDense ? 0 : 2 * 4 * (p.E + 1));
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FP8_ERR_CUDA;
   int64_t grid = c.sm_count;
