@@ -199,7 +199,8 @@ def fp8_set_wait_limit_ns(ns: int) -> int:
 # ------------------------------------------------------------------------------------------
 # allocation helpers (torch buffers of the right shapes, then the entry points above)
 
-def quantize_alloc(x, granularity, out_dtype, layout=None, offsets=None, padded_rows=None, stream=None):
+def quantize_alloc(x, granularity, out_dtype, layout=None, offsets=None, padded_rows=None, status=None,
+                   stream=None):
     """Returns (out or None, out_t or None, inv_scales). Shapes follow include/fp8lin.h."""
     dev = x.device
     if layout is None:
@@ -226,5 +227,5 @@ def quantize_alloc(x, granularity, out_dtype, layout=None, offsets=None, padded_
         else:
             out_t = torch.empty((B, C, R) if x.dim() == 3 else (C, R), dtype=fdt, device=dev)
             inv = torch.empty((B, C) if x.dim() == 3 else (C,), dtype=torch.float32, device=dev)
-    fp8_quantize(x, granularity, out_dtype, layout, out, out_t, inv, offsets, ws, stream=stream)
+    fp8_quantize(x, granularity, out_dtype, layout, out, out_t, inv, offsets, ws, status=status, stream=stream)
     return out, out_t, inv

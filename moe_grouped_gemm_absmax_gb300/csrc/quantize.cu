@@ -219,264 +219,432 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 }
 
 // ==========================================================================================
-// Columnwise with column-major output, single pass. Work unit = (row group g, strip of 64
-// columns). A cluster of kColCS CTAs shares the unit: each CTA pulls its share of the group's
-// rows (up to kColCap rows) into shared memory with TMA (128-byte swizzled rows of 64 bf16),
-// computes the per-column partial amax, the cluster exchanges the partials through distributed
-// shared memory, every CTA derives the 64 scales, casts its rows into a transposed FP8 tile and
-// writes whole 16-byte runs of the column-major output. A group larger than kColCS * kColCap
-// rows falls back to two passes over the group (amax, then re-read and cast).
-constexpr int kColCS = 8;
-constexpr int kColCap = 1024;
-constexpr int kColBox = 32;  // rows per TMA box
+// Columnwise with column-major output, single pass, register-resident.
+//
+// Work unit = (row group g, strips of 64 columns). A group of n rows needs k CTAs (k = the
+// power of two >= n / (128 NB), at most the cluster size cs); a cluster of cs CTAs then
+// processes cs / k strips of the group at once, one sub-team of k CTAs per strip, each member
+// holding up to 128 NB rows of its strip in registers:
+//   - loads: a thread reads 4 consecutive rows x 8 columns (four 16-byte loads; a warp reads 4
+//     whole 128-byte rows per instruction), keeps them in registers and folds |x| into packed
+//     per-column maxima;
+//   - the CTA's column maxima go to shared memory; one cluster barrier; each CTA folds its
+//     sub-team peers' maxima through distributed shared memory and derives the 64 scales;
+//   - cast from registers: each 4-row column pack becomes one 32-bit word of FP8 codes; the
+//     words are written into a transposed tile (64 columns x 128 rows per box, TMA 128-byte
+//     swizzle; the order of a thread's 8 columns is rotated by its chunk index so the shared
+//     stores are conflict-free), then TMA bulk-tensor stores write the column-major output.
+// Clusters are persistent and walk the units. Groups of more than cs * 128 NB rows take two
+// passes (amax over all rows, then re-read and cast).
 constexpr int kColThreads = 256;
+constexpr int kColCtrlBytes = 4096;
 
-struct ColSmem {
-  uint8_t in[kColCap * 128];   // TMA destination: row r at r * 128, 16-byte chunks XOR (r % 8)
-  uint8_t T[64 * kColCap];     // transposed codes: column c at c * kColCap, chunks XOR (c % 8)
-  uint32_t red[8][32];
-  uint32_t part[32];           // packed |bf16| maxima of column pairs (low half = even column)
+struct ColCtrl {
+  uint32_t part[2][32];    // this CTA's packed |bf16| column-pair maxima, by unit parity
+  uint32_t red[8][8][4];   // per warp, per 8-column chunk, 4 packed pairs
   float s32[64];
-  int64_t psum[8];
-  uint64_t bar;
+  int32_t total_units;
+  int32_t bad;
 };
+static_assert(sizeof(ColCtrl) <= kColCtrlBytes, "column kernel control block");
 
 struct ColParams {
+  const uint16_t* x;
   int64_t rows_total;
   int64_t C;
   int64_t n_groups;
-  int64_t group_rows;
-  const int32_t* ends;
-  uint8_t* out_t;
-  int64_t ld_out;
+  int64_t group_rows;  // dense modes
+  const int32_t* ends; // segment mode
   float* inv;
   int32_t* status;
-  uint64_t wait_ns;
   int64_t n_strips;
+  int cs;              // CTAs per cluster
+  int mode;            // 0: 2-D [C, R] output; 1: batched [B, C, R]; 2: segments [C, P]
+  int dense_k;         // dense modes: CTAs per strip
 };
 
-template <int FMT>
-FP8_DEVI uint32_t cast4(const float* f, float s, float fmax) {
-  float y[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float t = __fmul_rn(f[j], s);
-    y[j] = t > fmax ? fmax : (t < -fmax ? -fmax : t);
-  }
-  return cvt_fp8x2<FMT>(y[0], y[1]) | (cvt_fp8x2<FMT>(y[2], y[3]) << 16);
+struct ColUnit {
+  int64_t g, g0, n, pstart, write_end, chunk;
+  int64_t strip;       // this CTA's strip (may be >= n_strips: idle member)
+  int k, member, sub, rounds;
+};
+
+FP8_DEVI int ceil_pow2_int(int64_t v) {
+  int k = 1;
+  while (k < v) k <<= 1;
+  return k;
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(kColThreads, 1)
-    quant_cols_kernel(const __grid_constant__ CUtensorMap tmap, const ColParams p) {
-  constexpr float FMAX = FmtMax<FMT>::v;
-  cg::cluster_group cluster = cg::this_cluster();
-  const unsigned rank = cluster.block_rank();
-  extern __shared__ uint8_t smem_raw[];
-  ColSmem& S = *reinterpret_cast<ColSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t unit = blockIdx.x / kColCS;
-  const int64_t g = unit / p.n_strips;
-  const int64_t c0 = (unit % p.n_strips) * 64;
+// Sub-team size of a group of n rows: k CTAs of cap rows each, a power of two <= cs.
+FP8_DEVI int team_size(int64_t n, int cap, int cs) {
+  const int64_t need = ceil_div64(n, cap);
+  const int k = ceil_pow2_int(need < 1 ? 1 : need);
+  return k > cs ? cs : k;
+}
 
-  // ---- the group's rows (and, for segments, its padded start) ----
-  int64_t g0, g1, pstart = 0;
-  if (p.ends) {
+template <int NB>
+FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t unit, const int32_t* upre, const int32_t* ppre, int rank) {
+  constexpr int CAP = 128 * NB;
+  ColUnit u;
+  int64_t local;
+  if (p.mode == 2) {
+    int lo = 0, hi = (int)p.n_groups - 1;  // the segment whose unit range holds `unit`
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (upre[mid] <= unit) lo = mid;
+      else hi = mid - 1;
+    }
+    u.g = lo;
+    local = unit - upre[lo];
+    u.g0 = lo ? p.ends[lo - 1] : 0;
+    u.n = p.ends[lo] - u.g0;
+    u.pstart = ppre[lo];
+    u.write_end = round_up64(u.n, 128);
+    u.k = team_size(u.n, CAP, p.cs);
+  } else {
+    u.k = p.dense_k;
+    const int64_t upg = ceil_div64(p.n_strips, p.cs / u.k);
+    u.g = unit / upg;
+    local = unit % upg;
+    u.g0 = u.g * p.group_rows;
+    u.n = p.group_rows;
+    u.pstart = 0;
+    u.write_end = u.n;
+  }
+  u.sub = rank / u.k;
+  u.member = rank % u.k;
+  u.strip = local * (p.cs / u.k) + u.sub;
+  if (u.n <= (int64_t)u.k * CAP) {
+    u.chunk = round_up64(ceil_div64(u.n, u.k), 128);
+    u.rounds = u.n > 0 ? 1 : 0;
+  } else {
+    u.chunk = CAP;
+    u.rounds = (int)ceil_div64(u.n, (int64_t)u.k * CAP);
+  }
+  return u;
+}
+
+FP8_DEVI void tma_store_2d(const CUtensorMap* m, const void* src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+FP8_DEVI void tma_store_3d(const CUtensorMap* m, const void* src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+FP8_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+FP8_DEVI void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+FP8_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Column j (0..7) of a 16-byte vector of 8 bf16, as fp32.
+FP8_DEVI float col_of(const uint4& v, int j) {
+  const uint32_t w = j < 2 ? v.x : (j < 4 ? v.y : (j < 6 ? v.z : v.w));
+  return (j & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+}
+
+template <int FMT, int NB>
+__global__ void __launch_bounds__(kColThreads, NB <= 4 ? 2 : 1)
+    quant_cols_kernel(const __grid_constant__ CUtensorMap tm_out, const ColParams p) {
+  constexpr int CAP = 128 * NB;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int cs = p.cs;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* T = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  ColCtrl& S = *reinterpret_cast<ColCtrl*>(T + CAP * 64);
+  int32_t* upre = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(&S) + kColCtrlBytes);  // [E + 1]
+  int32_t* ppre = upre + (p.n_groups + 1);                                                    // [E + 1]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ch = lane & 7, rq = lane >> 3;  // 8-column chunk, row quad within the warp's 16 rows
+  const int64_t cluster_id = blockIdx.x / cs, n_clusters = gridDim.x / cs;
+
+  // ---- units: dense modes have a fixed count; segments need the offsets ----
+  int64_t total_units;
+  if (p.mode == 2) {
     int bad = 0;
-    int64_t ps = 0;
     for (int64_t e = tid; e < p.n_groups; e += kColThreads) {
       const int64_t cur = p.ends[e], prev = e ? p.ends[e - 1] : 0;
       if (cur < prev || (e == p.n_groups - 1 && cur != p.rows_total)) bad = 1;
-      if (e < g && cur >= prev) ps += round_up64(cur - prev, 128);
     }
     bad = __syncthreads_or(bad);
     if (bad) {
       if (blockIdx.x == 0 && tid == 0) set_status(p.status, FP8_DEV_BAD_OFFSETS);
-      return;  // every CTA of every cluster takes this branch: no cluster barrier is pending
+      return;  // every CTA takes this branch before any cluster barrier
     }
+    if (warp == 0) {  // prefix of units per segment and of padded segment lengths
+      int cu = 0, cp = 0;
+      for (int64_t base = 0; base < p.n_groups; base += 32) {
+        const int64_t i = base + lane;
+        int vu = 0, vp = 0;
+        if (i < p.n_groups) {
+          const int64_t n = p.ends[i] - (i ? p.ends[i - 1] : 0);
+          const int k = team_size(n, CAP, cs);
+          vu = (int)ceil_div64(p.n_strips, cs / k);
+          vp = (int)round_up64(n, 128);
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-    if (lane == 0) S.psum[warp] = ps;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int yu = __shfl_up_sync(0xffffffffu, vu, o);
+          const int yp = __shfl_up_sync(0xffffffffu, vp, o);
+          if (lane >= o) {
+            vu += yu;
+            vp += yp;
+          }
+        }
+        if (i < p.n_groups) {
+          upre[i + 1] = vu + cu;
+          ppre[i + 1] = vp + cp;
+        }
+        cu += __shfl_sync(0xffffffffu, vu, 31);
+        cp += __shfl_sync(0xffffffffu, vp, 31);
+      }
+      if (lane == 0) {
+        upre[0] = 0;
+        ppre[0] = 0;
+      }
+    }
     __syncthreads();
-    for (int w = 0; w < 8; ++w) pstart += S.psum[w];
-    g0 = g ? p.ends[g - 1] : 0;
-    g1 = p.ends[g];
+    total_units = upre[p.n_groups];
   } else {
-    g0 = g * p.group_rows;
-    g1 = g0 + p.group_rows;
+    total_units = p.n_groups * ceil_div64(p.n_strips, cs / p.dense_k);
   }
-  const int64_t n = g1 - g0;
-  const int64_t write_end = p.ends ? round_up64(n, 128) : n;
-  int64_t chunk;
-  int rounds;
-  if (n <= (int64_t)kColCS * kColCap) {
-    chunk = round_up64(ceil_div64(n, kColCS), 16);
-    rounds = n > 0 ? 1 : 0;
-  } else {
-    chunk = kColCap;
-    rounds = (int)ceil_div64(n, (int64_t)kColCS * kColCap);
-  }
+  if (tid == 0) tma_prefetch_desc(&tm_out);
 
-  if (tid == 0) {
-    mbar_init(&S.bar, 1);
-    fence_mbar_init();
-    tma_prefetch_desc(&tmap);
-  }
-  __syncthreads();
-
-  uint32_t phase = 0;
-  int ok = 1, pending = 0;
-  auto load = [&](int64_t rel0, int64_t rows) {
-    if (tid == 0) {
-      const int nbox = (int)ceil_div64(rows, kColBox);
-      mbar_arrive_expect_tx(&S.bar, (uint32_t)(nbox * kColBox * 128));
-      for (int b = 0; b < nbox; ++b)
-        tma_load_2d(S.in + b * kColBox * 128, &tmap, &S.bar, (int32_t)c0, (int32_t)(g0 + rel0 + b * kColBox));
-    }
-    pending = 1;
-  };
-  auto wait = [&]() {
-    const bool w = mbar_wait(&S.bar, phase, nullptr, p.wait_ns);
-    const int all = __syncthreads_and(w ? 1 : 0);
-    if (all) {
-      phase ^= 1;
-      pending = 0;
-    } else {
-      ok = 0;
-      if (tid == 0) set_status(p.status, FP8_DEV_TIMEOUT);
-    }
-  };
-
-  // ---- pass 1: partial column amax over this CTA's rows ----
-  uint32_t acc = 0;
-  for (int j = 0; j < rounds && ok; ++j) {
-    const int64_t rel0 = ((int64_t)j * kColCS + rank) * chunk;
-    const int64_t valid = n - rel0 < chunk ? n - rel0 : chunk;
-    if (valid <= 0) continue;
-    if (j > 0) {
-      fence_proxy_async_smem();
-      __syncthreads();
-    }
-    load(rel0, valid);
-    wait();
-    if (!ok) break;
-    for (int r = warp; r < valid; r += 8)
-      acc = absmax2(acc, *reinterpret_cast<const uint32_t*>(S.in + r * 128 + (((lane >> 2) ^ (r & 7)) << 4) +
-                                                            ((lane & 3) << 2)));
-  }
-  S.red[warp][lane] = acc;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t m = 0;
-    for (int w = 0; w < 8; ++w) m = __vmaxu2(m, S.red[w][lane]);
-    S.part[lane] = m;
-  }
-  cluster.sync();
-  if (warp == 0) {
-    uint32_t m = 0;
-    for (unsigned rr = 0; rr < (unsigned)kColCS; ++rr) m = __vmaxu2(m, cluster.map_shared_rank(S.part, rr)[lane]);
-    const Scale s0 = make_scale(bf16_bits_to_float(m & 0xFFFFu), FMAX);
-    const Scale s1 = make_scale(bf16_bits_to_float(m >> 16), FMAX);
-    S.s32[2 * lane] = s0.s32;
-    S.s32[2 * lane + 1] = s1.s32;
-    if (rank == 0) {
-      const int64_t col = c0 + 2 * lane;
-      if (col < p.C) p.inv[g * p.C + col] = s0.inv32;
-      if (col + 1 < p.C) p.inv[g * p.C + col + 1] = s1.inv32;
-    }
-  }
-  __syncthreads();
-
-  // ---- pass 2: cast into the transposed tile, write column-major runs ----
-  for (int j = 0; j < rounds && ok; ++j) {
-    const int64_t rel0 = ((int64_t)j * kColCS + rank) * chunk;
-    const int64_t valid = n - rel0 < chunk ? (n - rel0 > 0 ? n - rel0 : 0) : chunk;
-    const int64_t wrows = write_end - rel0 < chunk ? write_end - rel0 : chunk;
-    if (wrows <= 0) continue;
-    if (rounds > 1 && valid > 0) {
-      fence_proxy_async_smem();
-      __syncthreads();
-      load(rel0, valid);
-      wait();
-      if (!ok) break;
-    }
-    // lane -> column (cc * 8 + lane % 8), rows r0 .. r0 + 3 with r0 = 16 b + 4 (lane / 8)
-    for (int64_t b = warp; b * 16 < wrows; b += 8) {
-      const int r0 = (int)(b * 16) + 4 * (lane >> 3);
+  int parity = 0;
+  for (int64_t unit = cluster_id; unit < total_units; unit += n_clusters, parity ^= 1) {
+    const ColUnit u = col_unit<NB>(p, unit, upre, ppre, rank);
+    const bool on = u.strip < p.n_strips;
+    const int64_t c0 = u.strip * 64;
+    const bool ch_ok = on && c0 + ch * 8 < p.C;
+    // this thread's rows within a member's chunk: block b, rows 128 b + 16 warp + 4 rq + jj
+    uint4 v[NB][4];
+    auto load_round = [&](int r, int64_t* rel0_out, int64_t* valid_out) {
+      const int64_t rel0 = ((int64_t)r * u.k + u.member) * u.chunk;
+      int64_t valid = u.n - rel0;
+      valid = valid < 0 ? 0 : (valid < u.chunk ? valid : u.chunk);
+      const uint16_t* base = p.x + (u.g0 + rel0) * p.C + c0 + ch * 8;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const int cl = cc * 8 + (lane & 7);
-        float f[4];
+      for (int b = 0; b < NB; ++b)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          const int r = r0 + jj;
-          const uint16_t h =
-              *reinterpret_cast<const uint16_t*>(S.in + r * 128 + ((cc ^ (r & 7)) << 4) + ((lane & 7) << 1));
-          f[jj] = r < valid ? bf16_bits_to_float(h) : 0.0f;
+          const int row = 128 * b + 16 * warp + 4 * rq + jj;
+          v[b][jj] = (ch_ok && row < valid) ? ld_nc_v4(base + (int64_t)row * p.C) : make_uint4(0, 0, 0, 0);
         }
-        *reinterpret_cast<uint32_t*>(S.T + cl * kColCap + (((r0 >> 4) ^ (cl & 7)) << 4) + (r0 & 15)) =
-            cast4<FMT>(f, S.s32[cl], FMAX);
-      }
+      *rel0_out = rel0;
+      *valid_out = valid;
+    };
+
+    // ---- pass 1: packed per-column maxima (x: cols 0-1, y: 2-3, z: 4-5, w: 6-7 of the chunk) ----
+    uint32_t m4[4] = {0, 0, 0, 0};
+    for (int r = 0; r < u.rounds; ++r) {
+      int64_t rel0, valid;
+      load_round(r, &rel0, &valid);
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          m4[0] = absmax2(m4[0], v[b][jj].x);
+          m4[1] = absmax2(m4[1], v[b][jj].y);
+          m4[2] = absmax2(m4[2], v[b][jj].z);
+          m4[3] = absmax2(m4[3], v[b][jj].w);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m4[i] = __vmaxu2(m4[i], __shfl_xor_sync(0xffffffffu, m4[i], 8));
+      m4[i] = __vmaxu2(m4[i], __shfl_xor_sync(0xffffffffu, m4[i], 16));
+    }
+    if (rq == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) S.red[warp][ch][i] = m4[i];
     }
     __syncthreads();
-    const int nch = (int)(wrows / 16);
-    for (int i = tid; i < 64 * nch; i += kColThreads) {
-      const int cl = i / nch, k = i % nch;
-      const int64_t col = c0 + cl;
-      if (col < p.C) {
-        const uint4 v = *reinterpret_cast<const uint4*>(S.T + cl * kColCap + ((k ^ (cl & 7)) << 4));
-        const int64_t row0 = p.ends ? col * p.ld_out + pstart : (g * p.C + col) * p.ld_out;
-        *reinterpret_cast<uint4*>(p.out_t + row0 + rel0 + 16 * k) = v;
+    if (tid < 32) {  // pair t = columns 2t, 2t+1 = chunk t/4, word t%4
+      uint32_t m = 0;
+      for (int w = 0; w < 8; ++w) m = __vmaxu2(m, S.red[w][tid >> 2][tid & 3]);
+      S.part[parity][tid] = m;
+    }
+    cluster.sync();
+    if (tid < 32) {
+      uint32_t m = 0;
+      for (int i = 0; i < u.k; ++i)
+        m = __vmaxu2(m, cluster.map_shared_rank(&S.part[parity][0], u.sub * u.k + i)[tid]);
+      constexpr float FMAX = FmtMax<FMT>::v;
+      const Scale s0 = make_scale(bf16_bits_to_float(m & 0xFFFFu), FMAX);
+      const Scale s1 = make_scale(bf16_bits_to_float(m >> 16), FMAX);
+      S.s32[2 * tid] = s0.s32;
+      S.s32[2 * tid + 1] = s1.s32;
+      if (on && u.member == 0) {  // an empty segment gets the scales of an all-zero group
+        const int64_t col = c0 + 2 * tid;
+        if (col < p.C) p.inv[u.g * p.C + col] = s0.inv32;
+        if (col + 1 < p.C) p.inv[u.g * p.C + col + 1] = s1.inv32;
       }
     }
+    if (tid == 0) bulk_wait_read_all();  // the previous unit's stores have read the tile
     __syncthreads();
+    float sc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sc[j] = S.s32[ch * 8 + j];
+
+    // ---- pass 2: cast from registers into the transposed tile, store column-major ----
+    for (int r = 0; r < u.rounds; ++r) {
+      int64_t rel0, valid;
+      if (u.rounds > 1) {
+        load_round(r, &rel0, &valid);
+      } else {
+        rel0 = (int64_t)u.member * u.chunk;
+      }
+      int64_t wrows = u.write_end - rel0;
+      wrows = wrows < 0 ? 0 : (wrows < u.chunk ? wrows : u.chunk);
+      const int nbox = (int)ceil_div64(wrows, 128);
+      if (on && nbox > 0) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (b < nbox) {
+            uint32_t o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float s = sc[j];
+              o[j] = cvt_fp8x2<FMT>(__fmul_rn(col_of(v[b][0], j), s), __fmul_rn(col_of(v[b][1], j), s)) |
+                     (cvt_fp8x2<FMT>(__fmul_rn(col_of(v[b][2], j), s), __fmul_rn(col_of(v[b][3], j), s)) << 16);
+            }
+            // rotate by ch so that the lanes of a warp write 8 different column residues at once
+#pragma unroll
+            for (int sh = 1; sh < 8; sh <<= 1) {
+              const bool rot = (ch & sh) != 0;
+              uint32_t t[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) t[j] = rot ? o[(j + sh) & 7] : o[j];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) o[j] = t[j];
+            }
+            uint8_t* box = T + b * 8192;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int cl = ch * 8 + ((j + ch) & 7);
+              *reinterpret_cast<uint32_t*>(box + cl * 128 + (((warp ^ cl) & 7) << 4) + rq * 4) = o[j];
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0 && on && nbox > 0) {
+        for (int b = 0; b < nbox; ++b) {
+          const int32_t xo = (int32_t)(u.pstart + rel0 + 128 * b);
+          if (p.mode == 1)
+            tma_store_3d(&tm_out, T + b * 8192, xo, (int32_t)c0, (int32_t)u.g);
+          else
+            tma_store_2d(&tm_out, T + b * 8192, xo, (int32_t)c0);
+        }
+        bulk_commit();
+      }
+      if (u.rounds > 1) {
+        if (tid == 0) bulk_wait_read_all();
+        __syncthreads();
+      }
+    }
   }
-  // Drain a load still in flight after a timeout, then keep this CTA's shared memory alive
-  // until every peer has read its partial maxima.
-  if (pending && tid == 0) mbar_wait(&S.bar, phase, nullptr, p.wait_ns);
-  cluster.sync();
+  if (tid == 0) bulk_wait_all();
+  cluster.sync();  // peers may still read this CTA's partial maxima
+}
+
+template <int FMT, int NB>
+static int run_cols(const ColParams& p0, const CUtensorMap& tout, const Ctx& c) {
+  auto kern = quant_cols_kernel<FMT, NB>;
+  ColParams p = p0;
+  const size_t ctrl = kColCtrlBytes + (p.mode == 2 ? 8 * (size_t)(p.n_groups + 1) : 0);
+  const size_t smem = 1024 + (size_t)128 * NB * 64 + ctrl;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 128 * 8 * 64 + 65536) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return FP8_ERR_CUDA;
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kColThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int slots = 0;
+  for (int cs : {16, 8}) {
+    attr[0].val.clusterDim.x = cs;
+    cfg.gridDim = dim3(cs);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
+      p.cs = cs;
+      slots = n;
+      break;
+    }
+    cudaGetLastError();
+  }
+  if (slots == 0) return FP8_ERR_CUDA;
+  int64_t units;
+  if (p.mode == 2) {
+    units = p.n_groups * p.n_strips;  // upper bound; the kernel computes the exact count
+  } else {
+    int k = 1;
+    while (k * 128 * NB < p.group_rows && k < p.cs) k <<= 1;
+    p.dense_k = k;
+    units = p.n_groups * ((p.n_strips + p.cs / k - 1) / (p.cs / k));
+  }
+  const int64_t clusters = units < slots ? units : slots;
+  attr[0].val.clusterDim.x = p.cs;
+  cfg.gridDim = dim3((unsigned)(clusters * p.cs));
+  if (cudaLaunchKernelEx(&cfg, kern, tout, p) != cudaSuccess) return FP8_ERR_CUDA;
+  return FP8_OK;
 }
 
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
                       const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, const Ctx& c) {
   if (n_groups == 0 || C == 0) return FP8_OK;
-  CUtensorMap tmap;
-  const uint64_t dims[2] = {(uint64_t)C, (uint64_t)(rows_total > 0 ? rows_total : 1)};
-  const uint64_t strides[1] = {(uint64_t)C * 2};
-  const uint32_t box[2] = {64, kColBox};
-  int rc = make_tmap(&tmap, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc != FP8_OK) return rc;
-  ColParams p;
+  if (ends && n_groups > 6000) return FP8_ERR_UNSUPPORTED;  // prefix arrays live in shared memory
+  ColParams p = {};
+  p.x = static_cast<const uint16_t*>(x);
   p.rows_total = rows_total;
   p.C = C;
   p.n_groups = n_groups;
   p.group_rows = group_rows;
   p.ends = ends;
-  p.out_t = static_cast<uint8_t*>(out_t);
-  p.ld_out = ld_out;
   p.inv = inv;
   p.status = c.status;
-  p.wait_ns = c.wait_ns;
   p.n_strips = ceil_div64(C, 64);
-  const int64_t units = n_groups * p.n_strips;
-  const size_t smem = sizeof(ColSmem) + 1024;
-  auto kern = fmt == FP8_DT_E4M3 ? quant_cols_kernel<FP8_DT_E4M3> : quant_cols_kernel<FP8_DT_E5M2>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return FP8_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(units * kColCS));
-  cfg.blockDim = dim3(kColThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = c.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kColCS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, tmap, p) != cudaSuccess) return FP8_ERR_CUDA;
-  return FP8_OK;
+  p.mode = ends ? 2 : (n_groups > 1 ? 1 : 0);
+  p.cs = 16;
+  p.dense_k = 1;
+
+  CUtensorMap tout;
+  int rc;
+  if (p.mode == 1) {
+    const uint64_t dims[3] = {(uint64_t)group_rows, (uint64_t)C, (uint64_t)n_groups};
+    const uint64_t strides[2] = {(uint64_t)group_rows, (uint64_t)(C * group_rows)};
+    const uint32_t box[3] = {128, 64, 1};
+    rc = make_tmap(&tout, out_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    const uint64_t inner = p.mode == 2 ? (uint64_t)ld_out : (uint64_t)group_rows;
+    const uint64_t dims[2] = {inner, (uint64_t)C};
+    const uint64_t strides[1] = {(uint64_t)ld_out};
+    const uint32_t box[2] = {128, 64};
+    rc = make_tmap(&tout, out_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (rc != FP8_OK) return rc;
+  // 4 blocks of 128 rows per CTA (two CTAs per SM) unless a dense group needs more than
+  // 16 x 512 rows, then 8 blocks (one CTA per SM).
+  const bool big = p.mode != 2 && group_rows > 16 * 512;
+  if (fmt == FP8_DT_E4M3)
+    return big ? run_cols<FP8_DT_E4M3, 8>(p, tout, c) : run_cols<FP8_DT_E4M3, 4>(p, tout, c);
+  return big ? run_cols<FP8_DT_E5M2, 8>(p, tout, c) : run_cols<FP8_DT_E5M2, 4>(p, tout, c);
 }
 
 }  // namespace fp8lin

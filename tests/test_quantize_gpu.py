@@ -79,8 +79,10 @@ def test_colwise_transposed(fp8, R, C, fi):
     ofmt, dt, fmax = FMTS[fi]
     # column-gain input as in the backward-operand workload
     x = W.column_gain_bf16((R, C), 1e-3, -2, 2, 301 + R)
-    _, qt, inv = fp8.quantize_alloc(x.cuda(), fp8.GRAN_COL, dt)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, qt, inv = fp8.quantize_alloc(x.cuda(), fp8.GRAN_COL, dt, status=st)
     torch.cuda.synchronize()
+    assert int(st.item()) == 0
     q_ref, inv_ref = oracle.quantize_cols(bits(x), ofmt)
     assert np.array_equal(codes(qt), q_ref.T)
     assert np.array_equal(f32_bits(inv), inv_ref.view(np.uint32))
@@ -97,7 +99,7 @@ def test_colwise_special_columns(fp8):
         assert np.array_equal(f32_bits(inv), inv_ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("B,R,C", [(3, 64, 96), (4, 7168 // 8, 256), (2, 16, 8)])
+@pytest.mark.parametrize("B,R,C", [(3, 64, 96), (4, 7168 // 8, 256), (2, 16, 8), (40, 256, 200)])
 def test_colwise_batched_3d(fp8, B, R, C):
     """Per-expert column scales of a 3-D weight [E, K, N] (amax over K for each (e, n))."""
     x = W.normal_bf16((B, R, C), 0.02, 400 + B)
@@ -121,7 +123,8 @@ def _segpad(q_ref, ends, P):
 
 
 @pytest.mark.parametrize("counts", [[100, 0, 37, 500, 1], [0, 0, 64], [300, 0], [9000, 5, 0, 11000],
-                                    list(W.llama4_counts(0) // 4)])
+                                    list(W.llama4_counts(0) // 4), list(W.random_counts(3000, 40, 5, n_empty=9)),
+                                    [0] * 7 + [1000] + [0] * 9])
 @pytest.mark.parametrize("fi", [0, 1])
 def test_jagged_colwise(fp8, counts, fi):
     ofmt, dt, fmax = FMTS[fi]
@@ -133,9 +136,11 @@ def test_jagged_colwise(fp8, counts, fi):
     P = fp8.fp8_jagged_padded_rows(R, len(counts))
     canary = torch.full((C, P), 0x5A, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn if dt == 3 else torch.float8_e5m2)
     inv = torch.empty((len(counts), C), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
     fp8.fp8_quantize(x.cuda(), fp8.GRAN_COL, dt, fp8.LAYOUT_COL_MAJOR, None, canary, inv,
-                     torch.from_numpy(ends).cuda())
+                     torch.from_numpy(ends).cuda(), status=st)
     torch.cuda.synchronize()
+    assert int(st.item()) == 0
     q_ref, inv_ref = oracle.quantize_jagged_cols(bits(x), ends, ofmt)
     ref, used = _segpad(q_ref, ends, P)
     got = codes(canary)
