@@ -6,14 +6,22 @@
 //   grouped: per-row sA, per-expert-column sB, rows routed by cumulative offsets ("FP8 training
 //   on AMD GPUs with TorchTitan and TorchAO", "Scaling FP8 to MoE Architectures", Figure 3).
 //
-// Design (one persistent CTA per SM, 320 threads):
-//   warp 0      TMA producer: 128 x 128-byte A tile + 256 x 128-byte B tile per stage, 128-byte
-//               swizzle, into a 4-stage ring guarded by full/empty mbarriers;
-//   warp 1      allocates 512 TMEM columns; lane 0 issues tcgen05.mma (M=128, N=256; K=32 for
-//               FP8, K=16 for BF16) into one of two fp32 accumulators, and commits each stage
-//               back to the producer and each finished tile to the epilogue;
+// Design (persistent; 320 threads per CTA; CG = 1 or 2 CTAs per MMA):
+//   CG = 1: one CTA per SM computes 128 x 256 tiles;
+//   CG = 2: a cluster of two CTAs (a CTA pair on two SMs) computes 256 x 256 tiles with
+//           tcgen05.mma.cta_group::2: each CTA stages its own 128 rows of A and 128 of the 256
+//           rows of B, the even CTA issues the MMAs for both, and each CTA's tensor memory
+//           holds the accumulator of its own 128 rows. Per CTA a stage is 32 KB instead of
+//           48 KB, so the ring is 6 stages deep and B is read from L2 once per pair.
+//   warp 0      TMA producer (128-byte swizzle; K blocks of 128 bytes) into the stage ring,
+//               guarded by full/empty mbarriers (the pair's full barrier lives in the even CTA
+//               and counts both CTAs' bytes);
+//   warp 1      allocates 512 TMEM columns; lane 0 of the issuing CTA issues the MMAs (M=128
+//               or 256, N=256; K=32 for FP8, K=16 for BF16) into one of two fp32
+//               accumulators and commits each stage back to the producers and each finished
+//               tile to the epilogues (multicast to both CTAs of a pair);
 //   warps 2..9  epilogue: each warp owns 32 TMEM lanes (tile rows) and one half (128 columns)
-//               of the tile; the tile's column scales are staged once in shared memory;
+//               of its CTA's tile; the tile's column scales are staged once in shared memory;
 //               tcgen05.ld 32 columns at a time, sA[m] * sB[n] applied once, one rounding to
 //               bf16/fp32, masked stores. The second accumulator lets the next tile's MMAs
 //               overlap this epilogue.
@@ -26,16 +34,23 @@ namespace fp8lin {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BKB = 128;  // tile rows, tile columns, K bytes per stage
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BKB;
-constexpr int B_BYTES = BN * BKB;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BM = 128, BN = 256, BKB = 128;  // rows per CTA, tile columns, K bytes per stage
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;  // warps 2..9
 constexpr int kTmemCols = 2 * BN;
 constexpr int kMaxExperts = 2048;
 constexpr int kGroupM = 16;  // rasterization: tiles walk 16 M-blocks per N-block
+constexpr int kRingBytes = 196608;
+
+template <int CG>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
+  static constexpr int B_ROWS = BN / CG;                // this CTA's rows of B
+  static constexpr int B_BYTES = B_ROWS * BKB;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB or 32 KB
+  static constexpr int STAGES = kRingBytes / STAGE_BYTES;  // 4 or 6
+  static constexpr int TILE_M = BM * CG;
+};
 
 enum { kDense = 0, kJagM = 1, kJagK = 2 };
 enum { kFP8 = 0, kBF16 = 1 };
@@ -53,14 +68,14 @@ struct GemmParams {
   int64_t ldo;         // output row stride (elements)
   const int32_t* ends;
   int E;
-  int64_t total_rows;  // jagged: last valid offset
+  int64_t total_rows;  // jagged M: last valid offset
   uint32_t idesc;
   int32_t* status;
   uint64_t wait_ns;
 };
 
 struct Tile {
-  int64_t m0, n0;   // first row / column of D
+  int64_t m0, n0;   // first row / column of the (pair's) tile of D
   int64_t row_end;  // rows >= row_end are masked (segment end, or M)
   int64_t k0;       // first contraction coordinate
   int64_t nkb;      // K blocks
@@ -69,8 +84,8 @@ struct Tile {
 
 struct Shared {
   float sb[2][BN];  // per-tile column scales, alternating between consecutive tiles
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[6];
+  uint64_t empty[6];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -90,7 +105,7 @@ FP8_DEVI int find_expert(const int32_t* tpre, int E, int64_t t) {
   return lo;
 }
 
-template <int SCHED>
+template <int SCHED, int TILE_M>
 FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t, const int32_t* tpre, const int32_t* aux) {
   Tile T;
   if (SCHED == kDense) {
@@ -99,7 +114,7 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t, const int32_t* tpre, cons
     const int64_t first_m = g * kGroupM;
     const int64_t gsz = p.num_m - first_m < kGroupM ? p.num_m - first_m : kGroupM;
     const int64_t mb = first_m + r % gsz, nb = r / gsz;
-    T.m0 = mb * BM;
+    T.m0 = mb * TILE_M;
     T.n0 = nb * BN;
     T.row_end = p.M;
     T.k0 = 0;
@@ -109,7 +124,7 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t, const int32_t* tpre, cons
     const int e = find_expert(tpre, p.E, t);
     const int64_t local = t - tpre[e];
     const int64_t mb = local / p.num_n, nb = local % p.num_n;
-    T.m0 = aux[e] + mb * BM;  // aux[e] = segment start row
+    T.m0 = aux[e] + mb * TILE_M;  // aux[e] = segment start row
     T.n0 = nb * BN;
     T.row_end = aux[e + 1];
     T.k0 = 0;
@@ -119,7 +134,7 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t, const int32_t* tpre, cons
     const int64_t per = p.num_m * p.num_n;
     const int e = (int)(t / per);
     const int64_t local = t % per;
-    T.m0 = (local / p.num_n) * BM;
+    T.m0 = (local / p.num_n) * TILE_M;
     T.n0 = (local % p.num_n) * BN;
     T.row_end = p.M;
     T.k0 = aux[e];                             // aux[e] = padded start of segment e
@@ -129,17 +144,22 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t, const int32_t* tpre, cons
   return T;
 }
 
-template <int KIND, int SCHED, int A_MN, int B_MN>
+template <int KIND, int SCHED, int A_MN, int B_MN, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
+  using C = Cfg<CG>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Shared& S = *reinterpret_cast<Shared*>(smem + STAGES * STAGE_BYTES);
-  int32_t* tpre = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + kSharedBytes);
+  Shared& S = *reinterpret_cast<Shared*>(smem + kRingBytes);
+  int32_t* tpre = reinterpret_cast<int32_t*>(smem + kRingBytes + kSharedBytes);
   int32_t* aux = tpre + (p.E + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &S.abort;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0;  // 0 issues the pair's MMAs
+  const bool issuer = rank == 0;
+  const int64_t unit = blockIdx.x / CG, n_units = gridDim.x / CG;
 
   // ---- jagged schedules: validate offsets, per-expert tile prefix and row / K starts ----
   int64_t total;
@@ -152,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (cur < prev || (SCHED != kJagK && e == p.E - 1 && cur != p.total_rows)) bad = 1;
       const int64_t cnt = cur > prev ? cur - prev : 0;
       if (SCHED == kJagM) {
-        tpre[e + 1] = (int32_t)(((cnt + BM - 1) / BM) * p.num_n);
+        tpre[e + 1] = (int32_t)(((cnt + C::TILE_M - 1) / C::TILE_M) * p.num_n);
         aux[e + 1] = cur;
       } else {
         tpre[e + 1] = (int32_t)(p.num_m * p.num_n);
@@ -164,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       aux[0] = 0;
     }
     bad = __syncthreads_or(bad);
-    if (bad) {
+    if (bad) {  // both CTAs of a pair see the same offsets and leave together
       if (blockIdx.x == 0 && tid == 0) set_status(p.status, FP8_DEV_BAD_OFFSETS);
       return;
     }
@@ -207,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.tfull[b], 1);
-      mbar_init(&S.tempty[b], kEpiThreads / 32);
+      mbar_init(&S.tempty[b], CG * kEpiThreads / 32);
     }
     mbar_init(&S.drain, 1);
     S.abort = 0;
@@ -216,11 +236,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&S.tmem_base, kTmemCols);
-    tmem_relinquish();
+    if (CG == 2) {
+      tmem_alloc_pair(&S.tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&S.tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (CG == 2) cluster_barrier();  // the peer's barriers are initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = S.tmem_base;
 
@@ -236,37 +262,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile T = get_tile<SCHED>(p, t, tpre, aux);
+      for (int64_t t = unit; t < total && ok; t += n_units) {
+        const Tile T = get_tile<SCHED, C::TILE_M>(p, t, tpre, aux);
+        const int32_t am = (int32_t)(T.m0 + (int64_t)rank * BM);        // this CTA's A rows
+        const int32_t bn = (int32_t)(T.n0 + (int64_t)rank * C::B_ROWS);  // this CTA's B rows
         for (int64_t kb = 0; kb < T.nkb; ++kb) {
           if (!mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
             if (!*abort_flag) fail();
             ok = false;
             break;
           }
-          uint8_t* sa = smem + stage * STAGE_BYTES;
-          uint8_t* sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(&S.full[stage], STAGE_BYTES);
-          if (KIND == kFP8) {
-            const int32_t kx = (int32_t)(T.k0 + kb * BKB);
-            tma_load_2d(sa, &tmA, &S.full[stage], kx, (int32_t)T.m0);
-            if (SCHED == kJagM)
-              tma_load_3d(sb, &tmB, &S.full[stage], kx, (int32_t)T.n0, T.e);
-            else
-              tma_load_2d(sb, &tmB, &S.full[stage], kx, (int32_t)T.n0);
-          } else {
-            const int32_t kx = (int32_t)(kb * (BKB / 2));  // 64 bf16 per block
-            if (A_MN) {
-              tma_load_2d(sa, &tmA, &S.full[stage], (int32_t)T.m0, kx);
-              tma_load_2d(sa + 8192, &tmA, &S.full[stage], (int32_t)T.m0 + 64, kx);
+          uint8_t* sa = smem + stage * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          if (CG == 1) {
+            uint64_t* fb = &S.full[stage];
+            mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+            if (KIND == kFP8) {
+              const int32_t kx = (int32_t)(T.k0 + kb * BKB);
+              tma_load_2d(sa, &tmA, fb, kx, am);
+              if (SCHED == kJagM)
+                tma_load_3d(sb, &tmB, fb, kx, bn, T.e);
+              else
+                tma_load_2d(sb, &tmB, fb, kx, bn);
             } else {
-              tma_load_2d(sa, &tmA, &S.full[stage], kx, (int32_t)T.m0);
-            }
-            if (B_MN) {
+              const int32_t kx = (int32_t)(kb * (BKB / 2));  // 64 bf16 per block
+              if (A_MN) {
+                tma_load_2d(sa, &tmA, fb, am, kx);
+                tma_load_2d(sa + 8192, &tmA, fb, am + 64, kx);
+              } else {
+                tma_load_2d(sa, &tmA, fb, kx, am);
+              }
+              if (B_MN) {
 #pragma unroll
-              for (int h = 0; h < 4; ++h) tma_load_2d(sb + h * 8192, &tmB, &S.full[stage], (int32_t)T.n0 + 64 * h, kx);
+                for (int h = 0; h < C::B_ROWS / 64; ++h) tma_load_2d(sb + h * 8192, &tmB, fb, bn + 64 * h, kx);
+              } else {
+                tma_load_2d(sb, &tmB, fb, kx, bn);
+              }
+            }
+          } else {
+            // both CTAs' bytes are counted on the issuing CTA's full barrier
+            const uint32_t fb = mapa_shared(smem_u32(&S.full[stage]), 0);
+            if (issuer) mbar_arrive_expect_tx(&S.full[stage], 2 * C::STAGE_BYTES);
+            if (KIND == kFP8) {
+              const int32_t kx = (int32_t)(T.k0 + kb * BKB);
+              tma_load_2d_pair(sa, &tmA, fb, kx, am);
+              if (SCHED == kJagM)
+                tma_load_3d_pair(sb, &tmB, fb, kx, bn, T.e);
+              else
+                tma_load_2d_pair(sb, &tmB, fb, kx, bn);
             } else {
-              tma_load_2d(sb, &tmB, &S.full[stage], kx, (int32_t)T.n0);
+              const int32_t kx = (int32_t)(kb * (BKB / 2));
+              if (A_MN) {
+                tma_load_2d_pair(sa, &tmA, fb, am, kx);
+                tma_load_2d_pair(sa + 8192, &tmA, fb, am + 64, kx);
+              } else {
+                tma_load_2d_pair(sa, &tmA, fb, kx, am);
+              }
+              if (B_MN) {
+#pragma unroll
+                for (int h = 0; h < C::B_ROWS / 64; ++h) tma_load_2d_pair(sb + h * 8192, &tmB, fb, bn + 64 * h, kx);
+              } else {
+                tma_load_2d_pair(sb, &tmB, fb, kx, bn);
+              }
             }
           }
           ++issued;
@@ -276,22 +333,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Drain: the last (up to STAGES) loads must land before the CTA may exit.
-      const int64_t first = issued > STAGES ? issued - STAGES : 0;
-      for (int64_t i = first; i < issued; ++i)
-        mbar_wait(&S.full[i % STAGES], (uint32_t)((i / STAGES) & 1), nullptr, p.wait_ns);
+      // Drain: the last (up to STAGES) loads must land before the CTA (pair) may exit. For a
+      // pair, the issuing CTA's full barriers count both CTAs' loads.
+      if (issuer) {
+        const int64_t first = issued > STAGES ? issued - STAGES : 0;
+        for (int64_t i = first; i < issued; ++i)
+          mbar_wait(&S.full[i % STAGES], (uint32_t)((i / STAGES) & 1), nullptr, p.wait_ns);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ================================ MMA issuer ================================
-    if (lane == 0) {
+    if (lane == 0 && issuer) {
       int stage = 0;
       uint32_t phase = 0;
       int buf = 0;
       uint32_t aphase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile T = get_tile<SCHED>(p, t, tpre, aux);
+      for (int64_t t = unit; t < total && ok; t += n_units) {
+        const Tile T = get_tile<SCHED, C::TILE_M>(p, t, tpre, aux);
         if (T.nkb == 0) continue;
         if (!mbar_wait(&S.tempty[buf], aphase ^ 1, abort_flag, p.wait_ns)) {
           if (!*abort_flag) fail();
@@ -306,34 +366,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, 8192, 1024) : smem_desc(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc(sb + kk * 2048, 8192, 1024) : smem_desc(sb + kk * 32, 16, 1024);
             const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            if (KIND == kFP8)
-              umma_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
-            else
-              umma_f16(d_tmem, ad, bd, p.idesc, acc);
+            if (CG == 2) {
+              if (KIND == kFP8)
+                umma_f8f6f4_pair(d_tmem, ad, bd, p.idesc, acc);
+              else
+                umma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
+            } else {
+              if (KIND == kFP8)
+                umma_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
+              else
+                umma_f16(d_tmem, ad, bd, p.idesc, acc);
+            }
           }
-          umma_commit(&S.empty[stage]);  // frees the stage once these MMAs have read it
+          // frees the stage (in both CTAs of a pair) once these MMAs have read it
+          if (CG == 2)
+            umma_commit_pair(&S.empty[stage], 0x3);
+          else
+            umma_commit(&S.empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit(&S.tfull[buf]);  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue(s)
+        if (CG == 2)
+          umma_commit_pair(&S.tfull[buf], 0x3);
+        else
+          umma_commit(&S.tfull[buf]);
         if (++buf == 2) {
           buf = 0;
           aphase ^= 1;
         }
       }
       // Drain every MMA this thread issued before the tensor memory is released.
-      umma_commit(&S.drain);
-      mbar_wait(&S.drain, 0, nullptr, p.wait_ns);
+      if (CG == 2)
+        umma_commit_pair(&S.drain, 0x3);
+      else
+        umma_commit(&S.drain);
     }
     __syncwarp();
   } else {
@@ -341,12 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int c0 = ((warp - 2) >> 2) * (BN / 2);  // first tile column of this warp's half
     const int etid = tid - 64;           // 0..255 across the epilogue warps
-    const int row = q * 32 + lane;
+    const int row = (int)rank * BM + q * 32 + lane;  // row within the pair's tile
     const bool stage_sb = KIND == kFP8 && !p.sb_scalar;
     int buf = 0, sbi = 0;
     uint32_t aphase = 0;
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile T = get_tile<SCHED>(p, t, tpre, aux);
+    for (int64_t t = unit; t < total; t += n_units) {
+      const Tile T = get_tile<SCHED, C::TILE_M>(p, t, tpre, aux);
       const int64_t m = T.m0 + row;
       const bool row_ok = m < T.row_end;
       const int64_t orow = SCHED == kJagK ? (int64_t)T.e * p.M + m : m;
@@ -427,7 +504,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.tempty[buf]);
+      if (lane == 0) {  // the issuing CTA's barrier counts the epilogue warps of both CTAs
+        if (CG == 2)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&S.tempty[buf]), 0));
+        else
+          mbar_arrive(&S.tempty[buf]);
+      }
       if (++buf == 2) {
         buf = 0;
         aphase ^= 1;
@@ -437,27 +519,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (CG == 2) cluster_barrier();  // no remote arrive or load into a CTA that has left
   if (warp == 1) {
+    if (lane == 0) mbar_wait(&S.drain, 0, nullptr, p.wait_ns);  // the MMAs writing this CTA's TMEM
+    __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (CG == 2)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-template <int KIND, int SCHED, int A_MN, int B_MN>
+template <int KIND, int SCHED, int A_MN, int B_MN, int CG>
 int run(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int64_t total_tiles_hint, const Ctx& c) {
-  auto kern = gemm_kernel<KIND, SCHED, A_MN, B_MN>;
-  const size_t smem = 1024 + STAGES * STAGE_BYTES + kSharedBytes + (SCHED == kDense ? 0 : 2 * 4 * (p.E + 1));
+  auto kern = gemm_kernel<KIND, SCHED, A_MN, B_MN, CG>;
+  const size_t smem = 1024 + kRingBytes + kSharedBytes + (SCHED == kDense ? 0 : 2 * 4 * (p.E + 1));
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FP8_ERR_CUDA;
-  int64_t grid = c.sm_count;
-  if (total_tiles_hint > 0 && total_tiles_hint < grid) grid = total_tiles_hint;
-  if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads, smem, c.stream>>>(a, b, p);
-  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+  int64_t units = c.sm_count / CG;
+  if (total_tiles_hint > 0 && total_tiles_hint < units) units = total_tiles_hint;
+  if (units < 1) units = 1;
+  if (CG == 1) {
+    kern<<<(unsigned)units, kThreads, smem, c.stream>>>(a, b, p);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(units * CG));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, a, b, p) != cudaSuccess) return FP8_ERR_CUDA;
+  return FP8_OK;
 }
 
 }  // namespace
 
+// Pairs (CG = 2) serve problems with enough 256-row tiles to fill the GPU; small ones run on
+// single CTAs (CG = 1).
 int launch_gemm(const GemmArgs& g, const Ctx& c) {
   const bool fp8 = g.a_dtype != FP8_DT_BF16;
   GemmParams p = {};
@@ -472,59 +578,62 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   p.wait_ns = c.wait_ns;
   p.ends = g.ends;
   p.E = (int)g.E;
-  p.num_m = (g.M + BM - 1) / BM;
   p.num_n = (g.N + BN - 1) / BN;
   const int esz = fp8 ? 1 : 2;
   p.nkb = (g.K * esz + BKB - 1) / BKB;
   p.ldo = g.N;
   p.vec_ok = p.out_f32 ? (p.ldo % 4 == 0) : (p.ldo % 8 == 0);
   if (g.mode != -1 && (g.E < 1 || g.E > kMaxExperts)) return FP8_ERR_UNSUPPORTED;
+  // pair tiles when there are at least ~one per SM pair
+  const int64_t pair_tiles = ((g.M + 255) / 256) * p.num_n * (g.mode == FP8_GROUPED_JAGGED_K ? g.E : 1);
+  const bool pair = g.mode == FP8_GROUPED_JAGGED_M ? g.M >= 2048 : pair_tiles * 2 >= c.sm_count;
+  const int tile_m = pair ? 256 : 128;
+  p.num_m = (g.M + tile_m - 1) / tile_m;
 
   if (fp8) {
     const uint32_t af = g.a_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
     const uint32_t bf = g.b_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
-    p.idesc = make_idesc(af, bf, 0, 0, BM, BN);
+    p.idesc = make_idesc(af, bf, 0, 0, tile_m, BN);
     p.sa_scalar = g.sA_len == 1;
     p.sb_scalar = g.sB_len == 1;
     CUtensorMap ta, tb;
     const uint32_t boxA[2] = {BKB, BM};
     const uint64_t dA[2] = {(uint64_t)g.K, (uint64_t)g.M};
-    const uint64_t sA_[1] = {(uint64_t)g.K};
-    if (g.mode == -1) {
-      int rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, sA_, boxA, CU_TENSOR_MAP_SWIZZLE_128B);
-      if (rc) return rc;
+    const uint64_t strideK[1] = {(uint64_t)g.K};
+    const uint32_t b_rows = pair ? BN / 2 : BN;
+    int rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, strideK, boxA, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    if (g.mode == -1 || g.mode == FP8_GROUPED_JAGGED_K) {
       const uint64_t dB[2] = {(uint64_t)g.K, (uint64_t)g.N};
-      const uint32_t boxB[2] = {BKB, BN};
-      rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dB, sA_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
+      const uint32_t boxB[2] = {BKB, b_rows};
+      rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dB, strideK, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc) return rc;
-      return run<kFP8, kDense, 0, 0>(ta, tb, p, p.num_m * p.num_n, c);
+      if (g.mode == -1) {
+        const int64_t tiles = p.num_m * p.num_n;
+        return pair ? run<kFP8, kDense, 0, 0, 2>(ta, tb, p, tiles, c) : run<kFP8, kDense, 0, 0, 1>(ta, tb, p, tiles, c);
+      }
+      // jagged K: A = G^T [N_out, P], B = X^T [Kd, P]; tile space M = N_out, N = Kd; the
+      // offsets are checked for order and for fitting the padded length P.
+      p.total_rows = -1;
+      const int64_t tiles = (int64_t)g.E * p.num_m * p.num_n;
+      return pair ? run<kFP8, kJagK, 0, 0, 2>(ta, tb, p, tiles, c) : run<kFP8, kJagK, 0, 0, 1>(ta, tb, p, tiles, c);
     }
     if (g.mode == FP8_GROUPED_JAGGED_M) {
       p.total_rows = g.M;
-      int rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, sA_, boxA, CU_TENSOR_MAP_SWIZZLE_128B);
-      if (rc) return rc;
       const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.E};
       const uint64_t sB_[2] = {(uint64_t)g.K, (uint64_t)(g.N * g.K)};
-      const uint32_t boxB[3] = {BKB, BN, 1};
+      const uint32_t boxB[3] = {BKB, b_rows, 1};
       rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dB, sB_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc) return rc;
-      return run<kFP8, kJagM, 0, 0>(ta, tb, p, 0, c);
+      return pair ? run<kFP8, kJagM, 0, 0, 2>(ta, tb, p, 0, c) : run<kFP8, kJagM, 0, 0, 1>(ta, tb, p, 0, c);
     }
-    // jagged K: A = G^T [N_out, P], B = X^T [Kd, P]; tile space M = N_out, N = Kd. The offsets
-    // are checked for order and for fitting the padded length P.
-    p.total_rows = -1;
-    int rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, sA_, boxA, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (rc) return rc;
-    const uint64_t dB[2] = {(uint64_t)g.K, (uint64_t)g.N};
-    const uint32_t boxB[2] = {BKB, BN};
-    rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dB, sA_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (rc) return rc;
-    return run<kFP8, kJagK, 0, 0>(ta, tb, p, (int64_t)g.E * p.num_m * p.num_n, c);
+    return FP8_ERR_INVALID_ARG;
   }
 
   // BF16 (dense only)
   if (g.mode != -1) return FP8_ERR_UNSUPPORTED;
-  p.idesc = make_idesc(kFmtBF16, kFmtBF16, (uint32_t)g.a_mn, (uint32_t)g.b_mn, BM, BN);
+  p.idesc = make_idesc(kFmtBF16, kFmtBF16, (uint32_t)g.a_mn, (uint32_t)g.b_mn, tile_m, BN);
+  const uint32_t b_rows = pair ? BN / 2 : BN;
   CUtensorMap ta, tb;
   int rc;
   if (g.a_mn) {
@@ -547,15 +656,21 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   } else {
     const uint64_t d[2] = {(uint64_t)g.K, (uint64_t)g.N};
     const uint64_t s[1] = {(uint64_t)g.K * 2};
-    const uint32_t box[2] = {64, BN};
+    const uint32_t box[2] = {64, b_rows};
     rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, s, box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (rc) return rc;
   const int64_t tiles = p.num_m * p.num_n;
-  if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1>(ta, tb, p, tiles, c);
-  if (g.a_mn) return run<kBF16, kDense, 1, 0>(ta, tb, p, tiles, c);
-  if (g.b_mn) return run<kBF16, kDense, 0, 1>(ta, tb, p, tiles, c);
-  return run<kBF16, kDense, 0, 0>(ta, tb, p, tiles, c);
+  if (pair) {
+    if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 2>(ta, tb, p, tiles, c);
+    if (g.a_mn) return run<kBF16, kDense, 1, 0, 2>(ta, tb, p, tiles, c);
+    if (g.b_mn) return run<kBF16, kDense, 0, 1, 2>(ta, tb, p, tiles, c);
+    return run<kBF16, kDense, 0, 0, 2>(ta, tb, p, tiles, c);
+  }
+  if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 1>(ta, tb, p, tiles, c);
+  if (g.a_mn) return run<kBF16, kDense, 1, 0, 1>(ta, tb, p, tiles, c);
+  if (g.b_mn) return run<kBF16, kDense, 0, 1, 1>(ta, tb, p, tiles, c);
+  return run<kBF16, kDense, 0, 0, 1>(ta, tb, p, tiles, c);
 }
 
 }  // namespace fp8lin

@@ -31,7 +31,9 @@ def qrows(x, fmt):
     return c, inv, upload_codes(c, fmt), upload_f32(inv)
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (300, 520, 272), (1, 1, 16), (129, 257, 4096), (1000, 2000, 512)])
+# (1024, 4864, 256) and (1300, 4700, 160) have enough 256 x 256 tiles to run on CTA pairs
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (300, 520, 272), (1, 1, 16), (129, 257, 4096), (1000, 2000, 512),
+                                   (1024, 4864, 256), (1300, 4700, 160)])
 @pytest.mark.parametrize("types", [("e4m3", "e4m3"), ("e5m2", "e4m3"), ("e4m3", "e5m2")])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_dense_rowwise(fp8, M, N, K, types, out_dtype):
@@ -79,7 +81,7 @@ def test_dense_large_sampled_rows(fp8):
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (1, 0), (0, 1), (1, 1)])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 296, 136), (512, 768, 1024)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 296, 136), (512, 768, 1024), (1032, 4864, 192)])
 def test_bf16(fp8, a_mn, b_mn, M, N, K):
     a = W.normal_bf16((M, K), 1.0, 21 + M)
     b = W.normal_bf16((N, K), 1.0, 22 + N)

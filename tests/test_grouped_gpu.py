@@ -72,8 +72,9 @@ def test_jagged_m_single_expert_equals_dense(fp8):
     check_gemm(dense, ref, absacc, False)
 
 
+# the last case has enough 256 x 256 tiles per expert set to run on CTA pairs
 @pytest.mark.parametrize("counts,N,Kd", [([100, 0, 300, 37], 72, 200), ([0, 0, 130], 256, 256), ([500], 128, 64),
-                                         ([1, 127, 128, 129, 0], 40, 24)])
+                                         ([1, 127, 128, 129, 0], 40, 24), ([300, 0, 260, 90], 520, 2560)])
 def test_jagged_k(fp8, counts, N, Kd):
     counts = [int(c) for c in counts]
     E, M = len(counts), sum(counts)
