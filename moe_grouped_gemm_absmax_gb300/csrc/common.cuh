@@ -175,6 +175,24 @@ FP8_DEVI void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_
       : "memory");
 }
 
+// TMA bulk-tensor stores shared -> global, tracked per thread in bulk async-groups.
+FP8_DEVI void tma_store_2d(const CUtensorMap* m, const void* src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+FP8_DEVI void tma_store_3d(const CUtensorMap* m, const void* src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+FP8_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+FP8_DEVI void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+FP8_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+FP8_DEVI void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 // ------------------------------------------------------------------------------------------
 // tcgen05: tensor memory allocation, MMA issue, commit, loads, fences.
 FP8_DEVI void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -27,6 +27,8 @@
 //               overlap this epilogue.
 // Every wait is bounded; on a timeout the kernel raises FP8_DEV_TIMEOUT, drains in-flight TMA
 // and MMA work, frees its tensor memory and returns.
+#include <string.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -40,7 +42,7 @@ constexpr int kEpiThreads = 256;  // warps 2..9
 constexpr int kTmemCols = 2 * BN;
 constexpr int kMaxExperts = 2048;
 constexpr int kGroupM = 16;  // rasterization: tiles walk 16 M-blocks per N-block
-constexpr int kRingBytes = 196608;
+constexpr int kStageOut = 4096;  // per epilogue warp: output staging for TMA stores (pairs)
 
 template <int CG>
 struct Cfg {
@@ -48,7 +50,9 @@ struct Cfg {
   static constexpr int B_ROWS = BN / CG;                // this CTA's rows of B
   static constexpr int B_BYTES = B_ROWS * BKB;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB or 32 KB
-  static constexpr int STAGES = kRingBytes / STAGE_BYTES;  // 4 or 6
+  static constexpr int STAGES = CG == 2 ? 5 : 4;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;  // 160 KB or 192 KB
+  static constexpr int OUT_BYTES = CG == 2 ? 8 * kStageOut : 0;
   static constexpr int TILE_M = BM * CG;
 };
 
@@ -69,6 +73,7 @@ struct GemmParams {
   const int32_t* ends;
   int E;
   int64_t total_rows;  // jagged M: last valid offset
+  int tma_out;         // CTA pairs with 16-byte aligned output rows: TMA bulk-tensor stores
   uint32_t idesc;
   int32_t* status;
   uint64_t wait_ns;
@@ -84,8 +89,8 @@ struct Tile {
 
 struct Shared {
   float sb[2][BN];  // per-tile column scales, alternating between consecutive tiles
-  uint64_t full[6];
-  uint64_t empty[6];
+  uint64_t full[5];
+  uint64_t empty[5];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -147,13 +152,14 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t, const int32_t* tpre, cons
 template <int KIND, int SCHED, int A_MN, int B_MN, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   using C = Cfg<CG>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Shared& S = *reinterpret_cast<Shared*>(smem + kRingBytes);
-  int32_t* tpre = reinterpret_cast<int32_t*>(smem + kRingBytes + kSharedBytes);
+  uint8_t* out_stage = smem + C::RING_BYTES;  // [8 warps][kStageOut], pairs only
+  Shared& S = *reinterpret_cast<Shared*>(smem + C::RING_BYTES + C::OUT_BYTES);
+  int32_t* tpre = reinterpret_cast<int32_t*>(smem + C::RING_BYTES + C::OUT_BYTES + kSharedBytes);
   int32_t* aux = tpre + (p.E + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &S.abort;
@@ -234,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (CG == 2) tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     if (CG == 2) {
@@ -421,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = (int)rank * BM + q * 32 + lane;  // row within the pair's tile
     const bool stage_sb = KIND == kFP8 && !p.sb_scalar;
     int buf = 0, sbi = 0;
+    uint32_t oseq = 0;  // TMA stores issued by this warp
     uint32_t aphase = 0;
     for (int64_t t = unit; t < total; t += n_units) {
       const Tile T = get_tile<SCHED, C::TILE_M>(p, t, tpre, aux);
@@ -462,6 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float sb_all = (KIND == kFP8 && p.sb_scalar) ? __ldg(sbp) : 1.0f;
       const uint32_t taddr = tmem_base + (uint32_t)(buf * BN + c0) + ((uint32_t)(q * 32) << 16);
+      // Pairs write through shared memory with TMA bulk-tensor stores (32 rows x 32 columns per
+      // store), unless this warp's 32 rows run past the end of an expert's segment.
+      const int64_t wrow0 = T.m0 + (int64_t)rank * BM + q * 32;
+      const bool via_tma = CG == 2 && p.tma_out && (SCHED != kJagM || wrow0 + 32 <= T.row_end);
 #pragma unroll 1
       for (int ch = 0; ch < BN / 64; ++ch) {
         uint32_t v[32];
@@ -469,13 +481,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         const int cl = c0 + ch * 32;  // tile column of v[0]
         const int64_t n = T.n0 + cl;
-        if (row_ok && n < p.N) {
-          float f[32];
+        if (n >= p.N) continue;  // uniform across the warp
+        float f[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float sb = stage_sb ? sbs[cl + j] : sb_all;
-            f[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sa), sb);
+        for (int j = 0; j < 32; ++j) {
+          const float sb = stage_sb ? sbs[cl + j] : sb_all;
+          f[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sa), sb);
+        }
+        if (via_tma) {
+          uint8_t* st = out_stage + (warp - 2) * kStageOut;
+          if (!p.out_f32) {
+            st += (oseq & 1) * 2048;
+            if (lane == 0 && oseq >= 2) bulk_wait_read_1();  // this half's previous store has read it
+            __syncwarp();
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+              w[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            // row `lane` of a [32][64 B] box, 64-byte swizzle (16-byte chunk ^ (row / 2) % 4)
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+              *reinterpret_cast<uint4*>(st + lane * 64 + ((c4 ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+          } else {
+            if (lane == 0 && oseq >= 1) bulk_wait_read_all();
+            __syncwarp();
+            // row `lane` of a [32][128 B] box, 128-byte swizzle (16-byte chunk ^ row % 8)
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+              *reinterpret_cast<float4*>(st + lane * 128 + ((c8 ^ (lane & 7)) << 4)) =
+                  make_float4(f[4 * c8], f[4 * c8 + 1], f[4 * c8 + 2], f[4 * c8 + 3]);
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (SCHED == kJagK)
+              tma_store_3d(&tmO, st, (int32_t)n, (int32_t)wrow0, T.e);
+            else
+              tma_store_2d(&tmO, st, (int32_t)n, (int32_t)wrow0);
+            bulk_commit();
+          }
+          ++oseq;
+          continue;
+        }
+        if (row_ok) {
           const bool full = p.vec_ok && n + 32 <= p.N;
           if (p.out_f32) {
             float* o = static_cast<float*>(p.out) + orow * p.ldo + n;
@@ -517,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (CG == 2 && warp >= 2 && lane == 0) bulk_wait_all();  // this warp's output stores are done
   tc_fence_before();
   __syncthreads();
   if (CG == 2) cluster_barrier();  // no remote arrive or load into a CTA that has left
@@ -532,16 +584,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int KIND, int SCHED, int A_MN, int B_MN, int CG>
-int run(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int64_t total_tiles_hint, const Ctx& c) {
+int run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const GemmParams& p,
+        int64_t total_tiles_hint, const Ctx& c) {
   auto kern = gemm_kernel<KIND, SCHED, A_MN, B_MN, CG>;
-  const size_t smem = 1024 + kRingBytes + kSharedBytes + (SCHED == kDense ? 0 : 2 * 4 * (p.E + 1));
+  using C = Cfg<CG>;
+  const size_t smem = 1024 + C::RING_BYTES + C::OUT_BYTES + kSharedBytes + (SCHED == kDense ? 0 : 2 * 4 * (p.E + 1));
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FP8_ERR_CUDA;
   int64_t units = c.sm_count / CG;
   if (total_tiles_hint > 0 && total_tiles_hint < units) units = total_tiles_hint;
   if (units < 1) units = 1;
   if (CG == 1) {
-    kern<<<(unsigned)units, kThreads, smem, c.stream>>>(a, b, p);
+    kern<<<(unsigned)units, kThreads, smem, c.stream>>>(a, b, o, p);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
@@ -556,7 +610,7 @@ int run(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int64_t
   cfg.stream = c.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a, b, p) != cudaSuccess) return FP8_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, a, b, o, p) != cudaSuccess) return FP8_ERR_CUDA;
   return FP8_OK;
 }
 
@@ -589,6 +643,29 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   const bool pair = g.mode == FP8_GROUPED_JAGGED_M ? g.M >= 2048 : pair_tiles * 2 >= c.sm_count;
   const int tile_m = pair ? 256 : 128;
   p.num_m = (g.M + tile_m - 1) / tile_m;
+  // output tensor map for the pairs' TMA stores: boxes of 32 rows x 32 columns
+  CUtensorMap to;
+  memset(&to, 0, sizeof(to));
+  p.tma_out = 0;
+  if (pair && p.vec_ok && (reinterpret_cast<uintptr_t>(g.out) & 15) == 0) {
+    const CUtensorMapDataType odt = p.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle osw = p.out_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const uint64_t oes = p.out_f32 ? 4 : 2;
+    int rc;
+    if (g.mode == FP8_GROUPED_JAGGED_K) {
+      const uint64_t d[3] = {(uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.E};
+      const uint64_t st[2] = {(uint64_t)g.N * oes, (uint64_t)(g.M * g.N) * oes};
+      const uint32_t box[3] = {32, 32, 1};
+      rc = make_tmap(&to, g.out, odt, 3, d, st, box, osw);
+    } else {
+      const uint64_t d[2] = {(uint64_t)g.N, (uint64_t)g.M};
+      const uint64_t st[1] = {(uint64_t)g.N * oes};
+      const uint32_t box[2] = {32, 32};
+      rc = make_tmap(&to, g.out, odt, 2, d, st, box, osw);
+    }
+    if (rc) return rc;
+    p.tma_out = 1;
+  }
 
   if (fp8) {
     const uint32_t af = g.a_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
@@ -610,13 +687,13 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
       if (rc) return rc;
       if (g.mode == -1) {
         const int64_t tiles = p.num_m * p.num_n;
-        return pair ? run<kFP8, kDense, 0, 0, 2>(ta, tb, p, tiles, c) : run<kFP8, kDense, 0, 0, 1>(ta, tb, p, tiles, c);
+        return pair ? run<kFP8, kDense, 0, 0, 2>(ta, tb, to, p, tiles, c) : run<kFP8, kDense, 0, 0, 1>(ta, tb, to, p, tiles, c);
       }
       // jagged K: A = G^T [N_out, P], B = X^T [Kd, P]; tile space M = N_out, N = Kd; the
       // offsets are checked for order and for fitting the padded length P.
       p.total_rows = -1;
       const int64_t tiles = (int64_t)g.E * p.num_m * p.num_n;
-      return pair ? run<kFP8, kJagK, 0, 0, 2>(ta, tb, p, tiles, c) : run<kFP8, kJagK, 0, 0, 1>(ta, tb, p, tiles, c);
+      return pair ? run<kFP8, kJagK, 0, 0, 2>(ta, tb, to, p, tiles, c) : run<kFP8, kJagK, 0, 0, 1>(ta, tb, to, p, tiles, c);
     }
     if (g.mode == FP8_GROUPED_JAGGED_M) {
       p.total_rows = g.M;
@@ -625,7 +702,7 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
       const uint32_t boxB[3] = {BKB, b_rows, 1};
       rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dB, sB_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc) return rc;
-      return pair ? run<kFP8, kJagM, 0, 0, 2>(ta, tb, p, 0, c) : run<kFP8, kJagM, 0, 0, 1>(ta, tb, p, 0, c);
+      return pair ? run<kFP8, kJagM, 0, 0, 2>(ta, tb, to, p, 0, c) : run<kFP8, kJagM, 0, 0, 1>(ta, tb, to, p, 0, c);
     }
     return FP8_ERR_INVALID_ARG;
   }
@@ -662,15 +739,15 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   if (rc) return rc;
   const int64_t tiles = p.num_m * p.num_n;
   if (pair) {
-    if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 2>(ta, tb, p, tiles, c);
-    if (g.a_mn) return run<kBF16, kDense, 1, 0, 2>(ta, tb, p, tiles, c);
-    if (g.b_mn) return run<kBF16, kDense, 0, 1, 2>(ta, tb, p, tiles, c);
-    return run<kBF16, kDense, 0, 0, 2>(ta, tb, p, tiles, c);
+    if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 2>(ta, tb, to, p, tiles, c);
+    if (g.a_mn) return run<kBF16, kDense, 1, 0, 2>(ta, tb, to, p, tiles, c);
+    if (g.b_mn) return run<kBF16, kDense, 0, 1, 2>(ta, tb, to, p, tiles, c);
+    return run<kBF16, kDense, 0, 0, 2>(ta, tb, to, p, tiles, c);
   }
-  if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 1>(ta, tb, p, tiles, c);
-  if (g.a_mn) return run<kBF16, kDense, 1, 0, 1>(ta, tb, p, tiles, c);
-  if (g.b_mn) return run<kBF16, kDense, 0, 1, 1>(ta, tb, p, tiles, c);
-  return run<kBF16, kDense, 0, 0, 1>(ta, tb, p, tiles, c);
+  if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 1>(ta, tb, to, p, tiles, c);
+  if (g.a_mn) return run<kBF16, kDense, 1, 0, 1>(ta, tb, to, p, tiles, c);
+  if (g.b_mn) return run<kBF16, kDense, 0, 1, 1>(ta, tb, to, p, tiles, c);
+  return run<kBF16, kDense, 0, 0, 1>(ta, tb, to, p, tiles, c);
 }
 
 }  // namespace fp8lin

@@ -324,21 +324,7 @@ FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t unit, const int32_t* upre,
   return u;
 }
 
-FP8_DEVI void tma_store_2d(const CUtensorMap* m, const void* src, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(smem_u32(src)), "r"(x), "r"(y)
-               : "memory");
-}
-FP8_DEVI void tma_store_3d(const CUtensorMap* m, const void* src, int32_t x, int32_t y, int32_t z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-FP8_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-FP8_DEVI void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-FP8_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 
 // Column j (0..7) of a 16-byte vector of 8 bf16, as fp32.
 FP8_DEVI float col_of(const uint4& v, int j) {
