@@ -412,6 +412,13 @@ def max_over_ranks(v: float, ws: int) -> float:
     return float(t.item())
 
 
+def whole_job_value(units_per_step: float, steps: int, world_size: int, max_total_ms: float, unit: str) -> float:
+    """Throughput of the whole job: the work of every rank's steps over the slowest rank's time
+    (weak scaling: every rank runs its own replica of the workload)."""
+    scale = 1e9 if unit == "TFLOP/s" else 1e6  # flop/ms -> TFLOP/s, byte/ms -> GB/s
+    return units_per_step * steps * world_size / max_total_ms / scale
+
+
 def traffic_for(label: str):
     """ncu DRAM bytes per launch for a kernel label, from profiles/ncu_traffic.json; null when the
     kernel's source changed since the capture."""
@@ -518,7 +525,7 @@ def main():
     total_ms_max = max_over_ranks(total_ms, ws)
     units = step.total_units()
     scale = 1e9 if step.unit == "TFLOP/s" else 1e6  # flop/ms -> TFLOP/s, byte/ms -> GB/s
-    value = units * args.steps * ws / total_ms_max / scale
+    value = whole_job_value(units, args.steps, ws, total_ms_max, step.unit)
 
     kernels = []
     for (label, kind, amount, pk), ms in zip(step.kernels, per_kernel):
