@@ -214,6 +214,12 @@ int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* saved, const fp
                    fp8_tensor* dw, void* workspace, size_t workspace_bytes, int32_t* d_status,
                    void* stream);
 
+/* Test hook for failure detection: while enabled, every GEMM launch first waits on a barrier
+ * that nothing signals; the wait runs out after the wait limit (fp8_set_wait_limit_ns), the
+ * kernel reports FP8_DEV_TIMEOUT, drains and returns. Off by default. Returns the previous
+ * setting. */
+int fp8_set_test_stall(int enable);
+
 /*
  * fp8_quantize_tensor_noalloc — the tensorwise quantize of fp8_quantize (FP8_GRAN_TENSOR) for
  * callers that cannot allocate device memory. The pages have no counterpart: this entry point

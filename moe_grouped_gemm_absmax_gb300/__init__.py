@@ -78,6 +78,8 @@ def _load():
     L.fp8_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.fp8_set_wait_limit_ns.restype = ctypes.c_uint64
     L.fp8_quantize_tensor_noalloc.argtypes = [T, ctypes.c_int, ctypes.c_int, T, T, T, P]
+    L.fp8_set_test_stall.argtypes = [ctypes.c_int]
+    L.fp8_set_test_stall.restype = ctypes.c_int
     return L
 
 
@@ -86,7 +88,7 @@ lib = _load()
 # Symbols include/fp8lin.h declares (checked by the CPU tests against the header and the .so).
 EXPORTS = ("fp8_quantize", "fp8_scaled_mm", "fp8_grouped_mm", "fp8_linear_fwd", "fp8_linear_bwd",
            "fp8_workspace_size", "fp8_jagged_padded_rows", "fp8_status_string", "fp8_set_wait_limit_ns",
-           "fp8_quantize_tensor_noalloc")
+           "fp8_quantize_tensor_noalloc", "fp8_set_test_stall")
 
 
 def status_string(code: int) -> str:
@@ -194,6 +196,10 @@ def fp8_jagged_padded_rows(rows: int, n_segments: int) -> int:
 
 def fp8_set_wait_limit_ns(ns: int) -> int:
     return int(lib.fp8_set_wait_limit_ns(ns))
+
+
+def fp8_set_test_stall(enable: bool) -> int:
+    return int(lib.fp8_set_test_stall(1 if enable else 0))
 
 
 # ------------------------------------------------------------------------------------------

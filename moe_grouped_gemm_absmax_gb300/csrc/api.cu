@@ -10,6 +10,7 @@
 namespace fp8lin {
 
 static std::atomic<uint64_t> g_wait_ns{4000000000ull};
+static std::atomic<int> g_test_stall{0};
 
 int make_ctx(Ctx* ctx, void* stream, int32_t* status) {
   static std::mutex mu;
@@ -35,6 +36,7 @@ int make_ctx(Ctx* ctx, void* stream, int32_t* status) {
   ctx->stream = static_cast<cudaStream_t>(stream);
   ctx->status = status;
   ctx->wait_ns = g_wait_ns.load();
+  ctx->test_stall = g_test_stall.load();
   return FP8_OK;
 }
 
@@ -118,6 +120,8 @@ extern "C" int64_t fp8_jagged_padded_rows(int64_t rows, int64_t n_segments) {
 }
 
 extern "C" uint64_t fp8_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns ? ns : 1); }
+
+extern "C" int fp8_set_test_stall(int enable) { return g_test_stall.exchange(enable ? 1 : 0); }
 
 extern "C" const char* fp8_status_string(int code) {
   switch (code) {

@@ -43,6 +43,10 @@ constexpr int kTmemCols = 2 * BN;
 constexpr int kMaxExperts = 2048;
 constexpr int kGroupM = 16;  // rasterization: tiles walk 16 M-blocks per N-block
 constexpr int kStageOut = 4096;  // per epilogue warp: output staging for TMA stores (pairs)
+// Waits for work already in flight (TMA loads, MMAs) before tensor memory is freed or the CTA
+// leaves use this fixed bound, not the adjustable one, so a short limit never frees resources
+// under running hardware.
+constexpr uint64_t kDrainNs = 2000000000ull;
 
 template <int CG>
 struct Cfg {
@@ -74,6 +78,7 @@ struct GemmParams {
   int E;
   int64_t total_rows;  // jagged M: last valid offset
   int tma_out;         // CTA pairs with 16-byte aligned output rows: TMA bulk-tensor stores
+  int test_stall;      // wait first on a barrier nothing signals (failure-detection tests)
   uint32_t idesc;
   int32_t* status;
   uint64_t wait_ns;
@@ -94,6 +99,7 @@ struct Shared {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t never;   // signalled by no one: the failure-detection test hook waits on it
   uint32_t tmem_base;
   int abort;
 };
@@ -236,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.tempty[b], CG * kEpiThreads / 32);
     }
     mbar_init(&S.drain, 1);
+    mbar_init(&S.never, 1);
     S.abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -341,11 +348,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Drain: the last (up to STAGES) loads must land before the CTA (pair) may exit. For a
-      // pair, the issuing CTA's full barriers count both CTAs' loads.
+      // pair, the issuing CTA's full barriers count both CTAs' loads; after an abort the other
+      // CTA cannot observe them and lets its own last loads settle for 100 us instead.
       if (issuer) {
         const int64_t first = issued > STAGES ? issued - STAGES : 0;
         for (int64_t i = first; i < issued; ++i)
-          mbar_wait(&S.full[i % STAGES], (uint32_t)((i / STAGES) & 1), nullptr, p.wait_ns);
+          mbar_wait(&S.full[i % STAGES], (uint32_t)((i / STAGES) & 1), nullptr, kDrainNs);
+      } else if (!ok) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) {
+        }
       }
     }
     __syncwarp();
@@ -357,6 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int buf = 0;
       uint32_t aphase = 0;
       bool ok = true;
+      if (p.test_stall && !mbar_wait(&S.never, 0, abort_flag, p.wait_ns)) {
+        fail();
+        ok = false;
+      }
       for (int64_t t = unit; t < total && ok; t += n_units) {
         const Tile T = get_tile<SCHED, C::TILE_M>(p, t, tpre, aux);
         if (T.nkb == 0) continue;
@@ -573,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (CG == 2) cluster_barrier();  // no remote arrive or load into a CTA that has left
   if (warp == 1) {
-    if (lane == 0) mbar_wait(&S.drain, 0, nullptr, p.wait_ns);  // the MMAs writing this CTA's TMEM
+    if (lane == 0) mbar_wait(&S.drain, 0, nullptr, kDrainNs);  // the MMAs writing this CTA's TMEM
     __syncwarp();
     tc_fence_after();
     if (CG == 2)
@@ -630,6 +646,7 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   p.out_f32 = g.out_dtype == FP8_DT_F32;
   p.status = c.status;
   p.wait_ns = c.wait_ns;
+  p.test_stall = c.test_stall;
   p.ends = g.ends;
   p.E = (int)g.E;
   p.num_n = (g.N + BN - 1) / BN;

@@ -16,6 +16,7 @@ struct Ctx {
   uint64_t wait_ns;  // bound of every on-device wait
   int sm_count;
   int device;
+  int test_stall;    // failure-detection test hook (see fp8_set_test_stall)
 };
 
 // Fills ctx for the current device; returns FP8_OK or FP8_ERR_DEVICE.

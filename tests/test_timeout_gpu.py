@@ -1,0 +1,53 @@
+"""Failure detection without a GPU fault: every on-device wait of the GEMM kernels is bounded.
+The test hook fp8_set_test_stall makes the MMA issuer wait on a barrier that nothing signals;
+with a short wait limit that wait runs out, and the kernel must report FP8_DEV_TIMEOUT in the
+status word, stop its other warps, drain its in-flight TMA loads and MMAs, free its tensor
+memory and return, leaving the context usable (a normal GEMM afterwards is correct)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.gpu_util import bits, check_gemm, upload_codes, upload_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp8():
+    import moe_grouped_gemm_absmax_gb300 as m
+    return m
+
+
+def _operands(M, N, K, seed):
+    x = W.normal_bf16((M, K), 1.0, seed)
+    w = W.normal_bf16((N, K), 0.02, seed + 1)
+    ca, ia = oracle.quantize_rows(bits(x), oracle.E4M3)
+    cb, ib = oracle.quantize_rows(bits(w), oracle.E4M3)
+    return ca, ia, cb, ib
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 2048), (2048, 4096, 1024)])  # single CTAs, CTA pairs
+def test_wait_limit_expiry_reports_timeout_and_context_survives(fp8, M, N, K):
+    ca, ia, cb, ib = _operands(M, N, K, 5)
+    A, B, sA, sB = upload_codes(ca, 0), upload_codes(cb, 0), upload_f32(ia), upload_f32(ib)
+    out = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    old = fp8.fp8_set_wait_limit_ns(2_000_000)  # 2 ms
+    fp8.fp8_set_test_stall(True)
+    try:
+        fp8.fp8_scaled_mm(A, B, sA, sB, out, status=st)
+        torch.cuda.synchronize()
+    finally:
+        fp8.fp8_set_test_stall(False)
+        fp8.fp8_set_wait_limit_ns(old)
+    assert int(st.item()) & fp8.DEV_TIMEOUT
+    # the same call with the normal bound succeeds and is correct
+    st.zero_()
+    fp8.fp8_scaled_mm(A, B, sA, sB, out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows = np.arange(0, M, max(1, M // 64))
+    ref, absacc = oracle.gemm_fp8(ca, oracle.E4M3, cb, oracle.E4M3, ia, ib, rows=rows)
+    check_gemm(out[torch.from_numpy(rows).cuda()], ref, absacc, True)
