@@ -132,8 +132,11 @@ typedef struct fp8_tensor {
  *  inv_scales  fp32: [1] (tensor), [R] or [B*R] (row), [C], [B, C] or [E, C] (col).
  *  offsets     NULL, or int32 [E] cumulative segment ends (COL granularity, 2-D x only).
  *              Checked on the device: a bad vector sets FP8_DEV_BAD_OFFSETS.
- *  workspace   device memory of fp8_workspace_size(FP8_OP_QUANTIZE, ...) bytes (4 bytes for
- *              tensor granularity, 0 otherwise); may be NULL when that size is 0.
+ *  workspace   device memory, 16-byte aligned, of fp8_workspace_size(FP8_OP_QUANTIZE, groups,
+ *              C, granularity) bytes: 4 bytes for tensor granularity (the amax word), 4 bytes
+ *              per (group, column) for column granularity (groups = B for 3-D x, E with
+ *              offsets, else 1; the per-column amax and then the fp32 scale), 0 for row
+ *              granularity (workspace may then be NULL).
  * Bit-exactness: codes and inverse scales equal the recipe evaluated with an fp64 division,
  * an fp32 multiply and a round-to-nearest-even saturating cast (eps = 1e-12).
  */
@@ -248,9 +251,8 @@ int fp8_set_test_stall(int enable);
 int fp8_quantize_tensor_noalloc(const fp8_tensor* x, int out_dtype, int layout, fp8_tensor* out,
                                 fp8_tensor* out_t, fp8_tensor* inv_scale, void* stream);
 
-/* Workspace bytes for an operation. FP8_OP_QUANTIZE: (d0, d1, d2) unused except that
- * granularity selects 4 bytes (tensor) or 0. FP8_OP_LINEAR_FWD / FP8_OP_LINEAR_BWD:
- * (d0, d1, d2) = (M, K, N). */
+/* Workspace bytes for an operation. FP8_OP_QUANTIZE: (d0, d1) = (groups, columns) as described
+ * at fp8_quantize (d2 unused). FP8_OP_LINEAR_FWD / FP8_OP_LINEAR_BWD: (d0, d1, d2) = (M, K, N). */
 size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granularity,
                           int wgrad_mode);
 

@@ -205,6 +205,12 @@ def fp8_set_test_stall(enable: bool) -> int:
 # ------------------------------------------------------------------------------------------
 # allocation helpers (torch buffers of the right shapes, then the entry points above)
 
+def col_workspace(groups: int, cols: int, device) -> torch.Tensor:
+    """Workspace of a column-granularity fp8_quantize (one word per group and column)."""
+    n = fp8_workspace_size(OP_QUANTIZE, groups, cols, granularity=GRAN_COL)
+    return torch.empty(max(n // 4, 4), dtype=torch.int32, device=device)
+
+
 def quantize_alloc(x, granularity, out_dtype, layout=None, offsets=None, padded_rows=None, status=None,
                    stream=None):
     """Returns (out or None, out_t or None, inv_scales). Shapes follow include/fp8lin.h."""
@@ -230,8 +236,11 @@ def quantize_alloc(x, granularity, out_dtype, layout=None, offsets=None, padded_
             P = padded_rows or fp8_jagged_padded_rows(R, E)
             out_t = torch.empty((C, P), dtype=fdt, device=dev)
             inv = torch.empty((E, C), dtype=torch.float32, device=dev)
+            groups = E
         else:
             out_t = torch.empty((B, C, R) if x.dim() == 3 else (C, R), dtype=fdt, device=dev)
             inv = torch.empty((B, C) if x.dim() == 3 else (C,), dtype=torch.float32, device=dev)
+            groups = B
+        ws = col_workspace(groups, C, dev)
     fp8_quantize(x, granularity, out_dtype, layout, out, out_t, inv, offsets, ws, status=status, stream=stream)
     return out, out_t, inv

@@ -186,6 +186,10 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
     }
     case FP8_GRAN_COL: {
       FP8_CHECK(layout == FP8_LAYOUT_COL_MAJOR, FP8_ERR_UNSUPPORTED);
+      const int64_t groups = offsets ? (valid_desc(offsets) && offsets->ndim == 1 ? offsets->shape[0] : 0) : B;
+      FP8_CHECK(ws && (reinterpret_cast<uintptr_t>(ws) & 15u) == 0 && ws_bytes >= (size_t)(groups * C * 4),
+                FP8_ERR_WORKSPACE);
+      uint32_t* scratch = static_cast<uint32_t*>(ws);
       if (offsets) {
         FP8_CHECK(nd == 2, FP8_ERR_UNSUPPORTED);
         FP8_CHECK(valid_desc(offsets) && offsets->dtype == FP8_DT_I32 && offsets->ndim == 1 && offsets->shape[0] >= 1,
@@ -197,7 +201,7 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
         FP8_CHECK(P % 16 == 0, FP8_ERR_ALIGNMENT);
         FP8_CHECK(numel(inv) == E * C, FP8_ERR_INVALID_ARG);
         return launch_quant_cols(x->ptr, R, C, E, 0, static_cast<const int32_t*>(offsets->ptr), out_dtype,
-                                 out_t->ptr, P, static_cast<float*>(inv->ptr), c);
+                                 out_t->ptr, P, static_cast<float*>(inv->ptr), scratch, c);
       }
       FP8_CHECK(R % 16 == 0, FP8_ERR_ALIGNMENT);
       if (nd == 2)
@@ -206,7 +210,7 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
         FP8_CHECK(shape_is(out_t, 3, B, C, R), FP8_ERR_INVALID_ARG);
       FP8_CHECK(numel(inv) == B * C, FP8_ERR_INVALID_ARG);
       return launch_quant_cols(x->ptr, B * R, C, B, R, nullptr, out_dtype, out_t->ptr, R,
-                               static_cast<float*>(inv->ptr), c);
+                               static_cast<float*>(inv->ptr), scratch, c);
     }
     default:
       return FP8_ERR_INVALID_ARG;
@@ -376,7 +380,7 @@ static fp8_tensor T1(void* p, int dt, int64_t a) {
 
 // Workspace layout of the backward pass (each piece 256-byte aligned).
 struct BwdLayout {
-  size_t amax, dy_q, dy_inv, dyt_q, dyt_inv, wt_q, wt_inv, xt_q, xt_inv, total;
+  size_t amax, dy_q, dy_inv, dyt_q, dyt_inv, wt_q, wt_inv, xt_q, xt_inv, col_scratch, total;
 };
 static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad) {
   BwdLayout L = {};
@@ -396,14 +400,18 @@ static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad
   L.wt_inv = rows ? take((size_t)K * 4) : 0;
   L.xt_q = (fp8w && rows) ? take((size_t)(K * M)) : 0;
   L.xt_inv = (fp8w && rows) ? take((size_t)K * 4) : 0;
+  // per-column scratch of the column-wise quantizations (used one after the other)
+  L.col_scratch = rows ? take((size_t)(K > N ? K : N) * 4) : 0;
   L.total = off;
   return L;
 }
 
 extern "C" size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granularity, int wgrad_mode) {
   switch (op) {
-    case FP8_OP_QUANTIZE:
-      return granularity == FP8_GRAN_TENSOR ? 4 : 0;
+    case FP8_OP_QUANTIZE:  // (d0, d1) = (groups, columns) for FP8_GRAN_COL
+      if (granularity == FP8_GRAN_TENSOR) return 4;
+      if (granularity == FP8_GRAN_COL) return (size_t)(d0 > 0 ? d0 : 1) * (size_t)(d1 > 0 ? d1 : 0) * 4;
+      return 0;
     case FP8_OP_LINEAR_FWD:
       return granularity == FP8_GRAN_TENSOR ? 256 : 0;
     case FP8_OP_LINEAR_BWD:
@@ -487,7 +495,7 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
     fp8_tensor wt_q = T2(ws + L.wt_q, FP8_DT_E4M3, K, N);
     fp8_tensor wt_inv = T1(ws + L.wt_inv, FP8_DT_F32, K);
     FP8_TRY(quantize_impl(w, FP8_GRAN_COL, FP8_DT_E4M3, FP8_LAYOUT_COL_MAJOR, nullptr, &wt_q, &wt_inv, nullptr,
-                          nullptr, 0, c));
+                          ws + L.col_scratch, (size_t)K * 4, c));
     FP8_TRY(scaled_mm_impl(&dy_q, &wt_q, &dy_inv, &wt_inv, dx, 0, c));
   }
   if (need_dw) {
@@ -497,9 +505,9 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
       fp8_tensor xt_q = T2(ws + L.xt_q, FP8_DT_E4M3, K, M);
       fp8_tensor xt_inv = T1(ws + L.xt_inv, FP8_DT_F32, K);
       FP8_TRY(quantize_impl(dy, FP8_GRAN_COL, FP8_DT_E5M2, FP8_LAYOUT_COL_MAJOR, nullptr, &dyt_q, &dyt_inv, nullptr,
-                            nullptr, 0, c));
+                            ws + L.col_scratch, (size_t)N * 4, c));
       FP8_TRY(quantize_impl(x, FP8_GRAN_COL, FP8_DT_E4M3, FP8_LAYOUT_COL_MAJOR, nullptr, &xt_q, &xt_inv, nullptr,
-                            nullptr, 0, c));
+                            ws + L.col_scratch, (size_t)K * 4, c));
       FP8_TRY(scaled_mm_impl(&dyt_q, &xt_q, &dyt_inv, &xt_inv, dw, 0, c));
     } else {
       FP8_TRY(scaled_mm_impl(dy, x, nullptr, nullptr, dw, FP8_MM_A_MN_MAJOR | FP8_MM_B_MN_MAJOR, c));

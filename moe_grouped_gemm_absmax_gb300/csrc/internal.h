@@ -37,9 +37,10 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 // scale per column: either n_groups consecutive groups of group_rows rows (ends == null) or the
 // segments given by ends[n_groups] (segment-padded output, padded row count ld_out).
 // out_t row (g, c) starts at out_t + (g * C + c) * ld_out (dense) or out_t + c * ld_out + pstart_g
-// (segments). inv [n_groups, C].
+// (segments). inv [n_groups, C]. scratch: n_groups * C words of device memory.
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
-                      const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, const Ctx& c);
+                      const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, uint32_t* scratch,
+                      const Ctx& c);
 
 // --- GEMM launchers (gemm.cu) ---
 struct GemmArgs {

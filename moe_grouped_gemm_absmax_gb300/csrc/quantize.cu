@@ -7,12 +7,8 @@
 // dual row/column-major output), Level 2 (column-wise scales with the output tile transposed
 // on chip so the column-major writes are coalesced; single pass over the data), Level 3
 // (relaxed atomics for the commutative amax reduction).
-#include <cooperative_groups.h>
-
 #include "common.cuh"
 #include "internal.h"
-
-namespace cg = cooperative_groups;
 
 namespace fp8lin {
 
@@ -219,34 +215,24 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 }
 
 // ==========================================================================================
-// Columnwise with column-major output, single pass, register-resident.
-//
-// Work unit = (row group g, strips of 64 columns). A group of n rows needs k CTAs (k = the
-// power of two >= n / (128 NB), at most the cluster size cs); a cluster of cs CTAs then
-// processes cs / k strips of the group at once, one sub-team of k CTAs per strip, each member
-// holding up to 128 NB rows of its strip in registers:
-//   - loads: a thread reads 4 consecutive rows x 8 columns (four 16-byte loads; a warp reads 4
-//     whole 128-byte rows per instruction), keeps them in registers and folds |x| into packed
-//     per-column maxima;
-//   - the CTA's column maxima go to shared memory; one cluster barrier; each CTA folds its
-//     sub-team peers' maxima through distributed shared memory and derives the 64 scales;
-//   - cast from registers: each 4-row column pack becomes one 32-bit word of FP8 codes; the
-//     words are written into a transposed tile (64 columns x 128 rows per box, TMA 128-byte
-//     swizzle; the order of a thread's 8 columns is rotated by its chunk index so the shared
-//     stores are conflict-free), then TMA bulk-tensor stores write the column-major output.
-// Clusters are persistent and walk the units. Groups of more than cs * 128 NB rows take two
-// passes (amax over all rows, then re-read and cast).
+// Columnwise with column-major output: three stream-ordered kernels over (row group, 64-column
+// strip, row tile) work units, which never straddle a group (segment) boundary.
+//   1. colmax:   coalesced 16-byte loads (a warp reads four whole 128-byte row segments per
+//                instruction); per-column |x| maxima folded in registers, shuffles and shared
+//                memory; one relaxed atomic max per column per tile into a per-column scratch
+//                word (the bf16 bit pattern of the maximum).
+//   2. colscale: one thread per (group, column): the scale step; the fp32 scale replaces the
+//                amax word in the scratch and the inverse scale goes to the output.
+//   3. colcast:  the same loads, the fp32 multiply and the cast in registers; each 4-row column
+//                pack becomes one 32-bit word of FP8 codes, written into a transposed tile in
+//                shared memory (64 columns x 128 rows per box, TMA 128-byte swizzle; a thread's 8
+//                columns are rotated by its chunk index so the stores are conflict-free); TMA
+//                bulk-tensor stores write whole column-major boxes.
+// The cast pass re-reads the input. Work units walk the strips of a row tile first, so the
+// re-read mostly hits the 129 MB L2 when the tensor fits in it; larger tensors read it twice.
 constexpr int kColThreads = 256;
-constexpr int kColCtrlBytes = 4096;
-
-struct ColCtrl {
-  uint32_t part[2][32];    // this CTA's packed |bf16| column-pair maxima, by unit parity
-  uint32_t red[8][8][4];   // per warp, per 8-column chunk, 4 packed pairs
-  float s32[64];
-  int32_t total_units;
-  int32_t bad;
-};
-static_assert(sizeof(ColCtrl) <= kColCtrlBytes, "column kernel control block");
+constexpr int kColNB = 4;                  // 128-row blocks per work unit (512 rows)
+constexpr int kColTile = 128 * kColNB;
 
 struct ColParams {
   const uint16_t* x;
@@ -255,40 +241,25 @@ struct ColParams {
   int64_t n_groups;
   int64_t group_rows;  // dense modes
   const int32_t* ends; // segment mode
+  uint32_t* scratch;   // [n_groups, C]: amax bits, then fp32 scales
   float* inv;
   int32_t* status;
   int64_t n_strips;
-  int cs;              // CTAs per cluster
   int mode;            // 0: 2-D [C, R] output; 1: batched [B, C, R]; 2: segments [C, P]
-  int dense_k;         // dense modes: CTAs per strip
 };
 
 struct ColUnit {
-  int64_t g, g0, n, pstart, write_end, chunk;
-  int64_t strip;       // this CTA's strip (may be >= n_strips: idle member)
-  int k, member, sub, rounds;
+  int64_t g, g0, n, pstart, write_end, rt;  // group, first row, rows, padded start, rows written, tile start
+  int64_t c0;                                // first column of the strip
 };
 
-FP8_DEVI int ceil_pow2_int(int64_t v) {
-  int k = 1;
-  while (k < v) k <<= 1;
-  return k;
-}
-
-// Sub-team size of a group of n rows: k CTAs of cap rows each, a power of two <= cs.
-FP8_DEVI int team_size(int64_t n, int cap, int cs) {
-  const int64_t need = ceil_div64(n, cap);
-  const int k = ceil_pow2_int(need < 1 ? 1 : need);
-  return k > cs ? cs : k;
-}
-
-template <int NB>
-FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t unit, const int32_t* upre, const int32_t* ppre, int rank) {
-  constexpr int CAP = 128 * NB;
+// Units: dense modes have n_groups * tiles * strips; segments a prefix over the segments.
+// upre[e] = first unit of segment e; ppre[e] = padded start of segment e.
+FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t unit, const int32_t* upre, const int32_t* ppre) {
   ColUnit u;
   int64_t local;
   if (p.mode == 2) {
-    int lo = 0, hi = (int)p.n_groups - 1;  // the segment whose unit range holds `unit`
+    int lo = 0, hi = (int)p.n_groups - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (upre[mid] <= unit) lo = mid;
@@ -300,145 +271,109 @@ FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t unit, const int32_t* upre,
     u.n = p.ends[lo] - u.g0;
     u.pstart = ppre[lo];
     u.write_end = round_up64(u.n, 128);
-    u.k = team_size(u.n, CAP, p.cs);
   } else {
-    u.k = p.dense_k;
-    const int64_t upg = ceil_div64(p.n_strips, p.cs / u.k);
-    u.g = unit / upg;
-    local = unit % upg;
+    const int64_t tiles = ceil_div64(p.group_rows, kColTile);
+    u.g = unit / (tiles * p.n_strips);
+    local = unit % (tiles * p.n_strips);
     u.g0 = u.g * p.group_rows;
     u.n = p.group_rows;
     u.pstart = 0;
     u.write_end = u.n;
   }
-  u.sub = rank / u.k;
-  u.member = rank % u.k;
-  u.strip = local * (p.cs / u.k) + u.sub;
-  if (u.n <= (int64_t)u.k * CAP) {
-    u.chunk = round_up64(ceil_div64(u.n, u.k), 128);
-    u.rounds = u.n > 0 ? 1 : 0;
-  } else {
-    u.chunk = CAP;
-    u.rounds = (int)ceil_div64(u.n, (int64_t)u.k * CAP);
-  }
+  u.rt = (local / p.n_strips) * kColTile;
+  u.c0 = (local % p.n_strips) * 64;
   return u;
 }
 
-
-
-// Column j (0..7) of a 16-byte vector of 8 bf16, as fp32.
-FP8_DEVI float col_of(const uint4& v, int j) {
-  const uint32_t w = j < 2 ? v.x : (j < 4 ? v.y : (j < 6 ? v.z : v.w));
-  return (j & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+// Validates the offsets (segment mode) and builds the unit / padded-start prefixes in shared
+// memory; returns the number of units, or -1 after reporting bad offsets.
+FP8_DEVI int64_t col_setup(const ColParams& p, int32_t* upre, int32_t* ppre) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (p.mode != 2) return p.n_groups * ceil_div64(p.group_rows, kColTile) * p.n_strips;
+  int bad = 0;
+  for (int64_t e = tid; e < p.n_groups; e += kColThreads) {
+    const int64_t cur = p.ends[e], prev = e ? p.ends[e - 1] : 0;
+    if (cur < prev || (e == p.n_groups - 1 && cur != p.rows_total)) bad = 1;
+  }
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    if (blockIdx.x == 0 && tid == 0) set_status(p.status, FP8_DEV_BAD_OFFSETS);
+    return -1;
+  }
+  if (warp == 0) {
+    int cu = 0, cp = 0;
+    for (int64_t base = 0; base < p.n_groups; base += 32) {
+      const int64_t i = base + lane;
+      int vu = 0, vp = 0;
+      if (i < p.n_groups) {
+        const int64_t n = p.ends[i] - (i ? p.ends[i - 1] : 0);
+        vu = (int)(ceil_div64(n, kColTile) * p.n_strips);
+        vp = (int)round_up64(n, 128);
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int yu = __shfl_up_sync(0xffffffffu, vu, o);
+        const int yp = __shfl_up_sync(0xffffffffu, vp, o);
+        if (lane >= o) {
+          vu += yu;
+          vp += yp;
+        }
+      }
+      if (i < p.n_groups) {
+        upre[i + 1] = vu + cu;
+        ppre[i + 1] = vp + cp;
+      }
+      cu += __shfl_sync(0xffffffffu, vu, 31);
+      cp += __shfl_sync(0xffffffffu, vp, 31);
+    }
+    if (lane == 0) {
+      upre[0] = 0;
+      ppre[0] = 0;
+    }
+  }
+  __syncthreads();
+  return upre[p.n_groups];
 }
 
-template <int FMT, int NB>
-__global__ void __launch_bounds__(kColThreads, NB <= 4 ? 2 : 1)
-    quant_cols_kernel(const __grid_constant__ CUtensorMap tm_out, const ColParams p) {
-  constexpr int CAP = 128 * NB;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
-  const int cs = p.cs;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* T = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  ColCtrl& S = *reinterpret_cast<ColCtrl*>(T + CAP * 64);
-  int32_t* upre = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(&S) + kColCtrlBytes);  // [E + 1]
-  int32_t* ppre = upre + (p.n_groups + 1);                                                    // [E + 1]
+// This thread's 4 rows x 8 columns of every 128-row block of the unit (zeros outside the
+// group and the matrix): rows 128 b + 16 warp + 4 rq + jj, columns c0 + 8 ch .. + 7.
+FP8_DEVI void col_load(const ColParams& p, const ColUnit& u, int warp, int ch, int rq, uint4 (&v)[kColNB][4]) {
+  int64_t valid = u.n - u.rt;
+  valid = valid < 0 ? 0 : (valid < kColTile ? valid : kColTile);
+  const bool ch_ok = u.c0 + ch * 8 < p.C;
+  const uint16_t* base = p.x + (u.g0 + u.rt) * p.C + u.c0 + ch * 8;
+#pragma unroll
+  for (int b = 0; b < kColNB; ++b)
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int row = 128 * b + 16 * warp + 4 * rq + jj;
+      v[b][jj] = (ch_ok && row < valid) ? ld_nc_v4(base + (int64_t)row * p.C) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+__global__ void __launch_bounds__(kColThreads) colmax_kernel(const ColParams p) {
+  __shared__ uint32_t red[8][8][4];
+  extern __shared__ int32_t pre[];
+  int32_t* upre = pre;
+  int32_t* ppre = pre + (p.n_groups + 1);
+  const int64_t total = col_setup(p, upre, ppre);
+  if (total < 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ch = lane & 7, rq = lane >> 3;  // 8-column chunk, row quad within the warp's 16 rows
-  const int64_t cluster_id = blockIdx.x / cs, n_clusters = gridDim.x / cs;
-
-  // ---- units: dense modes have a fixed count; segments need the offsets ----
-  int64_t total_units;
-  if (p.mode == 2) {
-    int bad = 0;
-    for (int64_t e = tid; e < p.n_groups; e += kColThreads) {
-      const int64_t cur = p.ends[e], prev = e ? p.ends[e - 1] : 0;
-      if (cur < prev || (e == p.n_groups - 1 && cur != p.rows_total)) bad = 1;
-    }
-    bad = __syncthreads_or(bad);
-    if (bad) {
-      if (blockIdx.x == 0 && tid == 0) set_status(p.status, FP8_DEV_BAD_OFFSETS);
-      return;  // every CTA takes this branch before any cluster barrier
-    }
-    if (warp == 0) {  // prefix of units per segment and of padded segment lengths
-      int cu = 0, cp = 0;
-      for (int64_t base = 0; base < p.n_groups; base += 32) {
-        const int64_t i = base + lane;
-        int vu = 0, vp = 0;
-        if (i < p.n_groups) {
-          const int64_t n = p.ends[i] - (i ? p.ends[i - 1] : 0);
-          const int k = team_size(n, CAP, cs);
-          vu = (int)ceil_div64(p.n_strips, cs / k);
-          vp = (int)round_up64(n, 128);
-        }
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int yu = __shfl_up_sync(0xffffffffu, vu, o);
-          const int yp = __shfl_up_sync(0xffffffffu, vp, o);
-          if (lane >= o) {
-            vu += yu;
-            vp += yp;
-          }
-        }
-        if (i < p.n_groups) {
-          upre[i + 1] = vu + cu;
-          ppre[i + 1] = vp + cp;
-        }
-        cu += __shfl_sync(0xffffffffu, vu, 31);
-        cp += __shfl_sync(0xffffffffu, vp, 31);
-      }
-      if (lane == 0) {
-        upre[0] = 0;
-        ppre[0] = 0;
-      }
-    }
-    __syncthreads();
-    total_units = upre[p.n_groups];
-  } else {
-    total_units = p.n_groups * ceil_div64(p.n_strips, cs / p.dense_k);
-  }
-  if (tid == 0) tma_prefetch_desc(&tm_out);
-
-  int parity = 0;
-  for (int64_t unit = cluster_id; unit < total_units; unit += n_clusters, parity ^= 1) {
-    const ColUnit u = col_unit<NB>(p, unit, upre, ppre, rank);
-    const bool on = u.strip < p.n_strips;
-    const int64_t c0 = u.strip * 64;
-    const bool ch_ok = on && c0 + ch * 8 < p.C;
-    // this thread's rows within a member's chunk: block b, rows 128 b + 16 warp + 4 rq + jj
-    uint4 v[NB][4];
-    auto load_round = [&](int r, int64_t* rel0_out, int64_t* valid_out) {
-      const int64_t rel0 = ((int64_t)r * u.k + u.member) * u.chunk;
-      int64_t valid = u.n - rel0;
-      valid = valid < 0 ? 0 : (valid < u.chunk ? valid : u.chunk);
-      const uint16_t* base = p.x + (u.g0 + rel0) * p.C + c0 + ch * 8;
-#pragma unroll
-      for (int b = 0; b < NB; ++b)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int row = 128 * b + 16 * warp + 4 * rq + jj;
-          v[b][jj] = (ch_ok && row < valid) ? ld_nc_v4(base + (int64_t)row * p.C) : make_uint4(0, 0, 0, 0);
-        }
-      *rel0_out = rel0;
-      *valid_out = valid;
-    };
-
-    // ---- pass 1: packed per-column maxima (x: cols 0-1, y: 2-3, z: 4-5, w: 6-7 of the chunk) ----
+  const int ch = lane & 7, rq = lane >> 3;
+  for (int64_t unit = blockIdx.x; unit < total; unit += gridDim.x) {
+    const ColUnit u = col_unit(p, unit, upre, ppre);
+    uint4 v[kColNB][4];
+    col_load(p, u, warp, ch, rq, v);
     uint32_t m4[4] = {0, 0, 0, 0};
-    for (int r = 0; r < u.rounds; ++r) {
-      int64_t rel0, valid;
-      load_round(r, &rel0, &valid);
 #pragma unroll
-      for (int b = 0; b < NB; ++b)
+    for (int b = 0; b < kColNB; ++b)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          m4[0] = absmax2(m4[0], v[b][jj].x);
-          m4[1] = absmax2(m4[1], v[b][jj].y);
-          m4[2] = absmax2(m4[2], v[b][jj].z);
-          m4[3] = absmax2(m4[3], v[b][jj].w);
-        }
-    }
+      for (int jj = 0; jj < 4; ++jj) {
+        m4[0] = absmax2(m4[0], v[b][jj].x);
+        m4[1] = absmax2(m4[1], v[b][jj].y);
+        m4[2] = absmax2(m4[2], v[b][jj].z);
+        m4[3] = absmax2(m4[3], v[b][jj].w);
+      }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       m4[i] = __vmaxu2(m4[i], __shfl_xor_sync(0xffffffffu, m4[i], 8));
@@ -446,154 +381,112 @@ __global__ void __launch_bounds__(kColThreads, NB <= 4 ? 2 : 1)
     }
     if (rq == 0) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) S.red[warp][ch][i] = m4[i];
+      for (int i = 0; i < 4; ++i) red[warp][ch][i] = m4[i];
     }
     __syncthreads();
     if (tid < 32) {  // pair t = columns 2t, 2t+1 = chunk t/4, word t%4
       uint32_t m = 0;
-      for (int w = 0; w < 8; ++w) m = __vmaxu2(m, S.red[w][tid >> 2][tid & 3]);
-      S.part[parity][tid] = m;
+      for (int w = 0; w < 8; ++w) m = __vmaxu2(m, red[w][tid >> 2][tid & 3]);
+      const int64_t col = u.c0 + 2 * tid;
+      uint32_t* sc = p.scratch + u.g * p.C + col;
+      if (col < p.C && (m & 0xFFFFu)) red_max_relaxed(sc, m & 0xFFFFu);
+      if (col + 1 < p.C && (m >> 16)) red_max_relaxed(sc + 1, m >> 16);
     }
-    cluster.sync();
-    if (tid < 32) {
-      uint32_t m = 0;
-      for (int i = 0; i < u.k; ++i)
-        m = __vmaxu2(m, cluster.map_shared_rank(&S.part[parity][0], u.sub * u.k + i)[tid]);
-      constexpr float FMAX = FmtMax<FMT>::v;
-      const Scale s0 = make_scale(bf16_bits_to_float(m & 0xFFFFu), FMAX);
-      const Scale s1 = make_scale(bf16_bits_to_float(m >> 16), FMAX);
-      S.s32[2 * tid] = s0.s32;
-      S.s32[2 * tid + 1] = s1.s32;
-      if (on && u.member == 0) {  // an empty segment gets the scales of an all-zero group
-        const int64_t col = c0 + 2 * tid;
-        if (col < p.C) p.inv[u.g * p.C + col] = s0.inv32;
-        if (col + 1 < p.C) p.inv[u.g * p.C + col + 1] = s1.inv32;
-      }
-    }
-    if (tid == 0) bulk_wait_read_all();  // the previous unit's stores have read the tile
     __syncthreads();
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256) colscale_kernel(uint32_t* __restrict__ scratch, float* __restrict__ inv,
+                                                       int64_t n) {
+  const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (i >= n) return;
+  const Scale s = make_scale(bf16_bits_to_float(scratch[i]), FmtMax<FMT>::v);
+  reinterpret_cast<float*>(scratch)[i] = s.s32;
+  inv[i] = s.inv32;
+}
+
+// Column j (0..7) of a 16-byte vector of 8 bf16, as fp32.
+FP8_DEVI float col_of(const uint4& v, int j) {
+  const uint32_t w = j < 2 ? v.x : (j < 4 ? v.y : (j < 6 ? v.z : v.w));
+  return (j & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kColThreads) colcast_kernel(const __grid_constant__ CUtensorMap tm_out,
+                                                              const ColParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* T = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  int32_t* upre = reinterpret_cast<int32_t*>(T + kColNB * 8192);
+  int32_t* ppre = upre + (p.n_groups + 1);
+  const int64_t total = col_setup(p, upre, ppre);
+  if (total < 0) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ch = lane & 7, rq = lane >> 3;
+  if (tid == 0) tma_prefetch_desc(&tm_out);
+  const float* scales = reinterpret_cast<const float*>(p.scratch);
+  for (int64_t unit = blockIdx.x; unit < total; unit += gridDim.x) {
+    const ColUnit u = col_unit(p, unit, upre, ppre);
+    uint4 v[kColNB][4];
+    col_load(p, u, warp, ch, rq, v);
     float sc[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sc[j] = S.s32[ch * 8 + j];
-
-    // ---- pass 2: cast from registers into the transposed tile, store column-major ----
-    for (int r = 0; r < u.rounds; ++r) {
-      int64_t rel0, valid;
-      if (u.rounds > 1) {
-        load_round(r, &rel0, &valid);
-      } else {
-        rel0 = (int64_t)u.member * u.chunk;
-      }
-      int64_t wrows = u.write_end - rel0;
-      wrows = wrows < 0 ? 0 : (wrows < u.chunk ? wrows : u.chunk);
-      const int nbox = (int)ceil_div64(wrows, 128);
-      if (on && nbox > 0) {
+    for (int j = 0; j < 8; ++j) {
+      const int64_t col = u.c0 + ch * 8 + j;
+      sc[j] = col < p.C ? scales[u.g * p.C + col] : 0.0f;
+    }
+    int64_t wrows = u.write_end - u.rt;
+    wrows = wrows < 0 ? 0 : (wrows < kColTile ? wrows : kColTile);
+    const int nbox = (int)ceil_div64(wrows, 128);
+    if (tid == 0) bulk_wait_read_all();  // the previous unit's stores have read the tile
+    __syncthreads();
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          if (b < nbox) {
-            uint32_t o[8];
+    for (int b = 0; b < kColNB; ++b) {
+      if (b < nbox) {
+        uint32_t o[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float s = sc[j];
-              o[j] = cvt_fp8x2<FMT>(__fmul_rn(col_of(v[b][0], j), s), __fmul_rn(col_of(v[b][1], j), s)) |
-                     (cvt_fp8x2<FMT>(__fmul_rn(col_of(v[b][2], j), s), __fmul_rn(col_of(v[b][3], j), s)) << 16);
-            }
-            // rotate by ch so that the lanes of a warp write 8 different column residues at once
+        for (int j = 0; j < 8; ++j) {
+          const float s = sc[j];
+          o[j] = cvt_fp8x2<FMT>(__fmul_rn(col_of(v[b][0], j), s), __fmul_rn(col_of(v[b][1], j), s)) |
+                 (cvt_fp8x2<FMT>(__fmul_rn(col_of(v[b][2], j), s), __fmul_rn(col_of(v[b][3], j), s)) << 16);
+        }
+        // rotate by ch so that the lanes of a warp write 8 different column residues at once
 #pragma unroll
-            for (int sh = 1; sh < 8; sh <<= 1) {
-              const bool rot = (ch & sh) != 0;
-              uint32_t t[8];
+        for (int sh = 1; sh < 8; sh <<= 1) {
+          const bool rot = (ch & sh) != 0;
+          uint32_t t[8];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) t[j] = rot ? o[(j + sh) & 7] : o[j];
+          for (int j = 0; j < 8; ++j) t[j] = rot ? o[(j + sh) & 7] : o[j];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) o[j] = t[j];
-            }
-            uint8_t* box = T + b * 8192;
+          for (int j = 0; j < 8; ++j) o[j] = t[j];
+        }
+        uint8_t* box = T + b * 8192;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int cl = ch * 8 + ((j + ch) & 7);
-              *reinterpret_cast<uint32_t*>(box + cl * 128 + (((warp ^ cl) & 7) << 4) + rq * 4) = o[j];
-            }
-          }
+        for (int j = 0; j < 8; ++j) {
+          const int cl = ch * 8 + ((j + ch) & 7);
+          *reinterpret_cast<uint32_t*>(box + cl * 128 + (((warp ^ cl) & 7) << 4) + rq * 4) = o[j];
         }
       }
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0 && on && nbox > 0) {
-        for (int b = 0; b < nbox; ++b) {
-          const int32_t xo = (int32_t)(u.pstart + rel0 + 128 * b);
-          if (p.mode == 1)
-            tma_store_3d(&tm_out, T + b * 8192, xo, (int32_t)c0, (int32_t)u.g);
-          else
-            tma_store_2d(&tm_out, T + b * 8192, xo, (int32_t)c0);
-        }
-        bulk_commit();
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      for (int b = 0; b < nbox; ++b) {
+        const int32_t xo = (int32_t)(u.pstart + u.rt + 128 * b);
+        if (p.mode == 1)
+          tma_store_3d(&tm_out, T + b * 8192, xo, (int32_t)u.c0, (int32_t)u.g);
+        else
+          tma_store_2d(&tm_out, T + b * 8192, xo, (int32_t)u.c0);
       }
-      if (u.rounds > 1) {
-        if (tid == 0) bulk_wait_read_all();
-        __syncthreads();
-      }
+      bulk_commit();
     }
   }
   if (tid == 0) bulk_wait_all();
-  cluster.sync();  // peers may still read this CTA's partial maxima
-}
-
-template <int FMT, int NB>
-static int run_cols(const ColParams& p0, const CUtensorMap& tout, const Ctx& c) {
-  auto kern = quant_cols_kernel<FMT, NB>;
-  ColParams p = p0;
-  const size_t ctrl = kColCtrlBytes + (p.mode == 2 ? 8 * (size_t)(p.n_groups + 1) : 0);
-  const size_t smem = 1024 + (size_t)128 * NB * 64 + ctrl;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 128 * 8 * 64 + 65536) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return FP8_ERR_CUDA;
-    attr_done = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kColThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = c.stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int slots = 0;
-  for (int cs : {16, 8}) {
-    attr[0].val.clusterDim.x = cs;
-    cfg.gridDim = dim3(cs);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
-      p.cs = cs;
-      slots = n;
-      break;
-    }
-    cudaGetLastError();
-  }
-  if (slots == 0) return FP8_ERR_CUDA;
-  int64_t units;
-  if (p.mode == 2) {
-    units = p.n_groups * p.n_strips;  // upper bound; the kernel computes the exact count
-  } else {
-    int k = 1;
-    while (k * 128 * NB < p.group_rows && k < p.cs) k <<= 1;
-    p.dense_k = k;
-    units = p.n_groups * ((p.n_strips + p.cs / k - 1) / (p.cs / k));
-  }
-  const int64_t clusters = units < slots ? units : slots;
-  attr[0].val.clusterDim.x = p.cs;
-  cfg.gridDim = dim3((unsigned)(clusters * p.cs));
-  if (cudaLaunchKernelEx(&cfg, kern, tout, p) != cudaSuccess) return FP8_ERR_CUDA;
-  return FP8_OK;
 }
 
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
-                      const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, const Ctx& c) {
+                      const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, uint32_t* scratch,
+                      const Ctx& c) {
   if (n_groups == 0 || C == 0) return FP8_OK;
   if (ends && n_groups > 6000) return FP8_ERR_UNSUPPORTED;  // prefix arrays live in shared memory
   ColParams p = {};
@@ -603,12 +496,11 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   p.n_groups = n_groups;
   p.group_rows = group_rows;
   p.ends = ends;
+  p.scratch = scratch;
   p.inv = inv;
   p.status = c.status;
   p.n_strips = ceil_div64(C, 64);
   p.mode = ends ? 2 : (n_groups > 1 ? 1 : 0);
-  p.cs = 16;
-  p.dense_k = 1;
 
   CUtensorMap tout;
   int rc;
@@ -625,12 +517,35 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
     rc = make_tmap(&tout, out_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (rc != FP8_OK) return rc;
-  // 4 blocks of 128 rows per CTA (two CTAs per SM) unless a dense group needs more than
-  // 16 x 512 rows, then 8 blocks (one CTA per SM).
-  const bool big = p.mode != 2 && group_rows > 16 * 512;
+
+  const int64_t n_scales = n_groups * C;
+  if (cudaMemsetAsync(scratch, 0, (size_t)n_scales * 4, c.stream) != cudaSuccess) return FP8_ERR_CUDA;
+  // units: exact for dense modes; for segments an upper bound (each segment adds at most one
+  // partial tile) -- the kernels compute the exact count from the offsets
+  const int64_t units = p.mode == 2 ? (ceil_div64(rows_total, kColTile) + n_groups) * p.n_strips
+                                    : n_groups * ceil_div64(group_rows, kColTile) * p.n_strips;
+  const size_t pre_bytes = p.mode == 2 ? 8 * (size_t)(n_groups + 1) : 0;
+  if (units > 0) {
+    const int64_t cap_a = (int64_t)c.sm_count * 3;
+    colmax_kernel<<<(unsigned)(units < cap_a ? units : cap_a), kColThreads, pre_bytes, c.stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
+  }
+  const unsigned gs = (unsigned)ceil_div64(n_scales, 256);
   if (fmt == FP8_DT_E4M3)
-    return big ? run_cols<FP8_DT_E4M3, 8>(p, tout, c) : run_cols<FP8_DT_E4M3, 4>(p, tout, c);
-  return big ? run_cols<FP8_DT_E5M2, 8>(p, tout, c) : run_cols<FP8_DT_E5M2, 4>(p, tout, c);
+    colscale_kernel<FP8_DT_E4M3><<<gs, 256, 0, c.stream>>>(scratch, inv, n_scales);
+  else
+    colscale_kernel<FP8_DT_E5M2><<<gs, 256, 0, c.stream>>>(scratch, inv, n_scales);
+  if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
+  if (units > 0) {
+    auto kern = fmt == FP8_DT_E4M3 ? colcast_kernel<FP8_DT_E4M3> : colcast_kernel<FP8_DT_E5M2>;
+    const size_t smem = 1024 + kColNB * 8192 + pre_bytes;
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return FP8_ERR_CUDA;
+    const int64_t cap_b = (int64_t)c.sm_count * 3;
+    kern<<<(unsigned)(units < cap_b ? units : cap_b), kColThreads, smem, c.stream>>>(tout, p);
+    if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
+  }
+  return FP8_OK;
 }
 
 }  // namespace fp8lin

@@ -35,6 +35,7 @@ def test_host_helpers(fp8):
         assert P % 16 == 0 and P >= R + 127 * E
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_TENSOR) == 4
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_ROW) == 0
+    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 16, 5120, granularity=fp8.GRAN_COL) == 16 * 5120 * 4
     M, K, N = 256, 512, 128
     ws_row_bf16 = fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_ROW, fp8.WGRAD_BF16)
     ws_row_fp8 = fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_ROW, fp8.WGRAD_FP8)

@@ -138,7 +138,7 @@ def test_jagged_colwise(fp8, counts, fi):
     inv = torch.empty((len(counts), C), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     fp8.fp8_quantize(x.cuda(), fp8.GRAN_COL, dt, fp8.LAYOUT_COL_MAJOR, None, canary, inv,
-                     torch.from_numpy(ends).cuda(), status=st)
+                     torch.from_numpy(ends).cuda(), fp8.col_workspace(len(counts), C, "cuda"), status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     q_ref, inv_ref = oracle.quantize_jagged_cols(bits(x), ends, ofmt)
@@ -157,7 +157,7 @@ def test_jagged_bad_offsets_sets_status(fp8):
     for bad in ([10, 5, 64], [10, 20, 63]):
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         fp8.fp8_quantize(x, fp8.GRAN_COL, fp8.DT_E4M3, fp8.LAYOUT_COL_MAJOR, None, out, inv,
-                         torch.tensor(bad, dtype=torch.int32, device="cuda"), status=st)
+                         torch.tensor(bad, dtype=torch.int32, device="cuda"), fp8.col_workspace(3, 8, "cuda"), status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == fp8.DEV_BAD_OFFSETS
 
@@ -174,6 +174,10 @@ def test_argument_errors(fp8):
         fp8.fp8_quantize(x, fp8.GRAN_ROW, fp8.DT_E4M3, fp8.LAYOUT_ROW_MAJOR,
                          torch.zeros((16, 16), dtype=torch.float8_e4m3fn, device="cuda"), None, inv[:3])
     assert e.value.code == 1
+    with pytest.raises(fp8.Fp8Error) as e:  # column granularity without its per-column workspace
+        fp8.fp8_quantize(x, fp8.GRAN_COL, fp8.DT_E4M3, fp8.LAYOUT_COL_MAJOR, None,
+                         torch.zeros((16, 16), dtype=torch.float8_e4m3fn, device="cuda"), inv)
+    assert e.value.code == 4
     with pytest.raises(fp8.Fp8Error) as e:  # tensor granularity without workspace
         fp8.fp8_quantize(x, fp8.GRAN_TENSOR, fp8.DT_E4M3, fp8.LAYOUT_ROW_MAJOR,
                          torch.zeros((16, 16), dtype=torch.float8_e4m3fn, device="cuda"), None, inv[:1])
