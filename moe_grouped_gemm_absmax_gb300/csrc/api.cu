@@ -2,14 +2,48 @@
 // composition of the Linear forward / backward passes from the quantize and GEMM launchers.
 #include <cudaTypedefs.h>
 
+#include <string.h>
+
 #include <atomic>
 #include <mutex>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace fp8lin {
 
 static std::atomic<uint64_t> g_wait_ns{4000000000ull};
+
+// Table of the scale step (see ScaleTab): for the 128 bf16 mantissas m in [1, 2), the fp64
+// quotient fp8_max / m and its fp64 reciprocal, each rounded to fp32; the eps entry for amax
+// below eps; eps_below = the smallest bf16 pattern whose value is >= eps.
+static ScaleTab build_tab(double fp8_max) {
+  ScaleTab t;
+  for (int m7 = 0; m7 < 128; ++m7) {
+    const double m = 1.0 + m7 / 128.0;
+    const double s = fp8_max / m;
+    t.s[m7] = (float)s;
+    t.inv[m7] = (float)(1.0 / s);
+  }
+  const double se = fp8_max / kEps;
+  t.eps_s = (float)se;
+  t.eps_inv = (float)(1.0 / se);
+  uint32_t b = 0;
+  while (b < 0x7F80u) {
+    uint32_t u = b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    if ((double)f >= kEps) break;
+    ++b;
+  }
+  t.eps_below = b;
+  return t;
+}
+
+const ScaleTab& scale_tab(int fmt) {
+  static const ScaleTab e4 = build_tab(kE4M3Max), e5 = build_tab(kE5M2Max);
+  return fmt == FP8_DT_E4M3 ? e4 : e5;
+}
 static std::atomic<int> g_test_stall{0};
 
 int make_ctx(Ctx* ctx, void* stream, int32_t* status) {

@@ -17,7 +17,7 @@ namespace fp8lin {
 // Formats: largest finite magnitude (e4m3fn 1.75 * 2^8, e5m2 1.75 * 2^15).
 constexpr float kE4M3Max = 448.0f;
 constexpr float kE5M2Max = 57344.0f;
-// Lower clamp of amax before the fp64 division.
+// Lower clamp of amax in the scale step.
 constexpr double kEps = 1e-12;
 
 FP8_DEVI uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -37,18 +37,58 @@ FP8_DEVI void set_status(int32_t* st, int32_t bits) {
 // Scale step: scale64 = fp8_max / max(amax, eps) with an IEEE fp64 division; the fp32 multiply
 // uses scale64 rounded to fp32; the inverse handed to the GEMM is the correctly rounded fp64
 // reciprocal of scale64, rounded to fp32.
+//
+// The kernels take this step by table, with no fp64 arithmetic on the device (GB300's fp64 rate
+// is a small fraction of its fp32 rate, and the row-wise kernel would take the step once per
+// row). amax is a bf16 value m * 2^E with m one of 128 mantissas in [1, 2). Scaling by a power
+// of two commutes with round-to-nearest while the results stay normal, so
+//   RN64(fp8_max / amax)   = RN64(fp8_max / m) * 2^-E
+//   RN64(1 / scale64)      = RN64(1 / RN64(fp8_max / m)) * 2^E
+// and the same holds after rounding each to fp32. ScaleTab keeps, per m, the two fp32 factors,
+// computed on the host in IEEE fp64; the kernel applies 2^-E / 2^E exactly on the fp32 exponent
+// field. For every amax >= eps (and <= the largest bf16) both fp32 results are normal
+// (e5m2: scale <= 57344 / 1e-12 ~ 5.7e16; e4m3: scale >= 448 / 3.4e38 ~ 1.3e-36), so the table
+// reproduces the fp64 step bit for bit. amax below eps takes the eps entry; amax = +Inf gives
+// scale 0 and inverse +Inf, a NaN amax NaN for both, as the fp64 step would.
 struct Scale {
   float s32;
   float inv32;
 };
-FP8_DEVI Scale make_scale(float amax, float fp8_max) {
-  double a = static_cast<double>(amax);
-  a = a < kEps ? kEps : a;
-  double s = __ddiv_rn(static_cast<double>(fp8_max), a);
+struct ScaleTab {
+  float s[128];     // RN32(RN64(fp8_max / m)), m = 1 + i / 128
+  float inv[128];   // RN32(RN64(1 / RN64(fp8_max / m)))
+  uint32_t eps_below;  // bf16 patterns below this one encode values < eps
+  float eps_s, eps_inv;
+};
+FP8_DEVI Scale tab_scale(const ScaleTab& t, uint32_t amax_bits) {
   Scale r;
-  r.s32 = __double2float_rn(s);
-  r.inv32 = __double2float_rn(__drcp_rn(s));
+  if (amax_bits < t.eps_below) {
+    r.s32 = t.eps_s;
+    r.inv32 = t.eps_inv;
+  } else if (amax_bits < 0x7F80u) {
+    const int e = (int)(amax_bits >> 7) - 127;
+    const uint32_t m7 = amax_bits & 0x7Fu;
+    r.s32 = __int_as_float(__float_as_int(t.s[m7]) - (e << 23));
+    r.inv32 = __int_as_float(__float_as_int(t.inv[m7]) + (e << 23));
+  } else if (amax_bits == 0x7F80u) {
+    r.s32 = 0.0f;
+    r.inv32 = __int_as_float(0x7F800000);
+  } else {
+    r.s32 = __int_as_float(0x7FC00000);
+    r.inv32 = r.s32;
+  }
   return r;
+}
+
+// Two IEEE fp32 products in one instruction (mul.rn.f32x2): bit-identical to two __fmul_rn.
+FP8_DEVI float2 fmul2_rn(float2 a, float2 b) {
+  uint64_t ra, rb, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
 }
 
 // bf16 bit pattern -> fp32 (exact).
@@ -319,6 +359,17 @@ FP8_DEVI void tmem_ld32(uint32_t taddr, uint32_t* r) {
                : "r"(taddr));
 }
 FP8_DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The same wait, naming the 32 registers of the load it completes as in/out operands: the
+// compiler may not read, move or reuse them between the asynchronous load and this wait.
+FP8_DEVI void tmem_ld_wait_regs(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                 "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
 
 // Named barriers (ids > 0) for a subset of warps; bar_and also reduces a predicate (all true).
 FP8_DEVI void named_bar_sync(uint32_t id, uint32_t nthreads) {

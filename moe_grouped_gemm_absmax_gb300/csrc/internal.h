@@ -19,6 +19,10 @@ struct Ctx {
   int test_stall;    // failure-detection test hook (see fp8_set_test_stall)
 };
 
+struct ScaleTab;
+// The scale table of a format (FP8_DT_E4M3 / FP8_DT_E5M2), built once on the host in fp64.
+const ScaleTab& scale_tab(int fmt);
+
 // Fills ctx for the current device; returns FP8_OK or FP8_ERR_DEVICE.
 int make_ctx(Ctx* ctx, void* stream, int32_t* status);
 

@@ -35,7 +35,7 @@ constexpr int kRowVPT = 8;
 template <int FMT, int TPR>
 __global__ void __launch_bounds__(TPR > 256 ? TPR : 256)
     quant_rows_kernel(const uint4* __restrict__ x, int64_t R, int nvec, uint2* __restrict__ q,
-                      float* __restrict__ inv) {
+                      float* __restrict__ inv, const __grid_constant__ ScaleTab tab) {
   constexpr int CTA = TPR > 256 ? TPR : 256;
   constexpr int TEAMS = CTA / TPR;
   constexpr int WPT = TPR / 32;
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(TPR > 256 ? TPR : 256)
     if (t == 0) {
       uint32_t mm = 0;
       for (int w = 0; w < WPT; ++w) mm = max(mm, red[team * WPT + w]);
-      const Scale s = make_scale(bf16_bits_to_float(mm), FMAX);
+      const Scale s = tab_scale(tab, mm);
       sc[team] = s.s32;
       if (active) inv[r] = s.inv32;
     }
@@ -91,7 +91,7 @@ static int run_rows(const void* x, int64_t R, int nvec, void* q, float* inv, con
   const int64_t cap = (int64_t)c.sm_count * (2048 / CTA);
   const int grid = (int)(need < cap ? need : cap);
   quant_rows_kernel<FMT, TPR><<<grid, CTA, 0, c.stream>>>(static_cast<const uint4*>(x), R, nvec,
-                                                           static_cast<uint2*>(q), inv);
+                                                           static_cast<uint2*>(q), inv, scale_tab(FMT));
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -151,12 +151,13 @@ template <int FMT>
 __global__ void __launch_bounds__(256) quant_tensor_cast_kernel(const uint16_t* __restrict__ x, int64_t R,
                                                                 int64_t C, const uint32_t* __restrict__ amax_ws,
                                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
-                                                                float* __restrict__ inv) {
+                                                                float* __restrict__ inv,
+                                                                const __grid_constant__ ScaleTab tab) {
   constexpr float FMAX = FmtMax<FMT>::v;
   __shared__ float s_sc;
   __shared__ __align__(16) uint8_t T[kTcCols * kTcPitch];
   if (threadIdx.x == 0) {
-    const Scale s = make_scale(bf16_bits_to_float(*amax_ws), FMAX);
+    const Scale s = tab_scale(tab, *amax_ws);
     s_sc = s.s32;
     if (blockIdx.x == 0 && blockIdx.y == 0) *inv = s.inv32;
   }
@@ -207,10 +208,12 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
   if (grid.x == 0 || grid.y == 0) grid = dim3(1, 1);
   if (fmt == FP8_DT_E4M3)
     quant_tensor_cast_kernel<FP8_DT_E4M3><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_ws, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv);
+        static_cast<const uint16_t*>(x), R, C, amax_ws, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
+        scale_tab(fmt));
   else
     quant_tensor_cast_kernel<FP8_DT_E5M2><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_ws, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv);
+        static_cast<const uint16_t*>(x), R, C, amax_ws, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
+        scale_tab(fmt));
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -398,10 +401,10 @@ __global__ void __launch_bounds__(kColThreads) colmax_kernel(const ColParams p) 
 
 template <int FMT>
 __global__ void __launch_bounds__(256) colscale_kernel(uint32_t* __restrict__ scratch, float* __restrict__ inv,
-                                                       int64_t n) {
+                                                       int64_t n, const __grid_constant__ ScaleTab tab) {
   const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
   if (i >= n) return;
-  const Scale s = make_scale(bf16_bits_to_float(scratch[i]), FmtMax<FMT>::v);
+  const Scale s = tab_scale(tab, scratch[i]);
   reinterpret_cast<float*>(scratch)[i] = s.s32;
   inv[i] = s.inv32;
 }
@@ -532,9 +535,9 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   }
   const unsigned gs = (unsigned)ceil_div64(n_scales, 256);
   if (fmt == FP8_DT_E4M3)
-    colscale_kernel<FP8_DT_E4M3><<<gs, 256, 0, c.stream>>>(scratch, inv, n_scales);
+    colscale_kernel<FP8_DT_E4M3><<<gs, 256, 0, c.stream>>>(scratch, inv, n_scales, scale_tab(FP8_DT_E4M3));
   else
-    colscale_kernel<FP8_DT_E5M2><<<gs, 256, 0, c.stream>>>(scratch, inv, n_scales);
+    colscale_kernel<FP8_DT_E5M2><<<gs, 256, 0, c.stream>>>(scratch, inv, n_scales, scale_tab(FP8_DT_E5M2));
   if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
   if (units > 0) {
     auto kern = fmt == FP8_DT_E4M3 ? colcast_kernel<FP8_DT_E4M3> : colcast_kernel<FP8_DT_E5M2>;
@@ -558,10 +561,12 @@ int launch_quant_tensor_cast(const void* x, int64_t R, int64_t C, int fmt, void*
   if (grid.x == 0 || grid.y == 0) grid = dim3(1, 1);
   if (fmt == FP8_DT_E4M3)
     quant_tensor_cast_kernel<FP8_DT_E4M3><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_word, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv);
+        static_cast<const uint16_t*>(x), R, C, amax_word, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
+        scale_tab(fmt));
   else
     quant_tensor_cast_kernel<FP8_DT_E5M2><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_word, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv);
+        static_cast<const uint16_t*>(x), R, C, amax_word, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
+        scale_tab(fmt));
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

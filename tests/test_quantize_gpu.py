@@ -54,6 +54,38 @@ def test_rowwise_3d_and_empty(fp8):
     assert q0.numel() == 0
 
 
+def _every_amax(rows_per_pattern_cols: int):
+    """One row per non-negative finite bf16 pattern p (0x0000 .. 0x7F7F): p itself, its negation,
+    then values |v| <= p (p with lower mantissa bits cleared, and zeros), so that the row's amax
+    is exactly p and every scale the format can take is hit once."""
+    p = np.arange(0x7F80, dtype=np.uint16)
+    x = np.zeros((p.size, rows_per_pattern_cols), np.uint16)
+    x[:, 0] = p
+    x[:, 1] = p | 0x8000
+    x[:, 2] = p & 0xFFF0
+    x[:, 3] = (p & 0xFF80) | 0x8000
+    return x
+
+
+@pytest.mark.parametrize("fi", [0, 1])
+def test_scale_every_bf16_amax(fp8, fi):
+    """Exhaustive check of the scale step: the row scales (and, transposed, the column scales)
+    for every finite non-negative bf16 amax, below eps, subnormal, up to the largest bf16,
+    bit-identical with the oracle's fp64 division."""
+    ofmt, dt, _ = FMTS[fi]
+    xb = _every_amax(16)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16)
+    q, _, inv = fp8.quantize_alloc(x.cuda(), fp8.GRAN_ROW, dt)
+    q_ref, inv_ref = oracle.quantize_rows(xb, ofmt)
+    assert np.array_equal(f32_bits(inv), inv_ref.view(np.uint32))
+    assert np.array_equal(codes(q), q_ref)
+    xt = x.T.contiguous()  # [16, 32640]: one pattern per column
+    _, qt, invc = fp8.quantize_alloc(xt.cuda(), fp8.GRAN_COL, dt)
+    qc_ref, invc_ref = oracle.quantize_cols(np.ascontiguousarray(xb.T), ofmt)
+    assert np.array_equal(f32_bits(invc), invc_ref.view(np.uint32))
+    assert np.array_equal(codes(qt), qc_ref.T)
+
+
 @pytest.mark.parametrize("R,C", [(16, 8), (256, 512), (130 * 16, 200), (1024, 1000)])
 @pytest.mark.parametrize("fi", [0, 1])
 def test_tensorwise_dual_output(fp8, R, C, fi):
