@@ -116,43 +116,57 @@ FP8_DEVI int find_expert(const int32_t* tpre, int E, int64_t t) {
   return lo;
 }
 
+// Tile t of the persistent schedule. Tile indices, tile counts and block coordinates fit in 32
+// bits (the launcher checks), so the divisions here are 32-bit: they sit on the MMA issuer's and
+// the epilogue's per-tile path.
 template <int SCHED, int TILE_M>
-FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t, const int32_t* tpre, const int32_t* aux) {
+FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, const int32_t* aux) {
   Tile T;
+  const uint32_t t = (uint32_t)t64, num_n = (uint32_t)p.num_n;
   if (SCHED == kDense) {
-    const int64_t per_group = (int64_t)kGroupM * p.num_n;
-    const int64_t g = t / per_group, r = t % per_group;
-    const int64_t first_m = g * kGroupM;
-    const int64_t gsz = p.num_m - first_m < kGroupM ? p.num_m - first_m : kGroupM;
-    const int64_t mb = first_m + r % gsz, nb = r / gsz;
-    T.m0 = mb * TILE_M;
-    T.n0 = nb * BN;
+    const uint32_t per_group = (uint32_t)kGroupM * num_n;
+    const uint32_t g = t / per_group, r = t - g * per_group;
+    const uint32_t first_m = g * kGroupM;
+    const uint32_t left = (uint32_t)p.num_m - first_m;
+    const uint32_t gsz = left < (uint32_t)kGroupM ? left : (uint32_t)kGroupM;
+    const uint32_t nb = r / gsz, mb = first_m + (r - nb * gsz);
+    T.m0 = (int64_t)mb * TILE_M;
+    T.n0 = (int64_t)nb * BN;
     T.row_end = p.M;
     T.k0 = 0;
     T.nkb = p.nkb;
     T.e = 0;
   } else if (SCHED == kJagM) {
-    const int e = find_expert(tpre, p.E, t);
-    const int64_t local = t - tpre[e];
-    const int64_t mb = local / p.num_n, nb = local % p.num_n;
-    T.m0 = aux[e] + mb * TILE_M;  // aux[e] = segment start row
-    T.n0 = nb * BN;
+    const int e = find_expert(tpre, p.E, t64);
+    const uint32_t local = t - (uint32_t)tpre[e];
+    const uint32_t mb = local / num_n, nb = local - mb * num_n;
+    T.m0 = aux[e] + (int64_t)mb * TILE_M;  // aux[e] = segment start row
+    T.n0 = (int64_t)nb * BN;
     T.row_end = aux[e + 1];
     T.k0 = 0;
     T.nkb = p.nkb;
     T.e = e;
   } else {
-    const int64_t per = p.num_m * p.num_n;
-    const int e = (int)(t / per);
-    const int64_t local = t % per;
-    T.m0 = (local / p.num_n) * TILE_M;
-    T.n0 = (local % p.num_n) * BN;
+    const uint32_t per = (uint32_t)p.num_m * num_n;
+    const uint32_t e = t / per;
+    const uint32_t local = t - e * per;
+    const uint32_t mb = local / num_n, nb = local - mb * num_n;
+    T.m0 = (int64_t)mb * TILE_M;
+    T.n0 = (int64_t)nb * BN;
     T.row_end = p.M;
     T.k0 = aux[e];                             // aux[e] = padded start of segment e
     T.nkb = (aux[e + 1] - aux[e]) / BKB;       // padded length / 128
-    T.e = e;
+    T.e = (int)e;
   }
   return T;
+}
+
+// K blocks of tile t (all the MMA issuer needs to know about a tile).
+template <int SCHED>
+FP8_DEVI int64_t tile_nkb(const GemmParams& p, int64_t t, const int32_t* aux) {
+  if (SCHED != kJagK) return p.nkb;
+  const uint32_t e = (uint32_t)t / ((uint32_t)p.num_m * (uint32_t)p.num_n);
+  return (aux[e + 1] - aux[e]) / BKB;
 }
 
 template <int KIND, int SCHED, int A_MN, int B_MN, int CG>
@@ -374,15 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
       }
       for (int64_t t = unit; t < total && ok; t += n_units) {
-        const Tile T = get_tile<SCHED, C::TILE_M>(p, t, tpre, aux);
-        if (T.nkb == 0) continue;
+        const int64_t nkb = tile_nkb<SCHED>(p, t, aux);
+        if (nkb == 0) continue;
         if (!mbar_wait(&S.tempty[buf], aphase ^ 1, abort_flag, p.wait_ns)) {
           if (!*abort_flag) fail();
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-        for (int64_t kb = 0; kb < T.nkb; ++kb) {
+        for (int64_t kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&S.full[stage], phase, abort_flag, p.wait_ns)) {
             if (!*abort_flag) fail();
             ok = false;
@@ -446,16 +460,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     int buf = 0, sbi = 0;
     uint32_t oseq = 0;  // TMA stores issued by this warp
     uint32_t aphase = 0;
+    // The next tile and the scales it needs (this thread's row scale; its column scale, or the
+    // scalar one) are fetched one tile ahead, so the memory latency hides behind this tile.
+    Tile Tn;
+    float sa_nx = 1.0f, sb_nx = 1.0f;
+    auto fetch = [&](int64_t tt) {
+      Tn = get_tile<SCHED, C::TILE_M>(p, tt, tpre, aux);
+      if (KIND != kFP8) return;
+      const int64_t m = Tn.m0 + row;
+      const float* sbp = p.sB;
+      if (SCHED != kDense) sbp += (int64_t)Tn.e * p.N;
+      sa_nx = 1.0f;
+      if (m < Tn.row_end) {
+        if (SCHED == kJagK)
+          sa_nx = __ldg(p.sA + (int64_t)Tn.e * p.M + m);
+        else
+          sa_nx = p.sa_scalar ? __ldg(p.sA) : __ldg(p.sA + m);
+      }
+      if (stage_sb) {
+        const int64_t n = Tn.n0 + etid;
+        sb_nx = n < p.N ? __ldg(sbp + n) : 0.0f;
+      } else {
+        sb_nx = __ldg(sbp);
+      }
+    };
+    if (unit < total) fetch(unit);
     for (int64_t t = unit; t < total; t += n_units) {
-      const Tile T = get_tile<SCHED, C::TILE_M>(p, t, tpre, aux);
+      const Tile T = Tn;
+      const float sa = sa_nx, sb_mine = sb_nx;
+      if (t + n_units < total) fetch(t + n_units);
       const int64_t m = T.m0 + row;
       const bool row_ok = m < T.row_end;
       const int64_t orow = SCHED == kJagK ? (int64_t)T.e * p.M + m : m;
-      const float* sbp = p.sB;
-      if (KIND == kFP8 && SCHED != kDense) sbp += (int64_t)T.e * p.N;
       if (stage_sb) {  // one column scale per epilogue thread; reused by all 128 rows
-        const int64_t n = T.n0 + etid;
-        S.sb[sbi][etid] = n < p.N ? __ldg(sbp + n) : 0.0f;
+        S.sb[sbi][etid] = sb_mine;
         named_bar_sync(1, kEpiThreads);
       }
       const float* sbs = S.sb[sbi];
@@ -477,54 +515,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      float sa = 1.0f;
-      if (KIND == kFP8 && row_ok) {
-        if (SCHED == kJagK)
-          sa = __ldg(p.sA + (int64_t)T.e * p.M + m);
-        else
-          sa = p.sa_scalar ? __ldg(p.sA) : __ldg(p.sA + m);
-      }
-      const float sb_all = (KIND == kFP8 && p.sb_scalar) ? __ldg(sbp) : 1.0f;
+      const float sb_all = (KIND == kFP8 && p.sb_scalar) ? sb_mine : 1.0f;
       const uint32_t taddr = tmem_base + (uint32_t)(buf * BN + c0) + ((uint32_t)(q * 32) << 16);
-      // Pairs write through shared memory with TMA bulk-tensor stores (32 rows x 32 columns per
-      // store), unless this warp's 32 rows run past the end of an expert's segment.
+      // Pairs write through shared memory with TMA bulk-tensor stores of 32 rows x 128 bytes
+      // (64 bf16 columns, or 32 fp32), unless this warp's 32 rows run past the end of an
+      // expert's segment.
       const int64_t wrow0 = T.m0 + (int64_t)rank * BM + q * 32;
       const bool via_tma = CG == 2 && p.tma_out && (SCHED != kJagM || wrow0 + 32 <= T.row_end);
-#pragma unroll 1
+      uint8_t* st = out_stage + (warp - 2) * kStageOut;
+      // Two register sets: the load of the next 32 columns is in flight while the current ones
+      // are scaled and stored (tcgen05.wait::ld names the set it completes, so the compiler
+      // keeps that set in place until then).
+      uint32_t va[32], vb[32];
+      uint32_t w[32];  // bf16 pairs of two consecutive 32-column chunks (one 128-byte row)
+      tmem_ld32(taddr, va);
+#pragma unroll
       for (int ch = 0; ch < BN / 64; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(taddr + ch * 32, v);
-        tmem_ld_wait();
+        uint32_t* v = (ch & 1) ? vb : va;
+        tmem_ld_wait_regs(v);
+        if (ch + 1 < BN / 64) tmem_ld32(taddr + (ch + 1) * 32, (ch & 1) ? va : vb);
         const int cl = c0 + ch * 32;  // tile column of v[0]
         const int64_t n = T.n0 + cl;
-        if (n >= p.N) continue;  // uniform across the warp
+        // bf16 through TMA: the pair (ch - 1, ch) is stored once ch is done, unless the pair
+        // starts at or past N (uniform across the warp); columns past N are clipped by the copy
+        const bool pair_live = T.n0 + c0 + (ch & ~1) * 32 < p.N;
+        if (n >= p.N && !(via_tma && !p.out_f32 && pair_live)) continue;
         float f[32];
+        const float2 sa2 = make_float2(sa, sa);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float sb = stage_sb ? sbs[cl + j] : sb_all;
-          f[j] = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), sa), sb);
+        for (int j = 0; j < 32; j += 2) {
+          const float2 sb2 = stage_sb ? *reinterpret_cast<const float2*>(sbs + cl + j) : make_float2(sb_all, sb_all);
+          const float2 x = fmul2_rn(fmul2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sa2), sb2);
+          f[j] = x.x;
+          f[j + 1] = x.y;
         }
         if (via_tma) {
-          uint8_t* st = out_stage + (warp - 2) * kStageOut;
           if (!p.out_f32) {
-            st += (oseq & 1) * 2048;
-            if (lane == 0 && oseq >= 2) bulk_wait_read_1();  // this half's previous store has read it
-            __syncwarp();
-            uint32_t w[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
-              w[j] = *reinterpret_cast<const uint32_t*>(&h);
+              w[(ch & 1) * 16 + j] = *reinterpret_cast<const uint32_t*>(&h);
             }
-            // row `lane` of a [32][64 B] box, 64-byte swizzle (16-byte chunk ^ (row / 2) % 4)
+            if ((ch & 1) == 0) continue;
+            if (lane == 0 && oseq >= 1) bulk_wait_read_all();  // the previous store has read the buffer
+            __syncwarp();
+            // row `lane` of a [32][128 B] box, 128-byte swizzle (16-byte chunk ^ row % 8)
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-              *reinterpret_cast<uint4*>(st + lane * 64 + ((c4 ^ ((lane >> 1) & 3)) << 4)) =
-                  make_uint4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+            for (int c8 = 0; c8 < 8; ++c8)
+              *reinterpret_cast<uint4*>(st + lane * 128 + ((c8 ^ (lane & 7)) << 4)) =
+                  make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
           } else {
             if (lane == 0 && oseq >= 1) bulk_wait_read_all();
             __syncwarp();
-            // row `lane` of a [32][128 B] box, 128-byte swizzle (16-byte chunk ^ row % 8)
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8)
               *reinterpret_cast<float4*>(st + lane * 128 + ((c8 ^ (lane & 7)) << 4)) =
@@ -533,10 +575,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
+            const int32_t n_st = (int32_t)(p.out_f32 ? n : n - 32);
             if (SCHED == kJagK)
-              tma_store_3d(&tmO, st, (int32_t)n, (int32_t)wrow0, T.e);
+              tma_store_3d(&tmO, st, n_st, (int32_t)wrow0, T.e);
             else
-              tma_store_2d(&tmO, st, (int32_t)n, (int32_t)wrow0);
+              tma_store_2d(&tmO, st, n_st, (int32_t)wrow0);
             bulk_commit();
           }
           ++oseq;
@@ -554,17 +597,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + n;
-            uint32_t w[16];
+            uint32_t wd[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
-              w[j] = *reinterpret_cast<const uint32_t*>(&h);
+              wd[j] = *reinterpret_cast<const uint32_t*>(&h);
             }
             if (full) {
 #pragma unroll
-              for (int j = 0; j < 16; j += 4) *reinterpret_cast<uint4*>(o + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
+              for (int j = 0; j < 16; j += 4) *reinterpret_cast<uint4*>(o + 2 * j) = make_uint4(wd[j], wd[j + 1], wd[j + 2], wd[j + 3]);
             } else {
-              for (int j = 0; j < 32 && n + j < p.N; ++j) o[j] = (uint16_t)(w[j >> 1] >> (16 * (j & 1)));
+              for (int j = 0; j < 32 && n + j < p.N; ++j) o[j] = (uint16_t)(wd[j >> 1] >> (16 * (j & 1)));
             }
           }
         }
@@ -660,24 +703,30 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   const bool pair = g.mode == FP8_GROUPED_JAGGED_M ? g.M >= 2048 : pair_tiles * 2 >= c.sm_count;
   const int tile_m = pair ? 256 : 128;
   p.num_m = (g.M + tile_m - 1) / tile_m;
-  // output tensor map for the pairs' TMA stores: boxes of 32 rows x 32 columns
+  // the kernels index tiles with 32-bit arithmetic
+  const int64_t max_tiles = g.mode == FP8_GROUPED_JAGGED_K ? g.E * p.num_m * p.num_n
+                            : g.mode == FP8_GROUPED_JAGGED_M ? (p.num_m + g.E) * p.num_n
+                                                             : p.num_m * p.num_n;
+  if (max_tiles >= (int64_t)1 << 31) return FP8_ERR_UNSUPPORTED;
+  // output tensor map for the pairs' TMA stores: boxes of 32 rows x 128 bytes
   CUtensorMap to;
   memset(&to, 0, sizeof(to));
   p.tma_out = 0;
   if (pair && p.vec_ok && (reinterpret_cast<uintptr_t>(g.out) & 15) == 0) {
     const CUtensorMapDataType odt = p.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const CUtensorMapSwizzle osw = p.out_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle osw = CU_TENSOR_MAP_SWIZZLE_128B;
+    const uint32_t bx = p.out_f32 ? 32 : 64;  // 128-byte box rows
     const uint64_t oes = p.out_f32 ? 4 : 2;
     int rc;
     if (g.mode == FP8_GROUPED_JAGGED_K) {
       const uint64_t d[3] = {(uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.E};
       const uint64_t st[2] = {(uint64_t)g.N * oes, (uint64_t)(g.M * g.N) * oes};
-      const uint32_t box[3] = {32, 32, 1};
+      const uint32_t box[3] = {bx, 32, 1};
       rc = make_tmap(&to, g.out, odt, 3, d, st, box, osw);
     } else {
       const uint64_t d[2] = {(uint64_t)g.N, (uint64_t)g.M};
       const uint64_t st[1] = {(uint64_t)g.N * oes};
-      const uint32_t box[2] = {32, 32};
+      const uint32_t box[2] = {bx, 32};
       rc = make_tmap(&to, g.out, odt, 2, d, st, box, osw);
     }
     if (rc) return rc;
