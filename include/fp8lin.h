@@ -125,18 +125,20 @@ typedef struct fp8_tensor {
  *              FP8_LAYOUT_COL_MAJOR: `out_t` = codes transposed: [C, R] (2-D), [B, C, R]
  *                (3-D), or, with offsets, [C, P] in the segment-padded layout: segment e
  *                starts at column pstart_e = sum_{j<e} roundup(count_j, 128) and is followed
- *                by zero codes up to the next multiple of 128. P >=
- *                fp8_jagged_padded_rows(R, E) and P % 16 == 0. For 2-D/3-D, R % 16 == 0.
+ *                by zero codes up to the next multiple of 128. P >= R + 127 E and
+ *                P % 16 == 0; fp8_jagged_padded_rows(R, E) gives the recommended P.
+ *                For 2-D/3-D, R % 16 == 0.
  *              FP8_LAYOUT_BOTH: both (tensor granularity only: one read, two outputs).
  *              ROW granularity supports ROW_MAJOR; COL granularity supports COL_MAJOR.
  *  inv_scales  fp32: [1] (tensor), [R] or [B*R] (row), [C], [B, C] or [E, C] (col).
  *  offsets     NULL, or int32 [E] cumulative segment ends (COL granularity, 2-D x only).
  *              Checked on the device: a bad vector sets FP8_DEV_BAD_OFFSETS.
  *  workspace   device memory, 16-byte aligned, of fp8_workspace_size(FP8_OP_QUANTIZE, groups,
- *              C, granularity) bytes: 4 bytes for tensor granularity (the amax word), 4 bytes
- *              per (group, column) for column granularity (groups = B for 3-D x, E with
- *              offsets, else 1; the per-column amax and then the fp32 scale), 0 for row
- *              granularity (workspace may then be NULL).
+ *              C, granularity) bytes: 4 bytes for tensor granularity (the amax word); for
+ *              column granularity 4 bytes per (group, column) for the column maxima, rounded
+ *              up to 16 bytes (groups = B for 3-D x, E with offsets, else 1); 0 for row
+ *              granularity (workspace may then be NULL). Calls sharing a workspace must be
+ *              stream-ordered: the quantize clears and uses it.
  * Bit-exactness: codes and inverse scales equal the recipe evaluated with an fp64 division,
  * an fp32 multiply and a round-to-nearest-even saturating cast (eps = 1e-12).
  */
@@ -256,7 +258,11 @@ int fp8_quantize_tensor_noalloc(const fp8_tensor* x, int out_dtype, int layout, 
 size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granularity,
                           int wgrad_mode);
 
-/* Minimum padded row count P of the segment-padded column-major layout (see fp8_quantize). */
+/* Padded row count P for the segment-padded column-major layout (see fp8_quantize): the room
+ * the segments need, rows + 127 * n_segments, rounded up to a multiple of 128 so that every row
+ * of the [C, P] operand starts on a 128-byte line (the grouped GEMM's tile loads then read whole
+ * L2 lines; a P that is only a multiple of 16 is accepted but makes each 128-byte row chunk
+ * straddle two lines). Returns -1 for negative arguments. */
 int64_t fp8_jagged_padded_rows(int64_t rows, int64_t n_segments);
 
 /* Text for an FP8_ERR_* return code or an FP8_DEV_* status word. */

@@ -150,7 +150,7 @@ static int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
 extern "C" int64_t fp8_jagged_padded_rows(int64_t rows, int64_t n_segments) {
   if (rows < 0 || n_segments < 0) return -1;
-  return round_up(rows + 127 * n_segments, 16);
+  return round_up(rows + 127 * n_segments, 128);
 }
 
 extern "C" uint64_t fp8_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchange(ns ? ns : 1); }
@@ -221,7 +221,7 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
     case FP8_GRAN_COL: {
       FP8_CHECK(layout == FP8_LAYOUT_COL_MAJOR, FP8_ERR_UNSUPPORTED);
       const int64_t groups = offsets ? (valid_desc(offsets) && offsets->ndim == 1 ? offsets->shape[0] : 0) : B;
-      FP8_CHECK(ws && (reinterpret_cast<uintptr_t>(ws) & 15u) == 0 && ws_bytes >= (size_t)(groups * C * 4),
+      FP8_CHECK(ws && (reinterpret_cast<uintptr_t>(ws) & 15u) == 0 && ws_bytes >= (size_t)col_ws_words(groups, C) * 4,
                 FP8_ERR_WORKSPACE);
       uint32_t* scratch = static_cast<uint32_t*>(ws);
       if (offsets) {
@@ -231,7 +231,7 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
         const int64_t E = offsets->shape[0];
         FP8_CHECK(out_t->ndim == 2 && out_t->shape[0] == C, FP8_ERR_INVALID_ARG);
         const int64_t P = out_t->shape[1];
-        FP8_CHECK(P >= fp8_jagged_padded_rows(R, E), FP8_ERR_INVALID_ARG);
+        FP8_CHECK(P >= R + 127 * E, FP8_ERR_INVALID_ARG);
         FP8_CHECK(P % 16 == 0, FP8_ERR_ALIGNMENT);
         FP8_CHECK(numel(inv) == E * C, FP8_ERR_INVALID_ARG);
         return launch_quant_cols(x->ptr, R, C, E, 0, static_cast<const int32_t*>(offsets->ptr), out_dtype,
@@ -435,7 +435,7 @@ static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad
   L.xt_q = (fp8w && rows) ? take((size_t)(K * M)) : 0;
   L.xt_inv = (fp8w && rows) ? take((size_t)K * 4) : 0;
   // per-column scratch of the column-wise quantizations (used one after the other)
-  L.col_scratch = rows ? take((size_t)(K > N ? K : N) * 4) : 0;
+  L.col_scratch = rows ? take((size_t)col_ws_words(1, K > N ? K : N) * 4) : 0;
   L.total = off;
   return L;
 }
@@ -444,7 +444,7 @@ extern "C" size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2,
   switch (op) {
     case FP8_OP_QUANTIZE:  // (d0, d1) = (groups, columns) for FP8_GRAN_COL
       if (granularity == FP8_GRAN_TENSOR) return 4;
-      if (granularity == FP8_GRAN_COL) return (size_t)(d0 > 0 ? d0 : 1) * (size_t)(d1 > 0 ? d1 : 0) * 4;
+      if (granularity == FP8_GRAN_COL) return (size_t)col_ws_words(d0 > 0 ? d0 : 1, d1 > 0 ? d1 : 0) * 4;
       return 0;
     case FP8_OP_LINEAR_FWD:
       return granularity == FP8_GRAN_TENSOR ? 256 : 0;
@@ -529,7 +529,7 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
     fp8_tensor wt_q = T2(ws + L.wt_q, FP8_DT_E4M3, K, N);
     fp8_tensor wt_inv = T1(ws + L.wt_inv, FP8_DT_F32, K);
     FP8_TRY(quantize_impl(w, FP8_GRAN_COL, FP8_DT_E4M3, FP8_LAYOUT_COL_MAJOR, nullptr, &wt_q, &wt_inv, nullptr,
-                          ws + L.col_scratch, (size_t)K * 4, c));
+                          ws + L.col_scratch, (size_t)col_ws_words(1, K) * 4, c));
     FP8_TRY(scaled_mm_impl(&dy_q, &wt_q, &dy_inv, &wt_inv, dx, 0, c));
   }
   if (need_dw) {
@@ -539,9 +539,9 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
       fp8_tensor xt_q = T2(ws + L.xt_q, FP8_DT_E4M3, K, M);
       fp8_tensor xt_inv = T1(ws + L.xt_inv, FP8_DT_F32, K);
       FP8_TRY(quantize_impl(dy, FP8_GRAN_COL, FP8_DT_E5M2, FP8_LAYOUT_COL_MAJOR, nullptr, &dyt_q, &dyt_inv, nullptr,
-                            ws + L.col_scratch, (size_t)N * 4, c));
+                            ws + L.col_scratch, (size_t)col_ws_words(1, N) * 4, c));
       FP8_TRY(quantize_impl(x, FP8_GRAN_COL, FP8_DT_E4M3, FP8_LAYOUT_COL_MAJOR, nullptr, &xt_q, &xt_inv, nullptr,
-                            ws + L.col_scratch, (size_t)K * 4, c));
+                            ws + L.col_scratch, (size_t)col_ws_words(1, K) * 4, c));
       FP8_TRY(scaled_mm_impl(&dyt_q, &xt_q, &dyt_inv, &xt_inv, dw, 0, c));
     } else {
       FP8_TRY(scaled_mm_impl(dy, x, nullptr, nullptr, dw, FP8_MM_A_MN_MAJOR | FP8_MM_B_MN_MAJOR, c));

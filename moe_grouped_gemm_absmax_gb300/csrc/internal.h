@@ -42,6 +42,8 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 // segments given by ends[n_groups] (segment-padded output, padded row count ld_out).
 // out_t row (g, c) starts at out_t + (g * C + c) * ld_out (dense) or out_t + c * ld_out + pstart_g
 // (segments). inv [n_groups, C]. scratch: n_groups * C words of device memory.
+// Workspace words (4 bytes each) a column quantize of `groups` x C scales needs.
+int64_t col_ws_words(int64_t groups, int64_t C);
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
                       const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, uint32_t* scratch,
                       const Ctx& c);

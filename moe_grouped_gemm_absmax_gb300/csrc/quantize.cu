@@ -218,24 +218,35 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 }
 
 // ==========================================================================================
-// Columnwise with column-major output: three stream-ordered kernels over (row group, 64-column
-// strip, row tile) work units, which never straddle a group (segment) boundary.
-//   1. colmax:   coalesced 16-byte loads (a warp reads four whole 128-byte row segments per
-//                instruction); per-column |x| maxima folded in registers, shuffles and shared
-//                memory; one relaxed atomic max per column per tile into a per-column scratch
-//                word (the bf16 bit pattern of the maximum).
-//   2. colscale: one thread per (group, column): the scale step; the fp32 scale replaces the
-//                amax word in the scratch and the inverse scale goes to the output.
-//   3. colcast:  the same loads, the fp32 multiply and the cast in registers; each 4-row column
-//                pack becomes one 32-bit word of FP8 codes, written into a transposed tile in
-//                shared memory (64 columns x 128 rows per box, TMA 128-byte swizzle; a thread's 8
-//                columns are rotated by its chunk index so the stores are conflict-free); TMA
-//                bulk-tensor stores write whole column-major boxes.
-// The cast pass re-reads the input. Work units walk the strips of a row tile first, so the
-// re-read mostly hits the 129 MB L2 when the tensor fits in it; larger tensors read it twice.
+// Columnwise with column-major output: two streaming passes of one warp-specialized kernel
+// (one CTA per SM) over work units, a unit being a 256-row x 64-column tile of one row group
+// (segment); units never straddle a group boundary and are ordered group, row tile, strip, so a
+// CTA's contiguous range of units reads long row segments (several KB per row) and neighbouring
+// strips share DRAM pages and L2 lines. Every CTA takes one contiguous range of units:
+//   producer warp: streams the range's tiles into a 4-stage shared-memory ring with TMA
+//              (128-byte swizzle), ~128 KB of loads in flight per SM;
+//   8 consumer warps read each tile from the ring (conflict-free through the swizzle).
+//   pass 1 (max): a tile's per-column |x| maxima are folded by shuffles and shared memory into
+//              one relaxed atomic max per column on a per-(group, column) scratch word (the bf16
+//              bit pattern of the maximum).
+//   pass 2 (cast): the scale step for the tile's 64 columns from the scratch words (fetched one
+//              tile ahead; the strip's first tile also writes the inverse scales); the fp32
+//              multiply and the cast in
+//              registers; each 4-row column pack becomes one 32-bit word of FP8 codes in a
+//              transposed tile in shared memory (64 columns x 128 rows per box, 128-byte swizzle;
+//              a thread's 8 columns are rotated by its chunk index so the stores are
+//              conflict-free); TMA bulk-tensor stores write whole column-major boxes from two
+//              alternating tiles. Pass 2 walks each range backwards, so its first reads are the
+//              tiles pass 1 read last, still in L2.
+// The passes are stream-ordered launches: no CTA waits on another.
 constexpr int kColThreads = 256;
-constexpr int kColNB = 4;                  // 128-row blocks per work unit (512 rows)
+constexpr int kColNB = 2;                  // 128-row blocks per work unit (256 rows)
 constexpr int kColTile = 128 * kColNB;
+constexpr int kColStages = 4;
+constexpr int kColStageBytes = kColTile * 128;         // 256 rows x 64 bf16
+constexpr int kColOutBytes = (kColTile / 128) * 8192;  // 64 columns x 256 rows of codes
+constexpr int kColConsumerWarps = kColThreads / 32;    // 8
+constexpr uint64_t kColDrainNs = 2000000000ull;        // fixed bound: loads in flight before exit
 
 struct ColParams {
   const uint16_t* x;
@@ -244,47 +255,50 @@ struct ColParams {
   int64_t n_groups;
   int64_t group_rows;  // dense modes
   const int32_t* ends; // segment mode
-  uint32_t* scratch;   // [n_groups, C]: amax bits, then fp32 scales
+  uint32_t* scratch;   // [n_groups, C]: amax bits
   float* inv;
   int32_t* status;
   int64_t n_strips;
+  uint64_t wait_ns;
   int mode;            // 0: 2-D [C, R] output; 1: batched [B, C, R]; 2: segments [C, P]
 };
 
 struct ColUnit {
   int64_t g, g0, n, pstart, write_end, rt;  // group, first row, rows, padded start, rows written, tile start
-  int64_t c0;                                // first column of the strip
+  int64_t strip, c0;                         // strip and its first column
 };
 
-// Units: dense modes have n_groups * tiles * strips; segments a prefix over the segments.
-// upre[e] = first unit of segment e; ppre[e] = padded start of segment e.
-FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t unit, const int32_t* upre, const int32_t* ppre) {
+// Unit i: group, row tile, strip. Segment mode: upre[e] = first unit of segment e, ppre[e] = its
+// padded start.
+FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t i, const int32_t* upre, const int32_t* ppre) {
   ColUnit u;
   int64_t local;
   if (p.mode == 2) {
     int lo = 0, hi = (int)p.n_groups - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (upre[mid] <= unit) lo = mid;
+      if (upre[mid] <= i) lo = mid;
       else hi = mid - 1;
     }
     u.g = lo;
-    local = unit - upre[lo];
+    local = i - upre[lo];
     u.g0 = lo ? p.ends[lo - 1] : 0;
     u.n = p.ends[lo] - u.g0;
     u.pstart = ppre[lo];
     u.write_end = round_up64(u.n, 128);
   } else {
-    const int64_t tiles = ceil_div64(p.group_rows, kColTile);
-    u.g = unit / (tiles * p.n_strips);
-    local = unit % (tiles * p.n_strips);
+    const int64_t per = p.n_strips * ceil_div64(p.group_rows, kColTile);
+    u.g = i / per;
+    local = i - u.g * per;
     u.g0 = u.g * p.group_rows;
     u.n = p.group_rows;
     u.pstart = 0;
     u.write_end = u.n;
   }
-  u.rt = (local / p.n_strips) * kColTile;
-  u.c0 = (local % p.n_strips) * 64;
+  const int64_t rt = local / p.n_strips;
+  u.strip = local - rt * p.n_strips;
+  u.rt = rt * kColTile;
+  u.c0 = u.strip * 64;
   return u;
 }
 
@@ -292,9 +306,9 @@ FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t unit, const int32_t* upre,
 // memory; returns the number of units, or -1 after reporting bad offsets.
 FP8_DEVI int64_t col_setup(const ColParams& p, int32_t* upre, int32_t* ppre) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (p.mode != 2) return p.n_groups * ceil_div64(p.group_rows, kColTile) * p.n_strips;
+  if (p.mode != 2) return p.n_groups * p.n_strips * ceil_div64(p.group_rows, kColTile);
   int bad = 0;
-  for (int64_t e = tid; e < p.n_groups; e += kColThreads) {
+  for (int64_t e = tid; e < p.n_groups; e += blockDim.x) {
     const int64_t cur = p.ends[e], prev = e ? p.ends[e - 1] : 0;
     if (cur < prev || (e == p.n_groups - 1 && cur != p.rows_total)) bad = 1;
   }
@@ -338,154 +352,279 @@ FP8_DEVI int64_t col_setup(const ColParams& p, int32_t* upre, int32_t* ppre) {
   return upre[p.n_groups];
 }
 
-// This thread's 4 rows x 8 columns of every 128-row block of the unit (zeros outside the
-// group and the matrix): rows 128 b + 16 warp + 4 rq + jj, columns c0 + 8 ch .. + 7.
-FP8_DEVI void col_load(const ColParams& p, const ColUnit& u, int warp, int ch, int rq, uint4 (&v)[kColNB][4]) {
-  int64_t valid = u.n - u.rt;
-  valid = valid < 0 ? 0 : (valid < kColTile ? valid : kColTile);
-  const bool ch_ok = u.c0 + ch * 8 < p.C;
-  const uint16_t* base = p.x + (u.g0 + u.rt) * p.C + u.c0 + ch * 8;
-#pragma unroll
-  for (int b = 0; b < kColNB; ++b)
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const int row = 128 * b + 16 * warp + 4 * rq + jj;
-      v[b][jj] = (ch_ok && row < valid) ? ld_nc_v4(base + (int64_t)row * p.C) : make_uint4(0, 0, 0, 0);
-    }
-}
-
-__global__ void __launch_bounds__(kColThreads) colmax_kernel(const ColParams p) {
-  __shared__ uint32_t red[8][8][4];
-  extern __shared__ int32_t pre[];
-  int32_t* upre = pre;
-  int32_t* ppre = pre + (p.n_groups + 1);
-  const int64_t total = col_setup(p, upre, ppre);
-  if (total < 0) return;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ch = lane & 7, rq = lane >> 3;
-  for (int64_t unit = blockIdx.x; unit < total; unit += gridDim.x) {
-    const ColUnit u = col_unit(p, unit, upre, ppre);
-    uint4 v[kColNB][4];
-    col_load(p, u, warp, ch, rq, v);
-    uint32_t m4[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int b = 0; b < kColNB; ++b)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        m4[0] = absmax2(m4[0], v[b][jj].x);
-        m4[1] = absmax2(m4[1], v[b][jj].y);
-        m4[2] = absmax2(m4[2], v[b][jj].z);
-        m4[3] = absmax2(m4[3], v[b][jj].w);
-      }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      m4[i] = __vmaxu2(m4[i], __shfl_xor_sync(0xffffffffu, m4[i], 8));
-      m4[i] = __vmaxu2(m4[i], __shfl_xor_sync(0xffffffffu, m4[i], 16));
-    }
-    if (rq == 0) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) red[warp][ch][i] = m4[i];
-    }
-    __syncthreads();
-    if (tid < 32) {  // pair t = columns 2t, 2t+1 = chunk t/4, word t%4
-      uint32_t m = 0;
-      for (int w = 0; w < 8; ++w) m = __vmaxu2(m, red[w][tid >> 2][tid & 3]);
-      const int64_t col = u.c0 + 2 * tid;
-      uint32_t* sc = p.scratch + u.g * p.C + col;
-      if (col < p.C && (m & 0xFFFFu)) red_max_relaxed(sc, m & 0xFFFFu);
-      if (col + 1 < p.C && (m >> 16)) red_max_relaxed(sc + 1, m >> 16);
-    }
-    __syncthreads();
-  }
-}
-
-template <int FMT>
-__global__ void __launch_bounds__(256) colscale_kernel(uint32_t* __restrict__ scratch, float* __restrict__ inv,
-                                                       int64_t n, const __grid_constant__ ScaleTab tab) {
-  const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  if (i >= n) return;
-  const Scale s = tab_scale(tab, scratch[i]);
-  reinterpret_cast<float*>(scratch)[i] = s.s32;
-  inv[i] = s.inv32;
-}
-
 // Column j (0..7) of a 16-byte vector of 8 bf16, as fp32.
 FP8_DEVI float col_of(const uint4& v, int j) {
   const uint32_t w = j < 2 ? v.x : (j < 4 ? v.y : (j < 6 ? v.z : v.w));
   return (j & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(kColThreads) colcast_kernel(const __grid_constant__ CUtensorMap tm_out,
-                                                              const ColParams p) {
+// What the producer publishes with each stage: the unit's coordinates the consumers need.
+struct ColInfo {
+  int32_t g, c0, rt, valid, wrows, pstart;  // group, first column, tile start, rows of the group, rows written
+};
+struct ColShared {
+  uint64_t full[kColStages];   // the tile landed (TMA bytes) and the info was written
+  uint64_t scl[kColStages];    // pass 2: the stage's 64 scales were written
+  uint64_t empty[kColStages];  // the consumer warps are done with the stage
+  ColInfo info[kColStages];
+  float sc[kColStages][64];    // pass 2: the fp32 scales of the stage's 64 columns
+  uint32_t red[kColConsumerWarps][8][4];
+  int abort;
+};
+template <bool CAST>
+struct ColSmem {
+  static constexpr int bytes =
+      1024 + kColStages * kColStageBytes + (CAST ? 2 * kColOutBytes : 0) + (int)sizeof(ColShared);
+};
+
+template <int FMT, bool CAST>
+__global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __grid_constant__ CUtensorMap tm_in,
+                                                                        const __grid_constant__ CUtensorMap tm_out,
+                                                                        const ColParams p,
+                                                                        const __grid_constant__ ScaleTab tab) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* T = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int32_t* upre = reinterpret_cast<int32_t*>(T + kColNB * 8192);
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Tout = ring + kColStages * kColStageBytes;
+  ColShared& S = *reinterpret_cast<ColShared*>(Tout + (CAST ? 2 * kColOutBytes : 0));
+  int32_t* upre = reinterpret_cast<int32_t*>(&S + 1);
   int32_t* ppre = upre + (p.n_groups + 1);
-  const int64_t total = col_setup(p, upre, ppre);
-  if (total < 0) return;
+  const int64_t M = col_setup(p, upre, ppre);
+  if (M < 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ch = lane & 7, rq = lane >> 3;
-  if (tid == 0) tma_prefetch_desc(&tm_out);
-  const float* scales = reinterpret_cast<const float*>(p.scratch);
-  for (int64_t unit = blockIdx.x; unit < total; unit += gridDim.x) {
-    const ColUnit u = col_unit(p, unit, upre, ppre);
-    uint4 v[kColNB][4];
-    col_load(p, u, warp, ch, rq, v);
-    float sc[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int64_t col = u.c0 + ch * 8 + j;
-      sc[j] = col < p.C ? scales[u.g * p.C + col] : 0.0f;
+  // the scale table in shared memory: the lanes of a warp look up different entries at once
+  __shared__ ScaleTab stab;
+  if (CAST) {
+    static_assert(sizeof(ScaleTab) % 4 == 0, "table words");
+    for (int i = tid; i < (int)(sizeof(ScaleTab) / 4); i += blockDim.x)
+      reinterpret_cast<uint32_t*>(&stab)[i] = reinterpret_cast<const uint32_t*>(&tab)[i];
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kColStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.scl[s], 1);
+      mbar_init(&S.empty[s], kColConsumerWarps);
     }
-    int64_t wrows = u.write_end - u.rt;
-    wrows = wrows < 0 ? 0 : (wrows < kColTile ? wrows : kColTile);
-    const int nbox = (int)ceil_div64(wrows, 128);
-    if (tid == 0) bulk_wait_read_all();  // the previous unit's stores have read the tile
-    __syncthreads();
-#pragma unroll
-    for (int b = 0; b < kColNB; ++b) {
-      if (b < nbox) {
-        uint32_t o[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float s = sc[j];
-          o[j] = cvt_fp8x2<FMT>(__fmul_rn(col_of(v[b][0], j), s), __fmul_rn(col_of(v[b][1], j), s)) |
-                 (cvt_fp8x2<FMT>(__fmul_rn(col_of(v[b][2], j), s), __fmul_rn(col_of(v[b][3], j), s)) << 16);
-        }
-        // rotate by ch so that the lanes of a warp write 8 different column residues at once
-#pragma unroll
-        for (int sh = 1; sh < 8; sh <<= 1) {
-          const bool rot = (ch & sh) != 0;
-          uint32_t t[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) t[j] = rot ? o[(j + sh) & 7] : o[j];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) o[j] = t[j];
-        }
-        uint8_t* box = T + b * 8192;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int cl = ch * 8 + ((j + ch) & 7);
-          *reinterpret_cast<uint32_t*>(box + cl * 128 + (((warp ^ cl) & 7) << 4) + rq * 4) = o[j];
-        }
-      }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      for (int b = 0; b < nbox; ++b) {
-        const int32_t xo = (int32_t)(u.pstart + u.rt + 128 * b);
-        if (p.mode == 1)
-          tma_store_3d(&tm_out, T + b * 8192, xo, (int32_t)u.c0, (int32_t)u.g);
-        else
-          tma_store_2d(&tm_out, T + b * 8192, xo, (int32_t)u.c0);
-      }
-      bulk_commit();
+    S.abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_in);
+    if (CAST) tma_prefetch_desc(&tm_out);
+  }
+  // Groups without rows have no units: their inverse scales (amax 0) are written here.
+  if (CAST && blockIdx.x == 0) {
+    const Scale s0 = tab_scale(tab, 0u);
+    for (int64_t g = 0; g < p.n_groups; ++g) {
+      const int64_t n = p.mode == 2 ? p.ends[g] - (g ? p.ends[g - 1] : 0) : p.group_rows;
+      if (n > 0) continue;
+      for (int64_t c = tid; c < p.C; c += blockDim.x) p.inv[g * p.C + c] = s0.inv32;
     }
   }
-  if (tid == 0) bulk_wait_all();
+  __syncthreads();
+  // this CTA's contiguous range of units; pass 2 walks it backwards
+  const int64_t lo = M * blockIdx.x / gridDim.x, hi = M * (blockIdx.x + 1) / gridDim.x;
+  const int64_t cnt = hi - lo;
+  auto unit_at = [&](int64_t k) { return CAST ? hi - 1 - k : lo + k; };
+  volatile int* cta_abort = &S.abort;
+
+  if (warp == 0) {
+    // ============ producer warp: tiles by TMA; in pass 2 also each tile's 64 scales ============
+    int s = 0;
+    uint32_t ph = 0;
+    int64_t k = 0;
+    uint32_t am[2] = {0, 0};  // pass 2: amax words of the next unit's columns lane, lane + 32
+    auto fetch_amax = [&](const ColUnit& un) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t col = un.c0 + lane + 32 * h;
+        am[h] = col < p.C ? __ldcg(p.scratch + un.g * p.C + col) : 0u;
+      }
+    };
+    ColUnit u;
+    if (cnt > 0) {
+      u = col_unit(p, unit_at(0), upre, ppre);
+      if (CAST) fetch_amax(u);
+    }
+    for (; k < cnt; ++k) {
+      const bool got = lane == 0 ? mbar_wait(&S.empty[s], ph ^ 1, cta_abort, p.wait_ns) : true;
+      if (!__shfl_sync(0xffffffffu, got, 0)) {
+        if (lane == 0 && !*cta_abort) {
+          *cta_abort = 1;
+          set_status(p.status, FP8_DEV_TIMEOUT);
+        }
+        break;
+      }
+      if (lane == 0) {
+        int64_t valid = u.n - u.rt, wr = u.write_end - u.rt;
+        valid = valid < 0 ? 0 : (valid < kColTile ? valid : kColTile);
+        wr = wr < 0 ? 0 : (wr < kColTile ? wr : kColTile);
+        S.info[s] = ColInfo{(int32_t)u.g, (int32_t)u.c0, (int32_t)u.rt, (int32_t)valid, (int32_t)wr,
+                            (int32_t)u.pstart};
+        mbar_arrive_expect_tx(&S.full[s], kColStageBytes);
+        tma_load_2d(ring + s * kColStageBytes, &tm_in, &S.full[s], (int32_t)u.c0, (int32_t)(u.g0 + u.rt));
+      }
+      const ColUnit un = k + 1 < cnt ? col_unit(p, unit_at(k + 1), upre, ppre) : u;
+      if (CAST) {
+        // this unit's scales from the words fetched one unit earlier, then the next unit's words
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const Scale sv = tab_scale(stab, am[h]);
+          S.sc[s][lane + 32 * h] = sv.s32;
+          const int64_t col = u.c0 + lane + 32 * h;
+          if (u.rt == 0 && col < p.C) p.inv[u.g * p.C + col] = sv.inv32;  // the strip's first tile
+        }
+        if (k + 1 < cnt) fetch_amax(un);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.scl[s]);
+      }
+      u = un;
+      if (++s == kColStages) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+    // the loads in flight land before the CTA may leave (all consumed unless aborted)
+    if (lane == 0) {
+      const int64_t first = k > kColStages ? k - kColStages : 0;
+      for (int64_t j = first; j < k; ++j)
+        mbar_wait(&S.full[j % kColStages], (uint32_t)((j / kColStages) & 1), nullptr, kColDrainNs);
+    }
+  } else {
+    // ============ consumers: thread = 4 rows x 8 columns of each 128-row block ============
+    const int ct = tid - 32, cw = ct >> 5;
+    const int ch = lane & 7, rq = lane >> 3;
+    int s = 0;
+    uint32_t ph = 0;
+    int ncast = 0;
+    for (int64_t k = 0; k < cnt; ++k) {
+      bool got = mbar_wait(&S.full[s], ph, cta_abort, p.wait_ns);
+      if (CAST && got) got = mbar_wait(&S.scl[s], ph, cta_abort, p.wait_ns);
+      if (!named_bar_and(2, kColThreads, got)) {  // uniform decision across the consumer warps
+        if (!got && !*cta_abort) {
+          *cta_abort = 1;
+          set_status(p.status, FP8_DEV_TIMEOUT);
+        }
+        break;
+      }
+      const ColInfo info = S.info[s];
+      float sc[8];
+      if (CAST) {
+        const float4 a = *reinterpret_cast<const float4*>(&S.sc[s][ch * 8]);
+        const float4 b = *reinterpret_cast<const float4*>(&S.sc[s][ch * 8 + 4]);
+        sc[0] = a.x; sc[1] = a.y; sc[2] = a.z; sc[3] = a.w;
+        sc[4] = b.x; sc[5] = b.y; sc[6] = b.z; sc[7] = b.w;
+      }
+      const uint8_t* st = ring + s * kColStageBytes;
+      uint4 v[kColNB][4];
+      if (info.valid == kColTile) {
+#pragma unroll
+        for (int b = 0; b < kColNB; ++b)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int r = 128 * b + 16 * cw + 4 * rq + jj;
+            v[b][jj] = *reinterpret_cast<const uint4*>(st + r * 128 + ((ch ^ (r & 7)) << 4));
+          }
+      } else {
+#pragma unroll
+        for (int b = 0; b < kColNB; ++b)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int r = 128 * b + 16 * cw + 4 * rq + jj;  // rows past the group read as zeros
+            v[b][jj] = r < info.valid ? *reinterpret_cast<const uint4*>(st + r * 128 + ((ch ^ (r & 7)) << 4))
+                                      : make_uint4(0, 0, 0, 0);
+          }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[s]);  // this warp is done with the stage
+      if (++s == kColStages) {
+        s = 0;
+        ph ^= 1;
+      }
+      if (!CAST) {
+        uint32_t m4[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int b = 0; b < kColNB; ++b)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            m4[0] = absmax2(m4[0], v[b][jj].x);
+            m4[1] = absmax2(m4[1], v[b][jj].y);
+            m4[2] = absmax2(m4[2], v[b][jj].z);
+            m4[3] = absmax2(m4[3], v[b][jj].w);
+          }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          m4[q] = __vmaxu2(m4[q], __shfl_xor_sync(0xffffffffu, m4[q], 8));
+          m4[q] = __vmaxu2(m4[q], __shfl_xor_sync(0xffffffffu, m4[q], 16));
+        }
+        if (rq == 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) S.red[cw][ch][q] = m4[q];
+        }
+        named_bar_sync(1, kColThreads);
+        if (ct < 32) {  // pair t = columns 2t, 2t+1 = chunk t/4, word t%4
+          uint32_t m = 0;
+#pragma unroll
+          for (int w = 0; w < kColConsumerWarps; ++w) m = __vmaxu2(m, S.red[w][ct >> 2][ct & 3]);
+          const int64_t col = info.c0 + 2 * ct;
+          uint32_t* scw = p.scratch + (int64_t)info.g * p.C + col;
+          if (col < p.C && (m & 0xFFFFu)) red_max_relaxed(scw, m & 0xFFFFu);
+          if (col + 1 < p.C && (m >> 16)) red_max_relaxed(scw + 1, m >> 16);
+        }
+        named_bar_sync(1, kColThreads);
+      } else {
+        uint8_t* T = Tout + (ncast & 1) * kColOutBytes;
+        ++ncast;
+        if (ct == 0) bulk_wait_read_1();  // the store that last read this tile has done so
+        named_bar_sync(1, kColThreads);
+        const int nbox = (info.wrows + 127) / 128;
+#pragma unroll
+        for (int b = 0; b < kColNB; ++b) {
+          if (b < nbox) {
+            uint32_t o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float2 s2 = make_float2(sc[j], sc[j]);
+              const float2 x01 = fmul2_rn(make_float2(col_of(v[b][0], j), col_of(v[b][1], j)), s2);
+              const float2 x23 = fmul2_rn(make_float2(col_of(v[b][2], j), col_of(v[b][3], j)), s2);
+              o[j] = cvt_fp8x2<FMT>(x01.x, x01.y) | (cvt_fp8x2<FMT>(x23.x, x23.y) << 16);
+            }
+            // rotate by ch so that the lanes of a warp write 8 different column residues at once
+#pragma unroll
+            for (int sh = 1; sh < 8; sh <<= 1) {
+              const bool rot = (ch & sh) != 0;
+              uint32_t t[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) t[j] = rot ? o[(j + sh) & 7] : o[j];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) o[j] = t[j];
+            }
+            uint8_t* box = T + b * 8192;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int cl = ch * 8 + ((j + ch) & 7);
+              *reinterpret_cast<uint32_t*>(box + cl * 128 + (((cw ^ cl) & 7) << 4) + rq * 4) = o[j];
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, kColThreads);
+        if (ct == 0) {
+          for (int b = 0; b < nbox; ++b) {
+            const int32_t xo = info.pstart + info.rt + 128 * b;
+            if (p.mode == 1)
+              tma_store_3d(&tm_out, T + b * 8192, xo, info.c0, info.g);
+            else
+              tma_store_2d(&tm_out, T + b * 8192, xo, info.c0);
+          }
+          bulk_commit();
+        }
+      }
+    }
+    if (CAST && ct == 0) bulk_wait_all();
+  }
+  __syncthreads();
 }
+
+// Workspace words of a column quantize: the amax per (group, column), rounded to 16 bytes.
+int64_t col_ws_words(int64_t groups, int64_t C) { return round_up64(groups * C, 4); }
 
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
                       const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, uint32_t* scratch,
@@ -499,13 +638,14 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   p.n_groups = n_groups;
   p.group_rows = group_rows;
   p.ends = ends;
+  p.n_strips = ceil_div64(C, 64);
   p.scratch = scratch;
   p.inv = inv;
   p.status = c.status;
-  p.n_strips = ceil_div64(C, 64);
+  p.wait_ns = c.wait_ns;
   p.mode = ends ? 2 : (n_groups > 1 ? 1 : 0);
 
-  CUtensorMap tout;
+  CUtensorMap tout, tin;
   int rc;
   if (p.mode == 1) {
     const uint64_t dims[3] = {(uint64_t)group_rows, (uint64_t)C, (uint64_t)n_groups};
@@ -520,35 +660,38 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
     rc = make_tmap(&tout, out_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (rc != FP8_OK) return rc;
+  {
+    const uint64_t dims[2] = {(uint64_t)C, (uint64_t)(rows_total > 0 ? rows_total : 1)};
+    const uint64_t strides[1] = {(uint64_t)C * 2};
+    const uint32_t box[2] = {64, kColTile};
+    rc = make_tmap(&tin, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != FP8_OK) return rc;
+  }
 
-  const int64_t n_scales = n_groups * C;
-  if (cudaMemsetAsync(scratch, 0, (size_t)n_scales * 4, c.stream) != cudaSuccess) return FP8_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, (size_t)col_ws_words(n_groups, C) * 4, c.stream) != cudaSuccess) return FP8_ERR_CUDA;
   // units: exact for dense modes; for segments an upper bound (each segment adds at most one
   // partial tile) -- the kernels compute the exact count from the offsets
   const int64_t units = p.mode == 2 ? (ceil_div64(rows_total, kColTile) + n_groups) * p.n_strips
                                     : n_groups * ceil_div64(group_rows, kColTile) * p.n_strips;
-  const size_t pre_bytes = p.mode == 2 ? 8 * (size_t)(n_groups + 1) : 0;
+  const size_t pre = p.mode == 2 ? 8 * (size_t)(n_groups + 1) : 0;
+  const int64_t grid = units > 0 ? (units < c.sm_count ? units : c.sm_count) : 1;
+  const ScaleTab& tab = scale_tab(fmt);
+  // pass 1: column maxima
   if (units > 0) {
-    const int64_t cap_a = (int64_t)c.sm_count * 3;
-    colmax_kernel<<<(unsigned)(units < cap_a ? units : cap_a), kColThreads, pre_bytes, c.stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
-  }
-  const unsigned gs = (unsigned)ceil_div64(n_scales, 256);
-  if (fmt == FP8_DT_E4M3)
-    colscale_kernel<FP8_DT_E4M3><<<gs, 256, 0, c.stream>>>(scratch, inv, n_scales, scale_tab(FP8_DT_E4M3));
-  else
-    colscale_kernel<FP8_DT_E5M2><<<gs, 256, 0, c.stream>>>(scratch, inv, n_scales, scale_tab(FP8_DT_E5M2));
-  if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
-  if (units > 0) {
-    auto kern = fmt == FP8_DT_E4M3 ? colcast_kernel<FP8_DT_E4M3> : colcast_kernel<FP8_DT_E5M2>;
-    const size_t smem = 1024 + kColNB * 8192 + pre_bytes;
-    if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    auto k1 = fmt == FP8_DT_E4M3 ? colstream_kernel<FP8_DT_E4M3, false> : colstream_kernel<FP8_DT_E5M2, false>;
+    const size_t smem = ColSmem<false>::bytes + pre;
+    if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return FP8_ERR_CUDA;
-    const int64_t cap_b = (int64_t)c.sm_count * 3;
-    kern<<<(unsigned)(units < cap_b ? units : cap_b), kColThreads, smem, c.stream>>>(tout, p);
+    k1<<<(unsigned)grid, kColThreads + 32, smem, c.stream>>>(tin, tout, p, tab);
     if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
   }
-  return FP8_OK;
+  // pass 2: scales and cast (also writes the scales of groups without rows)
+  auto k2 = fmt == FP8_DT_E4M3 ? colstream_kernel<FP8_DT_E4M3, true> : colstream_kernel<FP8_DT_E5M2, true>;
+  const size_t smem2 = ColSmem<true>::bytes + pre;
+  if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
+    return FP8_ERR_CUDA;
+  k2<<<(unsigned)grid, kColThreads + 32, smem2, c.stream>>>(tin, tout, p, tab);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
 }  // namespace fp8lin

@@ -32,10 +32,12 @@ def test_header_declarations_are_exported(fp8):
 def test_host_helpers(fp8):
     for R, E in [(0, 1), (1, 1), (100, 3), (8192, 16), (131072, 256)]:
         P = fp8.fp8_jagged_padded_rows(R, E)
-        assert P % 16 == 0 and P >= R + 127 * E
+        assert P % 128 == 0 and R + 127 * E <= P < R + 127 * E + 128
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_TENSOR) == 4
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_ROW) == 0
+    # one amax word per (group, column), rounded up to 16 bytes
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 16, 5120, granularity=fp8.GRAN_COL) == 16 * 5120 * 4
+    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 1, 70, granularity=fp8.GRAN_COL) == 72 * 4
     M, K, N = 256, 512, 128
     ws_row_bf16 = fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_ROW, fp8.WGRAD_BF16)
     ws_row_fp8 = fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_ROW, fp8.WGRAD_FP8)

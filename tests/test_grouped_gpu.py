@@ -75,7 +75,9 @@ def test_jagged_m_single_expert_equals_dense(fp8):
 # the last case has enough 256 x 256 tiles per expert set to run on CTA pairs
 @pytest.mark.parametrize("counts,N,Kd", [([100, 0, 300, 37], 72, 200), ([0, 0, 130], 256, 256), ([500], 128, 64),
                                          ([1, 127, 128, 129, 0], 40, 24), ([300, 0, 260, 90], 520, 2560)])
-def test_jagged_k(fp8, counts, N, Kd):
+@pytest.mark.parametrize("pitch16", [False, True])
+def test_jagged_k(fp8, counts, N, Kd, pitch16):
+    """pitch16: the padded operands' row pitch is a multiple of 16 but not of 128 bytes."""
     counts = [int(c) for c in counts]
     E, M = len(counts), sum(counts)
     G = W.normal_bf16((M, N), 1e-3, 7)
@@ -84,6 +86,9 @@ def test_jagged_k(fp8, counts, N, Kd):
     cg, sg = oracle.quantize_jagged_cols(bits(G), ends, oracle.E5M2)
     cx, sx = oracle.quantize_jagged_cols(bits(X), ends, oracle.E4M3)
     P = fp8.fp8_jagged_padded_rows(M, E)
+    if pitch16:
+        P = W.ceil_div(M + 127 * E, 16) * 16
+        P += 16 if P % 128 == 0 else 0
     out = torch.full((E, N, Kd), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     fp8.fp8_grouped_mm(upload_codes(segpad_cols(cg, ends, P), oracle.E5M2), upload_codes(segpad_cols(cx, ends, P), oracle.E4M3),

@@ -103,7 +103,8 @@ def test_tensorwise_dual_output(fp8, R, C, fi):
     assert np.array_equal(codes(q1), q_ref) and np.array_equal(codes(qt1), q_ref.T)
 
 
-@pytest.mark.parametrize("R,C", [(16, 8), (512, 64), (1040, 200), (8192, 136), (9216, 72), (20480, 64)])
+@pytest.mark.parametrize("R,C", [(16, 8), (512, 64), (1040, 200), (8192, 136), (9216, 72), (20480, 64),
+                                 (2048, 2048), (1040, 4096)])
 @pytest.mark.parametrize("fi", [0, 1])
 def test_colwise_transposed(fp8, R, C, fi):
     """Column scales with column-major output; R = 20480 takes the two-pass path (groups above
@@ -131,7 +132,7 @@ def test_colwise_special_columns(fp8):
         assert np.array_equal(f32_bits(inv), inv_ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("B,R,C", [(3, 64, 96), (4, 7168 // 8, 256), (2, 16, 8), (40, 256, 200)])
+@pytest.mark.parametrize("B,R,C", [(3, 64, 96), (4, 7168 // 8, 256), (2, 16, 8), (40, 256, 200), (8, 1040, 512)])
 def test_colwise_batched_3d(fp8, B, R, C):
     """Per-expert column scales of a 3-D weight [E, K, N] (amax over K for each (e, n))."""
     x = W.normal_bf16((B, R, C), 0.02, 400 + B)
@@ -166,6 +167,9 @@ def test_jagged_colwise(fp8, counts, fi):
     x = W.normal_bf16((R, C), 1e-3, 500 + R)
     ends = W.ends_from_counts(counts)
     P = fp8.fp8_jagged_padded_rows(R, len(counts))
+    if fi == 1:  # a pitch that is a multiple of 16 but not of 128 bytes is accepted too
+        P = W.ceil_div(R + 127 * len(counts), 16) * 16
+        P += 16 if P % 128 == 0 else 0
     canary = torch.full((C, P), 0x5A, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn if dt == 3 else torch.float8_e5m2)
     inv = torch.empty((len(counts), C), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -178,6 +182,29 @@ def test_jagged_colwise(fp8, counts, fi):
     got = codes(canary)
     assert np.array_equal(got[:, :used], ref[:, :used])  # data and zero padding
     assert np.all(got[:, used:] == 0x5A)  # nothing written past the last padded segment
+    assert np.array_equal(f32_bits(inv), inv_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("counts", [list(W.llama4_counts(1) // 2), [700, 0, 1300, 5, 0, 2100]])
+def test_jagged_colwise_wide(fp8, counts):
+    """Segment columns with many 256-row x 64-column work units per CTA (C = 1024)."""
+    counts = [int(c) for c in counts]
+    R, C = sum(counts), 1024
+    x = W.normal_bf16((R, C), 1e-2, 600 + R)
+    ends = W.ends_from_counts(counts)
+    P = fp8.fp8_jagged_padded_rows(R, len(counts))
+    out = torch.full((C, P), 0x5A, dtype=torch.uint8, device="cuda").view(torch.float8_e5m2)
+    inv = torch.empty((len(counts), C), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fp8.fp8_quantize(x.cuda(), fp8.GRAN_COL, fp8.DT_E5M2, fp8.LAYOUT_COL_MAJOR, None, out, inv,
+                     torch.from_numpy(ends).cuda(), fp8.col_workspace(len(counts), C, "cuda"), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    q_ref, inv_ref = oracle.quantize_jagged_cols(bits(x), ends, oracle.E5M2)
+    ref, used = _segpad(q_ref, ends, P)
+    got = codes(out)
+    assert np.array_equal(got[:, :used], ref[:, :used])
+    assert np.all(got[:, used:] == 0x5A)
     assert np.array_equal(f32_bits(inv), inv_ref.view(np.uint32))
 
 
