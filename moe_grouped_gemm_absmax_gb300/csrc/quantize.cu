@@ -107,9 +107,92 @@ static int rows_dispatch(const void* x, int64_t R, int nvec, void* q, float* inv
   return FP8_ERR_UNSUPPORTED;
 }
 
+// Rowwise for rows of up to 16384 elements: a team of WPR warps (1, 2 or 4) per row. A team issues
+// all of its row's 16-byte loads at once (up to 16 per lane), folds |x|, combines its warps'
+// maxima through shared memory behind a barrier of the team alone (none for one warp), takes the
+// scale from the table (one row per team: every lane looks up the same entry), casts from
+// registers and stores 8 codes per lane and vector. Persistent teams walk the rows with a grid
+// stride, so at any time some teams load while others cast and store.
+constexpr int kRowWarpVPL = 16;
+template <int FMT, int WPR>
+__global__ void __launch_bounds__(256) quant_rows_warp_kernel(const uint4* __restrict__ x, int64_t R, int nvec,
+                                                              uint2* __restrict__ q, float* __restrict__ inv,
+                                                              const __grid_constant__ ScaleTab tab) {
+  constexpr int TPR = 32 * WPR;
+  __shared__ uint32_t red[2][8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int team = warp / WPR, t = threadIdx.x % TPR;
+  const int64_t team0 = (int64_t)blockIdx.x * (8 / WPR) + team;
+  const int64_t nteams = (int64_t)gridDim.x * (8 / WPR);
+  int par = 0;
+  for (int64_t r = team0; r < R; r += nteams) {
+    const uint4* xr = x + r * nvec;
+    uint4 v[kRowWarpVPL];
+    uint32_t acc = 0;
+#pragma unroll
+    for (int i = 0; i < kRowWarpVPL; ++i) {
+      const int c = t + TPR * i;
+      v[i] = c < nvec ? ld_nc_v4(xr + c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kRowWarpVPL; ++i) acc = absmax_vec8(acc, v[i]);
+    uint32_t m = __reduce_max_sync(0xffffffffu, absmax_fold(acc));
+    if (WPR > 1) {
+      if (lane == 0) red[par][warp] = m;
+      named_bar_sync(1 + team, TPR);
+#pragma unroll
+      for (int w = 0; w < WPR; ++w) m = max(m, red[par][team * WPR + w]);
+      par ^= 1;
+    }
+    const Scale sc = tab_scale(tab, m);
+    if (t == 0) inv[r] = sc.inv32;
+    uint2* qr = q + r * nvec;
+    const float2 s2 = make_float2(sc.s32, sc.s32);
+#pragma unroll
+    for (int i = 0; i < kRowWarpVPL; ++i) {
+      const int c = t + TPR * i;
+      if (c < nvec) {
+        const uint4 d = v[i];
+        float2 a = fmul2_rn(make_float2(__uint_as_float(d.x << 16), __uint_as_float(d.x & 0xFFFF0000u)), s2);
+        float2 b = fmul2_rn(make_float2(__uint_as_float(d.y << 16), __uint_as_float(d.y & 0xFFFF0000u)), s2);
+        uint2 o;
+        o.x = cvt_fp8x2<FMT>(a.x, a.y) | (cvt_fp8x2<FMT>(b.x, b.y) << 16);
+        a = fmul2_rn(make_float2(__uint_as_float(d.z << 16), __uint_as_float(d.z & 0xFFFF0000u)), s2);
+        b = fmul2_rn(make_float2(__uint_as_float(d.w << 16), __uint_as_float(d.w & 0xFFFF0000u)), s2);
+        o.y = cvt_fp8x2<FMT>(a.x, a.y) | (cvt_fp8x2<FMT>(b.x, b.y) << 16);
+        qr[c] = o;
+      }
+    }
+  }
+}
+
+template <int FMT, int WPR>
+static int run_rows_warp(const void* x, int64_t R, int nvec, void* q, float* inv, const Ctx& c) {
+  auto kern = quant_rows_warp_kernel<FMT, WPR>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+  // as many teams as fit at once, but no more than the rows, with the rows spread evenly
+  const int64_t slots = (int64_t)c.sm_count * per_sm * (8 / WPR);
+  const int64_t waves = ceil_div64(R, slots);
+  const int64_t teams = ceil_div64(R, waves);
+  kern<<<(unsigned)ceil_div64(teams, 8 / WPR), 256, 0, c.stream>>>(static_cast<const uint4*>(x), R, nvec,
+                                                                    static_cast<uint2*>(q), inv, scale_tab(FMT));
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+template <int FMT>
+static int rows_warp_dispatch(const void* x, int64_t R, int nvec, void* q, float* inv, const Ctx& c) {
+  if (nvec <= 32 * kRowWarpVPL) return run_rows_warp<FMT, 1>(x, R, nvec, q, inv, c);
+  if (nvec <= 64 * kRowWarpVPL) return run_rows_warp<FMT, 2>(x, R, nvec, q, inv, c);
+  return run_rows_warp<FMT, 4>(x, R, nvec, q, inv, c);
+}
+
 int launch_quant_rows(const void* x, int64_t R, int64_t C, int fmt, void* q, float* inv, const Ctx& c) {
   if (R == 0) return FP8_OK;
   const int nvec = (int)(C / 8);
+  if (nvec >= 64 && nvec <= 128 * kRowWarpVPL)
+    return fmt == FP8_DT_E4M3 ? rows_warp_dispatch<FP8_DT_E4M3>(x, R, nvec, q, inv, c)
+                              : rows_warp_dispatch<FP8_DT_E5M2>(x, R, nvec, q, inv, c);
   return fmt == FP8_DT_E4M3 ? rows_dispatch<FP8_DT_E4M3>(x, R, nvec, q, inv, c)
                             : rows_dispatch<FP8_DT_E5M2>(x, R, nvec, q, inv, c);
 }
