@@ -526,7 +526,7 @@ def main():
     ap.add_argument("--workload", default="llama3-8b-mlp-up", choices=list(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=64)
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=30)
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     ws, rank, local = dist_setup()
