@@ -23,7 +23,9 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
+        # FP8LIN_ORACLE_LIB: a deliberately broken copy of the oracle, built by the mutation test
+        # (tests/test_oracle_mutations.py) to show that the pins catch it.
+        path = os.environ.get("FP8LIN_ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
