@@ -91,9 +91,6 @@ FP8_DEVI float2 fmul2_rn(float2 a, float2 b) {
   return d;
 }
 
-// bf16 bit pattern -> fp32 (exact).
-FP8_DEVI float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
-
 // Round-to-nearest-even, saturating casts of two fp32 values into two packed FP8 codes;
 // `lo` lands in the low byte (the lower address).
 template <int FMT>
@@ -343,24 +340,15 @@ FP8_DEVI void tma_load_3d_pair(void* dst, const CUtensorMap* m, uint32_t bar_clu
       : "memory");
 }
 
-// 32 lanes x 32 bit, 16 consecutive columns: thread i of the warp receives lane (base + i).
-FP8_DEVI void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
 // 32 lanes x 32 bit, 32 consecutive columns.
 FP8_DEVI void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
                : "r"(taddr));
 }
-FP8_DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-// The same wait, naming the 32 registers of the load it completes as in/out operands: the
-// compiler may not read, move or reuse them between the asynchronous load and this wait.
+// Waits for this thread's tensor-memory loads (tcgen05.wait::ld), naming the 32 registers of the
+// load it completes as in/out operands: the compiler may not read, move or reuse them between the
+// asynchronous load and this wait.
 FP8_DEVI void tmem_ld_wait_regs(uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
