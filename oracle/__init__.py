@@ -51,6 +51,14 @@ def lib():
         L.orc_grouped_gemm_m.argtypes = [P, I, P, I, P, P, P, I64, I64, I64, I64, P, I64, P, P]
         L.orc_grouped_gemm_k.restype = I
         L.orc_grouped_gemm_k.argtypes = [P, I, P, I, P, P, P, I64, I64, I64, I64, P, I64, P, P]
+        L.orc_mx_scale.restype = ctypes.c_uint8
+        L.orc_mx_scale.argtypes = [ctypes.c_float, I]
+        L.orc_e8m0_decode.restype = ctypes.c_double
+        L.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
+        L.orc_mx_quantize_rows.restype = I
+        L.orc_mx_quantize_rows.argtypes = [P, I64, I64, I, P, P]
+        L.orc_gemm_mx.restype = I
+        L.orc_gemm_mx.argtypes = [P, I, P, I, P, P, I64, I64, I64, P, I64, P, P]
         L.orc_num_threads.restype = I
         _lib = L
     return _lib
@@ -235,4 +243,82 @@ def grouped_gemm_k(G, fmtG, X, fmtX, sG, sX, ends, nsel=None):
                                   _p(ns), 0 if ns is None else ns.size, _p(out), _p(absacc))
     if rc:
         raise ValueError("bad segment ends")
+    return out, absacc
+
+
+# ---- MXFP8 (blocks of 32 along the contraction, E8M0 power-of-two scales) ----
+
+MX_BLOCK = 32
+
+
+def mx_scale(amax: float, fmt: int) -> int:
+    """E8M0 code of the shared scale of a block whose largest magnitude is amax."""
+    return int(lib().orc_mx_scale(ctypes.c_float(amax), fmt))
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, np.uint8)
+    return np.array([lib().orc_e8m0_decode(int(v)) for v in c.ravel()], np.float64).reshape(c.shape)
+
+
+def mx_quantize_rows(x_bits, fmt: int):
+    """x [R, C] (C % 32 == 0): blocks of 32 along each row -> codes [R, C], E8M0 [R, C // 32]."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    sc = np.empty((R, C // MX_BLOCK), np.uint8)
+    if lib().orc_mx_quantize_rows(_p(x), R, C, fmt, _p(q), _p(sc)):
+        raise ValueError("the row length must be a multiple of 32")
+    return q, sc
+
+
+def mx_quantize_cols(x_bits, fmt: int):
+    """x [R, C] (R % 32 == 0): blocks of 32 rows down each column, i.e. the row blocks of x^T.
+    Returns the codes of x^T [C, R] (the column-major copy) and E8M0 [C, R // 32]."""
+    return mx_quantize_rows(np.ascontiguousarray(np.asarray(x_bits, np.uint16).T), fmt)
+
+
+def mx_padded_segments(ends, pad: int = 128):
+    """(start, count, padded start) of each segment when every segment is padded to `pad` rows."""
+    ends = np.asarray(ends, np.int64)
+    starts = np.concatenate([[0], ends[:-1]])
+    counts = ends - starts
+    padded = -(-counts // pad) * pad
+    pstarts = np.concatenate([[0], np.cumsum(padded)[:-1]])
+    return starts, counts, pstarts, int(padded.sum())
+
+
+def mx_quantize_jagged_cols(x_bits, ends, fmt: int, pad: int = 128):
+    """x [M, C] with rows in segments ending at `ends`: each segment's rows, padded with zeros to
+    a multiple of `pad`, are laid side by side along the token axis of x^T [C, P]; blocks of 32
+    tokens start at each segment's start. Returns the codes of that padded x^T [C, P] and
+    E8M0 [C, P // 32] (padding blocks are all-zero blocks)."""
+    x = np.asarray(x_bits, np.uint16)
+    M, C = x.shape
+    starts, counts, pstarts, P = mx_padded_segments(ends, pad)
+    if int(counts.sum()) != M or (counts < 0).any():
+        raise ValueError("bad segment ends")
+    xt = np.zeros((C, P), np.uint16)
+    for s, c, ps in zip(starts, counts, pstarts):
+        xt[:, ps:ps + c] = x[s:s + c].T
+    return mx_quantize_rows(xt, fmt)
+
+
+def gemm_mx(A, fmtA, B, fmtB, sA, sB, rows=None):
+    """out[i, n] = sum_k X_A[m, k // 32] X_B[n, k // 32] dec(A[m, k]) dec(B[n, k]); A [M, K],
+    B [N, K] codes, sA [M, K // 32], sB [N, K // 32] E8M0. Returns (out, absacc) in float64."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sA = _c(sA, np.uint8)
+    sB = _c(sB, np.uint8)
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2 and sA.shape == (M, K // MX_BLOCK) and sB.shape == (N, K // MX_BLOCK)
+    r = None if rows is None else _c(rows, np.int64)
+    cnt = M if r is None else r.size
+    out = np.empty((cnt, N), np.float64)
+    absacc = np.empty((cnt, N), np.float64)
+    if lib().orc_gemm_mx(_p(A), fmtA, _p(B), fmtB, _p(sA), _p(sB), M, N, K, _p(r), 0 if r is None else r.size,
+                         _p(out), _p(absacc)):
+        raise ValueError("the contraction length must be a multiple of 32")
     return out, absacc

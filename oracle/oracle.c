@@ -366,6 +366,100 @@ int orc_grouped_gemm_k(const uint8_t* G, int fmtG, const uint8_t* X, int fmtX, c
   return 0;
 }
 
+/* ---------------------------------------------------------------------------------------- */
+/* MXFP8. The pages name it as the fourth scaling granularity, a scale per group stored with the
+ * data ([P1] section "AMD FP8 format in TorchAO"), and as the next step for quantization and the
+ * grouped GEMM ([P1] "Summary and Next Steps"); they fix nothing more. The block, the shared
+ * scale and its rule are taken from the published OCP Microscaling Formats (MX) specification
+ * v1.0 (sections 5.1-5.2 and 6.3):
+ *   - a block is 32 consecutive elements along the contraction dimension;
+ *   - its shared scale is X = 2^(floor(log2(amax)) - emax_elem), emax_elem being the exponent
+ *     of the element format's largest normal (8 for e4m3: 448 = 1.75 * 2^8; 15 for e5m2);
+ *   - X is stored as E8M0: an unsigned biased exponent, bias 127, codes 0..254 for
+ *     2^-127..2^127 and 255 for NaN;
+ *   - each element is x / X cast to the element format, rounding to nearest even and
+ *     saturating at the largest finite value.
+ * An exponent below -127 (an all-zero block, log2(0) = -inf, or amax < 2^-119) is clamped to
+ * -127. A NaN or infinite amax gives the NaN scale. */
+
+static int mx_emax_elem(int fmt) { return fmt == ORC_E4M3 ? 8 : 15; }
+
+uint8_t orc_mx_scale(float amax, int fmt) {
+  if (isnan(amax) || isinf(amax)) return 0xFF;
+  int e = -127;
+  if (amax > 0.0f) {
+    int ex;
+    frexp((double)amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2(amax)) = ex - 1 */
+    e = (ex - 1) - mx_emax_elem(fmt);
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+  }
+  return (uint8_t)(e + 127);
+}
+
+double orc_e8m0_decode(uint8_t code) { return code == 0xFF ? NAN : ldexp(1.0, (int)code - 127); }
+
+int orc_mx_quantize_rows(const uint16_t* x, int64_t R, int64_t C, int fmt, uint8_t* q, uint8_t* sc) {
+  if (C % 32) return -1;
+  const int64_t nb = C / 32;
+  const double fmax8 = orc_fp8_max(fmt);
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint16_t* xb = x + r * C + b * 32;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; ++i) {
+        float a = fabsf(bf16_to_float(xb[i]));
+        if (a > amax || isnan(a)) amax = a;
+      }
+      uint8_t code = orc_mx_scale(amax, fmt);
+      double X = orc_e8m0_decode(code);
+      for (int i = 0; i < 32; ++i) {
+        /* x / X is exact in fp64 (X is a power of two). Its fp32 copy is exact too, except for
+         * magnitudes below 2^-126, far under half the smallest FP8 subnormal, which encode to a
+         * signed zero either way. */
+        double v = (double)bf16_to_float(xb[i]) / X;
+        if (v > fmax8) v = fmax8;
+        if (v < -fmax8) v = -fmax8;
+        q[r * C + b * 32 + i] = orc_fp8_encode((float)v, fmt);
+      }
+      sc[r * nb + b] = code;
+    }
+  }
+  return 0;
+}
+
+/* MX GEMM: out[i, n] = sum_k X_A[m, k / 32] * X_B[n, k / 32] * dec(A[m, k]) * dec(B[n, k]),
+ * m = rows[i] (or i); A [M, K] and B [N, K] row-major codes, sA [M, K / 32] and sB [N, K / 32]
+ * E8M0 codes. Every term is exact in fp64 (a product of two FP8 values and two powers of two);
+ * the sum runs in k order. */
+int orc_gemm_mx(const uint8_t* A, int fmtA, const uint8_t* B, int fmtB, const uint8_t* sA,
+                const uint8_t* sB, int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                int64_t n_rows, double* out, double* absacc) {
+  if (K % 32) return -1;
+  const int64_t nb = K / 32;
+  double ta[256], tb[256], ts[256];
+  decode_table(fmtA, ta);
+  decode_table(fmtB, tb);
+  for (int c = 0; c < 256; ++c) ts[c] = orc_e8m0_decode((uint8_t)c);
+  int64_t cnt = rows ? n_rows : M;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < cnt; ++i) {
+    int64_t m = rows ? rows[i] : i;
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0, aacc = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        double p = ts[sA[m * nb + k / 32]] * ts[sB[n * nb + k / 32]] * (ta[A[m * K + k]] * tb[B[n * K + k]]);
+        acc += p;
+        aacc += fabs(p);
+      }
+      out[i * N + n] = acc;
+      if (absacc) absacc[i * N + n] = aacc;
+    }
+  }
+  return 0;
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

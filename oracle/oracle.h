@@ -14,7 +14,11 @@
  *        section 5 "use_fast_accum".
  *  [P1]  "FP8 training on AMD GPUs with TorchTitan and TorchAO", section "Scaling FP8 to MoE
  *        Architectures" and Figure 3 (grouped GEMM: per-row activation scales,
- *        per-expert-column weight scales, an offsets tensor routing rows to experts).
+ *        per-expert-column weight scales, an offsets tensor routing rows to experts); section
+ *        "AMD FP8 format in TorchAO" (the four granularities, MXFP8 among them) and "Summary
+ *        and Next Steps" (MXFP8 quantization and grouped GEMM as the next step).
+ *  [OCP] OCP Microscaling Formats (MX) Specification v1.0, a published standard outside the
+ *        pages: the MX block of 32, the E8M0 scale and the rule that derives it from amax.
  *
  * Every floating-point step is written out in the order the recipe states. Inputs in bf16
  * are passed as raw uint16 bit patterns; FP8 values as raw uint8 codes.
@@ -93,6 +97,21 @@ int orc_grouped_gemm_k(const uint8_t* G, int fmtG, const uint8_t* X, int fmtX, c
                        const float* sX, const int32_t* ends, int64_t E, int64_t M, int64_t N,
                        int64_t K, const int64_t* nsel, int64_t n_sel, double* out,
                        double* absacc);
+
+/* MXFP8 (OCP Microscaling Formats v1.0; the pages name the format only): the E8M0 scale code
+ * of a 32-element block with this amax, 2^(floor(log2 amax) - emax_elem) clamped below at
+ * 2^-127 (255 = NaN for a NaN or infinite amax); the value of an E8M0 code. */
+uint8_t orc_mx_scale(float amax, int fmt);
+double orc_e8m0_decode(uint8_t code);
+/* Blocks of 32 consecutive elements along each row of x [R, C] (C a multiple of 32): q [R, C]
+ * codes, sc [R, C / 32] E8M0 scale codes. Returns 0, or -1 when C % 32 != 0. */
+int orc_mx_quantize_rows(const uint16_t* x, int64_t R, int64_t C, int fmt, uint8_t* q, uint8_t* sc);
+/* MX GEMM: out[i, n] = sum_k X_A[m, k/32] X_B[n, k/32] dec(A[m, k]) dec(B[n, k]), m = rows[i]
+ * (or i). A [M, K], B [N, K] row-major; sA [M, K/32], sB [N, K/32] E8M0 codes. absacc gets the
+ * sum of the terms' magnitudes. Returns 0, or -1 when K % 32 != 0. */
+int orc_gemm_mx(const uint8_t* A, int fmtA, const uint8_t* B, int fmtB, const uint8_t* sA,
+                const uint8_t* sB, int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                int64_t n_rows, double* out, double* absacc);
 
 /* Number of OpenMP threads the oracle runs on. */
 int orc_num_threads(void);

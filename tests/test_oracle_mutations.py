@@ -1,9 +1,11 @@
 """The pins have teeth: each plausible mistake below is planted in a copy of the oracle (the C
-source, on the CPU), the copy is compiled, and the oracle's pin tests (tests/test_oracle.py) are
-run against it in a subprocess; every mutant must make at least one pin fail. The mistakes cover
+source, on the CPU), the copy is compiled, and the oracle's pin tests (tests/test_oracle.py and
+tests/test_oracle_mx.py) are run against it in a subprocess; every mutant must make at least
+one pin fail. The mistakes cover
 each step of the recipe and of the GEMMs: rounding ties, the subnormal binade, the eps clamp,
 the direction of the scale, the inverse scale's rounding, a dropped product in the contraction,
-a segment boundary, the column of a transposed operand."""
+a segment boundary, the column of a transposed operand; for MXFP8 the scale rule's exponent,
+floor and clamp, the block amax, and the block index of a scale in the GEMM."""
 import os
 import re
 import subprocess
@@ -33,6 +35,16 @@ MUTANTS = {
                      "int64_t r0 = e ? ends[e - 1] + 1 : 0, r1 = ends[e];\n    if (r0 > r1) r0 = r1;\n    /* an empty segment"),
     # B read with A's column stride (a transposed-operand mix-up)
     "operand_stride": ("tb[B[n * b_sn + k * b_sk]]", "tb[B[n * b_sn + k * a_sk]]"),
+    # MX: e4m3's largest-normal exponent off by one
+    "mx_emax": ("return fmt == ORC_E4M3 ? 8 : 15;", "return fmt == ORC_E4M3 ? 7 : 15;"),
+    # MX: ceil(log2 amax) where the rule takes the floor
+    "mx_ceil_log2": ("e = (ex - 1) - mx_emax_elem(fmt);", "e = ex - mx_emax_elem(fmt);"),
+    # MX: no clamp of the scale exponent at -127
+    "mx_no_clamp": ("if (e < -127) e = -127;\n    if (e > 127)", "if (e > 127)"),
+    # MX: block amax taken over signed values, not magnitudes
+    "mx_signed_amax": ("float a = fabsf(bf16_to_float(xb[i]));", "float a = bf16_to_float(xb[i]);"),
+    # MX GEMM: B's first block scale used for every block
+    "mx_block_index": ("ts[sB[n * nb + k / 32]]", "ts[sB[n * nb]]"),
 }
 
 
@@ -52,8 +64,9 @@ def _build_mutant(name, tmp_path):
 
 def _run_pins(so):
     env = dict(os.environ, FP8LIN_ORACLE_LIB=str(so))
-    return subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle.py"), "-x", "-q",
-                           "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle.py"),
+                           os.path.join(ROOT, "tests", "test_oracle_mx.py"), "-x", "-q", "-p", "no:cacheprovider"],
+                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
 
 
 def test_unchanged_copy_passes(tmp_path):
