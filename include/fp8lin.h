@@ -21,6 +21,13 @@
  *       quantization (no intermediate tensors in HBM), the column-wise variant that writes a
  *       column-major output through on-chip staging (no separate transpose copy), and the
  *       dual output (row- and column-major from one read).
+ *  [MX] same page, section "AMD FP8 format in TorchAO" (MXFP8: a scale per group stored with the
+ *       data) and "Summary and Next Steps" (MXFP8 quantization and grouped GEMM next). The pages
+ *       give no more; block, scale and rule are those of the OCP Microscaling Formats (MX)
+ *       specification v1.0: blocks of 32 consecutive elements along the contraction dimension,
+ *       one E8M0 scale X = 2^(floor(log2(amax)) - emax_elem) per block (emax_elem 8 for e4m3,
+ *       15 for e5m2; exponent clamped below at -127), elements x / X cast round-to-nearest-even
+ *       with saturation. The GEMM computes sum_k X_A[m, k/32] X_B[n, k/32] A[m, k] B[n, k].
  *
  * Conventions for every entry point:
  *  - Tensors are described by fp8_tensor: a DEVICE pointer (global memory, 16-byte aligned),
@@ -56,11 +63,24 @@ enum {
   FP8_DT_F32 = 2,
   FP8_DT_E4M3 = 3, /* OCP float8 e4m3fn: bias 7, no Inf, max 448 */
   FP8_DT_E5M2 = 4, /* OCP float8 e5m2: bias 15, max 57344 */
-  FP8_DT_I32 = 5
+  FP8_DT_I32 = 5,
+  FP8_DT_E8M0 = 6  /* OCP E8M0 scale codes (MX): 2^(code - 127), 0xFF = NaN; one byte each */
 };
 
 /* scale granularity */
-enum { FP8_GRAN_TENSOR = 0, FP8_GRAN_ROW = 1, FP8_GRAN_COL = 2 };
+enum { FP8_GRAN_TENSOR = 0, FP8_GRAN_ROW = 1, FP8_GRAN_COL = 2, FP8_GRAN_MX = 3 };
+
+/*
+ * MX scale layout (FP8_GRAN_MX; [MX]). An MX operand with R rows (its non-contraction index) and
+ * contraction length K (K % 128 == 0) carries E8M0 codes for blocks of 32 along K, stored in
+ * 512-byte blocks [ceil(R / 128)][K / 128][512]; inside a block the code of row r, K block j
+ * (elements 32 j .. 32 j + 31) is at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + (j % 4). This is
+ * the order in which the tensor cores' block-scaled MMA reads scales from tensor memory, so the
+ * GEMM copies each block unchanged. Rows past R in the last 128-row block are never read for
+ * results. Bytes: fp8_mx_scale_bytes(R, K). Batched operands ([B, R, K]) repeat the layout per
+ * batch entry. With segment offsets, rows are placed in the segment-padded row space (segment e
+ * at padded rows pstart_e = sum_{j<e} roundup(count_j, 128)), P rows in all.
+ */
 
 /* output layouts of fp8_quantize (bit mask) */
 enum { FP8_LAYOUT_ROW_MAJOR = 1, FP8_LAYOUT_COL_MAJOR = 2, FP8_LAYOUT_BOTH = 3 };
@@ -114,6 +134,14 @@ typedef struct fp8_tensor {
  *  x           bf16 [R, C], or [B, R, C] for a batch of matrices (e.g. MoE expert weights).
  *              C % 8 == 0 (16-byte rows).
  *  granularity FP8_GRAN_TENSOR: one scale for all of x.
+ *              FP8_GRAN_MX:     MXFP8 ([MX]): one E8M0 scale per 32 elements; C % 128 == 0.
+ *                               ROW_MAJOR: blocks along rows, `out` in x's shape, scales over
+ *                               (rows R, contraction C). COL_MAJOR: blocks down columns (R % 128
+ *                               == 0 without offsets), `out_t` [C, R] ([B, C, R]), scales over
+ *                               (rows C, contraction R). BOTH: both from one read.
+ *                               With `offsets` (2-D x): segments padded to 128 rows; `out_t` is
+ *                               [C, P] as for COL granularity and the row-major scales use the
+ *                               padded row space, P % 128 == 0, P >= R + 127 E.
  *              FP8_GRAN_ROW:    one scale per row (amax over the C entries of the row);
  *                               a 3-D x is treated as [B*R, C].
  *              FP8_GRAN_COL:    one scale per column (amax over the R rows of the column), per
@@ -131,13 +159,18 @@ typedef struct fp8_tensor {
  *              FP8_LAYOUT_BOTH: both (tensor granularity only: one read, two outputs).
  *              ROW granularity supports ROW_MAJOR; COL granularity supports COL_MAJOR.
  *  inv_scales  fp32: [1] (tensor), [R] or [B*R] (row), [C], [B, C] or [E, C] (col).
+ *              MX: E8M0 bytes in the MX scale layout: ROW_MAJOR B * fp8_mx_scale_bytes(R, C)
+ *              (with offsets fp8_mx_scale_bytes(P, C)); COL_MAJOR B * fp8_mx_scale_bytes(C, R)
+ *              (with offsets fp8_mx_scale_bytes(C, P)); BOTH the row-major scales followed by
+ *              the column-major ones.
  *  offsets     NULL, or int32 [E] cumulative segment ends (COL granularity, 2-D x only).
  *              Checked on the device: a bad vector sets FP8_DEV_BAD_OFFSETS.
  *  workspace   device memory, 16-byte aligned, of fp8_workspace_size(FP8_OP_QUANTIZE, groups,
  *              C, granularity) bytes: 4 bytes for tensor granularity (the amax word); for
  *              column granularity 4 bytes per (group, column) for the column maxima, rounded
  *              up to 16 bytes (groups = B for 3-D x, E with offsets, else 1); 0 for row
- *              granularity (workspace may then be NULL). Calls sharing a workspace must be
+ *              granularity (workspace may then be NULL). MX: 4 * (E + 1) bytes rounded up to
+ *              16 with offsets (the padded segment starts), else 0. Calls sharing a workspace must be
  *              stream-ordered: the quantize clears and uses it.
  * Bit-exactness: codes and inverse scales equal the recipe evaluated with an fp64 division,
  * an fp32 multiply and a round-to-nearest-even saturating cast (eps = 1e-12).
@@ -157,6 +190,11 @@ int fp8_quantize(const fp8_tensor* x, int granularity, int out_dtype, int layout
  *  out  bf16 or fp32 [M, N]. Accumulation is fp32 in tensor memory; the dequantization
  *       sA[m] * sB[n] is applied once in the epilogue, followed by one rounding to out's type.
  *  K * element size must be a multiple of 16 bytes; M and N are arbitrary (>= 1).
+ *  MX ([MX]): sA and sB of dtype FP8_DT_E8M0 select the block-scaled GEMM,
+ *       out[m, n] = sum_k X_A[m, k/32] X_B[n, k/32] A[m, k] B[n, k], with A, B FP8 K-major,
+ *       sA fp8_mx_scale_bytes(M, K) bytes and sB fp8_mx_scale_bytes(N, K) bytes in the MX scale
+ *       layout, K % 128 == 0. The block scales are applied inside the tensor-core MMA
+ *       (tcgen05.mma block_scale); the epilogue only rounds.
  */
 int fp8_scaled_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA,
                   const fp8_tensor* sB, fp8_tensor* out, int flags, int32_t* d_status,
@@ -176,6 +214,11 @@ int fp8_scaled_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA
  *   A = G^T and B = X^T in the segment-padded column-major layout written by fp8_quantize
  *   (COL granularity with offsets): A FP8 [N, P], B FP8 [K, P]; sA fp32 [E, N]; sB fp32 [E, K];
  *   out bf16/fp32 [E, N, K]. An empty segment gives out[e] = 0.
+ * MX ([MX]; sA, sB of dtype FP8_DT_E8M0, K % 128 == 0, scales in the MX scale layout):
+ *   JAGGED_M: sA = the segment-padded row-major scales of A (fp8_quantize MX ROW_MAJOR with
+ *   offsets; P = 32 * bytes / K rows, P % 128 == 0, P >= M + 127 E); sB = E * fp8_mx_scale_bytes(N,
+ *   K) bytes. JAGGED_K: A = G^T [N, P] and B = X^T [K, P] from fp8_quantize MX COL_MAJOR with
+ *   offsets; sA = fp8_mx_scale_bytes(N, P), sB = fp8_mx_scale_bytes(K, P) bytes.
  */
 int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* offsets,
                    const fp8_tensor* sA, const fp8_tensor* sB, fp8_tensor* out, int mode,
@@ -264,6 +307,10 @@ size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granul
  * L2 lines; a P that is only a multiple of 16 is accepted but makes each 128-byte row chunk
  * straddle two lines). Returns -1 for negative arguments. */
 int64_t fp8_jagged_padded_rows(int64_t rows, int64_t n_segments);
+
+/* Bytes of the MX scales of an operand with `rows` rows and contraction length k (see the MX
+ * scale layout): ceil(rows / 128) * 128 * k / 32. Returns -1 unless rows >= 0 and k % 128 == 0. */
+int64_t fp8_mx_scale_bytes(int64_t rows, int64_t k);
 
 /* Text for an FP8_ERR_* return code or an FP8_DEV_* status word. */
 const char* fp8_status_string(int code);

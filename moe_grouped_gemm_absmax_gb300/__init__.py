@@ -19,8 +19,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libfp8lin.so")
 
 # enums of include/fp8lin.h
-DT_BF16, DT_F32, DT_E4M3, DT_E5M2, DT_I32 = 1, 2, 3, 4, 5
-GRAN_TENSOR, GRAN_ROW, GRAN_COL = 0, 1, 2
+DT_BF16, DT_F32, DT_E4M3, DT_E5M2, DT_I32, DT_E8M0 = 1, 2, 3, 4, 5, 6
+GRAN_TENSOR, GRAN_ROW, GRAN_COL, GRAN_MX = 0, 1, 2, 3
 LAYOUT_ROW_MAJOR, LAYOUT_COL_MAJOR, LAYOUT_BOTH = 1, 2, 3
 MM_FAST_ACCUM, MM_A_MN_MAJOR, MM_B_MN_MAJOR = 1, 2, 4
 GROUPED_JAGGED_M, GROUPED_JAGGED_K = 0, 1
@@ -36,6 +36,7 @@ _TORCH_DT = {
     torch.float8_e4m3fn: DT_E4M3,
     torch.float8_e5m2: DT_E5M2,
     torch.int32: DT_I32,
+    torch.uint8: DT_E8M0,  # MX scale codes travel as raw bytes
 }
 FP8_TORCH = {DT_E4M3: torch.float8_e4m3fn, DT_E5M2: torch.float8_e5m2}
 
@@ -73,6 +74,8 @@ def _load():
     L.fp8_workspace_size.restype = ctypes.c_size_t
     L.fp8_jagged_padded_rows.argtypes = [ctypes.c_int64, ctypes.c_int64]
     L.fp8_jagged_padded_rows.restype = ctypes.c_int64
+    L.fp8_mx_scale_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    L.fp8_mx_scale_bytes.restype = ctypes.c_int64
     L.fp8_status_string.argtypes = [ctypes.c_int]
     L.fp8_status_string.restype = ctypes.c_char_p
     L.fp8_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -88,7 +91,7 @@ lib = _load()
 # Symbols include/fp8lin.h declares (checked by the CPU tests against the header and the .so).
 EXPORTS = ("fp8_quantize", "fp8_scaled_mm", "fp8_grouped_mm", "fp8_linear_fwd", "fp8_linear_bwd",
            "fp8_workspace_size", "fp8_jagged_padded_rows", "fp8_status_string", "fp8_set_wait_limit_ns",
-           "fp8_quantize_tensor_noalloc", "fp8_set_test_stall")
+           "fp8_quantize_tensor_noalloc", "fp8_set_test_stall", "fp8_mx_scale_bytes")
 
 
 def status_string(code: int) -> str:
@@ -194,6 +197,10 @@ def fp8_jagged_padded_rows(rows: int, n_segments: int) -> int:
     return int(lib.fp8_jagged_padded_rows(rows, n_segments))
 
 
+def fp8_mx_scale_bytes(rows: int, k: int) -> int:
+    return int(lib.fp8_mx_scale_bytes(rows, k))
+
+
 def fp8_set_wait_limit_ns(ns: int) -> int:
     return int(lib.fp8_set_wait_limit_ns(ns))
 
@@ -244,3 +251,34 @@ def quantize_alloc(x, granularity, out_dtype, layout=None, offsets=None, padded_
         ws = col_workspace(groups, C, dev)
     fp8_quantize(x, granularity, out_dtype, layout, out, out_t, inv, offsets, ws, status=status, stream=stream)
     return out, out_t, inv
+
+
+def mx_quantize_alloc(x, out_dtype, layout=LAYOUT_ROW_MAJOR, offsets=None, padded_rows=None, status=None,
+                      stream=None):
+    """MXFP8 quantize (blocks of 32, E8M0 scales). Returns (out or None, out_t or None,
+    row-major scales or None, column-major scales or None); scales are uint8 tensors in the MX
+    scale layout of include/fp8lin.h."""
+    dev = x.device
+    fdt = FP8_TORCH[out_dtype]
+    R, C = x.shape[-2], x.shape[-1]
+    B = x.shape[0] if x.dim() == 3 else 1
+    out = torch.empty(x.shape, dtype=fdt, device=dev) if layout & LAYOUT_ROW_MAJOR else None
+    ws = None
+    if offsets is not None:
+        E = offsets.numel()
+        P = padded_rows or fp8_jagged_padded_rows(R, E)
+        out_t = torch.empty((C, P), dtype=fdt, device=dev) if layout & LAYOUT_COL_MAJOR else None
+        row_bytes = fp8_mx_scale_bytes(P, C) if layout & LAYOUT_ROW_MAJOR else 0
+        col_bytes = fp8_mx_scale_bytes(C, P) if layout & LAYOUT_COL_MAJOR else 0
+        ws = torch.empty(max(fp8_workspace_size(OP_QUANTIZE, E, C, granularity=GRAN_MX) // 4, 4), dtype=torch.int32,
+                         device=dev)
+    else:
+        out_t = None
+        if layout & LAYOUT_COL_MAJOR:
+            out_t = torch.empty((B, C, R) if x.dim() == 3 else (C, R), dtype=fdt, device=dev)
+        row_bytes = B * fp8_mx_scale_bytes(R, C) if layout & LAYOUT_ROW_MAJOR else 0
+        col_bytes = B * fp8_mx_scale_bytes(C, R) if layout & LAYOUT_COL_MAJOR else 0
+    row_bytes, col_bytes = max(row_bytes, 0), max(col_bytes, 0)  # bad shapes: the library rejects them
+    sf = torch.empty(row_bytes + col_bytes, dtype=torch.uint8, device=dev)
+    fp8_quantize(x, GRAN_MX, out_dtype, layout, out, out_t, sf, offsets, ws, status=status, stream=stream)
+    return out, out_t, (sf[:row_bytes] if row_bytes else None), (sf[row_bytes:] if col_bytes else None)

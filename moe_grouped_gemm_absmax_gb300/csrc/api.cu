@@ -148,6 +148,8 @@ static int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
 // ------------------------------------------------------------------------------------------
 
+extern "C" int64_t fp8_mx_scale_bytes(int64_t rows, int64_t k) { return mx_scale_bytes(rows, k); }
+
 extern "C" int64_t fp8_jagged_padded_rows(int64_t rows, int64_t n_segments) {
   if (rows < 0 || n_segments < 0) return -1;
   return round_up(rows + 127 * n_segments, 128);
@@ -182,7 +184,7 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
   FP8_CHECK(valid_desc(x) && x->dtype == FP8_DT_BF16 && (x->ndim == 2 || x->ndim == 3), FP8_ERR_INVALID_ARG);
   FP8_CHECK(is_fp8(out_dtype), FP8_ERR_INVALID_ARG);
   FP8_CHECK(layout >= 1 && layout <= 3, FP8_ERR_INVALID_ARG);
-  FP8_CHECK(valid_desc(inv) && inv->dtype == FP8_DT_F32, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(valid_desc(inv) && inv->dtype == (gran == FP8_GRAN_MX ? FP8_DT_E8M0 : FP8_DT_F32), FP8_ERR_INVALID_ARG);
   const int nd = x->ndim;
   const int64_t B = nd == 3 ? x->shape[0] : 1, R = x->shape[nd - 2], C = x->shape[nd - 1];
   FP8_CHECK(C % 8 == 0 && aligned16(x->ptr), FP8_ERR_ALIGNMENT);
@@ -246,6 +248,39 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
       return launch_quant_cols(x->ptr, B * R, C, B, R, nullptr, out_dtype, out_t->ptr, R,
                                static_cast<float*>(inv->ptr), scratch, c);
     }
+    case FP8_GRAN_MX: {
+      FP8_CHECK(C % 128 == 0, FP8_ERR_UNSUPPORTED);
+      uint8_t* sf = static_cast<uint8_t*>(inv->ptr);
+      if (offsets) {
+        FP8_CHECK(nd == 2, FP8_ERR_UNSUPPORTED);
+        FP8_CHECK(valid_desc(offsets) && offsets->dtype == FP8_DT_I32 && offsets->ndim == 1 && offsets->shape[0] >= 1,
+                  FP8_ERR_INVALID_ARG);
+        const int64_t E = offsets->shape[0];
+        // the padded row count: from out_t, else from the size of the row-major scales
+        const int64_t P = want_col ? (out_t->ndim == 2 ? out_t->shape[1] : -1) : numel(inv) * 32 / C;
+        FP8_CHECK(P >= R + 127 * E && P % 128 == 0, FP8_ERR_INVALID_ARG);
+        if (want_col) FP8_CHECK(shape_is(out_t, 2, C, P), FP8_ERR_INVALID_ARG);
+        const int64_t row_bytes = want_row ? mx_scale_bytes(P, C) : 0, col_bytes = want_col ? mx_scale_bytes(C, P) : 0;
+        FP8_CHECK(numel(inv) == row_bytes + col_bytes, FP8_ERR_INVALID_ARG);
+        FP8_CHECK(ws && (reinterpret_cast<uintptr_t>(ws) & 15u) == 0 && ws_bytes >= (size_t)round_up(4 * (E + 1), 16),
+                  FP8_ERR_WORKSPACE);
+        return launch_mx_quant(x->ptr, 1, R, C, out_dtype, want_row ? out->ptr : nullptr, sf,
+                               want_col ? out_t->ptr : nullptr, P, sf + row_bytes,
+                               static_cast<const int32_t*>(offsets->ptr), E, static_cast<int32_t*>(ws), c);
+      }
+      if (want_col) {
+        FP8_CHECK(R % 128 == 0, FP8_ERR_UNSUPPORTED);
+        if (nd == 2)
+          FP8_CHECK(shape_is(out_t, 2, C, R), FP8_ERR_INVALID_ARG);
+        else
+          FP8_CHECK(shape_is(out_t, 3, B, C, R), FP8_ERR_INVALID_ARG);
+      }
+      const int64_t row_bytes = want_row ? B * mx_scale_bytes(R, C) : 0;
+      const int64_t col_bytes = want_col ? B * mx_scale_bytes(C, R) : 0;
+      FP8_CHECK(numel(inv) == row_bytes + col_bytes, FP8_ERR_INVALID_ARG);
+      return launch_mx_quant(x->ptr, B, R, C, out_dtype, want_row ? out->ptr : nullptr, sf,
+                             want_col ? out_t->ptr : nullptr, R, sf + row_bytes, nullptr, 0, nullptr, c);
+    }
     default:
       return FP8_ERR_INVALID_ARG;
   }
@@ -300,8 +335,32 @@ static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_te
     const int64_t M = A->shape[0], K = A->shape[1], N = B->shape[0];
     FP8_CHECK(B->shape[1] == K && shape_is(out, 2, M, N), FP8_ERR_INVALID_ARG);
     FP8_CHECK(K % 16 == 0, FP8_ERR_ALIGNMENT);
-    FP8_CHECK(valid_desc(sA) && valid_desc(sB) && sA->dtype == FP8_DT_F32 && sB->dtype == FP8_DT_F32,
-              FP8_ERR_INVALID_ARG);
+    FP8_CHECK(valid_desc(sA) && valid_desc(sB), FP8_ERR_INVALID_ARG);
+    if (sA->dtype == FP8_DT_E8M0 || sB->dtype == FP8_DT_E8M0) {  // MX block scales
+      FP8_CHECK(sA->dtype == FP8_DT_E8M0 && sB->dtype == FP8_DT_E8M0, FP8_ERR_INVALID_ARG);
+      FP8_CHECK(K % 128 == 0, FP8_ERR_UNSUPPORTED);
+      FP8_CHECK(numel(sA) == mx_scale_bytes(M, K) && numel(sB) == mx_scale_bytes(N, K), FP8_ERR_INVALID_ARG);
+      FP8_CHECK(aligned16(sA->ptr) && aligned16(sB->ptr), FP8_ERR_ALIGNMENT);
+      FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
+      if (M == 0 || N == 0) return FP8_OK;
+      GemmArgs g = {};
+      g.A = A->ptr;
+      g.B = B->ptr;
+      g.a_dtype = A->dtype;
+      g.b_dtype = B->dtype;
+      g.out = out->ptr;
+      g.out_dtype = out->dtype;
+      g.M = M;
+      g.N = N;
+      g.K = K;
+      g.mode = -1;
+      g.mx = 1;
+      g.sfa = sA->ptr;
+      g.sfb = sB->ptr;
+      g.sfa_rows = M;
+      return launch_gemm(g, c);
+    }
+    FP8_CHECK(sA->dtype == FP8_DT_F32 && sB->dtype == FP8_DT_F32, FP8_ERR_INVALID_ARG);
     const int64_t la = numel(sA), lb = numel(sB);
     FP8_CHECK((la == 1 || la == M) && (lb == 1 || lb == N), FP8_ERR_INVALID_ARG);
     FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
@@ -343,8 +402,10 @@ extern "C" int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp
   FP8_CHECK(is_fp8(A->dtype) && is_fp8(B->dtype) && is_out(out->dtype), FP8_ERR_INVALID_ARG);
   FP8_CHECK(!(A->dtype == FP8_DT_E5M2 && B->dtype == FP8_DT_E5M2), FP8_ERR_UNSUPPORTED);
   FP8_CHECK(offsets->dtype == FP8_DT_I32 && offsets->ndim == 1 && offsets->shape[0] >= 1, FP8_ERR_INVALID_ARG);
-  FP8_CHECK(sA->dtype == FP8_DT_F32 && sB->dtype == FP8_DT_F32, FP8_ERR_INVALID_ARG);
+  const bool mx = sA->dtype == FP8_DT_E8M0;
+  FP8_CHECK(mx ? sB->dtype == FP8_DT_E8M0 : (sA->dtype == FP8_DT_F32 && sB->dtype == FP8_DT_F32), FP8_ERR_INVALID_ARG);
   FP8_CHECK(aligned16(A->ptr) && aligned16(B->ptr) && aligned16(out->ptr), FP8_ERR_ALIGNMENT);
+  if (mx) FP8_CHECK(aligned16(sA->ptr) && aligned16(sB->ptr), FP8_ERR_ALIGNMENT);
   const int64_t E = offsets->shape[0];
   GemmArgs g = {};
   g.A = A->ptr;
@@ -358,10 +419,30 @@ extern "C" int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp
   g.mode = mode;
   g.ends = static_cast<const int32_t*>(offsets->ptr);
   g.E = E;
+  if (mx) {
+    g.mx = 1;
+    g.sfa = sA->ptr;
+    g.sfb = sB->ptr;
+    g.sA = nullptr;
+    g.sB = nullptr;
+  }
   if (mode == FP8_GROUPED_JAGGED_M) {
     FP8_CHECK(A->ndim == 2 && B->ndim == 3 && B->shape[0] == E, FP8_ERR_INVALID_ARG);
     const int64_t M = A->shape[0], K = A->shape[1], N = B->shape[1];
     FP8_CHECK(B->shape[2] == K && shape_is(out, 2, M, N), FP8_ERR_INVALID_ARG);
+    if (mx) {
+      FP8_CHECK(K % 128 == 0, FP8_ERR_UNSUPPORTED);
+      const int64_t P = numel(sA) * 32 / K;  // the segment-padded rows of A's scales
+      FP8_CHECK(numel(sA) == mx_scale_bytes(P, K) && P % 128 == 0 && P >= M + 127 * E, FP8_ERR_INVALID_ARG);
+      FP8_CHECK(numel(sB) == E * mx_scale_bytes(N, K), FP8_ERR_INVALID_ARG);
+      FP8_CHECK(M < (int64_t(1) << 31) && E * N < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
+      g.M = M;
+      g.N = N;
+      g.K = K;
+      g.sfa_rows = P;
+      if (M == 0 || N == 0) return FP8_OK;
+      return launch_gemm(g, c);
+    }
     FP8_CHECK(numel(sA) == M && numel(sB) == E * N, FP8_ERR_INVALID_ARG);
     FP8_CHECK(K % 16 == 0, FP8_ERR_ALIGNMENT);
     FP8_CHECK(M < (int64_t(1) << 31) && E * N < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
@@ -377,6 +458,17 @@ extern "C" int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp
     FP8_CHECK(A->ndim == 2 && B->ndim == 2 && A->shape[1] == B->shape[1], FP8_ERR_INVALID_ARG);
     const int64_t N = A->shape[0], Kd = B->shape[0], P = A->shape[1];
     FP8_CHECK(shape_is(out, 3, E, N, Kd), FP8_ERR_INVALID_ARG);
+    if (mx) {
+      FP8_CHECK(P % 128 == 0, FP8_ERR_UNSUPPORTED);
+      FP8_CHECK(numel(sA) == mx_scale_bytes(N, P) && numel(sB) == mx_scale_bytes(Kd, P), FP8_ERR_INVALID_ARG);
+      g.M = N;
+      g.N = Kd;
+      g.K = P;
+      g.k_dim = Kd;
+      g.sfa_rows = N;
+      if (N == 0 || Kd == 0) return FP8_OK;
+      return launch_gemm(g, c);
+    }
     FP8_CHECK(numel(sA) == E * N && numel(sB) == E * Kd, FP8_ERR_INVALID_ARG);
     FP8_CHECK(P % 16 == 0, FP8_ERR_ALIGNMENT);
     g.M = N;
@@ -442,8 +534,9 @@ static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad
 
 extern "C" size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granularity, int wgrad_mode) {
   switch (op) {
-    case FP8_OP_QUANTIZE:  // (d0, d1) = (groups, columns) for FP8_GRAN_COL
+    case FP8_OP_QUANTIZE:  // (d0, d1) = (groups, columns) for FP8_GRAN_COL; (segments, -) for MX
       if (granularity == FP8_GRAN_TENSOR) return 4;
+      if (granularity == FP8_GRAN_MX) return d0 > 0 ? (size_t)round_up(4 * (d0 + 1), 16) : 0;
       if (granularity == FP8_GRAN_COL) return (size_t)col_ws_words(d0 > 0 ? d0 : 1, d1 > 0 ? d1 : 0) * 4;
       return 0;
     case FP8_OP_LINEAR_FWD:

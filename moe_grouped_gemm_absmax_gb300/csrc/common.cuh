@@ -211,6 +211,14 @@ FP8_DEVI void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+FP8_DEVI void tma_load_4d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x, int32_t y, int32_t z,
+                          int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
 
 // TMA bulk-tensor stores shared -> global, tracked per thread in bulk async-groups.
 FP8_DEVI void tma_store_2d(const CUtensorMap* m, const void* src, int32_t x, int32_t y) {
@@ -340,6 +348,53 @@ FP8_DEVI void tma_load_3d_pair(void* dst, const CUtensorMap* m, uint32_t bar_clu
       : "memory");
 }
 
+FP8_DEVI void tma_load_4d_pair(void* dst, const CUtensorMap* m, uint32_t bar_cluster_addr, int32_t x, int32_t y,
+                               int32_t z, int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster_addr), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
+// ---- MX block scaling: E8M0 scale factors in tensor memory ----
+// tcgen05.mma.kind::mxf8f6f4.block_scale.scale_vec::1X: one E8M0 scale per row per 32 K
+// elements (one MMA of K = 32). Scale factors live in tensor memory; a column of 32-bit words
+// holds four consecutive K-block scales per lane and the instruction descriptor picks the byte
+// (scale-factor id = K block % 4). Rows of A (and of B) map to tensor memory as row % 32 -> lane
+// (in each of the four lane quarters), row / 32 -> column. tcgen05.cp .32x128b.warpx4 copies a
+// 512-byte shared-memory block [32 lanes][4 columns][4 bytes] into that layout, repeated in the
+// four lane quarters.
+FP8_DEVI void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
+                      uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+FP8_DEVI void umma_mx_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa_tmem,
+                           uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// shared memory -> tensor memory, 32 rows x 128 bits, repeated in the four lane quarters.
+// Issued by the MMA thread; tcgen05.mma issued after it by the same thread sees the copy.
+FP8_DEVI void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// CTA pairs: each CTA's shared memory into its own tensor memory, issued by the even CTA.
+FP8_DEVI void tmem_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // 32 lanes x 32 bit, 32 consecutive columns.
 FP8_DEVI void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -387,6 +442,26 @@ FP8_DEVI uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_byt
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// Shared-memory descriptor without swizzle for the scale-factor copies: 8-row x 16-byte core
+// matrices, rows 16 bytes apart, core matrices `sbo_bytes` apart along the rows.
+FP8_DEVI uint64_t smem_desc_plain(uint32_t saddr, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: operand formats, K-major A and
+// B, N >> 3 at bit 17, E8M0 scales (bit 23), M >> 4 at bit 24. The scale-factor ids (which byte
+// of the scale column an MMA uses) go in bits 4-5 (B) and 29-30 (A), added per MMA.
+__host__ __device__ constexpr uint32_t make_idesc_mx(uint32_t a_fmt, uint32_t b_fmt, uint32_t M, uint32_t N) {
+  return (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+FP8_DEVI uint32_t idesc_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
+  return idesc | (b_id << 4) | (a_id << 29);
 }
 
 // Instruction descriptor for kind::f16 / kind::f8f6f4: fp32 accumulator, operand formats,

@@ -36,10 +36,8 @@ namespace fp8lin {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BKB = 128;  // rows per CTA, tile columns, K bytes per stage
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;  // warps 2..9
-constexpr int kTmemCols = 2 * BN;
+constexpr int BM = 128, BN = 256, BKB = 128;  // rows per CTA, tile columns (FP8 / BF16), K bytes per stage
+constexpr int kTmemCols = 512;
 constexpr int kMaxExperts = 2048;
 constexpr int kGroupM = 16;  // rasterization: tiles walk 16 M-blocks per N-block
 constexpr int kStageOut = 4096;  // per epilogue warp: output staging for TMA stores (pairs)
@@ -48,20 +46,33 @@ constexpr int kStageOut = 4096;  // per epilogue warp: output staging for TMA st
 // under running hardware.
 constexpr uint64_t kDrainNs = 2000000000ull;
 
-template <int CG>
-struct Cfg {
-  static constexpr int A_BYTES = BM * BKB;              // this CTA's 128 rows of A
-  static constexpr int B_ROWS = BN / CG;                // this CTA's rows of B
-  static constexpr int B_BYTES = B_ROWS * BKB;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB or 32 KB
-  static constexpr int STAGES = CG == 2 ? 5 : 4;
-  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;  // 160 KB or 192 KB
-  static constexpr int OUT_BYTES = CG == 2 ? 8 * kStageOut : 0;
-  static constexpr int TILE_M = BM * CG;
-};
-
 enum { kDense = 0, kJagM = 1, kJagK = 2 };
-enum { kFP8 = 0, kBF16 = 1 };
+enum { kFP8 = 0, kBF16 = 1, kMX = 2 };
+
+// MX (block-scaled) tiles are 192 columns wide: two accumulators (384 tensor-memory columns)
+// leave room for one scale-factor slot per ring stage. 192 = 6 groups of 32 columns, so a
+// tile's first column group sits at offset 0 or 2 inside a 4-group (128-row) scale block.
+// Twelve epilogue warps (three per lane quarter) take 64 columns each.
+template <int KIND, int CG>
+struct Cfg {
+  static constexpr int TBN = KIND == kMX ? 192 : BN;     // tile columns
+  static constexpr int EPI_WARPS = KIND == kMX ? 12 : 8;
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int WCOLS = TBN * 4 / EPI_WARPS;      // columns per epilogue warp: 128 or 64
+  static constexpr int A_BYTES = BM * BKB;               // this CTA's 128 rows of A
+  static constexpr int B_ROWS = TBN / CG;                // this CTA's rows of B
+  static constexpr int B_BYTES = B_ROWS * BKB;
+  static constexpr int SF_BYTES = KIND == kMX ? 3 * 512 : 0;  // one A scale block, two B scale blocks
+  static constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_BYTES;  // bytes the loads of a stage deliver
+  static constexpr int STAGE_BYTES = (TX_BYTES + 1023) / 1024 * 1024;
+  static constexpr int STAGES = CG == 2 ? 5 : 4;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int OUT_BYTES = CG == 2 ? EPI_WARPS * kStageOut : 0;
+  static constexpr int TILE_M = BM * CG;
+  static constexpr int SF_COL0 = 2 * TBN;                // first scale-factor slot (16 columns each)
+};
+static_assert(2 * 192 + 16 * 5 <= kTmemCols, "MX tensor-memory budget");
 
 struct GemmParams {
   int64_t M, N, K;     // tile space: rows of D, columns of D, contraction length (elements)
@@ -86,6 +97,7 @@ struct GemmParams {
 
 struct Tile {
   int64_t m0, n0;   // first row / column of the (pair's) tile of D
+  int64_t pm0;      // m0 in the segment-padded row space of the MX A scales (jagged M), else m0
   int64_t row_end;  // rows >= row_end are masked (segment end, or M)
   int64_t k0;       // first contraction coordinate
   int64_t nkb;      // K blocks
@@ -119,8 +131,9 @@ FP8_DEVI int find_expert(const int32_t* tpre, int E, int64_t t) {
 // Tile t of the persistent schedule. Tile indices, tile counts and block coordinates fit in 32
 // bits (the launcher checks), so the divisions here are 32-bit: they sit on the MMA issuer's and
 // the epilogue's per-tile path.
-template <int SCHED, int TILE_M>
-FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, const int32_t* aux) {
+template <int SCHED, int TILE_M, int TBN>
+FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, const int32_t* aux,
+                       const int32_t* pst) {
   Tile T;
   const uint32_t t = (uint32_t)t64, num_n = (uint32_t)p.num_n;
   if (SCHED == kDense) {
@@ -131,7 +144,8 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, co
     const uint32_t gsz = left < (uint32_t)kGroupM ? left : (uint32_t)kGroupM;
     const uint32_t nb = r / gsz, mb = first_m + (r - nb * gsz);
     T.m0 = (int64_t)mb * TILE_M;
-    T.n0 = (int64_t)nb * BN;
+    T.pm0 = T.m0;
+    T.n0 = (int64_t)nb * TBN;
     T.row_end = p.M;
     T.k0 = 0;
     T.nkb = p.nkb;
@@ -141,7 +155,8 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, co
     const uint32_t local = t - (uint32_t)tpre[e];
     const uint32_t mb = local / num_n, nb = local - mb * num_n;
     T.m0 = aux[e] + (int64_t)mb * TILE_M;  // aux[e] = segment start row
-    T.n0 = (int64_t)nb * BN;
+    T.pm0 = pst ? pst[e] + (int64_t)mb * TILE_M : T.m0;
+    T.n0 = (int64_t)nb * TBN;
     T.row_end = aux[e + 1];
     T.k0 = 0;
     T.nkb = p.nkb;
@@ -152,7 +167,8 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, co
     const uint32_t local = t - e * per;
     const uint32_t mb = local / num_n, nb = local - mb * num_n;
     T.m0 = (int64_t)mb * TILE_M;
-    T.n0 = (int64_t)nb * BN;
+    T.pm0 = T.m0;
+    T.n0 = (int64_t)nb * TBN;
     T.row_end = p.M;
     T.k0 = aux[e];                             // aux[e] = padded start of segment e
     T.nkb = (aux[e + 1] - aux[e]) / BKB;       // padded length / 128
@@ -170,17 +186,23 @@ FP8_DEVI int64_t tile_nkb(const GemmParams& p, int64_t t, const int32_t* aux) {
 }
 
 template <int KIND, int SCHED, int A_MN, int B_MN, int CG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
-  using C = Cfg<CG>;
+                const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmSA,
+                const __grid_constant__ CUtensorMap tmSB, const GemmParams p) {
+  using C = Cfg<KIND, CG>;
   constexpr int STAGES = C::STAGES;
+  constexpr int kThreads = C::THREADS;
+  constexpr int kEpiThreads = C::EPI_THREADS;
+  constexpr int TBN = C::TBN;
+  constexpr bool kPadRows = KIND == kMX && SCHED == kJagM;  // A scales in the segment-padded row space
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* out_stage = smem + C::RING_BYTES;  // [8 warps][kStageOut], pairs only
   Shared& S = *reinterpret_cast<Shared*>(smem + C::RING_BYTES + C::OUT_BYTES);
   int32_t* tpre = reinterpret_cast<int32_t*>(smem + C::RING_BYTES + C::OUT_BYTES + kSharedBytes);
   int32_t* aux = tpre + (p.E + 1);
+  int32_t* pst = kPadRows ? aux + (p.E + 1) : nullptr;  // padded segment starts
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &S.abort;
   const uint32_t rank = CG == 2 ? cluster_ctarank() : 0;  // 0 issues the pair's MMAs
@@ -200,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (SCHED == kJagM) {
         tpre[e + 1] = (int32_t)(((cnt + C::TILE_M - 1) / C::TILE_M) * p.num_n);
         aux[e + 1] = cur;
+        if (kPadRows) pst[e + 1] = (int32_t)((cnt + 127) / 128 * 128);
       } else {
         tpre[e + 1] = (int32_t)(p.num_m * p.num_n);
         aux[e + 1] = (int32_t)(((cnt + BKB - 1) / BKB) * BKB);
@@ -208,18 +231,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       tpre[0] = 0;
       aux[0] = 0;
+      if (kPadRows) pst[0] = 0;
     }
     bad = __syncthreads_or(bad);
     if (bad) {  // both CTAs of a pair see the same offsets and leave together
       if (blockIdx.x == 0 && tid == 0) set_status(p.status, FP8_DEV_BAD_OFFSETS);
       return;
     }
-    if (warp == 0) {  // inclusive scans (tile prefix always; padded K prefix for jagged K)
+    if (warp == 0) {  // inclusive scans (tile prefix always; padded prefix for jagged K / MX rows)
+      constexpr bool kScan2 = SCHED == kJagK || kPadRows;
+      int32_t* w_arr = SCHED == kJagK ? aux : pst;
       int carry = 0, carry2 = 0;
       for (int base = 0; base < p.E; base += 32) {
         const int i = base + lane;
         int v = i < p.E ? tpre[i + 1] : 0;
-        int w = (SCHED == kJagK && i < p.E) ? aux[i + 1] : 0;
+        int w = (kScan2 && i < p.E) ? w_arr[i + 1] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(0xffffffffu, v, o);
@@ -231,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (i < p.E) {
           tpre[i + 1] = v + carry;
-          if (SCHED == kJagK) aux[i + 1] = w + carry2;
+          if (kScan2) w_arr[i + 1] = w + carry2;
         }
         carry += __shfl_sync(0xffffffffu, v, 31);
         carry2 += __shfl_sync(0xffffffffu, w, 31);
@@ -262,6 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (CG == 2) tma_prefetch_desc(&tmO);
+    if (KIND == kMX) {
+      tma_prefetch_desc(&tmSA);
+      tma_prefetch_desc(&tmSB);
+    }
   }
   if (warp == 1) {
     if (CG == 2) {
@@ -291,9 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t issued = 0;
       bool ok = true;
       for (int64_t t = unit; t < total && ok; t += n_units) {
-        const Tile T = get_tile<SCHED, C::TILE_M>(p, t, tpre, aux);
+        const Tile T = get_tile<SCHED, C::TILE_M, TBN>(p, t, tpre, aux, pst);
         const int32_t am = (int32_t)(T.m0 + (int64_t)rank * BM);        // this CTA's A rows
         const int32_t bn = (int32_t)(T.n0 + (int64_t)rank * C::B_ROWS);  // this CTA's B rows
+        // MX scale blocks: this CTA's 128 A rows; the two 128-row B blocks holding the tile's
+        // columns (each CTA of a pair loads them in full: its accumulator spans all columns)
+        const int32_t sfa_rb = (int32_t)((T.pm0 + (int64_t)rank * BM) / 128);
+        const int32_t sfb_rb = (int32_t)(T.n0 / 128);
         for (int64_t kb = 0; kb < T.nkb; ++kb) {
           if (!mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
             if (!*abort_flag) fail();
@@ -302,10 +336,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
+          uint8_t* ssf = sa + C::A_BYTES + C::B_BYTES;
           if (CG == 1) {
             uint64_t* fb = &S.full[stage];
-            mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-            if (KIND == kFP8) {
+            mbar_arrive_expect_tx(fb, C::TX_BYTES);
+            if (KIND == kMX) {
+              const int32_t kx = (int32_t)(T.k0 + kb * BKB);
+              tma_load_2d(sa, &tmA, fb, kx, am);
+              if (SCHED == kJagM) {
+                tma_load_3d(sb, &tmB, fb, kx, bn, T.e);
+                tma_load_4d(ssf + 512, &tmSB, fb, 0, kx / 128, sfb_rb, T.e);
+              } else {
+                tma_load_2d(sb, &tmB, fb, kx, bn);
+                tma_load_3d(ssf + 512, &tmSB, fb, 0, kx / 128, sfb_rb);
+              }
+              tma_load_3d(ssf, &tmSA, fb, 0, kx / 128, sfa_rb);
+            } else if (KIND == kFP8) {
               const int32_t kx = (int32_t)(T.k0 + kb * BKB);
               tma_load_2d(sa, &tmA, fb, kx, am);
               if (SCHED == kJagM)
@@ -330,8 +376,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             // both CTAs' bytes are counted on the issuing CTA's full barrier
             const uint32_t fb = mapa_shared(smem_u32(&S.full[stage]), 0);
-            if (issuer) mbar_arrive_expect_tx(&S.full[stage], 2 * C::STAGE_BYTES);
-            if (KIND == kFP8) {
+            if (issuer) mbar_arrive_expect_tx(&S.full[stage], 2 * C::TX_BYTES);
+            if (KIND == kMX) {
+              const int32_t kx = (int32_t)(T.k0 + kb * BKB);
+              tma_load_2d_pair(sa, &tmA, fb, kx, am);
+              if (SCHED == kJagM) {
+                tma_load_3d_pair(sb, &tmB, fb, kx, bn, T.e);
+                tma_load_4d_pair(ssf + 512, &tmSB, fb, 0, kx / 128, sfb_rb, T.e);
+              } else {
+                tma_load_2d_pair(sb, &tmB, fb, kx, bn);
+                tma_load_3d_pair(ssf + 512, &tmSB, fb, 0, kx / 128, sfb_rb);
+              }
+              tma_load_3d_pair(ssf, &tmSA, fb, 0, kx / 128, sfa_rb);
+            } else if (KIND == kFP8) {
               const int32_t kx = (int32_t)(T.k0 + kb * BKB);
               tma_load_2d_pair(sa, &tmA, fb, kx, am);
               if (SCHED == kJagM)
@@ -390,12 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t t = unit; t < total && ok; t += n_units) {
         const int64_t nkb = tile_nkb<SCHED>(p, t, aux);
         if (nkb == 0) continue;
+        // MX: the B scales of the tile's first column group sit 0 or 2 columns into its slot
+        uint32_t sfb_off = 0;
+        if (KIND == kMX) sfb_off = (uint32_t)((get_tile<SCHED, C::TILE_M, TBN>(p, t, tpre, aux, pst).n0 / 32) & 3);
         if (!mbar_wait(&S.tempty[buf], aphase ^ 1, abort_flag, p.wait_ns)) {
           if (!*abort_flag) fail();
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * TBN);
         for (int64_t kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&S.full[stage], phase, abort_flag, p.wait_ns)) {
             if (!*abort_flag) fail();
@@ -405,6 +465,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
+          if (KIND == kMX) {
+            // this stage's scales into its tensor-memory slot: A (4 columns), then two B blocks
+            const uint32_t sf_t = tmem_base + (uint32_t)(C::SF_COL0 + 16 * stage);
+            const uint32_t ssf = sb + C::B_BYTES;
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+              if (CG == 2)
+                tmem_cp_sf_pair(sf_t + 4 * j, smem_desc_plain(ssf + 512 * j, 128));
+              else
+                tmem_cp_sf(sf_t + 4 * j, smem_desc_plain(ssf + 512 * j, 128));
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024);
+              const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+              const uint32_t id = idesc_sf_ids(p.idesc, (uint32_t)kk, (uint32_t)kk);
+              if (CG == 2)
+                umma_mx_pair(d_tmem, ad, bd, id, sf_t, sf_t + 4 + sfb_off, acc);
+              else
+                umma_mx(d_tmem, ad, bd, id, sf_t, sf_t + 4 + sfb_off, acc);
+            }
+          } else {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, 8192, 1024) : smem_desc(sa + kk * 32, 16, 1024);
@@ -421,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               else
                 umma_f16(d_tmem, ad, bd, p.idesc, acc);
             }
+          }
           }
           // frees the stage (in both CTAs of a pair) once these MMAs have read it
           if (CG == 2)
@@ -453,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================================ epilogue ================================
     const int q = warp & 3;              // TMEM lane quarter this warp may access
-    const int c0 = ((warp - 2) >> 2) * (BN / 2);  // first tile column of this warp's half
+    const int c0 = ((warp - 2) >> 2) * C::WCOLS;  // first tile column of this warp's share
     const int etid = tid - 64;           // 0..255 across the epilogue warps
     const int row = (int)rank * BM + q * 32 + lane;  // row within the pair's tile
     const bool stage_sb = KIND == kFP8 && !p.sb_scalar;
@@ -465,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Tile Tn;
     float sa_nx = 1.0f, sb_nx = 1.0f;
     auto fetch = [&](int64_t tt) {
-      Tn = get_tile<SCHED, C::TILE_M>(p, tt, tpre, aux);
+      Tn = get_tile<SCHED, C::TILE_M, TBN>(p, tt, tpre, aux, pst);
       if (KIND != kFP8) return;
       const int64_t m = Tn.m0 + row;
       const float* sbp = p.sB;
@@ -500,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sbi ^= 1;
       if (T.nkb == 0) {  // empty segment (jagged K): the result is zero
         if (row_ok) {
-          for (int64_t n = T.n0 + c0; n < T.n0 + c0 + BN / 2 && n < p.N; ++n) {
+          for (int64_t n = T.n0 + c0; n < T.n0 + c0 + C::WCOLS && n < p.N; ++n) {
             if (p.out_f32)
               static_cast<float*>(p.out)[orow * p.ldo + n] = 0.0f;
             else
@@ -516,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const float sb_all = (KIND == kFP8 && p.sb_scalar) ? sb_mine : 1.0f;
-      const uint32_t taddr = tmem_base + (uint32_t)(buf * BN + c0) + ((uint32_t)(q * 32) << 16);
+      const uint32_t taddr = tmem_base + (uint32_t)(buf * TBN + c0) + ((uint32_t)(q * 32) << 16);
       // Pairs write through shared memory with TMA bulk-tensor stores of 32 rows x 128 bytes
       // (64 bf16 columns, or 32 fp32), unless this warp's 32 rows run past the end of an
       // expert's segment.
@@ -529,11 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t va[32], vb[32];
       uint32_t w[32];  // bf16 pairs of two consecutive 32-column chunks (one 128-byte row)
       tmem_ld32(taddr, va);
+      constexpr int NCH = C::WCOLS / 32;
 #pragma unroll
-      for (int ch = 0; ch < BN / 64; ++ch) {
+      for (int ch = 0; ch < NCH; ++ch) {
         uint32_t* v = (ch & 1) ? vb : va;
         tmem_ld_wait_regs(v);
-        if (ch + 1 < BN / 64) tmem_ld32(taddr + (ch + 1) * 32, (ch & 1) ? va : vb);
+        if (ch + 1 < NCH) tmem_ld32(taddr + (ch + 1) * 32, (ch & 1) ? va : vb);
         const int cl = c0 + ch * 32;  // tile column of v[0]
         const int64_t n = T.n0 + cl;
         // bf16 through TMA: the pair (ch - 1, ch) is stored once ch is done, unless the pair
@@ -541,13 +626,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool pair_live = T.n0 + c0 + (ch & ~1) * 32 < p.N;
         if (n >= p.N && !(via_tma && !p.out_f32 && pair_live)) continue;
         float f[32];
-        const float2 sa2 = make_float2(sa, sa);
+        if (KIND == kMX) {  // the block scales were applied inside the MMA
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float2 sb2 = stage_sb ? *reinterpret_cast<const float2*>(sbs + cl + j) : make_float2(sb_all, sb_all);
-          const float2 x = fmul2_rn(fmul2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sa2), sb2);
-          f[j] = x.x;
-          f[j + 1] = x.y;
+          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        } else {
+          const float2 sa2 = make_float2(sa, sa);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 sb2 = stage_sb ? *reinterpret_cast<const float2*>(sbs + cl + j) : make_float2(sb_all, sb_all);
+            const float2 x = fmul2_rn(fmul2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sa2), sb2);
+            f[j] = x.x;
+            f[j + 1] = x.y;
+          }
         }
         if (via_tma) {
           if (!p.out_f32) {
@@ -643,18 +733,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int KIND, int SCHED, int A_MN, int B_MN, int CG>
-int run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const GemmParams& p,
-        int64_t total_tiles_hint, const Ctx& c) {
+int run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const CUtensorMap& sfa,
+        const CUtensorMap& sfb, const GemmParams& p, int64_t total_tiles_hint, const Ctx& c) {
   auto kern = gemm_kernel<KIND, SCHED, A_MN, B_MN, CG>;
-  using C = Cfg<CG>;
-  const size_t smem = 1024 + C::RING_BYTES + C::OUT_BYTES + kSharedBytes + (SCHED == kDense ? 0 : 2 * 4 * (p.E + 1));
+  using C = Cfg<KIND, CG>;
+  constexpr int kThreads = C::THREADS;
+  const int n_arrays = SCHED == kDense ? 0 : (KIND == kMX && SCHED == kJagM) ? 3 : 2;
+  const size_t smem = 1024 + C::RING_BYTES + C::OUT_BYTES + kSharedBytes + (size_t)n_arrays * 4 * (p.E + 1);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FP8_ERR_CUDA;
   int64_t units = c.sm_count / CG;
   if (total_tiles_hint > 0 && total_tiles_hint < units) units = total_tiles_hint;
   if (units < 1) units = 1;
   if (CG == 1) {
-    kern<<<(unsigned)units, kThreads, smem, c.stream>>>(a, b, o, p);
+    kern<<<(unsigned)units, kThreads, smem, c.stream>>>(a, b, o, sfa, sfb, p);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
@@ -669,8 +761,72 @@ int run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const 
   cfg.stream = c.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, a, b, o, p) != cudaSuccess) return FP8_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, a, b, o, sfa, sfb, p) != cudaSuccess) return FP8_ERR_CUDA;
   return FP8_OK;
+}
+
+// MX operands: the FP8 codes load as on the FP8 path; the E8M0 scales, stored as
+// [row blocks][K / 128][512 bytes], load through tensor maps over 128-word rows: a 3-D map
+// [row block][K group][128 words] (4-D with the expert for the grouped weights). Box: one A
+// block, two consecutive B blocks (a 192-column tile spans parts of at most two).
+int launch_mx(const GemmArgs& g, GemmParams& p, const CUtensorMap& to, bool pair, int tile_m, const Ctx& c) {
+  if (g.K % 128 || !g.sfa || !g.sfb) return FP8_ERR_UNSUPPORTED;
+  const uint32_t af = g.a_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
+  const uint32_t bf = g.b_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
+  constexpr int TBN = Cfg<kMX, 1>::TBN;
+  p.idesc = make_idesc_mx(af, bf, (uint32_t)tile_m, TBN);
+  const uint32_t b_rows = pair ? TBN / 2 : TBN;
+  const uint64_t kbg = (uint64_t)(g.K / 128);
+  const uint64_t rba = (uint64_t)((g.sfa_rows + 127) / 128);
+  const uint64_t rbb = (uint64_t)((g.N + 127) / 128);
+  CUtensorMap ta, tb, tsa, tsb;
+  const uint64_t dA[2] = {(uint64_t)g.K, (uint64_t)g.M};
+  const uint64_t strideK[1] = {(uint64_t)g.K};
+  const uint32_t boxA[2] = {BKB, BM};
+  int rc = make_tmap(&ta, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, strideK, boxA, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  {
+    const uint64_t d[3] = {128, kbg, rba};
+    const uint64_t st[2] = {512, 512 * kbg};
+    const uint32_t box[3] = {128, 1, 1};
+    rc = make_tmap(&tsa, g.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  }
+  if (g.mode == FP8_GROUPED_JAGGED_M) {
+    const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.E};
+    const uint64_t sB_[2] = {(uint64_t)g.K, (uint64_t)(g.N * g.K)};
+    const uint32_t boxB[3] = {BKB, b_rows, 1};
+    rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dB, sB_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    const uint64_t d[4] = {128, kbg, rbb, (uint64_t)g.E};
+    const uint64_t st[3] = {512, 512 * kbg, 512 * kbg * rbb};
+    const uint32_t box[4] = {128, 1, 2, 1};
+    rc = make_tmap(&tsb, g.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+    p.total_rows = g.M;
+    return pair ? run<kMX, kJagM, 0, 0, 2>(ta, tb, to, tsa, tsb, p, 0, c)
+                : run<kMX, kJagM, 0, 0, 1>(ta, tb, to, tsa, tsb, p, 0, c);
+  }
+  const uint64_t dB[2] = {(uint64_t)g.K, (uint64_t)g.N};
+  const uint32_t boxB[2] = {BKB, b_rows};
+  rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dB, strideK, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  {
+    const uint64_t d[3] = {128, kbg, rbb};
+    const uint64_t st[2] = {512, 512 * kbg};
+    const uint32_t box[3] = {128, 1, 2};
+    rc = make_tmap(&tsb, g.sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, d, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  }
+  if (g.mode == -1) {
+    const int64_t tiles = p.num_m * p.num_n;
+    return pair ? run<kMX, kDense, 0, 0, 2>(ta, tb, to, tsa, tsb, p, tiles, c)
+                : run<kMX, kDense, 0, 0, 1>(ta, tb, to, tsa, tsb, p, tiles, c);
+  }
+  p.total_rows = -1;
+  const int64_t tiles = (int64_t)g.E * p.num_m * p.num_n;
+  return pair ? run<kMX, kJagK, 0, 0, 2>(ta, tb, to, tsa, tsb, p, tiles, c)
+              : run<kMX, kJagK, 0, 0, 1>(ta, tb, to, tsa, tsb, p, tiles, c);
 }
 
 }  // namespace
@@ -692,7 +848,9 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   p.test_stall = c.test_stall;
   p.ends = g.ends;
   p.E = (int)g.E;
-  p.num_n = (g.N + BN - 1) / BN;
+  const bool mx = g.mx != 0;
+  const int tbn = mx ? Cfg<kMX, 1>::TBN : BN;
+  p.num_n = (g.N + tbn - 1) / tbn;
   const int esz = fp8 ? 1 : 2;
   p.nkb = (g.K * esz + BKB - 1) / BKB;
   p.ldo = g.N;
@@ -709,8 +867,9 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
                                                              : p.num_m * p.num_n;
   if (max_tiles >= (int64_t)1 << 31) return FP8_ERR_UNSUPPORTED;
   // output tensor map for the pairs' TMA stores: boxes of 32 rows x 128 bytes
-  CUtensorMap to;
+  CUtensorMap to, none;
   memset(&to, 0, sizeof(to));
+  memset(&none, 0, sizeof(none));
   p.tma_out = 0;
   if (pair && p.vec_ok && (reinterpret_cast<uintptr_t>(g.out) & 15) == 0) {
     const CUtensorMapDataType odt = p.out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -733,6 +892,7 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
     p.tma_out = 1;
   }
 
+  if (mx) return launch_mx(g, p, to, pair, tile_m, c);
   if (fp8) {
     const uint32_t af = g.a_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
     const uint32_t bf = g.b_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
@@ -753,13 +913,13 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
       if (rc) return rc;
       if (g.mode == -1) {
         const int64_t tiles = p.num_m * p.num_n;
-        return pair ? run<kFP8, kDense, 0, 0, 2>(ta, tb, to, p, tiles, c) : run<kFP8, kDense, 0, 0, 1>(ta, tb, to, p, tiles, c);
+        return pair ? run<kFP8, kDense, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c) : run<kFP8, kDense, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
       }
       // jagged K: A = G^T [N_out, P], B = X^T [Kd, P]; tile space M = N_out, N = Kd; the
       // offsets are checked for order and for fitting the padded length P.
       p.total_rows = -1;
       const int64_t tiles = (int64_t)g.E * p.num_m * p.num_n;
-      return pair ? run<kFP8, kJagK, 0, 0, 2>(ta, tb, to, p, tiles, c) : run<kFP8, kJagK, 0, 0, 1>(ta, tb, to, p, tiles, c);
+      return pair ? run<kFP8, kJagK, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c) : run<kFP8, kJagK, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
     }
     if (g.mode == FP8_GROUPED_JAGGED_M) {
       p.total_rows = g.M;
@@ -768,7 +928,7 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
       const uint32_t boxB[3] = {BKB, b_rows, 1};
       rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dB, sB_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc) return rc;
-      return pair ? run<kFP8, kJagM, 0, 0, 2>(ta, tb, to, p, 0, c) : run<kFP8, kJagM, 0, 0, 1>(ta, tb, to, p, 0, c);
+      return pair ? run<kFP8, kJagM, 0, 0, 2>(ta, tb, to, none, none, p, 0, c) : run<kFP8, kJagM, 0, 0, 1>(ta, tb, to, none, none, p, 0, c);
     }
     return FP8_ERR_INVALID_ARG;
   }
@@ -805,15 +965,15 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   if (rc) return rc;
   const int64_t tiles = p.num_m * p.num_n;
   if (pair) {
-    if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 2>(ta, tb, to, p, tiles, c);
-    if (g.a_mn) return run<kBF16, kDense, 1, 0, 2>(ta, tb, to, p, tiles, c);
-    if (g.b_mn) return run<kBF16, kDense, 0, 1, 2>(ta, tb, to, p, tiles, c);
-    return run<kBF16, kDense, 0, 0, 2>(ta, tb, to, p, tiles, c);
+    if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 2>(ta, tb, to, none, none, p, tiles, c);
+    if (g.a_mn) return run<kBF16, kDense, 1, 0, 2>(ta, tb, to, none, none, p, tiles, c);
+    if (g.b_mn) return run<kBF16, kDense, 0, 1, 2>(ta, tb, to, none, none, p, tiles, c);
+    return run<kBF16, kDense, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c);
   }
-  if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 1>(ta, tb, to, p, tiles, c);
-  if (g.a_mn) return run<kBF16, kDense, 1, 0, 1>(ta, tb, to, p, tiles, c);
-  if (g.b_mn) return run<kBF16, kDense, 0, 1, 1>(ta, tb, to, p, tiles, c);
-  return run<kBF16, kDense, 0, 0, 1>(ta, tb, to, p, tiles, c);
+  if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 1>(ta, tb, to, none, none, p, tiles, c);
+  if (g.a_mn) return run<kBF16, kDense, 1, 0, 1>(ta, tb, to, none, none, p, tiles, c);
+  if (g.b_mn) return run<kBF16, kDense, 0, 1, 1>(ta, tb, to, none, none, p, tiles, c);
+  return run<kBF16, kDense, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
 }
 
 }  // namespace fp8lin

@@ -48,6 +48,17 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
                       const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, uint32_t* scratch,
                       const Ctx& c);
 
+// --- MX quantize (mx.cu) ---
+// Bytes of the E8M0 scales of an operand with `rows` rows and contraction length k (k % 128 == 0):
+// [ceil(rows / 128)][k / 128][512]; -1 for bad arguments.
+int64_t mx_scale_bytes(int64_t rows, int64_t k);
+// x bf16 [batches, R, C] (C % 128 == 0). q: row-major codes (blocks along C) with scales sf; qt:
+// column-major codes [batches, C, ld_t] (blocks along R; R % 128 == 0 unless segmented) with
+// scales sft. Either output may be null. With ends (batches == 1): segments of rows, padded row
+// space of ld_t rows (ld_t % 128 == 0) for sf's rows and qt's columns; pstart_ws: E + 1 words.
+int launch_mx_quant(const void* x, int64_t batches, int64_t R, int64_t C, int fmt, void* q, void* sf, void* qt,
+                    int64_t ld_t, void* sft, const int32_t* ends, int64_t E, int32_t* pstart_ws, const Ctx& c);
+
 // --- GEMM launchers (gemm.cu) ---
 struct GemmArgs {
   // operands
@@ -66,6 +77,11 @@ struct GemmArgs {
   const int32_t* ends;
   int64_t E;
   int64_t k_dim;          // jagged K: the output's last dimension (X's columns)
+  // MX (block-scaled) operands: E8M0 scales in [row blocks][K / 128][512 B] blocks
+  int mx;
+  const void* sfa;        // A's scales; rows: M, or the segment-padded row count (jagged M)
+  const void* sfb;        // B's scales; rows: N (per expert for jagged M)
+  int64_t sfa_rows;
 };
 int launch_gemm(const GemmArgs& g, const Ctx& c);
 

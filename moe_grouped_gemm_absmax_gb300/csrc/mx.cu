@@ -1,0 +1,310 @@
+// MXFP8 block quantization on sm_103a: blocks of 32 consecutive elements along the contraction
+// dimension, one E8M0 (power-of-two) scale per block.
+//
+// The pages name MXFP8 as the granularity that packs a scale per group with the data ("FP8
+// training on AMD GPUs with TorchTitan and TorchAO", section "AMD FP8 format in TorchAO") and as
+// the next step for the quantization and grouped-GEMM kernels ("Summary and Next Steps"). The
+// block size, the E8M0 scale and its rule follow the OCP Microscaling Formats (MX) specification
+// v1.0: X = 2^(floor(log2(amax)) - emax_elem), emax_elem = 8 (e4m3) or 15 (e5m2), the exponent
+// clamped below at -127; each element is x / X, rounded to nearest even and saturated.
+//
+// One kernel serves the row-major output (blocks along a row), the column-major output (blocks
+// down a column, written transposed) and both from a single read. A CTA owns a tile of 128 rows
+// x 128 columns of bf16:
+//   - the row-major codes come straight from registers: each 16-byte load holds 8 elements of a
+//     row, four lanes hold a block of 32, two shuffles give the block amax, and the 16 lanes of a
+//     row store its 128 codes as one 128-byte segment;
+//   - for the column-major codes the tile is staged in shared memory, each thread reduces and
+//     casts 64 rows of one column, and the transposed codes leave through a second staging
+//     buffer as 128-byte rows.
+// The E8M0 scales are written in the tensor-core scale-factor layout the MX GEMM reads: for an
+// operand with rows r (its non-contraction index) and K blocks j, 512-byte blocks
+// [r / 128][j / 4], and inside one the code of (r, j) at byte (r % 32) * 16 + (r / 32 % 4) * 4 +
+// j % 4. A tile row's four block codes therefore form one aligned 32-bit word.
+// With segment offsets (MoE), tiles walk the segment-padded row space: segment e occupies padded
+// rows [pstart_e, pstart_e + roundup(count_e, 128)), so blocks never straddle two segments and
+// the padding quantizes as zeros.
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp8lin {
+
+namespace {
+
+constexpr int kTile = 128;             // rows and columns of a tile
+constexpr int kMxThreads = 256;
+constexpr int kInPitch = kTile + 8;    // bf16 per staged input row (272 bytes: 16-byte aligned rows)
+constexpr int kOutPitch = kTile + 16;  // bytes per staged output row (conflict-free 16-byte writes)
+constexpr int kMxSmem = kTile * kInPitch * 2 + kTile * kOutPitch;
+constexpr int kMaxSegments = 2048;
+
+// E8M0 code of a block from the bf16 pattern of its amax (sign cleared). For a normal amax,
+// floor(log2 amax) = exponent field - 127, so the code (exponent + 127) is field - emax_elem,
+// clamped at 0; a zero or subnormal amax lies below the clamp. Inf / NaN give the NaN code.
+template <int FMT>
+FP8_DEVI uint32_t mx_code(uint32_t amax_bits) {
+  constexpr int kEmax = FMT == FP8_DT_E4M3 ? 8 : 15;
+  const int ef = (int)(amax_bits >> 7);
+  if (ef == 255) return 0xFFu;
+  return ef > kEmax ? (uint32_t)(ef - kEmax) : 0u;
+}
+
+// 1 / X = 2^(127 - code) as an fp32 (a normal number for every code the rule produces).
+FP8_DEVI float mx_inv(uint32_t code) {
+  return code == 0xFFu ? __uint_as_float(0x7FC00000u) : __uint_as_float((254u - code) << 23);
+}
+
+// Two bf16 (one packed word) times a power of two, cast: the product is exact, so the only
+// rounding is the cast's (nearest even, saturating at the format's largest finite value).
+template <int FMT>
+FP8_DEVI uint32_t mx_cast2(uint32_t two_bf16, float inv) {
+  const float2 p = fmul2_rn(make_float2(__uint_as_float(two_bf16 << 16), __uint_as_float(two_bf16 & 0xFFFF0000u)),
+                            make_float2(inv, inv));
+  return cvt_fp8x2<FMT>(p.x, p.y);
+}
+
+struct MxArgs {
+  const uint16_t* x;
+  int64_t R, C;           // rows and columns of one batch entry (C % 128 == 0)
+  uint8_t* q;             // row-major codes in x's shape, or null
+  uint8_t* sf;            // their scales: [batch][rb_q][C / 128][512 B]
+  int64_t rb_q;           // 128-row blocks of sf per batch entry
+  uint8_t* qt;            // column-major codes [batch][C][ld_t], or null
+  int64_t ld_t;           // row length of qt: R, or the padded row count P with segments
+  uint8_t* sft;           // their scales: [batch][C / 128][ld_t / 128][512 B]
+  const int32_t* pstart;  // segments: padded starts [E + 1] (pstart[E] = padded rows in use)
+  const int32_t* ends;
+  int E;
+};
+
+template <int FMT, bool ROWS, bool COLS, bool JAG>
+__global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const MxArgs a) {
+  extern __shared__ __align__(16) uint8_t mx_smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t c0 = (int64_t)blockIdx.x * kTile;
+  const int64_t b = blockIdx.z;
+  int64_t row0, prow0;  // first source row of the tile; its padded row (scale position)
+  int valid;            // source rows in the tile
+  if (JAG) {
+    prow0 = (int64_t)blockIdx.y * kTile;
+    const int32_t used = __ldg(a.pstart + a.E);
+    if (prow0 >= used) return;  // past the last segment (or offsets rejected: used == 0)
+    int lo = 0, hi = a.E - 1;   // the last segment whose padded start is <= prow0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(a.pstart + mid) <= prow0) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t start = lo ? __ldg(a.ends + lo - 1) : 0;
+    const int64_t cnt = __ldg(a.ends + lo) - start;
+    const int64_t off = prow0 - __ldg(a.pstart + lo);
+    row0 = start + off;
+    valid = (int)(cnt - off < kTile ? cnt - off : kTile);
+  } else {
+    row0 = (int64_t)blockIdx.y * kTile;
+    prow0 = row0;
+    valid = (int)(a.R - row0 < kTile ? a.R - row0 : kTile);
+  }
+  const uint16_t* xb = a.x + b * a.R * a.C;
+
+  // ---- load: 8 vectors of 8 bf16 per thread; rows past the segment / tensor are zeros ----
+  uint4 v[8];
+  const int cc = (lane & 15) * 8;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int rr = it * 16 + warp * 2 + (lane >> 4);
+    v[it] = rr < valid ? ld_nc_v4(xb + (row0 + rr) * a.C + c0 + cc) : make_uint4(0, 0, 0, 0);
+  }
+
+  if (ROWS) {
+    const int64_t ncb = a.C / kTile;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int rr = it * 16 + warp * 2 + (lane >> 4);
+      uint32_t m = absmax_fold(absmax_vec8(0u, v[it]));
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      const uint32_t code = mx_code<FMT>(m);
+      const float inv = mx_inv(code);
+      uint2 o;
+      o.x = mx_cast2<FMT>(v[it].x, inv) | (mx_cast2<FMT>(v[it].y, inv) << 16);
+      o.y = mx_cast2<FMT>(v[it].z, inv) | (mx_cast2<FMT>(v[it].w, inv) << 16);
+      // the four block codes of this row, from lanes 0, 4, 8, 12 of its half-warp
+      const int hb = lane & 16;
+      const uint32_t word = __shfl_sync(0xffffffffu, code, hb) | (__shfl_sync(0xffffffffu, code, hb + 4) << 8) |
+                            (__shfl_sync(0xffffffffu, code, hb + 8) << 16) |
+                            (__shfl_sync(0xffffffffu, code, hb + 12) << 24);
+      if (rr < valid) {
+        *reinterpret_cast<uint2*>(a.q + (b * a.R + row0 + rr) * a.C + c0 + cc) = o;
+        if ((lane & 15) == 0) {
+          const int64_t pr = prow0 + rr;
+          uint8_t* blk = a.sf + ((b * a.rb_q + (pr >> 7)) * ncb + (c0 >> 7)) * 512;
+          *reinterpret_cast<uint32_t*>(blk + (pr & 31) * 16 + ((pr >> 5) & 3) * 4) = word;
+        }
+      }
+    }
+  }
+
+  if (COLS) {
+    uint16_t* sx = reinterpret_cast<uint16_t*>(mx_smem);
+    uint8_t* so = mx_smem + kTile * kInPitch * 2;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int rr = it * 16 + warp * 2 + (lane >> 4);
+      *reinterpret_cast<uint4*>(sx + rr * kInPitch + cc) = v[it];
+    }
+    __syncthreads();
+    // thread: column c of the tile, rows 64h .. 64h + 63 (blocks 2h and 2h + 1)
+    const int c = tid & (kTile - 1), h = tid >> 7;
+    uint32_t code2[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t m = 0;
+      const int r0 = 64 * h + 32 * j;
+#pragma unroll 8
+      for (int r = 0; r < 32; ++r) m = max(m, (uint32_t)(sx[(r0 + r) * kInPitch + c] & 0x7FFFu));
+      code2[j] = mx_code<FMT>(m);
+      const float inv = mx_inv(code2[j]);
+      uint32_t w[8];
+#pragma unroll
+      for (int r = 0; r < 32; r += 4) {
+        const uint32_t p01 = (uint32_t)sx[(r0 + r) * kInPitch + c] | ((uint32_t)sx[(r0 + r + 1) * kInPitch + c] << 16);
+        const uint32_t p23 =
+            (uint32_t)sx[(r0 + r + 2) * kInPitch + c] | ((uint32_t)sx[(r0 + r + 3) * kInPitch + c] << 16);
+        w[r / 4] = mx_cast2<FMT>(p01, inv) | (mx_cast2<FMT>(p23, inv) << 16);
+      }
+      uint8_t* dst = so + c * kOutPitch + r0;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    {
+      const int64_t nrb = a.ld_t / kTile;
+      uint8_t* blk = a.sft + ((b * (a.C / kTile) + (c0 >> 7)) * nrb + (prow0 >> 7)) * 512;
+      *reinterpret_cast<uint16_t*>(blk + (c & 31) * 16 + (c >> 5) * 4 + 2 * h) = (uint16_t)(code2[0] | (code2[1] << 8));
+    }
+    __syncthreads();
+    // the transposed tile: row c of qt holds 128 codes (rows prow0 .. prow0 + 127), 8 lanes each
+#pragma unroll
+    for (int i = 0; i < kTile / 32; ++i) {
+      const int cr = i * 32 + warp * 4 + (lane >> 3);
+      const int ch = (lane & 7) * 16;
+      const uint4 w = *reinterpret_cast<const uint4*>(so + cr * kOutPitch + ch);
+      *reinterpret_cast<uint4*>(a.qt + (b * a.C + c0 + cr) * a.ld_t + prow0 + ch) = w;
+    }
+  }
+}
+
+// Segment check and padded starts: pstart[e + 1] = pstart[e] + roundup(count_e, 128). Bad
+// offsets (decreasing, last != rows) or a padded total above P set FP8_DEV_BAD_OFFSETS and leave
+// pstart[E] = 0, so that the quantize kernel writes nothing.
+__global__ void __launch_bounds__(1024) mx_pstart_kernel(const int32_t* ends, int E, int64_t rows, int64_t P,
+                                                          int32_t* pstart, int32_t* status) {
+  __shared__ int32_t part[32];
+  __shared__ int bad_any;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) bad_any = 0;
+  __syncthreads();
+  // each thread owns segments 2 tid and 2 tid + 1
+  int32_t pad[2];
+  int bad = 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int e = 2 * tid + j;
+    pad[j] = 0;
+    if (e < E) {
+      const int32_t cur = ends[e], prev = e ? ends[e - 1] : 0;
+      if (cur < prev || (e == E - 1 && cur != rows)) bad = 1;
+      const int32_t cnt = cur > prev ? cur - prev : 0;
+      pad[j] = (cnt + 127) / 128 * 128;
+    }
+  }
+  if (bad) atomicOr(&bad_any, 1);
+  int32_t s = pad[0] + pad[1];
+  int32_t incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) part[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = part[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    part[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int32_t excl = incl - s + (warp ? part[warp - 1] : 0);
+  const int32_t total = part[31];
+  const bool ok = !bad_any && total <= P;
+  if (2 * tid < E) pstart[2 * tid] = excl;
+  if (2 * tid + 1 < E) pstart[2 * tid + 1] = excl + pad[0];
+  if (tid == 0) {
+    pstart[E] = ok ? total : 0;
+    if (!ok) set_status(status, FP8_DEV_BAD_OFFSETS);
+  }
+}
+
+template <int FMT, bool ROWS, bool COLS, bool JAG>
+int run_mx(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) {
+  auto kern = mx_quant_kernel<FMT, ROWS, COLS, JAG>;
+  const int smem = COLS ? kMxSmem : 0;
+  if (COLS && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return FP8_ERR_CUDA;
+  const dim3 grid((unsigned)(a.C / kTile), (unsigned)grid_y, (unsigned)batches);
+  kern<<<grid, kMxThreads, smem, c.stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+template <int FMT, bool JAG>
+int dispatch_layout(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) {
+  if (a.q && a.qt) return run_mx<FMT, true, true, JAG>(a, grid_y, batches, c);
+  if (a.q) return run_mx<FMT, true, false, JAG>(a, grid_y, batches, c);
+  return run_mx<FMT, false, true, JAG>(a, grid_y, batches, c);
+}
+
+}  // namespace
+
+int64_t mx_scale_bytes(int64_t rows, int64_t k) {
+  if (rows < 0 || k < 0 || k % 128) return -1;
+  return (rows + 127) / 128 * 128 * (k / 32);
+}
+
+int launch_mx_quant(const void* x, int64_t batches, int64_t R, int64_t C, int fmt, void* q, void* sf, void* qt,
+                    int64_t ld_t, void* sft, const int32_t* ends, int64_t E, int32_t* pstart_ws, const Ctx& c) {
+  if (C % kTile || (!q && !qt)) return FP8_ERR_INVALID_ARG;
+  if (ends && (E < 1 || E > kMaxSegments || batches != 1)) return FP8_ERR_UNSUPPORTED;
+  MxArgs a = {};
+  a.x = static_cast<const uint16_t*>(x);
+  a.R = R;
+  a.C = C;
+  a.q = static_cast<uint8_t*>(q);
+  a.sf = static_cast<uint8_t*>(sf);
+  a.qt = static_cast<uint8_t*>(qt);
+  a.ld_t = ld_t;
+  a.sft = static_cast<uint8_t*>(sft);
+  a.ends = ends;
+  a.E = (int)E;
+  if (R == 0 || C == 0 || batches == 0) return FP8_OK;
+  if (ends) {
+    // row-major scales and the column-major codes both live in the padded row space [0, P)
+    a.rb_q = ld_t / kTile;
+    a.pstart = pstart_ws;
+    mx_pstart_kernel<<<1, 1024, 0, c.stream>>>(ends, (int)E, R, ld_t, pstart_ws, c.status);
+    if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
+    const int64_t grid_y = ld_t / kTile;
+    return fmt == FP8_DT_E4M3 ? dispatch_layout<FP8_DT_E4M3, true>(a, grid_y, 1, c)
+                              : dispatch_layout<FP8_DT_E5M2, true>(a, grid_y, 1, c);
+  }
+  a.rb_q = (R + kTile - 1) / kTile;
+  const int64_t grid_y = (R + kTile - 1) / kTile;
+  if (grid_y > 65535 || batches > 65535) return FP8_ERR_UNSUPPORTED;
+  return fmt == FP8_DT_E4M3 ? dispatch_layout<FP8_DT_E4M3, false>(a, grid_y, batches, c)
+                            : dispatch_layout<FP8_DT_E5M2, false>(a, grid_y, batches, c);
+}
+
+}  // namespace fp8lin
