@@ -228,20 +228,22 @@ int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* o
  * ([Q] section 6: the autograd function saves the quantized tensors, not the bf16 inputs).
  * All buffers are caller-owned. */
 typedef struct fp8_linear_saved {
-  fp8_tensor x_q;   /* e4m3 [M, K] */
-  fp8_tensor x_inv; /* fp32 [1] (tensor) or [M] (row) */
-  fp8_tensor w_q;   /* e4m3 [N, K] */
-  fp8_tensor w_inv; /* fp32 [1] or [N] */
-  fp8_tensor xt_q;  /* tensor granularity: e4m3 [K, M], x column-major (FP8 weight-gradient);
-                       ptr may be NULL when the backward pass uses FP8_WGRAD_BF16 */
-  fp8_tensor wt_q;  /* tensor granularity: e4m3 [K, N], W column-major (grad-input) */
+  fp8_tensor x_q;    /* e4m3 [M, K] */
+  fp8_tensor x_inv;  /* fp32 [1] (tensor) or [M] (row); MX: E8M0 fp8_mx_scale_bytes(M, K) */
+  fp8_tensor w_q;    /* e4m3 [N, K] */
+  fp8_tensor w_inv;  /* fp32 [1] or [N]; MX: E8M0 fp8_mx_scale_bytes(N, K) */
+  fp8_tensor xt_q;   /* tensor and MX granularity: e4m3 [K, M], x column-major (FP8 weight
+                        gradient); ptr may be NULL when the backward pass uses FP8_WGRAD_BF16 */
+  fp8_tensor wt_q;   /* tensor and MX granularity: e4m3 [K, N], W column-major (grad-input) */
+  fp8_tensor xt_inv; /* MX only: E8M0 fp8_mx_scale_bytes(K, M) (blocks of 32 along M) */
+  fp8_tensor wt_inv; /* MX only: E8M0 fp8_mx_scale_bytes(K, N) (blocks of 32 along N) */
 } fp8_linear_saved;
 
 /*
- * fp8_linear_fwd — y = x W^T through FP8 ([Q], [L]): quantize x and W (e4m3; tensor or row
+ * fp8_linear_fwd — y = x W^T through FP8 ([Q], [L]): quantize x and W (e4m3; tensor, row or MX
  * granularity), then one scaled GEMM. x bf16 [M, K], w bf16 [N, K], y bf16/fp32 [M, N].
- * Tensor granularity writes x and W in both layouts (dual output) so that the backward pass
- * needs no transpose copy.
+ * Tensor and MX granularity write x and W in both layouts (dual output) so that the backward
+ * pass needs no transpose copy. MX ([MX]) needs M, K and N multiples of 128.
  */
 int fp8_linear_fwd(const fp8_tensor* x, const fp8_tensor* w, int granularity, int flags,
                    fp8_tensor* y, fp8_linear_saved* saved, void* workspace,
@@ -253,7 +255,8 @@ int fp8_linear_fwd(const fp8_tensor* x, const fp8_tensor* w, int granularity, in
  *  saved   from fp8_linear_fwd with the same granularity.
  *  x, w    the bf16 forward inputs. Row granularity needs w (W quantized per column over N for
  *          the grad-input GEMM). FP8_WGRAD_BF16 needs x; FP8_WGRAD_FP8 with row granularity
- *          needs x (quantized per column over M).
+ *          needs x (quantized per column over M). MX uses the saved column-major copies and
+ *          quantizes dY to MX e5m2 in both layouts from one read.
  *  dx      bf16/fp32 [M, K]; dw bf16/fp32 [N, K]. Either may be NULL to skip that GEMM.
  *  Both backward GEMMs run with full accumulation ([Q] section 5).
  */

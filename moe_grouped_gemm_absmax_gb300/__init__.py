@@ -47,7 +47,7 @@ class Fp8Tensor(ctypes.Structure):
 
 
 class Fp8LinearSaved(ctypes.Structure):
-    _fields_ = [(n, Fp8Tensor) for n in ("x_q", "x_inv", "w_q", "w_inv", "xt_q", "wt_q")]
+    _fields_ = [(n, Fp8Tensor) for n in ("x_q", "x_inv", "w_q", "w_inv", "xt_q", "wt_q", "xt_inv", "wt_inv")]
 
 
 class Fp8Error(RuntimeError):
@@ -155,14 +155,41 @@ def fp8_grouped_mm(A, B, offsets, sA, sB, out, mode, flags=0, status=None, strea
     _check(rc, "fp8_grouped_mm")
 
 
-def make_saved(x_q, x_inv, w_q, w_inv, xt_q=None, wt_q=None) -> Fp8LinearSaved:
+def make_saved(x_q, x_inv, w_q, w_inv, xt_q=None, wt_q=None, xt_inv=None, wt_inv=None) -> Fp8LinearSaved:
     s = Fp8LinearSaved()
     s.x_q, s.x_inv, s.w_q, s.w_inv = desc(x_q), desc(x_inv), desc(w_q), desc(w_inv)
-    if xt_q is not None:
-        s.xt_q = desc(xt_q)
-    if wt_q is not None:
-        s.wt_q = desc(wt_q)
+    for name, t in (("xt_q", xt_q), ("wt_q", wt_q), ("xt_inv", xt_inv), ("wt_inv", wt_inv)):
+        if t is not None:
+            setattr(s, name, desc(t))
     return s
+
+
+def linear_saved_alloc(M: int, K: int, N: int, granularity: int, keep_xt: bool = True, device="cuda"):
+    """Caller-owned buffers of fp8_linear_saved for a granularity; returns (saved, tensors) where
+    `tensors` keeps the torch buffers alive (x_q, x_inv, w_q, w_inv, xt_q, wt_q, xt_inv, wt_inv)."""
+    e4 = torch.float8_e4m3fn
+    x_q = torch.empty((M, K), dtype=e4, device=device)
+    w_q = torch.empty((N, K), dtype=e4, device=device)
+    xt_q = wt_q = xt_inv = wt_inv = None
+    if granularity == GRAN_MX:
+        u8 = torch.uint8
+        x_inv = torch.empty(fp8_mx_scale_bytes(M, K), dtype=u8, device=device)
+        w_inv = torch.empty(fp8_mx_scale_bytes(N, K), dtype=u8, device=device)
+        wt_q = torch.empty((K, N), dtype=e4, device=device)
+        wt_inv = torch.empty(fp8_mx_scale_bytes(K, N), dtype=u8, device=device)
+        if keep_xt:
+            xt_q = torch.empty((K, M), dtype=e4, device=device)
+            xt_inv = torch.empty(fp8_mx_scale_bytes(K, M), dtype=u8, device=device)
+    else:
+        tens = granularity == GRAN_TENSOR
+        x_inv = torch.empty(1 if tens else M, dtype=torch.float32, device=device)
+        w_inv = torch.empty(1 if tens else N, dtype=torch.float32, device=device)
+        if tens:
+            wt_q = torch.empty((K, N), dtype=e4, device=device)
+            if keep_xt:
+                xt_q = torch.empty((K, M), dtype=e4, device=device)
+    tensors = (x_q, x_inv, w_q, w_inv, xt_q, wt_q, xt_inv, wt_inv)
+    return make_saved(*tensors), tensors
 
 
 def fp8_linear_fwd(x, w, granularity, flags, y, saved: Fp8LinearSaved, workspace=None, status=None, stream=None):

@@ -9,8 +9,8 @@ them into autograd. No bias: the pages' hot path is the bias-free matmul, and a 
 non-FP8 step."""
 import torch
 
-from . import (GRAN_ROW, GRAN_TENSOR, MM_FAST_ACCUM, OP_LINEAR_BWD, OP_LINEAR_FWD, WGRAD_BF16, WGRAD_FP8,
-               fp8_linear_bwd, fp8_linear_fwd, fp8_workspace_size, make_saved)
+from . import (GRAN_MX, GRAN_ROW, GRAN_TENSOR, MM_FAST_ACCUM, OP_LINEAR_BWD, OP_LINEAR_FWD, WGRAD_BF16,
+               WGRAD_FP8, fp8_linear_bwd, fp8_linear_fwd, fp8_workspace_size, linear_saved_alloc, make_saved)
 
 
 def _workspace(nbytes, device):
@@ -31,27 +31,21 @@ class Fp8LinearFunction(torch.autograd.Function):
         w = weight.contiguous()
         M = x2.shape[0]
         dev = x.device
-        e4 = torch.float8_e4m3fn
-        tens = granularity == GRAN_TENSOR
-        x_q = torch.empty((M, K), dtype=e4, device=dev)
-        w_q = torch.empty((N, K), dtype=e4, device=dev)
-        x_inv = torch.empty(1 if tens else M, dtype=torch.float32, device=dev)
-        w_inv = torch.empty(1 if tens else N, dtype=torch.float32, device=dev)
-        xt_q = torch.empty((K, M), dtype=e4, device=dev) if tens else None
-        wt_q = torch.empty((K, N), dtype=e4, device=dev) if tens else None
-        saved = make_saved(x_q, x_inv, w_q, w_inv, xt_q, wt_q)
+        saved, bufs = linear_saved_alloc(M, K, N, granularity, keep_xt=wgrad_mode == WGRAD_FP8, device=dev)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         fp8_linear_fwd(x2, w, granularity, MM_FAST_ACCUM, y, saved,
                        _workspace(fp8_workspace_size(OP_LINEAR_FWD, M, K, N, granularity), dev))
-        ctx.save_for_backward(x2, w, x_q, x_inv, w_q, w_inv, *(t for t in (xt_q, wt_q) if t is not None))
+        # the FP8 copies and scales for the backward pass (absent ones as empty placeholders)
+        ctx.save_for_backward(x2, w, *(b if b is not None else x2.new_empty(0) for b in bufs))
+        ctx.present = tuple(b is not None for b in bufs)
         ctx.granularity, ctx.wgrad_mode, ctx.x_shape = granularity, wgrad_mode, x.shape
         return y.reshape(*x.shape[:-1], N)
 
     @staticmethod
     def backward(ctx, dy):
-        x2, w, x_q, x_inv, w_q, w_inv, *t = ctx.saved_tensors
-        xt_q, wt_q = (t[0], t[1]) if t else (None, None)
-        saved = make_saved(x_q, x_inv, w_q, w_inv, xt_q, wt_q)
+        x2, w, *bufs = ctx.saved_tensors
+        bufs = [b if keep else None for b, keep in zip(bufs, ctx.present)]
+        saved = make_saved(*bufs)
         M, K = x2.shape
         N = w.shape[0]
         dy2 = dy.reshape(-1, N).to(torch.bfloat16).contiguous()
@@ -63,7 +57,8 @@ class Fp8LinearFunction(torch.autograd.Function):
 
 
 class Fp8Linear(torch.nn.Module):
-    """Drop-in for a bias-free torch.nn.Linear: the weight stays bf16; the matmuls run in FP8."""
+    """Drop-in for a bias-free torch.nn.Linear: the weight stays bf16; the matmuls run in FP8
+    (granularity GRAN_TENSOR, GRAN_ROW or GRAN_MX; MX needs dimensions that are multiples of 128)."""
 
     def __init__(self, in_features, out_features, granularity=GRAN_ROW, wgrad_mode=WGRAD_BF16, weight=None,
                  device=None):
@@ -81,7 +76,7 @@ class Fp8Linear(torch.nn.Module):
         return Fp8LinearFunction.apply(x.to(torch.bfloat16), self.weight, self.granularity, self.wgrad_mode)
 
     def extra_repr(self):
-        g = {GRAN_ROW: "row", GRAN_TENSOR: "tensor"}[self.granularity]
+        g = {GRAN_ROW: "row", GRAN_TENSOR: "tensor", GRAN_MX: "mx"}[self.granularity]
         w = {WGRAD_BF16: "bf16", WGRAD_FP8: "fp8"}[self.wgrad_mode]
         return f"in_features={self.in_features}, out_features={self.out_features}, scaling={g}, wgrad={w}"
 

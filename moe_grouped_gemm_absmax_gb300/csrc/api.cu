@@ -517,6 +517,13 @@ static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad
     return o;
   };
   const bool rows = gran == FP8_GRAN_ROW, fp8w = wgrad == FP8_WGRAD_FP8;
+  if (gran == FP8_GRAN_MX) {  // dY in both layouts; its row-major then column-major MX scales
+    L.dy_q = take((size_t)(M * N));
+    L.dyt_q = fp8w ? take((size_t)(N * M)) : 0;
+    L.dy_inv = take((size_t)(mx_scale_bytes(M, N) + (fp8w ? mx_scale_bytes(N, M) : 0)));
+    L.total = off;
+    return L;
+  }
   L.amax = take(4);
   L.dy_q = take((size_t)(M * N));
   L.dy_inv = take((size_t)(rows ? M : 1) * 4);
@@ -530,6 +537,27 @@ static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad
   L.col_scratch = rows ? take((size_t)col_ws_words(1, K > N ? K : N) * 4) : 0;
   L.total = off;
   return L;
+}
+
+// MX quantize of a bf16 [R, C] matrix: row-major codes q [R, C] with scales q_sf and, when qt is
+// given, the column-major copy qt [C, R] with scales qt_sf, from one read of x.
+static int mx_both(const fp8_tensor* x, int fmt, const fp8_tensor* q, const fp8_tensor* q_sf, const fp8_tensor* qt,
+                   const fp8_tensor* qt_sf, const Ctx& c) {
+  FP8_CHECK(valid_desc(x) && x->ndim == 2 && x->dtype == FP8_DT_BF16, FP8_ERR_INVALID_ARG);
+  const int64_t R = x->shape[0], C = x->shape[1];
+  FP8_CHECK(C % 128 == 0 && (!qt || R % 128 == 0), FP8_ERR_UNSUPPORTED);
+  FP8_CHECK(valid_desc(q) && q->dtype == fmt && shape_is(q, 2, R, C), FP8_ERR_INVALID_ARG);
+  FP8_CHECK(valid_desc(q_sf) && q_sf->dtype == FP8_DT_E8M0 && numel(q_sf) == mx_scale_bytes(R, C),
+            FP8_ERR_INVALID_ARG);
+  FP8_CHECK(aligned16(x->ptr) && aligned16(q->ptr) && aligned16(q_sf->ptr), FP8_ERR_ALIGNMENT);
+  if (qt) {
+    FP8_CHECK(valid_desc(qt) && qt->dtype == fmt && shape_is(qt, 2, C, R), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(valid_desc(qt_sf) && qt_sf->dtype == FP8_DT_E8M0 && numel(qt_sf) == mx_scale_bytes(C, R),
+              FP8_ERR_INVALID_ARG);
+    FP8_CHECK(aligned16(qt->ptr) && aligned16(qt_sf->ptr), FP8_ERR_ALIGNMENT);
+  }
+  return launch_mx_quant(x->ptr, 1, R, C, fmt, q->ptr, q_sf->ptr, qt ? qt->ptr : nullptr, R,
+                         qt ? qt_sf->ptr : nullptr, nullptr, 0, nullptr, c);
 }
 
 extern "C" size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granularity, int wgrad_mode) {
@@ -564,6 +592,13 @@ extern "C" int fp8_linear_fwd(const fp8_tensor* x, const fp8_tensor* w, int gran
                           workspace, workspace_bytes, c));
     FP8_TRY(quantize_impl(w, FP8_GRAN_TENSOR, FP8_DT_E4M3, FP8_LAYOUT_BOTH, &saved->w_q, &saved->wt_q, &saved->w_inv,
                           nullptr, workspace, workspace_bytes, c));
+  } else if (granularity == FP8_GRAN_MX) {
+    // x and W in both layouts, each from one read (the column-major copies feed the backward
+    // GEMMs); x's column-major copy only when the caller keeps one (FP8 weight gradient)
+    FP8_CHECK(M % 128 == 0 && K % 128 == 0 && N % 128 == 0, FP8_ERR_UNSUPPORTED);
+    FP8_TRY(mx_both(x, FP8_DT_E4M3, &saved->x_q, &saved->x_inv, saved->xt_q.ptr ? &saved->xt_q : nullptr,
+                    &saved->xt_inv, c));
+    FP8_TRY(mx_both(w, FP8_DT_E4M3, &saved->w_q, &saved->w_inv, &saved->wt_q, &saved->wt_inv, c));
   } else if (granularity == FP8_GRAN_ROW) {
     FP8_TRY(quantize_impl(x, FP8_GRAN_ROW, FP8_DT_E4M3, FP8_LAYOUT_ROW_MAJOR, &saved->x_q, nullptr, &saved->x_inv,
                           nullptr, nullptr, 0, c));
@@ -583,7 +618,8 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
   Ctx c;
   FP8_TRY(make_ctx(&c, stream, d_status));
   FP8_CHECK(valid_desc(dy) && saved && dy->ndim == 2 && dy->dtype == FP8_DT_BF16, FP8_ERR_INVALID_ARG);
-  FP8_CHECK(granularity == FP8_GRAN_TENSOR || granularity == FP8_GRAN_ROW, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(granularity == FP8_GRAN_TENSOR || granularity == FP8_GRAN_ROW || granularity == FP8_GRAN_MX,
+            FP8_ERR_INVALID_ARG);
   FP8_CHECK(wgrad_mode == FP8_WGRAD_FP8 || wgrad_mode == FP8_WGRAD_BF16, FP8_ERR_INVALID_ARG);
   const int64_t M = dy->shape[0], N = dy->shape[1];
   FP8_CHECK(saved->x_q.ndim == 2 && saved->x_q.shape[0] == M, FP8_ERR_INVALID_ARG);
@@ -595,6 +631,27 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
   FP8_CHECK(aligned16(workspace), FP8_ERR_ALIGNMENT);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   fp8_tensor dy_q = T2(ws + L.dy_q, FP8_DT_E5M2, M, N);
+  if (granularity == FP8_GRAN_MX) {
+    // dY in both layouts from one read: rows (blocks along N) for dX = dY W, columns (blocks
+    // along M) for dW = dY^T x
+    FP8_CHECK(M % 128 == 0 && N % 128 == 0 && K % 128 == 0, FP8_ERR_UNSUPPORTED);
+    const bool want_dyt = fp8w && need_dw;
+    fp8_tensor dy_sf = T1(ws + L.dy_inv, FP8_DT_E8M0, mx_scale_bytes(M, N));
+    fp8_tensor dyt_q = T2(fp8w ? ws + L.dyt_q : nullptr, FP8_DT_E5M2, N, M);
+    fp8_tensor dyt_sf = T1(ws + L.dy_inv + mx_scale_bytes(M, N), FP8_DT_E8M0, mx_scale_bytes(N, M));
+    FP8_TRY(mx_both(dy, FP8_DT_E5M2, &dy_q, &dy_sf, want_dyt ? &dyt_q : nullptr, &dyt_sf, c));
+    if (dx && dx->ptr) FP8_TRY(scaled_mm_impl(&dy_q, &saved->wt_q, &dy_sf, &saved->wt_inv, dx, 0, c));
+    if (need_dw) {
+      if (fp8w) {
+        FP8_CHECK(saved->xt_q.ptr, FP8_ERR_INVALID_ARG);
+        FP8_TRY(scaled_mm_impl(&dyt_q, &saved->xt_q, &dyt_sf, &saved->xt_inv, dw, 0, c));
+      } else {
+        FP8_CHECK(valid_desc(x) && x->dtype == FP8_DT_BF16 && shape_is(x, 2, M, K), FP8_ERR_INVALID_ARG);
+        FP8_TRY(scaled_mm_impl(dy, x, nullptr, nullptr, dw, FP8_MM_A_MN_MAJOR | FP8_MM_B_MN_MAJOR, c));
+      }
+    }
+    return FP8_OK;
+  }
   fp8_tensor dy_inv = T1(ws + L.dy_inv, FP8_DT_F32, rows ? M : 1);
   fp8_tensor dyt_q = T2(fp8w ? ws + L.dyt_q : nullptr, FP8_DT_E5M2, N, M);
   if (!rows) {

@@ -18,13 +18,7 @@ def fp8():
 def _direct(fp8, x, w, dy, gran, wgrad):
     M, K = x.shape
     N = w.shape[0]
-    e4 = torch.float8_e4m3fn
-    tens = gran == fp8.GRAN_TENSOR
-    xq, wq = torch.empty((M, K), dtype=e4, device="cuda"), torch.empty((N, K), dtype=e4, device="cuda")
-    xi, wi = torch.empty(1 if tens else M, device="cuda"), torch.empty(1 if tens else N, device="cuda")
-    xt = torch.empty((K, M), dtype=e4, device="cuda") if tens else None
-    wt = torch.empty((K, N), dtype=e4, device="cuda") if tens else None
-    saved = fp8.make_saved(xq, xi, wq, wi, xt, wt)
+    saved, _bufs = fp8.linear_saved_alloc(M, K, N, gran, keep_xt=wgrad == fp8.WGRAD_FP8)
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
     dw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
@@ -37,7 +31,8 @@ def _direct(fp8, x, w, dy, gran, wgrad):
 
 
 @pytest.mark.parametrize("gran_name,wgrad_name", [("GRAN_ROW", "WGRAD_BF16"), ("GRAN_ROW", "WGRAD_FP8"),
-                                                  ("GRAN_TENSOR", "WGRAD_FP8")])
+                                                  ("GRAN_TENSOR", "WGRAD_FP8"), ("GRAN_MX", "WGRAD_FP8"),
+                                                  ("GRAN_MX", "WGRAD_BF16")])
 def test_function_matches_entry_points(fp8, gran_name, wgrad_name):
     from moe_grouped_gemm_absmax_gb300.autograd import Fp8LinearFunction
     gran, wgrad = getattr(fp8, gran_name), getattr(fp8, wgrad_name)

@@ -289,3 +289,47 @@ def test_mx_end_to_end_quantize_then_gemm(fp8):
     assert np.array_equal(codes(wq), cw) and np.array_equal(mx_unblock(ws, N, K), sw)
     ref, absacc = oracle.gemm_mx(cx, E4, cw, E4, sx, sw)
     check_gemm(out, ref, absacc, True)
+
+
+# ---------------------------------------------------------------------------- Linear
+
+@pytest.mark.parametrize("wgrad_name", ["WGRAD_FP8", "WGRAD_BF16"])
+def test_mx_linear_fwd_bwd(fp8, wgrad_name):
+    """The Linear with the MX recipe: x and W quantized to MX e4m3 in both layouts, dY to MX
+    e5m2 in both layouts; y = x W^T, dX = dY W (W's blocks along N), dW = dY^T x (blocks along
+    M) or the bf16 weight gradient."""
+    wgrad = getattr(fp8, wgrad_name)
+    M, K, N = 256, 384, 512
+    x, w, dy = W.linear_inputs(M, K, N, seed=17, outliers=True)
+    xd, wd, dyd = x.cuda(), w.cuda(), dy.cuda()
+    saved, bufs = fp8.linear_saved_alloc(M, K, N, fp8.GRAN_MX, keep_xt=wgrad == fp8.WGRAD_FP8)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fp8.fp8_linear_fwd(xd, wd, fp8.GRAN_MX, fp8.MM_FAST_ACCUM, y, saved, None, st)
+    ws = torch.empty(max(fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_MX, wgrad), 16),
+                     dtype=torch.uint8, device="cuda")
+    fp8.fp8_linear_bwd(dyd, saved, xd, wd, fp8.GRAN_MX, wgrad, dx, dw, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    x_q, x_inv, w_q, w_inv, xt_q, wt_q, xt_inv, wt_inv = bufs
+    cx, sx = oracle.mx_quantize_rows(bits(x), E4)
+    cw, sw = oracle.mx_quantize_rows(bits(w), E4)
+    cwt, swt = oracle.mx_quantize_cols(bits(w), E4)   # W^T [K, N], blocks along N
+    assert np.array_equal(codes(x_q), cx) and np.array_equal(mx_unblock(x_inv, M, K), sx)
+    assert np.array_equal(codes(w_q), cw) and np.array_equal(mx_unblock(w_inv, N, K), sw)
+    assert np.array_equal(codes(wt_q), cwt) and np.array_equal(mx_unblock(wt_inv, K, N), swt)
+    ref, absacc = oracle.gemm_mx(cx, E4, cw, E4, sx, sw)
+    check_gemm(y, ref, absacc, True)
+    cdy, sdy = oracle.mx_quantize_rows(bits(dy), E5)
+    ref, absacc = oracle.gemm_mx(cdy, E5, cwt, E4, sdy, swt)
+    check_gemm(dx, ref, absacc, True)
+    if wgrad == fp8.WGRAD_FP8:
+        cxt, sxt = oracle.mx_quantize_cols(bits(x), E4)    # x^T [K, M], blocks along M
+        assert np.array_equal(codes(xt_q), cxt) and np.array_equal(mx_unblock(xt_inv, K, M), sxt)
+        cdyt, sdyt = oracle.mx_quantize_cols(bits(dy), E5)  # dY^T [N, M]
+        ref, absacc = oracle.gemm_mx(cdyt, E5, cxt, E4, sdyt, sxt)
+    else:
+        ref, absacc = oracle.gemm_bf16(bits(dy), bits(x), a_trans=True, b_trans=True)
+    check_gemm(dw, ref, absacc, True)
