@@ -147,12 +147,18 @@ class DenseLinearStep(Step):
         self.h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (self.y, self.dx, self.dw)]
         self.d_in = [[torch.empty_like(t) for t in (self.x, self.w, self.dy)] for _ in range(2)]
         self.d_out = [[torch.empty_like(t) for t in (self.y, self.dx, self.dw)] for _ in range(2)]
-        self.saved = f.make_saved(self.xq, self.xi, self.wq, self.wi)
-        self.ws = torch.empty(max(f.fp8_workspace_size(f.OP_LINEAR_BWD, self.M, self.K, self.N, f.GRAN_ROW,
-                                                       f.WGRAD_BF16), 256), dtype=torch.uint8, device=dev)
+        self.e2e_buffers(dev)
         self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
         return sum(t.numel() * t.element_size() for t in self.h_in), \
             sum(t.numel() * t.element_size() for t in self.h_out)
+
+    def e2e_buffers(self, dev):
+        """Saved FP8 copies and the backward workspace of the public Linear entry points."""
+        f = self.fp8
+        self.e2e_gran, self.e2e_wgrad = f.GRAN_ROW, f.WGRAD_BF16
+        self.saved = f.make_saved(self.xq, self.xi, self.wq, self.wi)
+        self.ws = torch.empty(max(f.fp8_workspace_size(f.OP_LINEAR_BWD, self.M, self.K, self.N, f.GRAN_ROW,
+                                                       f.WGRAD_BF16), 256), dtype=torch.uint8, device=dev)
 
     def e2e_run_steps(self, n):
         """n steps through fp8_linear_fwd / fp8_linear_bwd, each with its host->device input copy
@@ -185,8 +191,8 @@ class DenseLinearStep(Step):
                 comp.wait_event(out_done[s])  # these outputs have been copied out
             x, w, dy = self.d_in[s]
             y, dx, dw = self.d_out[s]
-            f.fp8_linear_fwd(x, w, f.GRAN_ROW, f.MM_FAST_ACCUM, y, self.saved)
-            f.fp8_linear_bwd(dy, self.saved, x, w, f.GRAN_ROW, f.WGRAD_BF16, dx, dw, self.ws)
+            f.fp8_linear_fwd(x, w, self.e2e_gran, f.MM_FAST_ACCUM, y, self.saved)
+            f.fp8_linear_bwd(dy, self.saved, x, w, self.e2e_gran, self.e2e_wgrad, dx, dw, self.ws)
             done[s].record(comp)
             with torch.cuda.stream(self.s_out):
                 self.s_out.wait_event(done[s])
@@ -445,6 +451,216 @@ class MoeFwdBwdStep(Step):
         f.fp8_grouped_mm(self.dYt, self.At, self.ends, self.dYti, self.Ati, self.dW, f.GROUPED_JAGGED_K)
 
 
+class DenseMxLinearStep(DenseLinearStep):
+    """Linear fwd+bwd with MXFP8 everywhere: x, W (e4m3) and dY (e5m2) each quantized once into
+    both layouts (blocks of 32 along K for the row-major copies, along M / N for the column-major
+    ones); fwd, dX and dW are block-scaled FP8 GEMMs."""
+    dtype = "mxfp8 e4m3/e5m2 (E8M0 scales per 32, fp32 accumulate)"
+
+    def __init__(self, fp8, M, K, N, seed=0, device="cuda"):
+        self.fp8, self.M, self.K, self.N = fp8, M, K, N
+        self.name = "llama3-8b-mlp-up-mx" if (M, K, N) == (8192, 4096, 14336) else f"linear-mx-{M}x{K}x{N}"
+        self.x, self.w, self.dy = W.linear_inputs(M, K, N, seed=seed, device=device, outliers=True)
+        d = device
+        e4, e5, u8 = torch.float8_e4m3fn, torch.float8_e5m2, torch.uint8
+        sb = fp8.fp8_mx_scale_bytes
+        # codes in both layouts; each scale buffer holds the row-major scales, then the column-major ones
+        self.xq, self.xtq = torch.empty((M, K), dtype=e4, device=d), torch.empty((K, M), dtype=e4, device=d)
+        self.wq, self.wtq = torch.empty((N, K), dtype=e4, device=d), torch.empty((K, N), dtype=e4, device=d)
+        self.dyq, self.dytq = torch.empty((M, N), dtype=e5, device=d), torch.empty((N, M), dtype=e5, device=d)
+        self.xs = torch.empty(sb(M, K) + sb(K, M), dtype=u8, device=d)
+        self.wsc = torch.empty(sb(N, K) + sb(K, N), dtype=u8, device=d)
+        self.dys = torch.empty(sb(M, N) + sb(N, M), dtype=u8, device=d)
+        self.nx, self.nw, self.nd = sb(M, K), sb(N, K), sb(M, N)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=d)
+        self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=d)
+        f = 2.0 * M * N * K
+        dual = lambda r, c: 4 * r * c + 2 * (r * c // 32)  # bf16 read, two code copies, two scale sets
+        self.kernels = [
+            ("mx_quantize x e4m3 rows+cols", "hbm", dual(M, K), "hbm"),
+            ("mx_quantize W e4m3 rows+cols", "hbm", dual(N, K), "hbm"),
+            ("gemm_mx fwd", "tensor", f, "fp8"),
+            ("mx_quantize dY e5m2 rows+cols", "hbm", dual(M, N), "hbm"),
+            ("gemm_mx dX", "tensor", f, "fp8"),
+            ("gemm_mx dW", "tensor", f, "fp8"),
+        ]
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_quantize(self.x, f.GRAN_MX, f.DT_E4M3, f.LAYOUT_BOTH, self.xq, self.xtq, self.xs)
+        mark(1)
+        f.fp8_quantize(self.w, f.GRAN_MX, f.DT_E4M3, f.LAYOUT_BOTH, self.wq, self.wtq, self.wsc)
+        mark(2)
+        f.fp8_scaled_mm(self.xq, self.wq, self.xs[:self.nx], self.wsc[:self.nw], self.y, f.MM_FAST_ACCUM)
+        mark(3)
+        f.fp8_quantize(self.dy, f.GRAN_MX, f.DT_E5M2, f.LAYOUT_BOTH, self.dyq, self.dytq, self.dys)
+        mark(4)
+        f.fp8_scaled_mm(self.dyq, self.wtq, self.dys[:self.nd], self.wsc[self.nw:], self.dx, 0)
+        mark(5)
+        f.fp8_scaled_mm(self.dytq, self.xtq, self.dys[self.nd:], self.xs[self.nx:], self.dw, 0)
+
+    def e2e_buffers(self, dev):
+        f = self.fp8
+        self.e2e_gran, self.e2e_wgrad = f.GRAN_MX, f.WGRAD_FP8
+        self.saved, self.saved_bufs = f.linear_saved_alloc(self.M, self.K, self.N, f.GRAN_MX, keep_xt=True, device=dev)
+        self.ws = torch.empty(max(f.fp8_workspace_size(f.OP_LINEAR_BWD, self.M, self.K, self.N, f.GRAN_MX,
+                                                       f.WGRAD_FP8), 256), dtype=torch.uint8, device=dev)
+
+    def cpu_sample(self, rows):
+        return dense_mx_cpu_sample(self.x[:rows].cpu(), self.w.cpu(), self.dy[:rows].cpu(), self.M)
+
+
+def dense_mx_cpu_sample(x, w, dy, full_rows):
+    """The oracle's MX quantize and MX GEMMs of one Linear step on the first rows of x / dY."""
+    import oracle
+    M, K = x.shape
+    N = w.shape[0]
+    xb, wb, db = W.bf16_bits(x), W.bf16_bits(w), W.bf16_bits(dy)
+
+    def run():
+        xq, xs = oracle.mx_quantize_rows(xb, oracle.E4M3)
+        wq, ws = oracle.mx_quantize_rows(wb, oracle.E4M3)
+        oracle.gemm_mx(xq, oracle.E4M3, wq, oracle.E4M3, xs, ws)
+        dq, ds = oracle.mx_quantize_rows(db, oracle.E5M2)
+        wtq, wts = oracle.mx_quantize_cols(wb, oracle.E4M3)
+        oracle.gemm_mx(dq, oracle.E5M2, wtq, oracle.E4M3, ds, wts)
+        dtq, dts = oracle.mx_quantize_cols(db, oracle.E5M2)
+        xtq, xts = oracle.mx_quantize_cols(xb, oracle.E4M3)
+        oracle.gemm_mx(dtq, oracle.E5M2, xtq, oracle.E4M3, dts, xts)
+    return run, 3 * 2.0 * M * N * K, f"llama3-8b-mlp-up-mx step on the first {M} of {full_rows} tokens (all of W)"
+
+
+class MoeFwdMxStep(MoeFwdStep):
+    """The DeepSeek-V3-shaped grouped forward with MXFP8: A quantized with its scales in the
+    segment-padded row space, W[e] per expert, one block-scaled grouped GEMM."""
+    dtype = "mxfp8 e4m3 (E8M0 scales per 32, fp32 accumulate)"
+
+    def __init__(self, fp8, seed=0, device="cuda"):
+        self.fp8 = fp8
+        self.name = "dsv3-moe-fwd-mx"
+        d = W.WORKLOADS[self.name].dims
+        E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+        counts = W.dsv3_counts(seed)
+        self.A, self.Wt, ends, _ = W.moe_inputs(E, M, K, N, counts, seed=seed, device=device)
+        self.ends = torch.from_numpy(ends).to(device)
+        self.counts = counts
+        sb = fp8.fp8_mx_scale_bytes
+        self.P = fp8.fp8_jagged_padded_rows(M, E)
+        self.Aq = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=device)
+        self.As = torch.empty(sb(self.P, K), dtype=torch.uint8, device=device)
+        self.Wq = torch.empty((E, N, K), dtype=torch.float8_e4m3fn, device=device)
+        self.Ws = torch.empty(E * sb(N, K), dtype=torch.uint8, device=device)
+        self.ws_a = torch.empty(max(fp8.fp8_workspace_size(fp8.OP_QUANTIZE, E, K, granularity=fp8.GRAN_MX) // 4, 4),
+                                dtype=torch.int32, device=device)
+        self.out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.E, self.M, self.K, self.N = E, M, K, N
+        f = 2.0 * M * N * K
+        self.kernels = [("mx_quantize A e4m3 rows", "hbm", 3 * M * K + M * K // 32, "hbm"),
+                        ("mx_quantize W[e] e4m3 rows", "hbm", 3 * E * N * K + E * N * K // 32, "hbm"),
+                        ("grouped_gemm_mx jagged-M", "tensor", f, "fp8")]
+
+    @property
+    def attainable_ms(self):
+        pk = self.peak_of
+        return {"grouped_gemm_mx jagged-M": grouped_attainable_ms(self.counts, self.N, self.K, 2, pk["fp8"], pk["hbm"])}
+
+    def cpu_sample(self, rows):
+        import oracle
+        ends = self.ends.cpu().numpy()
+        ridx = np.sort(np.random.default_rng(0).choice(self.M, 64, replace=False))
+        experts = np.unique(np.searchsorted(ends, ridx, side="right"))
+        ab = W.bf16_bits(self.A[torch.as_tensor(ridx, device=self.A.device)].cpu())
+        wb = {int(e): W.bf16_bits(self.Wt[int(e)].cpu()) for e in experts}
+
+        def run():
+            aq, as_ = oracle.mx_quantize_rows(ab, oracle.E4M3)
+            for i, r in enumerate(ridx):
+                e = int(np.searchsorted(ends, r, side="right"))
+                wq, ws = oracle.mx_quantize_rows(wb[e], oracle.E4M3)
+                oracle.gemm_mx(aq[i:i + 1], oracle.E4M3, wq, oracle.E4M3, as_[i:i + 1], ws)
+        return run, 2.0 * 64 * self.N * self.K, "64 routed rows: their MX quantize, their experts' weights, their outputs"
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_quantize(self.A, f.GRAN_MX, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Aq, None, self.As, self.ends, self.ws_a)
+        mark(1)
+        f.fp8_quantize(self.Wt, f.GRAN_MX, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Wq, None, self.Ws)
+        mark(2)
+        f.fp8_grouped_mm(self.Aq, self.Wq, self.ends, self.As, self.Ws, self.out, f.GROUPED_JAGGED_M)
+
+
+class MoeFwdBwdMxStep(MoeFwdBwdStep):
+    """The Llama4-shaped grouped fwd + bwd with MXFP8: A, W[e] and dY are each read once and
+    quantized into both layouts (row-major for the jagged-M GEMMs, column-major for dX's
+    weights and for the jagged-K weight gradient); three block-scaled grouped GEMMs."""
+    dtype = "mxfp8 e4m3/e5m2 (E8M0 scales per 32, fp32 accumulate)"
+
+    def __init__(self, fp8, seed=0, device="cuda"):
+        self.fp8 = fp8
+        self.name = "llama4-moe-fwdbwd-mx"
+        d = W.WORKLOADS[self.name].dims
+        E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+        counts = W.llama4_counts(seed)
+        self.counts = counts
+        self.A, self.Wt, ends, self.dY = W.moe_inputs(E, M, K, N, counts, seed=seed, device=device, with_grad=True)
+        self.ends = torch.from_numpy(ends).to(device)
+        e4, e5, u8 = torch.float8_e4m3fn, torch.float8_e5m2, torch.uint8
+        sb = fp8.fp8_mx_scale_bytes
+        P = self.P = fp8.fp8_jagged_padded_rows(M, E)
+        dev = device
+        self.Aq, self.At = torch.empty((M, K), dtype=e4, device=dev), torch.empty((K, P), dtype=e4, device=dev)
+        self.A_s = torch.empty(sb(P, K) + sb(K, P), dtype=u8, device=dev)      # rows (padded), then A^T
+        self.Wq, self.Wtq = torch.empty((E, N, K), dtype=e4, device=dev), torch.empty((E, K, N), dtype=e4, device=dev)
+        self.W_s = torch.empty(E * (sb(N, K) + sb(K, N)), dtype=u8, device=dev)  # W[e] rows, then W[e]^T
+        self.dYq, self.dYt = torch.empty((M, N), dtype=e5, device=dev), torch.empty((N, P), dtype=e5, device=dev)
+        self.dY_s = torch.empty(sb(P, N) + sb(N, P), dtype=u8, device=dev)
+        self.out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        self.dW = torch.empty((E, N, K), dtype=torch.bfloat16, device=dev)
+        nws = max(fp8.fp8_workspace_size(fp8.OP_QUANTIZE, E, 0, granularity=fp8.GRAN_MX) // 4, 4)
+        self.ws_a = torch.empty(nws, dtype=torch.int32, device=dev)
+        self.ws_dy = torch.empty(nws, dtype=torch.int32, device=dev)
+        self.nA, self.nW, self.ndY = sb(P, K), E * sb(N, K), sb(P, N)
+        self.E, self.M, self.K, self.N = E, M, K, N
+        f = 2.0 * M * N * K
+        self.kernels = [("mx_quantize A e4m3 rows+cols jagged", "hbm", 4 * M * K + 2 * M * K // 32, "hbm"),
+                        ("mx_quantize W[e] e4m3 rows+cols", "hbm", 4 * E * N * K + 2 * E * N * K // 32, "hbm"),
+                        ("grouped_gemm_mx fwd jagged-M", "tensor", f, "fp8"),
+                        ("mx_quantize dY e5m2 rows+cols jagged", "hbm", 4 * M * N + 2 * M * N // 32, "hbm"),
+                        ("grouped_gemm_mx dX jagged-M", "tensor", f, "fp8"),
+                        ("grouped_gemm_mx dW jagged-K", "tensor", f, "fp8")]
+
+    @property
+    def attainable_ms(self):
+        pk = self.peak_of
+        c, N, K = self.counts, self.N, self.K
+        return {"grouped_gemm_mx fwd jagged-M": grouped_attainable_ms(c, N, K, 2, pk["fp8"], pk["hbm"]),
+                "grouped_gemm_mx dX jagged-M": grouped_attainable_ms(c, K, N, 2, pk["fp8"], pk["hbm"]),
+                "grouped_gemm_mx dW jagged-K": grouped_attainable_ms(c, N, K, 2, pk["fp8"], pk["hbm"], jagged_k=True)}
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_quantize(self.A, f.GRAN_MX, f.DT_E4M3, f.LAYOUT_BOTH, self.Aq, self.At, self.A_s, self.ends, self.ws_a)
+        mark(1)
+        f.fp8_quantize(self.Wt, f.GRAN_MX, f.DT_E4M3, f.LAYOUT_BOTH, self.Wq, self.Wtq, self.W_s)
+        mark(2)
+        f.fp8_grouped_mm(self.Aq, self.Wq, self.ends, self.A_s[:self.nA], self.W_s[:self.nW], self.out,
+                         f.GROUPED_JAGGED_M)
+        mark(3)
+        f.fp8_quantize(self.dY, f.GRAN_MX, f.DT_E5M2, f.LAYOUT_BOTH, self.dYq, self.dYt, self.dY_s, self.ends,
+                       self.ws_dy)
+        mark(4)
+        f.fp8_grouped_mm(self.dYq, self.Wtq, self.ends, self.dY_s[:self.ndY], self.W_s[self.nW:], self.dX,
+                         f.GROUPED_JAGGED_M)
+        mark(5)
+        f.fp8_grouped_mm(self.dYt, self.At, self.ends, self.dY_s[self.ndY:], self.A_s[self.nA:], self.dW,
+                         f.GROUPED_JAGGED_K)
+
+
 def make_step(fp8, name):
     if name == "llama3-8b-mlp-up":
         return DenseLinearStep(fp8, 8192, 4096, 14336)
@@ -456,6 +672,12 @@ def make_step(fp8, name):
         return MoeFwdStep(fp8)
     if name == "llama4-moe-fwdbwd":
         return MoeFwdBwdStep(fp8)
+    if name == "llama3-8b-mlp-up-mx":
+        return DenseMxLinearStep(fp8, 8192, 4096, 14336)
+    if name == "dsv3-moe-fwd-mx":
+        return MoeFwdMxStep(fp8)
+    if name == "llama4-moe-fwdbwd-mx":
+        return MoeFwdBwdMxStep(fp8)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -714,7 +936,8 @@ def main():
                 cfg[k] = getattr(step, k)
         line = {"metric": METRIC, "value": round(value, 2), "unit": step.unit, "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(total_ms_max / args.steps, 5), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "fp8 e4m3/e5m2 (fp32 accumulate), bf16 wgrad",
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": getattr(step, "dtype", "fp8 e4m3/e5m2 (fp32 accumulate), bf16 wgrad"),
                 "data": "synthetic", "config": cfg, "roofline": roofline, "kernels": kernels,
                 "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
                 "wall_s": round(wall, 3), "impl": "fp8lin"}

@@ -79,3 +79,20 @@ def segpad_cols(q_rows: np.ndarray, ends, P: int) -> np.ndarray:
         pos += -(-(e - prev) // 128) * 128
         prev = e
     return out
+
+
+def mx_offsets(rows, K):
+    """Byte offsets of (row r, K block j) in the MX scale layout of include/fp8lin.h, for the
+    given rows (an index array) and every j < K / 32: a pure index permutation."""
+    r = np.asarray(rows, np.int64)[:, None]
+    j = np.arange(K // 32, dtype=np.int64)[None, :]
+    return ((r // 128) * (K // 128) + j // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j % 4
+
+
+def mx_unblock_rows(sf, rows, K):
+    """Plain E8M0 codes [len(rows), K / 32] of the given rows, read from layout bytes (a device
+    tensor is indexed on the device; only the selected codes come back)."""
+    off = mx_offsets(rows, K)
+    if isinstance(sf, torch.Tensor):
+        return sf[torch.as_tensor(off.ravel(), device=sf.device)].cpu().numpy().reshape(off.shape)
+    return np.asarray(sf)[off]

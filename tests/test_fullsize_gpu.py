@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.gpu_util import bits, check_gemm, codes, f32_bits
+from tests.gpu_util import bits, check_gemm, codes, f32_bits, mx_unblock_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -166,3 +166,108 @@ def test_llama4_grouped_forward_backward(fp8, bench):
         check_gemm(st.dW[e][nsel][:, ksel], ref, acc, True)
         pstart += -(-cnt // 128) * 128
         prev = end
+
+
+# ---------------------------------------------------------------------------- MXFP8 workloads
+
+_mx_unblock_rows = mx_unblock_rows
+
+
+def test_llama3_mlp_up_mx(fp8, bench):
+    """The MX Linear at full size: sampled rows / columns of every quantized copy bit-exact, and
+    sampled elements of y, dX and dW within the GEMM tolerance."""
+    st = bench.make_step(fp8, "llama3-8b-mlp-up-mx")
+    st.run()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(21)
+    M, K, N = st.M, st.K, st.N
+    mi = np.sort(rng.choice(M, 6, replace=False))
+    ni = np.sort(rng.choice(N, 24, replace=False))
+    ki = np.sort(rng.choice(K, 24, replace=False))
+    msel, nsel, ksel = (torch.as_tensor(a, device="cuda") for a in (mi, ni, ki))
+    xr, xrs = oracle.mx_quantize_rows(_rows(st.x, mi), E4)
+    assert np.array_equal(codes(st.xq[msel]), xr) and np.array_equal(_mx_unblock_rows(st.xs[:st.nx], mi, K), xrs)
+    wr, wrs = oracle.mx_quantize_rows(_rows(st.w, ni), E4)
+    assert np.array_equal(codes(st.wq[nsel]), wr) and np.array_equal(_mx_unblock_rows(st.wsc[:st.nw], ni, K), wrs)
+    dyr, dyrs = oracle.mx_quantize_rows(_rows(st.dy, mi), E5)
+    wc, wcs = oracle.mx_quantize_rows(np.ascontiguousarray(_cols(st.w, ki).T), E4)  # W^T rows k, blocks along N
+    assert np.array_equal(codes(st.wtq[ksel]), wc) and np.array_equal(_mx_unblock_rows(st.wsc[st.nw:], ki, N), wcs)
+    ref, acc = oracle.gemm_mx(xr, E4, wr, E4, xrs, wrs)
+    check_gemm(st.y[msel][:, nsel], ref, acc, True)
+    ref, acc = oracle.gemm_mx(dyr, E5, wc, E4, dyrs, wcs)
+    check_gemm(st.dx[msel][:, ksel], ref, acc, True)
+    # dW[n, k] = sum over all M tokens of dY^T (blocks along M) and x^T (blocks along M)
+    dyc, dycs = oracle.mx_quantize_rows(np.ascontiguousarray(_cols(st.dy, ni).T), E5)
+    xc, xcs = oracle.mx_quantize_rows(np.ascontiguousarray(_cols(st.x, ki).T), E4)
+    assert np.array_equal(codes(st.dytq[nsel]), dyc) and np.array_equal(codes(st.xtq[ksel]), xc)
+    ref, acc = oracle.gemm_mx(dyc, E5, xc, E4, dycs, xcs)
+    check_gemm(st.dw[nsel][:, ksel], ref, acc, True)
+
+
+def test_dsv3_grouped_forward_mx(fp8, bench):
+    st = bench.make_step(fp8, "dsv3-moe-fwd-mx")
+    st.run()
+    torch.cuda.synchronize()
+    ends = st.ends.cpu().numpy()
+    starts, _, pstarts, _ = oracle.mx_padded_segments(ends)
+    rng = np.random.default_rng(23)
+    mi = np.concatenate([np.sort(rng.choice(st.M, 6, replace=False)), [0, st.M - 1]])
+    ni = np.sort(rng.choice(st.N, 24, replace=False))
+    nsel = torch.as_tensor(ni, device="cuda")
+    ar, ars = oracle.mx_quantize_rows(_rows(st.A, mi), E4)
+    assert np.array_equal(codes(st.Aq[torch.as_tensor(mi, device="cuda")]), ar)
+    for r, m in enumerate(mi):
+        e = _expert_of(ends, m)
+        prow = pstarts[e] + (m - starts[e])  # A's scales sit at the segment-padded row
+        assert np.array_equal(_mx_unblock_rows(st.As, [prow], st.K), ars[r:r + 1])
+        wq, ws = oracle.mx_quantize_rows(bits(st.Wt[e][nsel].cpu()), E4)
+        assert np.array_equal(codes(st.Wq[e][nsel]), wq)
+        per = st.Ws.numel() // st.E
+        assert np.array_equal(_mx_unblock_rows(st.Ws[e * per:(e + 1) * per], ni, st.K), ws)
+        ref, acc = oracle.gemm_mx(ar[r:r + 1], E4, wq, E4, ars[r:r + 1], ws)
+        check_gemm(st.out[int(m)][nsel].unsqueeze(0), ref, acc, True)
+
+
+def test_llama4_grouped_forward_backward_mx(fp8, bench):
+    st = bench.make_step(fp8, "llama4-moe-fwdbwd-mx")
+    st.run()
+    torch.cuda.synchronize()
+    ends = st.ends.cpu().numpy()
+    starts, counts, pstarts, _ = oracle.mx_padded_segments(ends)
+    rng = np.random.default_rng(24)
+    mi = np.sort(rng.choice(st.M, 5, replace=False))
+    ni = np.sort(rng.choice(st.N, 12, replace=False))
+    ki = np.sort(rng.choice(st.K, 12, replace=False))
+    nsel, ksel = torch.as_tensor(ni, device="cuda"), torch.as_tensor(ki, device="cuda")
+    E, N, K = st.E, st.N, st.K
+    sb = fp8.fp8_mx_scale_bytes
+    ar, ars = oracle.mx_quantize_rows(_rows(st.A, mi), E4)
+    dyr, dyrs = oracle.mx_quantize_rows(_rows(st.dY, mi), E5)
+    for r, m in enumerate(mi):
+        e = _expert_of(ends, m)
+        wb = bits(st.Wt[e].cpu())                      # [N, K]
+        wq, ws = oracle.mx_quantize_rows(wb[ni], E4)   # forward: W[e] rows n, blocks along K
+        ref, acc = oracle.gemm_mx(ar[r:r + 1], E4, wq, E4, ars[r:r + 1], ws)
+        check_gemm(st.out[int(m)][nsel].unsqueeze(0), ref, acc, True)
+        wt, wts = oracle.mx_quantize_rows(np.ascontiguousarray(wb[:, ki].T), E4)  # W[e]^T rows k, blocks along N
+        assert np.array_equal(codes(st.Wtq[e][ksel]), wt)
+        base = st.nW + e * sb(K, N)
+        assert np.array_equal(_mx_unblock_rows(st.W_s[base:base + sb(K, N)], ki, N), wts)
+        ref, acc = oracle.gemm_mx(dyr[r:r + 1], E5, wt, E4, dyrs[r:r + 1], wts)
+        check_gemm(st.dX[int(m)][ksel].unsqueeze(0), ref, acc, True)
+    # dW[e, n, k]: both operands MX-quantized along the tokens of each (padded) segment
+    gq, gs = oracle.mx_quantize_jagged_cols(_cols(st.dY, ni), ends, E5)
+    xq, xs = oracle.mx_quantize_jagged_cols(_cols(st.A, ki), ends, E4)
+    Pu = gq.shape[1]
+    assert np.array_equal(codes(st.dYt[nsel])[:, :Pu], gq) and np.array_equal(codes(st.At[ksel])[:, :Pu], xq)
+    assert np.array_equal(_mx_unblock_rows(st.dY_s[st.ndY:], ni, st.P)[:, :Pu // 32], gs)
+    assert np.array_equal(_mx_unblock_rows(st.A_s[st.nA:], ki, st.P)[:, :Pu // 32], xs)
+    padded = -(-counts // 128) * 128
+    for e in range(E):
+        got = st.dW[e][nsel][:, ksel]
+        if counts[e] == 0:
+            assert torch.count_nonzero(got).item() == 0
+            continue
+        ps, pe = pstarts[e], pstarts[e] + padded[e]
+        ref, acc = oracle.gemm_mx(gq[:, ps:pe], E5, xq[:, ps:pe], E4, gs[:, ps // 32:pe // 32], xs[:, ps // 32:pe // 32])
+        check_gemm(got, ref, acc, True)

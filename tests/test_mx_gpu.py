@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.gpu_util import bits, check_gemm, codes, upload_codes
+from tests.gpu_util import bits, check_gemm, codes, mx_offsets, upload_codes
 
 pytestmark = pytest.mark.gpu
 
@@ -31,10 +31,7 @@ def fp8():
 
 
 def _offsets(rows_padded, K):
-    """Byte offset of (row r, K block j) in the MX scale layout, for all r < rows_padded, j < K/32."""
-    r = np.arange(rows_padded)[:, None]
-    j = np.arange(K // 32)[None, :]
-    return ((r // 128) * (K // 128) + j // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j % 4
+    return mx_offsets(np.arange(rows_padded), K)
 
 
 def mx_unblock(sf, rows, K):

@@ -144,6 +144,22 @@ WORKLOADS = {
         "Llama4-shaped MoE grouped fwd+bwd: 16 experts, K=5120, N=8192, 8192 rows with "
         "Dirichlet(0.5) routing; A N(0,1), W [16,8192,5120] N(0,0.02), dY N(0,1e-3)",
         dict(E=16, M=8192, K=5120, N=8192)),
+    # the same shapes with MXFP8 (blocks of 32, E8M0 scales) for every operand of every GEMM
+    "llama3-8b-mlp-up-mx": Workload(
+        "llama3-8b-mlp-up-mx",
+        "the llama3-8b-mlp-up Linear and inputs, MXFP8: x, W e4m3 and dY e5m2 quantized in both "
+        "layouts from one read each; fwd, dX and dW all MX GEMMs",
+        dict(M=8192, K=4096, N=14336)),
+    "dsv3-moe-fwd-mx": Workload(
+        "dsv3-moe-fwd-mx",
+        "the dsv3-moe-fwd layer and inputs, MXFP8: A (segment-padded scales) and W[e] e4m3, MX "
+        "grouped GEMM",
+        dict(E=256, M=131072, K=7168, N=2048)),
+    "llama4-moe-fwdbwd-mx": Workload(
+        "llama4-moe-fwdbwd-mx",
+        "the llama4-moe-fwdbwd layer and inputs, MXFP8: A, W[e] and dY each quantized once in "
+        "both layouts; fwd, dX and dW MX grouped GEMMs",
+        dict(E=16, M=8192, K=5120, N=8192)),
 }
 
 
