@@ -49,16 +49,20 @@ constexpr uint64_t kDrainNs = 2000000000ull;
 enum { kDense = 0, kJagM = 1, kJagK = 2 };
 enum { kFP8 = 0, kBF16 = 1, kMX = 2 };
 
-// MX (block-scaled) tiles are 192 columns wide: two accumulators (384 tensor-memory columns)
-// leave room for one scale-factor slot per ring stage. 192 = 6 groups of 32 columns, so a
-// tile's first column group sits at offset 0 or 2 inside a 4-group (128-row) scale block.
-// Twelve epilogue warps (three per lane quarter) take 64 columns each.
+// MX (block-scaled) tiles are 256 columns wide like the FP8 ones (an MMA's cost is set per
+// instruction, so narrower tiles run the tensor cores below their rate), but they keep ONE
+// accumulator: its 256 tensor-memory columns plus one 16-column scale-factor slot per ring stage
+// fit in the 512 columns, two accumulators would not. Sixteen epilogue warps (four per lane
+// quarter, 64 columns each) move the accumulator into registers right after the tile's MMAs and
+// release it at once, so the next tile's MMAs wait only for those loads, not for the stores.
 template <int KIND, int CG>
 struct Cfg {
-  static constexpr int TBN = KIND == kMX ? 192 : BN;     // tile columns
-  static constexpr int EPI_WARPS = KIND == kMX ? 12 : 8;
+  static constexpr int TBN = BN;                          // tile columns
+  static constexpr int NBUF = KIND == kMX ? 1 : 2;        // accumulators in tensor memory
+  static constexpr int EPI_WARPS = KIND == kMX ? 16 : 8;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int SF_WARP = 2 + EPI_WARPS;           // MX: the warp that copies scales to TMEM
+  static constexpr int THREADS = 64 + EPI_THREADS + (KIND == kMX ? 32 : 0);
   static constexpr int WCOLS = TBN * 4 / EPI_WARPS;      // columns per epilogue warp: 128 or 64
   static constexpr int A_BYTES = BM * BKB;               // this CTA's 128 rows of A
   static constexpr int B_ROWS = TBN / CG;                // this CTA's rows of B
@@ -68,11 +72,11 @@ struct Cfg {
   static constexpr int STAGE_BYTES = (TX_BYTES + 1023) / 1024 * 1024;
   static constexpr int STAGES = CG == 2 ? 5 : 4;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-  static constexpr int OUT_BYTES = CG == 2 ? EPI_WARPS * kStageOut : 0;
+  static constexpr int OUT_BYTES = (CG == 2 && KIND != kMX) ? EPI_WARPS * kStageOut : 0;
   static constexpr int TILE_M = BM * CG;
-  static constexpr int SF_COL0 = 2 * TBN;                // first scale-factor slot (16 columns each)
+  static constexpr int SF_COL0 = NBUF * TBN;             // first scale-factor slot (16 columns each)
 };
-static_assert(2 * 192 + 16 * 5 <= kTmemCols, "MX tensor-memory budget");
+static_assert(Cfg<kMX, 2>::SF_COL0 + 16 * Cfg<kMX, 2>::STAGES <= kTmemCols, "MX tensor-memory budget");
 
 struct GemmParams {
   int64_t M, N, K;     // tile space: rows of D, columns of D, contraction length (elements)
@@ -112,6 +116,8 @@ struct Shared {
   uint64_t tempty[2];
   uint64_t drain;
   uint64_t never;   // signalled by no one: the failure-detection test hook waits on it
+  uint64_t sff[5];  // MX: a stage's scales are in tensor memory
+  uint64_t sf_drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -282,6 +288,8 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
       mbar_init(&S.tempty[b], CG * kEpiThreads / 32);
     }
     mbar_init(&S.drain, 1);
+    for (int s2 = 0; s2 < STAGES; ++s2) mbar_init(&S.sff[s2], 1);
+    mbar_init(&S.sf_drain, 1);
     mbar_init(&S.never, 1);
     S.abort = 0;
     fence_mbar_init();
@@ -440,6 +448,11 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
       int buf = 0;
       uint32_t aphase = 0;
       bool ok = true;
+      // MX: stage 0's A descriptor and the four scale-factor ids
+      const uint64_t mx_a_desc0 = smem_desc(smem_u32(smem), 16, 1024);
+      uint32_t mx_id[4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) mx_id[kk] = idesc_sf_ids(p.idesc, (uint32_t)kk, (uint32_t)kk);
       if (p.test_stall && !mbar_wait(&S.never, 0, abort_flag, p.wait_ns)) {
         fail();
         ok = false;
@@ -447,9 +460,6 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
       for (int64_t t = unit; t < total && ok; t += n_units) {
         const int64_t nkb = tile_nkb<SCHED>(p, t, aux);
         if (nkb == 0) continue;
-        // MX: the B scales of the tile's first column group sit 0 or 2 columns into its slot
-        uint32_t sfb_off = 0;
-        if (KIND == kMX) sfb_off = (uint32_t)((get_tile<SCHED, C::TILE_M, TBN>(p, t, tpre, aux, pst).n0 / 32) & 3);
         if (!mbar_wait(&S.tempty[buf], aphase ^ 1, abort_flag, p.wait_ns)) {
           if (!*abort_flag) fail();
           break;
@@ -457,7 +467,8 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * TBN);
         for (int64_t kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&S.full[stage], phase, abort_flag, p.wait_ns)) {
+          // MX: the scale warp's commit on sff[stage] follows the stage's full barrier
+          if (!mbar_wait(KIND == kMX ? &S.sff[stage] : &S.full[stage], phase, abort_flag, p.wait_ns)) {
             if (!*abort_flag) fail();
             ok = false;
             break;
@@ -466,26 +477,22 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t sb = sa + C::A_BYTES;
           if (KIND == kMX) {
-            // this stage's scales into its tensor-memory slot: A (4 columns), then two B blocks
+            // the stage's scales are in its tensor-memory slot (copied by the scale warp).
+            // Descriptors are offsets of per-kernel bases (address field in 16-byte units), so
+            // the single issuing thread spends few instructions per stage.
             const uint32_t sf_t = tmem_base + (uint32_t)(C::SF_COL0 + 16 * stage);
-            const uint32_t ssf = sb + C::B_BYTES;
-#pragma unroll
-            for (int j = 0; j < 3; ++j) {
-              if (CG == 2)
-                tmem_cp_sf_pair(sf_t + 4 * j, smem_desc_plain(ssf + 512 * j, 128));
-              else
-                tmem_cp_sf(sf_t + 4 * j, smem_desc_plain(ssf + 512 * j, 128));
-            }
+            const uint64_t soff = (uint64_t)((stage * C::STAGE_BYTES) >> 4);
+            const uint64_t ad0 = mx_a_desc0 + soff;
+            const uint32_t sfb_t = sf_t + 4;  // 256-column tiles start on a 128-row scale block
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024);
+              const uint64_t ad = ad0 + 2 * kk;
+              const uint64_t bd = ad + (C::A_BYTES >> 4);
               const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-              const uint32_t id = idesc_sf_ids(p.idesc, (uint32_t)kk, (uint32_t)kk);
               if (CG == 2)
-                umma_mx_pair(d_tmem, ad, bd, id, sf_t, sf_t + 4 + sfb_off, acc);
+                umma_mx_pair(d_tmem, ad, bd, mx_id[kk], sf_t, sfb_t, acc);
               else
-                umma_mx(d_tmem, ad, bd, id, sf_t, sf_t + 4 + sfb_off, acc);
+                umma_mx(d_tmem, ad, bd, mx_id[kk], sf_t, sfb_t, acc);
             }
           } else {
 #pragma unroll
@@ -522,7 +529,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
           umma_commit_pair(&S.tfull[buf], 0x3);
         else
           umma_commit(&S.tfull[buf]);
-        if (++buf == 2) {
+        if (++buf == C::NBUF) {
           buf = 0;
           aphase ^= 1;
         }
@@ -532,6 +539,52 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
         umma_commit_pair(&S.drain, 0x3);
       else
         umma_commit(&S.drain);
+    }
+    __syncwarp();
+  } else if (KIND == kMX && warp == C::SF_WARP) {
+    // ============================ MX scale copies ============================
+    // For every stage the MMA thread will consume: wait for its loads, copy its three scale
+    // blocks into the stage's tensor-memory slot (shared memory -> tensor memory), and commit
+    // them to sff[stage]. Issued apart from the MMAs so that a copy never waits behind them;
+    // the slot is free because the stage was refilled only after its previous MMAs completed.
+    if (lane == 0 && issuer) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint64_t cp_desc0 = smem_desc_plain(smem_u32(smem) + C::A_BYTES + C::B_BYTES, 128);
+      for (int64_t t = unit; t < total && ok; t += n_units) {
+        const int64_t nkb = tile_nkb<SCHED>(p, t, aux);
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&S.full[stage], phase, abort_flag, p.wait_ns)) {
+            if (!*abort_flag) fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_t = tmem_base + (uint32_t)(C::SF_COL0 + 16 * stage);
+          const uint64_t cd = cp_desc0 + (uint64_t)((stage * C::STAGE_BYTES) >> 4);
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            if (CG == 2)
+              tmem_cp_sf_pair(sf_t + 4 * j, cd + 32 * j);
+            else
+              tmem_cp_sf(sf_t + 4 * j, cd + 32 * j);
+          }
+          if (CG == 2)
+            umma_commit_pair(&S.sff[stage], 0x1);
+          else
+            umma_commit(&S.sff[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // every copy into either CTA's tensor memory completes before it is released
+      if (CG == 2)
+        umma_commit_pair(&S.sf_drain, 0x3);
+      else
+        umma_commit(&S.sf_drain);
     }
     __syncwarp();
   } else {
@@ -599,6 +652,59 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
         break;
       }
       tc_fence_after();
+      if (KIND == kMX) {
+        // this warp's 64 columns into registers, the accumulator back to the MMAs, then stores
+        const uint32_t taddr = tmem_base + (uint32_t)c0 + ((uint32_t)(q * 32) << 16);
+        uint32_t va[32], vb[32];
+        tmem_ld32(taddr, va);
+        tmem_ld32(taddr + 32, vb);
+        tmem_ld_wait_regs(va);
+        tmem_ld_wait_regs(vb);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (CG == 2)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&S.tempty[0]), 0));
+          else
+            mbar_arrive(&S.tempty[0]);
+        }
+        aphase ^= 1;
+        if (row_ok) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t* v = h ? vb : va;
+            const int64_t n = T.n0 + c0 + 32 * h;
+            if (n >= p.N) break;
+            const bool full = p.vec_ok && n + 32 <= p.N;
+            if (p.out_f32) {
+              float* o = static_cast<float*>(p.out) + orow * p.ldo + n;
+              if (full) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                  *reinterpret_cast<uint4*>(o + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              } else {
+                for (int j = 0; j < 32 && n + j < p.N; ++j) o[j] = __uint_as_float(v[j]);
+              }
+            } else {
+              uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + n;
+              uint32_t wd[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const __nv_bfloat162 hb = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                wd[j] = *reinterpret_cast<const uint32_t*>(&hb);
+              }
+              if (full) {
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                  *reinterpret_cast<uint4*>(o + 2 * j) = make_uint4(wd[j], wd[j + 1], wd[j + 2], wd[j + 3]);
+              } else {
+                for (int j = 0; j < 32 && n + j < p.N; ++j) o[j] = (uint16_t)(wd[j >> 1] >> (16 * (j & 1)));
+              }
+            }
+          }
+        }
+        continue;
+      }
       const float sb_all = (KIND == kFP8 && p.sb_scalar) ? sb_mine : 1.0f;
       const uint32_t taddr = tmem_base + (uint32_t)(buf * TBN + c0) + ((uint32_t)(q * 32) << 16);
       // Pairs write through shared memory with TMA bulk-tensor stores of 32 rows x 128 bytes
@@ -717,12 +823,15 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
     }
   }
 
-  if (CG == 2 && warp >= 2 && lane == 0) bulk_wait_all();  // this warp's output stores are done
+  if (CG == 2 && warp >= 2 && warp < 2 + C::EPI_WARPS && lane == 0) bulk_wait_all();  // this warp's stores are done
   tc_fence_before();
   __syncthreads();
   if (CG == 2) cluster_barrier();  // no remote arrive or load into a CTA that has left
   if (warp == 1) {
-    if (lane == 0) mbar_wait(&S.drain, 0, nullptr, kDrainNs);  // the MMAs writing this CTA's TMEM
+    if (lane == 0) {
+      mbar_wait(&S.drain, 0, nullptr, kDrainNs);  // the MMAs writing this CTA's TMEM
+      if (KIND == kMX) mbar_wait(&S.sf_drain, 0, nullptr, kDrainNs);  // and the scale copies
+    }
     __syncwarp();
     tc_fence_after();
     if (CG == 2)
@@ -892,7 +1001,10 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
     p.tma_out = 1;
   }
 
-  if (mx) return launch_mx(g, p, to, pair, tile_m, c);
+  if (mx) {
+    p.tma_out = 0;  // the MX epilogue stores straight from registers
+    return launch_mx(g, p, to, pair, tile_m, c);
+  }
   if (fp8) {
     const uint32_t af = g.a_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
     const uint32_t bf = g.b_dtype == FP8_DT_E4M3 ? kFmtE4M3 : kFmtE5M2;
