@@ -154,33 +154,40 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const MxArgs a) {
       *reinterpret_cast<uint4*>(sx + rr * kInPitch + cc) = v[it];
     }
     __syncthreads();
-    // thread: column c of the tile, rows 64h .. 64h + 63 (blocks 2h and 2h + 1)
-    const int c = tid & (kTile - 1), h = tid >> 7;
-    uint32_t code2[2];
+    // thread: the column pair (2 cp, 2 cp + 1) of the tile, rows 32 qb .. 32 qb + 31 (one block
+    // per column). A 32-bit shared load holds the pair's bf16 values of one row, so the block
+    // maxima of both columns come from packed 16-bit maxima, one per row.
+    const int cp = tid & 63, qb = tid >> 6;
+    const int r0 = 32 * qb;
+    uint32_t w[32];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      uint32_t m = 0;
-      const int r0 = 64 * h + 32 * j;
-#pragma unroll 8
-      for (int r = 0; r < 32; ++r) m = max(m, (uint32_t)(sx[(r0 + r) * kInPitch + c] & 0x7FFFu));
-      code2[j] = mx_code<FMT>(m);
-      const float inv = mx_inv(code2[j]);
-      uint32_t w[8];
+    for (int r = 0; r < 32; ++r) w[r] = *reinterpret_cast<const uint32_t*>(sx + (r0 + r) * kInPitch + 2 * cp);
+    uint32_t m2 = 0;
 #pragma unroll
-      for (int r = 0; r < 32; r += 4) {
-        const uint32_t p01 = (uint32_t)sx[(r0 + r) * kInPitch + c] | ((uint32_t)sx[(r0 + r + 1) * kInPitch + c] << 16);
-        const uint32_t p23 =
-            (uint32_t)sx[(r0 + r + 2) * kInPitch + c] | ((uint32_t)sx[(r0 + r + 3) * kInPitch + c] << 16);
-        w[r / 4] = mx_cast2<FMT>(p01, inv) | (mx_cast2<FMT>(p23, inv) << 16);
-      }
-      uint8_t* dst = so + c * kOutPitch + r0;
-      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+    for (int r = 0; r < 32; ++r) m2 = absmax2(m2, w[r]);
+    const uint32_t code_lo = mx_code<FMT>(m2 & 0xFFFFu), code_hi = mx_code<FMT>(m2 >> 16);
+    const float inv_lo = mx_inv(code_lo), inv_hi = mx_inv(code_hi);
+    uint32_t olo[8], ohi[8];
+#pragma unroll
+    for (int r = 0; r < 32; r += 4) {
+      // column 2 cp: the low halves of rows r .. r + 3; column 2 cp + 1: the high halves
+      const uint32_t l01 = (w[r] & 0xFFFFu) | (w[r + 1] << 16), l23 = (w[r + 2] & 0xFFFFu) | (w[r + 3] << 16);
+      const uint32_t h01 = (w[r] >> 16) | (w[r + 1] & 0xFFFF0000u), h23 = (w[r + 2] >> 16) | (w[r + 3] & 0xFFFF0000u);
+      olo[r / 4] = mx_cast2<FMT>(l01, inv_lo) | (mx_cast2<FMT>(l23, inv_lo) << 16);
+      ohi[r / 4] = mx_cast2<FMT>(h01, inv_hi) | (mx_cast2<FMT>(h23, inv_hi) << 16);
     }
+    uint8_t* dlo = so + (2 * cp) * kOutPitch + r0;
+    uint8_t* dhi = dlo + kOutPitch;
+    *reinterpret_cast<uint4*>(dlo) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+    *reinterpret_cast<uint4*>(dlo + 16) = make_uint4(olo[4], olo[5], olo[6], olo[7]);
+    *reinterpret_cast<uint4*>(dhi) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+    *reinterpret_cast<uint4*>(dhi + 16) = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
     {
       const int64_t nrb = a.ld_t / kTile;
       uint8_t* blk = a.sft + ((b * (a.C / kTile) + (c0 >> 7)) * nrb + (prow0 >> 7)) * 512;
-      *reinterpret_cast<uint16_t*>(blk + (c & 31) * 16 + (c >> 5) * 4 + 2 * h) = (uint16_t)(code2[0] | (code2[1] << 8));
+      const int c = 2 * cp;  // columns c and c + 1: same 32-column group, adjacent 16-byte rows
+      blk[(c & 31) * 16 + (c >> 5) * 4 + qb] = (uint8_t)code_lo;
+      blk[((c + 1) & 31) * 16 + (c >> 5) * 4 + qb] = (uint8_t)code_hi;
     }
     __syncthreads();
     // the transposed tile: row c of qt holds 128 codes (rows prow0 .. prow0 + 127), 8 lanes each
