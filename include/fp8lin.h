@@ -224,6 +224,33 @@ int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* o
                    const fp8_tensor* sA, const fp8_tensor* sB, fp8_tensor* out, int mode,
                    int flags, int32_t* d_status, void* stream);
 
+/*
+ * fp8_scaled_mm_amax — fp8_scaled_mm with the amax reduction of the NEXT quantization as side
+ * outputs of the epilogue ([T] Level 1: fewer kernels, no extra pass over HBM): row_amax[m] =
+ * max_n |out[m, n]| and col_amax[n] = max_m |out[m, n]| of the result as stored (bf16), as fp32
+ * values; col_amax may also be a single fp32 word, which then receives the maximum over the
+ * whole output (the tensorwise amax). These are exactly the maxima fp8_quantize computes on
+ * `out`, so fp8_quantize_from_amax then quantizes `out` from one read instead of two. out must
+ * be bf16, M and N as fp8_scaled_mm (dense); FP8 (not MX) or BF16 operands. Either amax pointer
+ * may be NULL. The call zeroes the amax buffers on its stream before the GEMM.
+ */
+int fp8_scaled_mm_amax(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA,
+                       const fp8_tensor* sB, fp8_tensor* out, int flags, fp8_tensor* row_amax,
+                       fp8_tensor* col_amax, int32_t* d_status, void* stream);
+
+/*
+ * fp8_quantize_from_amax — the scale and cast steps of fp8_quantize ([Q] section 2) with the amax
+ * step given: amax fp32 [1] (FP8_GRAN_TENSOR; ROW_MAJOR, COL_MAJOR or BOTH) or [C] (FP8_GRAN_COL,
+ * COL_MAJOR), holding bf16 values (the maxima of a bf16 tensor always are). x bf16 [R, C]; the
+ * outputs, inverse scales and their layouts as for fp8_quantize. When amax holds the true maxima
+ * of x (e.g. from fp8_scaled_mm_amax) the results are bit-identical to fp8_quantize's, from one
+ * read of x where fp8_quantize needs two. Row granularity: FP8_ERR_UNSUPPORTED (fp8_quantize
+ * reads each row once already). No workspace.
+ */
+int fp8_quantize_from_amax(const fp8_tensor* x, int granularity, int out_dtype, int layout,
+                           fp8_tensor* out, fp8_tensor* out_t, fp8_tensor* inv_scales,
+                           const fp8_tensor* amax, int32_t* d_status, void* stream);
+
 /* FP8 copies and inverse scales kept from the forward pass for the backward pass
  * ([Q] section 6: the autograd function saves the quantized tensors, not the bf16 inputs).
  * All buffers are caller-owned. */

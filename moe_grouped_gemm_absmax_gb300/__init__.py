@@ -81,6 +81,8 @@ def _load():
     L.fp8_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.fp8_set_wait_limit_ns.restype = ctypes.c_uint64
     L.fp8_quantize_tensor_noalloc.argtypes = [T, ctypes.c_int, ctypes.c_int, T, T, T, P]
+    L.fp8_scaled_mm_amax.argtypes = [T, T, T, T, T, ctypes.c_int, T, T, P, P]
+    L.fp8_quantize_from_amax.argtypes = [T, ctypes.c_int, ctypes.c_int, ctypes.c_int, T, T, T, T, P, P]
     L.fp8_set_test_stall.argtypes = [ctypes.c_int]
     L.fp8_set_test_stall.restype = ctypes.c_int
     return L
@@ -91,7 +93,8 @@ lib = _load()
 # Symbols include/fp8lin.h declares (checked by the CPU tests against the header and the .so).
 EXPORTS = ("fp8_quantize", "fp8_scaled_mm", "fp8_grouped_mm", "fp8_linear_fwd", "fp8_linear_bwd",
            "fp8_workspace_size", "fp8_jagged_padded_rows", "fp8_status_string", "fp8_set_wait_limit_ns",
-           "fp8_quantize_tensor_noalloc", "fp8_set_test_stall", "fp8_mx_scale_bytes")
+           "fp8_quantize_tensor_noalloc", "fp8_set_test_stall", "fp8_mx_scale_bytes", "fp8_scaled_mm_amax",
+           "fp8_quantize_from_amax")
 
 
 def status_string(code: int) -> str:
@@ -147,6 +150,22 @@ def fp8_scaled_mm(A, B, sA, sB, out, flags=0, status=None, stream=None):
     rc = lib.fp8_scaled_mm(_ref(desc(A)), _ref(desc(B)), _ref(desc(sA)), _ref(desc(sB)), _ref(desc(out)), flags,
                            _ptr(status), _stream(stream))
     _check(rc, "fp8_scaled_mm")
+
+
+def fp8_scaled_mm_amax(A, B, sA, sB, out, flags=0, row_amax=None, col_amax=None, status=None, stream=None):
+    """fp8_scaled_mm plus max |out| per row / per column (fp32 tensors [M] / [N]) from the epilogue."""
+    rc = lib.fp8_scaled_mm_amax(_ref(desc(A)), _ref(desc(B)), _ref(desc(sA)), _ref(desc(sB)), _ref(desc(out)), flags,
+                                _ref(desc(row_amax)), _ref(desc(col_amax)), _ptr(status), _stream(stream))
+    _check(rc, "fp8_scaled_mm_amax")
+
+
+def fp8_quantize_from_amax(x, granularity, out_dtype, layout, out=None, out_t=None, inv_scales=None, amax=None,
+                           status=None, stream=None):
+    """The scale and cast steps of fp8_quantize with the amax given (tensor [1] or column [C])."""
+    rc = lib.fp8_quantize_from_amax(_ref(desc(x)), granularity, out_dtype, layout, _ref(desc(out)),
+                                    _ref(desc(out_t)), _ref(desc(inv_scales)), _ref(desc(amax)), _ptr(status),
+                                    _stream(stream))
+    _check(rc, "fp8_quantize_from_amax")
 
 
 def fp8_grouped_mm(A, B, offsets, sA, sB, out, mode, flags=0, status=None, stream=None):

@@ -300,8 +300,12 @@ extern "C" int fp8_quantize(const fp8_tensor* x, int granularity, int out_dtype,
 
 static int dense_gemm(const void* A, int a_dt, int a_mn, const void* B, int b_dt, int b_mn, const float* sA,
                       int64_t sA_len, const float* sB, int64_t sB_len, void* out, int out_dt, int64_t M, int64_t N,
-                      int64_t K, const Ctx& c) {
+                      int64_t K, const Ctx& c, uint32_t* row_amax = nullptr, uint32_t* col_amax = nullptr,
+                      int amax_whole = 0) {
   GemmArgs g = {};
+  g.row_amax = row_amax;
+  g.col_amax = col_amax;
+  g.amax_whole = amax_whole;
   g.A = A;
   g.B = B;
   g.a_dtype = a_dt;
@@ -322,7 +326,8 @@ static int dense_gemm(const void* A, int a_dt, int a_mn, const void* B, int b_dt
 }
 
 static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA, const fp8_tensor* sB,
-                          fp8_tensor* out, int flags, const Ctx& c) {
+                          fp8_tensor* out, int flags, const Ctx& c, uint32_t* row_amax = nullptr,
+                          uint32_t* col_amax = nullptr, int amax_whole = 0) {
   FP8_CHECK(valid_desc(A) && valid_desc(B) && valid_desc(out) && A->ndim == 2 && B->ndim == 2 && out->ndim == 2,
             FP8_ERR_INVALID_ARG);
   FP8_CHECK(is_out(out->dtype), FP8_ERR_INVALID_ARG);
@@ -366,7 +371,8 @@ static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_te
     FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
     if (M == 0 || N == 0) return FP8_OK;
     return dense_gemm(A->ptr, A->dtype, 0, B->ptr, B->dtype, 0, static_cast<const float*>(sA->ptr), la,
-                      static_cast<const float*>(sB->ptr), lb, out->ptr, out->dtype, M, N, K, c);
+                      static_cast<const float*>(sB->ptr), lb, out->ptr, out->dtype, M, N, K, c, row_amax, col_amax,
+                      amax_whole);
   }
   FP8_CHECK(A->dtype == FP8_DT_BF16 && B->dtype == FP8_DT_BF16, FP8_ERR_INVALID_ARG);
   FP8_CHECK(sA == nullptr && sB == nullptr, FP8_ERR_INVALID_ARG);
@@ -377,7 +383,7 @@ static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_te
   FP8_CHECK(A->shape[1] % 8 == 0 && B->shape[1] % 8 == 0, FP8_ERR_ALIGNMENT);
   if (M == 0 || N == 0) return FP8_OK;
   return dense_gemm(A->ptr, FP8_DT_BF16, a_mn, B->ptr, FP8_DT_BF16, b_mn, nullptr, 0, nullptr, 0, out->ptr,
-                    out->dtype, M, N, K, c);
+                    out->dtype, M, N, K, c, row_amax, col_amax, amax_whole);
 }
 
 extern "C" int fp8_scaled_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA, const fp8_tensor* sB,
@@ -385,6 +391,69 @@ extern "C" int fp8_scaled_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8
   Ctx c;
   FP8_TRY(make_ctx(&c, stream, d_status));
   return scaled_mm_impl(A, B, sA, sB, out, flags, c);
+}
+
+extern "C" int fp8_scaled_mm_amax(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA,
+                                  const fp8_tensor* sB, fp8_tensor* out, int flags, fp8_tensor* row_amax,
+                                  fp8_tensor* col_amax, int32_t* d_status, void* stream) {
+  Ctx c;
+  FP8_TRY(make_ctx(&c, stream, d_status));
+  FP8_CHECK(valid_desc(out) && out->ndim == 2 && out->dtype == FP8_DT_BF16, FP8_ERR_UNSUPPORTED);
+  FP8_CHECK(!(sA && sA->dtype == FP8_DT_E8M0), FP8_ERR_UNSUPPORTED);  // MX outputs: no side outputs
+  const int64_t M = out->shape[0], N = out->shape[1];
+  uint32_t* ra = nullptr;
+  uint32_t* ca = nullptr;
+  if (row_amax) {
+    FP8_CHECK(valid_desc(row_amax) && row_amax->dtype == FP8_DT_F32 && numel(row_amax) == M, FP8_ERR_INVALID_ARG);
+    ra = static_cast<uint32_t*>(row_amax->ptr);
+  }
+  int whole = 0;
+  if (col_amax) {
+    FP8_CHECK(valid_desc(col_amax) && col_amax->dtype == FP8_DT_F32 && (numel(col_amax) == N || numel(col_amax) == 1),
+              FP8_ERR_INVALID_ARG);
+    ca = static_cast<uint32_t*>(col_amax->ptr);
+    whole = numel(col_amax) == 1 && N != 1;
+  }
+  // the maxima are folded in with atomic max from zero
+  if (ra && M > 0 && cudaMemsetAsync(ra, 0, (size_t)M * 4, c.stream) != cudaSuccess) return FP8_ERR_CUDA;
+  if (ca && cudaMemsetAsync(ca, 0, (size_t)numel(col_amax) * 4, c.stream) != cudaSuccess) return FP8_ERR_CUDA;
+  return scaled_mm_impl(A, B, sA, sB, out, flags, c, ra, ca, whole);
+}
+
+extern "C" int fp8_quantize_from_amax(const fp8_tensor* x, int granularity, int out_dtype, int layout,
+                                      fp8_tensor* out, fp8_tensor* out_t, fp8_tensor* inv_scales,
+                                      const fp8_tensor* amax, int32_t* d_status, void* stream) {
+  Ctx c;
+  FP8_TRY(make_ctx(&c, stream, d_status));
+  FP8_CHECK(valid_desc(x) && x->dtype == FP8_DT_BF16 && x->ndim == 2, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(is_fp8(out_dtype) && layout >= 1 && layout <= 3, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(valid_desc(inv_scales) && inv_scales->dtype == FP8_DT_F32, FP8_ERR_INVALID_ARG);
+  FP8_CHECK(valid_desc(amax) && amax->dtype == FP8_DT_F32, FP8_ERR_INVALID_ARG);
+  const int64_t R = x->shape[0], C = x->shape[1];
+  FP8_CHECK(C % 8 == 0 && aligned16(x->ptr), FP8_ERR_ALIGNMENT);
+  const bool want_row = layout & FP8_LAYOUT_ROW_MAJOR, want_col = layout & FP8_LAYOUT_COL_MAJOR;
+  if (want_row) {
+    FP8_CHECK(valid_desc(out) && out->dtype == out_dtype && shape_is(out, 2, R, C), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(aligned16(out->ptr), FP8_ERR_ALIGNMENT);
+  }
+  if (want_col) {
+    FP8_CHECK(valid_desc(out_t) && out_t->dtype == out_dtype && shape_is(out_t, 2, C, R), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(aligned16(out_t->ptr) && R % 16 == 0, FP8_ERR_ALIGNMENT);
+  }
+  const uint32_t* am = static_cast<const uint32_t*>(amax->ptr);
+  if (granularity == FP8_GRAN_TENSOR) {
+    FP8_CHECK(numel(amax) == 1 && numel(inv_scales) == 1, FP8_ERR_INVALID_ARG);
+    return launch_quant_tensor_cast(x->ptr, R, C, out_dtype, want_row ? out->ptr : nullptr,
+                                    want_col ? out_t->ptr : nullptr, static_cast<float*>(inv_scales->ptr), am, c, 16);
+  }
+  if (granularity == FP8_GRAN_COL) {
+    FP8_CHECK(layout == FP8_LAYOUT_COL_MAJOR, FP8_ERR_UNSUPPORTED);
+    FP8_CHECK(numel(amax) == C && numel(inv_scales) == C, FP8_ERR_INVALID_ARG);
+    FP8_CHECK(R < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
+    return launch_quant_cols(x->ptr, R, C, 1, R, nullptr, out_dtype, out_t->ptr, R,
+                             static_cast<float*>(inv_scales->ptr), nullptr, c, am);
+  }
+  return FP8_ERR_UNSUPPORTED;  // row granularity reads x once already
 }
 
 // ------------------------------------------------------------------------------------------

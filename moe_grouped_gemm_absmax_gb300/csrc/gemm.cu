@@ -94,6 +94,9 @@ struct GemmParams {
   int64_t total_rows;  // jagged M: last valid offset
   int tma_out;         // CTA pairs with 16-byte aligned output rows: TMA bulk-tensor stores
   int test_stall;      // wait first on a barrier nothing signals (failure-detection tests)
+  uint32_t* row_amax;  // side outputs (bf16 out): max |out| per row / column as fp32 words
+  uint32_t* col_amax;
+  int amax_whole;      // col_amax is a single word: the maximum over the whole output
   uint32_t idesc;
   int32_t* status;
   uint64_t wait_ns;
@@ -718,6 +721,34 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
       // keeps that set in place until then).
       uint32_t va[32], vb[32];
       uint32_t w[32];  // bf16 pairs of two consecutive 32-column chunks (one 128-byte row)
+      // Side outputs: the maxima of |out| as stored (bf16), per row over this warp's columns
+      // (one relaxed atomic max per row and tile) and per column over this warp's 32 rows (a
+      // warp max per column, one atomic per column and warp). Magnitudes of non-negative
+      // values order like their bit patterns, so the maxima are integer maxima; rows past the
+      // tile's end and columns past N count as zero. Called by the whole warp.
+      uint32_t racc = 0;
+      auto amax_chunk = [&](const uint32_t* wv, int64_t n) {
+        const int64_t left = p.N - n;
+        const int valid = left >= 32 ? 32 : (left > 0 ? (int)left : 0);
+        uint32_t mine = 0, chunk = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          uint32_t v = (wv[j >> 1] >> (16 * (j & 1))) & 0x7FFFu;
+          if (!row_ok || j >= valid) v = 0;
+          racc = v > racc ? v : racc;
+          chunk = v > chunk ? v : chunk;
+          if (p.col_amax && !p.amax_whole) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, v);
+            if (lane == j) mine = m;
+          }
+        }
+        if (p.col_amax && p.amax_whole) {  // one word for the whole output (the tensorwise amax)
+          const uint32_t m = __reduce_max_sync(0xffffffffu, chunk);
+          if (lane == 0 && m) red_max_relaxed(p.col_amax, m << 16);
+        } else if (p.col_amax && lane < valid && mine) {
+          red_max_relaxed(p.col_amax + n + lane, mine << 16);
+        }
+      };
       tmem_ld32(taddr, va);
       constexpr int NCH = C::WCOLS / 32;
 #pragma unroll
@@ -752,6 +783,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
               const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
               w[(ch & 1) * 16 + j] = *reinterpret_cast<const uint32_t*>(&h);
             }
+            if (KIND != kMX && (p.row_amax || p.col_amax)) amax_chunk(w + (ch & 1) * 16, n);
             if ((ch & 1) == 0) continue;
             if (lane == 0 && oseq >= 1) bulk_wait_read_all();  // the previous store has read the buffer
             __syncwarp();
@@ -781,6 +813,15 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
           ++oseq;
           continue;
         }
+        uint32_t wd[16];
+        if (!p.out_f32) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+            wd[j] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          if (KIND != kMX && (p.row_amax || p.col_amax)) amax_chunk(wd, n);
+        }
         if (row_ok) {
           const bool full = p.vec_ok && n + 32 <= p.N;
           if (p.out_f32) {
@@ -793,12 +834,6 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
             }
           } else {
             uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + n;
-            uint32_t wd[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
-              wd[j] = *reinterpret_cast<const uint32_t*>(&h);
-            }
             if (full) {
 #pragma unroll
               for (int j = 0; j < 16; j += 4) *reinterpret_cast<uint4*>(o + 2 * j) = make_uint4(wd[j], wd[j + 1], wd[j + 2], wd[j + 3]);
@@ -808,6 +843,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
           }
         }
       }
+      if (KIND != kMX && p.row_amax && row_ok && racc) red_max_relaxed(p.row_amax + orow, racc << 16);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {  // the issuing CTA's barrier counts the epilogue warps of both CTAs
@@ -955,6 +991,9 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   p.status = c.status;
   p.wait_ns = c.wait_ns;
   p.test_stall = c.test_stall;
+  p.row_amax = g.row_amax;
+  p.col_amax = g.col_amax;
+  p.amax_whole = g.amax_whole;
   p.ends = g.ends;
   p.E = (int)g.E;
   const bool mx = g.mx != 0;

@@ -44,9 +44,11 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 // (segments). inv [n_groups, C]. scratch: n_groups * C words of device memory.
 // Workspace words (4 bytes each) a column quantize of `groups` x C scales needs.
 int64_t col_ws_words(int64_t groups, int64_t C);
+// amax_given (optional): the column maxima as fp32 words [n_groups, C] (bf16 values); pass 1 is
+// skipped and scratch is not used.
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
                       const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, uint32_t* scratch,
-                      const Ctx& c);
+                      const Ctx& c, const uint32_t* amax_given = nullptr);
 
 // --- MX quantize (mx.cu) ---
 // Bytes of the E8M0 scales of an operand with `rows` rows and contraction length k (k % 128 == 0):
@@ -82,6 +84,10 @@ struct GemmArgs {
   const void* sfa;        // A's scales; rows: M, or the segment-padded row count (jagged M)
   const void* sfb;        // B's scales; rows: N (per expert for jagged M)
   int64_t sfa_rows;
+  // side outputs (dense, bf16 out): max |out| per row / per column as fp32 words, or null
+  uint32_t* row_amax;
+  uint32_t* col_amax;
+  int amax_whole;         // col_amax is one word: the maximum over the whole output
 };
 int launch_gemm(const GemmArgs& g, const Ctx& c);
 
@@ -90,6 +96,7 @@ int launch_gemm(const GemmArgs& g, const Ctx& c);
 namespace fp8lin {
 // Cast phase of the tensorwise quantize alone: reads the bf16 pattern of amax at `amax_word`
 // (already reduced) and writes q / qt / inv exactly as launch_quant_tensor does.
+// amax_shift: 0 when amax_word holds a bf16 pattern, 16 when it holds the fp32 value.
 int launch_quant_tensor_cast(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
-                             const uint32_t* amax_word, const Ctx& c);
+                             const uint32_t* amax_word, const Ctx& c, int amax_shift = 0);
 }  // namespace fp8lin

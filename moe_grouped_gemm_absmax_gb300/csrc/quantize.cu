@@ -233,14 +233,14 @@ constexpr int kTcRows = 128, kTcCols = 64, kTcPitch = 132;  // pitch: 33 words, 
 template <int FMT>
 __global__ void __launch_bounds__(256) quant_tensor_cast_kernel(const uint16_t* __restrict__ x, int64_t R,
                                                                 int64_t C, const uint32_t* __restrict__ amax_ws,
-                                                                uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
-                                                                float* __restrict__ inv,
+                                                                int amax_shift, uint8_t* __restrict__ q,
+                                                                uint8_t* __restrict__ qt, float* __restrict__ inv,
                                                                 const __grid_constant__ ScaleTab tab) {
   constexpr float FMAX = FmtMax<FMT>::v;
   __shared__ float s_sc;
   __shared__ __align__(16) uint8_t T[kTcCols * kTcPitch];
   if (threadIdx.x == 0) {
-    const Scale s = tab_scale(tab, *amax_ws);
+    const Scale s = tab_scale(tab, *amax_ws >> amax_shift);  // bf16 pattern, or an fp32 word holding one
     s_sc = s.s32;
     if (blockIdx.x == 0 && blockIdx.y == 0) *inv = s.inv32;
   }
@@ -291,11 +291,11 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
   if (grid.x == 0 || grid.y == 0) grid = dim3(1, 1);
   if (fmt == FP8_DT_E4M3)
     quant_tensor_cast_kernel<FP8_DT_E4M3><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_ws, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
+        static_cast<const uint16_t*>(x), R, C, amax_ws, 0, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
         scale_tab(fmt));
   else
     quant_tensor_cast_kernel<FP8_DT_E5M2><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_ws, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
+        static_cast<const uint16_t*>(x), R, C, amax_ws, 0, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
         scale_tab(fmt));
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -339,6 +339,7 @@ struct ColParams {
   int64_t group_rows;  // dense modes
   const int32_t* ends; // segment mode
   uint32_t* scratch;   // [n_groups, C]: amax bits
+  int amax_shift;      // pass 2 reads scratch >> amax_shift: 0 for bf16 patterns, 16 for fp32 words
   float* inv;
   int32_t* status;
   int64_t n_strips;
@@ -518,7 +519,7 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int64_t col = un.c0 + lane + 32 * h;
-        am[h] = col < p.C ? __ldcg(p.scratch + un.g * p.C + col) : 0u;
+        am[h] = col < p.C ? __ldcg(p.scratch + un.g * p.C + col) >> p.amax_shift : 0u;
       }
     };
     ColUnit u;
@@ -711,7 +712,7 @@ int64_t col_ws_words(int64_t groups, int64_t C) { return round_up64(groups * C, 
 
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
                       const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, uint32_t* scratch,
-                      const Ctx& c) {
+                      const Ctx& c, const uint32_t* amax_given) {
   if (n_groups == 0 || C == 0) return FP8_OK;
   if (ends && n_groups > 6000) return FP8_ERR_UNSUPPORTED;  // prefix arrays live in shared memory
   ColParams p = {};
@@ -751,7 +752,12 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
     if (rc != FP8_OK) return rc;
   }
 
-  if (cudaMemsetAsync(scratch, 0, (size_t)col_ws_words(n_groups, C) * 4, c.stream) != cudaSuccess) return FP8_ERR_CUDA;
+  if (amax_given) {
+    p.scratch = const_cast<uint32_t*>(amax_given);  // read only (pass 2)
+    p.amax_shift = 16;
+  } else if (cudaMemsetAsync(scratch, 0, (size_t)col_ws_words(n_groups, C) * 4, c.stream) != cudaSuccess) {
+    return FP8_ERR_CUDA;
+  }
   // units: exact for dense modes; for segments an upper bound (each segment adds at most one
   // partial tile) -- the kernels compute the exact count from the offsets
   const int64_t units = p.mode == 2 ? (ceil_div64(rows_total, kColTile) + n_groups) * p.n_strips
@@ -759,8 +765,8 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   const size_t pre = p.mode == 2 ? 8 * (size_t)(n_groups + 1) : 0;
   const int64_t grid = units > 0 ? (units < c.sm_count ? units : c.sm_count) : 1;
   const ScaleTab& tab = scale_tab(fmt);
-  // pass 1: column maxima
-  if (units > 0) {
+  // pass 1: column maxima (skipped when the caller supplies them)
+  if (units > 0 && !amax_given) {
     auto k1 = fmt == FP8_DT_E4M3 ? colstream_kernel<FP8_DT_E4M3, false> : colstream_kernel<FP8_DT_E5M2, false>;
     const size_t smem = ColSmem<false>::bytes + pre;
     if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -782,16 +788,18 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
 namespace fp8lin {
 
 int launch_quant_tensor_cast(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
-                             const uint32_t* amax_word, const Ctx& c) {
+                             const uint32_t* amax_word, const Ctx& c, int amax_shift) {
   dim3 grid((unsigned)ceil_div64(C, kTcCols), (unsigned)ceil_div64(R, kTcRows));
   if (grid.x == 0 || grid.y == 0) grid = dim3(1, 1);
   if (fmt == FP8_DT_E4M3)
     quant_tensor_cast_kernel<FP8_DT_E4M3><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_word, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
+        static_cast<const uint16_t*>(x), R, C, amax_word, amax_shift, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt),
+        inv,
         scale_tab(fmt));
   else
     quant_tensor_cast_kernel<FP8_DT_E5M2><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_word, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
+        static_cast<const uint16_t*>(x), R, C, amax_word, amax_shift, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt),
+        inv,
         scale_tab(fmt));
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
