@@ -661,6 +661,54 @@ class MoeFwdBwdMxStep(MoeFwdBwdStep):
                          f.GROUPED_JAGGED_K)
 
 
+class FusedAmaxStep(Step):
+    """The grad-input GEMM of the Llama3-8B MLP-up Linear, dX = dY W (rowwise FP8 operands,
+    quantized outside the timed region), with dX's column maxima as a side output of the GEMM's
+    epilogue, then dX quantized column-wise (e5m2, column-major: the previous layer's dY^T for an
+    FP8 weight gradient) from those maxima in one read. `alt_run` is the unfused chain timed in the
+    same run: the plain GEMM, then the two-pass column-wise quantize (amax pass + cast pass)."""
+    dtype = "fp8 e4m3/e5m2 (fp32 accumulate), bf16 dX"
+
+    def __init__(self, fp8, seed=0, device="cuda"):
+        self.fp8 = fp8
+        self.name = "llama3-8b-dx-colquant-fused"
+        d = W.WORKLOADS[self.name].dims
+        M, K, N = d["M"], d["K"], d["N"]
+        self.M, self.K, self.N = M, K, N
+        x, w, dy = W.linear_inputs(M, K, N, seed=seed, device=device, outliers=True)
+        self.dyq, _, self.dyi = fp8.quantize_alloc(dy, fp8.GRAN_ROW, fp8.DT_E5M2)
+        _, self.wtq, self.wti = fp8.quantize_alloc(w, fp8.GRAN_COL, fp8.DT_E4M3)
+        del x, w, dy
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+        self.amax = torch.empty(K, device=device)
+        self.dxt = torch.empty((K, M), dtype=torch.float8_e5m2, device=device)
+        self.dxti = torch.empty(K, device=device)
+        self.ws = fp8.col_workspace(1, K, device)
+        f = 2.0 * M * N * K
+        self.kernels = [("gemm_fp8 dX + column amax side output", "tensor", f, "fp8"),
+                        ("quantize_cols dX e5m2 from amax (one read)", "hbm", 3 * M * K + 4 * K, "hbm")]
+        self.alt_kernels = [("gemm_fp8 dX", "tensor", f, "fp8"),
+                            ("quantize_cols dX e5m2 (two passes)", "hbm", 3 * M * K + 4 * K, "hbm")]
+
+    def total_units(self):
+        return 2.0 * self.M * self.N * self.K
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_scaled_mm_amax(self.dyq, self.wtq, self.dyi, self.wti, self.dx, 0, col_amax=self.amax)
+        mark(1)
+        f.fp8_quantize_from_amax(self.dx, f.GRAN_COL, f.DT_E5M2, f.LAYOUT_COL_MAJOR, None, self.dxt, self.dxti,
+                                 self.amax)
+
+    def alt_run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_scaled_mm(self.dyq, self.wtq, self.dyi, self.wti, self.dx, 0)
+        mark(1)
+        f.fp8_quantize(self.dx, f.GRAN_COL, f.DT_E5M2, f.LAYOUT_COL_MAJOR, None, self.dxt, self.dxti, None, self.ws)
+
+
 def make_step(fp8, name):
     if name == "llama3-8b-mlp-up":
         return DenseLinearStep(fp8, 8192, 4096, 14336)
@@ -678,6 +726,8 @@ def make_step(fp8, name):
         return MoeFwdMxStep(fp8)
     if name == "llama4-moe-fwdbwd-mx":
         return MoeFwdBwdMxStep(fp8)
+    if name == "llama3-8b-dx-colquant-fused":
+        return FusedAmaxStep(fp8)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -903,6 +953,31 @@ def main():
                 "traffic": traffic_for(dk["kernel"]),
                 "peak_source": f"{peaks['src']} ({'2 x bf16 burst' if step.kernels[dom][3] == 'fp8' else step.kernels[dom][3]})"}
 
+    # the unfused alternative of a fused step, timed the same way (per-kernel events, flushed L2)
+    alt = None
+    if hasattr(step, "alt_run"):
+        for _ in range(args.warmup):
+            step.alt_run()
+        torch.cuda.synchronize()
+        na = len(step.alt_kernels)
+        aevs = [[torch.cuda.Event(enable_timing=True) for _ in range(na + 1)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            torch.amax(flush_rd)
+            ev = aevs[i]
+            step.alt_run(lambda k: ev[k].record(stream))
+            ev[na].record(stream)
+        torch.cuda.synchronize()
+        aper = np.zeros(na)
+        atot = 0.0
+        for ev in aevs:
+            aper += [ev[k].elapsed_time(ev[k + 1]) for k in range(na)]
+            atot += ev[0].elapsed_time(ev[na])
+        aper /= args.steps
+        alt = {"ms_per_step": round(atot / args.steps, 5),
+               "kernels": [{"kernel": lab, "ms": round(float(ms), 5)} for (lab, *_), ms in zip(step.alt_kernels, aper)],
+               "value": round(whole_job_value(units, args.steps, 1, atot, step.unit), 2)}
+
     # e2e through the public entry points with host buffers
     e2e = None
     if hasattr(step, "e2e_setup"):
@@ -940,6 +1015,7 @@ def main():
                 "dtype": getattr(step, "dtype", "fp8 e4m3/e5m2 (fp32 accumulate), bf16 wgrad"),
                 "data": "synthetic", "config": cfg, "roofline": roofline, "kernels": kernels,
                 "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
+                **({"unfused": alt} if alt else {}),
                 "wall_s": round(wall, 3), "impl": "fp8lin"}
         print(json.dumps(line))
     if ws > 1:

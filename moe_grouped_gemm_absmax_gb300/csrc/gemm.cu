@@ -46,7 +46,9 @@ constexpr int kStageOut = 4096;  // per epilogue warp: output staging for TMA st
 // under running hardware.
 constexpr uint64_t kDrainNs = 2000000000ull;
 
-enum { kDense = 0, kJagM = 1, kJagK = 2 };
+// kDenseAmax: the dense schedule whose epilogue also folds max |out| into the side outputs
+enum { kDense = 0, kJagM = 1, kJagK = 2, kDenseAmax = 3 };
+constexpr bool is_dense(int sched) { return sched == kDense || sched == kDenseAmax; }
 enum { kFP8 = 0, kBF16 = 1, kMX = 2 };
 
 // MX (block-scaled) tiles are 256 columns wide like the FP8 ones (an MMA's cost is set per
@@ -145,7 +147,7 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, co
                        const int32_t* pst) {
   Tile T;
   const uint32_t t = (uint32_t)t64, num_n = (uint32_t)p.num_n;
-  if (SCHED == kDense) {
+  if (is_dense(SCHED)) {
     const uint32_t per_group = (uint32_t)kGroupM * num_n;
     const uint32_t g = t / per_group, r = t - g * per_group;
     const uint32_t first_m = g * kGroupM;
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
 
   // ---- jagged schedules: validate offsets, per-expert tile prefix and row / K starts ----
   int64_t total;
-  if (SCHED == kDense) {
+  if (is_dense(SCHED)) {
     total = p.num_m * p.num_n;
   } else {
     int bad = 0;
@@ -609,7 +611,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
       if (KIND != kFP8) return;
       const int64_t m = Tn.m0 + row;
       const float* sbp = p.sB;
-      if (SCHED != kDense) sbp += (int64_t)Tn.e * p.N;
+      if (!is_dense(SCHED)) sbp += (int64_t)Tn.e * p.N;
       sa_nx = 1.0f;
       if (m < Tn.row_end) {
         if (SCHED == kJagK)
@@ -721,32 +723,50 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
       // keeps that set in place until then).
       uint32_t va[32], vb[32];
       uint32_t w[32];  // bf16 pairs of two consecutive 32-column chunks (one 128-byte row)
-      // Side outputs: the maxima of |out| as stored (bf16), per row over this warp's columns
-      // (one relaxed atomic max per row and tile) and per column over this warp's 32 rows (a
-      // warp max per column, one atomic per column and warp). Magnitudes of non-negative
-      // values order like their bit patterns, so the maxima are integer maxima; rows past the
-      // tile's end and columns past N count as zero. Called by the whole warp.
+      // Side outputs (dense schedule with amax): the maxima of |out| as stored (bf16), per row over
+      // this warp's columns (one relaxed atomic max per row and tile) and per column over this
+      // warp's 32 rows. Magnitudes of non-negative values order like their bit patterns, so all
+      // maxima are integer maxima on packed pairs (vmax2). The column maxima of a 32 x 32 chunk
+      // come from a butterfly across the lanes: each step keeps half of the words and folds in
+      // the partner lane's other half (16 shuffles per chunk); the lanes then hold one column
+      // pair each. Rows past the tile's end and columns past N count as zero.
       uint32_t racc = 0;
       auto amax_chunk = [&](const uint32_t* wv, int64_t n) {
         const int64_t left = p.N - n;
         const int valid = left >= 32 ? 32 : (left > 0 ? (int)left : 0);
-        uint32_t mine = 0, chunk = 0;
+        uint32_t m[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          uint32_t v = (wv[j >> 1] >> (16 * (j & 1))) & 0x7FFFu;
-          if (!row_ok || j >= valid) v = 0;
-          racc = v > racc ? v : racc;
-          chunk = v > chunk ? v : chunk;
-          if (p.col_amax && !p.amax_whole) {
-            const uint32_t m = __reduce_max_sync(0xffffffffu, v);
-            if (lane == j) mine = m;
+        for (int i = 0; i < 16; ++i) {
+          uint32_t v = wv[i] & 0x7FFF7FFFu;
+          if (!row_ok || 2 * i >= valid) v = 0;
+          else if (2 * i + 1 >= valid) v &= 0xFFFFu;
+          m[i] = v;
+          racc = __vmaxu2(racc, v);
+        }
+        if (!p.col_amax) return;
+        // step with distance d (16, 8, 4, 2): the lanes with bit d clear keep words [0, h), the
+        // others [h, 2h), each folding in the partner's copy of its kept half
+#pragma unroll
+        for (int h = 8; h >= 1; h >>= 1) {
+          const int d = 2 * h;
+          const bool upper = (lane & d) != 0;
+#pragma unroll
+          for (int i = 0; i < h; ++i) {
+            const uint32_t keep = upper ? m[i + h] : m[i];
+            const uint32_t give = upper ? m[i] : m[i + h];
+            m[i] = __vmaxu2(keep, __shfl_xor_sync(0xffffffffu, give, d));
           }
         }
-        if (p.col_amax && p.amax_whole) {  // one word for the whole output (the tensorwise amax)
-          const uint32_t m = __reduce_max_sync(0xffffffffu, chunk);
-          if (lane == 0 && m) red_max_relaxed(p.col_amax, m << 16);
-        } else if (p.col_amax && lane < valid && mine) {
-          red_max_relaxed(p.col_amax + n + lane, mine << 16);
+        m[0] = __vmaxu2(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
+        // the step of distance 2^k kept word bit (k - 1) from lane bit k, so lane l now holds the
+        // column pair of word l >> 1; the even lane reports its low column, the odd one its high
+        const int col = 2 * (lane >> 1) + (lane & 1);
+        const uint32_t mc = (lane & 1) ? (m[0] >> 16) : (m[0] & 0xFFFFu);
+        if (p.amax_whole) {
+          const uint32_t mw = __reduce_max_sync(0xffffffffu, mc);
+          if (lane == 0 && mw) red_max_relaxed(p.col_amax, mw << 16);
+        } else if (col < valid && mc) {
+          red_max_relaxed(p.col_amax + n + col, mc << 16);
         }
       };
       tmem_ld32(taddr, va);
@@ -783,7 +803,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
               const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
               w[(ch & 1) * 16 + j] = *reinterpret_cast<const uint32_t*>(&h);
             }
-            if (KIND != kMX && (p.row_amax || p.col_amax)) amax_chunk(w + (ch & 1) * 16, n);
+            if (SCHED == kDenseAmax) amax_chunk(w + (ch & 1) * 16, n);
             if ((ch & 1) == 0) continue;
             if (lane == 0 && oseq >= 1) bulk_wait_read_all();  // the previous store has read the buffer
             __syncwarp();
@@ -820,7 +840,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
             const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
             wd[j] = *reinterpret_cast<const uint32_t*>(&h);
           }
-          if (KIND != kMX && (p.row_amax || p.col_amax)) amax_chunk(wd, n);
+          if (SCHED == kDenseAmax) amax_chunk(wd, n);
         }
         if (row_ok) {
           const bool full = p.vec_ok && n + 32 <= p.N;
@@ -843,7 +863,10 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
           }
         }
       }
-      if (KIND != kMX && p.row_amax && row_ok && racc) red_max_relaxed(p.row_amax + orow, racc << 16);
+      if (SCHED == kDenseAmax && p.row_amax && row_ok) {
+        const uint32_t r = (racc & 0xFFFFu) > (racc >> 16) ? (racc & 0xFFFFu) : (racc >> 16);
+        if (r) red_max_relaxed(p.row_amax + orow, r << 16);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {  // the issuing CTA's barrier counts the epilogue warps of both CTAs
@@ -883,7 +906,7 @@ int run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const 
   auto kern = gemm_kernel<KIND, SCHED, A_MN, B_MN, CG>;
   using C = Cfg<KIND, CG>;
   constexpr int kThreads = C::THREADS;
-  const int n_arrays = SCHED == kDense ? 0 : (KIND == kMX && SCHED == kJagM) ? 3 : 2;
+  const int n_arrays = is_dense(SCHED) ? 0 : (KIND == kMX && SCHED == kJagM) ? 3 : 2;
   const size_t smem = 1024 + C::RING_BYTES + C::OUT_BYTES + kSharedBytes + (size_t)n_arrays * 4 * (p.E + 1);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FP8_ERR_CUDA;
@@ -1064,6 +1087,9 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
       if (rc) return rc;
       if (g.mode == -1) {
         const int64_t tiles = p.num_m * p.num_n;
+        if (p.row_amax || p.col_amax)
+          return pair ? run<kFP8, kDenseAmax, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c)
+                      : run<kFP8, kDenseAmax, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
         return pair ? run<kFP8, kDense, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c) : run<kFP8, kDense, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
       }
       // jagged K: A = G^T [N_out, P], B = X^T [Kd, P]; tile space M = N_out, N = Kd; the
@@ -1115,6 +1141,11 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   }
   if (rc) return rc;
   const int64_t tiles = p.num_m * p.num_n;
+  if (p.row_amax || p.col_amax) {  // side outputs: the weight-gradient layout (both MN-major) only
+    if (!(g.a_mn && g.b_mn)) return FP8_ERR_UNSUPPORTED;
+    return pair ? run<kBF16, kDenseAmax, 1, 1, 2>(ta, tb, to, none, none, p, tiles, c)
+                : run<kBF16, kDenseAmax, 1, 1, 1>(ta, tb, to, none, none, p, tiles, c);
+  }
   if (pair) {
     if (g.a_mn && g.b_mn) return run<kBF16, kDense, 1, 1, 2>(ta, tb, to, none, none, p, tiles, c);
     if (g.a_mn) return run<kBF16, kDense, 1, 0, 2>(ta, tb, to, none, none, p, tiles, c);

@@ -144,6 +144,11 @@ WORKLOADS = {
         "Llama4-shaped MoE grouped fwd+bwd: 16 experts, K=5120, N=8192, 8192 rows with "
         "Dirichlet(0.5) routing; A N(0,1), W [16,8192,5120] N(0,0.02), dY N(0,1e-3)",
         dict(E=16, M=8192, K=5120, N=8192)),
+    "llama3-8b-dx-colquant-fused": Workload(
+        "llama3-8b-dx-colquant-fused",
+        "the llama3-8b-mlp-up grad-input GEMM dX = dY W (rowwise FP8 operands) with dX's column "
+        "maxima from the GEMM epilogue, then dX quantized column-wise (e5m2, column-major) from them",
+        dict(M=8192, K=4096, N=14336)),
     # the same shapes with MXFP8 (blocks of 32, E8M0 scales) for every operand of every GEMM
     "llama3-8b-mlp-up-mx": Workload(
         "llama3-8b-mlp-up-mx",
