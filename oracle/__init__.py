@@ -59,6 +59,8 @@ def lib():
         L.orc_mx_quantize_rows.argtypes = [P, I64, I64, I, P, P]
         L.orc_gemm_mx.restype = I
         L.orc_gemm_mx.argtypes = [P, I, P, I, P, P, I64, I64, I64, P, I64, P, P]
+        L.orc_quantize_blocks.argtypes = [P, I64, I64, I64, I64, I, P, P]
+        L.orc_gemm_blockwise.argtypes = [P, I, P, I, P, P, I64, I64, I64, P, I64, P, P]
         L.orc_num_threads.restype = I
         _lib = L
     return _lib
@@ -321,4 +323,35 @@ def gemm_mx(A, fmtA, B, fmtB, sA, sB, rows=None):
     if lib().orc_gemm_mx(_p(A), fmtA, _p(B), fmtB, _p(sA), _p(sB), M, N, K, _p(r), 0 if r is None else r.size,
                          _p(out), _p(absacc)):
         raise ValueError("the contraction length must be a multiple of 32")
+    return out, absacc
+
+
+# ---- blockwise (1 x 128 activation tiles, 128 x 128 weight tiles) ----
+
+def quantize_blocks(x_bits, fmt: int, br: int, bc: int):
+    """Tiles of br x bc, each quantized by the recipe: codes [R, C], inv [ceil(R/br), ceil(C/bc)]."""
+    x = _c(x_bits, np.uint16)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    inv = np.empty((-(-R // br), -(-C // bc)), np.float32)
+    lib().orc_quantize_blocks(_p(x), R, C, br, bc, fmt, _p(q), _p(inv))
+    return q, inv
+
+
+def gemm_blockwise(A, fmtA, B, fmtB, sA, sB, rows=None):
+    """out[i, n] = sum_k sA[m, k // 128] sB[n // 128, k // 128] dec(A[m, k]) dec(B[n, k])."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sA = _c(sA, np.float32)
+    sB = _c(sB, np.float32)
+    M, K = A.shape
+    N, K2 = B.shape
+    kb = -(-K // 128)
+    assert K == K2 and sA.shape == (M, kb) and sB.shape == (-(-N // 128), kb)
+    r = None if rows is None else _c(rows, np.int64)
+    cnt = M if r is None else r.size
+    out = np.empty((cnt, N), np.float64)
+    absacc = np.empty((cnt, N), np.float64)
+    lib().orc_gemm_blockwise(_p(A), fmtA, _p(B), fmtB, _p(sA), _p(sB), M, N, K, _p(r), 0 if r is None else r.size,
+                             _p(out), _p(absacc))
     return out, absacc

@@ -367,6 +367,64 @@ int orc_grouped_gemm_k(const uint8_t* G, int fmtG, const uint8_t* X, int fmtX, c
 }
 
 /* ---------------------------------------------------------------------------------------- */
+/* Blockwise scaling. [P1] "AMD FP8 format in TorchAO" names a scale per fixed-size tile as the
+ * third granularity; the tile shapes are not given there. Reading: 1 x 128 tiles for activations
+ * and gradients (a scale per row and 128 consecutive elements of the contraction) and 128 x 128
+ * tiles for weights, each tile quantized by the recipe of [P3] section 2 (amax over the tile,
+ * fp64 scale with eps, fp32 multiply, clamp, cast, fp64 reciprocal). Edge tiles are smaller. */
+
+void orc_quantize_blocks(const uint16_t* x, int64_t R, int64_t C, int64_t br, int64_t bc, int fmt,
+                         uint8_t* q, float* inv) {
+  float fmax8 = (float)orc_fp8_max(fmt);
+  int64_t nbr = (R + br - 1) / br, nbc = (C + bc - 1) / bc;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t b = 0; b < nbr * nbc; ++b) {
+    int64_t r0 = (b / nbc) * br, c0 = (b % nbc) * bc;
+    int64_t r1 = r0 + br < R ? r0 + br : R, c1 = c0 + bc < C ? c0 + bc : C;
+    float amax = 0.0f;
+    for (int64_t r = r0; r < r1; ++r)
+      for (int64_t c = c0; c < c1; ++c) {
+        float a = fabsf(bf16_to_float(x[r * C + c]));
+        if (a > amax) amax = a;
+      }
+    float scale32, inv32;
+    orc_scale(amax, fmt, NULL, &scale32, &inv32);
+    for (int64_t r = r0; r < r1; ++r)
+      for (int64_t c = c0; c < c1; ++c) q[r * C + c] = scale_clamp_cast(bf16_to_float(x[r * C + c]), scale32, fmax8, fmt);
+    inv[b] = inv32;
+  }
+}
+
+/* Blockwise GEMM: out[i, n] = sum_k sA[m, k / 128] * sB[n / 128, k / 128] * dec(A[m, k]) * dec(B[n, k]),
+ * m = rows[i] (or i); A [M, K] and B [N, K] row-major codes; sA [M, ceil(K / 128)] (1 x 128
+ * tiles of A), sB [ceil(N / 128), ceil(K / 128)] (128 x 128 tiles of B). Each term is the fp64
+ * product of the two inverse scales and the two decoded values; the sum runs in k order. */
+void orc_gemm_blockwise(const uint8_t* A, int fmtA, const uint8_t* B, int fmtB, const float* sA,
+                        const float* sB, int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                        int64_t n_rows, double* out, double* absacc) {
+  double ta[256], tb[256];
+  decode_table(fmtA, ta);
+  decode_table(fmtB, tb);
+  int64_t kb = (K + 127) / 128;
+  int64_t cnt = rows ? n_rows : M;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < cnt; ++i) {
+    int64_t m = rows ? rows[i] : i;
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0, aacc = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        double s = (double)sA[m * kb + k / 128] * (double)sB[(n / 128) * kb + k / 128];
+        double p = s * (ta[A[m * K + k]] * tb[B[n * K + k]]);
+        acc += p;
+        aacc += fabs(p);
+      }
+      out[i * N + n] = acc;
+      if (absacc) absacc[i * N + n] = aacc;
+    }
+  }
+}
+
+/* ---------------------------------------------------------------------------------------- */
 /* MXFP8. The pages name it as the fourth scaling granularity, a scale per group stored with the
  * data ([P1] section "AMD FP8 format in TorchAO"), and as the next step for quantization and the
  * grouped GEMM ([P1] "Summary and Next Steps"); they fix nothing more. The block, the shared

@@ -98,6 +98,18 @@ int orc_grouped_gemm_k(const uint8_t* G, int fmtG, const uint8_t* X, int fmtX, c
                        int64_t K, const int64_t* nsel, int64_t n_sel, double* out,
                        double* absacc);
 
+/* Blockwise scaling (tiles of br x bc; the reading takes 1 x 128 for activations and gradients,
+ * 128 x 128 for weights): each tile quantized by the recipe. q [R, C] codes, inv
+ * [ceil(R/br), ceil(C/bc)] inverse scales. */
+void orc_quantize_blocks(const uint16_t* x, int64_t R, int64_t C, int64_t br, int64_t bc, int fmt,
+                         uint8_t* q, float* inv);
+/* Blockwise GEMM: out[i, n] = sum_k sA[m, k/128] sB[n/128, k/128] dec(A[m, k]) dec(B[n, k]),
+ * m = rows[i] (or i). A [M, K], B [N, K] row-major; sA [M, ceil(K/128)], sB [ceil(N/128),
+ * ceil(K/128)]. absacc gets the sum of the terms' magnitudes. */
+void orc_gemm_blockwise(const uint8_t* A, int fmtA, const uint8_t* B, int fmtB, const float* sA,
+                        const float* sB, int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                        int64_t n_rows, double* out, double* absacc);
+
 /* MXFP8 (OCP Microscaling Formats v1.0; the pages name the format only): the E8M0 scale code
  * of a 32-element block with this amax, 2^(floor(log2 amax) - emax_elem) clamped below at
  * 2^-127 (255 = NaN for a NaN or infinite amax); the value of an E8M0 code. */

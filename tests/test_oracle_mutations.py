@@ -1,11 +1,11 @@
 """The pins have teeth: each plausible mistake below is planted in a copy of the oracle (the C
-source, on the CPU), the copy is compiled, and the oracle's pin tests (tests/test_oracle.py and
-tests/test_oracle_mx.py) are run against it in a subprocess; every mutant must make at least
-one pin fail. The mistakes cover
-each step of the recipe and of the GEMMs: rounding ties, the subnormal binade, the eps clamp,
+source, on the CPU), the copy is compiled, and the oracle's pin tests (tests/test_oracle.py,
+tests/test_oracle_mx.py and tests/test_oracle_blocks.py) are run against it in a subprocess;
+every mutant must make at least one pin fail. The mistakes cover each step of the recipe and of the GEMMs: rounding ties, the subnormal binade, the eps clamp,
 the direction of the scale, the inverse scale's rounding, a dropped product in the contraction,
 a segment boundary, the column of a transposed operand; for MXFP8 the scale rule's exponent,
-floor and clamp, the block amax, and the block index of a scale in the GEMM."""
+floor and clamp, the block amax, and the block index of a scale in the GEMM; for blockwise
+scaling a tile's edge and the K block of each operand's scale."""
 import os
 import re
 import subprocess
@@ -45,6 +45,12 @@ MUTANTS = {
     "mx_signed_amax": ("float a = fabsf(bf16_to_float(xb[i]));", "float a = bf16_to_float(xb[i]);"),
     # MX GEMM: B's first block scale used for every block
     "mx_block_index": ("ts[sB[n * nb + k / 32]]", "ts[sB[n * nb]]"),
+    # blockwise: a tile's last row left out
+    "blk_tile_edge": ("int64_t r1 = r0 + br < R ? r0 + br : R, c1", "int64_t r1 = r0 + br - 1 < R ? r0 + br - 1 : R, c1"),
+    # blockwise GEMM: the weight tile's scale taken from the first K block only
+    "blk_weight_kblock": ("(double)sB[(n / 128) * kb + k / 128]", "(double)sB[(n / 128) * kb]"),
+    # blockwise GEMM: the activation's scale from 256-wide K blocks
+    "blk_act_kblock": ("(double)sA[m * kb + k / 128]", "(double)sA[m * kb + k / 256]"),
 }
 
 
@@ -65,7 +71,8 @@ def _build_mutant(name, tmp_path):
 def _run_pins(so):
     env = dict(os.environ, FP8LIN_ORACLE_LIB=str(so))
     return subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle.py"),
-                           os.path.join(ROOT, "tests", "test_oracle_mx.py"), "-x", "-q", "-p", "no:cacheprovider"],
+                           os.path.join(ROOT, "tests", "test_oracle_mx.py"), os.path.join(ROOT, "tests", "test_oracle_blocks.py"),
+                           "-x", "-q", "-p", "no:cacheprovider"],
                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
 
 
