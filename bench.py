@@ -709,6 +709,74 @@ class FusedAmaxStep(Step):
         f.fp8_quantize(self.dx, f.GRAN_COL, f.DT_E5M2, f.LAYOUT_COL_MAJOR, None, self.dxt, self.dxti, None, self.ws)
 
 
+class DenseBlockwiseLinearStep(DenseLinearStep):
+    """Linear fwd+bwd with blockwise scaling: x and dY in 1 x 128 tiles, W in 128 x 128 tiles
+    (both layouts from one read); fwd and dX blockwise FP8 GEMMs, dW in bf16."""
+    dtype = "fp8 e4m3/e5m2 blockwise (fp32 tile scales, fp32 accumulate), bf16 wgrad"
+
+    def __init__(self, fp8, M, K, N, seed=0, device="cuda"):
+        self.fp8, self.M, self.K, self.N = fp8, M, K, N
+        self.name = "llama3-8b-mlp-up-blockwise"
+        self.x, self.w, self.dy = W.linear_inputs(M, K, N, seed=seed, device=device, outliers=True)
+        d = device
+        e4, e5 = torch.float8_e4m3fn, torch.float8_e5m2
+        self.saved, self.bufs = fp8.linear_saved_alloc(M, K, N, fp8.GRAN_BLOCK_1x128, keep_xt=False, device=d)
+        (self.xq, self.xi, self.wq, self.wi, _, self.wtq, _, self.wti) = self.bufs
+        self.wboth = torch.empty(2 * (N // 128) * (K // 128), device=d)
+        self.dyq = torch.empty((M, N), dtype=e5, device=d)
+        self.dyi = torch.empty((M, N // 128), device=d)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=d)
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=d)
+        self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=d)
+        f = 2.0 * M * N * K
+        self.kernels = [
+            ("blk_quantize x e4m3 1x128", "hbm", 3 * M * K + 4 * M * K // 128, "hbm"),
+            ("blk_quantize W e4m3 128x128 rows+cols", "hbm", 4 * N * K, "hbm"),
+            ("gemm_blockwise fwd", "tensor", f, "fp8"),
+            ("blk_quantize dY e5m2 1x128", "hbm", 3 * M * N + 4 * M * N // 128, "hbm"),
+            ("gemm_blockwise dX", "tensor", f, "fp8"),
+            ("gemm_bf16 dW", "tensor", f, "bf16"),
+        ]
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        nw = (self.N // 128) * (self.K // 128)
+        mark(0)
+        f.fp8_quantize(self.x, f.GRAN_BLOCK_1x128, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.xq, None, self.xi)
+        mark(1)
+        f.fp8_quantize(self.w, f.GRAN_BLOCK_128x128, f.DT_E4M3, f.LAYOUT_BOTH, self.wq, self.wtq, self.wboth)
+        mark(2)
+        f.fp8_scaled_mm(self.xq, self.wq, self.xi, self.wboth[:nw], self.y, f.MM_FAST_ACCUM | f.MM_BLOCKWISE)
+        mark(3)
+        f.fp8_quantize(self.dy, f.GRAN_BLOCK_1x128, f.DT_E5M2, f.LAYOUT_ROW_MAJOR, self.dyq, None, self.dyi)
+        mark(4)
+        f.fp8_scaled_mm(self.dyq, self.wtq, self.dyi, self.wboth[nw:], self.dx, f.MM_BLOCKWISE)
+        mark(5)
+        f.fp8_scaled_mm(self.dy, self.x, None, None, self.dw, f.MM_A_MN_MAJOR | f.MM_B_MN_MAJOR)
+
+    def e2e_buffers(self, dev):
+        f = self.fp8
+        self.e2e_gran, self.e2e_wgrad = f.GRAN_BLOCK_1x128, f.WGRAD_BF16
+        self.saved, self.saved_bufs = f.linear_saved_alloc(self.M, self.K, self.N, f.GRAN_BLOCK_1x128, keep_xt=False,
+                                                           device=dev)
+        self.ws = torch.empty(max(f.fp8_workspace_size(f.OP_LINEAR_BWD, self.M, self.K, self.N, f.GRAN_BLOCK_1x128,
+                                                       f.WGRAD_BF16), 256), dtype=torch.uint8, device=dev)
+
+    def cpu_sample(self, rows):
+        import oracle
+        x, w, dy = self.x[:rows].cpu(), self.w.cpu(), self.dy[:rows].cpu()
+        xb, wb, db = W.bf16_bits(x), W.bf16_bits(w), W.bf16_bits(dy)
+
+        def run():
+            xq, xi = oracle.quantize_blocks(xb, oracle.E4M3, 1, 128)
+            wq, wi = oracle.quantize_blocks(wb, oracle.E4M3, 128, 128)
+            oracle.gemm_blockwise(xq, oracle.E4M3, wq, oracle.E4M3, xi, wi)
+            dq, di = oracle.quantize_blocks(db, oracle.E5M2, 1, 128)
+            oracle.gemm_blockwise(dq, oracle.E5M2, np.ascontiguousarray(wq.T), oracle.E4M3, di, np.ascontiguousarray(wi.T))
+            oracle.gemm_bf16(db, xb, a_trans=True, b_trans=True)
+        return run, 3 * 2.0 * rows * self.N * self.K, f"llama3-8b-mlp-up-blockwise step on the first {rows} of {self.M} tokens"
+
+
 def make_step(fp8, name):
     if name == "llama3-8b-mlp-up":
         return DenseLinearStep(fp8, 8192, 4096, 14336)
@@ -728,6 +796,8 @@ def make_step(fp8, name):
         return MoeFwdBwdMxStep(fp8)
     if name == "llama3-8b-dx-colquant-fused":
         return FusedAmaxStep(fp8)
+    if name == "llama3-8b-mlp-up-blockwise":
+        return DenseBlockwiseLinearStep(fp8, 8192, 4096, 14336)
     raise SystemExit(f"unknown workload {name}")
 
 

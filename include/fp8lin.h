@@ -21,6 +21,13 @@
  *       quantization (no intermediate tensors in HBM), the column-wise variant that writes a
  *       column-major output through on-chip staging (no separate transpose copy), and the
  *       dual output (row- and column-major from one read).
+ *  [B]  same page, section "AMD FP8 format in TorchAO": blockwise scaling, one scale per
+ *       fixed-size tile. The tile shapes are not given; this library takes 1 x 128 tiles for
+ *       activations and gradients (a scale per row and 128 consecutive contraction elements) and
+ *       128 x 128 tiles for weights, each tile quantized by the recipe [Q]. The GEMM computes
+ *       sum_k sA[m, k/128] sB[n/128, k/128] A[m, k] B[n, k]: the tensor cores accumulate each
+ *       128-deep K block separately in fp32 and the epilogue warps add the block products scaled
+ *       by sA * sB into fp32 registers.
  *  [MX] same page, section "AMD FP8 format in TorchAO" (MXFP8: a scale per group stored with the
  *       data) and "Summary and Next Steps" (MXFP8 quantization and grouped GEMM next). The pages
  *       give no more; block, scale and rule are those of the OCP Microscaling Formats (MX)
@@ -68,7 +75,14 @@ enum {
 };
 
 /* scale granularity */
-enum { FP8_GRAN_TENSOR = 0, FP8_GRAN_ROW = 1, FP8_GRAN_COL = 2, FP8_GRAN_MX = 3 };
+enum {
+  FP8_GRAN_TENSOR = 0,
+  FP8_GRAN_ROW = 1,
+  FP8_GRAN_COL = 2,
+  FP8_GRAN_MX = 3,
+  FP8_GRAN_BLOCK_1x128 = 4,   /* blockwise [B]: one scale per row and 128 consecutive columns */
+  FP8_GRAN_BLOCK_128x128 = 5  /* blockwise [B]: one scale per 128 x 128 tile */
+};
 
 /*
  * MX scale layout (FP8_GRAN_MX; [MX]). An MX operand with R rows (its non-contraction index) and
@@ -90,7 +104,9 @@ enum {
   FP8_MM_FAST_ACCUM = 1, /* accepted for parity with the pages' forward GEMM; the tcgen05
                             accumulator is fp32 in tensor memory either way */
   FP8_MM_A_MN_MAJOR = 2, /* BF16 only: A is given as [K, M] (M contiguous) */
-  FP8_MM_B_MN_MAJOR = 4  /* BF16 only: B is given as [K, N] (N contiguous) */
+  FP8_MM_B_MN_MAJOR = 4, /* BF16 only: B is given as [K, N] (N contiguous) */
+  FP8_MM_BLOCKWISE = 8   /* FP8 only: sA [M, K/128] (1 x 128 tiles of A) and sB [ceil(N/128), K/128]
+                            (128 x 128 tiles of B) inverse scales, K % 128 == 0 ([B]) */
 };
 
 /* grouped GEMM modes */
@@ -134,6 +150,12 @@ typedef struct fp8_tensor {
  *  x           bf16 [R, C], or [B, R, C] for a batch of matrices (e.g. MoE expert weights).
  *              C % 8 == 0 (16-byte rows).
  *  granularity FP8_GRAN_TENSOR: one scale for all of x.
+ *              FP8_GRAN_BLOCK_1x128 ([B]): one scale per row and 128 columns; ROW_MAJOR only;
+ *                               2-D x, C % 128 == 0; inv_scales fp32 [R, C / 128].
+ *              FP8_GRAN_BLOCK_128x128 ([B]): one scale per 128 x 128 tile; 2-D x, C % 128 == 0
+ *                               (and R % 128 == 0 for COL_MAJOR); inv_scales fp32: ROW_MAJOR
+ *                               [ceil(R/128), C/128]; COL_MAJOR [C/128, R/128] (the scales of the
+ *                               transposed operand); BOTH the first followed by the second.
  *              FP8_GRAN_MX:     MXFP8 ([MX]): one E8M0 scale per 32 elements; C % 128 == 0.
  *                               ROW_MAJOR: blocks along rows, `out` in x's shape, scales over
  *                               (rows R, contraction C). COL_MAJOR: blocks down columns (R % 128
@@ -267,8 +289,10 @@ typedef struct fp8_linear_saved {
 } fp8_linear_saved;
 
 /*
- * fp8_linear_fwd — y = x W^T through FP8 ([Q], [L]): quantize x and W (e4m3; tensor, row or MX
- * granularity), then one scaled GEMM. x bf16 [M, K], w bf16 [N, K], y bf16/fp32 [M, N].
+ * fp8_linear_fwd — y = x W^T through FP8 ([Q], [L]): quantize x and W (e4m3; tensor, row, MX or
+ * blockwise granularity), then one scaled GEMM. Blockwise (FP8_GRAN_BLOCK_1x128, [B]): x in 1 x 128
+ * tiles (x_inv [M, K/128]), W in 128 x 128 tiles in both layouts (w_inv [N/128, K/128], wt_inv
+ * [K/128, N/128]); K and N multiples of 128; the backward pass supports FP8_WGRAD_BF16 only. x bf16 [M, K], w bf16 [N, K], y bf16/fp32 [M, N].
  * Tensor and MX granularity write x and W in both layouts (dual output) so that the backward
  * pass needs no transpose copy. MX ([MX]) needs M, K and N multiples of 128.
  */

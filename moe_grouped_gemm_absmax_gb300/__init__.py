@@ -20,9 +20,9 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libfp8lin.so")
 
 # enums of include/fp8lin.h
 DT_BF16, DT_F32, DT_E4M3, DT_E5M2, DT_I32, DT_E8M0 = 1, 2, 3, 4, 5, 6
-GRAN_TENSOR, GRAN_ROW, GRAN_COL, GRAN_MX = 0, 1, 2, 3
+GRAN_TENSOR, GRAN_ROW, GRAN_COL, GRAN_MX, GRAN_BLOCK_1x128, GRAN_BLOCK_128x128 = 0, 1, 2, 3, 4, 5
 LAYOUT_ROW_MAJOR, LAYOUT_COL_MAJOR, LAYOUT_BOTH = 1, 2, 3
-MM_FAST_ACCUM, MM_A_MN_MAJOR, MM_B_MN_MAJOR = 1, 2, 4
+MM_FAST_ACCUM, MM_A_MN_MAJOR, MM_B_MN_MAJOR, MM_BLOCKWISE = 1, 2, 4, 8
 GROUPED_JAGGED_M, GROUPED_JAGGED_K = 0, 1
 WGRAD_FP8, WGRAD_BF16 = 0, 1
 OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD = 0, 1, 2
@@ -190,7 +190,13 @@ def linear_saved_alloc(M: int, K: int, N: int, granularity: int, keep_xt: bool =
     x_q = torch.empty((M, K), dtype=e4, device=device)
     w_q = torch.empty((N, K), dtype=e4, device=device)
     xt_q = wt_q = xt_inv = wt_inv = None
-    if granularity == GRAN_MX:
+    if granularity == GRAN_BLOCK_1x128:  # 1 x 128 tiles of x, 128 x 128 tiles of W (both layouts)
+        f32 = torch.float32
+        x_inv = torch.empty((M, K // 128), dtype=f32, device=device)
+        w_inv = torch.empty((N // 128, K // 128), dtype=f32, device=device)
+        wt_q = torch.empty((K, N), dtype=e4, device=device)
+        wt_inv = torch.empty((K // 128, N // 128), dtype=f32, device=device)
+    elif granularity == GRAN_MX:
         u8 = torch.uint8
         x_inv = torch.empty(fp8_mx_scale_bytes(M, K), dtype=u8, device=device)
         w_inv = torch.empty(fp8_mx_scale_bytes(N, K), dtype=u8, device=device)
@@ -328,3 +334,24 @@ def mx_quantize_alloc(x, out_dtype, layout=LAYOUT_ROW_MAJOR, offsets=None, padde
     sf = torch.empty(row_bytes + col_bytes, dtype=torch.uint8, device=dev)
     fp8_quantize(x, GRAN_MX, out_dtype, layout, out, out_t, sf, offsets, ws, status=status, stream=stream)
     return out, out_t, (sf[:row_bytes] if row_bytes else None), (sf[row_bytes:] if col_bytes else None)
+
+
+def blk_quantize_alloc(x, out_dtype, tile128=False, layout=LAYOUT_ROW_MAJOR, status=None, stream=None):
+    """Blockwise quantize: 1 x 128 tiles (row-major) or 128 x 128 tiles (row- and/or column-major).
+    Returns (out or None, out_t or None, inverse scales of out or None, of out_t or None)."""
+    dev = x.device
+    fdt = FP8_TORCH[out_dtype]
+    R, C = x.shape
+    out = torch.empty((R, C), dtype=fdt, device=dev) if layout & LAYOUT_ROW_MAJOR else None
+    out_t = torch.empty((C, R), dtype=fdt, device=dev) if layout & LAYOUT_COL_MAJOR else None
+    if not tile128:
+        inv = torch.empty((R, max(C // 128, 1)), dtype=torch.float32, device=dev)
+        fp8_quantize(x, GRAN_BLOCK_1x128, out_dtype, layout, out, out_t, inv, status=status, stream=stream)
+        return out, out_t, inv, None
+    nr = -(-R // 128) * (C // 128) if out is not None else 0
+    nc = (C // 128) * (R // 128) if out_t is not None else 0
+    inv = torch.empty(max(nr + nc, 1), dtype=torch.float32, device=dev)
+    fp8_quantize(x, GRAN_BLOCK_128x128, out_dtype, layout, out, out_t, inv[:nr + nc] if nr + nc else inv,
+                 status=status, stream=stream)
+    return (out, out_t, inv[:nr].view(-1, C // 128) if nr else None,
+            inv[nr:nr + nc].view(C // 128, R // 128) if nc else None)

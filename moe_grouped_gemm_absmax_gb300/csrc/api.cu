@@ -281,6 +281,24 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
       return launch_mx_quant(x->ptr, B, R, C, out_dtype, want_row ? out->ptr : nullptr, sf,
                              want_col ? out_t->ptr : nullptr, R, sf + row_bytes, nullptr, 0, nullptr, c);
     }
+    case FP8_GRAN_BLOCK_1x128: {
+      FP8_CHECK(offsets == nullptr && nd == 2 && layout == FP8_LAYOUT_ROW_MAJOR, FP8_ERR_UNSUPPORTED);
+      FP8_CHECK(C % 128 == 0, FP8_ERR_UNSUPPORTED);
+      FP8_CHECK(numel(inv) == R * (C / 128), FP8_ERR_INVALID_ARG);
+      return launch_blk_quant(x->ptr, R, C, out_dtype, false, out->ptr, nullptr, static_cast<float*>(inv->ptr),
+                              nullptr, c);
+    }
+    case FP8_GRAN_BLOCK_128x128: {
+      FP8_CHECK(offsets == nullptr && nd == 2, FP8_ERR_UNSUPPORTED);
+      FP8_CHECK(C % 128 == 0 && (!want_col || R % 128 == 0), FP8_ERR_UNSUPPORTED);
+      if (want_col) FP8_CHECK(shape_is(out_t, 2, C, R), FP8_ERR_INVALID_ARG);
+      const int64_t nrow = want_row ? ((R + 127) / 128) * (C / 128) : 0, ncol = want_col ? (C / 128) * (R / 128) : 0;
+      FP8_CHECK(numel(inv) == nrow + ncol, FP8_ERR_INVALID_ARG);
+      float* iv = static_cast<float*>(inv->ptr);
+      return launch_blk_quant(x->ptr, R, C, out_dtype, true, want_row ? out->ptr : nullptr,
+                              want_col ? out_t->ptr : nullptr, want_row ? iv : nullptr, want_col ? iv + nrow : nullptr,
+                              c);
+    }
     default:
       return FP8_ERR_INVALID_ARG;
   }
@@ -366,6 +384,27 @@ static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_te
       return launch_gemm(g, c);
     }
     FP8_CHECK(sA->dtype == FP8_DT_F32 && sB->dtype == FP8_DT_F32, FP8_ERR_INVALID_ARG);
+    if (flags & FP8_MM_BLOCKWISE) {  // [B]: sA [M, K/128], sB [ceil(N/128), K/128]
+      FP8_CHECK(K % 128 == 0 && !row_amax && !col_amax, FP8_ERR_UNSUPPORTED);
+      FP8_CHECK(numel(sA) == M * (K / 128) && numel(sB) == ((N + 127) / 128) * (K / 128), FP8_ERR_INVALID_ARG);
+      FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
+      if (M == 0 || N == 0) return FP8_OK;
+      GemmArgs g = {};
+      g.A = A->ptr;
+      g.B = B->ptr;
+      g.a_dtype = A->dtype;
+      g.b_dtype = B->dtype;
+      g.sA = static_cast<const float*>(sA->ptr);
+      g.sB = static_cast<const float*>(sB->ptr);
+      g.out = out->ptr;
+      g.out_dtype = out->dtype;
+      g.M = M;
+      g.N = N;
+      g.K = K;
+      g.mode = -1;
+      g.blockwise = 1;
+      return launch_gemm(g, c);
+    }
     const int64_t la = numel(sA), lb = numel(sB);
     FP8_CHECK((la == 1 || la == M) && (lb == 1 || lb == N), FP8_ERR_INVALID_ARG);
     FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
@@ -586,6 +625,12 @@ static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad
     return o;
   };
   const bool rows = gran == FP8_GRAN_ROW, fp8w = wgrad == FP8_WGRAD_FP8;
+  if (gran == FP8_GRAN_BLOCK_1x128) {  // dY in 1 x 128 tiles
+    L.dy_q = take((size_t)(M * N));
+    L.dy_inv = take((size_t)(M * ((N + 127) / 128)) * 4);
+    L.total = off;
+    return L;
+  }
   if (gran == FP8_GRAN_MX) {  // dY in both layouts; its row-major then column-major MX scales
     L.dy_q = take((size_t)(M * N));
     L.dyt_q = fp8w ? take((size_t)(N * M)) : 0;
@@ -668,6 +713,24 @@ extern "C" int fp8_linear_fwd(const fp8_tensor* x, const fp8_tensor* w, int gran
     FP8_TRY(mx_both(x, FP8_DT_E4M3, &saved->x_q, &saved->x_inv, saved->xt_q.ptr ? &saved->xt_q : nullptr,
                     &saved->xt_inv, c));
     FP8_TRY(mx_both(w, FP8_DT_E4M3, &saved->w_q, &saved->w_inv, &saved->wt_q, &saved->wt_inv, c));
+  } else if (granularity == FP8_GRAN_BLOCK_1x128) {
+    // [B]: x in 1 x 128 tiles; W in 128 x 128 tiles, both layouts from one read (the scales of
+    // the transposed copy are the same tiles, transposed)
+    FP8_CHECK(K % 128 == 0 && N % 128 == 0, FP8_ERR_UNSUPPORTED);
+    FP8_CHECK(valid_desc(&saved->x_inv) && saved->x_inv.dtype == FP8_DT_F32 && numel(&saved->x_inv) == M * (K / 128),
+              FP8_ERR_INVALID_ARG);
+    FP8_CHECK(valid_desc(&saved->w_inv) && valid_desc(&saved->wt_inv) && numel(&saved->w_inv) == (N / 128) * (K / 128) &&
+                  numel(&saved->wt_inv) == (N / 128) * (K / 128) && saved->w_inv.dtype == FP8_DT_F32 &&
+                  saved->wt_inv.dtype == FP8_DT_F32,
+              FP8_ERR_INVALID_ARG);
+    FP8_CHECK(shape_is(&saved->x_q, 2, M, K) && shape_is(&saved->w_q, 2, N, K) && shape_is(&saved->wt_q, 2, K, N),
+              FP8_ERR_INVALID_ARG);
+    FP8_TRY(quantize_impl(x, FP8_GRAN_BLOCK_1x128, FP8_DT_E4M3, FP8_LAYOUT_ROW_MAJOR, &saved->x_q, nullptr,
+                          &saved->x_inv, nullptr, nullptr, 0, c));
+    FP8_TRY(launch_blk_quant(w->ptr, N, K, FP8_DT_E4M3, true, saved->w_q.ptr, saved->wt_q.ptr,
+                             static_cast<float*>(saved->w_inv.ptr), static_cast<float*>(saved->wt_inv.ptr), c));
+    return scaled_mm_impl(&saved->x_q, &saved->w_q, &saved->x_inv, &saved->w_inv, y,
+                          (flags & FP8_MM_FAST_ACCUM) | FP8_MM_BLOCKWISE, c);
   } else if (granularity == FP8_GRAN_ROW) {
     FP8_TRY(quantize_impl(x, FP8_GRAN_ROW, FP8_DT_E4M3, FP8_LAYOUT_ROW_MAJOR, &saved->x_q, nullptr, &saved->x_inv,
                           nullptr, nullptr, 0, c));
@@ -687,7 +750,8 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
   Ctx c;
   FP8_TRY(make_ctx(&c, stream, d_status));
   FP8_CHECK(valid_desc(dy) && saved && dy->ndim == 2 && dy->dtype == FP8_DT_BF16, FP8_ERR_INVALID_ARG);
-  FP8_CHECK(granularity == FP8_GRAN_TENSOR || granularity == FP8_GRAN_ROW || granularity == FP8_GRAN_MX,
+  FP8_CHECK(granularity == FP8_GRAN_TENSOR || granularity == FP8_GRAN_ROW || granularity == FP8_GRAN_MX ||
+                granularity == FP8_GRAN_BLOCK_1x128,
             FP8_ERR_INVALID_ARG);
   FP8_CHECK(wgrad_mode == FP8_WGRAD_FP8 || wgrad_mode == FP8_WGRAD_BF16, FP8_ERR_INVALID_ARG);
   const int64_t M = dy->shape[0], N = dy->shape[1];
@@ -700,6 +764,23 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
   FP8_CHECK(aligned16(workspace), FP8_ERR_ALIGNMENT);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   fp8_tensor dy_q = T2(ws + L.dy_q, FP8_DT_E5M2, M, N);
+  if (granularity == FP8_GRAN_BLOCK_1x128) {
+    // [B]: dY in 1 x 128 tiles (along N) for dX = dY W with W's 128 x 128 tiles transposed;
+    // the weight gradient in bf16
+    FP8_CHECK(!(fp8w && need_dw), FP8_ERR_UNSUPPORTED);
+    FP8_CHECK(N % 128 == 0 && K % 128 == 0, FP8_ERR_UNSUPPORTED);
+    fp8_tensor dy_inv = T1(ws + L.dy_inv, FP8_DT_F32, M * (N / 128));
+    if (dx && dx->ptr) {
+      FP8_TRY(quantize_impl(dy, FP8_GRAN_BLOCK_1x128, FP8_DT_E5M2, FP8_LAYOUT_ROW_MAJOR, &dy_q, nullptr, &dy_inv,
+                            nullptr, nullptr, 0, c));
+      FP8_TRY(scaled_mm_impl(&dy_q, &saved->wt_q, &dy_inv, &saved->wt_inv, dx, FP8_MM_BLOCKWISE, c));
+    }
+    if (need_dw) {
+      FP8_CHECK(valid_desc(x) && x->dtype == FP8_DT_BF16 && shape_is(x, 2, M, K), FP8_ERR_INVALID_ARG);
+      FP8_TRY(scaled_mm_impl(dy, x, nullptr, nullptr, dw, FP8_MM_A_MN_MAJOR | FP8_MM_B_MN_MAJOR, c));
+    }
+    return FP8_OK;
+  }
   if (granularity == FP8_GRAN_MX) {
     // dY in both layouts from one read: rows (blocks along N) for dX = dY W, columns (blocks
     // along M) for dW = dY^T x

@@ -49,7 +49,10 @@ constexpr uint64_t kDrainNs = 2000000000ull;
 // kDenseAmax: the dense schedule whose epilogue also folds max |out| into the side outputs
 enum { kDense = 0, kJagM = 1, kJagK = 2, kDenseAmax = 3 };
 constexpr bool is_dense(int sched) { return sched == kDense || sched == kDenseAmax; }
-enum { kFP8 = 0, kBF16 = 1, kMX = 2 };
+// kBLK: FP8 operands with blockwise scales (A: 1 x 128 tiles, B: 128 x 128 tiles); the MMAs of
+// each 128-deep K block go to a fresh tensor-memory partial, which the epilogue warps scale by
+// sA[m, kb] * sB[n / 128, kb] and add into register accumulators ("promotion")
+enum { kFP8 = 0, kBF16 = 1, kMX = 2, kBLK = 3 };
 
 // MX (block-scaled) tiles are 256 columns wide like the FP8 ones (an MMA's cost is set per
 // instruction, so narrower tiles run the tensor cores below their rate), but they keep ONE
@@ -59,9 +62,12 @@ enum { kFP8 = 0, kBF16 = 1, kMX = 2 };
 // release it at once, so the next tile's MMAs wait only for those loads, not for the stores.
 template <int KIND, int CG>
 struct Cfg {
+  // kBLK: 256-column tiles and two K-block partials (the MMAs run one K block ahead of the
+  // promotion). 128-column tiles with four partials were slower: the MMA's cost is per
+  // instruction, so halving N halves the tensor-core rate.
   static constexpr int TBN = BN;                          // tile columns
-  static constexpr int NBUF = KIND == kMX ? 1 : 2;        // accumulators in tensor memory
-  static constexpr int EPI_WARPS = KIND == kMX ? 16 : 8;
+  static constexpr int NBUF = KIND == kMX ? 1 : 2;        // accumulators / K-block partials
+  static constexpr int EPI_WARPS = (KIND == kMX || KIND == kBLK) ? 16 : 8;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int SF_WARP = 2 + EPI_WARPS;           // MX: the warp that copies scales to TMEM
   static constexpr int THREADS = 64 + EPI_THREADS + (KIND == kMX ? 32 : 0);
@@ -74,7 +80,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = (TX_BYTES + 1023) / 1024 * 1024;
   static constexpr int STAGES = CG == 2 ? 5 : 4;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-  static constexpr int OUT_BYTES = (CG == 2 && KIND != kMX) ? EPI_WARPS * kStageOut : 0;
+  static constexpr int OUT_BYTES = (CG == 2 && KIND != kMX && KIND != kBLK) ? EPI_WARPS * kStageOut : 0;
   static constexpr int TILE_M = BM * CG;
   static constexpr int SF_COL0 = NBUF * TBN;             // first scale-factor slot (16 columns each)
 };
@@ -117,8 +123,8 @@ struct Shared {
   float sb[2][BN];  // per-tile column scales, alternating between consecutive tiles
   uint64_t full[5];
   uint64_t empty[5];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull[4];   // accumulators / K-block partials ready (NBUF of them in use)
+  uint64_t tempty[4];
   uint64_t drain;
   uint64_t never;   // signalled by no one: the failure-detection test hook waits on it
   uint64_t sff[5];  // MX: a stage's scales are in tensor memory
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NBUF; ++b) {
       mbar_init(&S.tfull[b], 1);
       mbar_init(&S.tempty[b], CG * kEpiThreads / 32);
     }
@@ -364,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
                 tma_load_3d(ssf + 512, &tmSB, fb, 0, kx / 128, sfb_rb);
               }
               tma_load_3d(ssf, &tmSA, fb, 0, kx / 128, sfa_rb);
-            } else if (KIND == kFP8) {
+            } else if (KIND == kFP8 || KIND == kBLK) {
               const int32_t kx = (int32_t)(T.k0 + kb * BKB);
               tma_load_2d(sa, &tmA, fb, kx, am);
               if (SCHED == kJagM)
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
                 tma_load_3d_pair(ssf + 512, &tmSB, fb, 0, kx / 128, sfb_rb);
               }
               tma_load_3d_pair(ssf, &tmSA, fb, 0, kx / 128, sfa_rb);
-            } else if (KIND == kFP8) {
+            } else if (KIND == kFP8 || KIND == kBLK) {
               const int32_t kx = (int32_t)(T.k0 + kb * BKB);
               tma_load_2d_pair(sa, &tmA, fb, kx, am);
               if (SCHED == kJagM)
@@ -465,13 +471,24 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
       for (int64_t t = unit; t < total && ok; t += n_units) {
         const int64_t nkb = tile_nkb<SCHED>(p, t, aux);
         if (nkb == 0) continue;
-        if (!mbar_wait(&S.tempty[buf], aphase ^ 1, abort_flag, p.wait_ns)) {
-          if (!*abort_flag) fail();
-          break;
+        if (KIND != kBLK) {
+          if (!mbar_wait(&S.tempty[buf], aphase ^ 1, abort_flag, p.wait_ns)) {
+            if (!*abort_flag) fail();
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * TBN);
+        uint32_t d_tmem = tmem_base + (uint32_t)(buf * TBN);
         for (int64_t kb = 0; kb < nkb; ++kb) {
+          if (KIND == kBLK) {  // each K block into the next free partial buffer
+            if (!mbar_wait(&S.tempty[buf], aphase ^ 1, abort_flag, p.wait_ns)) {
+              if (!*abort_flag) fail();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d_tmem = tmem_base + (uint32_t)(buf * TBN);
+          }
           // MX: the scale warp's commit on sff[stage] follows the stage's full barrier
           if (!mbar_wait(KIND == kMX ? &S.sff[stage] : &S.full[stage], phase, abort_flag, p.wait_ns)) {
             if (!*abort_flag) fail();
@@ -504,14 +521,14 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, 8192, 1024) : smem_desc(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc(sb + kk * 2048, 8192, 1024) : smem_desc(sb + kk * 32, 16, 1024);
-            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t acc = ((KIND != kBLK && kb > 0) || kk > 0) ? 1u : 0u;
             if (CG == 2) {
-              if (KIND == kFP8)
+              if (KIND == kFP8 || KIND == kBLK)
                 umma_f8f6f4_pair(d_tmem, ad, bd, p.idesc, acc);
               else
                 umma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
             } else {
-              if (KIND == kFP8)
+              if (KIND == kFP8 || KIND == kBLK)
                 umma_f8f6f4(d_tmem, ad, bd, p.idesc, acc);
               else
                 umma_f16(d_tmem, ad, bd, p.idesc, acc);
@@ -527,8 +544,19 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
             stage = 0;
             phase ^= 1;
           }
+          if (KIND == kBLK) {  // this K block's partial is ready for promotion
+            if (CG == 2)
+              umma_commit_pair(&S.tfull[buf], 0x3);
+            else
+              umma_commit(&S.tfull[buf]);
+            if (++buf == C::NBUF) {
+              buf = 0;
+              aphase ^= 1;
+            }
+          }
         }
         if (!ok) break;
+        if (KIND == kBLK) continue;
         // accumulator ready for the epilogue(s)
         if (CG == 2)
           umma_commit_pair(&S.tfull[buf], 0x3);
@@ -647,6 +675,98 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
               static_cast<float*>(p.out)[orow * p.ldo + n] = 0.0f;
             else
               static_cast<uint16_t*>(p.out)[orow * p.ldo + n] = 0;
+          }
+        }
+        continue;
+      }
+      if (KIND == kBLK) {
+        // promotion: for every K block, this warp's columns of the partial into registers, the
+        // partial back to the MMAs, then acc += partial * sA[m, kb] * sB[n / 128, kb] (the
+        // warp's columns lie in one 128-column scale block). Stores after the last block.
+        constexpr int WC = C::WCOLS, NL = WC / 16;
+        const int64_t KB = p.nkb;
+        const int64_t nb = (T.n0 + c0) / 128;
+        const bool col_live = T.n0 + c0 < p.N;
+        const float* sa_row = p.sA + (row_ok ? m : 0) * KB;
+        const float* sb_row = p.sB + (col_live ? nb : 0) * KB;
+        float acc[WC];
+#pragma unroll
+        for (int j = 0; j < WC; ++j) acc[j] = 0.0f;
+        float sa_k = __ldg(sa_row), sb_k = __ldg(sb_row);
+        const uint32_t tq = ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
+        bool live = true;
+        for (int64_t kb = 0; kb < T.nkb; ++kb) {
+          const float sk = sa_k * sb_k;
+          if (kb + 1 < T.nkb) {
+            sa_k = __ldg(sa_row + kb + 1);
+            sb_k = __ldg(sb_row + kb + 1);
+          }
+          if (!mbar_wait(&S.tfull[buf], aphase, abort_flag, p.wait_ns)) {
+            if (!*abort_flag) fail();
+            live = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (uint32_t)(buf * TBN) + tq;
+          // 16 columns at a time (the accumulators already hold WC registers); overlapping the
+          // loads with the adds through a second staging set measured no faster
+          uint32_t v[16];
+#pragma unroll
+          for (int h = 0; h + 1 < NL; ++h) {
+            tmem_ld16(taddr + 16 * h, v);
+            tmem_ld_wait_regs16(v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[16 * h + j] = fmaf(__uint_as_float(v[j]), sk, acc[16 * h + j]);
+          }
+          tmem_ld16(taddr + 16 * (NL - 1), v);
+          tmem_ld_wait_regs16(v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (CG == 2)
+              mbar_arrive_cluster(mapa_shared(smem_u32(&S.tempty[buf]), 0));
+            else
+              mbar_arrive(&S.tempty[buf]);
+          }
+          if (++buf == C::NBUF) {
+            buf = 0;
+            aphase ^= 1;
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[16 * (NL - 1) + j] = fmaf(__uint_as_float(v[j]), sk, acc[16 * (NL - 1) + j]);
+        }
+        if (!live) break;
+        if (row_ok) {
+#pragma unroll
+          for (int h = 0; h < WC / 32; ++h) {
+            const int64_t n = T.n0 + c0 + 32 * h;
+            if (n >= p.N) break;
+            const float* a = acc + 32 * h;
+            const bool full = p.vec_ok && n + 32 <= p.N;
+            if (p.out_f32) {
+              float* o = static_cast<float*>(p.out) + orow * p.ldo + n;
+              if (full) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(o + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
+              } else {
+                for (int j = 0; j < 32 && n + j < p.N; ++j) o[j] = a[j];
+              }
+            } else {
+              uint16_t* o = static_cast<uint16_t*>(p.out) + orow * p.ldo + n;
+              uint32_t wd[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const __nv_bfloat162 hb = __floats2bfloat162_rn(a[2 * j], a[2 * j + 1]);
+                wd[j] = *reinterpret_cast<const uint32_t*>(&hb);
+              }
+              if (full) {
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                  *reinterpret_cast<uint4*>(o + 2 * j) = make_uint4(wd[j], wd[j + 1], wd[j + 2], wd[j + 3]);
+              } else {
+                for (int j = 0; j < 32 && n + j < p.N; ++j) o[j] = (uint16_t)(wd[j >> 1] >> (16 * (j & 1)));
+              }
+            }
           }
         }
         continue;
@@ -1020,7 +1140,7 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   p.ends = g.ends;
   p.E = (int)g.E;
   const bool mx = g.mx != 0;
-  const int tbn = mx ? Cfg<kMX, 1>::TBN : BN;
+  const int tbn = mx ? Cfg<kMX, 1>::TBN : (g.blockwise ? Cfg<kBLK, 1>::TBN : BN);
   p.num_n = (g.N + tbn - 1) / tbn;
   const int esz = fp8 ? 1 : 2;
   p.nkb = (g.K * esz + BKB - 1) / BKB;
@@ -1087,11 +1207,23 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
       if (rc) return rc;
       if (g.mode == -1) {
         const int64_t tiles = p.num_m * p.num_n;
+        if (g.blockwise) {  // sA [M, K/128], sB [ceil(N/128), K/128]; 128-column tiles
+          if (g.K % 128 || p.row_amax || p.col_amax) return FP8_ERR_UNSUPPORTED;
+          constexpr int TB = Cfg<kBLK, 1>::TBN;
+          p.idesc = make_idesc(af, bf, 0, 0, tile_m, TB);
+          const uint32_t boxB2[2] = {BKB, pair ? TB / 2 : TB};
+          CUtensorMap tbb;
+          rc = make_tmap(&tbb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dB, strideK, boxB2, CU_TENSOR_MAP_SWIZZLE_128B);
+          if (rc) return rc;
+          return pair ? run<kBLK, kDense, 0, 0, 2>(ta, tbb, to, none, none, p, tiles, c)
+                      : run<kBLK, kDense, 0, 0, 1>(ta, tbb, to, none, none, p, tiles, c);
+        }
         if (p.row_amax || p.col_amax)
           return pair ? run<kFP8, kDenseAmax, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c)
                       : run<kFP8, kDenseAmax, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
         return pair ? run<kFP8, kDense, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c) : run<kFP8, kDense, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
       }
+      if (g.blockwise) return FP8_ERR_UNSUPPORTED;
       // jagged K: A = G^T [N_out, P], B = X^T [Kd, P]; tile space M = N_out, N = Kd; the
       // offsets are checked for order and for fitting the padded length P.
       p.total_rows = -1;
@@ -1099,6 +1231,7 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
       return pair ? run<kFP8, kJagK, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c) : run<kFP8, kJagK, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
     }
     if (g.mode == FP8_GROUPED_JAGGED_M) {
+      if (g.blockwise) return FP8_ERR_UNSUPPORTED;
       p.total_rows = g.M;
       const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.E};
       const uint64_t sB_[2] = {(uint64_t)g.K, (uint64_t)(g.N * g.K)};

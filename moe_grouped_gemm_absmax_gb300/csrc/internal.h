@@ -61,6 +61,13 @@ int64_t mx_scale_bytes(int64_t rows, int64_t k);
 int launch_mx_quant(const void* x, int64_t batches, int64_t R, int64_t C, int fmt, void* q, void* sf, void* qt,
                     int64_t ld_t, void* sft, const int32_t* ends, int64_t E, int32_t* pstart_ws, const Ctx& c);
 
+// --- blockwise quantize (blockwise.cu) ---
+// x bf16 [R, C] (C % 128 == 0). tile128 false: 1 x 128 tiles, row-major codes q, inv [R, C/128].
+// tile128 true: 128 x 128 tiles; q row-major and/or qt column-major [C, R] (R % 128 == 0);
+// inv [ceil(R/128), C/128] (may be null when qt is given) and inv_t [C/128, R/128] (with qt).
+int launch_blk_quant(const void* x, int64_t R, int64_t C, int fmt, bool tile128, void* q, void* qt, float* inv,
+                     float* inv_t, const Ctx& c);
+
 // --- GEMM launchers (gemm.cu) ---
 struct GemmArgs {
   // operands
@@ -88,6 +95,8 @@ struct GemmArgs {
   uint32_t* row_amax;
   uint32_t* col_amax;
   int amax_whole;         // col_amax is one word: the maximum over the whole output
+  int blockwise;          // FP8 operands with blockwise inverse scales: sA [M, K/128] (1 x 128 tiles),
+                          // sB [ceil(N/128), K/128] (128 x 128 tiles); dense only
 };
 int launch_gemm(const GemmArgs& g, const Ctx& c);
 

@@ -149,6 +149,11 @@ WORKLOADS = {
         "the llama3-8b-mlp-up grad-input GEMM dX = dY W (rowwise FP8 operands) with dX's column "
         "maxima from the GEMM epilogue, then dX quantized column-wise (e5m2, column-major) from them",
         dict(M=8192, K=4096, N=14336)),
+    "llama3-8b-mlp-up-blockwise": Workload(
+        "llama3-8b-mlp-up-blockwise",
+        "the llama3-8b-mlp-up Linear and inputs with blockwise scaling: x and dY in 1 x 128 tiles, W in "
+        "128 x 128 tiles; fwd and dX blockwise FP8 GEMMs, dW bf16",
+        dict(M=8192, K=4096, N=14336)),
     # the same shapes with MXFP8 (blocks of 32, E8M0 scales) for every operand of every GEMM
     "llama3-8b-mlp-up-mx": Workload(
         "llama3-8b-mlp-up-mx",
