@@ -60,7 +60,7 @@ enum { kFP8 = 0, kBF16 = 1, kMX = 2, kBLK = 3 };
 // fit in the 512 columns, two accumulators would not. Sixteen epilogue warps (four per lane
 // quarter, 64 columns each) move the accumulator into registers right after the tile's MMAs and
 // release it at once, so the next tile's MMAs wait only for those loads, not for the stores.
-template <int KIND, int CG>
+template <int KIND, int CG, int SCHED = 0>
 struct Cfg {
   // kBLK: 256-column tiles and two K-block partials (the MMAs run one K block ahead of the
   // promotion). 128-column tiles with four partials were slower: the MMA's cost is per
@@ -78,13 +78,18 @@ struct Cfg {
   static constexpr int SF_BYTES = KIND == kMX ? 3 * 512 : 0;  // one A scale block, two B scale blocks
   static constexpr int TX_BYTES = A_BYTES + B_BYTES + SF_BYTES;  // bytes the loads of a stage deliver
   static constexpr int STAGE_BYTES = (TX_BYTES + 1023) / 1024 * 1024;
-  static constexpr int STAGES = CG == 2 ? 5 : 4;
+  // MX with the contraction jagged: short K loops make the epilogue's stores the critical path,
+  // so those tiles store through shared memory with TMA (64 KB of staging for 16 warps), which
+  // leaves room for 4 stages; the other MX schedules store from registers and keep 5
+  static constexpr bool MX_TMA_OUT = KIND == kMX && CG == 2 && SCHED == 2;
+  static constexpr int STAGES = (CG == 2 && !MX_TMA_OUT) ? 5 : 4;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-  static constexpr int OUT_BYTES = (CG == 2 && KIND != kMX && KIND != kBLK) ? EPI_WARPS * kStageOut : 0;
+  static constexpr int OUT_BYTES = (CG == 2 && ((KIND != kMX && KIND != kBLK) || MX_TMA_OUT)) ? EPI_WARPS * kStageOut : 0;
   static constexpr int TILE_M = BM * CG;
   static constexpr int SF_COL0 = NBUF * TBN;             // first scale-factor slot (16 columns each)
 };
 static_assert(Cfg<kMX, 2>::SF_COL0 + 16 * Cfg<kMX, 2>::STAGES <= kTmemCols, "MX tensor-memory budget");
+static_assert(Cfg<kMX, 2, 2>::STAGES <= Cfg<kMX, 2>::STAGES, "MX jagged-K ring");
 
 struct GemmParams {
   int64_t M, N, K;     // tile space: rows of D, columns of D, contraction length (elements)
@@ -203,11 +208,11 @@ FP8_DEVI int64_t tile_nkb(const GemmParams& p, int64_t t, const int32_t* aux) {
 }
 
 template <int KIND, int SCHED, int A_MN, int B_MN, int CG>
-__global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmSA,
                 const __grid_constant__ CUtensorMap tmSB, const GemmParams p) {
-  using C = Cfg<KIND, CG>;
+  using C = Cfg<KIND, CG, SCHED>;
   constexpr int STAGES = C::STAGES;
   constexpr int kThreads = C::THREADS;
   constexpr int kEpiThreads = C::EPI_THREADS;
@@ -794,6 +799,33 @@ __global__ void __launch_bounds__(Cfg<KIND, CG>::THREADS, 1)
             mbar_arrive(&S.tempty[0]);
         }
         aphase ^= 1;
+        if (C::MX_TMA_OUT && p.tma_out && !p.out_f32 && T.n0 + c0 < p.N) {
+          // jagged K: bf16 through a 128-byte-swizzled [32 rows][128 B] box and one TMA store
+          // per warp and tile (columns past N are clipped by the copy)
+          const int64_t wrow0 = T.m0 + (int64_t)rank * BM + q * 32;
+          uint8_t* st = out_stage + (warp - 2) * kStageOut;
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(va[2 * j]), __uint_as_float(va[2 * j + 1]));
+            const __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(vb[2 * j]), __uint_as_float(vb[2 * j + 1]));
+            w[j] = *reinterpret_cast<const uint32_t*>(&h0);
+            w[16 + j] = *reinterpret_cast<const uint32_t*>(&h1);
+          }
+          if (lane == 0) bulk_wait_read_all();  // the previous tile's store has read the buffer
+          __syncwarp();
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<uint4*>(st + lane * 128 + ((c8 ^ (lane & 7)) << 4)) =
+                make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmO, st, (int32_t)(T.n0 + c0), (int32_t)wrow0, T.e);
+            bulk_commit();
+          }
+          continue;
+        }
         if (row_ok) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -1024,7 +1056,7 @@ template <int KIND, int SCHED, int A_MN, int B_MN, int CG>
 int run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const CUtensorMap& sfa,
         const CUtensorMap& sfb, const GemmParams& p, int64_t total_tiles_hint, const Ctx& c) {
   auto kern = gemm_kernel<KIND, SCHED, A_MN, B_MN, CG>;
-  using C = Cfg<KIND, CG>;
+  using C = Cfg<KIND, CG, SCHED>;
   constexpr int kThreads = C::THREADS;
   const int n_arrays = is_dense(SCHED) ? 0 : (KIND == kMX && SCHED == kJagM) ? 3 : 2;
   const size_t smem = 1024 + C::RING_BYTES + C::OUT_BYTES + kSharedBytes + (size_t)n_arrays * 4 * (p.E + 1);
@@ -1184,7 +1216,7 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   }
 
   if (mx) {
-    p.tma_out = 0;  // the MX epilogue stores straight from registers
+    if (g.mode != FP8_GROUPED_JAGGED_K) p.tma_out = 0;  // MX stores from registers except jagged K
     return launch_mx(g, p, to, pair, tile_m, c);
   }
   if (fp8) {
