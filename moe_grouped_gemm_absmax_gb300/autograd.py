@@ -9,7 +9,7 @@ them into autograd. No bias: the pages' hot path is the bias-free matmul, and a 
 non-FP8 step."""
 import torch
 
-from . import (GRAN_MX, GRAN_ROW, GRAN_TENSOR, MM_FAST_ACCUM, OP_LINEAR_BWD, OP_LINEAR_FWD, WGRAD_BF16,
+from . import (GRAN_BLOCK_1x128, GRAN_MX, GRAN_ROW, GRAN_TENSOR, MM_FAST_ACCUM, OP_LINEAR_BWD, OP_LINEAR_FWD, WGRAD_BF16,
                WGRAD_FP8, fp8_linear_bwd, fp8_linear_fwd, fp8_workspace_size, linear_saved_alloc, make_saved)
 
 
@@ -58,7 +58,8 @@ class Fp8LinearFunction(torch.autograd.Function):
 
 class Fp8Linear(torch.nn.Module):
     """Drop-in for a bias-free torch.nn.Linear: the weight stays bf16; the matmuls run in FP8
-    (granularity GRAN_TENSOR, GRAN_ROW or GRAN_MX; MX needs dimensions that are multiples of 128)."""
+    (granularity GRAN_TENSOR, GRAN_ROW, GRAN_MX or GRAN_BLOCK_1x128; MX and blockwise need
+    dimensions that are multiples of 128, blockwise a bf16 weight gradient)."""
 
     def __init__(self, in_features, out_features, granularity=GRAN_ROW, wgrad_mode=WGRAD_BF16, weight=None,
                  device=None):
@@ -76,7 +77,7 @@ class Fp8Linear(torch.nn.Module):
         return Fp8LinearFunction.apply(x.to(torch.bfloat16), self.weight, self.granularity, self.wgrad_mode)
 
     def extra_repr(self):
-        g = {GRAN_ROW: "row", GRAN_TENSOR: "tensor", GRAN_MX: "mx"}[self.granularity]
+        g = {GRAN_ROW: "row", GRAN_TENSOR: "tensor", GRAN_MX: "mx", GRAN_BLOCK_1x128: "blockwise"}[self.granularity]
         w = {WGRAD_BF16: "bf16", WGRAD_FP8: "fp8"}[self.wgrad_mode]
         return f"in_features={self.in_features}, out_features={self.out_features}, scaling={g}, wgrad={w}"
 

@@ -32,7 +32,7 @@ def _direct(fp8, x, w, dy, gran, wgrad):
 
 @pytest.mark.parametrize("gran_name,wgrad_name", [("GRAN_ROW", "WGRAD_BF16"), ("GRAN_ROW", "WGRAD_FP8"),
                                                   ("GRAN_TENSOR", "WGRAD_FP8"), ("GRAN_MX", "WGRAD_FP8"),
-                                                  ("GRAN_MX", "WGRAD_BF16")])
+                                                  ("GRAN_MX", "WGRAD_BF16"), ("GRAN_BLOCK_1x128", "WGRAD_BF16")])
 def test_function_matches_entry_points(fp8, gran_name, wgrad_name):
     from moe_grouped_gemm_absmax_gb300.autograd import Fp8LinearFunction
     gran, wgrad = getattr(fp8, gran_name), getattr(fp8, wgrad_name)

@@ -104,3 +104,47 @@ def test_grouped_graph_replay_matches_eager(fp8):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("gran_name,wgrad_name", [("GRAN_MX", "WGRAD_FP8"), ("GRAN_BLOCK_1x128", "WGRAD_BF16")])
+def test_mx_and_blockwise_linear_graph_replay(fp8, gran_name, wgrad_name):
+    """The MX and blockwise Linear forward + backward captured into one graph and replayed:
+    bit-identical to the eager calls."""
+    gran, wgrad = getattr(fp8, gran_name), getattr(fp8, wgrad_name)
+    M, K, N = 1024, 512, 768
+    x, w, dy = W.linear_inputs(M, K, N, seed=22, device="cuda", outliers=True)
+    saved, bufs = fp8.linear_saved_alloc(M, K, N, gran, keep_xt=wgrad == fp8.WGRAD_FP8)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(max(fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, gran, wgrad), 16), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        fp8.fp8_linear_fwd(x, w, gran, fp8.MM_FAST_ACCUM, y, saved, None, st)
+        fp8.fp8_linear_bwd(dy, saved, x, w, gran, wgrad, dx, dw, ws, st)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (y, dx, dw)] + [b.clone() for b in bufs if b is not None]
+    for t in (y, dx, dw):
+        t.fill_(float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for t in (y, dx, dw):
+        t.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    now = [y, dx, dw] + [b for b in bufs if b is not None]
+    for a, b in zip(now, eager):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
