@@ -62,15 +62,17 @@ enum { kFP8 = 0, kBF16 = 1, kMX = 2, kBLK = 3 };
 // release it at once, so the next tile's MMAs wait only for those loads, not for the stores.
 template <int KIND, int CG, int SCHED = 0>
 struct Cfg {
-  // kBLK: 256-column tiles and two K-block partials (the MMAs run one K block ahead of the
-  // promotion). 128-column tiles with four partials were slower: the MMA's cost is per
+  // kBLK: single-CTA 128 x 256 tiles and two K-block partials (the MMAs run one K block ahead
+  // of the promotion). 128-column tiles with four partials were slower: the MMA's cost is per
   // instruction, so halving N halves the tensor-core rate.
   static constexpr int TBN = BN;                          // tile columns
   static constexpr int NBUF = KIND == kMX ? 1 : 2;        // accumulators / K-block partials
   static constexpr int EPI_WARPS = (KIND == kMX || KIND == kBLK) ? 16 : 8;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-  static constexpr int SF_WARP = 2 + EPI_WARPS;           // MX: the warp that copies scales to TMEM
-  static constexpr int THREADS = 64 + EPI_THREADS + (KIND == kMX ? 32 : 0);
+  // MX: the warp that copies scales to tensor memory; kBLK: the warp that stages each K block's
+  // tile scales in shared memory ahead of the promotion
+  static constexpr int SF_WARP = 2 + EPI_WARPS;
+  static constexpr int THREADS = 64 + EPI_THREADS + ((KIND == kMX || KIND == kBLK) ? 32 : 0);
   static constexpr int WCOLS = TBN * 4 / EPI_WARPS;      // columns per epilogue warp: 128 or 64
   static constexpr int A_BYTES = BM * BKB;               // this CTA's 128 rows of A
   static constexpr int B_ROWS = TBN / CG;                // this CTA's rows of B
@@ -138,6 +140,17 @@ struct Shared {
   int abort;
 };
 constexpr int kSharedBytes = 2304;
+// kBLK: a ring of K-block tile scales in shared memory, filled by the scale warp ahead of the
+// promotion: per slot this CTA's 128 row scales and the tile's two 128-column block scales
+constexpr int kScGroup = 8;   // K blocks whose scales the scale warp loads in one burst
+constexpr int kScSlots = 16;  // two bursts: one being consumed while the next is loaded
+struct ScaleRing {
+  float a[kScSlots][128];
+  float b[kScSlots][4];
+  uint64_t full[kScSlots];   // 32 arrivals: every lane of the scale warp after its stores
+  uint64_t empty[kScSlots];  // one arrival per promoter warp after its reads
+};
+constexpr int kScaleRingBytes = (int)((sizeof(ScaleRing) + 127) / 128 * 128);
 static_assert(sizeof(Shared) <= kSharedBytes, "shared block");
 
 FP8_DEVI int find_expert(const int32_t* tpre, int E, int64_t t) {
@@ -224,6 +237,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
   Shared& S = *reinterpret_cast<Shared*>(smem + C::RING_BYTES + C::OUT_BYTES);
   int32_t* tpre = reinterpret_cast<int32_t*>(smem + C::RING_BYTES + C::OUT_BYTES + kSharedBytes);
   int32_t* aux = tpre + (p.E + 1);
+  ScaleRing& SR = *reinterpret_cast<ScaleRing*>(smem + C::RING_BYTES + C::OUT_BYTES + kSharedBytes);  // kBLK (dense)
   int32_t* pst = kPadRows ? aux + (p.E + 1) : nullptr;  // padded segment starts
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &S.abort;
@@ -306,6 +320,12 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
     mbar_init(&S.drain, 1);
     for (int s2 = 0; s2 < STAGES; ++s2) mbar_init(&S.sff[s2], 1);
     mbar_init(&S.sf_drain, 1);
+    if (KIND == kBLK) {
+      for (int i = 0; i < kScSlots; ++i) {
+        mbar_init(&SR.full[i], 32);
+        mbar_init(&SR.empty[i], C::EPI_WARPS);
+      }
+    }
     mbar_init(&S.never, 1);
     S.abort = 0;
     fence_mbar_init();
@@ -579,6 +599,53 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
         umma_commit(&S.drain);
     }
     __syncwarp();
+  } else if (KIND == kBLK && warp == C::SF_WARP) {
+    // ======================= blockwise: tile scales, K block by K block =======================
+    // For every K block of every tile this CTA computes: this CTA's 128 row scales
+    // sA[m, kb] (lane l holds rows l, l + 32, l + 64, l + 96) and the two 128-column block
+    // scales sB[n / 128, kb], into the next ring slot. The loads for kScGroup K blocks go out
+    // together (one memory latency per burst, not per block), and the ring holds two bursts.
+    int slot = 0;
+    uint32_t ph = 0;
+    const int64_t KB = p.nkb;
+    bool ok = true;
+    for (int64_t t = unit; t < total && ok; t += n_units) {
+      const Tile T = get_tile<SCHED, C::TILE_M, TBN>(p, t, tpre, aux, pst);
+      const int64_t r0 = T.m0 + (int64_t)rank * BM;
+      const int64_t nb = T.n0 / 128 + (lane & 1);
+      const bool b_live = lane < 2 && nb * 128 < p.N;
+      for (int64_t kb0 = 0; kb0 < T.nkb && ok; kb0 += kScGroup) {
+        float va[4][kScGroup], vb[kScGroup];
+#pragma unroll
+        for (int j = 0; j < kScGroup; ++j) {
+          const bool k_live = kb0 + j < T.nkb;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int64_t r = r0 + lane + 32 * i;
+            va[i][j] = (k_live && r < p.M) ? __ldg(p.sA + r * KB + kb0 + j) : 0.0f;
+          }
+          vb[j] = (k_live && b_live) ? __ldg(p.sB + nb * KB + kb0 + j) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kScGroup; ++j) {
+          if (kb0 + j >= T.nkb) break;
+          if (!mbar_wait(&SR.empty[slot], ph ^ 1, abort_flag, p.wait_ns)) {
+            if (!*abort_flag) fail();
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) SR.a[slot][lane + 32 * i] = va[i][j];
+          if (lane < 2) SR.b[slot][lane] = vb[j];
+          mbar_arrive(&SR.full[slot]);  // release: this lane's stores before the arrival
+          if (++slot == kScSlots) {
+            slot = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+    __syncwarp();
   } else if (KIND == kMX && warp == C::SF_WARP) {
     // ============================ MX scale copies ============================
     // For every stage the MMA thread will consume: wait for its loads, copy its three scale
@@ -633,6 +700,8 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
     const int row = (int)rank * BM + q * 32 + lane;  // row within the pair's tile
     const bool stage_sb = KIND == kFP8 && !p.sb_scalar;
     int buf = 0, sbi = 0;
+    int sc_slot = 0;       // kBLK: scale-ring slot and phase
+    uint32_t sc_ph = 0;
     uint32_t oseq = 0;  // TMA stores issued by this warp
     uint32_t aphase = 0;
     // The next tile and the scales it needs (this thread's row scale; its column scale, or the
@@ -689,22 +758,25 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
         // partial back to the MMAs, then acc += partial * sA[m, kb] * sB[n / 128, kb] (the
         // warp's columns lie in one 128-column scale block). Stores after the last block.
         constexpr int WC = C::WCOLS, NL = WC / 16;
-        const int64_t KB = p.nkb;
-        const int64_t nb = (T.n0 + c0) / 128;
-        const bool col_live = T.n0 + c0 < p.N;
-        const float* sa_row = p.sA + (row_ok ? m : 0) * KB;
-        const float* sb_row = p.sB + (col_live ? nb : 0) * KB;
+        const int bsel = c0 / 128;  // which of the tile's two 128-column scale blocks
         float acc[WC];
 #pragma unroll
         for (int j = 0; j < WC; ++j) acc[j] = 0.0f;
-        float sa_k = __ldg(sa_row), sb_k = __ldg(sb_row);
         const uint32_t tq = ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
         bool live = true;
         for (int64_t kb = 0; kb < T.nkb; ++kb) {
-          const float sk = sa_k * sb_k;
-          if (kb + 1 < T.nkb) {
-            sa_k = __ldg(sa_row + kb + 1);
-            sb_k = __ldg(sb_row + kb + 1);
+          // this K block's scales from the ring (staged ahead by the scale warp)
+          if (!mbar_wait(&SR.full[sc_slot], sc_ph, abort_flag, p.wait_ns)) {
+            if (!*abort_flag) fail();
+            live = false;
+            break;
+          }
+          const float sk = SR.a[sc_slot][q * 32 + lane] * SR.b[sc_slot][bsel];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&SR.empty[sc_slot]);
+          if (++sc_slot == kScSlots) {
+            sc_slot = 0;
+            sc_ph ^= 1;
           }
           if (!mbar_wait(&S.tfull[buf], aphase, abort_flag, p.wait_ns)) {
             if (!*abort_flag) fail();
@@ -1059,7 +1131,8 @@ int run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o, const 
   using C = Cfg<KIND, CG, SCHED>;
   constexpr int kThreads = C::THREADS;
   const int n_arrays = is_dense(SCHED) ? 0 : (KIND == kMX && SCHED == kJagM) ? 3 : 2;
-  const size_t smem = 1024 + C::RING_BYTES + C::OUT_BYTES + kSharedBytes + (size_t)n_arrays * 4 * (p.E + 1);
+  const size_t smem = 1024 + C::RING_BYTES + C::OUT_BYTES + kSharedBytes + (size_t)n_arrays * 4 * (p.E + 1) +
+                     (KIND == kBLK ? kScaleRingBytes : 0);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FP8_ERR_CUDA;
   int64_t units = c.sm_count / CG;
@@ -1179,9 +1252,12 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   p.ldo = g.N;
   p.vec_ok = p.out_f32 ? (p.ldo % 4 == 0) : (p.ldo % 8 == 0);
   if (g.mode != -1 && (g.E < 1 || g.E > kMaxExperts)) return FP8_ERR_UNSUPPORTED;
-  // pair tiles when there are at least ~one per SM pair
+  // pair tiles when there are at least ~one per SM pair. Blockwise scaling runs on single CTAs:
+  // its per-K-block commit / promotion / release cycle ran at half the speed across a CTA pair
+  // (1050 vs 560 us on 8192 x 14336 x 4096; 600 us for the pair even with the promotion's waits
+  // removed, so the pair's per-block commits, not the promotion, set that pace).
   const int64_t pair_tiles = ((g.M + 255) / 256) * p.num_n * (g.mode == FP8_GROUPED_JAGGED_K ? g.E : 1);
-  const bool pair = g.mode == FP8_GROUPED_JAGGED_M ? g.M >= 2048 : pair_tiles * 2 >= c.sm_count;
+  const bool pair = !g.blockwise && (g.mode == FP8_GROUPED_JAGGED_M ? g.M >= 2048 : pair_tiles * 2 >= c.sm_count);
   const int tile_m = pair ? 256 : 128;
   p.num_m = (g.M + tile_m - 1) / tile_m;
   // the kernels index tiles with 32-bit arithmetic
@@ -1247,8 +1323,7 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
           CUtensorMap tbb;
           rc = make_tmap(&tbb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dB, strideK, boxB2, CU_TENSOR_MAP_SWIZZLE_128B);
           if (rc) return rc;
-          return pair ? run<kBLK, kDense, 0, 0, 2>(ta, tbb, to, none, none, p, tiles, c)
-                      : run<kBLK, kDense, 0, 0, 1>(ta, tbb, to, none, none, p, tiles, c);
+          return run<kBLK, kDense, 0, 0, 1>(ta, tbb, to, none, none, p, tiles, c);
         }
         if (p.row_amax || p.col_amax)
           return pair ? run<kFP8, kDenseAmax, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c)
