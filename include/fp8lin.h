@@ -185,7 +185,8 @@ typedef struct fp8_tensor {
  *              (with offsets fp8_mx_scale_bytes(P, C)); COL_MAJOR B * fp8_mx_scale_bytes(C, R)
  *              (with offsets fp8_mx_scale_bytes(C, P)); BOTH the row-major scales followed by
  *              the column-major ones.
- *  offsets     NULL, or int32 [E] cumulative segment ends (COL granularity, 2-D x only).
+ *  offsets     NULL, or int32 [E] cumulative segment ends (COL granularity, 2-D x only);
+ *              E <= 2048.
  *              Checked on the device: a bad vector sets FP8_DEV_BAD_OFFSETS.
  *  workspace   device memory, 16-byte aligned, of fp8_workspace_size(FP8_OP_QUANTIZE, groups,
  *              C, granularity) bytes: 4 bytes for tensor granularity (the amax word); for

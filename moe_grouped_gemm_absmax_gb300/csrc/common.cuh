@@ -238,6 +238,18 @@ FP8_DEVI void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read
 FP8_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 FP8_DEVI void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
+// Asynchronous 4-byte copy global -> shared (zero-filled when `valid` is false), tracked per thread
+// in commit groups: a move of a register that a plain load is still filling waits for the load,
+// an asynchronous copy into shared memory does not.
+FP8_DEVI void cp_async4(void* smem_dst, const void* gsrc, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+FP8_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+FP8_DEVI void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // ------------------------------------------------------------------------------------------
 // tcgen05: tensor memory allocation, MMA issue, commit, loads, fences.
 FP8_DEVI void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -306,29 +306,32 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 // (segment); units never straddle a group boundary and are ordered group, row tile, strip, so a
 // CTA's contiguous range of units reads long row segments (several KB per row) and neighbouring
 // strips share DRAM pages and L2 lines. Every CTA takes one contiguous range of units:
-//   producer warp: streams the range's tiles into a 4-stage shared-memory ring with TMA
-//              (128-byte swizzle), ~128 KB of loads in flight per SM;
+//   producer warp: streams the range's tiles into a shared-memory ring with TMA (128-byte
+//              swizzle), 6 stages in pass 1 and 5 in pass 2: 160-192 KB of loads in flight per SM;
 //   8 consumer warps read each tile from the ring (conflict-free through the swizzle).
 //   pass 1 (max): a tile's per-column |x| maxima are folded by shuffles and shared memory into
 //              one relaxed atomic max per column on a per-(group, column) scratch word (the bf16
 //              bit pattern of the maximum).
-//   pass 2 (cast): the scale step for the tile's 64 columns from the scratch words (fetched one
-//              tile ahead; the strip's first tile also writes the inverse scales); the fp32
-//              multiply and the cast in
-//              registers; each 4-row column pack becomes one 32-bit word of FP8 codes in a
-//              transposed tile in shared memory (64 columns x 128 rows per box, 128-byte swizzle;
-//              a thread's 8 columns are rotated by its chunk index so the stores are
-//              conflict-free); TMA bulk-tensor stores write whole column-major boxes from two
-//              alternating tiles. Pass 2 walks each range backwards, so its first reads are the
-//              tiles pass 1 read last, still in L2.
+//   pass 2 (cast): the producer turns the scratch words into the tile's 64 scales (words
+//              fetched three tiles ahead; the strip's first tile also writes the inverse scales).
+//              Each consumer warp then owns 32 rows of the tile: a lane takes a column pair,
+//              multiplies in fp32 and casts in registers, writes its two 32-code rows of the
+//              transposed box (64 columns x 32 rows) in the warp's own staging buffer, and the
+//              warp's elected lane stores the box by TMA (two alternating buffers per warp), so
+//              the warps never wait on one another. Pass 2 walks each range backwards, so its
+//              first reads are the tiles pass 1 read last, still in L2.
 // The passes are stream-ordered launches: no CTA waits on another.
 constexpr int kColThreads = 256;
 constexpr int kColNB = 2;                  // 128-row blocks per work unit (256 rows)
 constexpr int kColTile = 128 * kColNB;
-constexpr int kColStages = 4;
+constexpr int kColStagesMax = 6;  // ring stages: 6 in pass 1, 5 in pass 2 (its staging boxes take the rest)
+template <bool CAST>
+constexpr int col_stages() { return CAST ? 5 : 6; }
 constexpr int kColStageBytes = kColTile * 128;         // 256 rows x 64 bf16
 constexpr int kColOutBytes = (kColTile / 128) * 8192;  // 64 columns x 256 rows of codes
+constexpr int kColWarpBox = 64 * 32;                   // pass 2: one warp's 64 columns x 32 rows of codes
 constexpr int kColConsumerWarps = kColThreads / 32;    // 8
+static_assert(2 * kColOutBytes == kColConsumerWarps * 2 * kColWarpBox, "pass-2 staging: two boxes per warp");
 constexpr uint64_t kColDrainNs = 2000000000ull;        // fixed bound: loads in flight before exit
 
 struct ColParams {
@@ -353,10 +356,12 @@ struct ColUnit {
 };
 
 // Unit i: group, row tile, strip. Segment mode: upre[e] = first unit of segment e, ppre[e] = its
-// padded start.
+// padded start, ppre[n_groups + 1 + e] = its first row (shared memory only: no global load on the
+// producer's path).
+// Unit indices fit 32 bits (the host checks), so the divisions are 32-bit.
 FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t i, const int32_t* upre, const int32_t* ppre) {
   ColUnit u;
-  int64_t local;
+  uint32_t local;
   if (p.mode == 2) {
     int lo = 0, hi = (int)p.n_groups - 1;
     while (lo < hi) {
@@ -365,29 +370,32 @@ FP8_DEVI ColUnit col_unit(const ColParams& p, int64_t i, const int32_t* upre, co
       else hi = mid - 1;
     }
     u.g = lo;
-    local = i - upre[lo];
-    u.g0 = lo ? p.ends[lo - 1] : 0;
-    u.n = p.ends[lo] - u.g0;
+    local = (uint32_t)(i - upre[lo]);
+    const int32_t* rpre = ppre + (p.n_groups + 1);
+    u.g0 = rpre[lo];
+    u.n = rpre[lo + 1] - u.g0;
     u.pstart = ppre[lo];
     u.write_end = round_up64(u.n, 128);
   } else {
-    const int64_t per = p.n_strips * ceil_div64(p.group_rows, kColTile);
-    u.g = i / per;
-    local = i - u.g * per;
+    const uint32_t per = (uint32_t)(p.n_strips * ceil_div64(p.group_rows, kColTile));
+    const uint32_t g = (uint32_t)i / per;
+    u.g = g;
+    local = (uint32_t)i - g * per;
     u.g0 = u.g * p.group_rows;
     u.n = p.group_rows;
     u.pstart = 0;
     u.write_end = u.n;
   }
-  const int64_t rt = local / p.n_strips;
-  u.strip = local - rt * p.n_strips;
-  u.rt = rt * kColTile;
+  const uint32_t ns = (uint32_t)p.n_strips;
+  const uint32_t rt = local / ns;
+  u.strip = local - rt * ns;
+  u.rt = (int64_t)rt * kColTile;
   u.c0 = u.strip * 64;
   return u;
 }
 
-// Validates the offsets (segment mode) and builds the unit / padded-start prefixes in shared
-// memory; returns the number of units, or -1 after reporting bad offsets.
+// Validates the offsets (segment mode) and builds the unit / padded-start / first-row prefixes in
+// shared memory; returns the number of units, or -1 after reporting bad offsets.
 FP8_DEVI int64_t col_setup(const ColParams& p, int32_t* upre, int32_t* ppre) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (p.mode != 2) return p.n_groups * p.n_strips * ceil_div64(p.group_rows, kColTile);
@@ -423,6 +431,7 @@ FP8_DEVI int64_t col_setup(const ColParams& p, int32_t* upre, int32_t* ppre) {
       if (i < p.n_groups) {
         upre[i + 1] = vu + cu;
         ppre[i + 1] = vp + cp;
+        ppre[p.n_groups + 1 + i + 1] = p.ends[i];
       }
       cu += __shfl_sync(0xffffffffu, vu, 31);
       cp += __shfl_sync(0xffffffffu, vp, 31);
@@ -430,6 +439,7 @@ FP8_DEVI int64_t col_setup(const ColParams& p, int32_t* upre, int32_t* ppre) {
     if (lane == 0) {
       upre[0] = 0;
       ppre[0] = 0;
+      ppre[p.n_groups + 1] = 0;
     }
   }
   __syncthreads();
@@ -447,18 +457,19 @@ struct ColInfo {
   int32_t g, c0, rt, valid, wrows, pstart;  // group, first column, tile start, rows of the group, rows written
 };
 struct ColShared {
-  uint64_t full[kColStages];   // the tile landed (TMA bytes) and the info was written
-  uint64_t scl[kColStages];    // pass 2: the stage's 64 scales were written
-  uint64_t empty[kColStages];  // the consumer warps are done with the stage
-  ColInfo info[kColStages];
-  float sc[kColStages][64];    // pass 2: the fp32 scales of the stage's 64 columns
+  uint64_t full[kColStagesMax];   // the tile landed (TMA bytes) and the info was written
+  uint64_t scl[kColStagesMax];    // pass 2: the stage's 64 scales were written
+  uint64_t empty[kColStagesMax];  // the consumer warps are done with the stage
+  ColInfo info[kColStagesMax];
+  float sc[kColStagesMax][64];    // pass 2: the fp32 scales of the stage's 64 columns
+  uint32_t am[4][64];             // pass 2: amax words of units k .. k + 3 (asynchronous copies)
   uint32_t red[kColConsumerWarps][8][4];
   int abort;
 };
 template <bool CAST>
 struct ColSmem {
   static constexpr int bytes =
-      1024 + kColStages * kColStageBytes + (CAST ? 2 * kColOutBytes : 0) + (int)sizeof(ColShared);
+      1024 + col_stages<CAST>() * kColStageBytes + (CAST ? 2 * kColOutBytes : 0) + (int)sizeof(ColShared);
 };
 
 template <int FMT, bool CAST>
@@ -467,6 +478,7 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
                                                                         const ColParams p,
                                                                         const __grid_constant__ ScaleTab tab) {
   extern __shared__ uint8_t smem_raw[];
+  constexpr int kColStages = col_stages<CAST>();
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Tout = ring + kColStages * kColStageBytes;
   ColShared& S = *reinterpret_cast<ColShared*>(Tout + (CAST ? 2 * kColOutBytes : 0));
@@ -514,19 +526,26 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
     int s = 0;
     uint32_t ph = 0;
     int64_t k = 0;
-    uint32_t am[2] = {0, 0};  // pass 2: amax words of the next unit's columns lane, lane + 32
-    auto fetch_amax = [&](const ColUnit& un) {
+    // units k, k + 1, k + 2 are decoded ahead; in pass 2 the amax words of unit k + 3's columns
+    // lane and lane + 32 are copied asynchronously into slot (k + 3) % 4 of a shared-memory ring
+    // (one commit group per unit, possibly empty), so their latency stays off this warp's path
+    ColUnit u0 = {}, u1 = {}, u2 = {};
+    auto decode = [&](int64_t kk, ColUnit& un) {
+      if (kk < cnt) un = col_unit(p, unit_at(kk), upre, ppre);
+      if (CAST) {
+        if (kk < cnt) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t col = un.c0 + lane + 32 * h;
-        am[h] = col < p.C ? __ldcg(p.scratch + un.g * p.C + col) >> p.amax_shift : 0u;
+          for (int h = 0; h < 2; ++h) {
+            const int64_t col = un.c0 + lane + 32 * h;
+            cp_async4(&S.am[kk & 3][lane + 32 * h], p.scratch + un.g * p.C + (col < p.C ? col : 0), col < p.C);
+          }
+        }
+        cp_async_commit();
       }
     };
-    ColUnit u;
-    if (cnt > 0) {
-      u = col_unit(p, unit_at(0), upre, ppre);
-      if (CAST) fetch_amax(u);
-    }
+    decode(0, u0);
+    decode(1, u1);
+    decode(2, u2);
     for (; k < cnt; ++k) {
       const bool got = lane == 0 ? mbar_wait(&S.empty[s], ph ^ 1, cta_abort, p.wait_ns) : true;
       if (!__shfl_sync(0xffffffffu, got, 0)) {
@@ -536,6 +555,7 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
         }
         break;
       }
+      const ColUnit& u = u0;
       if (lane == 0) {
         int64_t valid = u.n - u.rt, wr = u.write_end - u.rt;
         valid = valid < 0 ? 0 : (valid < kColTile ? valid : kColTile);
@@ -545,42 +565,43 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
         mbar_arrive_expect_tx(&S.full[s], kColStageBytes);
         tma_load_2d(ring + s * kColStageBytes, &tm_in, &S.full[s], (int32_t)u.c0, (int32_t)(u.g0 + u.rt));
       }
-      const ColUnit un = k + 1 < cnt ? col_unit(p, unit_at(k + 1), upre, ppre) : u;
       if (CAST) {
-        // this unit's scales from the words fetched one unit earlier, then the next unit's words
+        // this unit's scales from the words copied three units earlier (its group and the ones
+        // before it are complete once at most the two newer groups are pending)
+        cp_async_wait<2>();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const Scale sv = tab_scale(stab, am[h]);
+          const Scale sv = tab_scale(stab, S.am[k & 3][lane + 32 * h] >> p.amax_shift);
           S.sc[s][lane + 32 * h] = sv.s32;
           const int64_t col = u.c0 + lane + 32 * h;
           if (u.rt == 0 && col < p.C) p.inv[u.g * p.C + col] = sv.inv32;  // the strip's first tile
         }
-        if (k + 1 < cnt) fetch_amax(un);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.scl[s]);
       }
-      u = un;
+      u0 = u1;
+      u1 = u2;
+      decode(k + 3, u2);
       if (++s == kColStages) {
         s = 0;
         ph ^= 1;
       }
     }
     // the loads in flight land before the CTA may leave (all consumed unless aborted)
+    if (CAST) cp_async_wait<0>();
     if (lane == 0) {
       const int64_t first = k > kColStages ? k - kColStages : 0;
       for (int64_t j = first; j < k; ++j)
         mbar_wait(&S.full[j % kColStages], (uint32_t)((j / kColStages) & 1), nullptr, kColDrainNs);
     }
-  } else {
-    // ============ consumers: thread = 4 rows x 8 columns of each 128-row block ============
+  } else if (!CAST) {
+    // ============ pass 1 consumers: thread = 4 rows x 8 columns of each 128-row block ============
     const int ct = tid - 32, cw = ct >> 5;
     const int ch = lane & 7, rq = lane >> 3;
     int s = 0;
     uint32_t ph = 0;
-    int ncast = 0;
     for (int64_t k = 0; k < cnt; ++k) {
-      bool got = mbar_wait(&S.full[s], ph, cta_abort, p.wait_ns);
-      if (CAST && got) got = mbar_wait(&S.scl[s], ph, cta_abort, p.wait_ns);
+      const bool got = mbar_wait(&S.full[s], ph, cta_abort, p.wait_ns);
       if (!named_bar_and(2, kColThreads, got)) {  // uniform decision across the consumer warps
         if (!got && !*cta_abort) {
           *cta_abort = 1;
@@ -589,13 +610,6 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
         break;
       }
       const ColInfo info = S.info[s];
-      float sc[8];
-      if (CAST) {
-        const float4 a = *reinterpret_cast<const float4*>(&S.sc[s][ch * 8]);
-        const float4 b = *reinterpret_cast<const float4*>(&S.sc[s][ch * 8 + 4]);
-        sc[0] = a.x; sc[1] = a.y; sc[2] = a.z; sc[3] = a.w;
-        sc[4] = b.x; sc[5] = b.y; sc[6] = b.z; sc[7] = b.w;
-      }
       const uint8_t* st = ring + s * kColStageBytes;
       uint4 v[kColNB][4];
       if (info.valid == kColTile) {
@@ -622,87 +636,114 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
         s = 0;
         ph ^= 1;
       }
-      if (!CAST) {
-        uint32_t m4[4] = {0, 0, 0, 0};
+      uint32_t m4[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int b = 0; b < kColNB; ++b)
+      for (int b = 0; b < kColNB; ++b)
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            m4[0] = absmax2(m4[0], v[b][jj].x);
-            m4[1] = absmax2(m4[1], v[b][jj].y);
-            m4[2] = absmax2(m4[2], v[b][jj].z);
-            m4[3] = absmax2(m4[3], v[b][jj].w);
-          }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          m4[q] = __vmaxu2(m4[q], __shfl_xor_sync(0xffffffffu, m4[q], 8));
-          m4[q] = __vmaxu2(m4[q], __shfl_xor_sync(0xffffffffu, m4[q], 16));
+        for (int jj = 0; jj < 4; ++jj) {
+          m4[0] = absmax2(m4[0], v[b][jj].x);
+          m4[1] = absmax2(m4[1], v[b][jj].y);
+          m4[2] = absmax2(m4[2], v[b][jj].z);
+          m4[3] = absmax2(m4[3], v[b][jj].w);
         }
-        if (rq == 0) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) S.red[cw][ch][q] = m4[q];
-        }
-        named_bar_sync(1, kColThreads);
-        if (ct < 32) {  // pair t = columns 2t, 2t+1 = chunk t/4, word t%4
-          uint32_t m = 0;
+      for (int q = 0; q < 4; ++q) {
+        m4[q] = __vmaxu2(m4[q], __shfl_xor_sync(0xffffffffu, m4[q], 8));
+        m4[q] = __vmaxu2(m4[q], __shfl_xor_sync(0xffffffffu, m4[q], 16));
+      }
+      if (rq == 0) {
 #pragma unroll
-          for (int w = 0; w < kColConsumerWarps; ++w) m = __vmaxu2(m, S.red[w][ct >> 2][ct & 3]);
-          const int64_t col = info.c0 + 2 * ct;
-          uint32_t* scw = p.scratch + (int64_t)info.g * p.C + col;
-          if (col < p.C && (m & 0xFFFFu)) red_max_relaxed(scw, m & 0xFFFFu);
-          if (col + 1 < p.C && (m >> 16)) red_max_relaxed(scw + 1, m >> 16);
+        for (int q = 0; q < 4; ++q) S.red[cw][ch][q] = m4[q];
+      }
+      named_bar_sync(1, kColThreads);
+      if (ct < 32) {  // pair t = columns 2t, 2t+1 = chunk t/4, word t%4
+        uint32_t m = 0;
+#pragma unroll
+        for (int w = 0; w < kColConsumerWarps; ++w) m = __vmaxu2(m, S.red[w][ct >> 2][ct & 3]);
+        const int64_t col = info.c0 + 2 * ct;
+        uint32_t* scw = p.scratch + (int64_t)info.g * p.C + col;
+        if (col < p.C && (m & 0xFFFFu)) red_max_relaxed(scw, m & 0xFFFFu);
+        if (col + 1 < p.C && (m >> 16)) red_max_relaxed(scw + 1, m >> 16);
+      }
+      named_bar_sync(1, kColThreads);
+    }
+  } else {
+    // ====== pass 2 consumers: each warp casts 32 rows x 64 columns and stores them itself ======
+    // Lane l owns the column pair (2 l, 2 l + 1); a 32-bit shared load holds the pair's values of
+    // one row (the 128-byte swizzle permutes 16-byte chunks inside a row, so the 32 lanes still
+    // read one row's 128 bytes). Its 2 x 32 codes go to the warp's staging box [64 columns][32
+    // rows] and the warp's elected lane stores the box by TMA: no barrier across warps.
+    const int cw = warp - 1;
+    const int r0 = 32 * cw;  // the warp's rows within the unit
+    const uint32_t woff = ((uint32_t)(lane & 3) << 2);
+    uint8_t* wbuf = Tout + cw * 2 * kColWarpBox;
+    int s = 0, nb = 0;
+    uint32_t ph = 0;
+    for (int64_t k = 0; k < cnt; ++k) {
+      bool got = mbar_wait(&S.full[s], ph, cta_abort, p.wait_ns);
+      if (got) got = mbar_wait(&S.scl[s], ph, cta_abort, p.wait_ns);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0 && !*cta_abort) {
+          *cta_abort = 1;
+          set_status(p.status, FP8_DEV_TIMEOUT);
         }
-        named_bar_sync(1, kColThreads);
+        break;
+      }
+      const ColInfo info = S.info[s];
+      const float2 sc = *reinterpret_cast<const float2*>(&S.sc[s][2 * lane]);
+      const uint8_t* st = ring + s * kColStageBytes + r0 * 128 + woff;
+      uint32_t w[32];
+      if (info.valid >= r0 + 32) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          w[r] = *reinterpret_cast<const uint32_t*>(st + r * 128 + ((((uint32_t)lane >> 2) ^ (uint32_t)(r & 7)) << 4));
       } else {
-        uint8_t* T = Tout + (ncast & 1) * kColOutBytes;
-        ++ncast;
-        if (ct == 0) bulk_wait_read_1();  // the store that last read this tile has done so
-        named_bar_sync(1, kColThreads);
-        const int nbox = (info.wrows + 127) / 128;
 #pragma unroll
-        for (int b = 0; b < kColNB; ++b) {
-          if (b < nbox) {
-            uint32_t o[8];
+        for (int r = 0; r < 32; ++r)  // rows past the group read as zeros
+          w[r] = r0 + r < info.valid
+                     ? *reinterpret_cast<const uint32_t*>(st + r * 128 + ((((uint32_t)lane >> 2) ^ (uint32_t)(r & 7)) << 4))
+                     : 0u;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[s]);  // this warp is done with the stage
+      if (++s == kColStages) {
+        s = 0;
+        ph ^= 1;
+      }
+      if (r0 >= info.wrows) continue;  // nothing of this warp's rows is written
+      uint32_t olo[8], ohi[8];
+      const float2 slo = make_float2(sc.x, sc.x), shi = make_float2(sc.y, sc.y);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float2 s2 = make_float2(sc[j], sc[j]);
-              const float2 x01 = fmul2_rn(make_float2(col_of(v[b][0], j), col_of(v[b][1], j)), s2);
-              const float2 x23 = fmul2_rn(make_float2(col_of(v[b][2], j), col_of(v[b][3], j)), s2);
-              o[j] = cvt_fp8x2<FMT>(x01.x, x01.y) | (cvt_fp8x2<FMT>(x23.x, x23.y) << 16);
-            }
-            // rotate by ch so that the lanes of a warp write 8 different column residues at once
-#pragma unroll
-            for (int sh = 1; sh < 8; sh <<= 1) {
-              const bool rot = (ch & sh) != 0;
-              uint32_t t[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) t[j] = rot ? o[(j + sh) & 7] : o[j];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) o[j] = t[j];
-            }
-            uint8_t* box = T + b * 8192;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int cl = ch * 8 + ((j + ch) & 7);
-              *reinterpret_cast<uint32_t*>(box + cl * 128 + (((cw ^ cl) & 7) << 4) + rq * 4) = o[j];
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, kColThreads);
-        if (ct == 0) {
-          for (int b = 0; b < nbox; ++b) {
-            const int32_t xo = info.pstart + info.rt + 128 * b;
-            if (p.mode == 1)
-              tma_store_3d(&tm_out, T + b * 8192, xo, info.c0, info.g);
-            else
-              tma_store_2d(&tm_out, T + b * 8192, xo, info.c0);
-          }
-          bulk_commit();
-        }
+      for (int r = 0; r < 32; r += 4) {
+        // column 2 l: the low halves of rows r .. r + 3; column 2 l + 1: the high halves
+        const float2 l01 = fmul2_rn(make_float2(__uint_as_float(w[r] << 16), __uint_as_float(w[r + 1] << 16)), slo);
+        const float2 l23 = fmul2_rn(make_float2(__uint_as_float(w[r + 2] << 16), __uint_as_float(w[r + 3] << 16)), slo);
+        const float2 h01 = fmul2_rn(make_float2(__uint_as_float(w[r] & 0xFFFF0000u), __uint_as_float(w[r + 1] & 0xFFFF0000u)), shi);
+        const float2 h23 = fmul2_rn(make_float2(__uint_as_float(w[r + 2] & 0xFFFF0000u), __uint_as_float(w[r + 3] & 0xFFFF0000u)), shi);
+        olo[r / 4] = cvt_fp8x2<FMT>(l01.x, l01.y) | (cvt_fp8x2<FMT>(l23.x, l23.y) << 16);
+        ohi[r / 4] = cvt_fp8x2<FMT>(h01.x, h01.y) | (cvt_fp8x2<FMT>(h23.x, h23.y) << 16);
+      }
+      uint8_t* box = wbuf + nb * kColWarpBox;
+      nb ^= 1;
+      if (lane == 0) bulk_wait_read_1();  // the store that last read this box has done so
+      __syncwarp();
+      uint8_t* dst = box + lane * 64;  // rows 2 l and 2 l + 1 of the box: 32 codes each
+      *reinterpret_cast<uint4*>(dst) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+      *reinterpret_cast<uint4*>(dst + 16) = make_uint4(olo[4], olo[5], olo[6], olo[7]);
+      *reinterpret_cast<uint4*>(dst + 32) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+      *reinterpret_cast<uint4*>(dst + 48) = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int32_t xo = info.pstart + info.rt + r0;
+        if (p.mode == 1)
+          tma_store_3d(&tm_out, box, xo, info.c0, info.g);
+        else
+          tma_store_2d(&tm_out, box, xo, info.c0);
+        bulk_commit();
       }
     }
-    if (CAST && ct == 0) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   }
   __syncthreads();
 }
@@ -714,7 +755,7 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
                       const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, uint32_t* scratch,
                       const Ctx& c, const uint32_t* amax_given) {
   if (n_groups == 0 || C == 0) return FP8_OK;
-  if (ends && n_groups > 6000) return FP8_ERR_UNSUPPORTED;  // prefix arrays live in shared memory
+  if (ends && n_groups > 2048) return FP8_ERR_UNSUPPORTED;  // prefix arrays live in shared memory
   ColParams p = {};
   p.x = static_cast<const uint16_t*>(x);
   p.rows_total = rows_total;
@@ -734,14 +775,14 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   if (p.mode == 1) {
     const uint64_t dims[3] = {(uint64_t)group_rows, (uint64_t)C, (uint64_t)n_groups};
     const uint64_t strides[2] = {(uint64_t)group_rows, (uint64_t)(C * group_rows)};
-    const uint32_t box[3] = {128, 64, 1};
-    rc = make_tmap(&tout, out_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint32_t box[3] = {32, 64, 1};  // one warp's box: 32 rows (bytes) x 64 columns
+    rc = make_tmap(&tout, out_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     const uint64_t inner = p.mode == 2 ? (uint64_t)ld_out : (uint64_t)group_rows;
     const uint64_t dims[2] = {inner, (uint64_t)C};
     const uint64_t strides[1] = {(uint64_t)ld_out};
-    const uint32_t box[2] = {128, 64};
-    rc = make_tmap(&tout, out_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint32_t box[2] = {32, 64};  // one warp's box: 32 rows (bytes) x 64 columns
+    rc = make_tmap(&tout, out_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (rc != FP8_OK) return rc;
   {
@@ -762,7 +803,8 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   // partial tile) -- the kernels compute the exact count from the offsets
   const int64_t units = p.mode == 2 ? (ceil_div64(rows_total, kColTile) + n_groups) * p.n_strips
                                     : n_groups * ceil_div64(group_rows, kColTile) * p.n_strips;
-  const size_t pre = p.mode == 2 ? 8 * (size_t)(n_groups + 1) : 0;
+  if (units > INT32_MAX) return FP8_ERR_UNSUPPORTED;  // the kernels decode units in 32 bits
+  const size_t pre = p.mode == 2 ? 12 * (size_t)(n_groups + 1) : 0;
   const int64_t grid = units > 0 ? (units < c.sm_count ? units : c.sm_count) : 1;
   const ScaleTab& tab = scale_tab(fmt);
   // pass 1: column maxima (skipped when the caller supplies them)
