@@ -303,23 +303,24 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 // ==========================================================================================
 // Columnwise with column-major output: two streaming passes of one warp-specialized kernel
 // (one CTA per SM) over work units, a unit being a 256-row x 64-column tile of one row group
-// (segment); units never straddle a group boundary and are ordered group, row tile, strip, so a
-// CTA's contiguous range of units reads long row segments (several KB per row) and neighbouring
-// strips share DRAM pages and L2 lines. Every CTA takes one contiguous range of units:
-//   producer warp: streams the range's tiles into a shared-memory ring with TMA (128-byte
+// (segment); units never straddle a group boundary and are ordered group, row tile, strip, and
+// dealt to the CTAs round-robin, so that at any time the CTAs read neighbouring strips of the
+// same rows (long row segments: DRAM pages and L2 lines are shared). In every CTA:
+//   producer warp: streams its units' tiles into a shared-memory ring with TMA (128-byte
 //              swizzle), 6 stages in pass 1 and 5 in pass 2: 160-192 KB of loads in flight per SM;
 //   8 consumer warps read each tile from the ring (conflict-free through the swizzle).
 //   pass 1 (max): a tile's per-column |x| maxima are folded by shuffles and shared memory into
 //              one relaxed atomic max per column on a per-(group, column) scratch word (the bf16
 //              bit pattern of the maximum).
-//   pass 2 (cast): the producer turns the scratch words into the tile's 64 scales (words
-//              fetched three tiles ahead; the strip's first tile also writes the inverse scales).
+//   pass 2 (cast): the producer turns the scratch words into the tile's 64 scales (the words
+//              copied asynchronously into shared memory three tiles ahead; the strip's first
+//              tile also writes the inverse scales).
 //              Each consumer warp then owns 32 rows of the tile: a lane takes a column pair,
 //              multiplies in fp32 and casts in registers, writes its two 32-code rows of the
 //              transposed box (64 columns x 32 rows) in the warp's own staging buffer, and the
 //              warp's elected lane stores the box by TMA (two alternating buffers per warp), so
-//              the warps never wait on one another. Pass 2 walks each range backwards, so its
-//              first reads are the tiles pass 1 read last, still in L2.
+//              the warps never wait on one another. Pass 2 walks the unit order backwards, so
+//              its first reads are the tiles pass 1 read last, still in L2.
 // The passes are stream-ordered launches: no CTA waits on another.
 constexpr int kColThreads = 256;
 constexpr int kColNB = 2;                  // 128-row blocks per work unit (256 rows)
@@ -515,10 +516,14 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
     }
   }
   __syncthreads();
-  // this CTA's contiguous range of units; pass 2 walks it backwards
-  const int64_t lo = M * blockIdx.x / gridDim.x, hi = M * (blockIdx.x + 1) / gridDim.x;
-  const int64_t cnt = hi - lo;
-  auto unit_at = [&](int64_t k) { return CAST ? hi - 1 - k : lo + k; };
+  // units are dealt round-robin, so the CTAs read neighbouring strips of the same rows at the same
+  // time (DRAM pages stay open); pass 2 walks the order backwards, its first reads being the
+  // units pass 1 read last, still in L2
+  const int64_t cnt = (int64_t)blockIdx.x < M ? (M - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto unit_at = [&](int64_t k) {
+    const int64_t i = blockIdx.x + k * gridDim.x;
+    return CAST ? M - 1 - i : i;
+  };
   volatile int* cta_abort = &S.abort;
 
   if (warp == 0) {
