@@ -7,11 +7,14 @@ quantize x, quantize W, FP8 forward GEMM, quantize dY, quantize W column-wise (c
 output), FP8 grad-input GEMM, bf16 weight-gradient GEMM: 7 kernels, 2.886 TFLOP.
 
 Other workloads (`--workload`): linear-tensorwise-256x512, colwise-8192x14336, dsv3-moe-fwd,
-llama4-moe-fwdbwd.
+llama4-moe-fwdbwd, llama3-8b-dx-colquant-fused, llama3-8b-mlp-up-blockwise, llama3-8b-mlp-up-mx,
+dsv3-moe-fwd-mx, llama4-moe-fwdbwd-mx.
 
 `value` = whole-job throughput with inputs resident in HBM (CUDA events around each step on the
 launching stream, L2 flushed between steps outside the events: a 256 MiB write, then a 256 MiB
-read of a second buffer, so the cache is cold and holds no dirty lines of the flush);
+read of a second buffer, so the cache is cold and holds no dirty lines of the flush; a GPU spin
+before the first step gives the host a head start, so that no timed kernel waits for its own
+launch);
 `e2e` = the same metric through the public entry points with host buffers (pinned host->device
 copies of the step's inputs and device->host copies of its outputs inside the timed region).
 `--impl reference` times the CPU oracle (the plain C restatement used by the tests) on a bounded
@@ -24,6 +27,7 @@ the max over ranks, and `value` counts the work of all ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -802,9 +806,11 @@ def make_step(fp8, name):
 
 
 # ------------------------------------------------------------------------------------------
-# clocks: nvidia-smi sampled during the timed region
+# clocks: nvidia-smi sampled every 50 ms from before the warm-up on (its start-up stays out of the
+# timed region); the samples whose timestamps fall in the timed region are kept, or, when the
+# region is shorter than the sampling interval, the samples nearest to it on either side
 
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -815,12 +821,13 @@ class ClockSampler:
         self.gpu = gpu_index
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0, t1):
+        """Clock summary of the samples taken between t0 and t1 (time.time() seconds)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
@@ -829,22 +836,33 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if not inside:  # a region shorter than the interval: the nearest sample on either side
+            before = [r for r in rows if r[0] < t0]
+            after = [r for r in rows if r[0] > t1]
+            inside = before[-1:] + after[:1]
+            window = "nearest samples (timed region shorter than the 50 ms interval)"
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for n, v in zip(names, r[3]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [r[1] for r in inside]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
 
 
 # ------------------------------------------------------------------------------------------
@@ -965,15 +983,19 @@ def main():
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
     nk = len(step.kernels)
 
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     barrier(ws)
     torch.cuda.synchronize()
+    t_start = time.time()
     wall0 = time.perf_counter()
+    # a head start for the host (outside the events): the GPU spins ~1 ms per step while the
+    # host queues the steps, so that no timed kernel waits for its own launch
+    torch.cuda._sleep(2_000_000 * min(args.steps, 40))
     for i in range(args.steps):
         # evict L2 (outside the events): the write evicts the step's data, the read of another
         # buffer then evicts the write's dirty lines, so the first timed kernel does not pay
@@ -986,7 +1008,7 @@ def main():
     torch.cuda.synchronize()
     barrier(ws)
     wall = time.perf_counter() - wall0
-    clocks = sampler.stop() if sampler else None
+    clocks = sampler.stop(t_start, time.time()) if sampler else None
 
     per_kernel = np.zeros(nk)
     step_ms = []
@@ -1031,6 +1053,7 @@ def main():
         torch.cuda.synchronize()
         na = len(step.alt_kernels)
         aevs = [[torch.cuda.Event(enable_timing=True) for _ in range(na + 1)] for _ in range(args.steps)]
+        torch.cuda._sleep(2_000_000 * min(args.steps, 40))  # host head start, as for the step
         for i in range(args.steps):
             flush.zero_()
             torch.amax(flush_rd)
