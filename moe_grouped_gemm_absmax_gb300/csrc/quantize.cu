@@ -312,9 +312,10 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 //   pass 1 (max): a tile's per-column |x| maxima are folded by shuffles and shared memory into
 //              one relaxed atomic max per column on a per-(group, column) scratch word (the bf16
 //              bit pattern of the maximum).
-//   pass 2 (cast): the producer turns the scratch words into the tile's 64 scales (the words
-//              copied asynchronously into shared memory three tiles ahead; the strip's first
-//              tile also writes the inverse scales).
+//   pass 2 (cast): a scale warp beside the producer turns the scratch words into each tile's 64
+//              scales (the words copied asynchronously into shared memory three tiles ahead; the
+//              strip's first tile also writes the inverse scales), so the producer only issues
+//              loads: one warp doing both ran at ~1 us per tile, twice the time of the loads.
 //              Each consumer warp then owns 32 rows of the tile: a lane takes a column pair,
 //              multiplies in fp32 and casts in registers, writes its two 32-code rows of the
 //              transposed box (64 columns x 32 rows) in the warp's own staging buffer, and the
@@ -474,7 +475,7 @@ struct ColSmem {
 };
 
 template <int FMT, bool CAST>
-__global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __grid_constant__ CUtensorMap tm_in,
+__global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __grid_constant__ CUtensorMap tm_in,
                                                                         const __grid_constant__ CUtensorMap tm_out,
                                                                         const ColParams p,
                                                                         const __grid_constant__ ScaleTab tab) {
@@ -527,41 +528,22 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
   volatile int* cta_abort = &S.abort;
 
   if (warp == 0) {
-    // ============ producer warp: tiles by TMA; in pass 2 also each tile's 64 scales ============
-    int s = 0;
-    uint32_t ph = 0;
-    int64_t k = 0;
-    // units k, k + 1, k + 2 are decoded ahead; in pass 2 the amax words of unit k + 3's columns
-    // lane and lane + 32 are copied asynchronously into slot (k + 3) % 4 of a shared-memory ring
-    // (one commit group per unit, possibly empty), so their latency stays off this warp's path
-    ColUnit u0 = {}, u1 = {}, u2 = {};
-    auto decode = [&](int64_t kk, ColUnit& un) {
-      if (kk < cnt) un = col_unit(p, unit_at(kk), upre, ppre);
-      if (CAST) {
-        if (kk < cnt) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t col = un.c0 + lane + 32 * h;
-            cp_async4(&S.am[kk & 3][lane + 32 * h], p.scratch + un.g * p.C + (col < p.C ? col : 0), col < p.C);
+    // ==================== producer warp: one lane issues the tiles by TMA ====================
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int64_t k = 0;
+      ColUnit un = {};
+      if (cnt > 0) un = col_unit(p, unit_at(0), upre, ppre);
+      for (; k < cnt; ++k) {
+        if (!mbar_wait(&S.empty[s], ph ^ 1, cta_abort, p.wait_ns)) {
+          if (!*cta_abort) {
+            *cta_abort = 1;
+            set_status(p.status, FP8_DEV_TIMEOUT);
           }
+          break;
         }
-        cp_async_commit();
-      }
-    };
-    decode(0, u0);
-    decode(1, u1);
-    decode(2, u2);
-    for (; k < cnt; ++k) {
-      const bool got = lane == 0 ? mbar_wait(&S.empty[s], ph ^ 1, cta_abort, p.wait_ns) : true;
-      if (!__shfl_sync(0xffffffffu, got, 0)) {
-        if (lane == 0 && !*cta_abort) {
-          *cta_abort = 1;
-          set_status(p.status, FP8_DEV_TIMEOUT);
-        }
-        break;
-      }
-      const ColUnit& u = u0;
-      if (lane == 0) {
+        const ColUnit u = un;
         int64_t valid = u.n - u.rt, wr = u.write_end - u.rt;
         valid = valid < 0 ? 0 : (valid < kColTile ? valid : kColTile);
         wr = wr < 0 ? 0 : (wr < kColTile ? wr : kColTile);
@@ -569,35 +551,71 @@ __global__ void __launch_bounds__(kColThreads + 32, 1) colstream_kernel(const __
                             (int32_t)u.pstart};
         mbar_arrive_expect_tx(&S.full[s], kColStageBytes);
         tma_load_2d(ring + s * kColStageBytes, &tm_in, &S.full[s], (int32_t)u.c0, (int32_t)(u.g0 + u.rt));
+        if (k + 1 < cnt) un = col_unit(p, unit_at(k + 1), upre, ppre);
+        if (++s == kColStages) {
+          s = 0;
+          ph ^= 1;
+        }
       }
-      if (CAST) {
-        // this unit's scales from the words copied three units earlier (its group and the ones
-        // before it are complete once at most the two newer groups are pending)
+      // the loads in flight land before the CTA may leave (all consumed unless aborted)
+      const int64_t first = k > kColStages ? k - kColStages : 0;
+      for (int64_t j = first; j < k; ++j)
+        mbar_wait(&S.full[j % kColStages], (uint32_t)((j / kColStages) & 1), nullptr, kColDrainNs);
+    }
+  } else if (warp == kColConsumerWarps + 1) {
+    // ============ pass 2 scale warp: each tile's 64 scales, beside the TMA producer ============
+    // Units k, k + 1, k + 2 are decoded ahead; the amax words of unit k + 3's columns lane and
+    // lane + 32 are copied asynchronously into slot (k + 3) % 4 of a shared-memory ring (one commit
+    // group per unit, possibly empty), so their latency stays off this warp's path. A stage's
+    // scales are rewritten only after its consumers released it (the stage's empty barrier).
+    if (CAST) {
+      int s = 0;
+      uint32_t ph = 0;
+      ColUnit u0 = {}, u1 = {}, u2 = {};
+      auto decode = [&](int64_t kk, ColUnit& un) {
+        if (kk < cnt) {
+          un = col_unit(p, unit_at(kk), upre, ppre);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int64_t col = un.c0 + lane + 32 * h;
+            cp_async4(&S.am[kk & 3][lane + 32 * h], p.scratch + un.g * p.C + (col < p.C ? col : 0), col < p.C);
+          }
+        }
+        cp_async_commit();
+      };
+      decode(0, u0);
+      decode(1, u1);
+      decode(2, u2);
+      for (int64_t k = 0; k < cnt; ++k) {
+        const bool got = lane == 0 ? mbar_wait(&S.empty[s], ph ^ 1, cta_abort, p.wait_ns) : true;
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
+          if (lane == 0 && !*cta_abort) {
+            *cta_abort = 1;
+            set_status(p.status, FP8_DEV_TIMEOUT);
+          }
+          break;
+        }
+        // this unit's words were copied three units earlier: its group and the ones before it
+        // are complete once at most the two newer groups are pending
         cp_async_wait<2>();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const Scale sv = tab_scale(stab, S.am[k & 3][lane + 32 * h] >> p.amax_shift);
           S.sc[s][lane + 32 * h] = sv.s32;
-          const int64_t col = u.c0 + lane + 32 * h;
-          if (u.rt == 0 && col < p.C) p.inv[u.g * p.C + col] = sv.inv32;  // the strip's first tile
+          const int64_t col = u0.c0 + lane + 32 * h;
+          if (u0.rt == 0 && col < p.C) p.inv[u0.g * p.C + col] = sv.inv32;  // the strip's first tile
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.scl[s]);
+        u0 = u1;
+        u1 = u2;
+        decode(k + 3, u2);
+        if (++s == kColStages) {
+          s = 0;
+          ph ^= 1;
+        }
       }
-      u0 = u1;
-      u1 = u2;
-      decode(k + 3, u2);
-      if (++s == kColStages) {
-        s = 0;
-        ph ^= 1;
-      }
-    }
-    // the loads in flight land before the CTA may leave (all consumed unless aborted)
-    if (CAST) cp_async_wait<0>();
-    if (lane == 0) {
-      const int64_t first = k > kColStages ? k - kColStages : 0;
-      for (int64_t j = first; j < k; ++j)
-        mbar_wait(&S.full[j % kColStages], (uint32_t)((j / kColStages) & 1), nullptr, kColDrainNs);
+      cp_async_wait<0>();  // no copy lands after the CTA has left
     }
   } else if (!CAST) {
     // ============ pass 1 consumers: thread = 4 rows x 8 columns of each 128-row block ============
@@ -818,7 +836,7 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
     const size_t smem = ColSmem<false>::bytes + pre;
     if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return FP8_ERR_CUDA;
-    k1<<<(unsigned)grid, kColThreads + 32, smem, c.stream>>>(tin, tout, p, tab);
+    k1<<<(unsigned)grid, kColThreads + 64, smem, c.stream>>>(tin, tout, p, tab);
     if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
   }
   // pass 2: scales and cast (also writes the scales of groups without rows)
@@ -826,7 +844,7 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   const size_t smem2 = ColSmem<true>::bytes + pre;
   if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
     return FP8_ERR_CUDA;
-  k2<<<(unsigned)grid, kColThreads + 32, smem2, c.stream>>>(tin, tout, p, tab);
+  k2<<<(unsigned)grid, kColThreads + 64, smem2, c.stream>>>(tin, tout, p, tab);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
