@@ -247,6 +247,11 @@ FP8_DEVI void cp_async4(void* smem_dst, const void* gsrc, bool valid) {
                : "memory");
 }
 FP8_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// The mbarrier receives one arrival from this thread once all of its earlier cp.async copies have
+// landed (the barrier's expected count includes that arrival).
+FP8_DEVI void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 template <int N>
 FP8_DEVI void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 

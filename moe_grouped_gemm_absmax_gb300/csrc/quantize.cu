@@ -312,15 +312,16 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 //   pass 1 (max): a tile's per-column |x| maxima are folded by shuffles and shared memory into
 //              one relaxed atomic max per column on a per-(group, column) scratch word (the bf16
 //              bit pattern of the maximum).
-//   pass 2 (cast): a scale warp beside the producer turns the scratch words into each tile's 64
-//              scales (the words copied asynchronously into shared memory three tiles ahead; the
-//              strip's first tile also writes the inverse scales), so the producer only issues
-//              loads: one warp doing both ran at ~1 us per tile, twice the time of the loads.
-//              Each consumer warp then owns 32 rows of the tile: a lane takes a column pair,
-//              multiplies in fp32 and casts in registers, writes its two 32-code rows of the
-//              transposed box (64 columns x 32 rows) in the warp's own staging buffer, and the
-//              warp's elected lane stores the box by TMA (two alternating buffers per warp), so
-//              the warps never wait on one another. Pass 2 walks the unit order backwards, so
+//   pass 2 (cast): an amax warp beside the producer copies each tile's 64 column maxima from the
+//              scratch words into the stage asynchronously (the copies themselves arrive on the
+//              stage's barrier); one warp doing the scale step for the consumers ran at ~1 us per
+//              tile, twice the time of the loads.
+//              Each consumer warp then owns 32 rows of the tile: a lane takes a column pair, takes
+//              their scales from the table in shared memory (the strip's first tile also writes
+//              the inverse scales), multiplies in fp32 and casts in registers, writes its two
+//              32-code rows of the transposed box (64 columns x 32 rows) in the warp's own
+//              staging buffer, and the warp's elected lane stores the box by TMA (two alternating
+//              buffers per warp), so the warps never wait on one another. Pass 2 walks the unit order backwards, so
 //              its first reads are the tiles pass 1 read last, still in L2.
 // The passes are stream-ordered launches: no CTA waits on another.
 constexpr int kColThreads = 256;
@@ -460,11 +461,10 @@ struct ColInfo {
 };
 struct ColShared {
   uint64_t full[kColStagesMax];   // the tile landed (TMA bytes) and the info was written
-  uint64_t scl[kColStagesMax];    // pass 2: the stage's 64 scales were written
+  uint64_t scl[kColStagesMax];    // pass 2: the stage's 64 amax words landed (32 async arrivals)
   uint64_t empty[kColStagesMax];  // the consumer warps are done with the stage
   ColInfo info[kColStagesMax];
-  float sc[kColStagesMax][64];    // pass 2: the fp32 scales of the stage's 64 columns
-  uint32_t am[4][64];             // pass 2: amax words of units k .. k + 3 (asynchronous copies)
+  uint32_t am[kColStagesMax][64];  // pass 2: the amax words of the stage's 64 columns
   uint32_t red[kColConsumerWarps][8][4];
   int abort;
 };
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
   if (tid == 0) {
     for (int s = 0; s < kColStages; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.scl[s], 1);
+      mbar_init(&S.scl[s], 32);
       mbar_init(&S.empty[s], kColConsumerWarps);
     }
     S.abort = 0;
@@ -563,29 +563,15 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
         mbar_wait(&S.full[j % kColStages], (uint32_t)((j / kColStages) & 1), nullptr, kColDrainNs);
     }
   } else if (warp == kColConsumerWarps + 1) {
-    // ============ pass 2 scale warp: each tile's 64 scales, beside the TMA producer ============
-    // Units k, k + 1, k + 2 are decoded ahead; the amax words of unit k + 3's columns lane and
-    // lane + 32 are copied asynchronously into slot (k + 3) % 4 of a shared-memory ring (one commit
-    // group per unit, possibly empty), so their latency stays off this warp's path. A stage's
-    // scales are rewritten only after its consumers released it (the stage's empty barrier).
+    // ======== pass 2 amax warp: each tile's 64 column maxima, beside the TMA producer ========
+    // Once a stage is free, the words of its unit's columns lane and lane + 32 are copied
+    // asynchronously into the stage's slot, and each lane's copies complete an arrival on the
+    // stage's scl barrier when they land: nothing on this warp's path waits for memory.
     if (CAST) {
       int s = 0;
       uint32_t ph = 0;
-      ColUnit u0 = {}, u1 = {}, u2 = {};
-      auto decode = [&](int64_t kk, ColUnit& un) {
-        if (kk < cnt) {
-          un = col_unit(p, unit_at(kk), upre, ppre);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t col = un.c0 + lane + 32 * h;
-            cp_async4(&S.am[kk & 3][lane + 32 * h], p.scratch + un.g * p.C + (col < p.C ? col : 0), col < p.C);
-          }
-        }
-        cp_async_commit();
-      };
-      decode(0, u0);
-      decode(1, u1);
-      decode(2, u2);
+      ColUnit un = {};
+      if (cnt > 0) un = col_unit(p, unit_at(0), upre, ppre);
       for (int64_t k = 0; k < cnt; ++k) {
         const bool got = lane == 0 ? mbar_wait(&S.empty[s], ph ^ 1, cta_abort, p.wait_ns) : true;
         if (!__shfl_sync(0xffffffffu, got, 0)) {
@@ -595,21 +581,13 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
           }
           break;
         }
-        // this unit's words were copied three units earlier: its group and the ones before it
-        // are complete once at most the two newer groups are pending
-        cp_async_wait<2>();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const Scale sv = tab_scale(stab, S.am[k & 3][lane + 32 * h] >> p.amax_shift);
-          S.sc[s][lane + 32 * h] = sv.s32;
-          const int64_t col = u0.c0 + lane + 32 * h;
-          if (u0.rt == 0 && col < p.C) p.inv[u0.g * p.C + col] = sv.inv32;  // the strip's first tile
+          const int64_t col = un.c0 + lane + 32 * h;
+          cp_async4(&S.am[s][lane + 32 * h], p.scratch + un.g * p.C + (col < p.C ? col : 0), col < p.C);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.scl[s]);
-        u0 = u1;
-        u1 = u2;
-        decode(k + 3, u2);
+        cp_async_arrive_noinc(&S.scl[s]);
+        if (k + 1 < cnt) un = col_unit(p, unit_at(k + 1), upre, ppre);
         if (++s == kColStages) {
           s = 0;
           ph ^= 1;
@@ -713,7 +691,16 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
         break;
       }
       const ColInfo info = S.info[s];
-      const float2 sc = *reinterpret_cast<const float2*>(&S.sc[s][2 * lane]);
+      // the scale step for the lane's two columns (the table in shared memory); the first row
+      // tile of a strip also writes their inverse scales
+      const uint2 am2 = *reinterpret_cast<const uint2*>(&S.am[s][2 * lane]);
+      const Scale sv_lo = tab_scale(stab, am2.x >> p.amax_shift), sv_hi = tab_scale(stab, am2.y >> p.amax_shift);
+      const float2 sc = make_float2(sv_lo.s32, sv_hi.s32);
+      if (info.rt == 0 && cw == 0) {
+        const int64_t col = info.c0 + 2 * lane;
+        if (col < p.C) p.inv[(int64_t)info.g * p.C + col] = sv_lo.inv32;
+        if (col + 1 < p.C) p.inv[(int64_t)info.g * p.C + col + 1] = sv_hi.inv32;
+      }
       const uint8_t* st = ring + s * kColStageBytes + r0 * 128 + woff;
       uint32_t w[32];
       if (info.valid >= r0 + 32) {
