@@ -208,6 +208,37 @@ def test_jagged_colwise_wide(fp8, counts):
     assert np.array_equal(f32_bits(inv), inv_ref.view(np.uint32))
 
 
+def test_jagged_colwise_segment_limit(fp8):
+    """The most segments a column quantize takes (2048: its per-segment prefix arrays live in
+    shared memory), most of them a few rows long or empty; one segment more is rejected."""
+    C = 16
+    for E, ok in ((2048, True), (2049, False)):
+        counts = [int(c) for c in W.random_counts(6000, E, 7, n_empty=E // 4)]
+        R = sum(counts)
+        x = W.normal_bf16((R, C), 1.0, 700 + E)
+        ends = W.ends_from_counts(counts)
+        P = fp8.fp8_jagged_padded_rows(R, E)
+        out = torch.full((C, P), 0x5A, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+        inv = torch.empty((E, C), dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        args = (x.cuda(), fp8.GRAN_COL, fp8.DT_E4M3, fp8.LAYOUT_COL_MAJOR, None, out, inv,
+                torch.from_numpy(ends).cuda(), fp8.col_workspace(E, C, "cuda"))
+        if not ok:
+            with pytest.raises(fp8.Fp8Error) as e:
+                fp8.fp8_quantize(*args, status=st)
+            assert e.value.code == 2
+            continue
+        fp8.fp8_quantize(*args, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        q_ref, inv_ref = oracle.quantize_jagged_cols(bits(x), ends, oracle.E4M3)
+        ref, used = _segpad(q_ref, ends, P)
+        got = codes(out)
+        assert np.array_equal(got[:, :used], ref[:, :used])
+        assert np.all(got[:, used:] == 0x5A)
+        assert np.array_equal(f32_bits(inv), inv_ref.view(np.uint32))
+
+
 def test_jagged_bad_offsets_sets_status(fp8):
     x = W.normal_bf16((64, 8), 1.0, 9).cuda()
     P = fp8.fp8_jagged_padded_rows(64, 3)
