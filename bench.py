@@ -12,9 +12,9 @@ dsv3-moe-fwd-mx, llama4-moe-fwdbwd-mx.
 
 `value` = whole-job throughput with inputs resident in HBM (CUDA events around each step on the
 launching stream, L2 flushed between steps outside the events: a 256 MiB write, then a 256 MiB
-read of a second buffer, so the cache is cold and holds no dirty lines of the flush; a GPU spin
-before the first step gives the host a head start, so that no timed kernel waits for its own
-launch);
+read of a second buffer, so the cache is cold and holds no dirty lines of the flush, then a ~50 us
+GPU spin while the flush's write-backs drain; a GPU spin before the first step gives the host a
+head start, so that no timed kernel waits for its own launch);
 `e2e` = the same metric through the public entry points with host buffers (pinned host->device
 copies of the step's inputs and device->host copies of its outputs inside the timed region).
 `--impl reference` times the CPU oracle (the plain C restatement used by the tests) on a bounded
@@ -1002,6 +1002,9 @@ def main():
         # for writing the flush buffer back
         flush.zero_()
         torch.amax(flush_rd)
+        # let the flush's write-backs drain (~50 us spin) so the first timed kernel does not pay
+        # for them
+        torch.cuda._sleep(100_000)
         ev = evs[i]
         step.run(lambda k: ev[k].record(stream))
         ev[nk].record(stream)
@@ -1057,6 +1060,7 @@ def main():
         for i in range(args.steps):
             flush.zero_()
             torch.amax(flush_rd)
+            torch.cuda._sleep(100_000)  # the flush's write-backs drain, as for the step
             ev = aevs[i]
             step.alt_run(lambda k: ev[k].record(stream))
             ev[na].record(stream)
