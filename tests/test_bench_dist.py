@@ -51,3 +51,55 @@ def test_whole_job_value_is_weak_scaling():
     two = bench.whole_job_value(flop, 10, 2, 12.7, "TFLOP/s")
     assert abs(one - flop * 10 / 12.7 / 1e9) < 1e-9 * one and abs(two - 2 * one) < 1e-9 * two
     assert abs(bench.whole_job_value(3e8, 4, 1, 2.0, "GB/s") - 3e8 * 4 / 2.0 / 1e6) < 1e-6
+
+
+class _FakeSmi:
+    """Stands in for the nvidia-smi sampling process: fixed CSV output, no GPU."""
+
+    def __init__(self, out):
+        self.out = out
+
+    def terminate(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.out, ""
+
+
+def _smi_line(ts, sm, reasons=("Not Active",) * 4):
+    stamp = ts.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return f"{stamp}, 0, {sm}, 2070, 900.5, 0x0000000000000000, " + ", ".join(reasons)
+
+
+def test_clock_sampler_keeps_the_timed_window():
+    import datetime
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    lines = [_smi_line(t0, 1500),  # before the window (warm-up)
+             _smi_line(t0 + datetime.timedelta(seconds=1), 2070),
+             _smi_line(t0 + datetime.timedelta(seconds=1.05), 2055, ("Not Active", "Not Active", "Not Active", "Active")),
+             _smi_line(t0 + datetime.timedelta(seconds=2), 1200, ("Active", "Not Active", "Not Active", "Not Active"))]
+    s = object.__new__(bench.ClockSampler)
+    s.proc = _FakeSmi("\n".join(lines) + "\n")
+    w0, w1 = (t0 + datetime.timedelta(seconds=0.9)).timestamp(), (t0 + datetime.timedelta(seconds=1.1)).timestamp()
+    c = s.stop(w0, w1)
+    assert c["samples"] == 2 and c["window"] == "timed region"
+    assert c["sm_mhz"] == (2070 + 2055) / 2 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]  # the hw_slowdown sample lies outside the window
+
+
+def test_clock_sampler_nearest_samples_for_a_short_window():
+    import datetime
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    lines = [_smi_line(t0 + datetime.timedelta(seconds=x), sm) for x, sm in ((0.0, 1900), (0.05, 2000), (0.10, 2070))]
+    s = object.__new__(bench.ClockSampler)
+    s.proc = _FakeSmi("\n".join(lines) + "\n")
+    w0, w1 = (t0 + datetime.timedelta(seconds=0.06)).timestamp(), (t0 + datetime.timedelta(seconds=0.08)).timestamp()
+    c = s.stop(w0, w1)
+    assert c["samples"] == 2 and c["window"].startswith("nearest")
+    assert c["sm_mhz"] == (2000 + 2070) / 2
