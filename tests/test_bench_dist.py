@@ -3,8 +3,6 @@ replica; timing is the max over ranks and the value counts the work of all ranks
 import os
 import socket
 
-import pytest
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 

@@ -12,7 +12,6 @@ import pytest
 import torch
 
 import oracle
-import workloads as W
 from tests.gpu_util import bits, check_gemm, codes, f32_bits, mx_unblock_rows
 
 pytestmark = pytest.mark.gpu
