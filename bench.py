@@ -1,14 +1,15 @@
 """Benchmark of the FP8 dynamic-scaling linear on one or more GB300s (one process per GPU).
 
-Default workload: the Llama3-8B-shaped MLP-up Linear, forward + backward, rowwise scaling,
-M=8192 tokens, K=4096, N=14336, x with 1% outlier channels, forward and grad-input GEMMs in FP8
-(e4m3 / e5m2), the weight-gradient GEMM in bf16 (the high-precision wgrad recipe). One step =
-quantize x, quantize W, FP8 forward GEMM, quantize dY, quantize W column-wise (column-major
-output), FP8 grad-input GEMM, bf16 weight-gradient GEMM: 7 kernels, 2.886 TFLOP.
+Default workload: the DeepSeek-V3-shaped MoE layer forward (dsv3-moe-fwd): 256 experts, hidden
+K=7168, expert intermediate N=2048, 16384 tokens top-8 = 131072 routed rows with seeded Zipf(1.1)
+expert counts including 8 empty experts. One step = quantize the routed activations A
+[131072, 7168] rowwise (e4m3), quantize the expert weights W [256, 2048, 7168] per expert column
+(e4m3), and the grouped FP8 GEMM routed by the offsets (jagged M): 3 kernels, 3.85 TFLOP.
 
-Other workloads (`--workload`): linear-tensorwise-256x512, colwise-8192x14336, dsv3-moe-fwd,
-llama4-moe-fwdbwd, llama3-8b-dx-colquant-fused, llama3-8b-mlp-up-blockwise, llama3-8b-mlp-up-mx,
-dsv3-moe-fwd-mx, llama4-moe-fwdbwd-mx.
+Other workloads (`--workload`): llama3-8b-mlp-up (the Llama3-8B-shaped dense MLP-up Linear,
+forward + backward, rowwise), linear-tensorwise-256x512, colwise-8192x14336, llama4-moe-fwdbwd,
+llama3-8b-dx-colquant-fused, llama3-8b-mlp-up-blockwise, llama3-8b-mlp-up-mx, dsv3-moe-fwd-mx,
+llama4-moe-fwdbwd-mx.
 
 `value` = whole-job throughput with inputs resident in HBM (CUDA events around each step on the
 launching stream, L2 flushed between steps outside the events: a 256 MiB write, then a 256 MiB
@@ -379,6 +380,96 @@ class MoeFwdStep(Step):
         f.fp8_quantize(self.Wt, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Wq, None, self.Wi)
         mark(2)
         f.fp8_grouped_mm(self.Aq, self.Wq, self.ends, self.Ai, self.Wi, self.out, f.GROUPED_JAGGED_M)
+
+    # e2e: the layer through the public entry points (fp8_quantize, fp8_grouped_mm) with host
+    # buffers. Every step copies its inputs host -> device (A, the expert weights W and the
+    # offsets, from pinned memory) and its output device -> host; inputs and outputs are
+    # double-buffered on the device so the copies of the neighbouring steps run on the copy
+    # engines while a step computes.
+    def e2e_setup(self):
+        dev = self.A.device
+        ins = (self.A, self.Wt, self.ends)
+        self.h_in = [t.cpu().pin_memory() for t in ins]
+        self.h_out = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()]
+        self.d_in = [[torch.empty_like(t) for t in ins] for _ in range(2)]
+        self.d_out = [[torch.empty_like(self.out)] for _ in range(2)]
+        self.s_in, self.s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        return sum(t.numel() * t.element_size() for t in self.h_in), \
+            sum(t.numel() * t.element_size() for t in self.h_out)
+
+    def e2e_compute(self, d_in, d_out):
+        f = self.fp8
+        A, Wt, ends = d_in
+        f.fp8_quantize(A, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Aq, None, self.Ai)
+        f.fp8_quantize(Wt, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Wq, None, self.Wi)
+        f.fp8_grouped_mm(self.Aq, self.Wq, ends, self.Ai, self.Wi, d_out[0], f.GROUPED_JAGGED_M)
+
+    def e2e_run_steps(self, n):
+        return pipelined_e2e(self, n)
+
+
+def pipelined_e2e(step, n):
+    """n steps of step.e2e_compute, each with the host->device copy of its inputs (s_in) and the
+    device->host copy of its outputs (s_out), double-buffered; returns (start, end) CUDA events
+    spanning all of it."""
+    comp = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    in_ready, done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    start, end = ev(), ev()
+    start.record(step.s_in)
+
+    def copy_in(i):
+        s = i % 2
+        with torch.cuda.stream(step.s_in):
+            if i >= 2:
+                step.s_in.wait_event(done[s])  # the step that read these inputs has finished
+            for d, h in zip(step.d_in[s], step.h_in):
+                d.copy_(h, non_blocking=True)
+            in_ready[s].record(step.s_in)
+
+    copy_in(0)
+    for i in range(n):
+        s = i % 2
+        if i + 1 < n:
+            copy_in(i + 1)
+        comp.wait_event(in_ready[s])
+        if i >= 2:
+            comp.wait_event(out_done[s])  # these outputs have been copied out
+        step.e2e_compute(step.d_in[s], step.d_out[s])
+        done[s].record(comp)
+        with torch.cuda.stream(step.s_out):
+            step.s_out.wait_event(done[s])
+            for d, h in zip(step.d_out[s], step.h_out):
+                h.copy_(d, non_blocking=True)
+            out_done[s].record(step.s_out)
+    step.s_out.wait_stream(comp)
+    end.record(step.s_out)
+    return start, end
+
+
+def moe_fwd_cpu_sample(rows, seed=0):
+    """The oracle (as it stands) on `rows` routed rows of the dsv3-moe-fwd layer: the rows' rowwise
+    quantize, their experts' weights quantized per expert column, and the rows' grouped-GEMM
+    outputs. The sampled rows and their experts' weights are drawn on the host from the workload's
+    distributions (A N(0,1), W N(0,0.02)), seeded; counted in grouped-GEMM FLOPs."""
+    import oracle
+    d = W.WORKLOADS["dsv3-moe-fwd"].dims
+    M, K, N = d["M"], d["K"], d["N"]
+    ends = W.ends_from_counts(W.dsv3_counts(seed))
+    ridx = np.sort(np.random.default_rng(seed).choice(M, rows, replace=False))
+    rexp = np.searchsorted(ends, ridx, side="right")
+    ab = W.bf16_bits(W.normal_bf16((rows, K), 1.0, seed + 11))
+    wb = {int(e): W.bf16_bits(W.normal_bf16((N, K), 0.02, seed + 1000 + int(e))) for e in np.unique(rexp)}
+
+    def run():
+        aq, ai = oracle.quantize_rows(ab, oracle.E4M3)
+        wq = {e: oracle.quantize_rows(b, oracle.E4M3) for e, b in wb.items()}
+        for i, e in enumerate(rexp):
+            cw, iw = wq[int(e)]
+            oracle.gemm_fp8(aq[i:i + 1], oracle.E4M3, cw, oracle.E4M3, ai[i:i + 1], iw)
+    return run, 2.0 * rows * N * K, (f"{rows} of {M} routed rows (their experts: {len(wb)} of 256): the rows' "
+                                     f"quantize, their experts' weights quantized per expert column, their "
+                                     f"grouped-GEMM outputs")
 
 
 class MoeFwdBwdStep(Step):
@@ -929,16 +1020,20 @@ def cpu_cores():
 
 
 def run_reference(args, ws, rank):
-    """The oracle as it stands, on the host cores, on a bounded sample of the workload."""
+    """The oracle as it stands, on the host cores, on a bounded sample of the workload: every
+    step is the same sample."""
     if rank != 0:
         return
     import oracle
-    if args.workload != "llama3-8b-mlp-up":
-        print(json.dumps({"impl": "reference", "unavailable": "reference arm implemented for the default workload"}))
+    if args.workload == "llama3-8b-mlp-up":
+        x, w, dy = W.linear_inputs(16, 4096, 14336, seed=0, outliers=True)
+        run, flops, sample = dense_cpu_sample(x, w, dy, 8192)
+    elif args.workload == "dsv3-moe-fwd":
+        run, flops, sample = moe_fwd_cpu_sample(16)
+    else:
+        print(json.dumps({"impl": "reference", "unavailable": "reference arm implemented for the dsv3-moe-fwd and "
+                                                              "llama3-8b-mlp-up workloads"}))
         return
-    rows = 16
-    x, w, dy = W.linear_inputs(rows, 4096, 14336, seed=0, outliers=True)
-    run, flops, sample = dense_cpu_sample(x, w, dy, 8192)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -950,7 +1045,7 @@ def run_reference(args, ws, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "llama3-8b-mlp-up", "sample": sample},
+            "config": {"workload": args.workload, "sample": sample},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -962,10 +1057,11 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="fp8lin", choices=["fp8lin", "reference"])
-    ap.add_argument("--workload", default="llama3-8b-mlp-up", choices=list(W.WORKLOADS))
+    ap.add_argument("--workload", default="dsv3-moe-fwd", choices=list(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e measurement (profiling runs)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     ws, rank, local = dist_setup()
@@ -1077,7 +1173,7 @@ def main():
 
     # e2e through the public entry points with host buffers
     e2e = None
-    if hasattr(step, "e2e_setup"):
+    if hasattr(step, "e2e_setup") and not args.no_e2e:
         h2d, d2h = step.e2e_setup()
         step.e2e_run_steps(2)
         torch.cuda.synchronize()

@@ -54,9 +54,14 @@ __global__ void __launch_bounds__(1024) amax_finalize_kernel(uint32_t* __restric
 }
 
 // Device address of g_scratch, looked up once per device with that device current.
+constexpr int kMaxDevices = 64;
 uint32_t* scratch_address(int device, int* rc) {
   static std::mutex mu;
-  static uint32_t* addr[64];
+  static uint32_t* addr[kMaxDevices];
+  if (device < 0 || device >= kMaxDevices) {
+    *rc = FP8_ERR_DEVICE;
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[device]) {
     void* p = nullptr;
@@ -83,13 +88,20 @@ extern "C" int fp8_quantize_tensor_noalloc(const fp8_tensor* x, int out_dtype, i
   if (!x || x->dtype != FP8_DT_BF16 || x->ndim != 2 || x->shape[0] < 0 || x->shape[1] < 0) return FP8_ERR_INVALID_ARG;
   if (out_dtype != FP8_DT_E4M3 && out_dtype != FP8_DT_E5M2) return FP8_ERR_INVALID_ARG;
   if (layout < 1 || layout > 3) return FP8_ERR_INVALID_ARG;
-  if (!inv_scale || !inv_scale->ptr || inv_scale->dtype != FP8_DT_F32 || inv_scale->ndim < 1) return FP8_ERR_INVALID_ARG;
+  if (!inv_scale || !inv_scale->ptr || inv_scale->dtype != FP8_DT_F32 || inv_scale->ndim < 1 || inv_scale->ndim > 3)
+    return FP8_ERR_INVALID_ARG;
   int64_t inv_n = 1;
-  for (int i = 0; i < inv_scale->ndim; ++i) inv_n *= inv_scale->shape[i];
+  for (int i = 0; i < inv_scale->ndim; ++i) {
+    if (inv_scale->shape[i] != 1) return FP8_ERR_INVALID_ARG;  // exactly one scale
+    inv_n *= inv_scale->shape[i];
+  }
   if (inv_n != 1) return FP8_ERR_INVALID_ARG;
   const int64_t R = x->shape[0], C = x->shape[1];
   if (C % 8 != 0) return FP8_ERR_ALIGNMENT;
-  if (R * C > FP8_NOALLOC_MAX_ELEMENTS) return FP8_ERR_UNSUPPORTED;  // more partials than the array holds
+  // each extent within the limit before the product (no overflow), then the element count:
+  // more elements than the array's partial maxima cover is rejected
+  if (R >= ((int64_t)1 << 31) || C > FP8_NOALLOC_MAX_ELEMENTS) return FP8_ERR_UNSUPPORTED;
+  if (R * C > FP8_NOALLOC_MAX_ELEMENTS) return FP8_ERR_UNSUPPORTED;
   const bool want_row = layout & FP8_LAYOUT_ROW_MAJOR, want_col = layout & FP8_LAYOUT_COL_MAJOR;
   if (want_row) {
     if (!out || out->dtype != out_dtype || out->ndim != 2 || out->shape[0] != R || out->shape[1] != C)

@@ -1,12 +1,17 @@
 // Fused FP8 quantization kernels (sm_103a): amax -> fp64 scale -> fp32 multiply -> clamp ->
-// RNE saturating cast, one HBM read per element.
+// RNE saturating cast, with no intermediate tensor in HBM.
 //
 // Recipe: "FP8 Training: Quantization, Autograd, Torchao", section 2 "The quantization math".
 // Fusion and layout design: "FP8 training on AMD GPUs with TorchTitan and TorchAO", "Triton
 // Kernel Optimization": Level 1 (one kernel per quantization, no intermediates in HBM; the
 // dual row/column-major output), Level 2 (column-wise scales with the output tile transposed
-// on chip so the column-major writes are coalesced; single pass over the data), Level 3
-// (relaxed atomics for the commutative amax reduction).
+// on chip so the column-major writes are coalesced), Level 3 (relaxed atomics for the
+// commutative amax reduction).
+//
+// Reads of the bf16 input: the row-wise kernel reads each element once (a row's amax and its
+// cast come from the same registers). Tensor and column granularity need the amax of a whole
+// tensor or column before the first element can be cast, so they run an amax pass and a cast
+// pass; the cast pass re-reads the input (from L2 where it still holds it).
 #include "common.cuh"
 #include "internal.h"
 

@@ -9,7 +9,10 @@ epilogue; fp8_quantize_from_amax runs the scale and cast steps from given maxima
     holds at any size);
   - fp8_quantize_from_amax with maxima taken from the bf16 input by their plain definition
     (numpy max |x|) is bit-identical to the oracle's quantize;
-  - the fused chain (GEMM with side output, then quantize from amax) equals the unfused one
+  - the fused chain (GEMM with side output, then quantize from amax) against the oracle: on
+    integer-valued operands with power-of-two scales the fp32 accumulation is exact, so the
+    oracle's own GEMM rounded once to bf16 is the stored output, and the oracle's column-wise
+    quantize of it fixes the chain's codes and scales; the chain also equals the unfused one
     (GEMM, then the two-pass fp8_quantize) bit for bit."""
 import numpy as np
 import pytest
@@ -94,21 +97,39 @@ def test_quantize_from_amax_matches_oracle(fp8, R, C, fmt):
     assert np.array_equal(f32_bits(inv2), io.view(np.uint32))
 
 
-def test_fused_chain_equals_unfused(fp8):
-    """dX = dY W (FP8, rowwise) with its column amax, then dX quantized column-wise from those
-    maxima, against the GEMM followed by the two-pass column-wise fp8_quantize."""
-    M, K, N = 1024, 768, 512  # dX [M, K]
-    x, w, dy = W.linear_inputs(M, K, N, seed=9, device="cuda", outliers=True)
-    dyq, _, dyi = fp8.quantize_alloc(dy, fp8.GRAN_ROW, fp8.DT_E5M2)
-    _, wt, wti = fp8.quantize_alloc(w, fp8.GRAN_COL, fp8.DT_E4M3)
-    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
-    ca = torch.empty(K, device="cuda")
-    fp8.fp8_scaled_mm_amax(dyq, wt, dyi, wti, dx, 0, col_amax=ca)
-    qt = torch.empty((K, M), dtype=torch.float8_e5m2, device="cuda")
-    inv = torch.empty(K, device="cuda")
-    fp8.fp8_quantize_from_amax(dx, fp8.GRAN_COL, fp8.DT_E5M2, fp8.LAYOUT_COL_MAJOR, None, qt, inv, ca)
+def _exact_operands(M, N, K, seed):
+    """FP8 operands whose products and sums are exact in fp32: integer values in [-8, 8] (exact in
+    e5m2 and e4m3), per-row / per-column inverse scales that are powers of two, K * 64 < 2^24."""
+    rng = np.random.default_rng(seed)
+    a = rng.integers(-8, 9, size=(M, K)).astype(np.float32)
+    b = rng.integers(-8, 9, size=(N, K)).astype(np.float32)
+    sa = (2.0 ** rng.integers(-6, 3, size=M)).astype(np.float32)
+    sb = (2.0 ** rng.integers(-6, 3, size=N)).astype(np.float32)
+    return oracle.encode(a, oracle.E5M2), oracle.encode(b, oracle.E4M3), sa, sb
+
+
+def test_fused_chain_matches_oracle(fp8):
+    """The grad-input GEMM dX = dY W (e5m2 x e4m3, rowwise scales) with its column amax, then dX
+    quantized column-wise (e5m2, column-major) from those maxima: the stored dX, the maxima, the
+    codes and the inverse scales against the oracle; the chain against the unfused one."""
+    M, N, K = 1024, 768, 512  # dX [M, N], contraction K
+    ca, cb, sa, sb = _exact_operands(M, N, K, 9)
+    ref, _ = oracle.gemm_fp8(ca, oracle.E5M2, cb, oracle.E4M3, sa, sb)
+    ref_bf16 = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16)  # exact -> one RNE rounding
+    rb = bits(ref_bf16)
+    qo, io = oracle.quantize_cols(rb, oracle.E5M2)
+    dx = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    col = torch.empty(N, device="cuda")
+    fp8.fp8_scaled_mm_amax(upload_codes(ca, oracle.E5M2), upload_codes(cb, oracle.E4M3), upload_f32(sa),
+                           upload_f32(sb), dx, 0, col_amax=col)
+    qt = torch.empty((N, M), dtype=torch.float8_e5m2, device="cuda")
+    inv = torch.empty(N, device="cuda")
+    fp8.fp8_quantize_from_amax(dx, fp8.GRAN_COL, fp8.DT_E5M2, fp8.LAYOUT_COL_MAJOR, None, qt, inv, col)
     _, qt_ref, inv_ref = fp8.quantize_alloc(dx, fp8.GRAN_COL, fp8.DT_E5M2)
     torch.cuda.synchronize()
+    assert np.array_equal(bits(dx.cpu()), rb)
+    assert np.array_equal(col.cpu().numpy(), ref_bf16.float().abs().amax(dim=0).numpy())
+    assert np.array_equal(codes(qt), qo.T) and np.array_equal(f32_bits(inv), io.view(np.uint32))
     assert torch.equal(qt.view(torch.uint8), qt_ref.view(torch.uint8)) and torch.equal(inv, inv_ref)
 
 
