@@ -323,6 +323,13 @@ int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* saved, const fp
  * setting. */
 int fp8_set_test_stall(int enable);
 
+/* Test hook for the cast step ([Q] section 2: round to nearest even, saturating; [F] formats):
+ * out[i] = the FP8 code (out_dtype E4M3 or E5M2) that the quantize kernels' cast gives the fp32
+ * value whose bit pattern is first_bits + i, for 0 <= i < n (first_bits + n <= 2^32). out: n
+ * bytes of device memory. Values beyond +-fp8_max saturate to it, as clamping first would give.
+ * Asynchronous on `stream`. Returns FP8_OK, FP8_ERR_INVALID_ARG, FP8_ERR_DEVICE or FP8_ERR_CUDA. */
+int fp8_test_cast_bits(uint32_t first_bits, int64_t n, int out_dtype, void* out, void* stream);
+
 /*
  * fp8_quantize_tensor_noalloc — the tensorwise quantize of fp8_quantize (FP8_GRAN_TENSOR) for
  * callers that cannot allocate device memory. The pages have no counterpart: this entry point

@@ -84,6 +84,7 @@ def _load():
     L.fp8_scaled_mm_amax.argtypes = [T, T, T, T, T, ctypes.c_int, T, T, P, P]
     L.fp8_quantize_from_amax.argtypes = [T, ctypes.c_int, ctypes.c_int, ctypes.c_int, T, T, T, T, P, P]
     L.fp8_set_test_stall.argtypes = [ctypes.c_int]
+    L.fp8_test_cast_bits.argtypes = [ctypes.c_uint32, ctypes.c_int64, ctypes.c_int, P, P]
     L.fp8_set_test_stall.restype = ctypes.c_int
     return L
 
@@ -94,7 +95,7 @@ lib = _load()
 EXPORTS = ("fp8_quantize", "fp8_scaled_mm", "fp8_grouped_mm", "fp8_linear_fwd", "fp8_linear_bwd",
            "fp8_workspace_size", "fp8_jagged_padded_rows", "fp8_status_string", "fp8_set_wait_limit_ns",
            "fp8_quantize_tensor_noalloc", "fp8_set_test_stall", "fp8_mx_scale_bytes", "fp8_scaled_mm_amax",
-           "fp8_quantize_from_amax")
+           "fp8_quantize_from_amax", "fp8_test_cast_bits")
 
 
 def status_string(code: int) -> str:

@@ -159,6 +159,15 @@ extern "C" uint64_t fp8_set_wait_limit_ns(uint64_t ns) { return g_wait_ns.exchan
 
 extern "C" int fp8_set_test_stall(int enable) { return g_test_stall.exchange(enable ? 1 : 0); }
 
+extern "C" int fp8_test_cast_bits(uint32_t first_bits, int64_t n, int out_dtype, void* out, void* stream) {
+  if (!is_fp8(out_dtype) || n < 0 || n > ((int64_t)1 << 32) - (int64_t)first_bits) return FP8_ERR_INVALID_ARG;
+  if (n > 0 && !out) return FP8_ERR_INVALID_ARG;
+  Ctx c;
+  const int rc = make_ctx(&c, stream, nullptr);
+  if (rc != FP8_OK) return rc;
+  return launch_cast_bits(first_bits, n, out_dtype, out, c);
+}
+
 extern "C" const char* fp8_status_string(int code) {
   switch (code) {
     case FP8_OK: return "ok";

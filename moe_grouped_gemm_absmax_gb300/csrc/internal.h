@@ -106,6 +106,8 @@ namespace fp8lin {
 // Cast phase of the tensorwise quantize alone: reads the bf16 pattern of amax at `amax_word`
 // (already reduced) and writes q / qt / inv exactly as launch_quant_tensor does.
 // amax_shift: 0 when amax_word holds a bf16 pattern, 16 when it holds the fp32 value.
+// Test hook: out[i] = the kernels' cast (fmt) of the fp32 value with bit pattern first + i.
+int launch_cast_bits(uint32_t first, int64_t n, int fmt, void* out, const Ctx& c);
 int launch_quant_tensor_cast(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
                              const uint32_t* amax_word, const Ctx& c, int amax_shift = 0);
 }  // namespace fp8lin

@@ -862,3 +862,36 @@ int launch_quant_tensor_cast(const void* x, int64_t R, int64_t C, int fmt, void*
 }
 
 }  // namespace fp8lin
+
+namespace fp8lin {
+
+// Test hook: the cast of every quantize kernel (cvt.rn.satfinite, two values per instruction),
+// applied to the fp32 values whose bit patterns are first, first + 1, ..., first + n - 1. The
+// row-wise and column-wise kernels cast the scaled products without an explicit clamp (the
+// saturating cvt gives the same code as clamping to +-fp8_max first), so this covers their cast
+// step as it runs.
+template <int FMT>
+__global__ void __launch_bounds__(256) cast_bits_kernel(uint32_t first, int64_t n, uint8_t* __restrict__ out) {
+  const int64_t stride = 2 * (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x); i < n; i += stride) {
+    const float a = __uint_as_float(first + (uint32_t)i);
+    const float b = __uint_as_float(first + (uint32_t)(i + 1));
+    const uint32_t c = cvt_fp8x2<FMT>(a, b);
+    out[i] = (uint8_t)c;
+    if (i + 1 < n) out[i + 1] = (uint8_t)(c >> 8);
+  }
+}
+
+int launch_cast_bits(uint32_t first, int64_t n, int fmt, void* out, const Ctx& c) {
+  if (n <= 0) return FP8_OK;
+  const int64_t need = ceil_div64(n, 2 * 256);
+  const int64_t cap = (int64_t)c.sm_count * 8;
+  const unsigned grid = (unsigned)(need < cap ? need : cap);
+  if (fmt == FP8_DT_E4M3)
+    cast_bits_kernel<FP8_DT_E4M3><<<grid, 256, 0, c.stream>>>(first, n, static_cast<uint8_t*>(out));
+  else
+    cast_bits_kernel<FP8_DT_E5M2><<<grid, 256, 0, c.stream>>>(first, n, static_cast<uint8_t*>(out));
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+}  // namespace fp8lin

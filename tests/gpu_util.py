@@ -59,7 +59,7 @@ def upload_f32(a: np.ndarray) -> torch.Tensor:
 
 def check_gemm(got, ref, absacc, out_bf16, tol=2e-3):
     """|got - ref| <= tol * absacc (+ half a bf16 ulp of ref when the output is bf16)."""
-    got = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    got = got.detach().double().cpu().numpy() if isinstance(got, torch.Tensor) else got
     bound = tol * absacc + (2.0 ** -8 * np.abs(ref) if out_bf16 else 0.0) + 1e-30
     err = np.abs(got - ref)
     bad = err > bound

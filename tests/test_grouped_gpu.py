@@ -56,9 +56,9 @@ def test_jagged_m(fp8, counts, N, K):
     ([513, 511, 1024, 0], 264, 128, torch.bfloat16, oracle.E4M3),
 ])
 def test_jagged_m_pairs(fp8, counts, N, K, out_dtype, fa):
-    """At least 2048 rows: CTA pairs with transposed tiles (256 weight rows x N' tokens, N' the
-    expert's remaining tokens rounded up to 16): experts with 1, 15, 16, 17 tokens, 255-257,
-    empty experts, N not a multiple of 256, e4m3 and e5m2 activations, fp32 and bf16 outputs."""
+    """At least 2048 rows: CTA pairs with 256-row tiles that start at each expert's first row:
+    experts with 1, 15, 16, 17 tokens, 255-257, empty experts, N not a multiple of 256, e4m3 and
+    e5m2 activations, fp32 and bf16 outputs."""
     out, (ca, fa_, cw, ia, iw, ends) = _jagged_m_case(fp8, counts, N, K, out_dtype, seed=9, fa=fa)
     ref, absacc = oracle.grouped_gemm_m(ca, fa_, cw, oracle.E4M3, ia, iw, ends)
     check_gemm(out, ref, absacc, out_dtype == torch.bfloat16)
