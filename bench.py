@@ -323,15 +323,61 @@ class ColwiseStep(Step):
         f.fp8_quantize(self.xx, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.xq, None, self.xi)
 
 
-class MoeFwdStep(Step):
-    """DeepSeek-V3-shaped grouped GEMM forward: quantize A rowwise, W per (expert, n), grouped GEMM."""
+class TensorwiseQuantStep(Step):
+    """Tensorwise quantization of the llama3-8b-mlp-up tensors with the dual output (row-major and
+    column-major codes from one quantize, as the tensorwise Linear saves them for backward):
+    x [8192, 4096] and W [14336, 4096] to e4m3, dY [8192, 14336] to e5m2."""
+    unit = "GB/s"
 
     def __init__(self, fp8, seed=0, device="cuda"):
         self.fp8 = fp8
-        self.name = "dsv3-moe-fwd"
+        self.name = "llama3-8b-tensorwise-quant"
+        d = W.WORKLOADS[self.name].dims
+        M, K, N = d["M"], d["K"], d["N"]
+        self.x, self.w, self.dy = W.linear_inputs(M, K, N, seed=seed, device=device, outliers=True)
+        e4, e5 = torch.float8_e4m3fn, torch.float8_e5m2
+        self.bufs = []
+        for t, dt in ((self.x, e4), (self.w, e4), (self.dy, e5)):
+            R, C = t.shape
+            self.bufs.append((torch.empty((R, C), dtype=dt, device=device), torch.empty((C, R), dtype=dt, device=device),
+                              torch.empty(1, device=device), torch.empty(4, dtype=torch.int32, device=device)))
+        self.M, self.K, self.N = M, K, N
+        self.kernels = [("quantize_tensor x e4m3 dual", "hbm", 4 * M * K + 4, "hbm"),
+                        ("quantize_tensor W e4m3 dual", "hbm", 4 * N * K + 4, "hbm"),
+                        ("quantize_tensor dY e5m2 dual", "hbm", 4 * M * N + 4, "hbm")]
+
+    def total_units(self):
+        return float(sum(k[2] for k in self.kernels))
+
+    def launches_per_step(self):
+        return 2 * len(self.kernels)  # amax pass and cast pass per tensor
+
+    def cpu_sample(self, rows):
+        """The oracle's tensorwise quantize of x[:rows] (all columns)."""
+        import oracle
+        xb = W.bf16_bits(self.x[:rows].cpu())
+
+        def run():
+            oracle.quantize_tensor(xb, oracle.E4M3)
+        return run, 4.0 * xb.size + 4, f"tensorwise quantize of x[:{rows}] (dual-output bytes)"
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        for i, (t, dt) in enumerate(((self.x, f.DT_E4M3), (self.w, f.DT_E4M3), (self.dy, f.DT_E5M2))):
+            q, qt, inv, ws = self.bufs[i]
+            mark(i)
+            f.fp8_quantize(t, f.GRAN_TENSOR, dt, f.LAYOUT_BOTH, q, qt, inv, None, ws)
+
+
+class MoeFwdStep(Step):
+    """DeepSeek-V3-shaped grouped GEMM forward: quantize A rowwise, W per (expert, n), grouped GEMM."""
+
+    def __init__(self, fp8, seed=0, device="cuda", name="dsv3-moe-fwd"):
+        self.fp8 = fp8
+        self.name = name
         d = W.WORKLOADS[self.name].dims
         E, M, K, N = d["E"], d["M"], d["K"], d["N"]
-        counts = W.dsv3_counts(seed)
+        counts = W.dsv3_counts(seed) if name == "dsv3-moe-fwd" else W.dsv3_32e_counts(seed)
         self.A, self.Wt, ends, _ = W.moe_inputs(E, M, K, N, counts, seed=seed, device=device)
         self.ends = torch.from_numpy(ends).to(device)
         self.counts = counts
@@ -879,8 +925,10 @@ def make_step(fp8, name):
         return TensorwiseLinearStep(fp8)
     if name == "colwise-8192x14336":
         return ColwiseStep(fp8)
-    if name == "dsv3-moe-fwd":
-        return MoeFwdStep(fp8)
+    if name == "llama3-8b-tensorwise-quant":
+        return TensorwiseQuantStep(fp8)
+    if name in ("dsv3-moe-fwd", "dsv3-moe-fwd-32e"):
+        return MoeFwdStep(fp8, name=name)
     if name == "llama4-moe-fwdbwd":
         return MoeFwdBwdStep(fp8)
     if name == "llama3-8b-mlp-up-mx":

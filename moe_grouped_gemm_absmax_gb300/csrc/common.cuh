@@ -152,6 +152,36 @@ FP8_DEVI uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
+// L2 cache policies (createpolicy) for loads and stores that carry a cache hint. evict_last: lines
+// that a later pass reads again (the amax pass of a two-pass quantize keeps its input in L2 for
+// the cast pass); evict_first: a line's last use, or output that nothing reads soon, so that it
+// does not push out lines still to be re-read.
+FP8_DEVI uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+FP8_DEVI uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+FP8_DEVI uint4 ld_nc_v4_hint(const void* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+FP8_DEVI void st_v2_hint(void* p, uint2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(v.x), "r"(v.y), "l"(pol) : "memory");
+}
+FP8_DEVI void st_v4_hint(void* p, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(pol)
+               : "memory");
+}
+
 // ------------------------------------------------------------------------------------------
 // mbarrier
 FP8_DEVI void mbar_init(uint64_t* bar, uint32_t count) {
@@ -220,6 +250,15 @@ FP8_DEVI void tma_load_4d(void* dst, const CUtensorMap* m, uint64_t* bar, int32_
       : "memory");
 }
 
+// The same loads with an L2 cache policy (see l2_evict_last / l2_evict_first).
+FP8_DEVI void tma_load_2d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t x, int32_t y, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(pol)
+      : "memory");
+}
+
 // TMA bulk-tensor stores shared -> global, tracked per thread in bulk async-groups.
 FP8_DEVI void tma_store_2d(const CUtensorMap* m, const void* src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -231,6 +270,18 @@ FP8_DEVI void tma_store_3d(const CUtensorMap* m, const void* src, int32_t x, int
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(m)),
                "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+FP8_DEVI void tma_store_2d_hint(const CUtensorMap* m, const void* src, int32_t x, int32_t y, uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "l"(pol)
+               : "memory");
+}
+FP8_DEVI void tma_store_3d_hint(const CUtensorMap* m, const void* src, int32_t x, int32_t y, int32_t z, uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "l"(pol)
                : "memory");
 }
 FP8_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

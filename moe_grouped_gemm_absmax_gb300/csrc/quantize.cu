@@ -209,17 +209,18 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, 
                                                    uint32_t* __restrict__ amax_ws) {
   __shared__ uint32_t red[8];
   uint32_t acc = 0;
+  const uint64_t keep = l2_evict_last();  // the cast pass reads the tensor again
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (; i + 3 * stride < nvec; i += 4 * stride) {
-    const uint4 a = ld_nc_v4(x + i), b = ld_nc_v4(x + i + stride);
-    const uint4 d = ld_nc_v4(x + i + 2 * stride), e = ld_nc_v4(x + i + 3 * stride);
+    const uint4 a = ld_nc_v4_hint(x + i, keep), b = ld_nc_v4_hint(x + i + stride, keep);
+    const uint4 d = ld_nc_v4_hint(x + i + 2 * stride, keep), e = ld_nc_v4_hint(x + i + 3 * stride, keep);
     acc = absmax_vec8(acc, a);
     acc = absmax_vec8(acc, b);
     acc = absmax_vec8(acc, d);
     acc = absmax_vec8(acc, e);
   }
-  for (; i < nvec; i += stride) acc = absmax_vec8(acc, ld_nc_v4(x + i));
+  for (; i < nvec; i += stride) acc = absmax_vec8(acc, ld_nc_v4_hint(x + i, keep));
   const uint32_t m = __reduce_max_sync(0xffffffffu, absmax_fold(acc));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
   __syncthreads();
@@ -251,6 +252,9 @@ __global__ void __launch_bounds__(256) quant_tensor_cast_kernel(const uint16_t* 
   }
   __syncthreads();
   const float s32 = s_sc;
+  // the input's last use and output nothing re-reads soon: neither should push out of L2 the
+  // input lines other tiles still have to read
+  const uint64_t last = l2_evict_first();
   const int64_t r0 = (int64_t)blockIdx.y * kTcRows, c0 = (int64_t)blockIdx.x * kTcCols;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -259,8 +263,8 @@ __global__ void __launch_bounds__(256) quant_tensor_cast_kernel(const uint16_t* 
     const int64_t r = r0 + rr, col = c0 + cv * 8;
     uint2 o = make_uint2(0, 0);
     if (r < R && col < C) {
-      o = quant_vec8<FMT>(ld_nc_v4(x + r * C + col), s32, FMAX);
-      if (q) *reinterpret_cast<uint2*>(q + r * C + col) = o;
+      o = quant_vec8<FMT>(ld_nc_v4_hint(x + r * C + col, last), s32, FMAX);
+      if (q) st_v2_hint(q + r * C + col, o, last);
     }
     if (qt) {
 #pragma unroll
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(256) quant_tensor_cast_kernel(const uint16_t* 
     const int64_t col = c0 + cl, r = r0 + 16 * k;
     if (col < C && r < R) {  // R % 16 == 0: the 16-byte chunk is all in range
       const uint32_t* src = reinterpret_cast<const uint32_t*>(T + cl * kTcPitch + 16 * k);
-      *reinterpret_cast<uint4*>(qt + col * R + r) = make_uint4(src[0], src[1], src[2], src[3]);
+      st_v4_hint(qt + col * R + r, make_uint4(src[0], src[1], src[2], src[3]), last);
     }
   }
 }
@@ -535,6 +539,8 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
   if (warp == 0) {
     // ==================== producer warp: one lane issues the tiles by TMA ====================
     if (lane == 0) {
+      // pass 1 keeps what it reads in L2 for pass 2; pass 2's reads are the last use
+      const uint64_t pol = CAST ? l2_evict_first() : l2_evict_last();
       int s = 0;
       uint32_t ph = 0;
       int64_t k = 0;
@@ -555,7 +561,7 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
         S.info[s] = ColInfo{(int32_t)u.g, (int32_t)u.c0, (int32_t)u.rt, (int32_t)valid, (int32_t)wr,
                             (int32_t)u.pstart};
         mbar_arrive_expect_tx(&S.full[s], kColStageBytes);
-        tma_load_2d(ring + s * kColStageBytes, &tm_in, &S.full[s], (int32_t)u.c0, (int32_t)(u.g0 + u.rt));
+        tma_load_2d_hint(ring + s * kColStageBytes, &tm_in, &S.full[s], (int32_t)u.c0, (int32_t)(u.g0 + u.rt), pol);
         if (k + 1 < cnt) un = col_unit(p, unit_at(k + 1), upre, ppre);
         if (++s == kColStages) {
           s = 0;
@@ -681,6 +687,7 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
     // rows] and the warp's elected lane stores the box by TMA: no barrier across warps.
     const int cw = warp - 1;
     const int r0 = 32 * cw;  // the warp's rows within the unit
+    const uint64_t out_pol = l2_evict_first();  // the codes are not re-read by this pass
     const uint32_t woff = ((uint32_t)(lane & 3) << 2);
     uint8_t* wbuf = Tout + cw * 2 * kColWarpBox;
     int s = 0, nb = 0;
@@ -752,9 +759,9 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
       if (lane == 0) {
         const int32_t xo = info.pstart + info.rt + r0;
         if (p.mode == 1)
-          tma_store_3d(&tm_out, box, xo, info.c0, info.g);
+          tma_store_3d_hint(&tm_out, box, xo, info.c0, info.g, out_pol);
         else
-          tma_store_2d(&tm_out, box, xo, info.c0);
+          tma_store_2d_hint(&tm_out, box, xo, info.c0, out_pol);
         bulk_commit();
       }
     }

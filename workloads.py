@@ -129,6 +129,11 @@ WORKLOADS = {
         "Llama3-8B-shaped MLP-up Linear fwd+bwd, rowwise: x [8192,4096] N(0,1) with 1% channels "
         "x50, W [14336,4096] N(0,0.02), dY [8192,14336] N(0,1e-3); fwd+dX FP8 (e4m3/e5m2), dW bf16",
         dict(M=8192, K=4096, N=14336)),
+    "llama3-8b-tensorwise-quant": Workload(
+        "llama3-8b-tensorwise-quant",
+        "tensorwise quantize with the dual output (row- and column-major codes) of the llama3-8b-mlp-up "
+        "tensors: x [8192,4096] (1% channels x50) and W [14336,4096] to e4m3, dY [8192,14336] to e5m2",
+        dict(M=8192, K=4096, N=14336)),
     "colwise-8192x14336": Workload(
         "colwise-8192x14336",
         "columnwise e5m2 quantize + column-major output of G [8192,14336] N(0,1e-3) x 10^U(-2,2) "
@@ -139,6 +144,11 @@ WORKLOADS = {
         "DeepSeek-V3-shaped MoE grouped GEMM fwd: 256 experts, K=7168, N=2048, 131072 routed rows "
         "with Zipf(1.1) counts incl. 8 forced-empty experts; A N(0,1), W [256,2048,7168] N(0,0.02)",
         dict(E=256, M=131072, K=7168, N=2048)),
+    "dsv3-moe-fwd-32e": Workload(
+        "dsv3-moe-fwd-32e",
+        "the dsv3-moe-fwd layer cut to 32 experts and 16384 routed rows (Zipf(1.1) counts, 1 forced-empty "
+        "expert), same K and N: the size the full-metric profiler captures (about 2 GB on the device)",
+        dict(E=32, M=16384, K=7168, N=2048)),
     "llama4-moe-fwdbwd": Workload(
         "llama4-moe-fwdbwd",
         "Llama4-shaped MoE grouped fwd+bwd: 16 experts, K=5120, N=8192, 8192 rows with "
@@ -196,6 +206,10 @@ def moe_inputs(E: int, M: int, K: int, N: int, counts, seed: int = 0, device="cp
 
 def dsv3_counts(seed: int = 0, empty_first=False, empty_last=False) -> np.ndarray:
     return zipf_counts(131072, 256, 1.1, 8, seed, empty_first, empty_last)
+
+
+def dsv3_32e_counts(seed: int = 0) -> np.ndarray:
+    return zipf_counts(16384, 32, 1.1, 1, seed)
 
 
 def llama4_counts(seed: int = 0) -> np.ndarray:
