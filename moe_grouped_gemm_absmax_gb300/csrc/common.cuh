@@ -363,6 +363,18 @@ FP8_DEVI void cluster_barrier() {
 FP8_DEVI void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Relaxed arrivals (no release ordering), for barriers that only say "this warp's tensor-memory
+// loads of an accumulator have completed" (tcgen05.wait::ld returned, the values are in registers,
+// and tcgen05.fence::before_thread_sync precedes the arrival): no memory write of the arriving warp
+// has to become visible to the waiting thread. A release arrival would first wait for the warp's
+// outstanding memory operations; at cluster scope that took about 1 us per tile in the jagged-K
+// GEMM, whose epilogue had just issued its output stores.
+FP8_DEVI void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+FP8_DEVI void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 FP8_DEVI void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
                "r"(ncols)

@@ -801,9 +801,9 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
           __syncwarp();
           if (lane == 0) {
             if (CG == 2)
-              mbar_arrive_cluster(mapa_shared(smem_u32(&S.tempty[buf]), 0));
+              mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&S.tempty[buf]), 0));
             else
-              mbar_arrive(&S.tempty[buf]);
+              mbar_arrive_relaxed(&S.tempty[buf]);
           }
           if (++buf == C::NBUF) {
             buf = 0;
@@ -866,9 +866,9 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           if (CG == 2)
-            mbar_arrive_cluster(mapa_shared(smem_u32(&S.tempty[0]), 0));
+            mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&S.tempty[0]), 0));
           else
-            mbar_arrive(&S.tempty[0]);
+            mbar_arrive_relaxed(&S.tempty[0]);
         }
         aphase ^= 1;
         if (C::MX_TMA_OUT && p.tma_out && !p.out_f32 && T.n0 + c0 < p.N) {
@@ -1095,9 +1095,9 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
       __syncwarp();
       if (lane == 0) {  // the issuing CTA's barrier counts the epilogue warps of both CTAs
         if (CG == 2)
-          mbar_arrive_cluster(mapa_shared(smem_u32(&S.tempty[buf]), 0));
+          mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&S.tempty[buf]), 0));
         else
-          mbar_arrive(&S.tempty[buf]);
+          mbar_arrive_relaxed(&S.tempty[buf]);
       }
       if (++buf == 2) {
         buf = 0;
