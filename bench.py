@@ -1044,14 +1044,14 @@ def whole_job_value(units_per_step: float, steps: int, world_size: int, max_tota
     return units_per_step * steps * world_size / max_total_ms / scale
 
 
-def traffic_for(label: str):
-    """ncu DRAM bytes per launch for a kernel label, from profiles/ncu_traffic.json; null when the
-    kernel's source changed since the capture."""
+def traffic_for(workload: str, label: str):
+    """ncu DRAM bytes per launch for a kernel of a workload ("<workload>: <label>" in
+    profiles/ncu_traffic.json); null when the kernel's source changed since the capture."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    ent = d.get(label)
+    ent = d.get(f"{workload}: {label}")
     if not ent:
         return None
     src = os.path.join(ROOT, ent["source"])
@@ -1189,7 +1189,7 @@ def main():
     dk = kernels[dom]
     roofline = {"kernel": dk["kernel"], "bound": "tensor" if step.kernels[dom][1] == "tensor" else "hbm",
                 "achieved": dk["achieved"], "peak": dk["peak"], "unit": dk["unit"], "frac": dk["frac"],
-                "traffic": traffic_for(dk["kernel"]),
+                "traffic": traffic_for(step.name, dk["kernel"]),
                 "peak_source": f"{peaks['src']} ({'2 x bf16 burst' if step.kernels[dom][3] == 'fp8' else step.kernels[dom][3]})"}
 
     # the unfused alternative of a fused step, timed the same way (per-kernel events, flushed L2)

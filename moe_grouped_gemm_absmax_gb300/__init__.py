@@ -285,7 +285,7 @@ def quantize_alloc(x, granularity, out_dtype, layout=None, offsets=None, padded_
     ws = None
     if granularity == GRAN_TENSOR:
         inv = torch.empty(1, dtype=torch.float32, device=dev)
-        ws = torch.empty(1, dtype=torch.int32, device=dev)
+        ws = torch.empty(2, dtype=torch.int32, device=dev)  # amax word, grid-barrier count
         if layout & LAYOUT_COL_MAJOR:
             out_t = torch.empty((C, R), dtype=fdt, device=dev)
     elif granularity == GRAN_ROW:

@@ -217,7 +217,7 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
         FP8_CHECK(shape_is(out_t, 2, C, R), FP8_ERR_INVALID_ARG);
         FP8_CHECK(R % 16 == 0, FP8_ERR_ALIGNMENT);
       }
-      FP8_CHECK(ws && ws_bytes >= 4 && (reinterpret_cast<uintptr_t>(ws) & 3u) == 0, FP8_ERR_WORKSPACE);
+      FP8_CHECK(ws && ws_bytes >= 8 && (reinterpret_cast<uintptr_t>(ws) & 7u) == 0, FP8_ERR_WORKSPACE);
       return launch_quant_tensor(x->ptr, B * R, C, out_dtype, want_row ? out->ptr : nullptr,
                                  want_col ? out_t->ptr : nullptr, static_cast<float*>(inv->ptr),
                                  static_cast<uint32_t*>(ws), c);
@@ -647,7 +647,7 @@ static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad
     L.total = off;
     return L;
   }
-  L.amax = take(4);
+  L.amax = take(8);
   L.dy_q = take((size_t)(M * N));
   L.dy_inv = take((size_t)(rows ? M : 1) * 4);
   L.dyt_q = fp8w ? take((size_t)(N * M)) : 0;
@@ -686,7 +686,7 @@ static int mx_both(const fp8_tensor* x, int fmt, const fp8_tensor* q, const fp8_
 extern "C" size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granularity, int wgrad_mode) {
   switch (op) {
     case FP8_OP_QUANTIZE:  // (d0, d1) = (groups, columns) for FP8_GRAN_COL; (segments, -) for MX
-      if (granularity == FP8_GRAN_TENSOR) return 4;
+      if (granularity == FP8_GRAN_TENSOR) return 8;  // amax word, grid-barrier count
       if (granularity == FP8_GRAN_MX) return d0 > 0 ? (size_t)round_up(4 * (d0 + 1), 16) : 0;
       if (granularity == FP8_GRAN_COL) return (size_t)col_ws_words(d0 > 0 ? d0 : 1, d1 > 0 ? d1 : 0) * 4;
       return 0;
@@ -709,7 +709,7 @@ extern "C" int fp8_linear_fwd(const fp8_tensor* x, const fp8_tensor* w, int gran
   const int64_t M = x->shape[0], K = x->shape[1], N = w->shape[0];
   FP8_CHECK(w->shape[1] == K, FP8_ERR_INVALID_ARG);
   if (granularity == FP8_GRAN_TENSOR) {
-    FP8_CHECK(workspace && workspace_bytes >= 4, FP8_ERR_WORKSPACE);
+    FP8_CHECK(workspace && workspace_bytes >= 8, FP8_ERR_WORKSPACE);
     const int xl = saved->xt_q.ptr ? FP8_LAYOUT_BOTH : FP8_LAYOUT_ROW_MAJOR;
     FP8_TRY(quantize_impl(x, FP8_GRAN_TENSOR, FP8_DT_E4M3, xl, &saved->x_q, &saved->xt_q, &saved->x_inv, nullptr,
                           workspace, workspace_bytes, c));
@@ -815,7 +815,7 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
   fp8_tensor dyt_q = T2(fp8w ? ws + L.dyt_q : nullptr, FP8_DT_E5M2, N, M);
   if (!rows) {
     const int layout = (fp8w && need_dw) ? FP8_LAYOUT_BOTH : FP8_LAYOUT_ROW_MAJOR;
-    FP8_TRY(quantize_impl(dy, FP8_GRAN_TENSOR, FP8_DT_E5M2, layout, &dy_q, &dyt_q, &dy_inv, nullptr, ws + L.amax, 4,
+    FP8_TRY(quantize_impl(dy, FP8_GRAN_TENSOR, FP8_DT_E5M2, layout, &dy_q, &dyt_q, &dy_inv, nullptr, ws + L.amax, 8,
                           c));
     if (dx && dx->ptr)
       FP8_TRY(scaled_mm_impl(&dy_q, &saved->wt_q, &dy_inv, &saved->w_inv, dx, 0, c));

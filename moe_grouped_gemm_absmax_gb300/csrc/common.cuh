@@ -80,6 +80,21 @@ FP8_DEVI Scale tab_scale(const ScaleTab& t, uint32_t amax_bits) {
   return r;
 }
 
+// Largest finite magnitude of a format, at compile time.
+template <int FMT>
+struct FmtMax;
+template <>
+struct FmtMax<FP8_DT_E4M3> {
+  static constexpr float v = kE4M3Max;
+};
+template <>
+struct FmtMax<FP8_DT_E5M2> {
+  static constexpr float v = kE5M2Max;
+};
+
+__host__ __device__ constexpr int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr int64_t round_up64(int64_t a, int64_t b) { return ceil_div64(a, b) * b; }
+
 // Two IEEE fp32 products in one instruction (mul.rn.f32x2): bit-identical to two __fmul_rn.
 FP8_DEVI float2 fmul2_rn(float2 a, float2 b) {
   uint64_t ra, rb, rd;
@@ -180,6 +195,35 @@ FP8_DEVI void st_v4_hint(void* p, uint4 v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w), "l"(pol)
                : "memory");
+}
+
+// Grid barrier words (global memory, gpu scope): a release increment orders this thread's earlier
+// memory operations (e.g. a relaxed atomic max) before the count; the acquire load of the waiter
+// then sees them.
+FP8_DEVI void red_add_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+FP8_DEVI uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+FP8_DEVI uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Bounded wait until *p >= target (polling with a short back-off). False when limit_ns elapsed.
+FP8_DEVI bool wait_count_geq(const uint32_t* p, uint32_t target, uint64_t limit_ns) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t ns = 32;
+  for (;;) {
+    __nanosleep(ns);
+    if (ns < 512) ns <<= 1;
+    if (ld_acquire_gpu(p) >= target) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
 }
 
 // ------------------------------------------------------------------------------------------

@@ -33,8 +33,8 @@ int make_tmap(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int ra
 // --- quantize launchers (quantize.cu) ---
 // Rowwise: x bf16 [R, C] -> q [R, C], inv [R].
 int launch_quant_rows(const void* x, int64_t R, int64_t C, int fmt, void* q, float* inv, const Ctx& c);
-// Tensorwise: amax of x [R, C] into amax_ws (one u32, zeroed here), then the cast into q (row-major,
-// may be null) and/or qt ([C, R], may be null); inv [1].
+// Tensorwise in one cooperative launch: amax of x [R, C] into ws[0], a grid barrier on ws[1] (both
+// zeroed here), then the cast into q (row-major, may be null) and/or qt ([C, R], may be null); inv [1].
 int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
                         uint32_t* amax_ws, const Ctx& c);
 // Columnwise with column-major output. x viewed as [rows_total, C]. Groups of rows share one

@@ -1,5 +1,5 @@
-// Fused FP8 quantization kernels (sm_103a): amax -> fp64 scale -> fp32 multiply -> clamp ->
-// RNE saturating cast, with no intermediate tensor in HBM.
+// Tensorwise and column-wise FP8 quantization (sm_103a): amax -> fp64 scale (by table) -> fp32
+// multiply -> clamp -> RNE saturating cast, with no intermediate tensor in HBM. (Row-wise: rows.cu.)
 //
 // Recipe: "FP8 Training: Quantization, Autograd, Torchao", section 2 "The quantization math".
 // Fusion and layout design: "FP8 training on AMD GPUs with TorchTitan and TorchAO", "Triton
@@ -8,230 +8,17 @@
 // on chip so the column-major writes are coalesced), Level 3 (relaxed atomics for the
 // commutative amax reduction).
 //
-// Reads of the bf16 input: the row-wise kernel reads each element once (a row's amax and its
-// cast come from the same registers). Tensor and column granularity need the amax of a whole
-// tensor or column before the first element can be cast, so they run an amax pass and a cast
-// pass; the cast pass re-reads the input (from L2 where it still holds it).
+// Tensor and column granularity need the amax of a whole tensor or column before the first element
+// can be cast, so the input is read twice: an amax pass whose loads keep the lines in L2, then the
+// cast pass, which reads them again mostly from L2.
 #include "common.cuh"
 #include "internal.h"
 
 namespace fp8lin {
 
-template <int FMT>
-struct FmtMax;
-template <>
-struct FmtMax<FP8_DT_E4M3> {
-  static constexpr float v = kE4M3Max;
-};
-template <>
-struct FmtMax<FP8_DT_E5M2> {
-  static constexpr float v = kE5M2Max;
-};
-
-__host__ __device__ constexpr int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
-__host__ __device__ constexpr int64_t round_up64(int64_t a, int64_t b) { return ceil_div64(a, b) * b; }
 
 // ==========================================================================================
-// Rowwise: one scale per row. A team of TPR threads holds one row in registers (up to 8
-// 16-byte vectors per thread), reduces |x| with packed-bf16 integer max, derives the scale in
-// one thread, then casts from registers. Several teams share a CTA of at least 256 threads.
-constexpr int kRowVPT = 8;
-
-template <int FMT, int TPR>
-__global__ void __launch_bounds__(TPR > 256 ? TPR : 256)
-    quant_rows_kernel(const uint4* __restrict__ x, int64_t R, int nvec, uint2* __restrict__ q,
-                      float* __restrict__ inv, const __grid_constant__ ScaleTab tab) {
-  constexpr int CTA = TPR > 256 ? TPR : 256;
-  constexpr int TEAMS = CTA / TPR;
-  constexpr int WPT = TPR / 32;
-  constexpr float FMAX = FmtMax<FMT>::v;
-  __shared__ uint32_t red[CTA / 32];
-  __shared__ float sc[TEAMS];
-  const int team = threadIdx.x / TPR;
-  const int t = threadIdx.x % TPR;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-  for (int64_t base = (int64_t)blockIdx.x * TEAMS; base < R; base += (int64_t)gridDim.x * TEAMS) {
-    const int64_t r = base + team;
-    const bool active = r < R;
-    const uint4* xr = x + r * nvec;
-    uint4 v[kRowVPT];
-    uint32_t acc = 0;
-#pragma unroll
-    for (int i = 0; i < kRowVPT; ++i) {
-      const int c = t + i * TPR;
-      if (active && c < nvec) {
-        v[i] = ld_nc_v4(xr + c);
-        acc = absmax_vec8(acc, v[i]);
-      } else {
-        v[i] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    const uint32_t m = __reduce_max_sync(0xffffffffu, absmax_fold(acc));
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    if (t == 0) {
-      uint32_t mm = 0;
-      for (int w = 0; w < WPT; ++w) mm = max(mm, red[team * WPT + w]);
-      const Scale s = tab_scale(tab, mm);
-      sc[team] = s.s32;
-      if (active) inv[r] = s.inv32;
-    }
-    __syncthreads();
-    const float s32 = sc[team];
-    uint2* qr = q + r * nvec;
-#pragma unroll
-    for (int i = 0; i < kRowVPT; ++i) {
-      const int c = t + i * TPR;
-      if (active && c < nvec) qr[c] = quant_vec8<FMT>(v[i], s32, FMAX);
-    }
-  }
-}
-
-template <int FMT, int TPR>
-static int run_rows(const void* x, int64_t R, int nvec, void* q, float* inv, const Ctx& c) {
-  constexpr int CTA = TPR > 256 ? TPR : 256;
-  constexpr int TEAMS = CTA / TPR;
-  const int64_t need = ceil_div64(R, TEAMS);
-  const int64_t cap = (int64_t)c.sm_count * (2048 / CTA);
-  const int grid = (int)(need < cap ? need : cap);
-  quant_rows_kernel<FMT, TPR><<<grid, CTA, 0, c.stream>>>(static_cast<const uint4*>(x), R, nvec,
-                                                           static_cast<uint2*>(q), inv, scale_tab(FMT));
-  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
-}
-
-template <int FMT>
-static int rows_dispatch(const void* x, int64_t R, int nvec, void* q, float* inv, const Ctx& c) {
-  const int per = (nvec + kRowVPT - 1) / kRowVPT;  // threads needed at 8 vectors each
-  if (per <= 32) return run_rows<FMT, 32>(x, R, nvec, q, inv, c);
-  if (per <= 64) return run_rows<FMT, 64>(x, R, nvec, q, inv, c);
-  if (per <= 128) return run_rows<FMT, 128>(x, R, nvec, q, inv, c);
-  if (per <= 256) return run_rows<FMT, 256>(x, R, nvec, q, inv, c);
-  if (per <= 512) return run_rows<FMT, 512>(x, R, nvec, q, inv, c);
-  if (per <= 1024) return run_rows<FMT, 1024>(x, R, nvec, q, inv, c);
-  return FP8_ERR_UNSUPPORTED;
-}
-
-// Rowwise for rows of up to 16384 elements: a team of WPR warps (1, 2 or 4) per row. A team issues
-// all of its row's 16-byte loads at once (up to 16 per lane), folds |x|, combines its warps'
-// maxima through shared memory behind a barrier of the team alone (none for one warp), takes the
-// scale from the table (one row per team: every lane looks up the same entry), casts from
-// registers and stores 8 codes per lane and vector. Persistent teams walk the rows with a grid
-// stride, so at any time some teams load while others cast and store.
-constexpr int kRowWarpVPL = 16;
-template <int FMT, int WPR>
-__global__ void __launch_bounds__(256) quant_rows_warp_kernel(const uint4* __restrict__ x, int64_t R, int nvec,
-                                                              uint2* __restrict__ q, float* __restrict__ inv,
-                                                              const __grid_constant__ ScaleTab tab) {
-  constexpr int TPR = 32 * WPR;
-  __shared__ uint32_t red[2][8];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int team = warp / WPR, t = threadIdx.x % TPR;
-  const int64_t team0 = (int64_t)blockIdx.x * (8 / WPR) + team;
-  const int64_t nteams = (int64_t)gridDim.x * (8 / WPR);
-  int par = 0;
-  for (int64_t r = team0; r < R; r += nteams) {
-    const uint4* xr = x + r * nvec;
-    uint4 v[kRowWarpVPL];
-    uint32_t acc = 0;
-#pragma unroll
-    for (int i = 0; i < kRowWarpVPL; ++i) {
-      const int c = t + TPR * i;
-      v[i] = c < nvec ? ld_nc_v4(xr + c) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int i = 0; i < kRowWarpVPL; ++i) acc = absmax_vec8(acc, v[i]);
-    uint32_t m = __reduce_max_sync(0xffffffffu, absmax_fold(acc));
-    if (WPR > 1) {
-      if (lane == 0) red[par][warp] = m;
-      named_bar_sync(1 + team, TPR);
-#pragma unroll
-      for (int w = 0; w < WPR; ++w) m = max(m, red[par][team * WPR + w]);
-      par ^= 1;
-    }
-    const Scale sc = tab_scale(tab, m);
-    if (t == 0) inv[r] = sc.inv32;
-    uint2* qr = q + r * nvec;
-    const float2 s2 = make_float2(sc.s32, sc.s32);
-#pragma unroll
-    for (int i = 0; i < kRowWarpVPL; ++i) {
-      const int c = t + TPR * i;
-      if (c < nvec) {
-        const uint4 d = v[i];
-        float2 a = fmul2_rn(make_float2(__uint_as_float(d.x << 16), __uint_as_float(d.x & 0xFFFF0000u)), s2);
-        float2 b = fmul2_rn(make_float2(__uint_as_float(d.y << 16), __uint_as_float(d.y & 0xFFFF0000u)), s2);
-        uint2 o;
-        o.x = cvt_fp8x2<FMT>(a.x, a.y) | (cvt_fp8x2<FMT>(b.x, b.y) << 16);
-        a = fmul2_rn(make_float2(__uint_as_float(d.z << 16), __uint_as_float(d.z & 0xFFFF0000u)), s2);
-        b = fmul2_rn(make_float2(__uint_as_float(d.w << 16), __uint_as_float(d.w & 0xFFFF0000u)), s2);
-        o.y = cvt_fp8x2<FMT>(a.x, a.y) | (cvt_fp8x2<FMT>(b.x, b.y) << 16);
-        qr[c] = o;
-      }
-    }
-  }
-}
-
-template <int FMT, int WPR>
-static int run_rows_warp(const void* x, int64_t R, int nvec, void* q, float* inv, const Ctx& c) {
-  auto kern = quant_rows_warp_kernel<FMT, WPR>;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
-  // as many teams as fit at once, but no more than the rows, with the rows spread evenly
-  const int64_t slots = (int64_t)c.sm_count * per_sm * (8 / WPR);
-  const int64_t waves = ceil_div64(R, slots);
-  const int64_t teams = ceil_div64(R, waves);
-  kern<<<(unsigned)ceil_div64(teams, 8 / WPR), 256, 0, c.stream>>>(static_cast<const uint4*>(x), R, nvec,
-                                                                    static_cast<uint2*>(q), inv, scale_tab(FMT));
-  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
-}
-
-template <int FMT>
-static int rows_warp_dispatch(const void* x, int64_t R, int nvec, void* q, float* inv, const Ctx& c) {
-  if (nvec <= 32 * kRowWarpVPL) return run_rows_warp<FMT, 1>(x, R, nvec, q, inv, c);
-  if (nvec <= 64 * kRowWarpVPL) return run_rows_warp<FMT, 2>(x, R, nvec, q, inv, c);
-  return run_rows_warp<FMT, 4>(x, R, nvec, q, inv, c);
-}
-
-int launch_quant_rows(const void* x, int64_t R, int64_t C, int fmt, void* q, float* inv, const Ctx& c) {
-  if (R == 0) return FP8_OK;
-  const int nvec = (int)(C / 8);
-  if (nvec >= 64 && nvec <= 128 * kRowWarpVPL)
-    return fmt == FP8_DT_E4M3 ? rows_warp_dispatch<FP8_DT_E4M3>(x, R, nvec, q, inv, c)
-                              : rows_warp_dispatch<FP8_DT_E5M2>(x, R, nvec, q, inv, c);
-  return fmt == FP8_DT_E4M3 ? rows_dispatch<FP8_DT_E4M3>(x, R, nvec, q, inv, c)
-                            : rows_dispatch<FP8_DT_E5M2>(x, R, nvec, q, inv, c);
-}
-
-// ==========================================================================================
-// Tensorwise, phase 1: amax over the whole tensor. Grid-stride 16-byte loads, four in flight
-// per thread, warp max by redux, one relaxed atomic max per CTA on the bf16 bit pattern.
-__global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, int64_t nvec,
-                                                   uint32_t* __restrict__ amax_ws) {
-  __shared__ uint32_t red[8];
-  uint32_t acc = 0;
-  const uint64_t keep = l2_evict_last();  // the cast pass reads the tensor again
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < nvec; i += 4 * stride) {
-    const uint4 a = ld_nc_v4_hint(x + i, keep), b = ld_nc_v4_hint(x + i + stride, keep);
-    const uint4 d = ld_nc_v4_hint(x + i + 2 * stride, keep), e = ld_nc_v4_hint(x + i + 3 * stride, keep);
-    acc = absmax_vec8(acc, a);
-    acc = absmax_vec8(acc, b);
-    acc = absmax_vec8(acc, d);
-    acc = absmax_vec8(acc, e);
-  }
-  for (; i < nvec; i += stride) acc = absmax_vec8(acc, ld_nc_v4_hint(x + i, keep));
-  const uint32_t m = __reduce_max_sync(0xffffffffu, absmax_fold(acc));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t mm = 0;
-    for (int w = 0; w < 8; ++w) mm = max(mm, red[w]);
-    red_max_relaxed(amax_ws, mm);
-  }
-}
-
-// Tensorwise, phase 2: cast with the one scale; row-major output from registers and/or the
+// Tensorwise cast with a given amax (fp8_quantize_from_amax, the allocation-free variant): one scale; row-major output from registers and/or the
 // column-major output through a transposed 64 x 128 tile in shared memory (dual output from
 // one read). Tile: 128 rows x 64 columns.
 constexpr int kTcRows = 128, kTcCols = 64, kTcPitch = 132;  // pitch: 33 words, conflict-light
@@ -286,27 +73,151 @@ __global__ void __launch_bounds__(256) quant_tensor_cast_kernel(const uint16_t* 
   }
 }
 
-int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
-                        uint32_t* amax_ws, const Ctx& c) {
-  if (cudaMemsetAsync(amax_ws, 0, sizeof(uint32_t), c.stream) != cudaSuccess) return FP8_ERR_CUDA;
+// ==========================================================================================
+// Tensorwise in one launch. Every CTA is resident at once (cooperative launch), so the CTAs can
+// meet at a grid barrier between the two steps the recipe needs:
+//   amax   a grid-stride read of the whole tensor (8 independent 16-byte loads in flight per thread;
+//          the loads keep their lines in L2 for the cast), |x| folded as packed bf16 maxima, one
+//          relaxed atomic max per CTA on the workspace's amax word;
+//   barrier each CTA counts itself on the workspace's barrier word with a release increment (its
+//          atomic max is ordered before it) and waits, bounded, until all have (acquire loads);
+//   cast   the scale from the table, then the cast of the tensor read again, mostly from L2:
+//          row-major only by a grid-stride walk in the amax pass's order, 8-byte stores; with the
+//          column-major copy by 128 x 64 tiles transposed through shared memory (dual output).
+// A wait that runs out sets FP8_DEV_TIMEOUT and the CTA leaves without casting (the failure-detection
+// test hook fp8_set_test_stall makes it wait for one arrival that never comes).
+constexpr int kTfThreads = 256;
+constexpr int kTfUnroll = 8;
+
+template <int FMT>
+__global__ void __launch_bounds__(kTfThreads) quant_tensor_fused_kernel(
+    const uint16_t* __restrict__ x, int64_t R, int64_t C, uint32_t* __restrict__ ws, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ qt, float* __restrict__ inv, int32_t* status, uint64_t wait_ns, int test_stall,
+    const __grid_constant__ ScaleTab tab) {
+  constexpr float FMAX = FmtMax<FMT>::v;
+  __shared__ uint32_t red[kTfThreads / 32];
+  __shared__ float s_sc;
+  __shared__ int s_ok;
+  __shared__ __align__(16) uint8_t T[kTcCols * kTcPitch];
+  const int tid = threadIdx.x;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int64_t nvec = R * C / 8;
-  if (nvec > 0) {
-    const int64_t need = ceil_div64(nvec, 256 * 4);
-    const int64_t cap = (int64_t)c.sm_count * 8;
-    amax_kernel<<<(int)(need < cap ? need : cap), 256, 0, c.stream>>>(static_cast<const uint4*>(x), nvec, amax_ws);
-    if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
+  const int64_t stride = (int64_t)gridDim.x * kTfThreads;
+  const int64_t first = (int64_t)blockIdx.x * kTfThreads + tid;
+
+  // ---- amax ----
+  {
+    const uint64_t keep = l2_evict_last();
+    uint32_t acc = 0;
+    int64_t i = first;
+    for (; i + (kTfUnroll - 1) * stride < nvec; i += kTfUnroll * stride) {
+      uint4 v[kTfUnroll];
+#pragma unroll
+      for (int u = 0; u < kTfUnroll; ++u) v[u] = ld_nc_v4_hint(xv + i + u * stride, keep);
+#pragma unroll
+      for (int u = 0; u < kTfUnroll; ++u) acc = absmax_vec8(acc, v[u]);
+    }
+    for (; i < nvec; i += stride) acc = absmax_vec8(acc, ld_nc_v4_hint(xv + i, keep));
+    const uint32_t m = __reduce_max_sync(0xffffffffu, absmax_fold(acc));
+    if ((tid & 31) == 0) red[tid >> 5] = m;
   }
-  dim3 grid((unsigned)ceil_div64(C, kTcCols), (unsigned)ceil_div64(R, kTcRows));
-  if (grid.x == 0 || grid.y == 0) grid = dim3(1, 1);
-  if (fmt == FP8_DT_E4M3)
-    quant_tensor_cast_kernel<FP8_DT_E4M3><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_ws, 0, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
-        scale_tab(fmt));
-  else
-    quant_tensor_cast_kernel<FP8_DT_E5M2><<<grid, 256, 0, c.stream>>>(
-        static_cast<const uint16_t*>(x), R, C, amax_ws, 0, static_cast<uint8_t*>(q), static_cast<uint8_t*>(qt), inv,
-        scale_tab(fmt));
-  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+  __syncthreads();
+  // ---- grid barrier, then the scale ----
+  if (tid == 0) {
+    uint32_t mm = 0;
+    for (int w = 0; w < kTfThreads / 32; ++w) mm = max(mm, red[w]);
+    if (mm) red_max_relaxed(ws, mm);
+    red_add_release_gpu(ws + 1, 1u);
+    // the failure-detection test hook waits for one arrival more than there are CTAs
+    const bool ok = wait_count_geq(ws + 1, gridDim.x + (test_stall ? 1u : 0u), wait_ns);
+    if (!ok) set_status(status, FP8_DEV_TIMEOUT);
+    const Scale sc = tab_scale(tab, ld_relaxed_gpu(ws));
+    s_sc = sc.s32;
+    s_ok = ok;
+    if (blockIdx.x == 0 && ok) *inv = sc.inv32;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  const float s32 = s_sc;
+  const uint64_t last = l2_evict_first();  // the input's last use; output nothing re-reads soon
+
+  // ---- cast: row-major only ----
+  if (!qt) {
+    uint2* qv = reinterpret_cast<uint2*>(q);
+    int64_t i = first;
+    for (; i + (kTfUnroll - 1) * stride < nvec; i += kTfUnroll * stride) {
+      uint4 v[kTfUnroll];
+#pragma unroll
+      for (int u = 0; u < kTfUnroll; ++u) v[u] = ld_nc_v4_hint(xv + i + u * stride, last);
+#pragma unroll
+      for (int u = 0; u < kTfUnroll; ++u) st_v2_hint(qv + i + u * stride, quant_vec8<FMT>(v[u], s32, FMAX), last);
+    }
+    for (; i < nvec; i += stride) st_v2_hint(qv + i, quant_vec8<FMT>(ld_nc_v4_hint(xv + i, last), s32, FMAX), last);
+    return;
+  }
+  // ---- cast: tiles of 128 rows x 64 columns, the column-major copy through shared memory ----
+  const int64_t ncb = ceil_div64(C, kTcCols), ntiles = ceil_div64(R, kTcRows) * ncb;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t r0 = (t / ncb) * kTcRows, c0 = (t % ncb) * kTcCols;
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int vi = tid + kTfThreads * k;  // 128 rows x 8 vectors
+      const int64_t r = r0 + (vi >> 3), col = c0 + (vi & 7) * 8;
+      v[k] = (r < R && col < C) ? ld_nc_v4_hint(x + r * C + col, last) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int vi = tid + kTfThreads * k;
+      const int rr = vi >> 3, cv = vi & 7;
+      const int64_t r = r0 + rr, col = c0 + cv * 8;
+      const uint2 o = quant_vec8<FMT>(v[k], s32, FMAX);
+      if (q && r < R && col < C) st_v2_hint(q + r * C + col, o, last);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t w = j < 4 ? o.x : o.y;
+        T[(cv * 8 + j) * kTcPitch + rr] = (uint8_t)(w >> (8 * (j & 3)));
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < kTcCols * (kTcRows / 16); i += kTfThreads) {
+      const int cl = i >> 3, k = i & 7;
+      const int64_t col = c0 + cl, r = r0 + 16 * k;
+      if (col < C && r < R) {  // R % 16 == 0: the 16-byte chunk is all in range
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(T + cl * kTcPitch + 16 * k);
+        st_v4_hint(qt + col * R + r, make_uint4(src[0], src[1], src[2], src[3]), last);
+      }
+    }
+    __syncthreads();  // T is rewritten by the next tile
+  }
+}
+
+int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
+                        uint32_t* ws, const Ctx& c) {
+  // ws[0]: the amax word, ws[1]: the barrier count; both start at zero
+  if (cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), c.stream) != cudaSuccess) return FP8_ERR_CUDA;
+  auto kern = fmt == FP8_DT_E4M3 ? quant_tensor_fused_kernel<FP8_DT_E4M3> : quant_tensor_fused_kernel<FP8_DT_E5M2>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTfThreads, 0) != cudaSuccess || per_sm < 1)
+    return FP8_ERR_CUDA;
+  const int64_t nvec = R * C / 8;
+  const int64_t work = qt ? ceil_div64(R, kTcRows) * ceil_div64(C, kTcCols) : ceil_div64(nvec, kTfThreads * kTfUnroll);
+  const int64_t cap = (int64_t)c.sm_count * per_sm;
+  const unsigned grid = (unsigned)(work < 1 ? 1 : (work < cap ? work : cap));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: they meet at the grid barrier
+  attr[0].val.cooperative = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTfThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, static_cast<const uint16_t*>(x), R, C, ws, static_cast<uint8_t*>(q),
+                         static_cast<uint8_t*>(qt), inv, c.status, c.wait_ns, c.test_stall, scale_tab(fmt)) != cudaSuccess)
+    return FP8_ERR_CUDA;
+  return FP8_OK;
 }
 
 // ==========================================================================================

@@ -33,7 +33,7 @@ def test_host_helpers(fp8):
     for R, E in [(0, 1), (1, 1), (100, 3), (8192, 16), (131072, 256)]:
         P = fp8.fp8_jagged_padded_rows(R, E)
         assert P % 128 == 0 and R + 127 * E <= P < R + 127 * E + 128
-    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_TENSOR) == 4
+    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_TENSOR) == 8
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_ROW) == 0
     # one amax word per (group, column), rounded up to 16 bytes
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 16, 5120, granularity=fp8.GRAN_COL) == 16 * 5120 * 4

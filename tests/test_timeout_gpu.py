@@ -1,8 +1,10 @@
-"""Failure detection without a GPU fault: every on-device wait of the GEMM kernels is bounded.
-The test hook fp8_set_test_stall makes the MMA issuer wait on a barrier that nothing signals;
-with a short wait limit that wait runs out, and the kernel must report FP8_DEV_TIMEOUT in the
-status word, stop its other warps, drain its in-flight TMA loads and MMAs, free its tensor
-memory and return, leaving the context usable (a normal GEMM afterwards is correct)."""
+"""Failure detection without a GPU fault: every on-device wait of the GEMM kernels and of the
+tensorwise quantize's grid barrier is bounded. The test hook fp8_set_test_stall makes the GEMM's
+MMA issuer wait on a barrier that nothing signals, and the tensorwise quantize wait for one CTA
+more than it launched; with a short wait limit the wait runs out, and the kernel must report
+FP8_DEV_TIMEOUT in the status word, stop its other warps, drain its in-flight TMA loads and MMAs,
+free its tensor memory and return, leaving the context usable (a normal call afterwards is
+correct)."""
 import numpy as np
 import pytest
 import torch
@@ -51,3 +53,26 @@ def test_wait_limit_expiry_reports_timeout_and_context_survives(fp8, M, N, K):
     rows = np.arange(0, M, max(1, M // 64))
     ref, absacc = oracle.gemm_fp8(ca, oracle.E4M3, cb, oracle.E4M3, ia, ib, rows=rows)
     check_gemm(out[torch.from_numpy(rows).cuda()], ref, absacc, True)
+
+
+def test_tensorwise_barrier_expiry_reports_timeout_and_context_survives(fp8):
+    x = W.normal_bf16((1024, 2048), 1.0, 17)
+    xd = x.cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    old = fp8.fp8_set_wait_limit_ns(2_000_000)  # 2 ms
+    fp8.fp8_set_test_stall(True)
+    try:
+        fp8.quantize_alloc(xd, fp8.GRAN_TENSOR, fp8.DT_E4M3, layout=fp8.LAYOUT_BOTH, status=st)
+        torch.cuda.synchronize()
+    finally:
+        fp8.fp8_set_test_stall(False)
+        fp8.fp8_set_wait_limit_ns(old)
+    assert int(st.item()) & fp8.DEV_TIMEOUT
+    st.zero_()
+    q, qt, inv = fp8.quantize_alloc(xd, fp8.GRAN_TENSOR, fp8.DT_E4M3, layout=fp8.LAYOUT_BOTH, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    qo, io = oracle.quantize_tensor(bits(x), oracle.E4M3)
+    assert np.array_equal(q.view(torch.uint8).cpu().numpy(), qo)
+    assert np.array_equal(qt.view(torch.uint8).cpu().numpy(), qo.T)
+    assert np.array_equal(inv.cpu().numpy().view(np.uint32), io.view(np.uint32))
