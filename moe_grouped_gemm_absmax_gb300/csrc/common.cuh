@@ -220,7 +220,7 @@ FP8_DEVI bool wait_count_geq(const uint32_t* p, uint32_t target, uint64_t limit_
   uint32_t ns = 32;
   for (;;) {
     __nanosleep(ns);
-    if (ns < 512) ns <<= 1;
+    if (ns < 128) ns <<= 1;
     if (ld_acquire_gpu(p) >= target) return true;
     if (globaltimer() - t0 > limit_ns) return false;
   }
@@ -230,6 +230,9 @@ FP8_DEVI bool wait_count_geq(const uint32_t* p, uint32_t target, uint64_t limit_
 // mbarrier
 FP8_DEVI void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+FP8_DEVI void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 FP8_DEVI void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 FP8_DEVI void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

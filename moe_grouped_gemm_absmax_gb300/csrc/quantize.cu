@@ -155,17 +155,26 @@ __global__ void __launch_bounds__(kTfThreads) quant_tensor_fused_kernel(
     for (; i < nvec; i += stride) st_v2_hint(qv + i, quant_vec8<FMT>(ld_nc_v4_hint(xv + i, last), s32, FMAX), last);
     return;
   }
-  // ---- cast: tiles of 128 rows x 64 columns, the column-major copy through shared memory ----
+  // ---- cast: tiles of 128 rows x 64 columns, the column-major copy through shared memory; the
+  // next tile's loads are in flight while the current one is cast, transposed and stored ----
   const int64_t ncb = ceil_div64(C, kTcCols), ntiles = ceil_div64(R, kTcRows) * ncb;
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  auto load_tile = [&](int64_t t, uint4* v) {
     const int64_t r0 = (t / ncb) * kTcRows, c0 = (t % ncb) * kTcCols;
-    uint4 v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int vi = tid + kTfThreads * k;  // 128 rows x 8 vectors
       const int64_t r = r0 + (vi >> 3), col = c0 + (vi & 7) * 8;
       v[k] = (r < R && col < C) ? ld_nc_v4_hint(x + r * C + col, last) : make_uint4(0, 0, 0, 0);
     }
+  };
+  uint4 nx[4];
+  if ((int64_t)blockIdx.x < ntiles) load_tile(blockIdx.x, nx);
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t r0 = (t / ncb) * kTcRows, c0 = (t % ncb) * kTcCols;
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = nx[k];
+    if (t + gridDim.x < ntiles) load_tile(t + gridDim.x, nx);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int vi = tid + kTfThreads * k;
@@ -242,14 +251,16 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 //              32-code rows of the transposed box (64 columns x 32 rows) in the warp's own
 //              staging buffer, and the warp's elected lane stores the box by TMA (two alternating
 //              buffers per warp), so the warps never wait on one another. Pass 2 walks the unit order backwards, so
-//              its first reads are the tiles pass 1 read last, still in L2.
-// The passes are stream-ordered launches: no CTA waits on another.
+//              its first reads are the tiles pass 1 read last.
+// Both passes run in one launch: every CTA is resident (cooperative launch), and between the passes
+// each CTA counts itself on the workspace's barrier word (release) and waits, bounded, until all
+// have, so every column maximum is complete before pass 2 reads it. Pass 1's loads keep their lines
+// in L2 and pass 2 re-reads them right after the barrier, mostly from L2. With the maxima given
+// (fp8_quantize_from_amax) the launch runs pass 2 alone.
 constexpr int kColThreads = 256;
 constexpr int kColNB = 2;                  // 128-row blocks per work unit (256 rows)
 constexpr int kColTile = 128 * kColNB;
-constexpr int kColStagesMax = 6;  // ring stages: 6 in pass 1, 5 in pass 2 (its staging boxes take the rest)
-template <bool CAST>
-constexpr int col_stages() { return CAST ? 5 : 6; }
+constexpr int kColStages = 5;  // ring stages (pass 2's staging boxes take the rest of shared memory)
 constexpr int kColStageBytes = kColTile * 128;         // 256 rows x 64 bf16
 constexpr int kColOutBytes = (kColTile / 128) * 8192;  // 64 columns x 256 rows of codes
 constexpr int kColWarpBox = 64 * 32;                   // pass 2: one warp's 64 columns x 32 rows of codes
@@ -271,6 +282,9 @@ struct ColParams {
   int64_t n_strips;
   uint64_t wait_ns;
   int mode;            // 0: 2-D [C, R] output; 1: batched [B, C, R]; 2: segments [C, P]
+  int first_pass;      // 0: both passes; 1: pass 2 alone (maxima given)
+  uint32_t* barrier;   // grid-barrier count between the passes (zeroed by the launcher)
+  int test_stall;      // failure-detection test hook: the barrier waits for one arrival more
 };
 
 struct ColUnit {
@@ -380,30 +394,25 @@ struct ColInfo {
   int32_t g, c0, rt, valid, wrows, pstart;  // group, first column, tile start, rows of the group, rows written
 };
 struct ColShared {
-  uint64_t full[kColStagesMax];   // the tile landed (TMA bytes) and the info was written
-  uint64_t scl[kColStagesMax];    // pass 2: the stage's 64 amax words landed (32 async arrivals)
-  uint64_t empty[kColStagesMax];  // the consumer warps are done with the stage
-  ColInfo info[kColStagesMax];
-  uint32_t am[kColStagesMax][64];  // pass 2: the amax words of the stage's 64 columns
+  uint64_t full[kColStages];   // the tile landed (TMA bytes) and the info was written
+  uint64_t scl[kColStages];    // pass 2: the stage's 64 amax words landed (32 async arrivals)
+  uint64_t empty[kColStages];  // the consumer warps are done with the stage
+  ColInfo info[kColStages];
+  uint32_t am[kColStages][64];  // pass 2: the amax words of the stage's 64 columns
   uint32_t red[kColConsumerWarps][8][4];
   int abort;
 };
-template <bool CAST>
-struct ColSmem {
-  static constexpr int bytes =
-      1024 + col_stages<CAST>() * kColStageBytes + (CAST ? 2 * kColOutBytes : 0) + (int)sizeof(ColShared);
-};
+constexpr int kColSmemBytes = 1024 + kColStages * kColStageBytes + 2 * kColOutBytes + (int)sizeof(ColShared);
 
-template <int FMT, bool CAST>
+template <int FMT>
 __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __grid_constant__ CUtensorMap tm_in,
                                                                         const __grid_constant__ CUtensorMap tm_out,
                                                                         const ColParams p,
                                                                         const __grid_constant__ ScaleTab tab) {
   extern __shared__ uint8_t smem_raw[];
-  constexpr int kColStages = col_stages<CAST>();
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Tout = ring + kColStages * kColStageBytes;
-  ColShared& S = *reinterpret_cast<ColShared*>(Tout + (CAST ? 2 * kColOutBytes : 0));
+  ColShared& S = *reinterpret_cast<ColShared*>(Tout + 2 * kColOutBytes);
   int32_t* upre = reinterpret_cast<int32_t*>(&S + 1);
   int32_t* ppre = upre + (p.n_groups + 1);
   const int64_t M = col_setup(p, upre, ppre);
@@ -411,24 +420,25 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the scale table in shared memory: the lanes of a warp look up different entries at once
   __shared__ ScaleTab stab;
-  if (CAST) {
-    static_assert(sizeof(ScaleTab) % 4 == 0, "table words");
-    for (int i = tid; i < (int)(sizeof(ScaleTab) / 4); i += blockDim.x)
-      reinterpret_cast<uint32_t*>(&stab)[i] = reinterpret_cast<const uint32_t*>(&tab)[i];
-  }
-  if (tid == 0) {
+  static_assert(sizeof(ScaleTab) % 4 == 0, "table words");
+  for (int i = tid; i < (int)(sizeof(ScaleTab) / 4); i += blockDim.x)
+    reinterpret_cast<uint32_t*>(&stab)[i] = reinterpret_cast<const uint32_t*>(&tab)[i];
+  auto init_barriers = [&]() {
     for (int s = 0; s < kColStages; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.scl[s], 32);
       mbar_init(&S.empty[s], kColConsumerWarps);
     }
-    S.abort = 0;
     fence_mbar_init();
+  };
+  if (tid == 0) {
+    init_barriers();
+    S.abort = 0;
     tma_prefetch_desc(&tm_in);
-    if (CAST) tma_prefetch_desc(&tm_out);
+    tma_prefetch_desc(&tm_out);
   }
   // Groups without rows have no units: their inverse scales (amax 0) are written here.
-  if (CAST && blockIdx.x == 0) {
+  if (blockIdx.x == 0) {
     const Scale s0 = tab_scale(tab, 0u);
     for (int64_t g = 0; g < p.n_groups; ++g) {
       const int64_t n = p.mode == 2 ? p.ends[g] - (g ? p.ends[g - 1] : 0) : p.group_rows;
@@ -441,11 +451,38 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
   // time (DRAM pages stay open); pass 2 walks the order backwards, its first reads being the
   // units pass 1 read last, still in L2
   const int64_t cnt = (int64_t)blockIdx.x < M ? (M - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  volatile int* cta_abort = &S.abort;
+
+  for (int pass = p.first_pass; pass < 2; ++pass) {
+  const bool CAST = pass == 1;
+  if (CAST && p.first_pass == 0) {
+    // between the passes: every CTA's column maxima are complete before any CTA reads one
+    __syncthreads();
+    if (tid == 0) {
+      if (!*cta_abort) {
+        __threadfence();
+        red_add_release_gpu(p.barrier, 1u);
+        if (!wait_count_geq(p.barrier, gridDim.x + (p.test_stall ? 1u : 0u), p.wait_ns)) {
+          *cta_abort = 1;
+          set_status(p.status, FP8_DEV_TIMEOUT);
+        }
+      }
+      if (!*cta_abort) {  // every load of pass 1 was consumed: fresh barriers for pass 2
+        for (int s = 0; s < kColStages; ++s) {
+          mbar_inval(&S.full[s]);
+          mbar_inval(&S.scl[s]);
+          mbar_inval(&S.empty[s]);
+        }
+        init_barriers();
+      }
+    }
+    __syncthreads();
+    if (*cta_abort) break;
+  }
   auto unit_at = [&](int64_t k) {
     const int64_t i = blockIdx.x + k * gridDim.x;
     return CAST ? M - 1 - i : i;
   };
-  volatile int* cta_abort = &S.abort;
 
   if (warp == 0) {
     // ==================== producer warp: one lane issues the tiles by TMA ====================
@@ -678,11 +715,12 @@ __global__ void __launch_bounds__(kColThreads + 64, 1) colstream_kernel(const __
     }
     if (lane == 0) bulk_wait_all();
   }
+  }  // passes
   __syncthreads();
 }
 
 // Workspace words of a column quantize: the amax per (group, column), rounded to 16 bytes.
-int64_t col_ws_words(int64_t groups, int64_t C) { return round_up64(groups * C, 4); }
+int64_t col_ws_words(int64_t groups, int64_t C) { return round_up64(groups * C, 4) + 4; }  // + the barrier count
 
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
                       const int32_t* ends, int fmt, void* out_t, int64_t ld_out, float* inv, uint32_t* scratch,
@@ -702,6 +740,7 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   p.status = c.status;
   p.wait_ns = c.wait_ns;
   p.mode = ends ? 2 : (n_groups > 1 ? 1 : 0);
+  p.test_stall = c.test_stall;
 
   CUtensorMap tout, tin;
   int rc;
@@ -729,8 +768,11 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   if (amax_given) {
     p.scratch = const_cast<uint32_t*>(amax_given);  // read only (pass 2)
     p.amax_shift = 16;
-  } else if (cudaMemsetAsync(scratch, 0, (size_t)col_ws_words(n_groups, C) * 4, c.stream) != cudaSuccess) {
-    return FP8_ERR_CUDA;
+    p.first_pass = 1;
+  } else {
+    if (cudaMemsetAsync(scratch, 0, (size_t)col_ws_words(n_groups, C) * 4, c.stream) != cudaSuccess) return FP8_ERR_CUDA;
+    p.first_pass = 0;
+    p.barrier = scratch + round_up64(n_groups * C, 4);
   }
   // units: exact for dense modes; for segments an upper bound (each segment adds at most one
   // partial tile) -- the kernels compute the exact count from the offsets
@@ -740,22 +782,22 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   const size_t pre = p.mode == 2 ? 12 * (size_t)(n_groups + 1) : 0;
   const int64_t grid = units > 0 ? (units < c.sm_count ? units : c.sm_count) : 1;
   const ScaleTab& tab = scale_tab(fmt);
-  // pass 1: column maxima (skipped when the caller supplies them)
-  if (units > 0 && !amax_given) {
-    auto k1 = fmt == FP8_DT_E4M3 ? colstream_kernel<FP8_DT_E4M3, false> : colstream_kernel<FP8_DT_E5M2, false>;
-    const size_t smem = ColSmem<false>::bytes + pre;
-    if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return FP8_ERR_CUDA;
-    k1<<<(unsigned)grid, kColThreads + 64, smem, c.stream>>>(tin, tout, p, tab);
-    if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
-  }
-  // pass 2: scales and cast (also writes the scales of groups without rows)
-  auto k2 = fmt == FP8_DT_E4M3 ? colstream_kernel<FP8_DT_E4M3, true> : colstream_kernel<FP8_DT_E5M2, true>;
-  const size_t smem2 = ColSmem<true>::bytes + pre;
-  if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
+  auto kern = fmt == FP8_DT_E4M3 ? colstream_kernel<FP8_DT_E4M3> : colstream_kernel<FP8_DT_E5M2>;
+  const size_t smem = kColSmemBytes + pre;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FP8_ERR_CUDA;
-  k2<<<(unsigned)grid, kColThreads + 64, smem2, c.stream>>>(tin, tout, p, tab);
-  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: they meet between the passes
+  attr[0].val.cooperative = 1;
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kColThreads + 64);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tin, tout, p, tab) != cudaSuccess) return FP8_ERR_CUDA;
+  return FP8_OK;
 }
 
 }  // namespace fp8lin

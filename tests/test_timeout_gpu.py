@@ -1,7 +1,7 @@
 """Failure detection without a GPU fault: every on-device wait of the GEMM kernels and of the
-tensorwise quantize's grid barrier is bounded. The test hook fp8_set_test_stall makes the GEMM's
-MMA issuer wait on a barrier that nothing signals, and the tensorwise quantize wait for one CTA
-more than it launched; with a short wait limit the wait runs out, and the kernel must report
+grid barriers of the tensorwise and column-wise quantize is bounded. The test hook
+fp8_set_test_stall makes the GEMM's MMA issuer wait on a barrier that nothing signals, and the
+quantize kernels' grid barriers wait for one CTA more than they launched; with a short wait limit the wait runs out, and the kernel must report
 FP8_DEV_TIMEOUT in the status word, stop its other warps, drain its in-flight TMA loads and MMAs,
 free its tensor memory and return, leaving the context usable (a normal call afterwards is
 correct)."""
@@ -75,4 +75,37 @@ def test_tensorwise_barrier_expiry_reports_timeout_and_context_survives(fp8):
     qo, io = oracle.quantize_tensor(bits(x), oracle.E4M3)
     assert np.array_equal(q.view(torch.uint8).cpu().numpy(), qo)
     assert np.array_equal(qt.view(torch.uint8).cpu().numpy(), qo.T)
+    assert np.array_equal(inv.cpu().numpy().view(np.uint32), io.view(np.uint32))
+
+
+@pytest.mark.parametrize("counts", [None, [300, 0, 700, 24]])  # dense, jagged segments
+def test_colwise_barrier_expiry_reports_timeout_and_context_survives(fp8, counts):
+    R, C = 1024, 512
+    x = W.column_gain_bf16((R, C), 1e-3, -2, 2, seed=23)
+    xd = x.cuda()
+    offs = torch.tensor(W.ends_from_counts(counts), device="cuda") if counts else None
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    old = fp8.fp8_set_wait_limit_ns(2_000_000)  # 2 ms
+    fp8.fp8_set_test_stall(True)
+    try:
+        fp8.quantize_alloc(xd, fp8.GRAN_COL, fp8.DT_E5M2, offsets=offs, status=st)
+        torch.cuda.synchronize()
+    finally:
+        fp8.fp8_set_test_stall(False)
+        fp8.fp8_set_wait_limit_ns(old)
+    assert int(st.item()) & fp8.DEV_TIMEOUT
+    st.zero_()
+    _, qt, inv = fp8.quantize_alloc(xd, fp8.GRAN_COL, fp8.DT_E5M2, offsets=offs, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    if counts is None:
+        qo, io = oracle.quantize_cols(bits(x), oracle.E5M2)
+        assert np.array_equal(qt.view(torch.uint8).cpu().numpy(), qo.T)
+    else:
+        ends = W.ends_from_counts(counts)
+        qo, io = oracle.quantize_jagged_cols(bits(x), ends, oracle.E5M2)
+        from tests.gpu_util import segpad_cols
+        used = sum(-(-c // 128) * 128 for c in counts)
+        got = qt.view(torch.uint8).cpu().numpy()
+        assert np.array_equal(got[:, :used], segpad_cols(qo, ends, qt.shape[1])[:, :used])
     assert np.array_equal(inv.cpu().numpy().view(np.uint32), io.view(np.uint32))
