@@ -191,9 +191,8 @@ typedef struct fp8_tensor {
  *  workspace   device memory, 16-byte aligned, of fp8_workspace_size(FP8_OP_QUANTIZE, groups,
  *              C, granularity) bytes: 8 bytes for tensor granularity (the amax word and a
  *              grid-barrier count); for column granularity 4 bytes per (group, column) for the
- *              column maxima, rounded up to 16 bytes, plus 4 bytes per 64 columns (completion
- *              counts of the kernel's column chunks), rounded up to 16 bytes (groups = B for 3-D
- *              x, E with offsets, else 1); C <= 65536; 0 for row
+ *              column maxima, rounded up to 16 bytes, plus 16 bytes for a grid-barrier count
+ *              (groups = B for 3-D x, E with offsets, else 1); 0 for row
  *              granularity (workspace may then be NULL). MX: 4 * (E + 1) bytes rounded up to
  *              16 with offsets (the padded segment starts), else 0. Calls sharing a workspace must be
  *              stream-ordered: the quantize clears and uses it.

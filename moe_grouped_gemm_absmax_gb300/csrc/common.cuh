@@ -344,12 +344,6 @@ FP8_DEVI void cp_async4(void* smem_dst, const void* gsrc, bool valid) {
                "r"(valid ? 4 : 0)
                : "memory");
 }
-// Asynchronous 16-byte copy global -> shared through L2 only (no L1 allocation), `src_bytes`
-// (0..16) of them read and the rest zero-filled; both addresses 16-byte aligned.
-FP8_DEVI void cp_async16_cg(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(src_bytes)
-               : "memory");
-}
 FP8_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // The mbarrier receives one arrival from this thread once all of its earlier cp.async copies have
 // landed (the barrier's expected count includes that arrival).
