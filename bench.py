@@ -850,6 +850,48 @@ class FusedAmaxStep(Step):
         f.fp8_quantize(self.dx, f.GRAN_COL, f.DT_E5M2, f.LAYOUT_COL_MAJOR, None, self.dxt, self.dxti, None, self.ws)
 
 
+class FusedQuantOutStep(Step):
+    """The forward GEMM of the Llama3-8B MLP-up Linear, y = x W^T (rowwise FP8 operands, quantized
+    outside the timed region), whose epilogue writes y already quantized for the next layer: e4m3
+    codes with 1 x 128 block scales (the blockwise recipe's activation operand). `alt_run` is the
+    unfused chain timed in the same run: the GEMM with a bf16 output, then the 1 x 128 quantize of
+    it (the same codes and scales bit for bit)."""
+    dtype = "fp8 e4m3 (fp32 accumulate), e4m3 1x128 output"
+
+    def __init__(self, fp8, seed=0, device="cuda"):
+        self.fp8 = fp8
+        self.name = "llama3-8b-fwd-quant-fused"
+        d = W.WORKLOADS[self.name].dims
+        M, K, N = d["M"], d["K"], d["N"]
+        self.M, self.K, self.N = M, K, N
+        x, w, _ = W.linear_inputs(M, K, N, seed=seed, device=device, outliers=True)
+        self.xq, _, self.xi = fp8.quantize_alloc(x, fp8.GRAN_ROW, fp8.DT_E4M3)
+        self.wq, _, self.wi = fp8.quantize_alloc(w, fp8.GRAN_ROW, fp8.DT_E4M3)
+        del x, w
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.yq = torch.empty((M, N), dtype=torch.float8_e4m3fn, device=device)
+        self.yi = torch.empty((M, N // 128), device=device)
+        f = 2.0 * M * N * K
+        self.kernels = [("gemm_fp8 fwd, output quantized 1x128 in the epilogue", "tensor", f, "fp8")]
+        self.alt_kernels = [("gemm_fp8 fwd (bf16 output)", "tensor", f, "fp8"),
+                            ("blk_quantize y e4m3 1x128", "hbm", 3 * M * N + 4 * M * (N // 128), "hbm")]
+
+    def total_units(self):
+        return 2.0 * self.M * self.N * self.K
+
+    def run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_scaled_mm_quant(self.xq, self.wq, self.xi, self.wi, self.yq, self.yi, f.GRAN_BLOCK_1x128, f.MM_FAST_ACCUM)
+
+    def alt_run(self, mark=lambda s: None):
+        f = self.fp8
+        mark(0)
+        f.fp8_scaled_mm(self.xq, self.wq, self.xi, self.wi, self.y, f.MM_FAST_ACCUM)
+        mark(1)
+        f.fp8_quantize(self.y, f.GRAN_BLOCK_1x128, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.yq, None, self.yi)
+
+
 class DenseBlockwiseLinearStep(DenseLinearStep):
     """Linear fwd+bwd with blockwise scaling: x and dY in 1 x 128 tiles, W in 128 x 128 tiles
     (both layouts from one read); fwd and dX blockwise FP8 GEMMs, dW in bf16."""
@@ -939,6 +981,8 @@ def make_step(fp8, name):
         return MoeFwdBwdMxStep(fp8)
     if name == "llama3-8b-dx-colquant-fused":
         return FusedAmaxStep(fp8)
+    if name == "llama3-8b-fwd-quant-fused":
+        return FusedQuantOutStep(fp8)
     if name == "llama3-8b-mlp-up-blockwise":
         return DenseBlockwiseLinearStep(fp8, 8192, 4096, 14336)
     raise SystemExit(f"unknown workload {name}")

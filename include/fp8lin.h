@@ -263,6 +263,26 @@ int fp8_scaled_mm_amax(const fp8_tensor* A, const fp8_tensor* B, const fp8_tenso
                        fp8_tensor* col_amax, int32_t* d_status, void* stream);
 
 /*
+ * fp8_scaled_mm_quant — fp8_scaled_mm whose epilogue writes the NEXT quantization of its result
+ * instead of the result itself ([T] Level 1: the quantize fused into the producing kernel, no bf16
+ * round trip through HBM). The result out[m, n] = sA[m] sB[n] sum_k A[m, k] B[n, k] is rounded once
+ * to bf16 (exactly what fp8_scaled_mm stores in a bf16 output), then quantized along its rows:
+ *  out_granularity FP8_GRAN_BLOCK_1x128 ([B]): one scale per row and 128 columns by the recipe [Q];
+ *                  out_scales fp32 [M, N / 128] inverse scales.
+ *                  FP8_GRAN_MX ([MX]): blocks of 32 columns with E8M0 scales; out_scales E8M0
+ *                  bytes fp8_mx_scale_bytes(M, N) in the MX scale layout (rows M, contraction N),
+ *                  16-byte aligned.
+ *  out_q           FP8 (E4M3 or E5M2) [M, N] row-major codes.
+ *  A, B, sA, sB, flags as fp8_scaled_mm with FP8 operands and fp32 tensor / row scales
+ *  (FP8_MM_FAST_ACCUM only). N % 128 == 0.
+ * The codes and scales are bit-identical to fp8_scaled_mm with a bf16 output followed by
+ * fp8_quantize (FP8_GRAN_BLOCK_1x128 or FP8_GRAN_MX, ROW_MAJOR) of that output. No workspace.
+ */
+int fp8_scaled_mm_quant(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA,
+                        const fp8_tensor* sB, int flags, int out_granularity, fp8_tensor* out_q,
+                        fp8_tensor* out_scales, int32_t* d_status, void* stream);
+
+/*
  * fp8_quantize_from_amax — the scale and cast steps of fp8_quantize ([Q] section 2) with the amax
  * step given: amax fp32 [1] (FP8_GRAN_TENSOR; ROW_MAJOR, COL_MAJOR or BOTH) or [C] (FP8_GRAN_COL,
  * COL_MAJOR), holding bf16 values (the maxima of a bf16 tensor always are). x bf16 [R, C]; the

@@ -85,6 +85,7 @@ def _load():
     L.fp8_quantize_from_amax.argtypes = [T, ctypes.c_int, ctypes.c_int, ctypes.c_int, T, T, T, T, P, P]
     L.fp8_set_test_stall.argtypes = [ctypes.c_int]
     L.fp8_test_cast_bits.argtypes = [ctypes.c_uint32, ctypes.c_int64, ctypes.c_int, P, P]
+    L.fp8_scaled_mm_quant.argtypes = [T, T, T, T, ctypes.c_int, ctypes.c_int, T, T, P, P]
     L.fp8_set_test_stall.restype = ctypes.c_int
     return L
 
@@ -95,7 +96,7 @@ lib = _load()
 EXPORTS = ("fp8_quantize", "fp8_scaled_mm", "fp8_grouped_mm", "fp8_linear_fwd", "fp8_linear_bwd",
            "fp8_workspace_size", "fp8_jagged_padded_rows", "fp8_status_string", "fp8_set_wait_limit_ns",
            "fp8_quantize_tensor_noalloc", "fp8_set_test_stall", "fp8_mx_scale_bytes", "fp8_scaled_mm_amax",
-           "fp8_quantize_from_amax", "fp8_test_cast_bits")
+           "fp8_quantize_from_amax", "fp8_test_cast_bits", "fp8_scaled_mm_quant")
 
 
 def status_string(code: int) -> str:
@@ -158,6 +159,15 @@ def fp8_scaled_mm_amax(A, B, sA, sB, out, flags=0, row_amax=None, col_amax=None,
     rc = lib.fp8_scaled_mm_amax(_ref(desc(A)), _ref(desc(B)), _ref(desc(sA)), _ref(desc(sB)), _ref(desc(out)), flags,
                                 _ref(desc(row_amax)), _ref(desc(col_amax)), _ptr(status), _stream(stream))
     _check(rc, "fp8_scaled_mm_amax")
+
+
+def fp8_scaled_mm_quant(A, B, sA, sB, out_q, out_scales, out_granularity, flags=0, status=None, stream=None):
+    """fp8_scaled_mm whose epilogue writes the result's next quantization: codes out_q [M, N] and
+    1 x 128 (fp32 [M, N/128]) or MX (E8M0 bytes) scales out_scales."""
+    sdt = DT_E8M0 if out_granularity == GRAN_MX else None
+    rc = lib.fp8_scaled_mm_quant(_ref(desc(A)), _ref(desc(B)), _ref(desc(sA)), _ref(desc(sB)), flags, out_granularity,
+                                 _ref(desc(out_q)), _ref(desc(out_scales, sdt)), _ptr(status), _stream(stream))
+    _check(rc, "fp8_scaled_mm_quant")
 
 
 def fp8_quantize_from_amax(x, granularity, out_dtype, layout, out=None, out_t=None, inv_scales=None, amax=None,

@@ -468,6 +468,58 @@ extern "C" int fp8_scaled_mm_amax(const fp8_tensor* A, const fp8_tensor* B, cons
   return scaled_mm_impl(A, B, sA, sB, out, flags, c, ra, ca, whole);
 }
 
+extern "C" int fp8_scaled_mm_quant(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA,
+                                   const fp8_tensor* sB, int flags, int out_granularity, fp8_tensor* out_q,
+                                   fp8_tensor* out_scales, int32_t* d_status, void* stream) {
+  Ctx c;
+  FP8_TRY(make_ctx(&c, stream, d_status));
+  FP8_CHECK(valid_desc(A) && valid_desc(B) && valid_desc(sA) && valid_desc(sB) && valid_desc(out_q) &&
+                valid_desc(out_scales) && A->ndim == 2 && B->ndim == 2 && out_q->ndim == 2,
+            FP8_ERR_INVALID_ARG);
+  FP8_CHECK(is_fp8(A->dtype) && is_fp8(B->dtype) && is_fp8(out_q->dtype), FP8_ERR_INVALID_ARG);
+  FP8_CHECK(!(A->dtype == FP8_DT_E5M2 && B->dtype == FP8_DT_E5M2), FP8_ERR_UNSUPPORTED);
+  FP8_CHECK((flags & (FP8_MM_A_MN_MAJOR | FP8_MM_B_MN_MAJOR | FP8_MM_BLOCKWISE)) == 0, FP8_ERR_UNSUPPORTED);
+  FP8_CHECK(sA->dtype == FP8_DT_F32 && sB->dtype == FP8_DT_F32, FP8_ERR_INVALID_ARG);
+  const int64_t M = A->shape[0], K = A->shape[1], N = B->shape[0];
+  FP8_CHECK(B->shape[1] == K && shape_is(out_q, 2, M, N), FP8_ERR_INVALID_ARG);
+  const int64_t la = numel(sA), lb = numel(sB);
+  FP8_CHECK((la == 1 || la == M) && (lb == 1 || lb == N), FP8_ERR_INVALID_ARG);
+  FP8_CHECK(K % 16 == 0 && aligned16(A->ptr) && aligned16(B->ptr) && aligned16(out_q->ptr), FP8_ERR_ALIGNMENT);
+  FP8_CHECK(N % 128 == 0, FP8_ERR_UNSUPPORTED);  // whole 128-column row segments per epilogue lane
+  FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
+  int mx = 0;
+  if (out_granularity == FP8_GRAN_BLOCK_1x128) {
+    FP8_CHECK(out_scales->dtype == FP8_DT_F32 && numel(out_scales) == M * (N / 128), FP8_ERR_INVALID_ARG);
+  } else if (out_granularity == FP8_GRAN_MX) {
+    FP8_CHECK(out_scales->dtype == FP8_DT_E8M0 && numel(out_scales) == mx_scale_bytes(M, N), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(aligned16(out_scales->ptr), FP8_ERR_ALIGNMENT);
+    mx = 1;
+  } else {
+    return FP8_ERR_UNSUPPORTED;
+  }
+  if (M == 0 || N == 0) return FP8_OK;
+  GemmArgs g = {};
+  g.A = A->ptr;
+  g.B = B->ptr;
+  g.a_dtype = A->dtype;
+  g.b_dtype = B->dtype;
+  g.sA = static_cast<const float*>(sA->ptr);
+  g.sB = static_cast<const float*>(sB->ptr);
+  g.sA_len = la;
+  g.sB_len = lb;
+  g.out = nullptr;
+  g.out_dtype = FP8_DT_BF16;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.mode = -1;
+  g.q_out = out_q->ptr;
+  g.q_scales = out_scales->ptr;
+  g.q_mx = mx;
+  g.q_fmt = out_q->dtype;
+  return launch_gemm(g, c);
+}
+
 extern "C" int fp8_quantize_from_amax(const fp8_tensor* x, int granularity, int out_dtype, int layout,
                                       fp8_tensor* out, fp8_tensor* out_t, fp8_tensor* inv_scales,
                                       const fp8_tensor* amax, int32_t* d_status, void* stream) {

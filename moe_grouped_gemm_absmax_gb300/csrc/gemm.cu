@@ -46,9 +46,11 @@ constexpr int kStageOut = 4096;  // per epilogue warp: output staging for TMA st
 // under running hardware.
 constexpr uint64_t kDrainNs = 2000000000ull;
 
-// kDenseAmax: the dense schedule whose epilogue also folds max |out| into the side outputs
-enum { kDense = 0, kJagM = 1, kJagK = 2, kDenseAmax = 3 };
-constexpr bool is_dense(int sched) { return sched == kDense || sched == kDenseAmax; }
+// kDenseAmax: the dense schedule whose epilogue also folds max |out| into the side outputs;
+// kDenseQuant: the dense schedule whose epilogue writes the next quantization of the (bf16) result:
+// FP8 codes and 1 x 128 or MX scales along the rows
+enum { kDense = 0, kJagM = 1, kJagK = 2, kDenseAmax = 3, kDenseQuant = 4 };
+constexpr bool is_dense(int sched) { return sched == kDense || sched == kDenseAmax || sched == kDenseQuant; }
 // kBLK: FP8 operands with blockwise scales (A: 1 x 128 tiles, B: 128 x 128 tiles); the MMAs of
 // each 128-deep K block go to a fresh tensor-memory partial, which the epilogue warps scale by
 // sA[m, kb] * sB[n / 128, kb] and add into register accumulators ("promotion")
@@ -115,6 +117,13 @@ struct GemmParams {
   uint32_t idesc;
   int32_t* status;
   uint64_t wait_ns;
+  // kDenseQuant: the result's quantization (codes [M, N] row-major in q_fmt; scales: fp32 [M, N / 128]
+  // for 1 x 128 blocks, or E8M0 bytes in the MX scale layout for rows M, contraction N)
+  uint8_t* q_out;
+  void* q_scales;
+  int q_mx;
+  int q_fmt;
+  ScaleTab q_tab;
 };
 
 struct Tile {
@@ -936,6 +945,87 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
       }
       const float sb_all = (KIND == kFP8 && p.sb_scalar) ? sb_mine : 1.0f;
       const uint32_t taddr = tmem_base + (uint32_t)(buf * TBN + c0) + ((uint32_t)(q * 32) << 16);
+      if constexpr (SCHED == kDenseQuant) {
+        // The next quantization from the epilogue ("Triton Kernel Optimization", Level 1): this
+        // lane holds row m's tile columns c0 .. c0 + 127. They are scaled and rounded once to bf16
+        // (the result as fp8_scaled_mm stores it), the accumulator goes back to the MMAs, and the
+        // bf16 values are quantized along the row: one 1 x 128 block (scale by the recipe's table)
+        // or four MX blocks of 32 (E8M0 scales). Codes leave as the row's 128 bytes; the scales
+        // beside them.
+        static_assert(C::WCOLS == 128, "one 128-column row segment per lane");
+        uint32_t h[64];
+        const float2 sa2 = make_float2(sa, sa);
+        uint32_t v[32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          tmem_ld32(taddr + ch * 32, v);
+          tmem_ld_wait_regs(v);
+          const int cl = c0 + ch * 32;
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 sb2 = stage_sb ? *reinterpret_cast<const float2*>(sbs + cl + j) : make_float2(sb_all, sb_all);
+            const float2 x = fmul2_rn(fmul2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sa2), sb2);
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(x.x, x.y);
+            h[ch * 16 + j / 2] = *reinterpret_cast<const uint32_t*>(&hb);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (CG == 2)
+            mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&S.tempty[buf]), 0));
+          else
+            mbar_arrive_relaxed(&S.tempty[buf]);
+        }
+        if (++buf == 2) {
+          buf = 0;
+          aphase ^= 1;
+        }
+        const int64_t n0 = T.n0 + c0;
+        if (!row_ok || n0 >= p.N) continue;  // N % 128 == 0: the segment is all in range or all out
+        const bool e4 = p.q_fmt == FP8_DT_E4M3;
+        uint32_t qw[32];
+        if (p.q_mx) {
+          uint32_t codes = 0;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            uint32_t am = 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) am = absmax2(am, h[16 * b + j]);
+            const uint32_t code = e4 ? mx_code<FP8_DT_E4M3>(absmax_fold(am)) : mx_code<FP8_DT_E5M2>(absmax_fold(am));
+            const float inv = mx_inv(code);
+            codes |= code << (8 * b);
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              const uint32_t lo = e4 ? mx_cast2<FP8_DT_E4M3>(h[16 * b + j], inv) : mx_cast2<FP8_DT_E5M2>(h[16 * b + j], inv);
+              const uint32_t hi = e4 ? mx_cast2<FP8_DT_E4M3>(h[16 * b + j + 1], inv) : mx_cast2<FP8_DT_E5M2>(h[16 * b + j + 1], inv);
+              qw[8 * b + j / 2] = lo | (hi << 16);
+            }
+          }
+          // row m's four block codes: one aligned word of the MX scale layout (rows M, contraction N)
+          const int64_t off = ((m / 128) * (p.N / 128) + n0 / 128) * 512 + (m % 32) * 16 + ((m / 32) % 4) * 4;
+          *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.q_scales) + off) = codes;
+        } else {
+          uint32_t am = 0;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) am = absmax2(am, h[j]);
+          const Scale sc = tab_scale(p.q_tab, absmax_fold(am));
+          const float2 s2 = make_float2(sc.s32, sc.s32);
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            const float2 a = fmul2_rn(make_float2(__uint_as_float(h[j] << 16), __uint_as_float(h[j] & 0xFFFF0000u)), s2);
+            const float2 b = fmul2_rn(make_float2(__uint_as_float(h[j + 1] << 16), __uint_as_float(h[j + 1] & 0xFFFF0000u)), s2);
+            const uint32_t lo = e4 ? cvt_fp8x2<FP8_DT_E4M3>(a.x, a.y) : cvt_fp8x2<FP8_DT_E5M2>(a.x, a.y);
+            const uint32_t hi = e4 ? cvt_fp8x2<FP8_DT_E4M3>(b.x, b.y) : cvt_fp8x2<FP8_DT_E5M2>(b.x, b.y);
+            qw[j / 2] = lo | (hi << 16);
+          }
+          static_cast<float*>(p.q_scales)[m * (p.N / 128) + n0 / 128] = sc.inv32;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.q_out + m * p.N + n0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(qw[4 * i], qw[4 * i + 1], qw[4 * i + 2], qw[4 * i + 3]);
+        continue;
+      }
       // Pairs write through shared memory with TMA bulk-tensor stores of 32 rows x 128 bytes
       // (64 bf16 columns, or 32 fp32), unless this warp's 32 rows run past the end of an
       // expert's segment.
@@ -1328,6 +1418,15 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
         if (p.row_amax || p.col_amax)
           return pair ? run<kFP8, kDenseAmax, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c)
                       : run<kFP8, kDenseAmax, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
+        if (g.q_out) {
+          p.q_out = static_cast<uint8_t*>(g.q_out);
+          p.q_scales = g.q_scales;
+          p.q_mx = g.q_mx;
+          p.q_fmt = g.q_fmt;
+          p.q_tab = scale_tab(g.q_fmt);
+          return pair ? run<kFP8, kDenseQuant, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c)
+                      : run<kFP8, kDenseQuant, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
+        }
         return pair ? run<kFP8, kDense, 0, 0, 2>(ta, tb, to, none, none, p, tiles, c) : run<kFP8, kDense, 0, 0, 1>(ta, tb, to, none, none, p, tiles, c);
       }
       if (g.blockwise) return FP8_ERR_UNSUPPORTED;

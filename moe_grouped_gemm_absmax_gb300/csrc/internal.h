@@ -97,6 +97,13 @@ struct GemmArgs {
   int amax_whole;         // col_amax is one word: the maximum over the whole output
   int blockwise;          // FP8 operands with blockwise inverse scales: sA [M, K/128] (1 x 128 tiles),
                           // sB [ceil(N/128), K/128] (128 x 128 tiles); dense only
+  // quantized output (dense FP8, N % 128 == 0): codes [M, N] in q_fmt and scales of the result's
+  // bf16 rounding, 1 x 128 blocks (q_mx 0: fp32 inverse scales [M, N/128]) or MX blocks of 32
+  // (q_mx 1: E8M0 bytes in the MX scale layout for rows M, contraction N); out is then unused
+  void* q_out;
+  void* q_scales;
+  int q_mx;
+  int q_fmt;
 };
 int launch_gemm(const GemmArgs& g, const Ctx& c);
 

@@ -38,31 +38,6 @@ constexpr int kOutPitch = kTile + 16;  // bytes per staged output row (conflict-
 constexpr int kMxSmem = kTile * kInPitch * 2 + kTile * kOutPitch;
 constexpr int kMaxSegments = 2048;
 
-// E8M0 code of a block from the bf16 pattern of its amax (sign cleared). For a normal amax,
-// floor(log2 amax) = exponent field - 127, so the code (exponent + 127) is field - emax_elem,
-// clamped at 0; a zero or subnormal amax lies below the clamp. Inf / NaN give the NaN code.
-template <int FMT>
-FP8_DEVI uint32_t mx_code(uint32_t amax_bits) {
-  constexpr int kEmax = FMT == FP8_DT_E4M3 ? 8 : 15;
-  const int ef = (int)(amax_bits >> 7);
-  if (ef == 255) return 0xFFu;
-  return ef > kEmax ? (uint32_t)(ef - kEmax) : 0u;
-}
-
-// 1 / X = 2^(127 - code) as an fp32 (a normal number for every code the rule produces).
-FP8_DEVI float mx_inv(uint32_t code) {
-  return code == 0xFFu ? __uint_as_float(0x7FC00000u) : __uint_as_float((254u - code) << 23);
-}
-
-// Two bf16 (one packed word) times a power of two, cast: the product is exact, so the only
-// rounding is the cast's (nearest even, saturating at the format's largest finite value).
-template <int FMT>
-FP8_DEVI uint32_t mx_cast2(uint32_t two_bf16, float inv) {
-  const float2 p = fmul2_rn(make_float2(__uint_as_float(two_bf16 << 16), __uint_as_float(two_bf16 & 0xFFFF0000u)),
-                            make_float2(inv, inv));
-  return cvt_fp8x2<FMT>(p.x, p.y);
-}
-
 struct MxArgs {
   const uint16_t* x;
   int64_t R, C;           // rows and columns of one batch entry (C % 128 == 0)

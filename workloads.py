@@ -159,6 +159,12 @@ WORKLOADS = {
         "the llama3-8b-mlp-up grad-input GEMM dX = dY W (rowwise FP8 operands) with dX's column "
         "maxima from the GEMM epilogue, then dX quantized column-wise (e5m2, column-major) from them",
         dict(M=8192, K=4096, N=14336)),
+    "llama3-8b-fwd-quant-fused": Workload(
+        "llama3-8b-fwd-quant-fused",
+        "the llama3-8b-mlp-up forward GEMM y = x W^T (rowwise FP8 operands) with y quantized in the GEMM "
+        "epilogue (e4m3, 1 x 128 block scales: the next layer's activation operand), against the GEMM with "
+        "a bf16 output followed by the 1 x 128 quantize",
+        dict(M=8192, K=4096, N=14336)),
     "llama3-8b-mlp-up-blockwise": Workload(
         "llama3-8b-mlp-up-blockwise",
         "the llama3-8b-mlp-up Linear and inputs with blockwise scaling: x and dY in 1 x 128 tiles, W in "
