@@ -172,6 +172,10 @@ int launch_blk_quant(const void* x, int64_t R, int64_t C, int fmt, bool tile128,
   if (C % kBT || (!q && !qt) || (!tile128 && qt) || (qt && R % kBT)) return FP8_ERR_UNSUPPORTED;
   if ((R + kBT - 1) / kBT > 65535) return FP8_ERR_UNSUPPORTED;
   if (R == 0 || C == 0) return FP8_OK;
+  if (!tile128) {  // 1 x 128 tiles: the row kernel's teams where the row length suits them
+    const int rc = launch_quant_rows_blk128(x, R, C, fmt, q, inv, c);
+    if (rc != FP8_ERR_UNSUPPORTED) return rc;
+  }
   BlkArgs a;
   a.x = static_cast<const uint16_t*>(x);
   a.R = R;

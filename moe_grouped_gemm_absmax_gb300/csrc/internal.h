@@ -33,6 +33,9 @@ int make_tmap(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int ra
 // --- quantize launchers (quantize.cu) ---
 // Rowwise: x bf16 [R, C] -> q [R, C], inv [R].
 int launch_quant_rows(const void* x, int64_t R, int64_t C, int fmt, void* q, float* inv, const Ctx& c);
+// Blockwise 1 x 128 by the row kernel: x bf16 [R, C] -> q [R, C], inv [R, C / 128]; 512 <= C <= 16384,
+// C % 128 == 0, else FP8_ERR_UNSUPPORTED (nothing launched).
+int launch_quant_rows_blk128(const void* x, int64_t R, int64_t C, int fmt, void* q, float* inv, const Ctx& c);
 // Tensorwise in one cooperative launch: amax of x [R, C] into ws[0], a grid barrier on ws[1] (both
 // zeroed here), then the cast into q (row-major, may be null) and/or qt ([C, R], may be null); inv [1].
 int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,

@@ -98,8 +98,14 @@ static int rows_dispatch(const void* x, int64_t R, int nvec, void* q, float* inv
 // scale from the table (one row per team: every lane looks up the same entry), casts from
 // registers and stores 8 codes per lane and vector. Persistent teams walk the rows with a grid
 // stride, so at any time some teams load while others cast and store.
+//
+// B128: blockwise 1 x 128 tiles instead of whole rows ("FP8 training on AMD GPUs with TorchTitan and
+// TorchAO", "AMD FP8 format in TorchAO": a scale per tile). A tile is 16 consecutive 16-byte vectors,
+// i.e. the vectors one load step gives 16 consecutive lanes of a warp; those lanes reduce its amax by
+// shuffles, take its scale from the table, and the first of them writes the tile's inverse scale
+// (inv [R, C / 128]).
 constexpr int kRowWarpVPL = 16;
-template <int FMT, int WPR>
+template <int FMT, int WPR, bool B128 = false>
 __global__ void __launch_bounds__(256) quant_rows_warp_kernel(const uint4* __restrict__ x, int64_t R, int nvec,
                                                               uint2* __restrict__ q, float* __restrict__ inv,
                                                               const __grid_constant__ ScaleTab tab) {
@@ -118,6 +124,30 @@ __global__ void __launch_bounds__(256) quant_rows_warp_kernel(const uint4* __res
     for (int i = 0; i < kRowWarpVPL; ++i) {
       const int c = t + TPR * i;
       v[i] = c < nvec ? ld_nc_v4(xr + c) : make_uint4(0, 0, 0, 0);
+    }
+    if (B128) {
+      uint2* qr = q + r * nvec;
+#pragma unroll
+      for (int i = 0; i < kRowWarpVPL; ++i) {
+        const int c = t + TPR * i;
+        uint32_t a = absmax_fold(absmax_vec8(0u, v[i]));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, o));  // the 16-lane tile
+        if (c >= nvec) continue;  // uniform across the tile's 16 lanes (nvec % 16 == 0)
+        const Scale sc = tab_scale(tab, a);
+        if ((t & 15) == 0) inv[r * (nvec / 16) + c / 16] = sc.inv32;
+        const float2 s2 = make_float2(sc.s32, sc.s32);
+        const uint4 d = v[i];
+        float2 e = fmul2_rn(make_float2(__uint_as_float(d.x << 16), __uint_as_float(d.x & 0xFFFF0000u)), s2);
+        float2 f = fmul2_rn(make_float2(__uint_as_float(d.y << 16), __uint_as_float(d.y & 0xFFFF0000u)), s2);
+        uint2 o;
+        o.x = cvt_fp8x2<FMT>(e.x, e.y) | (cvt_fp8x2<FMT>(f.x, f.y) << 16);
+        e = fmul2_rn(make_float2(__uint_as_float(d.z << 16), __uint_as_float(d.z & 0xFFFF0000u)), s2);
+        f = fmul2_rn(make_float2(__uint_as_float(d.w << 16), __uint_as_float(d.w & 0xFFFF0000u)), s2);
+        o.y = cvt_fp8x2<FMT>(e.x, e.y) | (cvt_fp8x2<FMT>(f.x, f.y) << 16);
+        qr[c] = o;
+      }
+      continue;
     }
 #pragma unroll
     for (int i = 0; i < kRowWarpVPL; ++i) acc = absmax_vec8(acc, v[i]);
@@ -151,9 +181,9 @@ __global__ void __launch_bounds__(256) quant_rows_warp_kernel(const uint4* __res
   }
 }
 
-template <int FMT, int WPR>
+template <int FMT, int WPR, bool B128 = false>
 static int run_rows_warp(const void* x, int64_t R, int nvec, void* q, float* inv, const Ctx& c) {
-  auto kern = quant_rows_warp_kernel<FMT, WPR>;
+  auto kern = quant_rows_warp_kernel<FMT, WPR, B128>;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
   // as many teams as fit at once, but no more than the rows, with the rows spread evenly
@@ -170,6 +200,20 @@ static int rows_warp_dispatch(const void* x, int64_t R, int nvec, void* q, float
   if (nvec <= 32 * kRowWarpVPL) return run_rows_warp<FMT, 1>(x, R, nvec, q, inv, c);
   if (nvec <= 64 * kRowWarpVPL) return run_rows_warp<FMT, 2>(x, R, nvec, q, inv, c);
   return run_rows_warp<FMT, 4>(x, R, nvec, q, inv, c);
+}
+
+// Blockwise 1 x 128 tiles of rows of 512-16384 elements (C % 128 == 0): the row kernel's teams with
+// a scale per 16-lane tile. Returns FP8_ERR_UNSUPPORTED outside that range.
+int launch_quant_rows_blk128(const void* x, int64_t R, int64_t C, int fmt, void* q, float* inv, const Ctx& c) {
+  const int nvec = (int)(C / 8);
+  if (C % 128 || nvec < 64 || nvec > 128 * kRowWarpVPL) return FP8_ERR_UNSUPPORTED;
+  if (R == 0) return FP8_OK;
+  const bool e4 = fmt == FP8_DT_E4M3;
+  if (nvec <= 32 * kRowWarpVPL)
+    return e4 ? run_rows_warp<FP8_DT_E4M3, 1, true>(x, R, nvec, q, inv, c) : run_rows_warp<FP8_DT_E5M2, 1, true>(x, R, nvec, q, inv, c);
+  if (nvec <= 64 * kRowWarpVPL)
+    return e4 ? run_rows_warp<FP8_DT_E4M3, 2, true>(x, R, nvec, q, inv, c) : run_rows_warp<FP8_DT_E5M2, 2, true>(x, R, nvec, q, inv, c);
+  return e4 ? run_rows_warp<FP8_DT_E4M3, 4, true>(x, R, nvec, q, inv, c) : run_rows_warp<FP8_DT_E5M2, 4, true>(x, R, nvec, q, inv, c);
 }
 
 int launch_quant_rows(const void* x, int64_t R, int64_t C, int fmt, void* q, float* inv, const Ctx& c) {

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads as W
-from tests.gpu_util import bits, check_gemm, codes, f32_bits, upload_codes, upload_f32
+from tests.gpu_util import bits, check_gemm, codes, f32_bits, special_rows, upload_codes, upload_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -29,9 +29,14 @@ def _inputs(R, C, seed):
     return x.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("R,C,fmt", [(300, 384, E4), (128, 128, E5), (77, 256, E4)])
+# rows of 512-16384 elements run on the row-wise kernel's warp teams (1, 2 or 4 warps per row), the
+# others on the tile kernel; the special rows probe ties, subnormals, zeros and an outlier per tile
+@pytest.mark.parametrize("R,C,fmt", [(300, 384, E4), (128, 128, E5), (77, 256, E4), (300, 512, E4), (77, 4096, E5),
+                                     (40, 8192, E4), (5, 16384, E5), (9, 16256, E4)])
 def test_quantize_1x128(fp8, R, C, fmt):
     x = _inputs(R, C, R)
+    sp = special_rows(C, 448.0 if fmt == E4 else 57344.0)
+    x = torch.cat([x, sp]) if R > 16 else x
     q, _, inv, _ = fp8.blk_quantize_alloc(x.cuda(), TDT[fmt])
     torch.cuda.synchronize()
     qo, io = oracle.quantize_blocks(bits(x), fmt, 1, 128)
