@@ -191,7 +191,8 @@ typedef struct fp8_tensor {
  *  workspace   device memory, 16-byte aligned, of fp8_workspace_size(FP8_OP_QUANTIZE, groups,
  *              C, granularity) bytes: 8 bytes for tensor granularity (the amax word and a
  *              grid-barrier count); for column granularity 4 bytes per (group, column) for the
- *              column maxima, rounded up to 16 bytes, plus 16 bytes for a grid-barrier count
+ *              column maxima, rounded up to 16 bytes, plus 4 bytes per (group, 64-column strip)
+ *              for the chunk completion counts, rounded up to 16 bytes
  *              (groups = B for 3-D x, E with offsets, else 1); 0 for row
  *              granularity (workspace may then be NULL). MX: 4 * (E + 1) bytes rounded up to
  *              16 with offsets (the padded segment starts), else 0. Calls sharing a workspace must be
@@ -339,8 +340,8 @@ int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* saved, const fp
                    void* stream);
 
 /* Test hook for failure detection: while enabled, every GEMM launch first waits on a barrier
- * that nothing signals, and the grid barriers of the tensorwise and column-wise quantize wait for
- * one arrival more than there are CTAs; the wait runs out after the wait limit (fp8_set_wait_limit_ns), the
+ * that nothing signals, the grid barrier of the tensorwise quantize and the chunk completion
+ * counts of the column-wise quantize wait for one arrival more than there are CTAs; the wait runs out after the wait limit (fp8_set_wait_limit_ns), the
  * kernel reports FP8_DEV_TIMEOUT, drains and returns. Off by default. Returns the previous
  * setting. */
 int fp8_set_test_stall(int enable);

@@ -44,7 +44,8 @@ int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, v
 // scale per column: either n_groups consecutive groups of group_rows rows (ends == null) or the
 // segments given by ends[n_groups] (segment-padded output, padded row count ld_out).
 // out_t row (g, c) starts at out_t + (g * C + c) * ld_out (dense) or out_t + c * ld_out + pstart_g
-// (segments). inv [n_groups, C]. scratch: n_groups * C words of device memory.
+// (segments). inv [n_groups, C]. scratch: col_ws_words(n_groups, C) words of device memory, 16-byte
+// aligned; C % 4 == 0 unless the maxima are given.
 // Workspace words (4 bytes each) a column quantize of `groups` x C scales needs.
 int64_t col_ws_words(int64_t groups, int64_t C);
 // amax_given (optional): the column maxima as fp32 words [n_groups, C] (bf16 values); pass 1 is

@@ -35,9 +35,10 @@ def test_host_helpers(fp8):
         assert P % 128 == 0 and R + 127 * E <= P < R + 127 * E + 128
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_TENSOR) == 8
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_ROW) == 0
-    # one amax word per (group, column), rounded up to 16 bytes, then 16 bytes for the grid-barrier count
-    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 16, 5120, granularity=fp8.GRAN_COL) == 16 * 5120 * 4 + 16
-    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 1, 70, granularity=fp8.GRAN_COL) == 72 * 4 + 16
+    # one amax word per (group, column), then one completion count per (group, 64-column strip),
+    # each part rounded up to 16 bytes
+    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 16, 5120, granularity=fp8.GRAN_COL) == 16 * 5120 * 4 + 16 * 80 * 4
+    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 1, 70, granularity=fp8.GRAN_COL) == 72 * 4 + 4 * 4
     M, K, N = 256, 512, 128
     ws_row_bf16 = fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_ROW, fp8.WGRAD_BF16)
     ws_row_fp8 = fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_ROW, fp8.WGRAD_FP8)

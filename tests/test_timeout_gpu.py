@@ -1,7 +1,8 @@
-"""Failure detection without a GPU fault: every on-device wait of the GEMM kernels and of the
-grid barriers of the tensorwise and column-wise quantize is bounded. The test hook
-fp8_set_test_stall makes the GEMM's MMA issuer wait on a barrier that nothing signals, and the
-quantize kernels' grid barriers wait for one CTA more than they launched; with a short wait limit the wait runs out, and the kernel must report
+"""Failure detection without a GPU fault: every on-device wait of the GEMM kernels, of the grid
+barrier of the tensorwise quantize and of the chunk completion counts of the column-wise quantize
+is bounded. The test hook fp8_set_test_stall makes the GEMM's MMA issuer wait on a barrier that
+nothing signals, and the quantize kernels wait for one CTA more than they launched; with a short
+wait limit the wait runs out, and the kernel must report
 FP8_DEV_TIMEOUT in the status word, stop its other warps, drain its in-flight TMA loads and MMAs,
 free its tensor memory and return, leaving the context usable (a normal call afterwards is
 correct)."""
