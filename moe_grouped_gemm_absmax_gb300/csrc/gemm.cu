@@ -135,15 +135,16 @@ struct Tile {
   int e;            // expert (jagged)
 };
 
+constexpr int kMaxStages = 5;  // ring stages the barrier arrays below hold
 struct Shared {
   float sb[2][BN];  // per-tile column scales, alternating between consecutive tiles
-  uint64_t full[5];
-  uint64_t empty[5];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[4];   // accumulators / K-block partials ready (NBUF of them in use)
   uint64_t tempty[4];
   uint64_t drain;
   uint64_t never;   // signalled by no one: the failure-detection test hook waits on it
-  uint64_t sff[5];  // MX: a stage's scales are in tensor memory
+  uint64_t sff[kMaxStages];  // MX: a stage's scales are in tensor memory
   uint64_t sf_drain;
   uint32_t tmem_base;
   int abort;
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
                 const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmSA,
                 const __grid_constant__ CUtensorMap tmSB, const GemmParams p) {
   using C = Cfg<KIND, CG, SCHED>;
+  static_assert(C::STAGES <= kMaxStages && C::NBUF <= 4, "ring and accumulator barriers fit the shared block");
   constexpr int STAGES = C::STAGES;
   constexpr int kThreads = C::THREADS;
   constexpr int kEpiThreads = C::EPI_THREADS;

@@ -40,6 +40,11 @@ int launch_quant_rows_blk128(const void* x, int64_t R, int64_t C, int fmt, void*
 // zeroed here), then the cast into q (row-major, may be null) and/or qt ([C, R], may be null); inv [1].
 int launch_quant_tensor(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
                         uint32_t* amax_ws, const Ctx& c);
+// The same with up to 12 tiles of 128 x 64 per SM kept in shared memory between the two reads
+// (tensor.cu); for shapes where tensor_stash_ok holds (the outputs can leave by TMA).
+bool tensor_stash_ok(int64_t R, int64_t C, bool has_q, bool has_qt);
+int launch_quant_tensor_stash(const void* x, int64_t R, int64_t C, int fmt, void* q, void* qt, float* inv,
+                              uint32_t* amax_ws, const Ctx& c);
 // Columnwise with column-major output. x viewed as [rows_total, C]. Groups of rows share one
 // scale per column: either n_groups consecutive groups of group_rows rows (ends == null) or the
 // segments given by ends[n_groups] (segment-padded output, padded row count ld_out).
