@@ -108,7 +108,7 @@ class DenseLinearStep(Step):
         self.dyi = torch.empty(M, device=d)
         self.wtq = torch.empty((K, N), dtype=e4, device=d)
         self.wti = torch.empty(K, device=d)
-        self.wsc = fp8.col_workspace(1, K, d)
+        self.wsc = fp8.col_workspace(1, K, N, d)  # W [N, K] column-wise
         self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=d)
         self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=d)
         f = 2.0 * M * N * K
@@ -292,7 +292,7 @@ class ColwiseStep(Step):
         self.xx = W.normal_bf16((RX, CX), 1.0, seed + 1, device)
         self.gt = torch.empty((C, R), dtype=torch.float8_e5m2, device=device)
         self.gi = torch.empty(C, device=device)
-        self.gsc = fp8.col_workspace(1, C, device)
+        self.gsc = fp8.col_workspace(1, C, R, device)
         self.xq = torch.empty((RX, CX), dtype=torch.float8_e4m3fn, device=device)
         self.xi = torch.empty(RX, device=device)
         self.R, self.C, self.RX, self.CX = R, C, RX, CX
@@ -542,9 +542,9 @@ class MoeFwdBwdStep(Step):
         self.dYt, self.dYti = torch.empty((N, P), dtype=e5, device=device), torch.empty((E, N), device=device)
         self.At, self.Ati = torch.empty((K, P), dtype=e4, device=device), torch.empty((E, K), device=device)
         self.dW = torch.empty((E, N, K), dtype=torch.bfloat16, device=device)
-        self.ws_w = fp8.col_workspace(E, K, device)
-        self.ws_dy = fp8.col_workspace(E, N, device)
-        self.ws_a = fp8.col_workspace(E, K, device)
+        self.ws_w = fp8.col_workspace(E, K, E * N, device)
+        self.ws_dy = fp8.col_workspace(E, N, M, device)
+        self.ws_a = fp8.col_workspace(E, K, M, device)
         self.E, self.M, self.K, self.N = E, M, K, N
         f = 2.0 * M * N * K
         self.kernels = [("quantize_rows A e4m3", "hbm", 3 * M * K + 4 * M, "hbm"),
@@ -824,7 +824,7 @@ class FusedAmaxStep(Step):
         self.amax = torch.empty(K, device=device)
         self.dxt = torch.empty((K, M), dtype=torch.float8_e5m2, device=device)
         self.dxti = torch.empty(K, device=device)
-        self.ws = fp8.col_workspace(1, K, device)
+        self.ws = fp8.col_workspace(1, K, M, device)
         f = 2.0 * M * N * K
         self.kernels = [("gemm_fp8 dX + column amax side output", "tensor", f, "fp8"),
                         ("quantize_cols dX e5m2 from amax (one read)", "hbm", 3 * M * K + 4 * K, "hbm")]

@@ -189,10 +189,10 @@ typedef struct fp8_tensor {
  *              E <= 2048.
  *              Checked on the device: a bad vector sets FP8_DEV_BAD_OFFSETS.
  *  workspace   device memory, 16-byte aligned, of fp8_workspace_size(FP8_OP_QUANTIZE, groups,
- *              C, granularity) bytes: 8 bytes for tensor granularity (the amax word and a
- *              grid-barrier count); for column granularity 4 bytes per (group, column) for the
- *              column maxima, rounded up to 16 bytes, plus 4 bytes per (group, 64-column strip)
- *              for the chunk completion counts, rounded up to 16 bytes
+ *              C, rows, granularity) bytes: 8 bytes for tensor granularity (the amax word and a
+ *              grid-barrier count); for column granularity 128 bytes (the 64 column maxima of a
+ *              256-row x 64-column tile) per tile, (ceil(rows / 256) + groups) * ceil(C / 64)
+ *              tiles, rows = all rows of x (B * R for 3-D x)
  *              (groups = B for 3-D x, E with offsets, else 1); 0 for row
  *              granularity (workspace may then be NULL). MX: 4 * (E + 1) bytes rounded up to
  *              16 with offsets (the padded segment starts), else 0. Calls sharing a workspace must be
@@ -340,8 +340,8 @@ int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* saved, const fp
                    void* stream);
 
 /* Test hook for failure detection: while enabled, every GEMM launch first waits on a barrier
- * that nothing signals, the grid barrier of the tensorwise quantize and the chunk completion
- * counts of the column-wise quantize wait for one arrival more than there are CTAs; the wait runs out after the wait limit (fp8_set_wait_limit_ns), the
+ * that nothing signals, the grid barrier of the tensorwise quantize waits for one arrival more
+ * than there are CTAs, and the column-wise quantize sees no tile maxima as written; the wait runs out after the wait limit (fp8_set_wait_limit_ns), the
  * kernel reports FP8_DEV_TIMEOUT, drains and returns. Off by default. Returns the previous
  * setting. */
 int fp8_set_test_stall(int enable);
@@ -381,8 +381,9 @@ int fp8_test_cast_bits(uint32_t first_bits, int64_t n, int out_dtype, void* out,
 int fp8_quantize_tensor_noalloc(const fp8_tensor* x, int out_dtype, int layout, fp8_tensor* out,
                                 fp8_tensor* out_t, fp8_tensor* inv_scale, void* stream);
 
-/* Workspace bytes for an operation. FP8_OP_QUANTIZE: (d0, d1) = (groups, columns) as described
- * at fp8_quantize (d2 unused). FP8_OP_LINEAR_FWD / FP8_OP_LINEAR_BWD: (d0, d1, d2) = (M, K, N). */
+/* Workspace bytes for an operation. FP8_OP_QUANTIZE: (d0, d1, d2) = (groups, columns, rows of x
+ * over all groups) as described at fp8_quantize (d2 is used by column granularity only).
+ * FP8_OP_LINEAR_FWD / FP8_OP_LINEAR_BWD: (d0, d1, d2) = (M, K, N). */
 size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2, int granularity,
                           int wgrad_mode);
 

@@ -275,9 +275,9 @@ def fp8_set_test_stall(enable: bool) -> int:
 # ------------------------------------------------------------------------------------------
 # allocation helpers (torch buffers of the right shapes, then the entry points above)
 
-def col_workspace(groups: int, cols: int, device) -> torch.Tensor:
-    """Workspace of a column-granularity fp8_quantize (one word per group and column)."""
-    n = fp8_workspace_size(OP_QUANTIZE, groups, cols, granularity=GRAN_COL)
+def col_workspace(groups: int, cols: int, rows: int, device) -> torch.Tensor:
+    """Workspace of a column-granularity fp8_quantize of `rows` rows (all groups) x `cols` columns."""
+    n = fp8_workspace_size(OP_QUANTIZE, groups, cols, rows, granularity=GRAN_COL)
     return torch.empty(max(n // 4, 4), dtype=torch.int32, device=device)
 
 
@@ -311,7 +311,7 @@ def quantize_alloc(x, granularity, out_dtype, layout=None, offsets=None, padded_
             out_t = torch.empty((B, C, R) if x.dim() == 3 else (C, R), dtype=fdt, device=dev)
             inv = torch.empty((B, C) if x.dim() == 3 else (C,), dtype=torch.float32, device=dev)
             groups = B
-        ws = col_workspace(groups, C, dev)
+        ws = col_workspace(groups, C, B * R, dev)
     fp8_quantize(x, granularity, out_dtype, layout, out, out_t, inv, offsets, ws, status=status, stream=stream)
     return out, out_t, inv
 

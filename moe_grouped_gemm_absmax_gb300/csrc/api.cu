@@ -232,7 +232,8 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
     case FP8_GRAN_COL: {
       FP8_CHECK(layout == FP8_LAYOUT_COL_MAJOR, FP8_ERR_UNSUPPORTED);
       const int64_t groups = offsets ? (valid_desc(offsets) && offsets->ndim == 1 ? offsets->shape[0] : 0) : B;
-      FP8_CHECK(ws && (reinterpret_cast<uintptr_t>(ws) & 15u) == 0 && ws_bytes >= (size_t)col_ws_words(groups, C) * 4,
+      FP8_CHECK(ws && (reinterpret_cast<uintptr_t>(ws) & 15u) == 0 &&
+                    ws_bytes >= (size_t)col_ws_words(groups > 0 ? groups : 1, C, B * R) * 4,
                 FP8_ERR_WORKSPACE);
       uint32_t* scratch = static_cast<uint32_t*>(ws);
       if (offsets) {
@@ -675,7 +676,7 @@ static fp8_tensor T1(void* p, int dt, int64_t a) {
 
 // Workspace layout of the backward pass (each piece 256-byte aligned).
 struct BwdLayout {
-  size_t amax, dy_q, dy_inv, dyt_q, dyt_inv, wt_q, wt_inv, xt_q, xt_inv, col_scratch, total;
+  size_t amax, dy_q, dy_inv, dyt_q, dyt_inv, wt_q, wt_inv, xt_q, xt_inv, col_scratch, col_scratch_bytes, total;
 };
 static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad) {
   BwdLayout L = {};
@@ -709,7 +710,12 @@ static BwdLayout bwd_layout(int64_t M, int64_t K, int64_t N, int gran, int wgrad
   L.xt_q = (fp8w && rows) ? take((size_t)(K * M)) : 0;
   L.xt_inv = (fp8w && rows) ? take((size_t)K * 4) : 0;
   // per-column scratch of the column-wise quantizations (used one after the other)
-  L.col_scratch = rows ? take((size_t)col_ws_words(1, K > N ? K : N) * 4) : 0;
+  // the column quantizes of W [N, K], dY [M, N] and x [M, K] share one scratch
+  int64_t cw = col_ws_words(1, K, N);
+  if (col_ws_words(1, N, M) > cw) cw = col_ws_words(1, N, M);
+  if (col_ws_words(1, K, M) > cw) cw = col_ws_words(1, K, M);
+  L.col_scratch = rows ? take((size_t)cw * 4) : 0;
+  L.col_scratch_bytes = rows ? (size_t)cw * 4 : 0;
   L.total = off;
   return L;
 }
@@ -740,7 +746,9 @@ extern "C" size_t fp8_workspace_size(int op, int64_t d0, int64_t d1, int64_t d2,
     case FP8_OP_QUANTIZE:  // (d0, d1) = (groups, columns) for FP8_GRAN_COL; (segments, -) for MX
       if (granularity == FP8_GRAN_TENSOR) return 8;  // amax word, grid-barrier count
       if (granularity == FP8_GRAN_MX) return d0 > 0 ? (size_t)round_up(4 * (d0 + 1), 16) : 0;
-      if (granularity == FP8_GRAN_COL) return (size_t)col_ws_words(d0 > 0 ? d0 : 1, d1 > 0 ? d1 : 0) * 4;
+      // (d0, d1, d2) = (groups, columns, rows of x over all groups) for FP8_GRAN_COL
+      if (granularity == FP8_GRAN_COL)
+        return (size_t)col_ws_words(d0 > 0 ? d0 : 1, d1 > 0 ? d1 : 0, d2 > 0 ? d2 : 0) * 4;
       return 0;
     case FP8_OP_LINEAR_FWD:
       return granularity == FP8_GRAN_TENSOR ? 256 : 0;
@@ -890,7 +898,7 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
     fp8_tensor wt_q = T2(ws + L.wt_q, FP8_DT_E4M3, K, N);
     fp8_tensor wt_inv = T1(ws + L.wt_inv, FP8_DT_F32, K);
     FP8_TRY(quantize_impl(w, FP8_GRAN_COL, FP8_DT_E4M3, FP8_LAYOUT_COL_MAJOR, nullptr, &wt_q, &wt_inv, nullptr,
-                          ws + L.col_scratch, (size_t)col_ws_words(1, K) * 4, c));
+                          ws + L.col_scratch, L.col_scratch_bytes, c));
     FP8_TRY(scaled_mm_impl(&dy_q, &wt_q, &dy_inv, &wt_inv, dx, 0, c));
   }
   if (need_dw) {
@@ -900,9 +908,9 @@ extern "C" int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* save
       fp8_tensor xt_q = T2(ws + L.xt_q, FP8_DT_E4M3, K, M);
       fp8_tensor xt_inv = T1(ws + L.xt_inv, FP8_DT_F32, K);
       FP8_TRY(quantize_impl(dy, FP8_GRAN_COL, FP8_DT_E5M2, FP8_LAYOUT_COL_MAJOR, nullptr, &dyt_q, &dyt_inv, nullptr,
-                            ws + L.col_scratch, (size_t)col_ws_words(1, N) * 4, c));
+                            ws + L.col_scratch, L.col_scratch_bytes, c));
       FP8_TRY(quantize_impl(x, FP8_GRAN_COL, FP8_DT_E4M3, FP8_LAYOUT_COL_MAJOR, nullptr, &xt_q, &xt_inv, nullptr,
-                            ws + L.col_scratch, (size_t)col_ws_words(1, K) * 4, c));
+                            ws + L.col_scratch, L.col_scratch_bytes, c));
       FP8_TRY(scaled_mm_impl(&dyt_q, &xt_q, &dyt_inv, &xt_inv, dw, 0, c));
     } else {
       FP8_TRY(scaled_mm_impl(dy, x, nullptr, nullptr, dw, FP8_MM_A_MN_MAJOR | FP8_MM_B_MN_MAJOR, c));

@@ -12,23 +12,22 @@
 // persistent cooperative launch (one CTA per SM):
 //   pass 1 (amax): a producer warp streams 256-row x 64-column tiles ("units") from HBM through a
 //     TMA ring (128-byte swizzle; the loads keep their lines in L2); 4 warps fold each tile's
-//     column maxima by shuffles and shared memory into one relaxed atomic max per column on a
-//     per-(group, column) word, and after the CTA's last unit of a chunk count the CTA on the
-//     chunk's completion word (release);
-//   pass 2 (cast): a second producer warp waits (bounded, acquire) until a chunk's word shows
-//     every CTA done with it, then streams the same units again, now from L2, through its own
-//     ring, with each unit's 64 column maxima copied asynchronously beside it; 8 warps each take
-//     32 rows of a tile: a lane per column pair, scale by table, cast in registers, write the
-//     transposed 64 x 32 box to the warp's staging buffer and store it by TMA (no barrier across
-//     warps).
-// A chunk is a set of whole column strips of one group, all their row tiles, a few MB of input,
-// so its maxima are final once its word is full. Units are ordered group, chunk, row tile, strip
-// (neighbouring CTAs read neighbouring strips of the same rows: long DRAM row segments) and dealt
-// round-robin, in the same order in both passes, so a tile's second read is by the SM that made
-// the first. Pass 1 may run at most a fixed number of units ahead of pass 2 (and never into a
-// chunk before pass 2 has reached the chunks before it), which keeps every tile between its two
-// reads in L2 whatever the tensor's size, and cannot deadlock: a chunk's pass 1 waits only for the
-// pass 2 of earlier chunks, whose pass 1 is complete.
+//     column maxima by shuffles and shared memory and store them as the unit's partial: 64
+//     16-bit maxima, each with bit 15 set ("written"; bf16 magnitudes leave it free), in a
+//     workspace the launcher zeroed;
+//   pass 2 (cast): a second producer warp streams the same units again, now from L2, through its
+//     own ring; two gatherer warps take each unit's strip maxima from the partials of the strip's
+//     row tiles, polling (bounded) until every field reads as written, so no fence, counter or
+//     barrier separates the passes; 8 warps each take 32 rows of a tile: a lane per column pair,
+//     scale by table, cast in registers, write the transposed 64 x 32 box to the warp's staging
+//     buffer and store it by TMA (no barrier across warps).
+// Units are ordered group, chunk, row tile, strip (a chunk: whole 64-column strips of one group,
+// a few MB; neighbouring CTAs read neighbouring strips of the same rows: long DRAM row segments)
+// and dealt round-robin, in the same order in both passes, so a tile's second read is by the SM
+// that made the first. Pass 1 may run at most a fixed number of units ahead of pass 2 (and never
+// into a chunk before pass 2 has reached the chunks before it), which keeps every tile between
+// its two reads in L2 whatever the tensor's size, and cannot deadlock: a chunk's pass 1 waits only
+// for the pass 2 of earlier chunks, whose pass 1 is complete.
 // With the maxima given (fp8_quantize_from_amax) the launch runs pass 2 alone.
 #include "common.cuh"
 #include "internal.h"
@@ -43,14 +42,14 @@ constexpr int kCqMaxStages = 4;               // per ring
 constexpr int kCqP1Warps = 4;                 // pass-1 (amax) warps
 constexpr int kCqP2Warps = 8;                 // pass-2 (cast) warps, 32 rows each
 constexpr int kCqP1Threads = 32 * kCqP1Warps;
-constexpr int kCqPubs = 2;                    // publisher warps (chunk c: publisher c % kCqPubs)
-constexpr int kCqP1Warp0 = 2 + kCqPubs;       // warps: 0, 1 producers; publishers; pass 1; pass 2
+constexpr int kCqGathers = 3;                 // pass-2 warps gathering the maxima (unit k: warp k % gathers)
+constexpr int kCqP1Warp0 = 2 + kCqGathers;    // warps: 0, 1 producers; gatherers; pass 1; pass 2
 constexpr int kCqP2Warp0 = kCqP1Warp0 + kCqP1Warps;
 constexpr int kCqThreads = 32 * (kCqP2Warp0 + kCqP2Warps);
-constexpr int kCqSlots = 4;                   // per publisher: pass-1 unit maxima handed over
+constexpr uint32_t kCqWritten = 0x80008000u;  // a partial's 16-bit fields carry bit 15 once written
 constexpr int kCqBox = 64 * 32;               // a pass-2 warp's staging box: 64 columns x 32 rows of codes
 constexpr int kCqChunkUnits = 256;            // units per chunk: 8 MB of input
-constexpr int kCqLagUnits = 1280;             // pass 1 leads pass 2 by at most 40 MB of input
+constexpr int kCqLagUnits = 1024;             // pass 1 leads pass 2 by at most 32 MB of input
 constexpr int kCqMaxSegments = 2048;          // segment tables live in shared memory
 constexpr uint64_t kCqDrainNs = 2000000000ull;  // fixed bound: loads in flight before exit
 
@@ -59,15 +58,15 @@ struct CqParams {
   int64_t C, n_groups, group_rows;
   int32_t n_strips;
   int32_t mode;         // 0: 2-D [C, R] output; 1: batched [B, C, R]; 2: segments [C, P]
-  uint32_t* amax;       // [n_groups, C] amax words: bf16 patterns, or fp32 words when given
-  int32_t amax_shift;   // 0: bf16 patterns; 16: fp32 words holding bf16 values
-  int32_t given;        // 1: the maxima are given, pass 2 alone
-  uint32_t* done;       // per chunk: CTAs done with the chunk's pass 1 (zeroed by the launcher)
+  const uint32_t* amax;  // given maxima: fp32 words [n_groups, C] holding bf16 values (pass 2 alone)
+  int32_t given;         // 1: the maxima are given
+  uint32_t* part;        // per unit: its 64 column maxima, 32 packed words (zeroed by the launcher)
   float* inv;
   int32_t* status;
   uint64_t wait_ns;
   int32_t chunk_units, lag_units, stages_a, stages_b;
-  int32_t test_stall;   // failure-detection test hook: each chunk waits for one CTA more
+  int32_t gathers;      // gatherer warps in use: at most stages_b (see the gatherers)
+  int32_t test_stall;   // failure-detection test hook: no partial ever reads as written
 };
 
 // A group of n rows: row tiles, strips per chunk and chunks (the strips split as evenly as the
@@ -93,14 +92,15 @@ FP8_DEVI CqShape cq_shape(int64_t n, int32_t n_strips, int32_t chunk_units) {
 }
 
 struct CqUnit {
-  int32_t g, rt, c0, valid, wrows, pstart, chunk, chunk_first, row;
+  int32_t g, rt, c0, valid, wrows, pstart, chunk_first, row;
+  int32_t pbase, rtn;  // the unit's strip: its first partial (row tile 0) and its row tiles
 };
 
 // Segment tables in shared memory (segment mode): [0, n] unit starts, [n + 1, 2n + 1] padded
-// output starts, [2n + 2, 3n + 2] first rows, [3n + 3, 4n + 3] chunk starts.
+// output starts, [2n + 2, 3n + 2] first rows.
 // Unit i -> group, chunk, row tile, strip. Unit and row indices fit 32 bits (the host checks).
 FP8_DEVI CqUnit cq_unit(const CqParams& p, int32_t i, const int32_t* pre, const CqShape& dense) {
-  int32_t g, ufirst, cfirst, g0, pstart, n, wend;
+  int32_t g, ufirst, g0, pstart, n, wend;
   CqShape sh;
   if (p.mode == 2) {
     const int32_t ng = (int32_t)p.n_groups;
@@ -115,7 +115,6 @@ FP8_DEVI CqUnit cq_unit(const CqParams& p, int32_t i, const int32_t* pre, const 
     pstart = pre[ng + 1 + g];
     g0 = pre[2 * ng + 2 + g];
     n = pre[2 * ng + 2 + g + 1] - g0;
-    cfirst = pre[3 * ng + 3 + g];
     wend = (n + 127) & ~127;
     sh = cq_shape(n, p.n_strips, p.chunk_units);
   } else {
@@ -123,7 +122,6 @@ FP8_DEVI CqUnit cq_unit(const CqParams& p, int32_t i, const int32_t* pre, const 
     const int32_t per = sh.rt_n * p.n_strips;
     g = i / per;
     ufirst = g * per;
-    cfirst = g * sh.nch;
     n = (int32_t)p.group_rows;
     g0 = g * n;
     pstart = 0;
@@ -136,24 +134,25 @@ FP8_DEVI CqUnit cq_unit(const CqParams& p, int32_t i, const int32_t* pre, const 
   const int32_t w = min(sh.sc, p.n_strips - j * sh.sc);
   const int32_t rt = rem / w;
   CqUnit u;
+  const int32_t strip = j * sh.sc + (rem - rt * w);
   u.g = g;
   u.rt = rt * kCqTile;
-  u.c0 = (j * sh.sc + (rem - rt * w)) * 64;
+  u.c0 = strip * 64;
+  u.pbase = ufirst + strip * sh.rt_n;  // a group's partials: strip-major, so a strip's are contiguous
+  u.rtn = sh.rt_n;
   u.valid = min(max(n - u.rt, 0), kCqTile);
   u.wrows = min(max(wend - u.rt, 0), kCqTile);
   u.pstart = pstart;
-  u.chunk = cfirst + j;
   u.chunk_first = ufirst + j * span;
   u.row = g0 + u.rt;
   return u;
 }
 
-// Validates the offsets and builds the segment tables (segment mode); the number of units and
-// of chunks. False after reporting bad offsets (every thread returns the same).
-FP8_DEVI bool cq_setup(const CqParams& p, int32_t* pre, const CqShape& dense, int32_t* units, int32_t* chunks) {
+// Validates the offsets and builds the segment tables (segment mode); the number of units.
+// False after reporting bad offsets (every thread returns the same).
+FP8_DEVI bool cq_setup(const CqParams& p, int32_t* pre, const CqShape& dense, int32_t* units) {
   if (p.mode != 2) {
     *units = (int32_t)p.n_groups * dense.rt_n * p.n_strips;
-    *chunks = (int32_t)p.n_groups * dense.nch;
     return true;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -169,68 +168,55 @@ FP8_DEVI bool cq_setup(const CqParams& p, int32_t* pre, const CqShape& dense, in
     return false;
   }
   if (warp == 0) {
-    int32_t cu = 0, cp = 0, cc = 0;
+    int32_t cu = 0, cp = 0;
     for (int32_t base = 0; base < ng; base += 32) {
       const int32_t i = base + lane;
-      int32_t vu = 0, vp = 0, vc = 0;
+      int32_t vu = 0, vp = 0;
       if (i < ng) {
         const int32_t n = p.ends[i] - (i ? p.ends[i - 1] : 0);
-        const CqShape sh = cq_shape(n, p.n_strips, p.chunk_units);
-        vu = sh.rt_n * p.n_strips;
+        vu = (int32_t)((n + kCqTile - 1) / kCqTile) * p.n_strips;
         vp = (n + 127) & ~127;
-        vc = sh.nch;
       }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int32_t yu = __shfl_up_sync(0xffffffffu, vu, o);
         const int32_t yp = __shfl_up_sync(0xffffffffu, vp, o);
-        const int32_t yc = __shfl_up_sync(0xffffffffu, vc, o);
         if (lane >= o) {
           vu += yu;
           vp += yp;
-          vc += yc;
         }
       }
       if (i < ng) {
         pre[i + 1] = vu + cu;
         pre[ng + 1 + i + 1] = vp + cp;
         pre[2 * ng + 2 + i + 1] = p.ends[i];
-        pre[3 * ng + 3 + i + 1] = vc + cc;
       }
       cu += __shfl_sync(0xffffffffu, vu, 31);
       cp += __shfl_sync(0xffffffffu, vp, 31);
-      cc += __shfl_sync(0xffffffffu, vc, 31);
     }
     if (lane == 0) {
       pre[0] = 0;
       pre[ng + 1] = 0;
       pre[2 * ng + 2] = 0;
-      pre[3 * ng + 3] = 0;
     }
   }
   __syncthreads();
   *units = pre[ng];
-  *chunks = pre[3 * ng + 3 + ng];
   return true;
 }
 
 // What a producer publishes with each stage.
 struct CqInfo {
-  int32_t g, c0, rt, valid, wrows, pstart, chunk, next_chunk;
+  int32_t g, c0, rt, valid, wrows, pstart, pidx;
 };
 struct CqShared {
   uint64_t full_a[kCqMaxStages];   // pass 1: the tile landed
   uint64_t empty_a[kCqMaxStages];  // pass 1: the amax warps are done with the stage
-  uint64_t full_b[kCqMaxStages];   // pass 2: the tile and its 64 maxima landed (1 + 32 arrivals)
+  uint64_t full_b[kCqMaxStages];   // pass 2: the tile landed and its maxima were gathered (2 arrivals)
   uint64_t empty_b[kCqMaxStages];  // pass 2: the cast warps are done with the stage
   CqInfo info_a[kCqMaxStages], info_b[kCqMaxStages];
-  uint32_t am[kCqMaxStages][64];   // pass 2: the amax words of the stage's 64 columns
+  uint32_t am[kCqMaxStages][32];   // pass 2: the stage's 64 column maxima, packed bf16 pairs
   uint32_t red[kCqP1Warps][8][4];
-  uint64_t slot_full[kCqPubs][kCqSlots];   // a unit's 64 column maxima (32 packed words) are in the slot
-  uint64_t slot_empty[kCqPubs][kCqSlots];  // the publisher has taken them
-  uint32_t slot[kCqPubs][kCqSlots][32];
-  int32_t slot_g[kCqPubs][kCqSlots], slot_c0[kCqPubs][kCqSlots];  // slot_g -1: no more units
-  int32_t slot_chunk[kCqPubs][kCqSlots], slot_next[kCqPubs][kCqSlots];
   int32_t p2_next;                 // this CTA's next pass-2 unit: all of its units below are issued
   int abort;
 };
@@ -239,20 +225,6 @@ FP8_DEVI void cq_fail(volatile int* abort, int32_t* status) {
   if (!*abort) {
     *abort = 1;
     set_status(status, FP8_DEV_TIMEOUT);
-  }
-}
-
-// Bounded wait until a chunk's completion word reaches `target` (acquire), giving up when
-// another role of the CTA has aborted.
-FP8_DEVI bool cq_wait_done(const uint32_t* w, uint32_t target, const volatile int* abort, uint64_t limit_ns) {
-  if (ld_acquire_gpu(w) >= target) return true;
-  const uint64_t t0 = globaltimer();
-  uint32_t ns = 32;
-  for (;;) {
-    __nanosleep(ns);
-    if (ns < 256) ns <<= 1;
-    if (ld_acquire_gpu(w) >= target) return true;
-    if (*abort || globaltimer() - t0 > limit_ns) return false;
   }
 }
 
@@ -268,10 +240,17 @@ FP8_DEVI bool cq_wait_lead(const volatile int32_t* p2_next, int32_t target, cons
   }
 }
 
-FP8_DEVI void cp_async16_cg(void* smem_dst, const void* gsrc, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
-               "r"(valid ? 16 : 0)
+// The 16-byte vector at p (gpu scope: another SM's stores become visible to it).
+FP8_DEVI uint4 ld_relaxed_v4(const uint32_t* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
                : "memory");
+  return v;
+}
+FP8_DEVI void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 template <int FMT>
@@ -289,8 +268,8 @@ __global__ void __launch_bounds__(kCqThreads, 1) colpipe_kernel(const __grid_con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const CqShape dense = p.mode == 2 ? CqShape{0, 1, 0} : cq_shape(p.group_rows, p.n_strips, p.chunk_units);
-  int32_t M, NC;
-  if (!cq_setup(p, pre, dense, &M, &NC)) return;
+  int32_t M;
+  if (!cq_setup(p, pre, dense, &M)) return;
   static_assert(sizeof(ScaleTab) % 4 == 0, "table words");
   for (int i = tid; i < (int)(sizeof(ScaleTab) / 4); i += blockDim.x)
     reinterpret_cast<uint32_t*>(&stab)[i] = reinterpret_cast<const uint32_t*>(&tab)[i];
@@ -299,14 +278,9 @@ __global__ void __launch_bounds__(kCqThreads, 1) colpipe_kernel(const __grid_con
     for (int s = 0; s < kCqMaxStages; ++s) {
       mbar_init(&S.full_a[s], 1);
       mbar_init(&S.empty_a[s], kCqP1Warps);
-      mbar_init(&S.full_b[s], 1 + 32);
+      mbar_init(&S.full_b[s], 2);
       mbar_init(&S.empty_b[s], kCqP2Warps);
     }
-    for (int j = 0; j < kCqPubs; ++j)
-      for (int s = 0; s < kCqSlots; ++s) {
-        mbar_init(&S.slot_full[j][s], 1);
-        mbar_init(&S.slot_empty[j][s], 1);
-      }
     fence_mbar_init();
     S.abort = 0;
     S.p2_next = cnt > 0 ? (int32_t)blockIdx.x : INT32_MAX;
@@ -339,7 +313,6 @@ __global__ void __launch_bounds__(kCqThreads, 1) colpipe_kernel(const __grid_con
         const int32_t i = (int32_t)blockIdx.x + k * (int32_t)gridDim.x;
         const CqUnit u = nx;
         if (k + 1 < cnt) nx = cq_unit(p, i + (int32_t)gridDim.x, pre, dense);
-        const int32_t next_chunk = k + 1 < cnt ? nx.chunk : NC;
         // the lead over pass 2: at most lag units, and no unit of a chunk before pass 2 has
         // issued everything below the chunk
         const int32_t lead = min(i - p.lag_units, u.chunk_first);
@@ -347,7 +320,7 @@ __global__ void __launch_bounds__(kCqThreads, 1) colpipe_kernel(const __grid_con
           cq_fail(abort, p.status);
           break;
         }
-        S.info_a[s] = CqInfo{u.g, u.c0, u.rt, u.valid, u.wrows, u.pstart, u.chunk, next_chunk};
+        S.info_a[s] = CqInfo{u.g, u.c0, u.rt, u.valid, u.wrows, u.pstart, u.pbase + u.rt / kCqTile};
         mbar_arrive_expect_tx(&S.full_a[s], kCqStageBytes);
         tma_load_2d_hint(ring_a + s * kCqStageBytes, &tm_in, &S.full_a[s], u.c0, u.row, pol);
         if (++s == p.stages_a) {
@@ -360,103 +333,94 @@ __global__ void __launch_bounds__(kCqThreads, 1) colpipe_kernel(const __grid_con
         mbar_wait(&S.full_a[j % p.stages_a], (uint32_t)((j / p.stages_a) & 1), nullptr, kCqDrainNs);
     }
   } else if (warp == 1) {
-    // ==== pass-2 producer: per unit, once its chunk's maxima are final, the tile (from L2) by ====
-    // TMA and its 64 amax words by asynchronous copies that arrive on the stage's barrier
-    const uint64_t pol = l2_evict_first();  // the tile's last use
-    const uint32_t need = gridDim.x + (p.test_stall ? 1u : 0u);
-    int s = 0;
-    uint32_t ph = 0;
-    int32_t k = 0, have = -1;  // the chunk whose maxima are known final
-    CqUnit nx = {};
-    if (cnt > 0) nx = cq_unit(p, (int32_t)blockIdx.x, pre, dense);
-    for (; k < cnt; ++k) {
-      const int32_t i = (int32_t)blockIdx.x + k * (int32_t)gridDim.x;
-      const CqUnit u = nx;
-      if (k + 1 < cnt) nx = cq_unit(p, i + (int32_t)gridDim.x, pre, dense);
-      bool got = true;
-      if (lane == 0) {
-        got = mbar_wait(&S.empty_b[s], ph ^ 1, abort, p.wait_ns);
-        if (got && !p.given && u.chunk != have) {
-          got = cq_wait_done(p.done + u.chunk, need, abort, p.wait_ns);
-          have = u.chunk;
-        }
-      }
-      __syncwarp();  // the acquire orders the lanes' reads of the maxima after the chunk's pass 1
-      if (!__shfl_sync(0xffffffffu, got, 0)) {
-        if (lane == 0) cq_fail(abort, p.status);
-        break;
-      }
-      if (lane == 0) {
-        S.info_b[s] = CqInfo{u.g, u.c0, u.rt, u.valid, u.wrows, u.pstart, u.chunk, 0};
-        mbar_arrive_expect_tx(&S.full_b[s], kCqStageBytes);
-        tma_load_2d_hint(ring_b + s * kCqStageBytes, &tm_in, &S.full_b[s], u.c0, u.row, pol);
-      }
-      const uint32_t* arow = p.amax + (int64_t)u.g * p.C;
-      if (p.given) {  // caller's fp32 words (4-byte aligned)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t col = u.c0 + lane + 32 * h;
-          cp_async4(&S.am[s][lane + 32 * h], arow + (col < p.C ? col : 0), col < p.C);
-        }
-      } else if (lane < 16) {  // the kernel's own words: 16 bytes each, not cached in L1
-        const int64_t col = u.c0 + 4 * lane;
-        cp_async16_cg(&S.am[s][4 * lane], arow + (col < p.C ? col : 0), col < p.C);
-      }
-      cp_async_arrive_noinc(&S.full_b[s]);
-      if (lane == 0) *p2_next = i + (int32_t)gridDim.x;
-      if (++s == p.stages_b) {
-        s = 0;
-        ph ^= 1;
-      }
-    }
-    cp_async_wait<0>();  // no copy lands after the CTA has left
-    if (lane == 0)
-      for (int32_t j = k > p.stages_b ? k - p.stages_b : 0; j < k; ++j)
-        mbar_wait(&S.full_b[j % p.stages_b], (uint32_t)((j / p.stages_b) & 1), nullptr, kCqDrainNs);
-  } else if (warp < kCqP1Warp0) {
-    // ==== publishers: the atomic column maxima of each pass-1 unit and the chunk completions ====
-    // Publisher j takes the units of the chunks c with c % kCqPubs == j; a lane takes a column
-    // pair of the unit: one relaxed atomic max per column. After the CTA's last unit of a chunk
-    // the chunk is complete for this CTA, and the publisher counts it at once (a fence for the
-    // lanes' maxima, then the count; chunks in which the CTA has no unit are counted with it), so
-    // one publisher's fence overlaps the other's work.
-    const int j = warp - 2;
-    if (!p.given) {
-      auto count = [&](int32_t from, int32_t to, bool fence) {
-        if (from >= to) return;
-        if (fence) asm volatile("fence.acq_rel.gpu;" ::: "memory");  // every lane's maxima, then the counts
-        __syncwarp();
-        if (lane == 0) {
-          if (fence) asm volatile("fence.acq_rel.gpu;" ::: "memory");
-          for (int32_t c = from; c < to; ++c)
-            asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(p.done + c) : "memory");
-        }
-      };
-      if (j == 0) count(0, cnt > 0 ? cq_unit(p, (int32_t)blockIdx.x, pre, dense).chunk : NC, false);
+    // ============ pass-2 producer: one lane streams the CTA's units again (from L2) ============
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first();  // the tile's last use
       int s = 0;
       uint32_t ph = 0;
-      for (;;) {
-        const bool got = lane == 0 ? mbar_wait(&S.slot_full[j][s], ph, abort, p.wait_ns) : true;
-        if (!__shfl_sync(0xffffffffu, got, 0)) {
-          if (lane == 0) cq_fail(abort, p.status);
+      int32_t k = 0;
+      for (; k < cnt; ++k) {
+        const int32_t i = (int32_t)blockIdx.x + k * (int32_t)gridDim.x;
+        const CqUnit u = cq_unit(p, i, pre, dense);
+        if (!mbar_wait(&S.empty_b[s], ph ^ 1, abort, p.wait_ns)) {
+          cq_fail(abort, p.status);
           break;
         }
-        const int32_t g = S.slot_g[j][s];
-        if (g < 0) break;  // the CTA's units are all handed over
-        const uint32_t m = S.slot[j][s][lane];
-        const int64_t col = S.slot_c0[j][s] + 2 * lane;
-        uint32_t* aw = p.amax + (int64_t)g * p.C + col;
-        const int32_t chunk = S.slot_chunk[j][s], next = S.slot_next[j][s];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.slot_empty[j][s]);
-        if (++s == kCqSlots) {
+        S.info_b[s] = CqInfo{u.g, u.c0, u.rt, u.valid, u.wrows, u.pstart, 0};
+        mbar_arrive_expect_tx(&S.full_b[s], kCqStageBytes);
+        tma_load_2d_hint(ring_b + s * kCqStageBytes, &tm_in, &S.full_b[s], u.c0, u.row, pol);
+        *p2_next = i + (int32_t)gridDim.x;
+        if (++s == p.stages_b) {
           s = 0;
           ph ^= 1;
         }
-        if (col < p.C && (m & 0xFFFFu)) red_max_relaxed(aw, m & 0xFFFFu);
-        if (col + 1 < p.C && (m >> 16)) red_max_relaxed(aw + 1, m >> 16);
-        count(chunk, next, true);
       }
+      for (int32_t j = k > p.stages_b ? k - p.stages_b : 0; j < k; ++j)  // loads in flight land before exit
+        mbar_wait(&S.full_b[j % p.stages_b], (uint32_t)((j / p.stages_b) & 1), nullptr, kCqDrainNs);
+    }
+  } else if (warp < kCqP1Warp0) {
+    // = pass-2 gatherers: each unit's 64 column maxima into its stage (unit k: warp k % gathers) =
+    // A strip's maxima are the maxima of its row tiles' partials, each written once by pass 1
+    // with bit 15 set in every 16-bit field: a field without it is not written yet, so the warp
+    // polls (bounded) until all are, with no counter or fence between the passes. Lane l reads
+    // 16-byte vector l % 8 (8 columns) of the row tiles l / 8, l / 8 + 4, ...
+    // The gatherers wait on the stages' empty barriers out of order; a parity wait is exact only
+    // while its waiter is at most one phase ahead, which holds when gathers <= stages_b: a warp's
+    // previous unit k - gathers needed unit k - gathers - stages_b consumed, and the cast warps
+    // consume in order, so the stage's use before the previous one is complete.
+    const int gw = warp - 2;
+    const int q = lane & 7, r0 = lane >> 3;
+    for (int32_t k = gw; k < cnt && gw < p.gathers; k += p.gathers) {
+      const int s = k % p.stages_b;
+      const CqUnit u = cq_unit(p, (int32_t)blockIdx.x + k * (int32_t)gridDim.x, pre, dense);
+      const bool free = lane == 0 ? mbar_wait(&S.empty_b[s], (uint32_t)(((k / p.stages_b) & 1) ^ 1), abort, p.wait_ns) : true;
+      if (!__shfl_sync(0xffffffffu, free, 0)) {
+        if (lane == 0) cq_fail(abort, p.status);
+        break;
+      }
+      if (p.given) {  // the caller's fp32 words hold bf16 values: their upper halves
+        const uint32_t* arow = p.amax + (int64_t)u.g * p.C;
+        const int64_t col = u.c0 + 2 * lane;
+        const uint32_t lo = col < p.C ? arow[col] >> 16 : 0u, hi = col + 1 < p.C ? arow[col + 1] >> 16 : 0u;
+        S.am[s][lane] = (lo & 0x7FFFu) | ((hi & 0x7FFFu) << 16);
+      } else {
+        const uint32_t* base = p.part + (int64_t)u.pbase * 32 + 4 * q;
+        uint4 acc = make_uint4(0, 0, 0, 0);
+        bool ok = true;
+        for (int32_t r = r0; r < u.rtn && ok; r += 4) {
+          uint4 v = ld_relaxed_v4(base + (int64_t)r * 32);
+          bool done = !p.test_stall && ((v.x & v.y & v.z & v.w & kCqWritten) == kCqWritten);
+          if (!done) {
+            const uint64_t t0 = globaltimer();
+            while (!done) {
+              __nanosleep(64);
+              v = ld_relaxed_v4(base + (int64_t)r * 32);
+              done = !p.test_stall && ((v.x & v.y & v.z & v.w & kCqWritten) == kCqWritten);
+              if (!done && (*abort || globaltimer() - t0 > p.wait_ns)) {
+                ok = false;
+                break;
+              }
+            }
+          }
+          acc = make_uint4(__vmaxu2(acc.x, v.x), __vmaxu2(acc.y, v.y), __vmaxu2(acc.z, v.z), __vmaxu2(acc.w, v.w));
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) cq_fail(abort, p.status);
+          break;
+        }
+#pragma unroll
+        for (int d = 8; d <= 16; d <<= 1) {
+          acc.x = __vmaxu2(acc.x, __shfl_xor_sync(0xffffffffu, acc.x, d));
+          acc.y = __vmaxu2(acc.y, __shfl_xor_sync(0xffffffffu, acc.y, d));
+          acc.z = __vmaxu2(acc.z, __shfl_xor_sync(0xffffffffu, acc.z, d));
+          acc.w = __vmaxu2(acc.w, __shfl_xor_sync(0xffffffffu, acc.w, d));
+        }
+        if (lane < 8)
+          *reinterpret_cast<uint4*>(&S.am[s][4 * q]) = make_uint4(acc.x & 0x7FFF7FFFu, acc.y & 0x7FFF7FFFu,
+                                                                  acc.z & 0x7FFF7FFFu, acc.w & 0x7FFF7FFFu);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.full_b[s]);
     }
   } else if (warp < kCqP2Warp0) {
     // ============ pass-1 amax warps: thread = 4 rows x 8 columns of 4 row groups per tile ============
@@ -465,45 +429,10 @@ __global__ void __launch_bounds__(kCqThreads, 1) colpipe_kernel(const __grid_con
       const int ch = lane & 7, rq = lane >> 3;
       int s = 0;
       uint32_t ph = 0;
-      int sl[kCqPubs] = {};
-      uint32_t sph[kCqPubs] = {};
-      // hands a unit's maxima (or, with g = -1, the end) to publisher j
-      auto hand_over = [&](int jp, int32_t g, int32_t c0, int32_t chunk, int32_t next, uint32_t m) {
-        int q = 0;
-        uint32_t qph = 0;
-#pragma unroll
-        for (int t = 0; t < kCqPubs; ++t)
-          if (t == jp) {
-            q = sl[t];
-            qph = sph[t];
-          }
-        const bool free = lane == 0 ? mbar_wait(&S.slot_empty[jp][q], qph ^ 1, abort, p.wait_ns) : true;
-        if (!__shfl_sync(0xffffffffu, free, 0)) {
-          if (lane == 0) cq_fail(abort, p.status);  // the next stage wait sees the abort
-          return;
-        }
-        S.slot[jp][q][lane] = m;
-        if (lane == 0) {
-          S.slot_g[jp][q] = g;
-          S.slot_c0[jp][q] = c0;
-          S.slot_chunk[jp][q] = chunk;
-          S.slot_next[jp][q] = next;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.slot_full[jp][q]);
-#pragma unroll
-        for (int t = 0; t < kCqPubs; ++t)
-          if (t == jp && ++sl[t] == kCqSlots) {
-            sl[t] = 0;
-            sph[t] ^= 1;
-          }
-      };
-      bool finished = true;
       for (int32_t k = 0; k < cnt; ++k) {
         const bool got = mbar_wait(&S.full_a[s], ph, abort, p.wait_ns);
         if (!named_bar_and(2, kCqP1Threads, got)) {  // uniform decision across the amax warps
           if (!got) cq_fail(abort, p.status);
-          finished = false;
           break;
         }
         const CqInfo info = S.info_a[s];
@@ -547,16 +476,14 @@ __global__ void __launch_bounds__(kCqThreads, 1) colpipe_kernel(const __grid_con
           for (int q = 0; q < 4; ++q) S.red[cw][ch][q] = m4[q];
         }
         named_bar_sync(1, kCqP1Threads);
-        if (cw == 0) {  // pair t = columns 2t, 2t+1 = chunk t/4, word t%4: to the chunk's publisher
+        if (cw == 0) {  // pair t = columns 2t, 2t+1 = chunk t/4, word t%4: the unit's partial
           uint32_t m = 0;
 #pragma unroll
           for (int w = 0; w < kCqP1Warps; ++w) m = __vmaxu2(m, S.red[w][lane >> 2][lane & 3]);
-          hand_over(info.chunk % kCqPubs, info.g, info.c0, info.chunk, info.next_chunk, m);
+          st_relaxed_u32(p.part + (int64_t)info.pidx * 32 + lane, m | kCqWritten);
         }
         named_bar_sync(1, kCqP1Threads);  // red[] is free again
       }
-      if (cw == 0 && finished && !*abort)
-        for (int jp = 0; jp < kCqPubs; ++jp) hand_over(jp, -1, 0, 0, 0, 0u);
     }
   } else {
     // ====== pass-2 cast warps: each casts 32 rows x 64 columns of a tile and stores them ======
@@ -580,8 +507,8 @@ __global__ void __launch_bounds__(kCqThreads, 1) colpipe_kernel(const __grid_con
       const CqInfo info = S.info_b[s];
       // the scale step for the lane's two columns (table in shared memory); the first row tile
       // of a strip also writes their inverse scales
-      const uint2 am2 = *reinterpret_cast<const uint2*>(&S.am[s][2 * lane]);
-      const Scale sv_lo = tab_scale(stab, am2.x >> p.amax_shift), sv_hi = tab_scale(stab, am2.y >> p.amax_shift);
+      const uint32_t am2 = S.am[s][lane];
+      const Scale sv_lo = tab_scale(stab, am2 & 0xFFFFu), sv_hi = tab_scale(stab, am2 >> 16);
       if (info.rt == 0 && cw == 0) {
         const int64_t col = info.c0 + 2 * lane;
         if (col < p.C) p.inv[(int64_t)info.g * p.C + col] = sv_lo.inv32;
@@ -650,10 +577,11 @@ size_t cq_smem(int sa, int sb, size_t pre) {
 
 }  // namespace
 
-// Workspace words of a column quantize: the amax per (group, column), then a completion word per
-// chunk (at most one per 64-column strip of each group), each part rounded to 16 bytes.
-int64_t col_ws_words(int64_t groups, int64_t C) {
-  return round_up64(groups * C, 4) + round_up64(groups * ceil_div64(C, 64), 4);
+// Workspace words of a column quantize: one partial (32 words: the 64 column maxima of a
+// 256-row x 64-column unit) per unit; a group of n rows has ceil(n / 256) units per 64-column
+// strip, so rows_total / 256 + groups bounds the row tiles of all groups.
+int64_t col_ws_words(int64_t groups, int64_t C, int64_t rows_total) {
+  return (ceil_div64(rows_total, kCqTile) + groups) * ceil_div64(C, 64) * 32;
 }
 
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,
@@ -662,7 +590,6 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   if (n_groups == 0 || C == 0) return FP8_OK;
   if (ends && n_groups > kCqMaxSegments) return FP8_ERR_UNSUPPORTED;
   if (rows_total > INT32_MAX) return FP8_ERR_UNSUPPORTED;  // rows are TMA coordinates
-  if (!amax_given && C % 4 != 0) return FP8_ERR_UNSUPPORTED;  // 16-byte copies of the amax words
   CqParams p = {};
   p.ends = ends;
   p.C = C;
@@ -701,20 +628,19 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   }
 
   if (amax_given) {
-    p.amax = const_cast<uint32_t*>(amax_given);  // read only (pass 2)
-    p.amax_shift = 16;
+    p.amax = amax_given;  // read only (pass 2 alone)
     p.given = 1;
-  } else {
-    if (cudaMemsetAsync(scratch, 0, (size_t)col_ws_words(n_groups, C) * 4, c.stream) != cudaSuccess) return FP8_ERR_CUDA;
-    p.amax = scratch;
-    p.done = scratch + round_up64(n_groups * C, 4);
+  } else {  // every partial starts unwritten
+    if (cudaMemsetAsync(scratch, 0, (size_t)col_ws_words(n_groups, C, rows_total) * 4, c.stream) != cudaSuccess)
+      return FP8_ERR_CUDA;
+    p.part = scratch;
   }
   // units: exact for dense groups; for segments an upper bound (each segment adds at most one
   // partial tile) -- the kernel computes the exact count from the offsets
   const int64_t units = ends ? (ceil_div64(rows_total, kCqTile) + n_groups) * p.n_strips
                              : n_groups * ceil_div64(group_rows, kCqTile) * p.n_strips;
   if (units > INT32_MAX - 2 * (int64_t)c.sm_count - kCqLagUnits) return FP8_ERR_UNSUPPORTED;  // 32-bit unit indices
-  const size_t pre = ends ? 16 * (size_t)(n_groups + 1) : 0;
+  const size_t pre = ends ? 12 * (size_t)(n_groups + 1) : 0;
   // two rings of 32 KB stages: 3 + 3 where the segment tables leave room, else fewer
   int sa = 3, sb = 3;
   if (cq_smem(sa, sb, pre) > kCqSmemMax) sb = 2;
@@ -722,6 +648,7 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
   if (cq_smem(sa, sb, pre) > kCqSmemMax) return FP8_ERR_UNSUPPORTED;
   p.stages_a = sa;
   p.stages_b = sb;
+  p.gathers = kCqGathers < sb ? kCqGathers : sb;
   const size_t smem = cq_smem(sa, sb, pre) - sizeof(ScaleTab);  // the table is static shared memory
   const int64_t grid = units > 0 ? (units < c.sm_count ? units : c.sm_count) : 1;
   const ScaleTab& tab = scale_tab(fmt);
@@ -730,7 +657,7 @@ int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_gr
     return FP8_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: they wait on one another's chunks
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: they wait on one another's maxima
   attr[0].val.cooperative = 1;
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kCqThreads);

@@ -49,10 +49,11 @@ int launch_quant_tensor_stash(const void* x, int64_t R, int64_t C, int fmt, void
 // scale per column: either n_groups consecutive groups of group_rows rows (ends == null) or the
 // segments given by ends[n_groups] (segment-padded output, padded row count ld_out).
 // out_t row (g, c) starts at out_t + (g * C + c) * ld_out (dense) or out_t + c * ld_out + pstart_g
-// (segments). inv [n_groups, C]. scratch: col_ws_words(n_groups, C) words of device memory, 16-byte
-// aligned; C % 4 == 0 unless the maxima are given.
-// Workspace words (4 bytes each) a column quantize of `groups` x C scales needs.
-int64_t col_ws_words(int64_t groups, int64_t C);
+// (segments). inv [n_groups, C]. scratch: col_ws_words(n_groups, C, rows_total) words of device
+// memory, 16-byte aligned (unused when the maxima are given).
+// Workspace words (4 bytes each) a column quantize of `groups` x C scales over rows_total rows of
+// input (all groups) needs.
+int64_t col_ws_words(int64_t groups, int64_t C, int64_t rows_total);
 // amax_given (optional): the column maxima as fp32 words [n_groups, C] (bf16 values); pass 1 is
 // skipped and scratch is not used.
 int launch_quant_cols(const void* x, int64_t rows_total, int64_t C, int64_t n_groups, int64_t group_rows,

@@ -35,10 +35,10 @@ def test_host_helpers(fp8):
         assert P % 128 == 0 and R + 127 * E <= P < R + 127 * E + 128
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_TENSOR) == 8
     assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, granularity=fp8.GRAN_ROW) == 0
-    # one amax word per (group, column), then one completion count per (group, 64-column strip),
-    # each part rounded up to 16 bytes
-    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 16, 5120, granularity=fp8.GRAN_COL) == 16 * 5120 * 4 + 16 * 80 * 4
-    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 1, 70, granularity=fp8.GRAN_COL) == 72 * 4 + 4 * 4
+    # one 128-byte partial (64 column maxima) per 256-row x 64-column unit: (rows / 256 + groups)
+    # row tiles bound the units of every 64-column strip
+    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 16, 5120, 16 * 8192, granularity=fp8.GRAN_COL) == (512 + 16) * 80 * 128
+    assert fp8.fp8_workspace_size(fp8.OP_QUANTIZE, 1, 70, 300, granularity=fp8.GRAN_COL) == (2 + 1) * 2 * 128
     M, K, N = 256, 512, 128
     ws_row_bf16 = fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_ROW, fp8.WGRAD_BF16)
     ws_row_fp8 = fp8.fp8_workspace_size(fp8.OP_LINEAR_BWD, M, K, N, fp8.GRAN_ROW, fp8.WGRAD_FP8)

@@ -150,7 +150,7 @@ def test_quantize_cols(fp8, R, C):
     qt = Guarded((C, R), torch.float8_e4m3fn)
     inv = Guarded((C,), torch.float32)
     fp8.fp8_quantize(x.cuda(), fp8.GRAN_COL, fp8.DT_E4M3, fp8.LAYOUT_COL_MAJOR, None, qt.t, inv.t, None,
-                     fp8.col_workspace(1, C, "cuda"))
+                     fp8.col_workspace(1, C, R, "cuda"))
     torch.cuda.synchronize()
     assert qt.intact() and inv.intact()
     qo, io = oracle.quantize_cols(bits(x), oracle.E4M3)
@@ -167,7 +167,7 @@ def test_quantize_jagged_cols(fp8):
     inv = Guarded((E, C), torch.float32)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     fp8.fp8_quantize(x.cuda(), fp8.GRAN_COL, fp8.DT_E5M2, fp8.LAYOUT_COL_MAJOR, None, qt.t, inv.t,
-                     torch.from_numpy(ends).cuda(), fp8.col_workspace(E, C, "cuda"), status=st)
+                     torch.from_numpy(ends).cuda(), fp8.col_workspace(E, C, M, "cuda"), status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and qt.intact() and inv.intact()
     qo, io = oracle.quantize_jagged_cols(bits(x), ends, oracle.E5M2)

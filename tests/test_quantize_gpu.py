@@ -174,7 +174,7 @@ def test_jagged_colwise(fp8, counts, fi):
     inv = torch.empty((len(counts), C), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     fp8.fp8_quantize(x.cuda(), fp8.GRAN_COL, dt, fp8.LAYOUT_COL_MAJOR, None, canary, inv,
-                     torch.from_numpy(ends).cuda(), fp8.col_workspace(len(counts), C, "cuda"), status=st)
+                     torch.from_numpy(ends).cuda(), fp8.col_workspace(len(counts), C, R, "cuda"), status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     q_ref, inv_ref = oracle.quantize_jagged_cols(bits(x), ends, ofmt)
@@ -197,7 +197,7 @@ def test_jagged_colwise_wide(fp8, counts):
     inv = torch.empty((len(counts), C), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     fp8.fp8_quantize(x.cuda(), fp8.GRAN_COL, fp8.DT_E5M2, fp8.LAYOUT_COL_MAJOR, None, out, inv,
-                     torch.from_numpy(ends).cuda(), fp8.col_workspace(len(counts), C, "cuda"), status=st)
+                     torch.from_numpy(ends).cuda(), fp8.col_workspace(len(counts), C, R, "cuda"), status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     q_ref, inv_ref = oracle.quantize_jagged_cols(bits(x), ends, oracle.E5M2)
@@ -222,7 +222,7 @@ def test_jagged_colwise_segment_limit(fp8):
         inv = torch.empty((E, C), dtype=torch.float32, device="cuda")
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         args = (x.cuda(), fp8.GRAN_COL, fp8.DT_E4M3, fp8.LAYOUT_COL_MAJOR, None, out, inv,
-                torch.from_numpy(ends).cuda(), fp8.col_workspace(E, C, "cuda"))
+                torch.from_numpy(ends).cuda(), fp8.col_workspace(E, C, R, "cuda"))
         if not ok:
             with pytest.raises(fp8.Fp8Error) as e:
                 fp8.fp8_quantize(*args, status=st)
@@ -247,7 +247,7 @@ def test_jagged_bad_offsets_sets_status(fp8):
     for bad in ([10, 5, 64], [10, 20, 63]):
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         fp8.fp8_quantize(x, fp8.GRAN_COL, fp8.DT_E4M3, fp8.LAYOUT_COL_MAJOR, None, out, inv,
-                         torch.tensor(bad, dtype=torch.int32, device="cuda"), fp8.col_workspace(3, 8, "cuda"), status=st)
+                         torch.tensor(bad, dtype=torch.int32, device="cuda"), fp8.col_workspace(3, 8, 100, "cuda"), status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == fp8.DEV_BAD_OFFSETS
 
