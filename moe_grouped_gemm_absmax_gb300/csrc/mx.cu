@@ -231,6 +231,90 @@ __global__ void __launch_bounds__(1024) mx_pstart_kernel(const int32_t* ends, in
   }
 }
 
+// Row-major output alone: teams of WPR warps per row walk the rows (grid-stride), like the
+// row-wise FP8 kernel: a lane holds vectors t, t + TPR, ... of 8 bf16, so the four lanes 4k .. 4k + 3
+// of a load step hold one block of 32 (two shuffles give its amax) and 16 lanes hold one
+// 128-column scale word (four block codes gathered by shuffles, written by the first lane).
+// With segments the scales go to the padded row of the row's segment (pstart[e] + row - start_e);
+// the team's rows increase, so its segment index only moves forward.
+constexpr int kMxRowVPL = 16;  // vectors of 8 per lane: rows of up to 16 * 32 * WPR * 8 elements
+template <int FMT, int WPR, bool JAG>
+__global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* __restrict__ x, int64_t rows, int64_t R,
+                                                      int nvec, uint2* __restrict__ q, uint8_t* __restrict__ sf,
+                                                      int64_t rb_q, const int32_t* __restrict__ pstart,
+                                                      const int32_t* __restrict__ ends, int E) {
+  constexpr int TPR = 32 * WPR;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int team = warp / WPR, t = threadIdx.x % TPR;
+  const int64_t team0 = (int64_t)blockIdx.x * (8 / WPR) + team;
+  const int64_t nteams = (int64_t)gridDim.x * (8 / WPR);
+  const int64_t ncb = nvec / 16;  // 128-column scale blocks per row
+  if (JAG && __ldg(pstart + E) == 0) return;  // offsets rejected: nothing is written
+  int e = 0;
+  for (int64_t r = team0; r < rows; r += nteams) {
+    int64_t b = 0, pr = r;  // batch entry; the row's position in the scale layout
+    if (JAG) {
+      while (e < E - 1 && __ldg(ends + e) <= r) ++e;
+      pr = __ldg(pstart + e) + (r - (e ? __ldg(ends + e - 1) : 0));
+    } else {
+      b = r / R;
+      pr = r - b * R;
+    }
+    const uint4* xr = x + r * nvec;
+    uint4 v[kMxRowVPL];
+#pragma unroll
+    for (int i = 0; i < kMxRowVPL; ++i) {
+      const int c = t + TPR * i;
+      v[i] = c < nvec ? ld_nc_v4(xr + c) : make_uint4(0, 0, 0, 0);
+    }
+    uint2* qr = q + r * nvec;
+    uint8_t* srow = sf + (b * rb_q + (pr >> 7)) * ncb * 512 + (pr & 31) * 16 + ((pr >> 5) & 3) * 4;
+#pragma unroll
+    for (int i = 0; i < kMxRowVPL; ++i) {
+      const int c = t + TPR * i;
+      if (TPR * i >= nvec) break;  // uniform: nvec % 16 == 0 and every lane's c < nvec below it
+      uint32_t m = absmax_fold(absmax_vec8(0u, v[i]));
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      const uint32_t code = mx_code<FMT>(m);
+      const float inv = mx_inv(code);
+      const int hb = lane & 16;
+      const uint32_t word = __shfl_sync(0xffffffffu, code, hb) | (__shfl_sync(0xffffffffu, code, hb + 4) << 8) |
+                            (__shfl_sync(0xffffffffu, code, hb + 8) << 16) |
+                            (__shfl_sync(0xffffffffu, code, hb + 12) << 24);
+      if (c < nvec) {
+        uint2 o;
+        o.x = mx_cast2<FMT>(v[i].x, inv) | (mx_cast2<FMT>(v[i].y, inv) << 16);
+        o.y = mx_cast2<FMT>(v[i].z, inv) | (mx_cast2<FMT>(v[i].w, inv) << 16);
+        qr[c] = o;
+        if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(srow + (int64_t)(c / 16) * 512) = word;
+      }
+    }
+  }
+}
+
+template <int FMT, int WPR, bool JAG>
+int run_mx_rows(const MxArgs& a, int64_t rows, const Ctx& c) {
+  auto kern = mx_rows_kernel<FMT, WPR, JAG>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+  const int64_t slots = (int64_t)c.sm_count * per_sm * (8 / WPR);  // teams resident at once
+  const int64_t waves = ceil_div64(rows, slots);
+  const int64_t teams = ceil_div64(rows, waves);
+  kern<<<(unsigned)ceil_div64(teams, 8 / WPR), 256, 0, c.stream>>>(
+      reinterpret_cast<const uint4*>(a.x), rows, a.R, (int)(a.C / 8), reinterpret_cast<uint2*>(a.q), a.sf, a.rb_q,
+      a.pstart, a.ends, a.E);
+  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+template <int FMT, bool JAG>
+int dispatch_mx_rows(const MxArgs& a, int64_t rows, const Ctx& c) {
+  const int nvec = (int)(a.C / 8);
+  if (nvec <= 32 * kMxRowVPL) return run_mx_rows<FMT, 1, JAG>(a, rows, c);
+  if (nvec <= 64 * kMxRowVPL) return run_mx_rows<FMT, 2, JAG>(a, rows, c);
+  return run_mx_rows<FMT, 4, JAG>(a, rows, c);
+}
+
 template <int FMT, bool ROWS, bool COLS, bool JAG>
 int run_mx(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) {
   auto kern = mx_quant_kernel<FMT, ROWS, COLS, JAG>;
@@ -245,6 +329,8 @@ int run_mx(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) {
 template <int FMT, bool JAG>
 int dispatch_layout(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) {
   if (a.q && a.qt) return run_mx<FMT, true, true, JAG>(a, grid_y, batches, c);
+  // the row-major output alone by row teams, for rows of up to 4 * 32 * 16 vectors of 8
+  if (a.q && a.C / 8 <= 128 * kMxRowVPL) return dispatch_mx_rows<FMT, JAG>(a, a.R * batches, c);
   if (a.q) return run_mx<FMT, true, false, JAG>(a, grid_y, batches, c);
   return run_mx<FMT, false, true, JAG>(a, grid_y, batches, c);
 }

@@ -72,7 +72,7 @@ def _mx_rows_input(R, C, seed):
 # ---------------------------------------------------------------------------- quantize
 
 @pytest.mark.parametrize("shape,fmt", [((256, 256), E4), ((300, 384), E4), ((77, 128), E5), ((3, 128, 384), E4),
-                                       ((1, 1024), E5)])
+                                       ((1, 1024), E5), ((70, 7168), E4), ((40, 12288), E5), ((2, 9, 4096), E4)])
 def test_mx_quantize_rows(fp8, shape, fmt):
     x = _mx_rows_input(int(np.prod(shape[:-1])), shape[-1], 3).reshape(shape)
     q, _, sf, _ = fp8.mx_quantize_alloc(x.cuda(), TDT[fmt], fp8.LAYOUT_ROW_MAJOR)
@@ -126,6 +126,25 @@ def test_mx_quantize_jagged(fp8, counts, C, fmt):
     assert np.array_equal(mx_unblock(sft, C, P)[:, :used // 32], so)
     qr, sr = oracle.mx_quantize_rows(bits(x), fmt)
     assert np.array_equal(codes(q), qr)
+    sfr = mx_unblock(sf, P, C)
+    starts, cnts, pstarts, _ = oracle.mx_padded_segments(ends)
+    for s0, c, ps in zip(starts, cnts, pstarts):
+        assert np.array_equal(sfr[ps:ps + c], sr[s0:s0 + c])
+
+
+@pytest.mark.parametrize("counts,C,fmt", [([40, 0, 200, 1, 130], 256, E5), ([300, 17, 0, 0, 256, 90], 7168, E4)])
+def test_mx_quantize_jagged_rows_only(fp8, counts, C, fmt):
+    """The row-major output alone with segments: codes in x's rows, scales at the padded rows of
+    each row's segment (the layout the jagged-M GEMM reads)."""
+    M = sum(counts)
+    x = _mx_rows_input(M, C, 9)
+    ends = W.ends_from_counts(counts)
+    q, qt, sf, sft = fp8.mx_quantize_alloc(x.cuda(), TDT[fmt], fp8.LAYOUT_ROW_MAJOR, offsets=_up(ends))
+    torch.cuda.synchronize()
+    assert qt is None and sft is None
+    qr, sr = oracle.mx_quantize_rows(bits(x), fmt)
+    assert np.array_equal(codes(q), qr)
+    P = fp8.fp8_jagged_padded_rows(M, len(counts))
     sfr = mx_unblock(sf, P, C)
     starts, cnts, pstarts, _ = oracle.mx_padded_segments(ends)
     for s0, c, ps in zip(starts, cnts, pstarts):
