@@ -103,6 +103,24 @@ def test_tensorwise_dual_output(fp8, R, C, fi):
     assert np.array_equal(codes(q1), q_ref) and np.array_equal(codes(qt1), q_ref.T)
 
 
+@pytest.mark.parametrize("R,C,layout", [(4096, 4096, "both"), (4112, 4160, "both"), (4112, 4104, "col"),
+                                         (6144, 2112, "col"), (16, 64, "both")])
+def test_tensorwise_stash_shapes(fp8, R, C, layout):
+    """The tensorwise kernel that keeps each SM's last 12 tiles of 128 x 64 on chip: enough tiles
+    that its ring wraps (2048+ tiles over 152 SMs), ragged last tile rows and columns, the
+    column-major output alone."""
+    ofmt, dt, fmax = FMTS[0]
+    x = _input(R, C, 300 + R + C, fmax)
+    lay = fp8.LAYOUT_BOTH if layout == "both" else fp8.LAYOUT_COL_MAJOR
+    q, qt, inv = fp8.quantize_alloc(x.cuda(), fp8.GRAN_TENSOR, dt, layout=lay)
+    torch.cuda.synchronize()
+    q_ref, inv_ref = oracle.quantize_tensor(bits(x), ofmt)
+    assert np.array_equal(codes(qt), q_ref.T)
+    if layout == "both":
+        assert np.array_equal(codes(q), q_ref)
+    assert np.array_equal(f32_bits(inv), inv_ref.view(np.uint32))
+
+
 @pytest.mark.parametrize("R,C", [(16, 8), (512, 64), (1040, 200), (8192, 136), (9216, 72), (20480, 64),
                                  (2048, 2048), (1040, 4096)])
 @pytest.mark.parametrize("fi", [0, 1])
