@@ -99,7 +99,8 @@ struct GemmParams {
   int64_t M, N, K;     // tile space: rows of D, columns of D, contraction length (elements)
   int64_t num_m, num_n;
   int64_t nkb;         // K blocks per tile (dense, jagged M)
-  int64_t group_m;     // dense: tiles walk group_m M-blocks per N-block
+  int64_t group_m;     // dense: tiles walk group_m M-blocks per N-block (group_n == 0), or
+  int64_t group_n;     //        group_n N-blocks per M-block
   const float* sA;
   const float* sB;
   int sa_scalar, sb_scalar;
@@ -183,13 +184,26 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, co
   Tile T;
   const uint32_t t = (uint32_t)t64, num_n = (uint32_t)p.num_n;
   if (is_dense(SCHED)) {
-    const uint32_t gm = (uint32_t)p.group_m;
-    const uint32_t per_group = gm * num_n;
-    const uint32_t g = t / per_group, r = t - g * per_group;
-    const uint32_t first_m = g * gm;
-    const uint32_t left = (uint32_t)p.num_m - first_m;
-    const uint32_t gsz = left < gm ? left : gm;
-    const uint32_t nb = r / gsz, mb = first_m + (r - nb * gsz);
+    uint32_t mb, nb;
+    if (p.group_n == 0) {
+      const uint32_t gm = (uint32_t)p.group_m;
+      const uint32_t per_group = gm * num_n;
+      const uint32_t g = t / per_group, r = t - g * per_group;
+      const uint32_t first_m = g * gm;
+      const uint32_t left = (uint32_t)p.num_m - first_m;
+      const uint32_t gsz = left < gm ? left : gm;
+      nb = r / gsz;
+      mb = first_m + (r - nb * gsz);
+    } else {
+      const uint32_t gn = (uint32_t)p.group_n;
+      const uint32_t per_group = gn * (uint32_t)p.num_m;
+      const uint32_t g = t / per_group, r = t - g * per_group;
+      const uint32_t first_n = g * gn;
+      const uint32_t left = num_n - first_n;
+      const uint32_t gsz = left < gn ? left : gn;
+      mb = r / gsz;
+      nb = first_n + (r - mb * gsz);
+    }
     T.m0 = (int64_t)mb * TILE_M;
     T.pm0 = T.m0;
     T.n0 = (int64_t)nb * TBN;
@@ -1354,16 +1368,25 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
   const bool pair = !g.blockwise && (g.mode == FP8_GROUPED_JAGGED_M ? g.M >= 2048 : pair_tiles * 2 >= c.sm_count);
   const int tile_m = pair ? 256 : 128;
   p.num_m = (g.M + tile_m - 1) / tile_m;
-  // Dense tiles walk the M-blocks of a group, then the next N-block: a group's A panels (tile_m
-  // rows x K) are re-read by every N-block, from L2 while the group's panels fit in ~32 MB, and
-  // every group reads all of B once. Measured on the Llama3 MLP shapes (DRAM bytes read): the
-  // forward (1 MB panels) 152 MB with 16 M-blocks per group, 115 MB with all 32; the grad-input
-  // and bf16 weight-gradient GEMMs (~4 MB panels) 573 / 1179 MB with 16, 483 / 1048 MB with 8.
+  // Dense tiles walk a group of M-blocks before the next N-block (or a group of N-blocks before
+  // the next M-block): the group's panels (tile rows x K) are re-read by every block of the other
+  // dimension, from L2 while the group fits in ~32 MB, and every group reads all of the other
+  // operand once. The orientation with fewer bytes read by that count is taken. Measured on the
+  // Llama3 MLP shapes (DRAM bytes read): the forward (1 MB panels) 152 MB with 16 M-blocks per
+  // group, 115 MB with all 32; the grad-input and bf16 weight-gradient GEMMs (~4 MB panels)
+  // 573 / 1179 MB with 16 M-blocks, 483 / 1048 MB with 8.
   {
-    const int64_t panel = (int64_t)tile_m * g.K * esz;
-    int64_t gm = panel > 0 ? kGroupBytes / panel : p.num_m;
-    if (gm > p.num_m) gm = p.num_m;
-    p.group_m = gm < 1 ? 1 : gm;  // never zero: it divides the tile index
+    auto group = [](int64_t panel, int64_t blocks) {
+      int64_t gsz = panel > 0 ? kGroupBytes / panel : blocks;
+      if (gsz > blocks) gsz = blocks;
+      return gsz < 1 ? (int64_t)1 : gsz;  // never zero: it divides the tile index
+    };
+    const int64_t pa = (int64_t)tile_m * g.K * esz, pb = (int64_t)tbn * g.K * esz;  // panel bytes
+    const int64_t gm = group(pa, p.num_m), gn = group(pb, p.num_n);
+    const int64_t by_m = p.num_m * pa + (p.num_m + gm - 1) / gm * p.num_n * pb;  // A once, B per group
+    const int64_t by_n = p.num_n * pb + (p.num_n + gn - 1) / gn * p.num_m * pa;  // B once, A per group
+    p.group_m = gm;
+    p.group_n = by_n < by_m ? gn : 0;
   }
   // the kernels index tiles with 32-bit arithmetic
   const int64_t max_tiles = g.mode == FP8_GROUPED_JAGGED_K ? g.E * p.num_m * p.num_n
