@@ -16,7 +16,7 @@
 //     16-bit maxima, each with bit 15 set ("written"; bf16 magnitudes leave it free), in a
 //     workspace the launcher zeroed;
 //   pass 2 (cast): a second producer warp streams the same units again, now from L2, through its
-//     own ring; two gatherer warps take each unit's strip maxima from the partials of the strip's
+//     own ring; three gatherer warps take each unit's strip maxima from the partials of the strip's
 //     row tiles, polling (bounded) until every field reads as written, so no fence, counter or
 //     barrier separates the passes; 8 warps each take 32 rows of a tile: a lane per column pair,
 //     scale by table, cast in registers, write the transposed 64 x 32 box to the warp's staging
