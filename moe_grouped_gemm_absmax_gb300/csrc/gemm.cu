@@ -25,6 +25,10 @@
 //               tcgen05.ld 32 columns at a time, sA[m] * sB[n] applied once, one rounding to
 //               bf16/fp32, masked stores. The second accumulator lets the next tile's MMAs
 //               overlap this epilogue.
+// Grouped with rows jagged by expert (FP8, pairs): an expert's last tile, when it has fewer than
+// 256 rows, is computed transposed: its 256 weight rows are the MMA's M and its rows, rounded up
+// to 16, the MMA's N, loaded with a row box of 32, 64 or 128 per CTA. These GEMMs are bound by
+// operand traffic from L2, so a short tail costs the bytes and MMAs of its own rows.
 // Every wait is bounded; on a timeout the kernel raises FP8_DEV_TIMEOUT, drains in-flight TMA
 // and MMA work, frees its tensor memory and returns.
 #include <string.h>
@@ -126,6 +130,10 @@ struct GemmParams {
   int q_mx;
   int q_fmt;
   ScaleTab q_tab;
+  // FP8 jagged M on CTA pairs: an expert's last tile, when it holds fewer than 256 rows, is
+  // computed transposed (weight rows on the MMA's M side, the tile's rows as its N)
+  int tail_t;
+  uint32_t idesc_t;    // the transposed tile's instruction descriptor, N field zero
 };
 
 struct Tile {
@@ -135,6 +143,7 @@ struct Tile {
   int64_t k0;       // first contraction coordinate
   int64_t nkb;      // K blocks
   int e;            // expert (jagged)
+  int tt;           // jagged M, transposed tail tile: its rows (1..255); 0 for an ordinary tile
 };
 
 constexpr int kMaxStages = 5;  // ring stages the barrier arrays below hold
@@ -211,6 +220,7 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, co
     T.k0 = 0;
     T.nkb = p.nkb;
     T.e = 0;
+    T.tt = 0;
   } else if (SCHED == kJagM) {
     const int e = find_expert(tpre, p.E, t64);
     const uint32_t local = t - (uint32_t)tpre[e];
@@ -222,6 +232,7 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, co
     T.k0 = 0;
     T.nkb = p.nkb;
     T.e = e;
+    T.tt = (p.tail_t && T.row_end - T.m0 < TILE_M) ? (int)(T.row_end - T.m0) : 0;
   } else {
     const uint32_t per = (uint32_t)p.num_m * num_n;
     const uint32_t e = t / per;
@@ -234,6 +245,7 @@ FP8_DEVI Tile get_tile(const GemmParams& p, int64_t t64, const int32_t* tpre, co
     T.k0 = aux[e];                             // aux[e] = padded start of segment e
     T.nkb = (aux[e + 1] - aux[e]) / BKB;       // padded length / 128
     T.e = (int)e;
+    T.tt = 0;
   }
   return T;
 }
@@ -258,6 +270,9 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
   constexpr int kEpiThreads = C::EPI_THREADS;
   constexpr int TBN = C::TBN;
   constexpr bool kPadRows = KIND == kMX && SCHED == kJagM;  // A scales in the segment-padded row space
+  // FP8 jagged M on pairs: transposed tail tiles, whose row boxes of 32 and 64 rows come in the
+  // tmSA and tmSB slots (unused by FP8 operands); 128-row boxes are tmA's own
+  constexpr bool kTail = KIND == kFP8 && SCHED == kJagM && CG == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* out_stage = smem + C::RING_BYTES;  // [8 warps][kStageOut], pairs only
@@ -359,7 +374,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (CG == 2) tma_prefetch_desc(&tmO);
-    if (KIND == kMX) {
+    if (KIND == kMX || (kTail && p.tail_t)) {
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
@@ -399,6 +414,14 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
         // columns (each CTA of a pair loads them in full: its accumulator spans all columns)
         const int32_t sfa_rb = (int32_t)((T.pm0 + (int64_t)rank * BM) / 128);
         const int32_t sfb_rb = (int32_t)(T.n0 / 128);
+        // transposed tail tile: each CTA holds N' / 2 of its rows (N' = rows rounded up to 16),
+        // loaded with the smallest row box that covers them; the weight rows take the A side
+        int tail_half = 0, tail_box = 0;
+        if (kTail && T.tt) {
+          tail_half = (T.tt + 15) / 16 * 8;
+          tail_box = tail_half <= 32 ? 32 : (tail_half <= 64 ? 64 : 128);
+        }
+        const uint32_t tx = tail_box ? (uint32_t)(C::A_BYTES + tail_box * BKB) : (uint32_t)C::TX_BYTES;
         for (int64_t kb = 0; kb < T.nkb; ++kb) {
           if (!mbar_wait(&S.empty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
             if (!*abort_flag) fail();
@@ -447,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
           } else {
             // both CTAs' bytes are counted on the issuing CTA's full barrier
             const uint32_t fb = mapa_shared(smem_u32(&S.full[stage]), 0);
-            if (issuer) mbar_arrive_expect_tx(&S.full[stage], 2 * C::TX_BYTES);
+            if (issuer) mbar_arrive_expect_tx(&S.full[stage], 2 * tx);
             if (KIND == kMX) {
               const int32_t kx = (int32_t)(T.k0 + kb * BKB);
               tma_load_2d_pair(sa, &tmA, fb, kx, am);
@@ -461,11 +484,17 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
               tma_load_3d_pair(ssf, &tmSA, fb, 0, kx / 128, sfa_rb);
             } else if (KIND == kFP8 || KIND == kBLK) {
               const int32_t kx = (int32_t)(T.k0 + kb * BKB);
-              tma_load_2d_pair(sa, &tmA, fb, kx, am);
-              if (SCHED == kJagM)
-                tma_load_3d_pair(sb, &tmB, fb, kx, bn, T.e);
-              else
-                tma_load_2d_pair(sb, &tmB, fb, kx, bn);
+              if (kTail && tail_box) {
+                tma_load_3d_pair(sa, &tmB, fb, kx, bn, T.e);  // this CTA's 128 weight rows
+                const CUtensorMap* tm = tail_box == 32 ? &tmSA : (tail_box == 64 ? &tmSB : &tmA);
+                tma_load_2d_pair(sb, tm, fb, kx, (int32_t)(T.m0 + (int64_t)rank * tail_half));
+              } else {
+                tma_load_2d_pair(sa, &tmA, fb, kx, am);
+                if (SCHED == kJagM)
+                  tma_load_3d_pair(sb, &tmB, fb, kx, bn, T.e);
+                else
+                  tma_load_2d_pair(sb, &tmB, fb, kx, bn);
+              }
             } else {
               const int32_t kx = (int32_t)(kb * (BKB / 2));
               if (A_MN) {
@@ -523,6 +552,11 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
       for (int64_t t = unit; t < total && ok; t += n_units) {
         const int64_t nkb = tile_nkb<SCHED>(p, t, aux);
         if (nkb == 0) continue;
+        uint32_t idesc = p.idesc;
+        if (kTail && p.tail_t) {  // transposed tail tile: swapped formats, N = N'
+          const int tt = get_tile<SCHED, C::TILE_M, TBN>(p, t, tpre, aux, pst).tt;
+          if (tt) idesc = p.idesc_t | ((uint32_t)((tt + 15) / 16 * 2) << 17);
+        }
         if (KIND != kBLK) {
           if (!mbar_wait(&S.tempty[buf], aphase ^ 1, abort_flag, p.wait_ns)) {
             if (!*abort_flag) fail();
@@ -576,7 +610,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
             const uint32_t acc = ((KIND != kBLK && kb > 0) || kk > 0) ? 1u : 0u;
             if (CG == 2) {
               if (KIND == kFP8 || KIND == kBLK)
-                umma_f8f6f4_pair(d_tmem, ad, bd, p.idesc, acc);
+                umma_f8f6f4_pair(d_tmem, ad, bd, idesc, acc);
               else
                 umma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
             } else {
@@ -738,6 +772,12 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
     auto fetch = [&](int64_t tt) {
       Tn = get_tile<SCHED, C::TILE_M, TBN>(p, tt, tpre, aux, pst);
       if (KIND != kFP8) return;
+      if (kTail && Tn.tt) {  // this thread's weight-row scale; the staged scales are the rows'
+        const int64_t n = Tn.n0 + row;
+        sa_nx = n < p.N ? __ldg(p.sB + (int64_t)Tn.e * p.N + n) : 0.0f;
+        sb_nx = etid < Tn.tt ? (p.sa_scalar ? __ldg(p.sA) : __ldg(p.sA + Tn.m0 + etid)) : 0.0f;
+        return;
+      }
       const int64_t m = Tn.m0 + row;
       const float* sbp = p.sB;
       if (!is_dense(SCHED)) sbp += (int64_t)Tn.e * p.N;
@@ -763,7 +803,7 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
       const int64_t m = T.m0 + row;
       const bool row_ok = m < T.row_end;
       const int64_t orow = SCHED == kJagK ? (int64_t)T.e * p.M + m : m;
-      if (stage_sb) {  // one column scale per epilogue thread; reused by all 128 rows
+      if (stage_sb || (kTail && T.tt)) {  // one column scale per epilogue thread; reused by all 128 rows
         S.sb[sbi][etid] = sb_mine;
         named_bar_sync(1, kEpiThreads);
       }
@@ -963,6 +1003,49 @@ __global__ void __launch_bounds__(Cfg<KIND, CG, SCHED>::THREADS, 1)
       }
       const float sb_all = (KIND == kFP8 && p.sb_scalar) ? sb_mine : 1.0f;
       const uint32_t taddr = tmem_base + (uint32_t)(buf * TBN + c0) + ((uint32_t)(q * 32) << 16);
+      if (kTail && T.tt) {
+        // transposed tail tile: lane = weight row n (an output column), tensor-memory column j =
+        // the tile's row m0 + j. Rounded as the ordinary tiles round, (acc * sA[m]) * sB[n]. For
+        // each row the warp's lanes hold 32 consecutive output columns: every store instruction
+        // writes 64 (bf16) or 128 (fp32) contiguous bytes; rows past the tile's end are skipped.
+        const int64_t n = T.n0 + row;
+        const bool n_ok = n < p.N;
+        const float2 sn2 = make_float2(sa, sa);
+        uint32_t v[32];
+        for (int ch = 0; ch < C::WCOLS / 32; ++ch) {
+          const int cl = c0 + ch * 32;
+          if (cl >= T.tt) break;  // uniform across the warp
+          tmem_ld32(taddr + ch * 32, v);
+          tmem_ld_wait_regs(v);
+          const int nr = T.tt - cl < 32 ? T.tt - cl : 32;
+          const int64_t o0 = (T.m0 + cl) * p.ldo + n;
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 x = fmul2_rn(fmul2_rn(make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1])),
+                                               *reinterpret_cast<const float2*>(sbs + cl + j)),
+                                      sn2);
+            if (n_ok && j < nr) {
+              if (p.out_f32) {
+                float* o = static_cast<float*>(p.out) + o0 + j * p.ldo;
+                o[0] = x.x;
+                if (j + 1 < nr) o[p.ldo] = x.y;
+              } else {
+                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + o0 + j * p.ldo;
+                o[0] = __float2bfloat16_rn(x.x);
+                if (j + 1 < nr) o[p.ldo] = __float2bfloat16_rn(x.y);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&S.tempty[buf]), 0));
+        if (++buf == 2) {
+          buf = 0;
+          aphase ^= 1;
+        }
+        continue;
+      }
       if constexpr (SCHED == kDenseQuant) {
         // The next quantization from the epilogue ("Triton Kernel Optimization", Level 1): this
         // lane holds row m's tile columns c0 .. c0 + 127. They are scaled and rounded once to bf16
@@ -1482,7 +1565,20 @@ int launch_gemm(const GemmArgs& g, const Ctx& c) {
       const uint32_t boxB[3] = {BKB, b_rows, 1};
       rc = make_tmap(&tb, g.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dB, sB_, boxB, CU_TENSOR_MAP_SWIZZLE_128B);
       if (rc) return rc;
-      return pair ? run<kFP8, kJagM, 0, 0, 2>(ta, tb, to, none, none, p, 0, c) : run<kFP8, kJagM, 0, 0, 1>(ta, tb, to, none, none, p, 0, c);
+      if (!pair) return run<kFP8, kJagM, 0, 0, 1>(ta, tb, to, none, none, p, 0, c);
+      // An expert's last tile with fewer than 256 rows runs transposed: the expert's 256 weight
+      // rows as the MMA's M, the tile's rows rounded up to 16 as its N, and only the row boxes
+      // that cover them loaded (32, 64 or 128 rows per CTA), so a short tail costs the MMAs and
+      // the operand bytes of its rows, not of 256.
+      CUtensorMap t32, t64;
+      const uint32_t box32[2] = {BKB, 32}, box64[2] = {BKB, 64};
+      rc = make_tmap(&t32, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, strideK, box32, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc) return rc;
+      rc = make_tmap(&t64, g.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dA, strideK, box64, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc) return rc;
+      p.tail_t = 1;
+      p.idesc_t = make_idesc(bf, af, 0, 0, 256, 0);
+      return run<kFP8, kJagM, 0, 0, 2>(ta, tb, to, t32, t64, p, 0, c);
     }
     return FP8_ERR_INVALID_ARG;
   }

@@ -54,11 +54,16 @@ def test_jagged_m(fp8, counts, N, K):
     ([1, 15, 16, 17, 0, 255, 256, 257, 1200, 300], 300, 256, torch.float32, oracle.E4M3),
     ([0, 2100, 3, 0, 33], 1040, 512, torch.bfloat16, oracle.E5M2),
     ([513, 511, 1024, 0], 264, 128, torch.bfloat16, oracle.E4M3),
+    ([64, 65, 100, 128, 129, 200, 240, 241, 31, 32, 48, 49, 1000], 520, 256, torch.bfloat16, oracle.E4M3),
+    ([1000, 49, 48, 32, 31, 241, 240, 200, 129, 128, 100, 65, 64], 136, 384, torch.float32, oracle.E5M2),
 ])
 def test_jagged_m_pairs(fp8, counts, N, K, out_dtype, fa):
     """At least 2048 rows: CTA pairs with 256-row tiles that start at each expert's first row:
     experts with 1, 15, 16, 17 tokens, 255-257, empty experts, N not a multiple of 256, e4m3 and
-    e5m2 activations, fp32 and bf16 outputs."""
+    e5m2 activations, fp32 and bf16 outputs. An expert's last tile with fewer than 256 rows runs
+    transposed with row boxes of 32, 64 or 128 per CTA (tails up to 64, 128, 255 rows): the last
+    two cases put tails on both sides of each boundary (64/65, 128/129), at 31/32, 48/49 and
+    240/241."""
     out, (ca, fa_, cw, ia, iw, ends) = _jagged_m_case(fp8, counts, N, K, out_dtype, seed=9, fa=fa)
     ref, absacc = oracle.grouped_gemm_m(ca, fa_, cw, oracle.E4M3, ia, iw, ends)
     check_gemm(out, ref, absacc, out_dtype == torch.bfloat16)
