@@ -7,10 +7,11 @@
 //
 // The scale needs the amax of the whole tensor, so every element is read twice. One cooperative
 // launch, one CTA per SM, tiles of 128 rows x 64 columns dealt round-robin:
-//   pass 1: a producer warp streams the CTA's tiles through a ring of 12 shared-memory slots by
-//           TMA (192 KB in flight per SM); 8 warps fold |x| and release each slot. The last 12
-//           tiles of every CTA are never overwritten: they stay on chip (29 MB over 152 SMs), and
-//           the tiles read just before them are the newest lines in L2;
+//   pass 1: a producer warp streams the CTA's tiles through a ring of 8 shared-memory slots by
+//           TMA (128 KB in flight per SM); 8 warps fold |x| and release each slot. The last 8
+//           tiles of every CTA are never overwritten: they stay on chip (19 MB over 152 SMs), and
+//           the tiles read just before them are the newest lines in L2 (8 slots timed faster
+//           than 6, 10 or 12);
 //   barrier: the CTA's maximum goes to the workspace's amax word (relaxed atomic), the CTA counts
 //           itself on the barrier word (release) and waits, bounded, until all have (acquire);
 //   pass 2: the tiles in reverse order: the slots' own tiles first, then each freed slot is
@@ -27,7 +28,7 @@ namespace {
 
 constexpr int kTsRows = 128, kTsCols = 64;
 constexpr int kTsTileBytes = kTsRows * kTsCols * 2;  // 16 KB of bf16, 128-byte swizzled rows
-constexpr int kTsSlots = 12;
+constexpr int kTsSlots = 8;
 constexpr int kTsWarps = 8;                          // two groups of 4: group g casts tiles j = g mod 2
 constexpr int kTsThreads = 32 * (kTsWarps + 1);      // + the producer warp
 constexpr int kTsBox = 64 * 32;                      // one warp's box of codes (either layout)
@@ -155,8 +156,8 @@ __global__ void __launch_bounds__(kTsThreads, 1)
   const float s32 = S.s32;
 
   // ============================ pass 2: the cast, newest tile first ============================
-  // Sequence j handles the CTA's tile k = cnt - 1 - j in slot k % 12; the first 12 are in their
-  // slots already, each later one is loaded into the slot the tile 12 steps earlier freed.
+  // Sequence j handles the CTA's tile k = cnt - 1 - j in slot k % 8; the first 8 are in their
+  // slots already, each later one is loaded into the slot the tile 8 steps earlier freed.
   if (warp == kTsWarps) {
     if (lane == 0) {
       int64_t j = 0;

@@ -137,6 +137,12 @@ def test_llama4_grouped_forward_backward(fp8, bench):
     ends = st.ends.cpu().numpy()
     rng = np.random.default_rng(14)
     mi = np.sort(rng.choice(st.M, 6, replace=False))
+    # the first and last rows of two experts' last tiles with fewer than 256 rows (the forward and
+    # dX compute those tiles transposed)
+    tail = np.asarray(st.counts) % 256
+    for e in np.flatnonzero(tail > 0)[:2]:
+        mi = np.concatenate([mi, [ends[e] - tail[e], ends[e] - 1]])
+    mi = np.unique(mi)
     ni = np.sort(rng.choice(st.N, 16, replace=False))
     ki = np.sort(rng.choice(st.K, 16, replace=False))
     nsel, ksel = torch.as_tensor(ni, device="cuda"), torch.as_tensor(ki, device="cuda")

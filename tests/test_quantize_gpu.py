@@ -106,9 +106,9 @@ def test_tensorwise_dual_output(fp8, R, C, fi):
 @pytest.mark.parametrize("R,C,layout", [(4096, 4096, "both"), (4112, 4160, "both"), (4112, 4104, "col"),
                                          (6144, 2112, "col"), (16, 64, "both")])
 def test_tensorwise_stash_shapes(fp8, R, C, layout):
-    """The tensorwise kernel that keeps each SM's last 12 tiles of 128 x 64 on chip: enough tiles
-    that its ring wraps (2048+ tiles over 152 SMs), ragged last tile rows and columns, the
-    column-major output alone."""
+    """The tensorwise kernel that keeps each SM's last 8 tiles of 128 x 64 on chip: enough tiles
+    that its ring wraps (2048+ tiles over 152 SMs, 13+ per SM), ragged last tile rows and columns,
+    the column-major output alone, a single tile."""
     ofmt, dt, fmax = FMTS[0]
     x = _input(R, C, 300 + R + C, fmax)
     lay = fp8.LAYOUT_BOTH if layout == "both" else fp8.LAYOUT_COL_MAJOR
