@@ -175,9 +175,13 @@ def _segpad(q_ref, ends, P):
 
 @pytest.mark.parametrize("counts", [[100, 0, 37, 500, 1], [0, 0, 64], [300, 0], [9000, 5, 0, 11000],
                                     list(W.llama4_counts(0) // 4), list(W.random_counts(3000, 40, 5, n_empty=9)),
-                                    [0] * 7 + [1000] + [0] * 9])
+                                    [0] * 7 + [1000] + [0] * 9,
+                                    [31, 32, 33, 63, 64, 65, 95, 96, 97, 127, 128, 129, 224, 225, 255, 256, 257, 511]])
 @pytest.mark.parametrize("fi", [0, 1])
 def test_jagged_colwise(fp8, counts, fi):
+    """Column scales per segment, written into the segment-padded column-major layout; a segment's
+    last, partial 256-row tile loads only the 32-row boxes holding its rows (the last case puts
+    segment tails on both sides of each 32-row boundary)."""
     ofmt, dt, fmax = FMTS[fi]
     counts = [int(c) for c in counts]
     R = sum(counts)
