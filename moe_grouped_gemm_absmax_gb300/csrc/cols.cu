@@ -43,6 +43,7 @@ constexpr int kCqP1Warps = 4;                 // pass-1 (amax) warps
 constexpr int kCqP2Warps = 8;                 // pass-2 (cast) warps, 32 rows each
 constexpr int kCqP1Threads = 32 * kCqP1Warps;
 constexpr int kCqGathers = 3;                 // pass-2 warps gathering the maxima (unit k: warp k % gathers)
+constexpr int kCqBatch = 4;                   // partials a gatherer lane loads at once (4 and 8 timed alike)
 constexpr int kCqP1Warp0 = 2 + kCqGathers;    // warps: 0, 1 producers; gatherers; pass 1; pass 2
 constexpr int kCqP2Warp0 = kCqP1Warp0 + kCqP1Warps;
 constexpr int kCqThreads = 32 * (kCqP2Warp0 + kCqP2Warps);
@@ -387,22 +388,43 @@ __global__ void __launch_bounds__(kCqThreads, 1) colpipe_kernel(const __grid_con
         const uint32_t* base = p.part + (int64_t)u.pbase * 32 + 4 * q;
         uint4 acc = make_uint4(0, 0, 0, 0);
         bool ok = true;
-        for (int32_t r = r0; r < u.rtn && ok; r += 4) {
-          uint4 v = ld_relaxed_v4(base + (int64_t)r * 32);
-          bool done = !p.test_stall && ((v.x & v.y & v.z & v.w & kCqWritten) == kCqWritten);
-          if (!done) {
-            const uint64_t t0 = globaltimer();
-            while (!done) {
-              __nanosleep(64);
-              v = ld_relaxed_v4(base + (int64_t)r * 32);
-              done = !p.test_stall && ((v.x & v.y & v.z & v.w & kCqWritten) == kCqWritten);
-              if (!done && (*abort || globaltimer() - t0 > p.wait_ns)) {
-                ok = false;
-                break;
+        // kCqBatch partials per lane in flight at once (a tall strip has one per row tile; rows
+        // past the strip count as written zeros). A batch that is not all written yet is taken
+        // again entry by entry, each polled (bounded) until written.
+        for (int32_t r = r0; r < u.rtn && ok; r += 4 * kCqBatch) {
+          uint4 v[kCqBatch];
+#pragma unroll
+          for (int j = 0; j < kCqBatch; ++j)
+            v[j] = r + 4 * j < u.rtn ? ld_relaxed_v4(base + (int64_t)(r + 4 * j) * 32)
+                                     : make_uint4(kCqWritten, kCqWritten, kCqWritten, kCqWritten);
+          uint32_t all = p.test_stall ? 0u : kCqWritten;
+#pragma unroll
+          for (int j = 0; j < kCqBatch; ++j) all &= v[j].x & v[j].y & v[j].z & v[j].w;
+          if (all == kCqWritten) {
+#pragma unroll
+            for (int j = 0; j < kCqBatch; ++j)
+              acc = make_uint4(__vmaxu2(acc.x, v[j].x), __vmaxu2(acc.y, v[j].y), __vmaxu2(acc.z, v[j].z),
+                               __vmaxu2(acc.w, v[j].w));
+            continue;
+          }
+#pragma unroll 1
+          for (int32_t rr = r; rr < u.rtn && rr < r + 4 * kCqBatch && ok; rr += 4) {
+            uint4 w = ld_relaxed_v4(base + (int64_t)rr * 32);
+            bool done = !p.test_stall && ((w.x & w.y & w.z & w.w & kCqWritten) == kCqWritten);
+            if (!done) {
+              const uint64_t t0 = globaltimer();
+              while (!done) {
+                __nanosleep(64);
+                w = ld_relaxed_v4(base + (int64_t)rr * 32);
+                done = !p.test_stall && ((w.x & w.y & w.z & w.w & kCqWritten) == kCqWritten);
+                if (!done && (*abort || globaltimer() - t0 > p.wait_ns)) {
+                  ok = false;
+                  break;
+                }
               }
             }
+            acc = make_uint4(__vmaxu2(acc.x, w.x), __vmaxu2(acc.y, w.y), __vmaxu2(acc.z, w.z), __vmaxu2(acc.w, w.w));
           }
-          acc = make_uint4(__vmaxu2(acc.x, v.x), __vmaxu2(acc.y, v.y), __vmaxu2(acc.z, v.z), __vmaxu2(acc.w, v.w));
         }
         if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) cq_fail(abort, p.status);
