@@ -732,6 +732,13 @@ class MoeFwdMxStep(MoeFwdStep):
         mark(2)
         f.fp8_grouped_mm(self.Aq, self.Wq, self.ends, self.As, self.Ws, self.out, f.GROUPED_JAGGED_M)
 
+    def e2e_compute(self, d_in, d_out):
+        f = self.fp8
+        A, Wt, ends = d_in
+        f.fp8_quantize(A, f.GRAN_MX, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Aq, None, self.As, ends, self.ws_a)
+        f.fp8_quantize(Wt, f.GRAN_MX, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.Wq, None, self.Ws)
+        f.fp8_grouped_mm(self.Aq, self.Wq, ends, self.As, self.Ws, d_out[0], f.GROUPED_JAGGED_M)
+
 
 class MoeFwdBwdMxStep(MoeFwdBwdStep):
     """The Llama4-shaped grouped fwd + bwd with MXFP8: A, W[e] and dY are each read once and
