@@ -996,22 +996,40 @@ def make_step(fp8, name):
 
 
 # ------------------------------------------------------------------------------------------
-# clocks: nvidia-smi sampled every 50 ms from before the warm-up on (its start-up stays out of the
+# clocks: nvidia-smi sampled every 20 ms from before the warm-up on (its start-up stays out of the
 # timed region); the samples whose timestamps fall in the timed region are kept, or, when the
-# region is shorter than the sampling interval, the samples nearest to it on either side
+# region is shorter than the sampling interval, the samples nearest to it on either side. The GPU
+# is named to nvidia-smi by its UUID (its index there need not be torch's when
+# CUDA_VISIBLE_DEVICES remaps devices), or by the index when the UUID is not accepted.
 
 CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+CLOCK_INTERVAL_MS = 20
+
+
+def smi_gpu_id(gpu_index):
+    """The id nvidia-smi knows this CUDA device by: "GPU-<uuid>" when nvidia-smi accepts it."""
+    try:
+        uid = "GPU-" + str(torch.cuda.get_device_properties(gpu_index).uuid)
+        r = subprocess.run(["nvidia-smi", f"--id={uid}", "--query-gpu=index", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=20)
+        if r.returncode == 0 and r.stdout.strip():
+            return uid
+    except Exception:  # no UUID in this torch, no nvidia-smi, or it refused the id
+        pass
+    return str(gpu_index)
+
+
 class ClockSampler:
     def __init__(self, gpu_index):
         self.proc = None
-        self.gpu = gpu_index
+        self.gpu = smi_gpu_id(gpu_index)
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", str(CLOCK_INTERVAL_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -1042,7 +1060,7 @@ class ClockSampler:
             before = [r for r in rows if r[0] < t0]
             after = [r for r in rows if r[0] > t1]
             inside = before[-1:] + after[:1]
-            window = "nearest samples (timed region shorter than the 50 ms interval)"
+            window = f"nearest samples (timed region shorter than the {CLOCK_INTERVAL_MS} ms interval)"
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in inside:
@@ -1052,7 +1070,7 @@ class ClockSampler:
         sm = [r[1] for r in inside]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(r[2] for r in inside) if inside else None,
-                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+                "reasons": sorted(reasons), "samples": len(inside), "window": window, "gpu": self.gpu}
 
 
 # ------------------------------------------------------------------------------------------

@@ -81,9 +81,10 @@ def test_clock_sampler_keeps_the_timed_window():
              _smi_line(t0 + datetime.timedelta(seconds=2), 1200, ("Active", "Not Active", "Not Active", "Not Active"))]
     s = object.__new__(bench.ClockSampler)
     s.proc = _FakeSmi("\n".join(lines) + "\n")
+    s.gpu = "GPU-00000000-0000-0000-0000-000000000000"
     w0, w1 = (t0 + datetime.timedelta(seconds=0.9)).timestamp(), (t0 + datetime.timedelta(seconds=1.1)).timestamp()
     c = s.stop(w0, w1)
-    assert c["samples"] == 2 and c["window"] == "timed region"
+    assert c["samples"] == 2 and c["window"] == "timed region" and c["gpu"] == s.gpu
     assert c["sm_mhz"] == (2070 + 2055) / 2 and c["sm_max_mhz"] == 2070
     assert c["reasons"] == ["sw_power_cap"]  # the hw_slowdown sample lies outside the window
 
@@ -97,7 +98,23 @@ def test_clock_sampler_nearest_samples_for_a_short_window():
     lines = [_smi_line(t0 + datetime.timedelta(seconds=x), sm) for x, sm in ((0.0, 1900), (0.05, 2000), (0.10, 2070))]
     s = object.__new__(bench.ClockSampler)
     s.proc = _FakeSmi("\n".join(lines) + "\n")
+    s.gpu = "0"
     w0, w1 = (t0 + datetime.timedelta(seconds=0.06)).timestamp(), (t0 + datetime.timedelta(seconds=0.08)).timestamp()
     c = s.stop(w0, w1)
     assert c["samples"] == 2 and c["window"].startswith("nearest")
     assert c["sm_mhz"] == (2000 + 2070) / 2
+
+
+def test_smi_gpu_id_falls_back_to_the_index(monkeypatch):
+    """Without a usable UUID (no GPU here) or with nvidia-smi refusing it, the sampler names the
+    GPU by its index."""
+    import subprocess
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class _Refused:
+        returncode, stdout = 6, ""
+
+    monkeypatch.setattr(subprocess, "run", lambda *a, **k: _Refused())
+    assert bench.smi_gpu_id(3) == "3"
