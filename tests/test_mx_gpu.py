@@ -72,8 +72,11 @@ def _mx_rows_input(R, C, seed):
 # ---------------------------------------------------------------------------- quantize
 
 @pytest.mark.parametrize("shape,fmt", [((256, 256), E4), ((300, 384), E4), ((77, 128), E5), ((3, 128, 384), E4),
-                                       ((1, 1024), E5), ((70, 7168), E4), ((40, 12288), E5), ((2, 9, 4096), E4)])
+                                       ((1, 1024), E5), ((70, 7168), E4), ((40, 12288), E5), ((2, 9, 4096), E4),
+                                       ((40, 16512), E4), ((2, 9, 16512), E5)])
 def test_mx_quantize_rows(fp8, shape, fmt):
+    """Row blocks alone; rows longer than 16384 elements take the tiled pipeline (the last two
+    cases, one of them with 9-row batch entries inside a tile's 128 rows)."""
     x = _mx_rows_input(int(np.prod(shape[:-1])), shape[-1], 3).reshape(shape)
     q, _, sf, _ = fp8.mx_quantize_alloc(x.cuda(), TDT[fmt], fp8.LAYOUT_ROW_MAJOR)
     torch.cuda.synchronize()
@@ -88,8 +91,11 @@ def test_mx_quantize_rows(fp8, shape, fmt):
 
 
 @pytest.mark.parametrize("shape,fmt,layout", [((256, 256), E5, "col"), ((384, 128), E4, "both"),
-                                              ((2, 128, 256), E4, "both"), ((128, 640), E5, "col")])
+                                              ((2, 128, 256), E4, "both"), ((128, 640), E5, "col"),
+                                              ((4096, 3072), E5, "both"), ((3, 1024, 2048), E4, "col")])
 def test_mx_quantize_cols_and_both(fp8, shape, fmt, layout):
+    """Column blocks (and row blocks from the same read) through the tiled pipeline; the last two
+    cases give every CTA more tiles than its 4-stage ring holds."""
     x = _mx_rows_input(int(np.prod(shape[:-1])), shape[-1], 5).reshape(shape)
     lay = fp8.LAYOUT_COL_MAJOR if layout == "col" else fp8.LAYOUT_BOTH
     q, qt, sf, sft = fp8.mx_quantize_alloc(x.cuda(), TDT[fmt], lay)
@@ -110,7 +116,8 @@ def test_mx_quantize_cols_and_both(fp8, shape, fmt, layout):
 
 
 @pytest.mark.parametrize("counts,C,fmt", [([40, 0, 200, 1, 130], 256, E5), ([0, 0, 128], 128, E4),
-                                          ([300, 17, 0, 0, 256, 90], 384, E4)])
+                                          ([300, 17, 0, 0, 256, 90], 384, E4),
+                                          (list(W.llama4_counts(1) // 2), 2048, E5)])
 def test_mx_quantize_jagged(fp8, counts, C, fmt):
     """Segments padded to 128 rows: column-major codes [C, P] and scales per (column, 32-token
     block of a segment); row-major scales at the padded rows. Both from one read."""
