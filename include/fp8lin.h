@@ -341,9 +341,10 @@ int fp8_linear_bwd(const fp8_tensor* dy, const fp8_linear_saved* saved, const fp
 
 /* Test hook for failure detection: while enabled, every GEMM launch first waits on a barrier
  * that nothing signals, the grid barrier of the tensorwise quantize waits for one arrival more
- * than there are CTAs, and the column-wise quantize sees no tile maxima as written; the wait runs out after the wait limit (fp8_set_wait_limit_ns), the
- * kernel reports FP8_DEV_TIMEOUT, drains and returns. Off by default. Returns the previous
- * setting. */
+ * than there are CTAs, the column-wise quantize sees no tile maxima as written, and the MX
+ * quantize with a column-major output of a dense tensor loads no tile into its ring; the wait
+ * runs out after the wait limit (fp8_set_wait_limit_ns), the kernel reports FP8_DEV_TIMEOUT,
+ * drains and returns. Off by default. Returns the previous setting. */
 int fp8_set_test_stall(int enable);
 
 /* Test hook for the cast step ([Q] section 2: round to nearest even, saturating; [F] formats):

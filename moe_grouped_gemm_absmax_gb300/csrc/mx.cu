@@ -225,7 +225,7 @@ FP8_DEVI MpTile mp_tile(const MxArgs& a, int64_t t, int64_t ncols, int64_t grid_
 template <int FMT, bool ROWS, bool COLS>
 __global__ void __launch_bounds__(kMpThreads, 1)
     mx_pipe_kernel(const __grid_constant__ CUtensorMap tm_x, const MxArgs a, int64_t ncols, int64_t grid_y,
-                   int64_t n_tiles, int32_t* status, uint64_t wait_ns) {
+                   int64_t n_tiles, int32_t* status, uint64_t wait_ns, int test_stall) {
   extern __shared__ uint8_t mp_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mp_raw) + 1023) & ~uintptr_t(1023));
   MpShared& S = *reinterpret_cast<MpShared*>(ring + kMpStages * kMpStageBytes);
@@ -250,7 +250,8 @@ __global__ void __launch_bounds__(kMpThreads, 1)
 
   if (warp == kMpWarps) {
     // ================= producer: one lane streams the CTA's tiles by TMA =================
-    if (lane == 0) {
+    // (the failure-detection test hook: no tile is loaded, so the consumers' first wait runs out)
+    if (lane == 0 && !test_stall) {
       int s = 0;
       uint32_t ph = 0;
       int64_t issued = 0;
@@ -536,7 +537,8 @@ int run_mx_pipe(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) 
   if (rc != FP8_OK) return rc;
   const int64_t ncols = a.C / kTile, n_tiles = ncols * grid_y * batches;
   const int64_t grid = n_tiles < c.sm_count ? n_tiles : c.sm_count;
-  kern<<<(unsigned)grid, kMpThreads, kMpSmem, c.stream>>>(tm, a, ncols, grid_y, n_tiles, c.status, c.wait_ns);
+  kern<<<(unsigned)grid, kMpThreads, kMpSmem, c.stream>>>(tm, a, ncols, grid_y, n_tiles, c.status, c.wait_ns,
+                                                           c.test_stall);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 

@@ -1,8 +1,9 @@
 """Failure detection without a GPU fault: every on-device wait of the GEMM kernels, of the grid
-barrier of the tensorwise quantize and of the chunk completion counts of the column-wise quantize
-is bounded. The test hook fp8_set_test_stall makes the GEMM's MMA issuer wait on a barrier that
-nothing signals, and the quantize kernels wait for one CTA more than they launched; with a short
-wait limit the wait runs out, and the kernel must report
+barrier of the tensorwise quantize, of the column-wise quantize's partial maxima and of the MX
+quantize's load ring is bounded. The test hook fp8_set_test_stall makes the GEMM's MMA issuer wait
+on a barrier that nothing signals, the tensorwise quantize wait for one CTA more than it
+launched, the column-wise gatherers read no partial as written and the MX producer load nothing;
+with a short wait limit the wait runs out, and the kernel must report
 FP8_DEV_TIMEOUT in the status word, stop its other warps, drain its in-flight TMA loads and MMAs,
 free its tensor memory and return, leaving the context usable (a normal call afterwards is
 correct)."""
@@ -110,3 +111,28 @@ def test_colwise_barrier_expiry_reports_timeout_and_context_survives(fp8, counts
         got = qt.view(torch.uint8).cpu().numpy()
         assert np.array_equal(got[:, :used], segpad_cols(qo, ends, qt.shape[1])[:, :used])
     assert np.array_equal(inv.cpu().numpy().view(np.uint32), io.view(np.uint32))
+
+
+def test_mx_ring_expiry_reports_timeout_and_context_survives(fp8):
+    """The pipelined MX quantize (column-major output of a dense tensor): with the hook on its
+    producer loads nothing, the consumers' bounded wait runs out, the status says so, and the
+    next call on the same context is bit-exact against the oracle."""
+    x = W.normal_bf16((512, 384), 1.0, 23)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    old = fp8.fp8_set_wait_limit_ns(2_000_000)  # 2 ms
+    fp8.fp8_set_test_stall(True)
+    try:
+        fp8.mx_quantize_alloc(x.cuda(), fp8.DT_E4M3, fp8.LAYOUT_BOTH, status=st)
+        torch.cuda.synchronize()
+    finally:
+        fp8.fp8_set_test_stall(False)
+        fp8.fp8_set_wait_limit_ns(old)
+    assert int(st.item()) & fp8.DEV_TIMEOUT
+    st.zero_()
+    q, qt, sf, sft = fp8.mx_quantize_alloc(x.cuda(), fp8.DT_E4M3, fp8.LAYOUT_BOTH, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    qo, so = oracle.mx_quantize_cols(bits(x), oracle.E4M3)
+    assert np.array_equal(qt.cpu().view(torch.uint8).numpy(), qo)
+    qr, sr = oracle.mx_quantize_rows(bits(x), oracle.E4M3)
+    assert np.array_equal(q.cpu().view(torch.uint8).numpy(), qr)
