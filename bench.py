@@ -401,11 +401,11 @@ class MoeFwdStep(Step):
         return {"grouped_gemm_fp8 jagged-M": grouped_attainable_ms(self.counts, self.N, self.K, 2, pk["fp8"], pk["hbm"])}
 
     def cpu_sample(self, rows):
-        """The oracle on 64 routed rows (their row quantize, their experts' weights quantized per
-        column, their grouped-GEMM outputs), counted in grouped-GEMM FLOPs."""
+        """The oracle on `rows` routed rows (their row quantize, their experts' weights quantized
+        per column, their grouped-GEMM outputs), counted in grouped-GEMM FLOPs."""
         import oracle
         ends = self.ends.cpu().numpy()
-        ridx = np.sort(np.random.default_rng(0).choice(self.M, 64, replace=False))
+        ridx = np.sort(np.random.default_rng(0).choice(self.M, rows, replace=False))
         experts = np.unique(np.searchsorted(ends, ridx, side="right"))
         ab = W.bf16_bits(self.A[torch.as_tensor(ridx, device=self.A.device)].cpu())
         wb = {int(e): W.bf16_bits(self.Wt[int(e)].cpu()) for e in experts}
@@ -416,7 +416,7 @@ class MoeFwdStep(Step):
                 e = int(np.searchsorted(ends, r, side="right"))
                 wq, wi = oracle.quantize_rows(wb[e], oracle.E4M3)
                 oracle.gemm_fp8(aq[i:i + 1], oracle.E4M3, wq, oracle.E4M3, ai[i:i + 1], wi)
-        return run, 2.0 * 64 * self.N * self.K, "64 routed rows: their quantize, their experts' weights, their outputs"
+        return run, 2.0 * rows * self.N * self.K, f"{rows} routed rows: their quantize, their experts' weights, their outputs"
 
     def run(self, mark=lambda s: None):
         f = self.fp8
@@ -1309,8 +1309,26 @@ def main():
         t0 = time.perf_counter()
         run()
         dt = time.perf_counter() - t0
-        cpu = {"value": work / dt / (1e12 if step.unit == "TFLOP/s" else 1e9), "unit": step.unit,
-               "cores": oracle.num_threads(), "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+        scale = 1e12 if step.unit == "TFLOP/s" else 1e9
+        cores = oracle.num_threads()
+        cpu = {"value": work / dt / scale, "unit": step.unit,
+               "cores": cores, "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+        # the same oracle on one core, on an eighth of the sample (skipped when that would take
+        # more than ~40 s by the multi-core rate)
+        run1, work1, sample1 = step.cpu_sample(max(1, args.cpu_rows // 8))
+        est = dt * (work1 / work) * cores
+        if est <= 40.0:
+            oracle.set_num_threads(1)
+            try:
+                t0 = time.perf_counter()
+                run1()
+                dt1 = time.perf_counter() - t0
+            finally:
+                oracle.set_num_threads(cores)
+            cpu.update({"value_1core": work1 / dt1 / scale, "sample_1core": sample1, "seconds_1core": round(dt1, 2)})
+        else:
+            cpu["value_1core"] = None
+            cpu["note_1core"] = f"skipped: about {est:.0f} s on one core"
 
     launches = getattr(step, "launches_per_step", lambda: nk)() * args.steps
     if rank == 0:

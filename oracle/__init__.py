@@ -62,6 +62,8 @@ def lib():
         L.orc_quantize_blocks.argtypes = [P, I64, I64, I64, I64, I, P, P]
         L.orc_gemm_blockwise.argtypes = [P, I, P, I, P, P, I64, I64, I64, P, I64, P, P]
         L.orc_num_threads.restype = I
+        L.orc_set_num_threads.argtypes = [I]
+        L.orc_set_num_threads.restype = None
         _lib = L
     return _lib
 
@@ -76,6 +78,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return lib().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (timing only)."""
+    lib().orc_set_num_threads(int(n))
 
 
 def fp8_max(fmt: int) -> float:

@@ -525,3 +525,12 @@ int orc_num_threads(void) {
   return 1;
 #endif
 }
+
+/* The thread count of the parallel loops that follow (timing only: results do not depend on it). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

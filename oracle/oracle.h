@@ -127,6 +127,7 @@ int orc_gemm_mx(const uint8_t* A, int fmtA, const uint8_t* B, int fmtB, const ui
 
 /* Number of OpenMP threads the oracle runs on. */
 int orc_num_threads(void);
+void orc_set_num_threads(int n);
 
 #ifdef __cplusplus
 }

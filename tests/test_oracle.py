@@ -449,3 +449,27 @@ def test_grouped_k_reductions():
         prev = end
     out_s, _ = oracle.grouped_gemm_k(G, E5M2, X, E4M3, sG, sX, ends, nsel=[9, 2])
     assert np.array_equal(out_s, out[:, [9, 2]])
+
+
+def test_oracle_results_do_not_depend_on_its_thread_count():
+    """The 1-core baseline times the same arithmetic: quantize and GEMM give the same bits on one
+    thread as on all of them (each output element is computed by one thread, in a fixed order)."""
+    import workloads as W
+    x = W.bf16_bits(W.normal_bf16((96, 160), 1.0, 31))
+    w = W.bf16_bits(W.normal_bf16((64, 160), 0.02, 32))
+    n = oracle.num_threads()
+
+    def chain():
+        xq, xi = oracle.quantize_rows(x, oracle.E4M3)
+        wq, wi = oracle.quantize_cols(w.T.copy(), oracle.E4M3)
+        out, _ = oracle.gemm_fp8(xq, oracle.E4M3, wq.T.copy(), oracle.E4M3, xi, wi)
+        return xq, xi, wq, wi, out
+
+    try:
+        oracle.set_num_threads(1)
+        one = chain()
+    finally:
+        oracle.set_num_threads(n)
+    many = chain()
+    for a, b in zip(one, many):
+        assert np.array_equal(np.asarray(a).view(np.uint8), np.asarray(b).view(np.uint8))
