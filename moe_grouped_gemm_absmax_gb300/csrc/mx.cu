@@ -178,10 +178,10 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const MxArgs a) {
 }
 
 // The same tiles through a persistent pipeline (dense and batched tensors; column-major output,
-// with or without the row-major one): one CTA per SM walks its tiles (t = CTA, CTA + grid, ...;
-// tile columns fastest, so neighbouring CTAs read neighbouring 256-byte pieces of the same rows);
-// a producer warp streams each 128 x 128 tile into a 4-stage ring as two 128-byte-swizzled TMA
-// boxes of 64 columns, and 8 warps per tile
+// with or without the row-major one): one CTA per SM walks its tiles (t = CTA, CTA + grid, ...; tile columns fastest,
+// so neighbouring CTAs read neighbouring 256-byte pieces of the same rows); a producer warp
+// streams each 128 x 128 tile into a 4-stage ring as two 128-byte-swizzled TMA boxes of 64
+// columns, and 8 warps per tile
 //   - row blocks: a thread per (row, block) pair twice over, four 16-byte shared loads hold the
 //     block's 32 elements; four consecutive lanes hold a row's four blocks (shuffles gather the
 //     scale word); the codes go straight to global memory, 32 bytes a thread;
