@@ -8,16 +8,10 @@
 // v1.0: X = 2^(floor(log2(amax)) - emax_elem), emax_elem = 8 (e4m3) or 15 (e5m2), the exponent
 // clamped below at -127; each element is x / X, rounded to nearest even and saturated.
 //
-// Two kernels serve the column-major output (blocks down a column, written transposed), alone or
-// with the row-major one (blocks along a row) from a single read: a persistent pipelined kernel
-// (below) for dense and batched tensors, and this one for segments. A CTA owns a tile of 128 rows
-// x 128 columns of bf16:
-//   - the row-major codes come straight from registers: each 16-byte load holds 8 elements of a
-//     row, four lanes hold a block of 32, two shuffles give the block amax, and the 16 lanes of a
-//     row store its 128 codes as one 128-byte segment;
-//   - for the column-major codes the tile is staged in shared memory, each thread reduces and
-//     casts 64 rows of one column, and the transposed codes leave through a second staging
-//     buffer as 128-byte rows.
+// The row-major output alone runs on row teams (mx_rows_kernel). The column-major output (blocks
+// down a column, written transposed), alone or with the row-major one (blocks along a row) from a
+// single read, runs on a persistent pipelined kernel over tiles of 128 rows x 128 columns
+// (mx_pipe_kernel, below).
 // The E8M0 scales are written in the tensor-core scale-factor layout the MX GEMM reads: for an
 // operand with rows r (its non-contraction index) and K blocks j, 512-byte blocks
 // [r / 128][j / 4], and inside one the code of (r, j) at byte (r % 32) * 16 + (r / 32 % 4) * 4 +
@@ -33,10 +27,6 @@ namespace fp8lin {
 namespace {
 
 constexpr int kTile = 128;             // rows and columns of a tile
-constexpr int kMxThreads = 256;
-constexpr int kInPitch = kTile + 8;    // bf16 per staged input row (272 bytes: 16-byte aligned rows)
-constexpr int kOutPitch = kTile + 16;  // bytes per staged output row (conflict-free 16-byte writes)
-constexpr int kMxSmem = kTile * kInPitch * 2 + kTile * kOutPitch;
 constexpr int kMaxSegments = 2048;
 
 struct MxArgs {
@@ -53,132 +43,8 @@ struct MxArgs {
   int E;
 };
 
-template <int FMT, bool ROWS, bool COLS, bool JAG>
-__global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const MxArgs a) {
-  extern __shared__ __align__(16) uint8_t mx_smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t c0 = (int64_t)blockIdx.x * kTile;
-  const int64_t b = blockIdx.z;
-  int64_t row0, prow0;  // first source row of the tile; its padded row (scale position)
-  int valid;            // source rows in the tile
-  if (JAG) {
-    prow0 = (int64_t)blockIdx.y * kTile;
-    const int32_t used = __ldg(a.pstart + a.E);
-    if (prow0 >= used) return;  // past the last segment (or offsets rejected: used == 0)
-    int lo = 0, hi = a.E - 1;   // the last segment whose padded start is <= prow0
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(a.pstart + mid) <= prow0) lo = mid;
-      else hi = mid - 1;
-    }
-    const int64_t start = lo ? __ldg(a.ends + lo - 1) : 0;
-    const int64_t cnt = __ldg(a.ends + lo) - start;
-    const int64_t off = prow0 - __ldg(a.pstart + lo);
-    row0 = start + off;
-    valid = (int)(cnt - off < kTile ? cnt - off : kTile);
-  } else {
-    row0 = (int64_t)blockIdx.y * kTile;
-    prow0 = row0;
-    valid = (int)(a.R - row0 < kTile ? a.R - row0 : kTile);
-  }
-  const uint16_t* xb = a.x + b * a.R * a.C;
-
-  // ---- load: 8 vectors of 8 bf16 per thread; rows past the segment / tensor are zeros ----
-  uint4 v[8];
-  const int cc = (lane & 15) * 8;
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int rr = it * 16 + warp * 2 + (lane >> 4);
-    v[it] = rr < valid ? ld_nc_v4(xb + (row0 + rr) * a.C + c0 + cc) : make_uint4(0, 0, 0, 0);
-  }
-
-  if (ROWS) {
-    const int64_t ncb = a.C / kTile;
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int rr = it * 16 + warp * 2 + (lane >> 4);
-      uint32_t m = absmax_fold(absmax_vec8(0u, v[it]));
-      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      const uint32_t code = mx_code<FMT>(m);
-      const float inv = mx_inv(code);
-      uint2 o;
-      o.x = mx_cast2<FMT>(v[it].x, inv) | (mx_cast2<FMT>(v[it].y, inv) << 16);
-      o.y = mx_cast2<FMT>(v[it].z, inv) | (mx_cast2<FMT>(v[it].w, inv) << 16);
-      // the four block codes of this row, from lanes 0, 4, 8, 12 of its half-warp
-      const int hb = lane & 16;
-      const uint32_t word = __shfl_sync(0xffffffffu, code, hb) | (__shfl_sync(0xffffffffu, code, hb + 4) << 8) |
-                            (__shfl_sync(0xffffffffu, code, hb + 8) << 16) |
-                            (__shfl_sync(0xffffffffu, code, hb + 12) << 24);
-      if (rr < valid) {
-        *reinterpret_cast<uint2*>(a.q + (b * a.R + row0 + rr) * a.C + c0 + cc) = o;
-        if ((lane & 15) == 0) {
-          const int64_t pr = prow0 + rr;
-          uint8_t* blk = a.sf + ((b * a.rb_q + (pr >> 7)) * ncb + (c0 >> 7)) * 512;
-          *reinterpret_cast<uint32_t*>(blk + (pr & 31) * 16 + ((pr >> 5) & 3) * 4) = word;
-        }
-      }
-    }
-  }
-
-  if (COLS) {
-    uint16_t* sx = reinterpret_cast<uint16_t*>(mx_smem);
-    uint8_t* so = mx_smem + kTile * kInPitch * 2;
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int rr = it * 16 + warp * 2 + (lane >> 4);
-      *reinterpret_cast<uint4*>(sx + rr * kInPitch + cc) = v[it];
-    }
-    __syncthreads();
-    // thread: the column pair (2 cp, 2 cp + 1) of the tile, rows 32 qb .. 32 qb + 31 (one block
-    // per column). A 32-bit shared load holds the pair's bf16 values of one row, so the block
-    // maxima of both columns come from packed 16-bit maxima, one per row.
-    const int cp = tid & 63, qb = tid >> 6;
-    const int r0 = 32 * qb;
-    uint32_t w[32];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) w[r] = *reinterpret_cast<const uint32_t*>(sx + (r0 + r) * kInPitch + 2 * cp);
-    uint32_t m2 = 0;
-#pragma unroll
-    for (int r = 0; r < 32; ++r) m2 = absmax2(m2, w[r]);
-    const uint32_t code_lo = mx_code<FMT>(m2 & 0xFFFFu), code_hi = mx_code<FMT>(m2 >> 16);
-    const float inv_lo = mx_inv(code_lo), inv_hi = mx_inv(code_hi);
-    uint32_t olo[8], ohi[8];
-#pragma unroll
-    for (int r = 0; r < 32; r += 4) {
-      // column 2 cp: the low halves of rows r .. r + 3; column 2 cp + 1: the high halves
-      const uint32_t l01 = (w[r] & 0xFFFFu) | (w[r + 1] << 16), l23 = (w[r + 2] & 0xFFFFu) | (w[r + 3] << 16);
-      const uint32_t h01 = (w[r] >> 16) | (w[r + 1] & 0xFFFF0000u), h23 = (w[r + 2] >> 16) | (w[r + 3] & 0xFFFF0000u);
-      olo[r / 4] = mx_cast2<FMT>(l01, inv_lo) | (mx_cast2<FMT>(l23, inv_lo) << 16);
-      ohi[r / 4] = mx_cast2<FMT>(h01, inv_hi) | (mx_cast2<FMT>(h23, inv_hi) << 16);
-    }
-    uint8_t* dlo = so + (2 * cp) * kOutPitch + r0;
-    uint8_t* dhi = dlo + kOutPitch;
-    *reinterpret_cast<uint4*>(dlo) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-    *reinterpret_cast<uint4*>(dlo + 16) = make_uint4(olo[4], olo[5], olo[6], olo[7]);
-    *reinterpret_cast<uint4*>(dhi) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-    *reinterpret_cast<uint4*>(dhi + 16) = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
-    {
-      const int64_t nrb = a.ld_t / kTile;
-      uint8_t* blk = a.sft + ((b * (a.C / kTile) + (c0 >> 7)) * nrb + (prow0 >> 7)) * 512;
-      const int c = 2 * cp;  // columns c and c + 1: same 32-column group, adjacent 16-byte rows
-      blk[(c & 31) * 16 + (c >> 5) * 4 + qb] = (uint8_t)code_lo;
-      blk[((c + 1) & 31) * 16 + (c >> 5) * 4 + qb] = (uint8_t)code_hi;
-    }
-    __syncthreads();
-    // the transposed tile: row c of qt holds 128 codes (rows prow0 .. prow0 + 127), 8 lanes each
-#pragma unroll
-    for (int i = 0; i < kTile / 32; ++i) {
-      const int cr = i * 32 + warp * 4 + (lane >> 3);
-      const int ch = (lane & 7) * 16;
-      const uint4 w = *reinterpret_cast<const uint4*>(so + cr * kOutPitch + ch);
-      *reinterpret_cast<uint4*>(a.qt + (b * a.C + c0 + cr) * a.ld_t + prow0 + ch) = w;
-    }
-  }
-}
-
-// The same tiles through a persistent pipeline (dense and batched tensors; column-major output,
-// with or without the row-major one): one CTA per SM walks its tiles (t = CTA, CTA + grid, ...; tile columns fastest,
+// Tiles of 128 x 128 bf16 through a persistent pipeline (column-major output, with or without the
+// row-major one; dense, batched or segments): one CTA per SM walks its tiles (t = CTA, CTA + grid, ...; tile columns fastest,
 // so neighbouring CTAs read neighbouring 256-byte pieces of the same rows); a producer warp
 // streams each 128 x 128 tile into a 4-stage ring as two 128-byte-swizzled TMA boxes of 64
 // columns, and 8 warps per tile
@@ -188,8 +54,8 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const MxArgs a) {
 //   - column blocks: a thread per (column pair, 32-row quarter), 32 four-byte shared loads (a
 //     warp reads one 128-byte box row at a time: conflict-free); the codes go to the
 //     column-major output, 32 bytes per column;
-// then release the stage. Loads of the next tiles are in flight while a tile is cast, which the
-// one-tile-per-CTA kernel above leaves to its 4 resident CTAs per SM.
+// then release the stage. Loads of the next tiles are in flight while a tile is cast (a kernel
+// with one tile per CTA and no overlap inside a CTA timed 14-26% slower on dense tensors).
 constexpr int kMpStages = 4;
 constexpr int kMpWarps = 8;                           // consumer warps
 constexpr int kMpThreads = 32 * (kMpWarps + 1);       // + the producer warp
@@ -222,14 +88,57 @@ FP8_DEVI MpTile mp_tile(const MxArgs& a, int64_t t, int64_t ncols, int64_t grid_
   return T;
 }
 
-template <int FMT, bool ROWS, bool COLS>
+// Segments: a CTA's tiles are described once, before its loops (a thread per tile), so that no
+// segment lookup sits on the producer's or the consumers' path: tile t of the padded rows in use
+// (t mod ncols: its 128-column tile) finds its segment by binary search on the padded starts.
+constexpr int kMpMaxTiles = 512;  // descriptors per CTA (the launcher sizes the grid to fit)
+struct MpDesc {
+  int32_t row0, prow0, c0, valid;
+};
+FP8_DEVI MpDesc mp_desc(const MxArgs& a, int64_t t, int64_t ncols) {
+  MpDesc D;
+  const int64_t ty = t / ncols;
+  D.c0 = (int32_t)((t - ty * ncols) * kTile);
+  D.prow0 = (int32_t)(ty * kTile);
+  int lo = 0, hi = a.E - 1;  // the last segment whose padded start is <= prow0
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.pstart + mid) <= D.prow0) lo = mid;
+    else hi = mid - 1;
+  }
+  const int32_t start = lo ? __ldg(a.ends + lo - 1) : 0, cnt = __ldg(a.ends + lo) - start;
+  const int32_t off = D.prow0 - __ldg(a.pstart + lo);
+  D.row0 = start + off;
+  D.valid = cnt - off < kTile ? cnt - off : kTile;
+  return D;
+}
+
+template <int FMT, bool ROWS, bool COLS, bool JAG>
 __global__ void __launch_bounds__(kMpThreads, 1)
     mx_pipe_kernel(const __grid_constant__ CUtensorMap tm_x, const MxArgs a, int64_t ncols, int64_t grid_y,
                    int64_t n_tiles, int32_t* status, uint64_t wait_ns, int test_stall) {
   extern __shared__ uint8_t mp_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mp_raw) + 1023) & ~uintptr_t(1023));
   MpShared& S = *reinterpret_cast<MpShared*>(ring + kMpStages * kMpStageBytes);
+  MpDesc* desc = reinterpret_cast<MpDesc*>(&S + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // segments: only the row tiles of the padded rows in use (none when the offsets were rejected)
+  const int64_t n_run = JAG ? ncols * (__ldg(a.pstart + a.E) / kTile) : n_tiles;
+  const int64_t cnt = (int64_t)blockIdx.x < n_run ? (n_run - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  if (JAG)
+    for (int64_t k = tid; k < cnt; k += blockDim.x) desc[k] = mp_desc(a, blockIdx.x + k * (int64_t)gridDim.x, ncols);
+  // tile k of this CTA
+  auto tile_k = [&](int64_t k) {
+    if (!JAG) return mp_tile(a, blockIdx.x + k * (int64_t)gridDim.x, ncols, grid_y);
+    const MpDesc D = desc[k];
+    MpTile T;
+    T.row0 = D.row0;
+    T.prow0 = D.prow0;
+    T.b = 0;
+    T.c0 = D.c0;
+    T.valid = D.valid;
+    return T;
+  };
   if (tid == 0) {
     for (int s = 0; s < kMpStages; ++s) {
       mbar_init(&S.full[s], 1);
@@ -255,8 +164,8 @@ __global__ void __launch_bounds__(kMpThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       int64_t issued = 0;
-      for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-        const MpTile T = mp_tile(a, t, ncols, grid_y);
+      for (int64_t k = 0; k < cnt; ++k) {
+        const MpTile T = tile_k(k);
         if (!mbar_wait(&S.empty[s], ph ^ 1, abort, wait_ns)) {
           fail();
           break;
@@ -281,8 +190,8 @@ __global__ void __launch_bounds__(kMpThreads, 1)
   const int64_t ncb = a.C / kTile;
   int s = 0;
   uint32_t ph = 0;
-  for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-    const MpTile T = mp_tile(a, t, ncols, grid_y);
+  for (int64_t k = 0; k < cnt; ++k) {
+    const MpTile T = tile_k(k);
     if (!__all_sync(0xffffffffu, mbar_wait(&S.full[s], ph, abort, wait_ns))) {
       if (lane == 0) fail();
       break;
@@ -512,22 +421,12 @@ int dispatch_mx_rows(const MxArgs& a, int64_t rows, const Ctx& c) {
 }
 
 template <int FMT, bool ROWS, bool COLS, bool JAG>
-int run_mx(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) {
-  auto kern = mx_quant_kernel<FMT, ROWS, COLS, JAG>;
-  const int smem = COLS ? kMxSmem : 0;
-  if (COLS && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return FP8_ERR_CUDA;
-  const dim3 grid((unsigned)(a.C / kTile), (unsigned)grid_y, (unsigned)batches);
-  kern<<<grid, kMxThreads, smem, c.stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
-}
-
-template <int FMT, bool ROWS, bool COLS>
 int run_mx_pipe(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) {
-  auto kern = mx_pipe_kernel<FMT, ROWS, COLS>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMpSmem) != cudaSuccess)
+  auto kern = mx_pipe_kernel<FMT, ROWS, COLS, JAG>;
+  const int smem = kMpSmem + (JAG ? kMpMaxTiles * (int)sizeof(MpDesc) : 0);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return FP8_ERR_CUDA;
-  const int64_t rows_total = a.R * batches;
+  const int64_t rows_total = JAG ? a.R : a.R * batches;
   if (rows_total > INT32_MAX || a.C > INT32_MAX) return FP8_ERR_UNSUPPORTED;  // TMA coordinates
   CUtensorMap tm;
   const uint64_t dims[2] = {(uint64_t)a.C, (uint64_t)rows_total};
@@ -536,26 +435,23 @@ int run_mx_pipe(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) 
   const int rc = make_tmap(&tm, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != FP8_OK) return rc;
   const int64_t ncols = a.C / kTile, n_tiles = ncols * grid_y * batches;
-  const int64_t grid = n_tiles < c.sm_count ? n_tiles : c.sm_count;
-  kern<<<(unsigned)grid, kMpThreads, kMpSmem, c.stream>>>(tm, a, ncols, grid_y, n_tiles, c.status, c.wait_ns,
-                                                           c.test_stall);
+  int64_t grid = n_tiles < c.sm_count ? n_tiles : c.sm_count;
+  if (JAG && ceil_div64(n_tiles, grid) > kMpMaxTiles) grid = ceil_div64(n_tiles, kMpMaxTiles);  // descriptors fit
+  if (grid > INT32_MAX) return FP8_ERR_UNSUPPORTED;
+  kern<<<(unsigned)grid, kMpThreads, smem, c.stream>>>(tm, a, ncols, grid_y, n_tiles, c.status, c.wait_ns,
+                                                       c.test_stall);
   return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
-// Dense and batched tensors take the pipelined kernel. With segments the one-tile-per-CTA kernel
-// stays: on the Llama4-shaped segments (16 experts, 8192 tokens) it timed as fast for 5120
-// columns and faster for 8192 (73 against 90 us), where the pipelined one won on every dense
-// shape (8192 x 4096: 36 -> 32 us, 14336 x 4096: 59 -> 51, 8192 x 14336: 109 -> 86, 16 x
-// 8192 x 5120: 598 -> 444).
+// The column-major output (with or without the row-major one) on the pipelined kernel; the
+// row-major output alone on row teams while a row fits their registers.
 template <int FMT, bool JAG>
 int dispatch_layout(const MxArgs& a, int64_t grid_y, int64_t batches, const Ctx& c) {
-  if (a.q && a.qt) return JAG ? run_mx<FMT, true, true, JAG>(a, grid_y, batches, c)
-                              : run_mx_pipe<FMT, true, true>(a, grid_y, batches, c);
+  if (a.q && a.qt) return run_mx_pipe<FMT, true, true, JAG>(a, grid_y, batches, c);
   // the row-major output alone by row teams, for rows of up to 4 * 32 * 16 vectors of 8
   if (a.q && a.C / 8 <= 128 * kMxRowVPL) return dispatch_mx_rows<FMT, JAG>(a, a.R * batches, c);
-  if (a.q) return JAG ? run_mx<FMT, true, false, JAG>(a, grid_y, batches, c)
-                      : run_mx_pipe<FMT, true, false>(a, grid_y, batches, c);
-  return JAG ? run_mx<FMT, false, true, JAG>(a, grid_y, batches, c) : run_mx_pipe<FMT, false, true>(a, grid_y, batches, c);
+  if (a.q) return run_mx_pipe<FMT, true, false, JAG>(a, grid_y, batches, c);
+  return run_mx_pipe<FMT, false, true, JAG>(a, grid_y, batches, c);
 }
 
 }  // namespace
