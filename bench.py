@@ -268,18 +268,25 @@ class TensorwiseLinearStep(Step):
         return 9  # three tensorwise quantizes (amax + cast kernels each) and three GEMMs
 
     def cpu_sample(self, rows):
-        """The whole step in the oracle (it is small)."""
-        import oracle
-        xb, wb, db = (W.bf16_bits(t.cpu()) for t in (self.x, self.w, self.dy))
+        return tensorwise_linear_cpu_sample(self.x.cpu(), self.w.cpu(), self.dy.cpu())
 
-        def run():
-            xq, xi = oracle.quantize_tensor(xb, oracle.E4M3)
-            wq, wi = oracle.quantize_tensor(wb, oracle.E4M3)
-            oracle.gemm_fp8(xq, oracle.E4M3, wq, oracle.E4M3, xi, wi)
-            dq, di = oracle.quantize_tensor(db, oracle.E5M2)
-            oracle.gemm_fp8(dq, oracle.E5M2, wq, oracle.E4M3, di, wi, b_trans=True)
-            oracle.gemm_fp8(dq, oracle.E5M2, xq, oracle.E4M3, di, xi, a_trans=True, b_trans=True)
-        return run, self.total_units(), "the whole step"
+
+def tensorwise_linear_cpu_sample(x, w, dy):
+    """The whole tensorwise Linear step in the oracle (it is small): one scale per tensor, fwd, dX
+    and dW FP8 GEMMs."""
+    import oracle
+    M, K = x.shape
+    N = w.shape[0]
+    xb, wb, db = W.bf16_bits(x), W.bf16_bits(w), W.bf16_bits(dy)
+
+    def run():
+        xq, xi = oracle.quantize_tensor(xb, oracle.E4M3)
+        wq, wi = oracle.quantize_tensor(wb, oracle.E4M3)
+        oracle.gemm_fp8(xq, oracle.E4M3, wq, oracle.E4M3, xi, wi)
+        dq, di = oracle.quantize_tensor(db, oracle.E5M2)
+        oracle.gemm_fp8(dq, oracle.E5M2, wq, oracle.E4M3, di, wi, b_trans=True)
+        oracle.gemm_fp8(dq, oracle.E5M2, xq, oracle.E4M3, di, xi, a_trans=True, b_trans=True)
+    return run, 3 * 2.0 * M * N * K, "the whole step"
 
 
 class ColwiseStep(Step):
@@ -305,15 +312,7 @@ class ColwiseStep(Step):
     def cpu_sample(self, rows):
         """The oracle's column quantize on the first 1024 columns of G (all 8192 rows) and its row
         quantize on the first 1024 rows of X."""
-        import oracle
-        gb = W.bf16_bits(self.g[:, :1024].cpu())
-        xb = W.bf16_bits(self.xx[:1024].cpu())
-
-        def run():
-            oracle.quantize_cols(gb, oracle.E5M2)
-            oracle.quantize_rows(xb, oracle.E4M3)
-        work = 3.0 * gb.size + 4 * 1024 + 3.0 * xb.size + 4 * 1024
-        return run, work, "column quantize of G[:, :1024] and row quantize of X[:1024]"
+        return colwise_cpu_sample(self.g[:, :1024].cpu(), self.xx[:1024].cpu())
 
     def run(self, mark=lambda s: None):
         f = self.fp8
@@ -321,6 +320,19 @@ class ColwiseStep(Step):
         f.fp8_quantize(self.g, f.GRAN_COL, f.DT_E5M2, f.LAYOUT_COL_MAJOR, None, self.gt, self.gi, None, self.gsc)
         mark(1)
         f.fp8_quantize(self.xx, f.GRAN_ROW, f.DT_E4M3, f.LAYOUT_ROW_MAJOR, self.xq, None, self.xi)
+
+
+def colwise_cpu_sample(g, x):
+    """The oracle's column-wise e5m2 quantize of G's columns (over all their rows) and its row-wise
+    e4m3 quantize of X's rows, counted in algorithmic bytes."""
+    import oracle
+    gb, xb = W.bf16_bits(g), W.bf16_bits(x)
+
+    def run():
+        oracle.quantize_cols(gb, oracle.E5M2)
+        oracle.quantize_rows(xb, oracle.E4M3)
+    work = 3.0 * gb.size + 4 * gb.shape[1] + 3.0 * xb.size + 4 * xb.shape[0]
+    return run, work, f"column quantize of G[:, :{gb.shape[1]}] and row quantize of X[:{xb.shape[0]}]"
 
 
 class TensorwiseQuantStep(Step):
@@ -354,12 +366,7 @@ class TensorwiseQuantStep(Step):
 
     def cpu_sample(self, rows):
         """The oracle's tensorwise quantize of x[:rows] (all columns)."""
-        import oracle
-        xb = W.bf16_bits(self.x[:rows].cpu())
-
-        def run():
-            oracle.quantize_tensor(xb, oracle.E4M3)
-        return run, 4.0 * xb.size + 4, f"tensorwise quantize of x[:{rows}] (dual-output bytes)"
+        return tensorwise_quant_cpu_sample(self.x[:rows].cpu())
 
     def run(self, mark=lambda s: None):
         f = self.fp8
@@ -367,6 +374,16 @@ class TensorwiseQuantStep(Step):
             q, qt, inv, ws = self.bufs[i]
             mark(i)
             f.fp8_quantize(t, f.GRAN_TENSOR, dt, f.LAYOUT_BOTH, q, qt, inv, None, ws)
+
+
+def tensorwise_quant_cpu_sample(x):
+    """The oracle's tensorwise e4m3 quantize of x, counted in the dual output's bytes."""
+    import oracle
+    xb = W.bf16_bits(x)
+
+    def run():
+        oracle.quantize_tensor(xb, oracle.E4M3)
+    return run, 4.0 * xb.size + 4, f"tensorwise quantize of x[:{xb.shape[0]}] (dual-output bytes)"
 
 
 class MoeFwdStep(Step):
@@ -493,29 +510,87 @@ def pipelined_e2e(step, n):
     return start, end
 
 
-def moe_fwd_cpu_sample(rows, seed=0):
-    """The oracle (as it stands) on `rows` routed rows of the dsv3-moe-fwd layer: the rows' rowwise
-    quantize, their experts' weights quantized per expert column, and the rows' grouped-GEMM
-    outputs. The sampled rows and their experts' weights are drawn on the host from the workload's
-    distributions (A N(0,1), W N(0,0.02)), seeded; counted in grouped-GEMM FLOPs."""
+def moe_fwd_cpu_sample(rows, seed=0, name="dsv3-moe-fwd", mx=False):
+    """The oracle (as it stands) on `rows` routed rows of a DeepSeek-V3-shaped MoE forward layer:
+    the rows' quantize (rowwise, or MX blocks of 32 along K), their experts' weights quantized the
+    same way per expert row, and the rows' grouped-GEMM outputs. The sampled rows and their
+    experts' weights are drawn on the host from the workload's distributions (A N(0,1),
+    W N(0,0.02)), seeded; counted in grouped-GEMM FLOPs."""
     import oracle
-    d = W.WORKLOADS["dsv3-moe-fwd"].dims
-    M, K, N = d["M"], d["K"], d["N"]
-    ends = W.ends_from_counts(W.dsv3_counts(seed))
+    d = W.WORKLOADS[name].dims
+    E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+    counts = W.dsv3_32e_counts(seed) if name == "dsv3-moe-fwd-32e" else W.dsv3_counts(seed)
+    ends = W.ends_from_counts(counts)
     ridx = np.sort(np.random.default_rng(seed).choice(M, rows, replace=False))
     rexp = np.searchsorted(ends, ridx, side="right")
     ab = W.bf16_bits(W.normal_bf16((rows, K), 1.0, seed + 11))
     wb = {int(e): W.bf16_bits(W.normal_bf16((N, K), 0.02, seed + 1000 + int(e))) for e in np.unique(rexp)}
+    quant, gemm = (oracle.mx_quantize_rows, oracle.gemm_mx) if mx else (oracle.quantize_rows, oracle.gemm_fp8)
 
     def run():
-        aq, ai = oracle.quantize_rows(ab, oracle.E4M3)
-        wq = {e: oracle.quantize_rows(b, oracle.E4M3) for e, b in wb.items()}
+        aq, ai = quant(ab, oracle.E4M3)
+        wq = {e: quant(b, oracle.E4M3) for e, b in wb.items()}
         for i, e in enumerate(rexp):
             cw, iw = wq[int(e)]
-            oracle.gemm_fp8(aq[i:i + 1], oracle.E4M3, cw, oracle.E4M3, ai[i:i + 1], iw)
-    return run, 2.0 * rows * N * K, (f"{rows} of {M} routed rows (their experts: {len(wb)} of 256): the rows' "
-                                     f"quantize, their experts' weights quantized per expert column, their "
+            gemm(aq[i:i + 1], oracle.E4M3, cw, oracle.E4M3, ai[i:i + 1], iw)
+    return run, 2.0 * rows * N * K, (f"{rows} of {M} routed rows (their experts: {len(wb)} of {E}): the rows' "
+                                     f"{'MX ' if mx else ''}quantize, their experts' weights quantized "
+                                     f"{'in blocks of 32 along K' if mx else 'per expert column'}, their "
                                      f"grouped-GEMM outputs")
+
+
+def moe_fwdbwd_cpu_sample(rows, seed=0, mx=False):
+    """The oracle (as it stands) on a sample of the Llama4-shaped MoE fwd + bwd layer: `rows` routed
+    rows (their quantize, their experts' weights quantized for the forward and, over N, for the
+    grad-input GEMM, the rows' forward and grad-input outputs), and a 64 x 64 block of the weight
+    gradient of the sampled expert with the fewest rows (its segment's dY and A columns quantized
+    per segment column, then the contraction over the segment). Inputs drawn on the host from the
+    workload's distributions, seeded; counted in GEMM FLOPs."""
+    import oracle
+    name = "llama4-moe-fwdbwd-mx" if mx else "llama4-moe-fwdbwd"
+    d = W.WORKLOADS[name].dims
+    E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+    counts = W.llama4_counts(seed)
+    ends = W.ends_from_counts(counts)
+    ridx = np.sort(np.random.default_rng(seed).choice(M, rows, replace=False))
+    rexp = np.searchsorted(ends, ridx, side="right")
+    ab = W.bf16_bits(W.normal_bf16((rows, K), 1.0, seed + 11))
+    db = W.bf16_bits(W.normal_bf16((rows, N), 1e-3, seed + 12))
+    wb = {int(e): W.bf16_bits(W.normal_bf16((N, K), 0.02, seed + 1000 + int(e))) for e in np.unique(rexp)}
+    e0 = min(wb, key=lambda e: int(counts[e]))
+    c0, nb = int(counts[e0]), 64
+    gb = W.bf16_bits(W.normal_bf16((c0, nb), 1e-3, seed + 13))
+    xb = W.bf16_bits(W.normal_bf16((c0, nb), 1.0, seed + 14))
+    seg = np.array([c0], np.int32)
+    E4, E5 = oracle.E4M3, oracle.E5M2
+
+    def run():
+        if mx:
+            aq, as_ = oracle.mx_quantize_rows(ab, E4)
+            dq, ds = oracle.mx_quantize_rows(db, E5)
+            wq = {e: (oracle.mx_quantize_rows(b, E4), oracle.mx_quantize_cols(b, E4)) for e, b in wb.items()}
+            for i, e in enumerate(rexp):
+                (cw, sw), (ct, st) = wq[int(e)]
+                oracle.gemm_mx(aq[i:i + 1], E4, cw, E4, as_[i:i + 1], sw)
+                oracle.gemm_mx(dq[i:i + 1], E5, ct, E4, ds[i:i + 1], st)
+            gq, gs = oracle.mx_quantize_jagged_cols(gb, seg, E5)
+            xq, xs = oracle.mx_quantize_jagged_cols(xb, seg, E4)
+            oracle.gemm_mx(gq, E5, xq, E4, gs, xs)
+        else:
+            aq, ai = oracle.quantize_rows(ab, E4)
+            dq, di = oracle.quantize_rows(db, E5)
+            wq = {e: (oracle.quantize_rows(b, E4), oracle.quantize_cols(b, E4)) for e, b in wb.items()}
+            for i, e in enumerate(rexp):
+                (cw, iw), (cc, ic) = wq[int(e)]
+                oracle.gemm_fp8(aq[i:i + 1], E4, cw, E4, ai[i:i + 1], iw)
+                oracle.gemm_fp8(dq[i:i + 1], E5, cc, E4, di[i:i + 1], ic, b_trans=True)
+            gq, gi = oracle.quantize_jagged_cols(gb, seg, E5)
+            xq, xi = oracle.quantize_jagged_cols(xb, seg, E4)
+            oracle.grouped_gemm_k(gq, E5, xq, E4, gi, xi, seg)
+    work = 2 * 2.0 * rows * N * K + 2.0 * c0 * nb * nb
+    return run, work, (f"{rows} of {M} routed rows (their experts: {len(wb)} of {E}): their {'MX ' if mx else ''}"
+                       f"quantize, their experts' weights in both layouts, their fwd and dX outputs; the "
+                       f"{nb} x {nb} dW block of expert {e0} ({c0} rows)")
 
 
 class MoeFwdBwdStep(Step):
@@ -953,18 +1028,25 @@ class DenseBlockwiseLinearStep(DenseLinearStep):
                                                        f.WGRAD_BF16), 256), dtype=torch.uint8, device=dev)
 
     def cpu_sample(self, rows):
-        import oracle
-        x, w, dy = self.x[:rows].cpu(), self.w.cpu(), self.dy[:rows].cpu()
-        xb, wb, db = W.bf16_bits(x), W.bf16_bits(w), W.bf16_bits(dy)
+        return blockwise_cpu_sample(self.x[:rows].cpu(), self.w.cpu(), self.dy[:rows].cpu(), self.M)
 
-        def run():
-            xq, xi = oracle.quantize_blocks(xb, oracle.E4M3, 1, 128)
-            wq, wi = oracle.quantize_blocks(wb, oracle.E4M3, 128, 128)
-            oracle.gemm_blockwise(xq, oracle.E4M3, wq, oracle.E4M3, xi, wi)
-            dq, di = oracle.quantize_blocks(db, oracle.E5M2, 1, 128)
-            oracle.gemm_blockwise(dq, oracle.E5M2, np.ascontiguousarray(wq.T), oracle.E4M3, di, np.ascontiguousarray(wi.T))
-            oracle.gemm_bf16(db, xb, a_trans=True, b_trans=True)
-        return run, 3 * 2.0 * rows * self.N * self.K, f"llama3-8b-mlp-up-blockwise step on the first {rows} of {self.M} tokens"
+
+def blockwise_cpu_sample(x, w, dy, full_rows):
+    """The oracle's blockwise Linear step on the first rows of x / dY and all of W: 1 x 128 tiles
+    for x and dY, 128 x 128 tiles for W, blockwise fwd and dX GEMMs, bf16 dW."""
+    import oracle
+    rows, K = x.shape
+    N = w.shape[0]
+    xb, wb, db = W.bf16_bits(x), W.bf16_bits(w), W.bf16_bits(dy)
+
+    def run():
+        xq, xi = oracle.quantize_blocks(xb, oracle.E4M3, 1, 128)
+        wq, wi = oracle.quantize_blocks(wb, oracle.E4M3, 128, 128)
+        oracle.gemm_blockwise(xq, oracle.E4M3, wq, oracle.E4M3, xi, wi)
+        dq, di = oracle.quantize_blocks(db, oracle.E5M2, 1, 128)
+        oracle.gemm_blockwise(dq, oracle.E5M2, np.ascontiguousarray(wq.T), oracle.E4M3, di, np.ascontiguousarray(wi.T))
+        oracle.gemm_bf16(db, xb, a_trans=True, b_trans=True)
+    return run, 3 * 2.0 * rows * N * K, f"llama3-8b-mlp-up-blockwise step on the first {rows} of {full_rows} tokens"
 
 
 def make_step(fp8, name):
@@ -1136,35 +1218,110 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def _bf16_bits_of(out64):
+    """fp64 GEMM outputs as the bf16 bit patterns the GEMM stores (round to nearest even)."""
+    return W.bf16_bits(torch.from_numpy(np.ascontiguousarray(out64)).to(torch.bfloat16))
+
+
+def dx_colquant_cpu_sample(rows, seed=0):
+    """The oracle on the first `rows` rows of the Llama3-8B grad-input GEMM dX = dY W (dY rowwise
+    e5m2 and W per column e4m3, quantized before the sample as the step quantizes them outside its
+    timed region), dX rounded to bf16, then dX quantized column-wise (e5m2) over those rows."""
+    import oracle
+    d = W.WORKLOADS["llama3-8b-dx-colquant-fused"].dims
+    M, K, N = d["M"], d["K"], d["N"]
+    _, w, dy = W.linear_inputs(rows, K, N, seed=seed, outliers=True)
+    dq, di = oracle.quantize_rows(W.bf16_bits(dy), oracle.E5M2)
+    wc, wi = oracle.quantize_cols(W.bf16_bits(w), oracle.E4M3)
+
+    def run():
+        out, _ = oracle.gemm_fp8(dq, oracle.E5M2, wc, oracle.E4M3, di, wi, b_trans=True)
+        oracle.quantize_cols(_bf16_bits_of(out), oracle.E5M2)
+    return run, 2.0 * rows * N * K, f"dX for the first {rows} of {M} rows, then its column-wise quantize over them"
+
+
+def fwd_quant_cpu_sample(rows, seed=0):
+    """The oracle on the first `rows` rows of the Llama3-8B forward GEMM y = x W^T (rowwise e4m3
+    operands, quantized before the sample as the step quantizes them outside its timed region),
+    y rounded to bf16, then its 1 x 128 e4m3 quantize."""
+    import oracle
+    d = W.WORKLOADS["llama3-8b-fwd-quant-fused"].dims
+    M, K, N = d["M"], d["K"], d["N"]
+    x, w, _ = W.linear_inputs(rows, K, N, seed=seed, outliers=True)
+    xq, xi = oracle.quantize_rows(W.bf16_bits(x), oracle.E4M3)
+    wq, wi = oracle.quantize_rows(W.bf16_bits(w), oracle.E4M3)
+
+    def run():
+        out, _ = oracle.gemm_fp8(xq, oracle.E4M3, wq, oracle.E4M3, xi, wi)
+        oracle.quantize_blocks(_bf16_bits_of(out), oracle.E4M3, 1, 128)
+    return run, 2.0 * rows * N * K, f"y for the first {rows} of {M} rows, then its 1 x 128 quantize"
+
+
+# Rows (tokens or routed rows) of each workload's host-drawn oracle sample; every sample takes a
+# few seconds or less on 8-16 host cores.
+SAMPLE_ROWS = {"llama3-8b-mlp-up": 16, "llama3-8b-mlp-up-blockwise": 16, "llama3-8b-mlp-up-mx": 32,
+               "llama3-8b-tensorwise-quant": 2048, "colwise-8192x14336": 1024, "dsv3-moe-fwd": 16,
+               "dsv3-moe-fwd-32e": 16, "dsv3-moe-fwd-mx": 16, "llama4-moe-fwdbwd": 4, "llama4-moe-fwdbwd-mx": 4,
+               "llama3-8b-dx-colquant-fused": 16, "llama3-8b-fwd-quant-fused": 16}
+
+
+def host_cpu_sample(name, rows=None):
+    """(run, work, sample) of the oracle on a sample of workload `name` drawn on the host (seeded,
+    from the workload's distributions; no device memory): the reference arm's step, and the CPU
+    baseline of the steps that keep no host-side inputs. `rows` defaults to SAMPLE_ROWS[name];
+    the tensorwise Linear is always run whole."""
+    r = rows if rows is not None else SAMPLE_ROWS.get(name)
+    d = W.WORKLOADS[name].dims
+    if name == "linear-tensorwise-256x512":
+        return tensorwise_linear_cpu_sample(*W.linear_inputs(d["M"], d["K"], d["N"], seed=0))
+    if name in ("llama3-8b-mlp-up", "llama3-8b-mlp-up-mx", "llama3-8b-mlp-up-blockwise"):
+        x, w, dy = W.linear_inputs(r, d["K"], d["N"], seed=0, outliers=True)
+        fn = {"llama3-8b-mlp-up": dense_cpu_sample, "llama3-8b-mlp-up-mx": dense_mx_cpu_sample,
+              "llama3-8b-mlp-up-blockwise": blockwise_cpu_sample}[name]
+        return fn(x, w, dy, d["M"])
+    if name == "llama3-8b-tensorwise-quant":
+        return tensorwise_quant_cpu_sample(W.outlier_channels_bf16((r, d["K"]), 1.0, 0.01, 50.0, 0))
+    if name == "colwise-8192x14336":
+        return colwise_cpu_sample(W.column_gain_bf16((d["R"], r), 1e-3, -2, 2, 0),
+                                  W.normal_bf16((r, d["CX"]), 1.0, 1))
+    if name in ("dsv3-moe-fwd", "dsv3-moe-fwd-32e", "dsv3-moe-fwd-mx"):
+        return moe_fwd_cpu_sample(r, name="dsv3-moe-fwd" if name.endswith("-mx") else name,
+                                  mx=name.endswith("-mx"))
+    if name in ("llama4-moe-fwdbwd", "llama4-moe-fwdbwd-mx"):
+        return moe_fwdbwd_cpu_sample(r, mx=name.endswith("-mx"))
+    if name == "llama3-8b-dx-colquant-fused":
+        return dx_colquant_cpu_sample(r)
+    if name == "llama3-8b-fwd-quant-fused":
+        return fwd_quant_cpu_sample(r)
+    raise KeyError(name)
+
+
+def workload_unit(name):
+    return "GB/s" if name in ("colwise-8192x14336", "llama3-8b-tensorwise-quant") else "TFLOP/s"
+
+
 def run_reference(args, ws, rank):
-    """The oracle as it stands, on the host cores, on a bounded sample of the workload: every
-    step is the same sample."""
+    """The oracle as it stands, on the host cores, on a bounded sample of the workload drawn on
+    the host: every step is the same sample."""
     if rank != 0:
         return
     import oracle
-    if args.workload == "llama3-8b-mlp-up":
-        x, w, dy = W.linear_inputs(16, 4096, 14336, seed=0, outliers=True)
-        run, flops, sample = dense_cpu_sample(x, w, dy, 8192)
-    elif args.workload == "dsv3-moe-fwd":
-        run, flops, sample = moe_fwd_cpu_sample(16)
-    else:
-        print(json.dumps({"impl": "reference", "unavailable": "reference arm implemented for the dsv3-moe-fwd and "
-                                                              "llama3-8b-mlp-up workloads"}))
-        return
+    run, work, sample = host_cpu_sample(args.workload)
+    unit = workload_unit(args.workload)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         run()
     dt = time.perf_counter() - t0
-    value = flops * args.steps / dt / 1e12
+    value = work * args.steps / dt / (1e12 if unit == "TFLOP/s" else 1e9)
     cores = oracle.num_threads()
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "sample": sample},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
 
@@ -1303,9 +1460,12 @@ def main():
                        "the neighbouring steps' compute on separate streams"}
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and hasattr(step, "cpu_sample"):
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
-        run, work, sample = step.cpu_sample(args.cpu_rows)
+        # steps that keep no host-side inputs take the host-drawn sample, scaled like --cpu-rows
+        cpu_sample = getattr(step, "cpu_sample", None) or (
+            lambda r: host_cpu_sample(step.name, max(1, SAMPLE_ROWS[step.name] * r // args.cpu_rows)))
+        run, work, sample = cpu_sample(args.cpu_rows)
         t0 = time.perf_counter()
         run()
         dt = time.perf_counter() - t0
@@ -1315,7 +1475,7 @@ def main():
                "cores": cores, "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
         # the same oracle on one core, on an eighth of the sample (skipped when that would take
         # more than ~40 s by the multi-core rate)
-        run1, work1, sample1 = step.cpu_sample(max(1, args.cpu_rows // 8))
+        run1, work1, sample1 = cpu_sample(max(1, args.cpu_rows // 8))
         est = dt * (work1 / work) * cores
         if est <= 40.0:
             oracle.set_num_threads(1)
