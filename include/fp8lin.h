@@ -214,7 +214,8 @@ int fp8_quantize(const fp8_tensor* x, int granularity, int out_dtype, int layout
  *  sB   fp32 [1] or [N]; NULL for BF16 operands.
  *  out  bf16 or fp32 [M, N]. Accumulation is fp32 in tensor memory; the dequantization
  *       sA[m] * sB[n] is applied once in the epilogue, followed by one rounding to out's type.
- *  K * element size must be a multiple of 16 bytes; M and N are arbitrary (>= 1).
+ *  K * element size must be a multiple of 16 bytes; M and N are arbitrary (>= 1). K == 0 (an
+ *  empty contraction) writes out = 0 (every element an empty sum) with one cudaMemsetAsync.
  *  MX ([MX]): sA and sB of dtype FP8_DT_E8M0 select the block-scaled GEMM,
  *       out[m, n] = sum_k X_A[m, k/32] X_B[n, k/32] A[m, k] B[n, k], with A, B FP8 K-major,
  *       sA fp8_mx_scale_bytes(M, K) bytes and sB fp8_mx_scale_bytes(N, K) bytes in the MX scale
@@ -228,7 +229,8 @@ int fp8_scaled_mm(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA
 /*
  * fp8_grouped_mm — the MoE grouped GEMM of [G], one persistent launch; the offsets stay on the
  * device. offsets: int32 [E] cumulative segment ends (non-decreasing, last = total rows);
- * empty segments are allowed anywhere.
+ * empty segments are allowed anywhere. The contraction must have at least one column: K >= 1
+ * (JAGGED_M) and P >= 1 (JAGGED_K), else FP8_ERR_UNSUPPORTED.
  *
  * FP8_GROUPED_JAGGED_M (forward / grad-input):
  *   out[r, n] = sA[r] * sB[e, n] * sum_k A[r, k] * B[e, n, k]   for r in segment e.
@@ -275,7 +277,7 @@ int fp8_scaled_mm_amax(const fp8_tensor* A, const fp8_tensor* B, const fp8_tenso
  *                  16-byte aligned.
  *  out_q           FP8 (E4M3 or E5M2) [M, N] row-major codes.
  *  A, B, sA, sB, flags as fp8_scaled_mm with FP8 operands and fp32 tensor / row scales
- *  (FP8_MM_FAST_ACCUM only). N % 128 == 0.
+ *  (FP8_MM_FAST_ACCUM only). N % 128 == 0; K >= 1 (K == 0: FP8_ERR_UNSUPPORTED).
  * The codes and scales are bit-identical to fp8_scaled_mm with a bf16 output followed by
  * fp8_quantize (FP8_GRAN_BLOCK_1x128 or FP8_GRAN_MX, ROW_MAJOR) of that output. No workspace.
  */

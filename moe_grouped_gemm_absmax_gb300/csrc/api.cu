@@ -267,6 +267,7 @@ static int quantize_impl(const fp8_tensor* x, int gran, int out_dtype, int layou
                   FP8_ERR_INVALID_ARG);
         const int64_t E = offsets->shape[0];
         // the padded row count: from out_t, else from the size of the row-major scales
+        if (C == 0) return FP8_OK;  // no columns: no codes and no scales to write
         const int64_t P = want_col ? (out_t->ndim == 2 ? out_t->shape[1] : -1) : numel(inv) * 32 / C;
         FP8_CHECK(P >= R + 127 * E && P % 128 == 0, FP8_ERR_INVALID_ARG);
         if (want_col) FP8_CHECK(shape_is(out_t, 2, C, P), FP8_ERR_INVALID_ARG);
@@ -353,6 +354,12 @@ static int dense_gemm(const void* A, int a_dt, int a_mn, const void* B, int b_dt
   return launch_gemm(g, c);
 }
 
+// An empty contraction (K == 0): every output element is an empty sum, stored as +0.
+static int zero_out(const fp8_tensor* out, int64_t M, int64_t N, const Ctx& c) {
+  const size_t bytes = (size_t)M * (size_t)N * (out->dtype == FP8_DT_F32 ? 4u : 2u);
+  return cudaMemsetAsync(out->ptr, 0, bytes, c.stream) == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
 static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_tensor* sA, const fp8_tensor* sB,
                           fp8_tensor* out, int flags, const Ctx& c, uint32_t* row_amax = nullptr,
                           uint32_t* col_amax = nullptr, int amax_whole = 0) {
@@ -376,6 +383,7 @@ static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_te
       FP8_CHECK(aligned16(sA->ptr) && aligned16(sB->ptr), FP8_ERR_ALIGNMENT);
       FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
       if (M == 0 || N == 0) return FP8_OK;
+      if (K == 0) return zero_out(out, M, N, c);
       GemmArgs g = {};
       g.A = A->ptr;
       g.B = B->ptr;
@@ -399,6 +407,7 @@ static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_te
       FP8_CHECK(numel(sA) == M * (K / 128) && numel(sB) == ((N + 127) / 128) * (K / 128), FP8_ERR_INVALID_ARG);
       FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
       if (M == 0 || N == 0) return FP8_OK;
+      if (K == 0) return zero_out(out, M, N, c);
       GemmArgs g = {};
       g.A = A->ptr;
       g.B = B->ptr;
@@ -419,6 +428,7 @@ static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_te
     FP8_CHECK((la == 1 || la == M) && (lb == 1 || lb == N), FP8_ERR_INVALID_ARG);
     FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
     if (M == 0 || N == 0) return FP8_OK;
+    if (K == 0) return zero_out(out, M, N, c);
     return dense_gemm(A->ptr, A->dtype, 0, B->ptr, B->dtype, 0, static_cast<const float*>(sA->ptr), la,
                       static_cast<const float*>(sB->ptr), lb, out->ptr, out->dtype, M, N, K, c, row_amax, col_amax,
                       amax_whole);
@@ -431,6 +441,7 @@ static int scaled_mm_impl(const fp8_tensor* A, const fp8_tensor* B, const fp8_te
   FP8_CHECK(K == K2 && shape_is(out, 2, M, N), FP8_ERR_INVALID_ARG);
   FP8_CHECK(A->shape[1] % 8 == 0 && B->shape[1] % 8 == 0, FP8_ERR_ALIGNMENT);
   if (M == 0 || N == 0) return FP8_OK;
+  if (K == 0) return zero_out(out, M, N, c);
   return dense_gemm(A->ptr, FP8_DT_BF16, a_mn, B->ptr, FP8_DT_BF16, b_mn, nullptr, 0, nullptr, 0, out->ptr,
                     out->dtype, M, N, K, c, row_amax, col_amax, amax_whole);
 }
@@ -487,6 +498,7 @@ extern "C" int fp8_scaled_mm_quant(const fp8_tensor* A, const fp8_tensor* B, con
   FP8_CHECK((la == 1 || la == M) && (lb == 1 || lb == N), FP8_ERR_INVALID_ARG);
   FP8_CHECK(K % 16 == 0 && aligned16(A->ptr) && aligned16(B->ptr) && aligned16(out_q->ptr), FP8_ERR_ALIGNMENT);
   FP8_CHECK(N % 128 == 0, FP8_ERR_UNSUPPORTED);  // whole 128-column row segments per epilogue lane
+  FP8_CHECK(K > 0, FP8_ERR_UNSUPPORTED);          // an empty contraction: not implemented here
   FP8_CHECK(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), FP8_ERR_UNSUPPORTED);
   int mx = 0;
   if (out_granularity == FP8_GRAN_BLOCK_1x128) {
@@ -600,6 +612,7 @@ extern "C" int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp
     FP8_CHECK(A->ndim == 2 && B->ndim == 3 && B->shape[0] == E, FP8_ERR_INVALID_ARG);
     const int64_t M = A->shape[0], K = A->shape[1], N = B->shape[1];
     FP8_CHECK(B->shape[2] == K && shape_is(out, 2, M, N), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(K > 0, FP8_ERR_UNSUPPORTED);  // an empty contraction: not implemented here
     if (mx) {
       FP8_CHECK(K % 128 == 0, FP8_ERR_UNSUPPORTED);
       const int64_t P = numel(sA) * 32 / K;  // the segment-padded rows of A's scales
@@ -628,6 +641,7 @@ extern "C" int fp8_grouped_mm(const fp8_tensor* A, const fp8_tensor* B, const fp
     FP8_CHECK(A->ndim == 2 && B->ndim == 2 && A->shape[1] == B->shape[1], FP8_ERR_INVALID_ARG);
     const int64_t N = A->shape[0], Kd = B->shape[0], P = A->shape[1];
     FP8_CHECK(shape_is(out, 3, E, N, Kd), FP8_ERR_INVALID_ARG);
+    FP8_CHECK(P > 0, FP8_ERR_UNSUPPORTED);  // no padded token columns at all: not implemented here
     if (mx) {
       FP8_CHECK(P % 128 == 0, FP8_ERR_UNSUPPORTED);
       FP8_CHECK(numel(sA) == mx_scale_bytes(N, P) && numel(sB) == mx_scale_bytes(Kd, P), FP8_ERR_INVALID_ARG);
