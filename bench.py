@@ -1257,8 +1257,9 @@ def fwd_quant_cpu_sample(rows, seed=0):
     return run, 2.0 * rows * N * K, f"y for the first {rows} of {M} rows, then its 1 x 128 quantize"
 
 
-# Rows (tokens or routed rows) of each workload's host-drawn oracle sample; every sample takes a
-# few seconds or less on 8-16 host cores.
+# Size of each workload's host-drawn oracle sample: tokens or routed rows; for the column-wise
+# workload the columns of G and the rows of X. Every sample takes a few seconds or less on 8-16
+# host cores.
 SAMPLE_ROWS = {"llama3-8b-mlp-up": 16, "llama3-8b-mlp-up-blockwise": 16, "llama3-8b-mlp-up-mx": 32,
                "llama3-8b-tensorwise-quant": 2048, "colwise-8192x14336": 1024, "dsv3-moe-fwd": 16,
                "dsv3-moe-fwd-32e": 16, "dsv3-moe-fwd-mx": 16, "llama4-moe-fwdbwd": 4, "llama4-moe-fwdbwd-mx": 4,
