@@ -1301,6 +1301,103 @@ def workload_unit(name):
     return "GB/s" if name in ("colwise-8192x14336", "llama3-8b-tensorwise-quant") else "TFLOP/s"
 
 
+def _host_bf16(shape, std, seed, outlier_cols=None, col_gain=None, chunk_rows=2048):
+    """A full-size ~N(0, std^2) bf16 tensor drawn on the host in row chunks (bounded fp32 staging),
+    optionally with outlier columns x50 or a per-column gain 10^U(lo, hi)."""
+    R, C = shape
+    g = torch.Generator().manual_seed(seed)
+    out = torch.empty((R, C), dtype=torch.bfloat16)
+    gain = None
+    if outlier_cols is not None:
+        gain = torch.ones(C)
+        gain[torch.randperm(C, generator=torch.Generator().manual_seed(seed + 7919))[:max(1, round(outlier_cols * C))]] = 50.0
+    elif col_gain is not None:
+        lo, hi = col_gain
+        u = torch.rand(C, generator=torch.Generator().manual_seed(seed + 104729), dtype=torch.float64)
+        gain = torch.pow(10.0, lo + (hi - lo) * u).float()
+    for r0 in range(0, R, chunk_rows):
+        t = torch.randn(min(chunk_rows, R - r0), C, generator=g).mul_(std)
+        if gain is not None:
+            t.mul_(gain[None, :])
+        out[r0:r0 + t.shape[0]] = t.to(torch.bfloat16)
+    return out
+
+
+def full_quantize_cpu(name):
+    """The oracle's quantize steps of workload `name` on its full-size tensors (drawn on the host
+    from the workload's distributions), each timed alone: [(label, elements, algorithmic bytes,
+    seconds)]. Only the quantize call is timed, not the draw."""
+    import oracle
+    d = W.WORKLOADS[name].dims
+    E4, E5 = oracle.E4M3, oracle.E5M2
+    jobs = []  # (label, draw, quantize(bits), bytes)
+    if name == "dsv3-moe-fwd":
+        E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+        jobs = [("A e4m3 rows", lambda: _host_bf16((M, K), 1.0, 0), lambda b: oracle.quantize_rows(b, E4),
+                 3 * M * K + 4 * M),
+                ("W[e] e4m3 per expert column", lambda: _host_bf16((E * N, K), 0.02, 1),
+                 lambda b: oracle.quantize_rows(b, E4), 3 * E * N * K + 4 * E * N)]
+    elif name == "llama3-8b-mlp-up":
+        M, K, N = d["M"], d["K"], d["N"]
+        jobs = [("x e4m3 rows", lambda: _host_bf16((M, K), 1.0, 0, outlier_cols=0.01),
+                 lambda b: oracle.quantize_rows(b, E4), 3 * M * K + 4 * M),
+                ("W e4m3 rows", lambda: _host_bf16((N, K), 0.02, 1), lambda b: oracle.quantize_rows(b, E4),
+                 3 * N * K + 4 * N),
+                ("W e4m3 columns", lambda: _host_bf16((N, K), 0.02, 1), lambda b: oracle.quantize_cols(b, E4),
+                 3 * N * K + 4 * K),
+                ("dY e5m2 rows", lambda: _host_bf16((M, N), 1e-3, 2), lambda b: oracle.quantize_rows(b, E5),
+                 3 * M * N + 4 * M)]
+    elif name == "colwise-8192x14336":
+        R, C, RX, CX = d["R"], d["C"], d["RX"], d["CX"]
+        jobs = [("G e5m2 columns", lambda: _host_bf16((R, C), 1e-3, 0, col_gain=(-2, 2)),
+                 lambda b: oracle.quantize_cols(b, E5), 3 * R * C + 4 * C),
+                ("X e4m3 rows", lambda: _host_bf16((RX, CX), 1.0, 1), lambda b: oracle.quantize_rows(b, E4),
+                 3 * RX * CX + 4 * RX)]
+    elif name == "llama4-moe-fwdbwd":
+        E, M, K, N = d["E"], d["M"], d["K"], d["N"]
+        ends = W.ends_from_counts(W.llama4_counts(0))
+        jobs = [("A e4m3 rows", lambda: _host_bf16((M, K), 1.0, 0), lambda b: oracle.quantize_rows(b, E4),
+                 3 * M * K + 4 * M),
+                ("W[e] e4m3 rows", lambda: _host_bf16((E * N, K), 0.02, 1), lambda b: oracle.quantize_rows(b, E4),
+                 3 * E * N * K + 4 * E * N),
+                ("W[e] e4m3 columns (per expert)", lambda: _host_bf16((E * N, K), 0.02, 1),
+                 lambda b: [oracle.quantize_cols(b[e * N:(e + 1) * N], E4) for e in range(E)], 3 * E * N * K + 4 * E * K),
+                ("dY e5m2 rows", lambda: _host_bf16((M, N), 1e-3, 2), lambda b: oracle.quantize_rows(b, E5),
+                 3 * M * N + 4 * M),
+                ("dY e5m2 segment columns", lambda: _host_bf16((M, N), 1e-3, 2),
+                 lambda b: oracle.quantize_jagged_cols(b, ends, E5), 3 * M * N + 4 * E * N),
+                ("A e4m3 segment columns", lambda: _host_bf16((M, K), 1.0, 0),
+                 lambda b: oracle.quantize_jagged_cols(b, ends, E4), 3 * M * K + 4 * E * K)]
+    elif name == "linear-tensorwise-256x512":
+        M, K, N = d["M"], d["K"], d["N"]
+        jobs = [(f"{t} tensorwise", (lambda r=r, c=c, sd=sd, sdn=sdn: _host_bf16((r, c), sd, sdn)),
+                 (lambda b, f=f: oracle.quantize_tensor(b, f)), 3 * r * c + 4)
+                for t, r, c, sd, sdn, f in (("x e4m3", M, K, 1.0, 0, E4), ("W e4m3", N, K, 0.02, 1, E4),
+                                            ("dY e5m2", M, N, 1e-3, 2, E5))]
+    else:
+        raise KeyError(f"full-tensor quantize timing covers the five base workloads, not {name}")
+    out = []
+    for label, draw, quant, nbytes in jobs:
+        xb = W.bf16_bits(draw())
+        t0 = time.perf_counter()
+        quant(xb)
+        dt = time.perf_counter() - t0
+        out.append((label, int(xb.size), int(nbytes), dt))
+        del xb
+    return out
+
+
+def run_cpu_full_quantize(args):
+    """One JSON line: the oracle's quantize of every full-size tensor of the workload on the host
+    cores (GB/s of algorithmic bytes: 2 read + 1 written per element, plus the scales)."""
+    import oracle
+    rows = full_quantize_cpu(args.workload)
+    print(json.dumps({"impl": "reference", "kind": "oracle full-tensor quantize", "workload": args.workload,
+                      "cores": oracle.num_threads(),
+                      "tensors": [{"tensor": l, "elements": n, "GB/s": round(b / max(dt, 1e-9) / 1e9, 4), "seconds": round(dt, 3)}
+                                  for l, n, b, dt in rows]}))
+
+
 def run_reference(args, ws, rank):
     """The oracle as it stands, on the host cores, on a bounded sample of the workload drawn on
     the host: every step is the same sample."""
@@ -1337,9 +1434,14 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e measurement (profiling runs)")
+    ap.add_argument("--cpu-full-quantize", action="store_true",
+                    help="only time the oracle's quantize of the workload's full-size tensors on the host cores")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     ws, rank, local = dist_setup()
+    if args.cpu_full_quantize:
+        run_cpu_full_quantize(args)
+        return
     if args.impl == "reference":
         run_reference(args, ws, rank)
         return

@@ -63,3 +63,16 @@ def test_reference_line_contract():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_full_tensor_quantize_line():
+    """`bench.py --cpu-full-quantize` times the oracle's quantize of each full-size tensor of a
+    workload: one entry per tensor with its element count, rate and seconds."""
+    p = subprocess.run([sys.executable, "bench.py", "--cpu-full-quantize", "--workload", "linear-tensorwise-256x512"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    d = json.loads(p.stdout.strip().splitlines()[-1])
+    assert d["kind"] == "oracle full-tensor quantize" and d["cores"] >= 1
+    assert [t["tensor"] for t in d["tensors"]] == ["x e4m3 tensorwise", "W e4m3 tensorwise", "dY e5m2 tensorwise"]
+    assert [t["elements"] for t in d["tensors"]] == [256 * 512, 256 * 512, 256 * 256]
+    assert all(t["GB/s"] > 0 and t["seconds"] >= 0 for t in d["tensors"])
